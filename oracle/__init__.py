@@ -1,0 +1,22 @@
+"""CPU oracle (float64) for the Q4_0 / Q8_0 prefill projections.
+
+TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline legs use it. It shares no code with the CUDA
+library and never imports it.
+"""
+
+from .qref import (  # noqa: F401
+    Q4_0,
+    Q8_0,
+    fp16_bits_to_f64,
+    block_scales_and_codes,
+    dequant_f64,
+    dequant_f32,
+    qgemm_f64,
+    qgemm,
+    silu_f64,
+    gate_up_swiglu_f64,
+    gate_up_swiglu,
+    qgemm_f16_inputs_f64,
+    gate_up_swiglu_f16_inputs_f64,
+)

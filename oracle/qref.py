@@ -1,0 +1,167 @@
+"""Plain CPU oracle for the Q4_0 / Q8_0 prefill projections (float64).
+
+TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import or call
+this module. The product path (the CUDA library and its binding) never does,
+and this module imports nothing from it.
+
+What is computed, and where the pages define it:
+
+* Block formats (the GGUF blocks, which the pages' kernels read in their
+  on-disk array-of-blocks order: oxibonsai-kernels 0.1.4
+  src/gpu_backend/cuda_q_std_prefill.rs, module doc, section "Weight layout"):
+  Q4_0 = fp16 ``d`` (little endian, bytes 0-1) + 16 bytes, byte ``j`` holding
+  element ``j`` in its low nibble and ``j+16`` in its high nibble,
+  ``w = d * (q - 8)``; the same page's test ``make_q4_0_zeros`` fixes the block
+  size (18 bytes), the position of ``d`` and the fp16 encoding of 1.0
+  (``0x00, 0x3C``). Q8_0 = fp16 ``d`` + 32 int8, ``w = d * q`` (32 elements per
+  block, the ``k.div_ceil(32)`` dequant grid of aprender-serve 0.70.2
+  src/cuda/executor/gdn_prefill_ops.rs, ``qwen35_dequant_f32``).
+* Projection ``Y[T][n] = X[T][k] . W[n][k]^T`` (aprender-serve 0.70.2
+  src/cuda/executor/gdn_prefill_ops.rs, doc of ``qwen35_project_rows``),
+  optionally ``+ R[T][n]`` (the residual add that follows the down / output
+  projections: oxibonsai-kernels 0.1.4 ``encode_q_std_ffn_phase`` step 3 and
+  aprender-serve src/gguf/cuda/forward_qwen35_cuda_prefill.rs
+  ``prefill_ffn_rows``).
+* Fused gate/up SwiGLU ``silu(X . Wg^T) * (X . Wu^T)`` with
+  ``silu(g) = g / (1 + exp(-g))`` (oxibonsai-kernels ``encode_q_std_ffn_phase``
+  step 2; the unfused twin gate GEMM, up GEMM, ``fused_swiglu_into`` in
+  ``prefill_ffn_rows``).
+
+Every product is accumulated in float64 and the result is rounded to float32
+once. The f16-input mode rounds ``X`` and the dequantized ``W`` to fp16 first
+(the fp16 leg of ``qwen35_project_rows_f16``: fp16 in, fp32 accumulate), then
+accumulates exactly the same way.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+Q4_0 = 2
+Q8_0 = 8
+_QK = 32
+_BLOCK_BYTES = {Q4_0: 18, Q8_0: 34}
+
+
+# --------------------------------------------------------------------------
+# fp16 decode, written from the IEEE 754 binary16 definition:
+# 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+#   e == 0        : (-1)^s * 2^-14 * (f / 1024)          (zero / subnormal)
+#   0 < e < 31    : (-1)^s * 2^(e-15) * (1 + f / 1024)   (normal)
+#   e == 31       : (-1)^s * inf if f == 0, else NaN
+# --------------------------------------------------------------------------
+def fp16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    bits = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    s = (bits >> 15) & 1
+    e = (bits >> 10) & 0x1F
+    f = bits & 0x3FF
+    sign = np.where(s == 1, -1.0, 1.0)
+    frac = f.astype(np.float64) / 1024.0
+    normal = sign * np.ldexp(1.0 + frac, (e - 15).astype(np.int64))
+    sub = sign * np.ldexp(frac, -14)
+    special = np.where(f == 0, sign * np.inf, np.nan)
+    return np.where(e == 0, sub, np.where(e == 31, special, normal))
+
+
+def _blocks(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
+    if qtype not in _BLOCK_BYTES:
+        raise ValueError(f"unsupported qtype {qtype}")
+    if k % _QK:
+        raise ValueError("k must be a multiple of 32")
+    bb = _BLOCK_BYTES[qtype]
+    raw = np.ascontiguousarray(W, dtype=np.uint8).reshape(-1)
+    if raw.size != n * (k // _QK) * bb:
+        raise ValueError("weight byte count does not match n, k")
+    return raw.reshape(n, k // _QK, bb)
+
+
+def block_scales_and_codes(qtype: int, W: np.ndarray, n: int, k: int):
+    """Split the blocks into fp16 scale bits ``[n][k/32]`` and signed codes ``q'``.
+
+    ``q'`` is ``nibble - 8`` for Q4_0 and the int8 value for Q8_0, shape
+    ``[n][k/32][32]`` (int64), element order as stored.
+    """
+    blk = _blocks(qtype, W, n, k)
+    d_bits = blk[..., 0].astype(np.uint16) | (blk[..., 1].astype(np.uint16) << 8)
+    payload = blk[..., 2:]
+    if qtype == Q4_0:
+        low = (payload & 0x0F).astype(np.int64)   # elements 0..15
+        high = (payload >> 4).astype(np.int64)    # elements 16..31
+        codes = np.concatenate([low, high], axis=-1) - 8
+    else:
+        codes = payload.view(np.int8).astype(np.int64)
+    return d_bits, codes
+
+
+def dequant_f64(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
+    """``Wf[i][j] = fp16(d_{i, j/32}) * q'_{i,j}`` in float64, shape ``[n][k]``."""
+    d_bits, codes = block_scales_and_codes(qtype, W, n, k)
+    d = fp16_bits_to_f64(d_bits)
+    return (d[..., None] * codes.astype(np.float64)).reshape(n, k)
+
+
+def dequant_f32(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
+    """The standalone dequant export: ``f32(d) * f32(q')``.
+
+    ``d`` has at most 11 significant bits and ``|q'| <= 128`` at most 8, so the
+    float64 product is exact and so is its conversion to float32 (the range of
+    an fp16 scale times 128 is well inside float32's normal range, and fp16
+    subnormal scales times small integers stay exact in float32).
+    """
+    return dequant_f64(qtype, W, n, k).astype(np.float32)
+
+
+def _as_f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float32).astype(np.float64)
+
+
+def qgemm_f64(qtype: int, W, n: int, k: int, X, residual=None) -> np.ndarray:
+    """``Y = X . Wf^T (+ R)`` in float64, shape ``[T][n]``."""
+    Wf = dequant_f64(qtype, W, n, k)
+    X64 = _as_f64(X).reshape(-1, k)
+    Y = X64 @ Wf.T
+    if residual is not None:
+        Y = Y + _as_f64(residual).reshape(Y.shape)
+    return Y
+
+
+def qgemm(qtype: int, W, n: int, k: int, X, residual=None) -> np.ndarray:
+    """``Y = X . Wf^T (+ R)``, accumulated in float64, rounded to float32 once."""
+    return qgemm_f64(qtype, W, n, k, X, residual).astype(np.float32)
+
+
+def silu_f64(g: np.ndarray) -> np.ndarray:
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g))
+
+
+def gate_up_swiglu_f64(qtype: int, Wg, Wu, n: int, k: int, X) -> np.ndarray:
+    g = qgemm_f64(qtype, Wg, n, k, X)
+    u = qgemm_f64(qtype, Wu, n, k, X)
+    return silu_f64(g) * u
+
+
+def gate_up_swiglu(qtype: int, Wg, Wu, n: int, k: int, X) -> np.ndarray:
+    """``silu(X . Wg^T) * (X . Wu^T)`` in float64, rounded to float32 once."""
+    return gate_up_swiglu_f64(qtype, Wg, Wu, n, k, X).astype(np.float32)
+
+
+# --------------------------------------------------------------------------
+# fp16-input mode: the same products after rounding both operands to fp16
+# (round to nearest even, numpy's float32 -> float16 conversion). Isolates
+# the accumulation error of an fp16-input leg from its input rounding.
+# --------------------------------------------------------------------------
+def qgemm_f16_inputs_f64(qtype: int, W, n: int, k: int, X, residual=None) -> np.ndarray:
+    W16 = dequant_f32(qtype, W, n, k).astype(np.float16).astype(np.float64)
+    X16 = np.asarray(X, dtype=np.float32).reshape(-1, k).astype(np.float16).astype(np.float64)
+    Y = X16 @ W16.T
+    if residual is not None:
+        Y = Y + _as_f64(residual).reshape(Y.shape)
+    return Y
+
+
+def gate_up_swiglu_f16_inputs_f64(qtype: int, Wg, Wu, n: int, k: int, X) -> np.ndarray:
+    g = qgemm_f16_inputs_f64(qtype, Wg, n, k, X)
+    u = qgemm_f16_inputs_f64(qtype, Wu, n, k, X)
+    return silu_f64(g) * u

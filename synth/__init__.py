@@ -1,0 +1,23 @@
+"""Seeded synthetic inputs for the Q4_0 / Q8_0 prefill GEMM.
+
+This package is shared by the CUDA path's tests and benchmark and by the CPU
+oracle's tests. It only *makes* inputs: seeded normal draws and the GGUF block
+encoder that turns an f32 weight into Q4_0 / Q8_0 bytes. It holds none of the
+arithmetic the prefill path computes (block decoding, the products, the
+epilogues): that lives, twice and independently, in ``oracle/`` and in the
+CUDA library.
+"""
+
+from .gen import (  # noqa: F401
+    Q4_0,
+    Q8_0,
+    BLOCK_ELEMS,
+    block_bytes,
+    quantize,
+    quantize_q4_0,
+    quantize_q8_0,
+    weight_f32,
+    activations,
+    make_case,
+    WORKLOADS,
+)

@@ -1,0 +1,136 @@
+"""Seeded generators and the GGUF Q4_0 / Q8_0 block encoder.
+
+Recipe (the same for every workload):
+
+* weights ``W ~ N(0, 0.02)``, activations ``X ~ N(0, 1)`` and residuals
+  ``R ~ N(0, 1)`` are drawn with numpy's ``default_rng(seed)`` (PCG64) as
+  float64 ``standard_normal`` values, scaled, then cast to float32;
+* seeds: ``W`` uses ``seed``, ``X`` ``seed+1``, ``R`` ``seed+2``, the up weight of
+  a gate/up pair ``seed+3`` and a down weight ``seed+4``;
+* the f32 weight is encoded into GGUF blocks of 32 elements:
+
+  - Q4_0 (18 bytes): fp16 scale ``d`` (little endian), then 16 bytes; byte ``j``
+    holds element ``j`` in its low nibble and element ``j+16`` in its high
+    nibble. The encoder takes the block's signed element of largest magnitude
+    ``m`` and sets ``d = m / -8`` so that ``m`` itself maps to nibble 0; every
+    element gets ``q = clamp(round(w / d) + 8, 0, 15)``.
+  - Q8_0 (34 bytes): fp16 ``d = max|w| / 127`` then 32 int8
+    ``q = clamp(round(w / d), -127, 127)``.
+
+  ``round`` is half away from zero, ``w / d`` uses the f32 ``d`` before it is
+  rounded to fp16 (round to nearest even) for storage, and an all-zero block
+  gets ``d = 0`` with ``q = 8`` (Q4_0) or ``q = 0`` (Q8_0).
+
+This is the inverse direction of what the prefill path computes; the decoding
+and the products are not here.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+Q4_0 = 2  # GGUF type id
+Q8_0 = 8  # GGUF type id
+BLOCK_ELEMS = 32
+_BLOCK_BYTES = {Q4_0: 18, Q8_0: 34}
+
+
+def block_bytes(qtype: int) -> int:
+    """Bytes of one 32-element block of ``qtype``."""
+    return _BLOCK_BYTES[qtype]
+
+
+def _round_half_away(v: np.ndarray) -> np.ndarray:
+    v = v.astype(np.float64)
+    return np.sign(v) * np.floor(np.abs(v) + 0.5)
+
+
+def _pack_scale(d32: np.ndarray) -> np.ndarray:
+    """fp16 bits of ``d`` (RNE) as two little-endian bytes, shape ``[..., 2]``."""
+    bits = d32.astype(np.float16).view(np.uint16)
+    return np.stack([(bits & 0xFF).astype(np.uint8), (bits >> 8).astype(np.uint8)], axis=-1)
+
+
+def quantize_q4_0(w: np.ndarray) -> np.ndarray:
+    """Encode an f32 ``[n][k]`` weight (k % 32 == 0) into Q4_0 bytes ``[n][k/32*18]``."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n, k = w.shape
+    assert k % BLOCK_ELEMS == 0
+    blk = w.reshape(n, k // BLOCK_ELEMS, BLOCK_ELEMS)
+    idx = np.argmax(np.abs(blk), axis=-1)[..., None]
+    m = np.take_along_axis(blk, idx, axis=-1)[..., 0]
+    d = (m / np.float32(-8.0)).astype(np.float32)
+    safe = np.where(d == 0, np.float32(1.0), d)
+    ratio = (blk / safe[..., None]).astype(np.float32)
+    q = np.clip(_round_half_away(ratio) + 8, 0, 15).astype(np.uint8)
+    q = np.where((d == 0)[..., None], np.uint8(8), q)
+    out = np.empty((n, k // BLOCK_ELEMS, 18), dtype=np.uint8)
+    out[..., 0:2] = _pack_scale(d)
+    out[..., 2:18] = q[..., :16] | (q[..., 16:] << 4)
+    return out.reshape(n, -1)
+
+
+def quantize_q8_0(w: np.ndarray) -> np.ndarray:
+    """Encode an f32 ``[n][k]`` weight (k % 32 == 0) into Q8_0 bytes ``[n][k/32*34]``."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n, k = w.shape
+    assert k % BLOCK_ELEMS == 0
+    blk = w.reshape(n, k // BLOCK_ELEMS, BLOCK_ELEMS)
+    amax = np.max(np.abs(blk), axis=-1)
+    d = (amax / np.float32(127.0)).astype(np.float32)
+    safe = np.where(d == 0, np.float32(1.0), d)
+    ratio = (blk / safe[..., None]).astype(np.float32)
+    q = np.clip(_round_half_away(ratio), -127, 127).astype(np.int8)
+    q = np.where((d == 0)[..., None], np.int8(0), q)
+    out = np.empty((n, k // BLOCK_ELEMS, 34), dtype=np.uint8)
+    out[..., 0:2] = _pack_scale(d)
+    out[..., 2:34] = q.view(np.uint8)
+    return out.reshape(n, -1)
+
+
+def quantize(qtype: int, w: np.ndarray) -> np.ndarray:
+    if qtype == Q4_0:
+        return quantize_q4_0(w)
+    if qtype == Q8_0:
+        return quantize_q8_0(w)
+    raise ValueError(f"unsupported qtype {qtype}")
+
+
+def weight_f32(n: int, k: int, seed: int, sigma: float = 0.02) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((n, k)) * sigma).astype(np.float32)
+
+
+def activations(rows: int, cols: int, seed: int, sigma: float = 1.0) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((rows, cols)) * sigma).astype(np.float32)
+
+
+def make_case(qtype: int, n: int, k: int, T: int, *, residual: bool = False,
+              gate_up: bool = False, seed: int = 0) -> dict:
+    """One seeded problem: quantized ``W`` (and ``Wu`` for a gate/up pair), ``X``, ``R``.
+
+    Returns numpy arrays: ``W``/``Wu`` uint8 ``[n][k/32*bytes]``, ``X`` f32
+    ``[T][k]``, ``R`` f32 ``[T][n]`` or ``None``.
+    """
+    case = {"qtype": qtype, "n": n, "k": k, "T": T}
+    case["W"] = quantize(qtype, weight_f32(n, k, seed))
+    case["Wu"] = quantize(qtype, weight_f32(n, k, seed + 3)) if gate_up else None
+    case["X"] = activations(T, k, seed + 1)
+    case["R"] = activations(T, n, seed + 2) if residual else None
+    return case
+
+
+# Named workloads: shapes of the prefill projections the pages run, at their
+# chunk sizes (512 rows by default, 2048 on a unified-memory box).
+WORKLOADS = {
+    # Q8_0 GEMM, 256 x 512 weight, 16 tokens (the small reference problem)
+    "q8_0_n256_k512_t16": dict(qtype=Q8_0, n=256, k=512, T=16),
+    # Q4_0 GEMM + residual, 4096 x 4096, 512 tokens
+    "q4_0_n4096_k4096_t512_res": dict(qtype=Q4_0, n=4096, k=4096, T=512, residual=True),
+    # fused gate/up SwiGLU, 12288 x 4096 each, then down 4096 x 12288 + residual
+    "swiglu_q4_0_n12288_k4096_t512": dict(qtype=Q4_0, n=12288, k=4096, T=512, gate_up=True),
+    "down_q4_0_n4096_k12288_t512_res": dict(qtype=Q4_0, n=4096, k=12288, T=512, residual=True),
+    "swiglu_q8_0_n12288_k4096_t512": dict(qtype=Q8_0, n=12288, k=4096, T=512, gate_up=True),
+    "down_q8_0_n4096_k12288_t512_res": dict(qtype=Q8_0, n=4096, k=12288, T=512, residual=True),
+}

@@ -1,0 +1,286 @@
+"""Pins of the CPU oracle to facts outside itself (no GPU).
+
+* hand-built blocks with values derived from the block definitions
+  (``tests/golden/*.txt``, each with its source);
+* the fp16 decoder against two independent decoders over all 65,536 bit
+  patterns;
+* exactly representable fp16 values (the dequant test idea of aprender-serve
+  0.70.2 src/cuda/executor/gdn_prefill_ops.rs, ``f16_weight_dequantizes_on_the_device``);
+* brute force: exact rational dot products on tiny shapes, with an independent
+  block parser (``struct``) and an independent fp16 decoder;
+* invariants that any correct implementation satisfies exactly.
+"""
+
+import math
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def load_golden(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, _, rest = line.partition(" ")
+            out[key] = rest.split()
+    qtype = int(out["qtype"][0])
+    byts = np.array([int(b, 16) for b in out["bytes"]], dtype=np.uint8)
+    vals = np.array([float(v) for v in out["values"]], dtype=np.float64)
+    return qtype, byts, vals
+
+
+GOLDEN_FILES = sorted(f for f in os.listdir(GOLDEN) if f.endswith(".txt"))
+
+
+@pytest.mark.parametrize("name", GOLDEN_FILES)
+def test_golden_block_dequant(name):
+    qtype, byts, vals = load_golden(name)
+    got64 = oracle.dequant_f64(qtype, byts, 1, 32)[0]
+    got32 = oracle.dequant_f32(qtype, byts, 1, 32)[0]
+    np.testing.assert_array_equal(got64, vals)
+    np.testing.assert_array_equal(got32.astype(np.float64), vals)
+
+
+def test_golden_files_present():
+    assert {"q4_0_zero_block.txt", "q4_0_nibble_order.txt", "q8_0_half_scale.txt",
+            "q8_0_subnormal_scale.txt", "q4_0_negative_scale.txt"} <= set(GOLDEN_FILES)
+
+
+# ---------------------------------------------------------------- fp16 decode
+def _struct_half(bits):
+    return struct.unpack("<e", struct.pack("<H", int(bits)))[0]
+
+
+def test_fp16_decode_all_patterns_vs_numpy_and_struct():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = oracle.fp16_bits_to_f64(bits)
+    ref = bits.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    np.testing.assert_array_equal(ours[~nan], ref[~nan])
+    # signed zeros keep their sign
+    assert np.array_equal(np.signbit(ours[~nan]), np.signbit(ref[~nan]))
+    # a third, unrelated decoder on a stride of patterns
+    for b in range(0, 65536, 97):
+        s = _struct_half(b)
+        if math.isnan(s):
+            assert math.isnan(ours[b])
+        else:
+            assert ours[b] == s
+
+
+def test_fp16_exactly_representable_values():
+    # i * 0.5 - 16 for i in 0..127: exactly representable, distinct and signed.
+    want = [i * 0.5 - 16.0 for i in range(128)]
+    bits = [struct.unpack("<H", struct.pack("<e", v))[0] for v in want]
+    got = oracle.fp16_bits_to_f64(np.array(bits, dtype=np.uint16))
+    assert list(got) == want
+
+
+def test_fp16_decode_landmarks():
+    assert oracle.fp16_bits_to_f64(np.uint16(0x3C00)) == 1.0       # page bytes 0x00, 0x3C
+    assert oracle.fp16_bits_to_f64(np.uint16(0x0001)) == 2.0 ** -24
+    assert oracle.fp16_bits_to_f64(np.uint16(0x03FF)) == 1023 * 2.0 ** -24
+    assert oracle.fp16_bits_to_f64(np.uint16(0x0400)) == 2.0 ** -14
+    assert oracle.fp16_bits_to_f64(np.uint16(0x7BFF)) == 65504.0
+    assert oracle.fp16_bits_to_f64(np.uint16(0xC000)) == -2.0
+    assert oracle.fp16_bits_to_f64(np.uint16(0x7C00)) == np.inf
+
+
+# ---------------------------------------------------------------- brute force
+def _parse_block_independent(qtype, blk: bytes):
+    """(Fraction d, list of 32 int codes) via struct, not the oracle's decoder."""
+    d = Fraction(struct.unpack("<e", blk[0:2])[0])
+    if qtype == synth.Q4_0:
+        lo = [(b & 0xF) - 8 for b in blk[2:18]]
+        hi = [(b >> 4) - 8 for b in blk[2:18]]
+        return d, lo + hi
+    return d, list(struct.unpack("32b", blk[2:34]))
+
+
+def _random_blocks(rng, qtype, n, k):
+    """Random raw bytes with finite scales (exponent field kept below 31)."""
+    bb = synth.block_bytes(qtype)
+    raw = rng.integers(0, 256, size=(n, k // 32, bb), dtype=np.uint8)
+    hi = raw[..., 1]
+    raw[..., 1] = np.where((hi & 0x7C) == 0x7C, hi & 0xBF, hi)  # clear one exp bit
+    return raw.reshape(n, -1)
+
+
+def _exact_qgemm(qtype, W, n, k, X, R):
+    bb = synth.block_bytes(qtype)
+    rows = []
+    for i in range(n):
+        wrow = []
+        for b in range(k // 32):
+            blk = bytes(W[i, b * bb:(b + 1) * bb])
+            d, codes = _parse_block_independent(qtype, blk)
+            wrow.extend(d * c for c in codes)
+        rows.append(wrow)
+    T = X.shape[0]
+    Y = [[None] * n for _ in range(T)]
+    for t in range(T):
+        xs = [Fraction(float(v)) for v in X[t]]
+        for i in range(n):
+            acc = sum(x * w for x, w in zip(xs, rows[i]))
+            if R is not None:
+                acc += Fraction(float(R[t, i]))
+            Y[t][i] = acc
+    return Y, rows
+
+
+def _ulp32(x):
+    x = abs(np.float32(x))
+    return float(np.spacing(x)) if x != 0 else float(np.spacing(np.float32(0)))
+
+
+@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
+@pytest.mark.parametrize("n,k,T,res", [(3, 32, 2, False), (5, 64, 3, True), (2, 96, 1, True)])
+def test_brute_force_exact_rationals(qtype, n, k, T, res):
+    rng = np.random.default_rng(1234 + n + k + T + qtype)
+    W = _random_blocks(rng, qtype, n, k)
+    X = rng.standard_normal((T, k)).astype(np.float32)
+    R = rng.standard_normal((T, n)).astype(np.float32) if res else None
+    exact, wrows = _exact_qgemm(qtype, W, n, k, X, R)
+    got = oracle.qgemm(qtype, W, n, k, X, R)
+    assert got.shape == (T, n) and got.dtype == np.float32
+    n_equal = 0
+    for t in range(T):
+        for i in range(n):
+            e = exact[t][i]
+            mag = sum(abs(Fraction(float(X[t, j])) * wrows[i][j]) for j in range(k))
+            bound = 0.5 * _ulp32(float(e)) + float(mag) * (k + 2) * 2.0 ** -52
+            assert abs(float(got[t, i]) - float(e)) <= bound, (t, i)
+            n_equal += float(got[t, i]) == float(np.float32(float(e)))
+    assert n_equal >= T * n - 1
+
+
+@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
+def test_brute_force_dequant_exact(qtype):
+    rng = np.random.default_rng(77 + qtype)
+    n, k = 4, 64
+    W = _random_blocks(rng, qtype, n, k)
+    _, rows = _exact_qgemm(qtype, W, n, k, np.zeros((1, k), np.float32), None)
+    got = oracle.dequant_f32(qtype, W, n, k)
+    for i in range(n):
+        for j in range(k):
+            assert Fraction(float(got[i, j])) == rows[i][j]
+
+
+@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
+def test_brute_force_swiglu(qtype):
+    rng = np.random.default_rng(99 + qtype)
+    n, k, T = 4, 64, 3
+    Wg = synth.quantize(qtype, (rng.standard_normal((n, k)) * 0.3).astype(np.float32))
+    Wu = synth.quantize(qtype, (rng.standard_normal((n, k)) * 0.3).astype(np.float32))
+    X = rng.standard_normal((T, k)).astype(np.float32)
+    g, _ = _exact_qgemm(qtype, Wg, n, k, X, None)
+    u, _ = _exact_qgemm(qtype, Wu, n, k, X, None)
+    got = oracle.gate_up_swiglu(qtype, Wg, Wu, n, k, X)
+    for t in range(T):
+        for i in range(n):
+            gf, uf = float(g[t][i]), float(u[t][i])
+            want = gf / (1.0 + math.exp(-gf)) * uf
+            assert abs(float(got[t, i]) - want) <= _ulp32(want) + 1e-12 * abs(want)
+
+
+# ---------------------------------------------------------------- invariants
+@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
+def test_identity_x_returns_dequantized_weight(qtype):
+    n, k = 8, 64
+    W = synth.quantize(qtype, synth.weight_f32(n, k, seed=5))
+    X = np.eye(k, dtype=np.float32)
+    Y = oracle.qgemm(qtype, W, n, k, X)
+    np.testing.assert_array_equal(Y, oracle.dequant_f32(qtype, W, n, k).T)
+
+
+@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
+def test_scaling_and_permutation(qtype):
+    n, k, T = 16, 128, 7
+    case = synth.make_case(qtype, n, k, T, seed=3)
+    Y = oracle.qgemm(qtype, case["W"], n, k, case["X"])
+    np.testing.assert_array_equal(oracle.qgemm(qtype, case["W"], n, k, 2 * case["X"]), 2 * Y)
+    perm = np.random.default_rng(0).permutation(T)
+    np.testing.assert_array_equal(oracle.qgemm(qtype, case["W"], n, k, case["X"][perm]), Y[perm])
+
+
+def test_q4_block_reencoded_as_q8_dequantizes_identically():
+    n, k = 6, 96
+    W4 = synth.quantize_q4_0(synth.weight_f32(n, k, seed=11))
+    blk = W4.reshape(n, k // 32, 18)
+    W8 = np.empty((n, k // 32, 34), dtype=np.uint8)
+    W8[..., 0:2] = blk[..., 0:2]
+    lo = (blk[..., 2:] & 0xF).astype(np.int16) - 8
+    hi = (blk[..., 2:] >> 4).astype(np.int16) - 8
+    W8[..., 2:] = np.concatenate([lo, hi], axis=-1).astype(np.int8).view(np.uint8)
+    np.testing.assert_array_equal(oracle.dequant_f32(synth.Q4_0, W4, n, k),
+                                  oracle.dequant_f32(synth.Q8_0, W8.reshape(n, -1), n, k))
+
+
+def test_zero_codes_give_residual_and_zero_swiglu():
+    n, k, T = 5, 64, 4
+    Wz = np.zeros((n, k // 32, 34), np.uint8)
+    Wz[..., 1] = 0x3C  # d = 1.0, every q = 0
+    Wz = Wz.reshape(n, -1)
+    X = synth.activations(T, k, 1)
+    R = synth.activations(T, n, 2)
+    np.testing.assert_array_equal(oracle.qgemm(synth.Q8_0, Wz, n, k, X, R), R)
+    Wu = synth.quantize_q8_0(synth.weight_f32(n, k, 4))
+    np.testing.assert_array_equal(oracle.gate_up_swiglu(synth.Q8_0, Wz, Wu, n, k, X),
+                                  np.zeros((T, n), np.float32))
+
+
+def test_residual_is_added_once():
+    n, k, T = 8, 64, 3
+    case = synth.make_case(synth.Q4_0, n, k, T, residual=True, seed=9)
+    y0 = oracle.qgemm_f64(synth.Q4_0, case["W"], n, k, case["X"])
+    y1 = oracle.qgemm_f64(synth.Q4_0, case["W"], n, k, case["X"], case["R"])
+    np.testing.assert_allclose(y1 - y0, case["R"].astype(np.float64), rtol=0, atol=1e-12)
+
+
+def test_f16_input_mode_rounds_both_operands():
+    n, k, T = 4, 64, 2
+    case = synth.make_case(synth.Q4_0, n, k, T, seed=21)
+    X = case["X"] * np.float32(1.0 + 2.0 ** -20)  # not fp16-representable
+    a = oracle.qgemm_f16_inputs_f64(synth.Q4_0, case["W"], n, k, X)
+    X16 = X.astype(np.float16).astype(np.float32)
+    W16 = oracle.dequant_f32(synth.Q4_0, case["W"], n, k).astype(np.float16).astype(np.float64)
+    b = X16.astype(np.float64) @ W16.T
+    np.testing.assert_allclose(a, b, rtol=1e-15, atol=0)
+
+
+# ---------------------------------------------------------------- encoder
+@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
+def test_quantizer_round_trip(qtype):
+    n, k = 64, 256
+    w = synth.weight_f32(n, k, seed=2)
+    W = synth.quantize(qtype, w)
+    d_bits, _ = oracle.block_scales_and_codes(qtype, W, n, k)
+    d = np.abs(oracle.fp16_bits_to_f64(d_bits))
+    err = np.abs(oracle.dequant_f64(qtype, W, n, k) - w.astype(np.float64)).reshape(n, k // 32, 32)
+    # Q8_0 rounds to the nearest code; Q4_0 may also clamp 16 -> 15 (one more step).
+    # The fp16 rounding of d adds at most 2^-11 relative on top.
+    step = 0.5 if qtype == synth.Q8_0 else 1.0
+    lim = d[..., None] * (step + 128 * 2.0 ** -11) + 1e-12
+    assert np.all(err <= lim)
+
+
+def test_q4_0_encoder_maps_signed_extreme_to_nibble_zero():
+    w = np.zeros((1, 32), np.float32)
+    w[0, 5] = 0.8
+    w[0, 9] = -0.4
+    W = synth.quantize_q4_0(w)
+    d_bits, codes = oracle.block_scales_and_codes(synth.Q4_0, W, 1, 32)
+    assert oracle.fp16_bits_to_f64(d_bits)[0, 0] == float(np.float16(-0.1))
+    assert codes[0, 0, 5] == -8 and codes[0, 0, 9] == 4 and codes[0, 0, 0] == 0
