@@ -1,0 +1,388 @@
+"""Benchmark of the Q4_0 prefill GEMM (+ residual) on GB300.
+
+One step = one pass of the hot path over one batch: ``apr_qgemm`` on the
+Q4_0 4096 x 4096 weight with T = 512 token rows and a residual, i.e. the
+fp32 -> fp16 activation pass, then the tcgen05 GEMM whose warps stream the raw
+blocks, decode them in registers, run the MMA and add the residual in the
+epilogue. Inputs are seeded synthetic data (numpy PCG64, seed 0; W ~ N(0,0.02)
+quantized to Q4_0, X and R ~ N(0,1)), resident in HBM. Eight input sets
+(W, X, R, Y: 277 MB, more than twice the 129 MB L2) rotate between steps.
+
+Printed (one JSON line, rank 0): the step throughput in TFLOP/s (2 T n k per
+step), the roofline of the dominant kernel (the GEMM, timed alone with CUDA
+events through ``apr_qgemm_f16_in``), the end-to-end throughput through the
+same public call with host buffers (pinned X and R copied in, Y copied out,
+every step), the CPU oracle's throughput on the host cores, and the SM clocks
+sampled during the timed region.
+
+``--impl reference`` times the CPU oracle (there is no other implementation
+of this path to run) on the same workload, a bounded sample of W rows per
+step.
+
+Multi-GPU: under torchrun every rank runs its own replica (the projections
+shard over independent problems; no collective is on the data path); the
+timed region is bracketed by barriers, the slowest rank's time is used and
+``value`` counts the work of all ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+# the CPU oracle uses every host core this process may run on
+_CORES = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+os.environ.setdefault("OPENBLAS_NUM_THREADS", str(_CORES))
+os.environ.setdefault("OMP_NUM_THREADS", str(_CORES))
+
+import numpy as np  # noqa: E402
+
+METRIC = "Q4_0/Q8_0 prefill GEMM TFLOP/s at T=512 (% tensor peak); GEMV GB/s (% HBM)"
+WORKLOAD = "q4_0_gemm_residual_n4096_k4096_t512"
+QTYPE, N, K, T = 2, 4096, 4096, 512
+SETS = 8
+FLOP = 2.0 * T * N * K
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d["bf16_tflops"], d["hbm_gbs"], "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ ranks
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_over_ranks(elapsed_s: float, units: float, world: int):
+    """(max elapsed over ranks, sum of units over ranks); needs an initialised
+    process group when world > 1."""
+    if world == 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]) if parts[3] not in ("", "[N/A]") else 0.0,
+                             parts[4], parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[4]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[0] for r in loaded])), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(loaded)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(rows: int):
+    """Times the oracle on the first `rows` weight rows with all T tokens."""
+    import oracle
+    import synth
+
+    case = synth.make_case(QTYPE, N, K, T, residual=True, seed=0)
+    bb = synth.block_bytes(QTYPE)
+    Wr = case["W"][:rows]
+    Rr = np.ascontiguousarray(case["R"][:, :rows])
+    t0 = time.perf_counter()
+    oracle.qgemm(QTYPE, Wr, rows, K, case["X"], Rr)
+    dt = time.perf_counter() - t0
+    return dt, 2.0 * T * rows * K, bb
+
+
+def cpu_baseline(budget_s: float = 10.0):
+    rows = 256
+    dt, flop, _ = oracle_sample(rows)
+    # grow the sample to about `budget_s` of CPU work (bounded by the full weight)
+    rows = int(min(N, max(rows, rows * budget_s / max(dt, 1e-3))))
+    dt, flop, _ = oracle_sample(rows)
+    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": _CORES, "kind": "oracle",
+            "sample": f"float64 oracle (numpy/OpenBLAS) on {rows} of the {N} weight rows, all {T} tokens, k={K}, "
+                      f"with residual: {dt:.2f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    # each step: the oracle on a bounded sample of rows, sized so that the
+    # whole run stays within about two minutes
+    total = args.steps + args.warmup
+    probe_dt, _, _ = oracle_sample(64)
+    per_row = probe_dt / 64
+    rows = int(max(8, min(N, (100.0 / max(total, 1)) / max(per_row, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_sample(rows)
+    t = 0.0
+    flop = 0.0
+    for _ in range(args.steps):
+        dt, f, _ = oracle_sample(rows)
+        t += dt
+        flop += f
+    value = flop / t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "qtype": "Q4_0", "n": N, "k": K, "T": T, "residual": True},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _CORES, "kind": "oracle",
+                         "sample": f"{rows} of the {N} weight rows per step, all {T} tokens"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args):
+    import torch
+
+    import quantized_weight_prefill_q4_gb300 as q
+    import synth
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+
+    # seeded inputs: set 0 is the seed-0 case; the other sets are copies
+    case = synth.make_case(QTYPE, N, K, T, residual=True, seed=0)
+    sets = []
+    for i in range(SETS):
+        sets.append(dict(W=torch.from_numpy(case["W"]).to(dev), X=torch.from_numpy(case["X"]).to(dev),
+                         R=torch.from_numpy(case["R"]).to(dev), Y=torch.empty((T, N), device=dev),
+                         X16=torch.empty((T, K), dtype=torch.float16, device=dev)))
+    torch.cuda.synchronize()
+
+    def step(i):
+        s = sets[i % SETS]
+        q.apr_qgemm(QTYPE, s["W"], N, K, s["X"], T, s["Y"], s["R"], stream=stream)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    q.apr_stream_status(stream)
+
+    # ---- timed region: K steps, events on the launching stream
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        # keep the GPU busy while the sampler sees it (also the roofline runs below)
+    barrier(ws)
+    elapsed = e0.elapsed_time(e1) / 1e3
+    q.apr_stream_status(stream)
+    t_max, flop_all = reduce_over_ranks(elapsed, FLOP * args.steps, ws)
+    value = flop_all / t_max / 1e12
+
+    # ---- dominant kernel alone: the tcgen05 GEMM on fp16 activations
+    for s in sets:
+        q.apr_convert_f32_to_f16(s["X"], T * K, s["X16"], stream=stream)
+    reps = max(200, min(args.steps, 2000))
+    for i in range(10):
+        s = sets[i % SETS]
+        q.apr_qgemm_f16_in(QTYPE, s["W"], N, K, s["X16"], T, s["Y"], s["R"], stream=stream)
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for i in range(reps):
+        s = sets[i % SETS]
+        q.apr_qgemm_f16_in(QTYPE, s["W"], N, K, s["X16"], T, s["Y"], s["R"], stream=stream)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    gemm_s = g0.elapsed_time(g1) / 1e3 / reps
+    q.apr_stream_status(stream)
+    peak_tf, peak_gbs, peak_kind = _peaks()
+    achieved = FLOP / gemm_s / 1e12
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        with open(tp) as f:
+            traffic = json.load(f).get(WORKLOAD)
+
+    # ---- small-T GEMV (T = 1), the other half of the metric
+    gemv = None
+    if rank == 0:
+        gemv = gemv_rate(q, synth, dev, stream, peak_gbs)
+
+    # ---- end to end: host buffers, copies inside the timed region
+    e2e_steps = max(20, min(args.steps, 200))
+    hX = torch.from_numpy(case["X"]).pin_memory()
+    hR = torch.from_numpy(case["R"]).pin_memory()
+    hY = torch.empty((T, N), dtype=torch.float32).pin_memory()
+    s0 = sets[0]
+    for _ in range(3):
+        s0["X"].copy_(hX, non_blocking=True)
+        s0["R"].copy_(hR, non_blocking=True)
+        q.apr_qgemm(QTYPE, s0["W"], N, K, s0["X"], T, s0["Y"], s0["R"], stream=stream)
+        hY.copy_(s0["Y"], non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(ws)
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for i in range(e2e_steps):
+        s = sets[i % SETS]
+        s["X"].copy_(hX, non_blocking=True)
+        s["R"].copy_(hR, non_blocking=True)
+        q.apr_qgemm(QTYPE, s["W"], N, K, s["X"], T, s["Y"], s["R"], stream=stream)
+        hY.copy_(s["Y"], non_blocking=True)
+    x1.record(stream)
+    torch.cuda.synchronize()
+    q.apr_stream_status(stream)
+    e2e_t, e2e_flop = reduce_over_ranks(x0.elapsed_time(x1) / 1e3, FLOP * e2e_steps, ws)
+    assert np.isfinite(hY.numpy()).all()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "qtype": "Q4_0", "n": N, "k": K, "T": T, "residual": True,
+                       "leg": "f16 inputs, f32 accumulate", "l2": f"{SETS} rotating input sets (277 MB > 2x L2)",
+                       "parallelism": f"replicas x{ws}"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                         "frac": achieved / peak_tf, "traffic": traffic,
+                         "kernel": "gemm_tc_kernel<Q4_0, residual, BN=128>",
+                         "peak_kind": f"{peak_kind} bf16 dense burst (fp16 has the same nominal rate)",
+                         "kernel_ms": gemm_s * 1e3},
+            "e2e": {"value": e2e_flop / e2e_t / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": 2 * T * N * 4, "d2h_bytes_per_step": T * N * 4},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk.summary(),
+            "gemv": gemv,
+        }
+        if not args.no_cpu:
+            line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def gemv_rate(q, synth, dev, stream, peak_gbs):
+    """T = 1 GEMV over a Q4_0 4096 x 4096 weight, 16 rotating weights (151 MB)."""
+    import torch
+
+    n, k, nsets = 4096, 4096, 16
+    c = synth.make_case(QTYPE, n, k, 1, seed=0)
+    Ws = [torch.from_numpy(c["W"]).to(dev) for _ in range(nsets)]
+    X = torch.from_numpy(c["X"]).to(dev)
+    Y = torch.empty((1, n), device=dev)
+    for i in range(20):
+        q.apr_qgemv(QTYPE, Ws[i % nsets], n, k, X, 1, Y, stream=stream)
+    torch.cuda.synchronize()
+    reps = 2000
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(reps):
+        q.apr_qgemv(QTYPE, Ws[i % nsets], n, k, X, 1, Y, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    q.apr_stream_status(stream)
+    dt = a.elapsed_time(b) / 1e3 / reps
+    byts = n * (k // 32) * 18 + k * 4 + n * 4
+    gbs = byts / dt / 1e9
+    return {"workload": "q4_0_gemv_n4096_k4096_t1", "GB/s": gbs, "frac_hbm": gbs / peak_gbs, "us": dt * 1e6}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+/*
+ * apr_qgemm.h — C ABI of the GB300 (sm_103a) prefill projections over GGUF
+ * Q4_0 / Q8_0 block-quantized weights.
+ *
+ * Every projection of a batched (chunked) prompt prefill is ONE product over
+ * the chunk's T token rows, instead of T per-token GEMVs:
+ *
+ *     Y[T][n] = X[T][k] . dequant(W)[n][k]^T  (+ R[T][n])
+ *
+ * (aprender-serve 0.70.2, src/cuda/executor/gdn_prefill_ops.rs, doc of
+ * qwen35_project_rows: all operands row major, W is [n x k]; the chunked
+ * driver of src/gguf/cuda/forward_qwen35_cuda_prefill.rs, module doc, runs
+ * every projection as one product over the chunk's rows.)
+ *
+ * Weight format (GGUF blocks of 32 weights along k, kept in their on-disk
+ * array-of-blocks order — oxibonsai-kernels 0.1.4,
+ * src/gpu_backend/cuda_q_std_prefill.rs, module doc "Weight layout"; block
+ * size and scale position from that page's test make_q4_0_zeros):
+ *   Q4_0 (18 bytes): fp16 d (little endian) then 16 bytes; byte j holds
+ *                    element j in its low nibble and element j+16 in its high
+ *                    nibble; w = d * (nibble - 8).
+ *   Q8_0 (34 bytes): fp16 d then 32 int8 q; w = d * q.
+ * Row i of W is the k/32 consecutive blocks starting at byte i*(k/32)*bytes.
+ *
+ * Memory and streams. Every pointer argument named W, Wu, X, residual, Y or
+ * out is a DEVICE pointer on the current CUDA device, owned by the caller and
+ * never freed or retained by the library. Every call is asynchronous on the
+ * given stream (NULL = the legacy default stream): a return of APR_OK means the
+ * work was enqueued. X, residual, Y and out are float32, row major, densely
+ * packed (row stride = number of columns). Device pointers must be 16-byte
+ * aligned. The GEMM path takes a stream-ordered scratch of T*k*2 bytes (the
+ * fp16 copy of X) from a memory pool the library owns per device; it is
+ * released on the same stream when the call's work is done. Weights are
+ * never dequantized to memory: blocks are decoded in registers.
+ *
+ * Errors. Arguments are checked on the host before anything is enqueued:
+ *   APR_E_INVAL   null pointer with nonzero sizes, n < 0, T < 0, k <= 0,
+ *                 k % 32 != 0, a size beyond the documented limits, or an
+ *                 unknown leg / path
+ *   APR_E_QTYPE   qtype is not APR_Q4_0 or APR_Q8_0
+ *   APR_E_ALIGN   a pointer is not 16-byte aligned
+ *   APR_E_ALIAS   Y overlaps X, W or Wu, or overlaps residual without being
+ *                 exactly the same buffer (Y == residual is allowed: it gives
+ *                 Y += X.W^T, the accumulate form of the pages' batch kernels)
+ *   APR_E_DEVICE  no CUDA device, or the device is not compute capability 10.3
+ *   APR_E_NOMEM   the scratch pool could not provide the fp16 copy of X
+ *   APR_E_LAUNCH  a CUDA launch or API call failed (see apr_last_error)
+ *   APR_E_TIMEOUT reported by apr_stream_status: a bounded device-side wait
+ *                 expired and the kernel gave up (results are garbage)
+ * T == 0 or n == 0 is a successful no-op (oxibonsai-kernels
+ * try_cuda_prefill_q_std returns at once for an empty batch). On any error Y
+ * is unspecified and must be discarded.
+ *
+ * Limits: n, T <= 2^24, k <= 2^20, n*k/32 blocks <= 2^31.
+ */
+#ifndef APR_QGEMM_H
+#define APR_QGEMM_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* apr_stream_t;
+
+/* GGUF tensor type ids. */
+enum { APR_Q4_0 = 2, APR_Q8_0 = 8 };
+
+/*
+ * Arithmetic legs (aprender-serve gdn_prefill_ops.rs, module doc, group 1):
+ *   APR_LEG_F16        X and the decoded weights are rounded to fp16, products
+ *                      accumulate in fp32 on the tensor cores, Y is fp32
+ *                      (the pages' f16 leg, their default).
+ *   APR_LEG_EXACT_F32  fp32 inputs, fp32 accumulation, no reduced-precision
+ *                      rounding of X or W (the pages' f32 leg, kept for
+ *                      projections that feed a recurrence).
+ */
+enum { APR_LEG_F16 = 0, APR_LEG_EXACT_F32 = 1 };
+
+/* Kernel choice: AUTO applies the T rule below; the others force a path. */
+enum { APR_PATH_AUTO = 0, APR_PATH_GEMV = 1, APR_PATH_GEMM = 2 };
+
+enum {
+  APR_OK = 0,
+  APR_E_INVAL = -1,
+  APR_E_QTYPE = -2,
+  APR_E_ALIGN = -3,
+  APR_E_ALIAS = -4,
+  APR_E_DEVICE = -5,
+  APR_E_LAUNCH = -6,
+  APR_E_TIMEOUT = -7,
+  APR_E_NOMEM = -8
+};
+
+/*
+ * The T rule: with APR_PATH_AUTO, 1 <= T <= apr_gemv_max_T() runs the small-T
+ * GEMV (exact fp32 arithmetic whatever the leg), T above it runs the GEMM.
+ */
+#define APR_GEMV_MAX_T 16
+int apr_gemv_max_T(void);
+
+/*
+ * Y = X . dequant(W)^T (+ residual), fp16 leg, T rule.
+ *   qtype     APR_Q4_0 or APR_Q8_0
+ *   W         [n rows][k/32 blocks] GGUF blocks
+ *   X         [T][k] f32;  Y [T][n] f32, overwritten
+ *   residual  [T][n] f32 or NULL; may be Y itself (accumulate)
+ * The residual variant is the residual-add GEMM of oxibonsai-kernels
+ * (gemm_q4_0_residual / gemm_q8_0_residual; the down and output projections
+ * are followed by a residual add in encode_q_std_ffn_phase step 3 and
+ * prefill_ffn_rows).
+ */
+int apr_qgemm(int qtype, const void* W, int n, int k, const float* X, int T,
+              float* Y, const float* residual, apr_stream_t stream);
+
+/*
+ * Fused gate/up SwiGLU: Y = silu(X . Wg^T) * (X . Wu^T), silu(g) = g/(1+e^-g).
+ * Wg and Wu are two [n][k] weights of the same qtype (the pages keep them as
+ * one buffer, gate rows then up rows: oxibonsai-kernels try_cuda_prefill_q_std
+ * and launch_fused_gate_up_swiglu_q4_0; here they are two pointers, which
+ * covers that buffer with Wu = Wg + n*k/32*bytes). No residual. fp16 leg,
+ * T rule.
+ */
+int apr_qgemm_gate_up_swiglu(int qtype, const void* Wg, const void* Wu, int n, int k,
+                             const float* X, int T, float* Y, apr_stream_t stream);
+
+/*
+ * Small-T GEMV, 1 <= T <= APR_GEMV_MAX_T (T == 0 is a no-op): one warp per W
+ * row, coalesced 16-byte block loads, T fp32 accumulators, exact fp32
+ * arithmetic, optional residual (gemv_q4_0_pf / gemv_q8_0_pf of
+ * oxibonsai-kernels, used for the last-token lm_head in
+ * try_cuda_prefill_q_std). T > APR_GEMV_MAX_T gives APR_E_INVAL.
+ */
+int apr_qgemv(int qtype, const void* W, int n, int k, const float* X, int T,
+              float* Y, const float* residual, apr_stream_t stream);
+
+/*
+ * Full form. Wu != NULL selects the gate/up SwiGLU product (W is the gate;
+ * residual must be NULL). leg and path as above; APR_PATH_GEMV needs
+ * T <= APR_GEMV_MAX_T. The exact leg on the GEMM path runs fp32 FFMA.
+ */
+typedef struct apr_qgemm_args {
+  int qtype;
+  int leg;
+  int path;
+  const void* W;
+  const void* Wu;
+  int n;
+  int k;
+  int T;
+  const float* X;
+  const float* residual;
+  float* Y;
+  apr_stream_t stream;
+} apr_qgemm_args;
+int apr_qgemm_ex(const apr_qgemm_args* args);
+
+/*
+ * The fp16 leg in two calls, for callers that keep their own fp16 copy of the
+ * activations (the pages' f16 leg also rounds the activation rows to fp16 in a
+ * pass of its own, convert_f32_to_f16, before its fp16 GEMM:
+ * aprender-serve gdn_prefill_ops.rs qwen35_project_rows_f16).
+ *
+ * apr_convert_f32_to_f16: X16[i] = fp16(X[i]) (round to nearest even) for
+ *   0 <= i < count; X (f32) and X16 (fp16, 2 bytes each) are device buffers,
+ *   16-byte aligned, not overlapping. count == 0 is a no-op.
+ * apr_qgemm_f16_in: as apr_qgemm (Wu == NULL) or apr_qgemm_gate_up_swiglu
+ *   (Wu != NULL, residual must be NULL) on the tensor cores, with X16 [T][k]
+ *   fp16 already converted; needs k % 256 == 0 (APR_E_INVAL otherwise), takes
+ *   no scratch and ignores the T rule (always the GEMM).
+ */
+int apr_convert_f32_to_f16(const float* X, long long count, void* X16, apr_stream_t stream);
+int apr_qgemm_f16_in(int qtype, const void* W, const void* Wu, int n, int k, const void* X16, int T,
+                     float* Y, const float* residual, apr_stream_t stream);
+
+/*
+ * Standalone dequant: out[n][k] f32 = f32(d) * f32(q'), bit exact (the product
+ * of an fp16 scale and a code of at most 8 bits is exact in fp32). The device
+ * dequant of aprender-serve gdn_prefill_ops.rs qwen35_dequant_f32 (Q8_0 and
+ * the other formats it dispatches), here for Q4_0 and Q8_0 and meant for
+ * tests: the projections never write decoded weights to memory.
+ */
+int apr_dequant(int qtype, const void* W, int n, int k, float* out, apr_stream_t stream);
+
+/*
+ * Synchronizes the stream, then reports and clears the device status word:
+ * APR_OK, APR_E_TIMEOUT if a kernel's bounded wait expired since the last
+ * call, or APR_E_LAUNCH if the stream reported a CUDA error.
+ */
+int apr_stream_status(apr_stream_t stream);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* apr_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* APR_QGEMM_H */

@@ -1,0 +1,232 @@
+"""ctypes binding of libapr_qgemm (include/apr_qgemm.h), same names.
+
+Argument marshalling only: tensors become device pointers, sizes are checked
+against the tensors so that no call can address past an allocation, and a
+nonzero status raises :class:`AprError`. Every step of the computation runs
+in the CUDA library; there is no fallback, and importing this module fails if
+the library has not been built.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libapr_qgemm.so")
+
+APR_Q4_0 = 2
+APR_Q8_0 = 8
+APR_LEG_F16 = 0
+APR_LEG_EXACT_F32 = 1
+APR_PATH_AUTO = 0
+APR_PATH_GEMV = 1
+APR_PATH_GEMM = 2
+APR_OK = 0
+APR_E_INVAL = -1
+APR_E_QTYPE = -2
+APR_E_ALIGN = -3
+APR_E_ALIAS = -4
+APR_E_DEVICE = -5
+APR_E_LAUNCH = -6
+APR_E_TIMEOUT = -7
+APR_E_NOMEM = -8
+APR_GEMV_MAX_T = 16
+
+BLOCK_BYTES = {APR_Q4_0: 18, APR_Q8_0: 34}
+
+# Every symbol include/apr_qgemm.h declares.
+EXPORTS = (
+    "apr_gemv_max_T",
+    "apr_qgemm",
+    "apr_qgemm_gate_up_swiglu",
+    "apr_qgemv",
+    "apr_qgemm_ex",
+    "apr_convert_f32_to_f16",
+    "apr_qgemm_f16_in",
+    "apr_dequant",
+    "apr_stream_status",
+    "apr_last_error",
+)
+
+
+class AprError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"apr status {status}: {message}")
+        self.status = status
+
+
+class _Args(ctypes.Structure):
+    _fields_ = [
+        ("qtype", ctypes.c_int),
+        ("leg", ctypes.c_int),
+        ("path", ctypes.c_int),
+        ("W", ctypes.c_void_p),
+        ("Wu", ctypes.c_void_p),
+        ("n", ctypes.c_int),
+        ("k", ctypes.c_int),
+        ("T", ctypes.c_int),
+        ("X", ctypes.c_void_p),
+        ("residual", ctypes.c_void_p),
+        ("Y", ctypes.c_void_p),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built: run quantized_weight_prefill_q4_gb300.build.build_library() (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, ci = ctypes.c_void_p, ctypes.c_int
+    sig = {
+        "apr_gemv_max_T": ([], ci),
+        "apr_qgemm": ([ci, vp, ci, ci, vp, ci, vp, vp, vp], ci),
+        "apr_qgemm_gate_up_swiglu": ([ci, vp, vp, ci, ci, vp, ci, vp, vp], ci),
+        "apr_qgemv": ([ci, vp, ci, ci, vp, ci, vp, vp, vp], ci),
+        "apr_qgemm_ex": ([ctypes.POINTER(_Args)], ci),
+        "apr_convert_f32_to_f16": ([vp, ctypes.c_longlong, vp, vp], ci),
+        "apr_qgemm_f16_in": ([ci, vp, vp, ci, ci, vp, ci, vp, vp, vp], ci),
+        "apr_dequant": ([ci, vp, ci, ci, vp, vp], ci),
+        "apr_stream_status": ([vp], ci),
+        "apr_last_error": ([], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    return lib
+
+
+_lib = _load()
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def _check(status: int) -> int:
+    if status != APR_OK:
+        raise AprError(status, _lib.apr_last_error().decode(errors="replace"))
+    return status
+
+
+def _ptr(x, name: str, *, dtype=None, min_bytes: int = 0):
+    """Device pointer of a CUDA tensor (checked), an int (trusted), or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    import torch
+
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{name}: expected a CUDA tensor or a device pointer, got {type(x).__name__}")
+    if not x.is_cuda:
+        raise ValueError(f"{name}: tensor is on {x.device}, the library takes device memory")
+    if not x.is_contiguous():
+        raise ValueError(f"{name}: tensor must be contiguous")
+    if dtype is not None and x.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {x.dtype}")
+    nbytes = x.numel() * x.element_size()
+    if nbytes < min_bytes:
+        raise ValueError(f"{name}: holds {nbytes} bytes, the call addresses {min_bytes}")
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _sizes(qtype, n, k, T):
+    bb = BLOCK_BYTES.get(qtype, 0)
+    n_, k_, T_ = max(n, 0), max(k, 0), max(T, 0)
+    return n_ * (k_ // 32) * bb, T_ * k_ * 4, T_ * n_ * 4
+
+
+def _dtypes():
+    import torch
+
+    return torch.uint8, torch.float32
+
+
+def apr_gemv_max_T() -> int:
+    return _lib.apr_gemv_max_T()
+
+
+def apr_last_error() -> str:
+    return _lib.apr_last_error().decode(errors="replace")
+
+
+def apr_qgemm(qtype, W, n, k, X, T, Y, residual=None, stream=None) -> int:
+    u8, f32 = _dtypes()
+    wb, xb, yb = _sizes(qtype, n, k, T)
+    return _check(_lib.apr_qgemm(qtype, _ptr(W, "W", dtype=u8, min_bytes=wb), n, k,
+                                 _ptr(X, "X", dtype=f32, min_bytes=xb), T,
+                                 _ptr(Y, "Y", dtype=f32, min_bytes=yb),
+                                 _ptr(residual, "residual", dtype=f32, min_bytes=yb), _stream(stream)))
+
+
+def apr_qgemm_gate_up_swiglu(qtype, Wg, Wu, n, k, X, T, Y, stream=None) -> int:
+    u8, f32 = _dtypes()
+    wb, xb, yb = _sizes(qtype, n, k, T)
+    return _check(_lib.apr_qgemm_gate_up_swiglu(qtype, _ptr(Wg, "Wg", dtype=u8, min_bytes=wb),
+                                                _ptr(Wu, "Wu", dtype=u8, min_bytes=wb), n, k,
+                                                _ptr(X, "X", dtype=f32, min_bytes=xb), T,
+                                                _ptr(Y, "Y", dtype=f32, min_bytes=yb), _stream(stream)))
+
+
+def apr_qgemv(qtype, W, n, k, X, T, Y, residual=None, stream=None) -> int:
+    u8, f32 = _dtypes()
+    wb, xb, yb = _sizes(qtype, n, k, T)
+    return _check(_lib.apr_qgemv(qtype, _ptr(W, "W", dtype=u8, min_bytes=wb), n, k,
+                                 _ptr(X, "X", dtype=f32, min_bytes=xb), T,
+                                 _ptr(Y, "Y", dtype=f32, min_bytes=yb),
+                                 _ptr(residual, "residual", dtype=f32, min_bytes=yb), _stream(stream)))
+
+
+def apr_qgemm_ex(qtype, W, n, k, X, T, Y, *, residual=None, Wu=None, leg=APR_LEG_F16, path=APR_PATH_AUTO,
+                 stream=None) -> int:
+    u8, f32 = _dtypes()
+    wb, xb, yb = _sizes(qtype, n, k, T)
+    a = _Args(qtype, leg, path, _ptr(W, "W", dtype=u8, min_bytes=wb), _ptr(Wu, "Wu", dtype=u8, min_bytes=wb),
+              n, k, T, _ptr(X, "X", dtype=f32, min_bytes=xb), _ptr(residual, "residual", dtype=f32, min_bytes=yb),
+              _ptr(Y, "Y", dtype=f32, min_bytes=yb), _stream(stream))
+    return _check(_lib.apr_qgemm_ex(ctypes.byref(a)))
+
+
+def apr_convert_f32_to_f16(X, count, X16, stream=None) -> int:
+    import torch
+
+    return _check(_lib.apr_convert_f32_to_f16(_ptr(X, "X", dtype=torch.float32, min_bytes=4 * max(count, 0)), count,
+                                              _ptr(X16, "X16", dtype=torch.float16, min_bytes=2 * max(count, 0)),
+                                              _stream(stream)))
+
+
+def apr_qgemm_f16_in(qtype, W, n, k, X16, T, Y, residual=None, Wu=None, stream=None) -> int:
+    import torch
+
+    u8, f32 = _dtypes()
+    wb, xb, yb = _sizes(qtype, n, k, T)
+    return _check(_lib.apr_qgemm_f16_in(qtype, _ptr(W, "W", dtype=u8, min_bytes=wb),
+                                        _ptr(Wu, "Wu", dtype=u8, min_bytes=wb), n, k,
+                                        _ptr(X16, "X16", dtype=torch.float16, min_bytes=xb // 2), T,
+                                        _ptr(Y, "Y", dtype=f32, min_bytes=yb),
+                                        _ptr(residual, "residual", dtype=f32, min_bytes=yb), _stream(stream)))
+
+
+def apr_dequant(qtype, W, n, k, out, stream=None) -> int:
+    u8, f32 = _dtypes()
+    wb, _, _ = _sizes(qtype, n, k, 0)
+    ob = max(n, 0) * max(k, 0) * 4
+    return _check(_lib.apr_dequant(qtype, _ptr(W, "W", dtype=u8, min_bytes=wb), n, k,
+                                   _ptr(out, "out", dtype=f32, min_bytes=ob), _stream(stream)))
+
+
+def apr_stream_status(stream=None) -> int:
+    return _check(_lib.apr_stream_status(_stream(stream)))

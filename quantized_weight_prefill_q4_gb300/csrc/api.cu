@@ -1,0 +1,281 @@
+// C ABI of libapr_qgemm: argument checks, the T rule, scratch, launches.
+//
+// Argument checking follows the pattern of aprender-serve 0.70.2
+// src/cuda/executor/gdn_prefill_ops.rs (qp_launch checks every pointer
+// argument before a launch; qwen35_dequant_f32 refuses a weight type it has no
+// kernel for) and oxibonsai-kernels 0.1.4 try_cuda_prefill_q_std (an empty
+// batch returns success without work).
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "apr_qgemm.h"
+#include "apr_internal.h"
+
+using namespace apr;
+
+namespace {
+
+// Status word of the kernels' bounded waits, one per device (module-scope
+// __device__ variables exist once per device that loads the library).
+__device__ unsigned g_status;
+
+thread_local char t_msg[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_msg, sizeof t_msg, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::once_flag once;
+  int checked = 0;          // APR_OK or APR_E_DEVICE
+  unsigned* status = nullptr;
+  cudaMemPool_t pool = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+
+int device_state(DeviceState** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return fail(APR_E_DEVICE, "no usable CUDA device (%s)", cudaGetErrorString(e));
+  }
+  DeviceState& st = g_dev[dev];
+  std::call_once(st.once, [&st, dev] {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess || prop.major != 10 || prop.minor != 3) {
+      cudaGetLastError();
+      st.checked = APR_E_DEVICE;
+      return;
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) {
+      cudaGetLastError();
+      st.checked = APR_E_DEVICE;
+      return;
+    }
+    st.status = static_cast<unsigned*>(p);
+    cudaMemPoolProps props;
+    memset(&props, 0, sizeof props);
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    if (cudaMemPoolCreate(&st.pool, &props) != cudaSuccess) {
+      cudaGetLastError();
+      st.checked = APR_E_DEVICE;
+      return;
+    }
+    uint64_t keep = UINT64_MAX;  // keep freed scratch in the pool
+    cudaMemPoolSetAttribute(st.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    st.checked = APR_OK;
+  });
+  if (st.checked != APR_OK)
+    return fail(APR_E_DEVICE, "device %d is not a compute capability 10.3 GPU (GB300) or failed to initialise", dev);
+  *out = &st;
+  return APR_OK;
+}
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+struct Problem {
+  int qtype, leg, path;
+  const void* W;
+  const void* Wu;
+  int n, k, T;
+  const float* X;
+  const float* R;
+  float* Y;
+  cudaStream_t s;
+};
+
+// Host-side checks; returns APR_OK, an error, or 1 for "nothing to do".
+int check(const Problem& p, size_t x_elem_bytes = 4) {
+  if (p.qtype != APR_Q4_0 && p.qtype != APR_Q8_0) return fail(APR_E_QTYPE, "unsupported qtype %d", p.qtype);
+  if (p.leg != APR_LEG_F16 && p.leg != APR_LEG_EXACT_F32) return fail(APR_E_INVAL, "unknown leg %d", p.leg);
+  if (p.path != APR_PATH_AUTO && p.path != APR_PATH_GEMV && p.path != APR_PATH_GEMM)
+    return fail(APR_E_INVAL, "unknown path %d", p.path);
+  if (p.n < 0 || p.T < 0 || p.k <= 0 || p.k % 32 != 0)
+    return fail(APR_E_INVAL, "bad sizes n=%d k=%d T=%d (need n >= 0, T >= 0, k > 0, k %% 32 == 0)", p.n, p.k, p.T);
+  if (p.n > (1 << 24) || p.T > (1 << 24) || p.k > (1 << 20) || (int64_t)p.n * (p.k / 32) > (int64_t)1 << 31)
+    return fail(APR_E_INVAL, "sizes beyond the supported limits");
+  if (p.path == APR_PATH_GEMV && p.T > APR_GEMV_MAX_T)
+    return fail(APR_E_INVAL, "the GEMV path takes T <= %d (got %d)", APR_GEMV_MAX_T, p.T);
+  if (p.n == 0 || p.T == 0) return 1;
+  if (!p.W || !p.X || !p.Y) return fail(APR_E_INVAL, "null pointer (W, X or Y)");
+  const void* ptrs[5] = {p.W, p.Wu, p.X, p.R, p.Y};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return fail(APR_E_ALIGN, "pointer %p is not 16-byte aligned", q);
+  const size_t wbytes = (size_t)p.n * (size_t)(p.k / 32) * (size_t)block_bytes(p.qtype);
+  const size_t xbytes = (size_t)p.T * (size_t)p.k * x_elem_bytes;
+  const size_t ybytes = (size_t)p.T * (size_t)p.n * 4;
+  if (overlap(p.Y, ybytes, p.X, xbytes)) return fail(APR_E_ALIAS, "Y overlaps X");
+  if (overlap(p.Y, ybytes, p.W, wbytes)) return fail(APR_E_ALIAS, "Y overlaps W");
+  if (p.Wu && overlap(p.Y, ybytes, p.Wu, wbytes)) return fail(APR_E_ALIAS, "Y overlaps Wu");
+  if (p.R && p.R != p.Y && overlap(p.Y, ybytes, p.R, ybytes))
+    return fail(APR_E_ALIAS, "Y partially overlaps residual");
+  if (p.Wu && p.R) return fail(APR_E_INVAL, "the gate/up SwiGLU product takes no residual");
+  return APR_OK;
+}
+
+int check_f16_in(const Problem& p) { return check(p, 2); }
+
+int launched(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(APR_E_LAUNCH, "%s: %s", what, cudaGetErrorString(e));
+  return APR_OK;
+}
+
+int run(const Problem& p) {
+  int rc = check(p);
+  if (rc == 1) return APR_OK;
+  if (rc != APR_OK) return rc;
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != APR_OK) return rc;
+
+  int path = p.path;
+  if (path == APR_PATH_AUTO) path = p.T <= APR_GEMV_MAX_T ? APR_PATH_GEMV : APR_PATH_GEMM;
+  if (path == APR_PATH_GEMV)
+    return launched(launch_gemv(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, p.R, p.s), "gemv");
+  // GEMM: the tensor-core leg needs every raw 256-column chunk of a weight row
+  // to start on a 16-byte boundary (k % 256 == 0); the exact leg and other k
+  // run the FFMA kernel.
+  if (p.leg == APR_LEG_EXACT_F32 || p.k % 256 != 0)
+    return launched(launch_gemm_simt(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, p.R, p.s), "gemm_simt");
+
+  const size_t count = (size_t)p.T * (size_t)p.k;
+  void* x16 = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&x16, count * 2, st->pool, p.s);
+  if (e != cudaSuccess) return fail(APR_E_NOMEM, "scratch for fp16 X (%zu bytes): %s", count * 2, cudaGetErrorString(e));
+  rc = launched(launch_x_to_f16(p.X, static_cast<uint16_t*>(x16), count, p.s), "x_to_f16");
+  if (rc == APR_OK) {
+    char msg[256] = "";
+    if (launch_gemm_tc(p.qtype, p.W, p.Wu, p.n, p.k, static_cast<const uint16_t*>(x16), p.T, p.Y, p.R, st->status,
+                       p.s, msg, sizeof msg) != 0)
+      rc = fail(APR_E_LAUNCH, "%s", msg);
+  }
+  e = cudaFreeAsync(x16, p.s);
+  if (rc == APR_OK && e != cudaSuccess) rc = fail(APR_E_LAUNCH, "cudaFreeAsync: %s", cudaGetErrorString(e));
+  return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int apr_gemv_max_T(void) { return APR_GEMV_MAX_T; }
+
+const char* apr_last_error(void) { return t_msg; }
+
+int apr_qgemm(int qtype, const void* W, int n, int k, const float* X, int T, float* Y, const float* residual,
+              apr_stream_t stream) {
+  t_msg[0] = 0;
+  return run(Problem{qtype, APR_LEG_F16, APR_PATH_AUTO, W, nullptr, n, k, T, X, residual, Y, (cudaStream_t)stream});
+}
+
+int apr_qgemm_gate_up_swiglu(int qtype, const void* Wg, const void* Wu, int n, int k, const float* X, int T, float* Y,
+                             apr_stream_t stream) {
+  t_msg[0] = 0;
+  if (!Wu && n > 0 && T > 0) return fail(APR_E_INVAL, "null up weight");
+  return run(Problem{qtype, APR_LEG_F16, APR_PATH_AUTO, Wg, Wu, n, k, T, X, nullptr, Y, (cudaStream_t)stream});
+}
+
+int apr_qgemv(int qtype, const void* W, int n, int k, const float* X, int T, float* Y, const float* residual,
+              apr_stream_t stream) {
+  t_msg[0] = 0;
+  return run(Problem{qtype, APR_LEG_EXACT_F32, APR_PATH_GEMV, W, nullptr, n, k, T, X, residual, Y,
+                     (cudaStream_t)stream});
+}
+
+int apr_qgemm_ex(const apr_qgemm_args* a) {
+  t_msg[0] = 0;
+  if (!a) return fail(APR_E_INVAL, "null argument struct");
+  return run(Problem{a->qtype, a->leg, a->path, a->W, a->Wu, a->n, a->k, a->T, a->X, a->residual, a->Y,
+                     (cudaStream_t)a->stream});
+}
+
+int apr_convert_f32_to_f16(const float* X, long long count, void* X16, apr_stream_t stream) {
+  t_msg[0] = 0;
+  if (count < 0) return fail(APR_E_INVAL, "negative count");
+  if (count == 0) return APR_OK;
+  if (!X || !X16) return fail(APR_E_INVAL, "null pointer");
+  if (!aligned16(X) || !aligned16(X16)) return fail(APR_E_ALIGN, "X and X16 must be 16-byte aligned");
+  if (overlap(X, (size_t)count * 4, X16, (size_t)count * 2)) return fail(APR_E_ALIAS, "X16 overlaps X");
+  DeviceState* st = nullptr;
+  const int rc = device_state(&st);
+  if (rc != APR_OK) return rc;
+  return launched(launch_x_to_f16(X, static_cast<uint16_t*>(X16), (size_t)count, (cudaStream_t)stream),
+                  "convert_f32_to_f16");
+}
+
+int apr_qgemm_f16_in(int qtype, const void* W, const void* Wu, int n, int k, const void* X16, int T, float* Y,
+                     const float* residual, apr_stream_t stream) {
+  t_msg[0] = 0;
+  // Checked as an f32 problem of the same shape, then against the fp16 size.
+  Problem p{qtype, APR_LEG_F16, APR_PATH_GEMM, W, Wu, n, k, T, static_cast<const float*>(X16), residual, Y,
+            (cudaStream_t)stream};
+  if (k % 256 != 0 && k > 0) return fail(APR_E_INVAL, "the fp16-input GEMM needs k %% 256 == 0 (got %d)", k);
+  int rc = check_f16_in(p);
+  if (rc == 1) return APR_OK;
+  if (rc != APR_OK) return rc;
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != APR_OK) return rc;
+  char msg[256] = "";
+  if (launch_gemm_tc(qtype, W, Wu, n, k, static_cast<const uint16_t*>(X16), T, Y, residual, st->status,
+                     (cudaStream_t)stream, msg, sizeof msg) != 0)
+    return fail(APR_E_LAUNCH, "%s", msg);
+  return APR_OK;
+}
+
+int apr_dequant(int qtype, const void* W, int n, int k, float* out, apr_stream_t stream) {
+  t_msg[0] = 0;
+  if (qtype != APR_Q4_0 && qtype != APR_Q8_0) return fail(APR_E_QTYPE, "unsupported qtype %d", qtype);
+  if (n < 0 || k <= 0 || k % 32 != 0) return fail(APR_E_INVAL, "bad sizes n=%d k=%d", n, k);
+  if (n > (1 << 24) || k > (1 << 20) || (int64_t)n * (k / 32) > (int64_t)1 << 31)
+    return fail(APR_E_INVAL, "sizes beyond the supported limits");
+  if (n == 0) return APR_OK;
+  if (!W || !out) return fail(APR_E_INVAL, "null pointer");
+  const size_t wbytes = (size_t)n * (size_t)(k / 32) * (size_t)block_bytes(qtype);
+  if (overlap(out, (size_t)n * k * 4, W, wbytes)) return fail(APR_E_ALIAS, "out overlaps W");
+  DeviceState* st = nullptr;
+  const int rc = device_state(&st);
+  if (rc != APR_OK) return rc;
+  return launched(launch_dequant(qtype, W, n, k, out, (cudaStream_t)stream), "dequant");
+}
+
+int apr_stream_status(apr_stream_t stream) {
+  t_msg[0] = 0;
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != APR_OK) return rc;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(APR_E_LAUNCH, "stream: %s", cudaGetErrorString(e));
+  unsigned v = 0;
+  e = cudaMemcpy(&v, st->status, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(APR_E_LAUNCH, "status read: %s", cudaGetErrorString(e));
+  if (v) {
+    const unsigned zero = 0;
+    cudaMemcpy(st->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    return fail(APR_E_TIMEOUT, "a kernel's bounded wait gave up (status 0x%x)", v);
+  }
+  return APR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,37 @@
+// Launchers shared between the C ABI (api.cu) and the kernel files. Host only.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace apr {
+
+constexpr int kQ4_0 = 2;
+constexpr int kQ8_0 = 8;
+
+inline int block_bytes(int qtype) { return qtype == kQ4_0 ? 18 : 34; }
+
+// Epilogue of a projection.
+enum Epilogue { kEpiPlain = 0, kEpiResidual = 1, kEpiSwiGLU = 2 };
+
+// Standalone dequant (dequant.cu).
+cudaError_t launch_dequant(int qtype, const void* W, int n, int k, float* out, cudaStream_t s);
+
+// Small-T GEMV, exact fp32 (gemv.cu). Wu != nullptr: gate/up SwiGLU.
+cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
+                        float* Y, const float* R, cudaStream_t s);
+
+// Exact-fp32 FFMA GEMM for any k % 32 == 0 (gemm_simt.cu).
+cudaError_t launch_gemm_simt(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
+                             float* Y, const float* R, cudaStream_t s);
+
+// fp16 copy of X, round to nearest even (gemm_tc.cu).
+cudaError_t launch_x_to_f16(const float* X, uint16_t* X16, size_t count, cudaStream_t s);
+
+// tcgen05 fp16-input GEMM; needs k % 256 == 0 and X16 = fp16(X) (gemm_tc.cu).
+// `status` is the device status word.
+int launch_gemm_tc(int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T,
+                   float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len);
+
+}  // namespace apr

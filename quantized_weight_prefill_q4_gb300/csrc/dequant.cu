@@ -1,0 +1,53 @@
+// Standalone block dequant: out[n][k] = f32(d) * f32(q'), bit exact.
+//
+// The device dequant of aprender-serve 0.70.2 src/cuda/executor/gdn_prefill_ops.rs
+// (qwen35_dequant_f32: one 32-element block per warp, one element per lane),
+// kept for tests; the projections decode blocks in registers instead.
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "apr_internal.h"
+
+namespace apr {
+namespace {
+
+template <int QT>
+__global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict__ W, int n, int k,
+                                                      float* __restrict__ out) {
+  constexpr int BB = QT == kQ4_0 ? 18 : 34;
+  const size_t total = (size_t)n * (size_t)k;
+  const size_t nb_row = (size_t)(k / 32);
+  for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const size_t row = idx / (size_t)k;
+    const uint32_t col = (uint32_t)(idx - row * (size_t)k);
+    const uint8_t* blk = W + (row * nb_row + col / 32) * BB;
+    const uint32_t e = col & 31u;
+    const uint16_t dbits = (uint16_t)blk[0] | ((uint16_t)blk[1] << 8);
+    const float d = __half2float(__ushort_as_half(dbits));  // exact widening
+    int q;
+    if (QT == kQ4_0) {
+      const uint32_t byte = blk[2 + (e & 15u)];
+      q = (int)((e < 16 ? byte : (byte >> 4)) & 0xFu) - 8;
+    } else {
+      q = (int)(int8_t)blk[2 + e];
+    }
+    out[idx] = d * (float)q;  // exact: <= 11 x 8 significant bits
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dequant(int qtype, const void* W, int n, int k, float* out, cudaStream_t s) {
+  const size_t total = (size_t)n * (size_t)k;
+  size_t blocks = (total + 255) / 256;
+  if (blocks > 152 * 64) blocks = 152 * 64;
+  if (qtype == kQ4_0)
+    dequant_kernel<kQ4_0><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);
+  else
+    dequant_kernel<kQ8_0><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);
+  return cudaGetLastError();
+}
+
+}  // namespace apr

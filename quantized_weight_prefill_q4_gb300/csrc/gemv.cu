@@ -1,0 +1,238 @@
+// Small-T GEMV over Q4_0 / Q8_0 blocks, exact fp32 arithmetic.
+//
+// Y[t][i] = sum_j X[t][j] * d_{i,j/32} * q'_{i,j} (+ R[t][i]) for T <= 16 token
+// rows, or silu(g) * u for a gate/up pair. The single-token GEMVs of
+// oxibonsai-kernels 0.1.4 src/gpu_backend/cuda_q_std_prefill.rs
+// (gemv_q4_0_pf / gemv_q8_0_pf, launched for the last-token lm_head), widened
+// to T accumulators so that one weight read serves up to 16 tokens.
+//
+// Layout of the work: one warp owns RW consecutive W rows at a time. The warp
+// walks the row in segments of 32 blocks; each segment is copied from global
+// memory with coalesced 16-byte loads (when every row starts on a 16-byte
+// boundary, i.e. k % 256 == 0; 2-byte loads otherwise) into a per-warp shared
+// buffer, then lane l decodes block l of the segment and multiplies it with
+// the matching 32 columns of each of the T activation rows (read through the
+// read-only cache; every warp of an SM walks the same columns). Per block the
+// lane keeps sum_j x_j * q'_j and scales it by d once; at the end of the row
+// the 32 lanes' partial sums are reduced with shuffles.
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "apr_internal.h"
+
+namespace apr {
+namespace {
+
+constexpr int kWarps = 8;
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+template <int QT, int TMAX, int RW, bool VEC, bool SWI>
+__global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const uint8_t* __restrict__ W,
+                                                           const uint8_t* __restrict__ Wu, int n, int k,
+                                                           const float* __restrict__ X, int T,
+                                                           float* Y,
+                                                           const float* R) {
+  constexpr int BB = QT == kQ4_0 ? 18 : 34;
+  constexpr int SEG = 32 * BB;
+  constexpr int NM = SWI ? 2 : 1;
+  __shared__ __align__(16) uint8_t stage[kWarps][NM * RW][SEG];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nb = k >> 5;
+  const size_t row_bytes = (size_t)nb * BB;
+  const int ngroups = (n + RW - 1) / RW;
+
+  for (int grp = blockIdx.x * kWarps + warp; grp < ngroups; grp += gridDim.x * kWarps) {
+    const int r0 = grp * RW;
+    float acc[NM][RW][TMAX];
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int r = 0; r < RW; ++r)
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t) acc[m][r][t] = 0.f;
+
+    for (int s = 0; s < nb; s += 32) {
+      const int nblk = min(32, nb - s);
+      const int seg_bytes = nblk * BB;
+      // ---- stage the segment of each row (and of the up rows)
+#pragma unroll
+      for (int m = 0; m < NM; ++m) {
+#pragma unroll
+        for (int r = 0; r < RW; ++r) {
+          const int row = r0 + r;
+          if (row >= n) continue;
+          const uint8_t* src = (m ? Wu : W) + (size_t)row * row_bytes + (size_t)s * BB;
+          uint8_t* dst = stage[warp][m * RW + r];
+          if (VEC) {
+            for (int c = lane; c < seg_bytes / 16; c += 32)
+              *reinterpret_cast<uint4*>(dst + c * 16) = ldg_nc_v4(src + c * 16);
+          } else {
+            for (int c = lane; c < seg_bytes / 2; c += 32)
+              *reinterpret_cast<uint16_t*>(dst + c * 2) = __ldg(reinterpret_cast<const unsigned short*>(src) + c);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane < nblk) {
+        const int col0 = (s + lane) * 32;
+        float part[NM][RW][TMAX];
+        float dsc[NM][RW];
+#pragma unroll
+        for (int m = 0; m < NM; ++m)
+#pragma unroll
+          for (int r = 0; r < RW; ++r) {
+            const uint8_t* blk = stage[warp][m * RW + r] + lane * BB;
+            const uint16_t db = *reinterpret_cast<const uint16_t*>(blk);
+            dsc[m][r] = __half2float(__ushort_as_half(db));
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) part[m][r][t] = 0.f;
+          }
+        // Q4_0: half h covers payload bytes 8h..8h+7, i.e. elements 8h..8h+7
+        // (low nibbles) and 16+8h..16+8h+7 (high nibbles).
+        // Q8_0: quarter h covers elements 8h..8h+7.
+        constexpr int NPART = QT == kQ4_0 ? 2 : 4;
+        constexpr int NE = QT == kQ4_0 ? 16 : 8;  // elements per part
+#pragma unroll
+        for (int h = 0; h < NPART; ++h) {
+          float wq[NM][RW][NE];
+#pragma unroll
+          for (int m = 0; m < NM; ++m)
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+              const uint8_t* pay = stage[warp][m * RW + r] + lane * BB + 2;
+              if constexpr (QT == kQ4_0) {
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                  const uint32_t two = *reinterpret_cast<const uint16_t*>(pay + 8 * h + e);
+                  wq[m][r][e] = (float)((int)(two & 0xFu) - 8);
+                  wq[m][r][e + 1] = (float)((int)((two >> 8) & 0xFu) - 8);
+                  wq[m][r][8 + e] = (float)((int)((two >> 4) & 0xFu) - 8);
+                  wq[m][r][8 + e + 1] = (float)((int)((two >> 12) & 0xFu) - 8);
+                }
+              } else {
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                  const uint32_t two = *reinterpret_cast<const uint16_t*>(pay + 8 * h + e);
+                  wq[m][r][e] = (float)(int8_t)(two & 0xFFu);
+                  wq[m][r][e + 1] = (float)(int8_t)(two >> 8);
+                }
+              }
+            }
+#pragma unroll
+          for (int t = 0; t < TMAX; ++t) {
+            if (t < T) {
+              const float* xr = X + (size_t)t * k + col0 + 8 * h;
+              const float4 a0 = __ldg(reinterpret_cast<const float4*>(xr));
+              const float4 a1 = __ldg(reinterpret_cast<const float4*>(xr + 4));
+              float xv[NE];
+              xv[0] = a0.x; xv[1] = a0.y; xv[2] = a0.z; xv[3] = a0.w;
+              xv[4] = a1.x; xv[5] = a1.y; xv[6] = a1.z; xv[7] = a1.w;
+              if constexpr (NE == 16) {
+                const float4 b0 = __ldg(reinterpret_cast<const float4*>(xr + 16));
+                const float4 b1 = __ldg(reinterpret_cast<const float4*>(xr + 20));
+                xv[8] = b0.x; xv[9] = b0.y; xv[10] = b0.z; xv[11] = b0.w;
+                xv[12] = b1.x; xv[13] = b1.y; xv[14] = b1.z; xv[15] = b1.w;
+              }
+#pragma unroll
+              for (int m = 0; m < NM; ++m)
+#pragma unroll
+                for (int r = 0; r < RW; ++r)
+#pragma unroll
+                  for (int e = 0; e < NE; ++e)
+                    part[m][r][t] = fmaf(wq[m][r][e], xv[e], part[m][r][t]);
+            }
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < NM; ++m)
+#pragma unroll
+          for (int r = 0; r < RW; ++r)
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) acc[m][r][t] = fmaf(dsc[m][r], part[m][r][t], acc[m][r][t]);
+      }
+      __syncwarp();
+    }
+
+    // ---- reduce over the lanes; lane t stores token t
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int r = 0; r < RW; ++r)
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t) {
+          float v = acc[m][r][t];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          acc[m][r][t] = v;
+        }
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+      const int row = r0 + r;
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        if (lane == t && t < T && row < n) {
+          const size_t o = (size_t)t * n + row;
+          float v;
+          if (SWI)
+            v = silu_mul(acc[0][r][t], acc[NM - 1][r][t]);
+          else
+            v = acc[0][r][t] + (R ? R[o] : 0.f);
+          Y[o] = v;
+        }
+      }
+    }
+  }
+}
+
+template <int QT, int TMAX, bool SWI>
+cudaError_t launch_t(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y,
+                     const float* R, cudaStream_t s) {
+  constexpr int RW = (TMAX >= 8 || SWI) ? 1 : 2;
+  const int ngroups = (n + RW - 1) / RW;
+  int blocks = (ngroups + kWarps - 1) / kWarps;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  const bool vec = (k % 256) == 0;
+  if (vec)
+    gemv_kernel<QT, TMAX, RW, true, SWI><<<blocks, kWarps * 32, 0, s>>>(
+        (const uint8_t*)W, (const uint8_t*)Wu, n, k, X, T, Y, R);
+  else
+    gemv_kernel<QT, TMAX, RW, false, SWI><<<blocks, kWarps * 32, 0, s>>>(
+        (const uint8_t*)W, (const uint8_t*)Wu, n, k, X, T, Y, R);
+  return cudaGetLastError();
+}
+
+template <int QT, bool SWI>
+cudaError_t launch_q(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y,
+                     const float* R, cudaStream_t s) {
+  if (T <= 1) return launch_t<QT, 1, SWI>(W, Wu, n, k, X, T, Y, R, s);
+  if (T <= 2) return launch_t<QT, 2, SWI>(W, Wu, n, k, X, T, Y, R, s);
+  if (T <= 4) return launch_t<QT, 4, SWI>(W, Wu, n, k, X, T, Y, R, s);
+  if (T <= 8) return launch_t<QT, 8, SWI>(W, Wu, n, k, X, T, Y, R, s);
+  return launch_t<QT, 16, SWI>(W, Wu, n, k, X, T, Y, R, s);
+}
+
+}  // namespace
+
+cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
+                        float* Y, const float* R, cudaStream_t s) {
+  const bool swi = Wu != nullptr;
+  if (qtype == kQ4_0)
+    return swi ? launch_q<kQ4_0, true>(W, Wu, n, k, X, T, Y, R, s)
+               : launch_q<kQ4_0, false>(W, Wu, n, k, X, T, Y, R, s);
+  return swi ? launch_q<kQ8_0, true>(W, Wu, n, k, X, T, Y, R, s)
+             : launch_q<kQ8_0, false>(W, Wu, n, k, X, T, Y, R, s);
+}
+
+}  // namespace apr

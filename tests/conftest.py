@@ -8,3 +8,18 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+
+
+import pytest  # noqa: E402
+
+
+@pytest.fixture(scope="session")
+def q():
+    """The binding, with the library built (in-tree) first."""
+    from quantized_weight_prefill_q4_gb300.build import build_library
+
+    build_library()
+    import quantized_weight_prefill_q4_gb300 as pkg
+
+    pkg.library()
+    return pkg

@@ -1,0 +1,122 @@
+"""The C-ABI library on the host (no GPU needed, no kernel launched).
+
+* it builds, loads and exports every symbol include/apr_qgemm.h declares;
+* the header and the binding agree on names and constants;
+* argument errors come back as the documented status codes before anything
+  touches the device (pointer checks as in aprender-serve 0.70.2
+  src/cuda/executor/gdn_prefill_ops.rs qp_launch; empty batch = success as in
+  oxibonsai-kernels 0.1.4 try_cuda_prefill_q_std).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "apr_qgemm.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(apr_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(q):
+    names = declared_functions()
+    assert len(names) == 10, names
+    lib = q.library()
+    for name in names:
+        assert hasattr(lib, name), name
+    assert sorted(q.EXPORTS) == names
+
+
+def test_header_constants_match_binding(q):
+    text = open(HEADER).read()
+    for name in ["APR_Q4_0", "APR_Q8_0", "APR_LEG_F16", "APR_LEG_EXACT_F32", "APR_PATH_AUTO", "APR_PATH_GEMV",
+                 "APR_PATH_GEMM", "APR_OK", "APR_E_INVAL", "APR_E_QTYPE", "APR_E_ALIGN", "APR_E_ALIAS",
+                 "APR_E_DEVICE", "APR_E_LAUNCH", "APR_E_TIMEOUT", "APR_E_NOMEM"]:
+        m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
+        assert m, name
+        assert int(m.group(1)) == getattr(q, name), name
+    assert q.library().apr_gemv_max_T() == q.APR_GEMV_MAX_T == 16
+
+
+# Raw calls through ctypes with fake (never dereferenced) addresses: every
+# case fails on the host before any CUDA call, except the last ones, which
+# pass the checks and then find no usable device here (or no-op).
+A = 1 << 20  # a 16-byte aligned fake address
+
+
+def call(q, *args):
+    return q.library().apr_qgemm(*args)
+
+
+@pytest.mark.parametrize("args,code,needle", [
+    ((5, A, 64, 64, 2 * A, 8, 3 * A, None, None), -2, "qtype"),
+    ((2, A, 64, 33, 2 * A, 8, 3 * A, None, None), -1, "k"),
+    ((2, A, 64, 0, 2 * A, 8, 3 * A, None, None), -1, "k"),
+    ((2, A, -1, 64, 2 * A, 8, 3 * A, None, None), -1, "n="),
+    ((2, A, 64, 64, 2 * A, -3, 3 * A, None, None), -1, "T="),
+    ((2, None, 64, 64, 2 * A, 8, 3 * A, None, None), -1, "null"),
+    ((2, A, 64, 64, None, 8, 3 * A, None, None), -1, "null"),
+    ((2, A, 64, 64, 2 * A, 8, None, None, None), -1, "null"),
+    ((2, A + 4, 64, 64, 2 * A, 8, 3 * A, None, None), -3, "aligned"),
+    ((2, A, 64, 64, 2 * A + 8, 8, 3 * A, None, None), -3, "aligned"),
+    ((2, A, 64, 64, 2 * A, 8, 3 * A + 2, None, None), -3, "aligned"),
+    ((2, A, 64, 64, 2 * A, 8, 3 * A, 4 * A + 4, None), -3, "aligned"),
+    ((2, A, 64, 64, 2 * A, 8, 2 * A + 16, None, None), -4, "X"),
+    ((2, A, 64, 64, 2 * A, 8, A + 32, None, None), -4, "W"),
+    ((2, A, 64, 64, 2 * A, 8, 3 * A, 3 * A + 16, None), -4, "residual"),
+    ((2, A, (1 << 24) + 1, 64, 2 * A, 8, 3 * A, None, None), -1, "limits"),
+    ((2, A, 64, (1 << 20) + 32, 2 * A, 8, 3 * A, None, None), -1, "limits"),
+])
+def test_argument_errors(q, args, code, needle):
+    assert call(q, *args) == code
+    assert needle in q.apr_last_error()
+
+
+def test_empty_batch_is_success_without_device(q):
+    assert call(q, 2, A, 64, 64, 2 * A, 0, 3 * A, None, None) == 0
+    assert call(q, 8, A, 0, 64, 2 * A, 5, 3 * A, None, None) == 0
+    assert call(q, 2, None, 64, 64, None, 0, None, None, None) == 0
+
+
+def test_swiglu_and_gemv_specific_errors(q):
+    lib = q.library()
+    assert lib.apr_qgemm_gate_up_swiglu(2, A, None, 64, 64, 2 * A, 8, 3 * A, None) == -1
+    assert lib.apr_qgemv(2, A, 64, 64, 2 * A, 17, 3 * A, None, None) == -1
+    assert "T <= 16" in q.apr_last_error()
+    args = q.capi._Args(2, 0, 0, A, 5 * A, 64, 64, 8, 2 * A, 4 * A, 3 * A, None)
+    assert lib.apr_qgemm_ex(ctypes.byref(args)) == -1       # SwiGLU with a residual
+    args = q.capi._Args(2, 7, 0, A, None, 64, 64, 8, 2 * A, None, 3 * A, None)
+    assert lib.apr_qgemm_ex(ctypes.byref(args)) == -1       # unknown leg
+    args = q.capi._Args(2, 0, 9, A, None, 64, 64, 8, 2 * A, None, 3 * A, None)
+    assert lib.apr_qgemm_ex(ctypes.byref(args)) == -1       # unknown path
+    assert lib.apr_qgemm_ex(None) == -1
+    assert lib.apr_dequant(3, A, 4, 64, 2 * A, None) == -2
+    assert lib.apr_dequant(2, A, 4, 48, 2 * A, None) == -1
+    assert lib.apr_dequant(2, A, 4, 64, A + 16, None) == -4
+
+
+def test_valid_call_without_gpu_reports_device(q):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # Y == residual exactly is allowed (accumulate form)
+    assert call(q, 2, A, 64, 64, 2 * A, 8, 3 * A, 3 * A, None) == -5
+    assert "device" in q.apr_last_error()
+    assert q.library().apr_stream_status(None) == -5
+
+
+def test_binding_rejects_host_tensors(q):
+    import torch
+
+    W = torch.zeros(64 * 2 * 18, dtype=torch.uint8)
+    X = torch.zeros(8, 64)
+    Y = torch.zeros(8, 64)
+    with pytest.raises(ValueError, match="device memory"):
+        q.apr_qgemm(q.APR_Q4_0, W, 64, 64, X, 8, Y, stream=0)
