@@ -152,7 +152,7 @@ int run(const Problem& p) {
   int path = p.path;
   if (path == APR_PATH_AUTO) path = p.T <= APR_GEMV_MAX_T ? APR_PATH_GEMV : APR_PATH_GEMM;
   if (path == APR_PATH_GEMV)
-    return launched(launch_gemv(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, p.R, p.s), "gemv");
+    return launched(launch_gemv(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, p.R, st->status, p.s), "gemv");
   // GEMM: the tensor-core leg needs every raw 256-column chunk of a weight row
   // to start on a 16-byte boundary (k % 256 == 0); the exact leg and other k
   // run the FFMA kernel.

@@ -18,9 +18,14 @@ enum Epilogue { kEpiPlain = 0, kEpiResidual = 1, kEpiSwiGLU = 2 };
 // Standalone dequant (dequant.cu).
 cudaError_t launch_dequant(int qtype, const void* W, int n, int k, float* out, cudaStream_t s);
 
-// Small-T GEMV, exact fp32 (gemv.cu). Wu != nullptr: gate/up SwiGLU.
+// Small-T GEMV, exact fp32. Wu != nullptr: gate/up SwiGLU. Takes the bulk-copy
+// kernel (gemv_bulk.cu) when it applies, else the staged kernel (gemv.cu).
 cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
-                        float* Y, const float* R, cudaStream_t s);
+                        float* Y, const float* R, unsigned* status, cudaStream_t s);
+size_t gemv_bulk_smem(int qtype, int k, int T, bool swiglu);
+bool gemv_bulk_fits(int qtype, int k, int T, bool swiglu);
+cudaError_t launch_gemv_bulk(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
+                             float* Y, const float* R, unsigned* status, cudaStream_t s);
 
 // Exact-fp32 FFMA GEMM for any k % 32 == 0 (gemm_simt.cu).
 cudaError_t launch_gemm_simt(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,

@@ -49,16 +49,19 @@ constexpr int BK = 64;          // k per operand stage: one 128-byte row of fp16
 constexpr int CHUNK = 256;      // k per raw TMA chunk
 constexpr int SUBS = CHUNK / BK;
 
-template <int QT, int EPI, int BN_>
+template <int QT, int EPI, int BN_, bool RTMA_ = false>
 struct Cfg {
   static constexpr int BN = BN_;
   static constexpr int NM = EPI == kEpiSwiGLU ? 2 : 1;
+  // residual tile [BN tokens][128 rows] f32 fetched by TMA at kernel start
+  static constexpr bool RTMA = RTMA_ && EPI == kEpiResidual;
+  static constexpr int R_BYTES = RTMA ? BN * BM * 4 : 0;
   static constexpr int BB = QT == kQ4_0 ? 18 : 34;
   static constexpr int RAW_ROW = CHUNK / 32 * BB;     // 144 / 272 bytes
   static constexpr int RAW_BYTES = BM * RAW_ROW;      // one raw slot
   static constexpr int A_BYTES = BM * BK * 2;         // 16 KB
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int S_AB = NM == 1 ? 4 : (QT == kQ4_0 ? 3 : 2);
+  static constexpr int S_AB = NM == 1 ? (RTMA ? (QT == kQ4_0 ? 3 : 2) : 4) : (QT == kQ4_0 ? 3 : 2);
   static constexpr int S_RAW = NM == 1 ? (QT == kQ4_0 ? 3 : 2) : (QT == kQ4_0 ? 4 : 3);
   static constexpr int NTHREADS = 128 + 128 * NM;
   static constexpr int TMEM_COLS = NM * BN;
@@ -66,8 +69,9 @@ struct Cfg {
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + S_AB * NM * A_BYTES;
   static constexpr int OFF_RAW = OFF_B + S_AB * B_BYTES;
-  static constexpr int OFF_BAR = OFF_RAW + S_RAW * RAW_BYTES;
-  static constexpr int NBAR = 3 * S_AB + 2 * S_RAW + 2;
+  static constexpr int OFF_R = OFF_RAW + S_RAW * RAW_BYTES;
+  static constexpr int OFF_BAR = OFF_R + R_BYTES;
+  static constexpr int NBAR = 3 * S_AB + 2 * S_RAW + 3;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + alignment slack
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -172,17 +176,18 @@ __device__ __forceinline__ void dequant_row_stage(const uint8_t* src, uint8_t* a
 }
 
 // ---------------------------------------------------------------- kernel
-template <int QT, int EPI, int BN>
-__global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
+template <int QT, int EPI, int BN, bool RTMA>
+__global__ void __launch_bounds__(Cfg<QT, EPI, BN, RTMA>::NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWu,
-                   const __grid_constant__ CUtensorMap tmX, int n, int k, int T, float* Y, const float* R,
-                   unsigned* status) {
-  using C = Cfg<QT, EPI, BN>;
+                   const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmR, int n, int k,
+                   int T, float* Y, const float* R, unsigned* status) {
+  using C = Cfg<QT, EPI, BN, RTMA>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem + C::OFF_A;
   uint8_t* sB = smem + C::OFF_B;
   uint8_t* sRaw = smem + C::OFF_RAW;
+  const float* sR = reinterpret_cast<const float*>(smem + C::OFF_R);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* fullA = bars;
   uint64_t* fullB = bars + C::S_AB;
@@ -191,6 +196,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
   uint64_t* rawEmpty = rawFull + C::S_RAW;
   uint64_t* accFull = rawEmpty + C::S_RAW;
   uint64_t* drain = accFull + 1;
+  uint64_t* rFull = drain + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -213,6 +219,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
     }
     mbar_init(accFull, 1);
     mbar_init(drain, 1);
+    mbar_init(rFull, 1);
     abort_flag[0] = 0;   // set by a wait that gives up
     abort_flag[1] = 0;   // never set: drain waits ignore the abort
     fence_mbar_init();
@@ -228,6 +235,10 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmW);
       if (C::NM == 2) tma_prefetch_desc(&tmWu);
+      if (C::RTMA) {  // the residual tile is needed only by the epilogue: fetch it first
+        mbar_arrive_expect_tx(rFull, C::R_BYTES);
+        tma_load_2d(smem + C::OFF_R, &tmR, m0, t0, rFull);
+      }
       int last_issued[C::S_RAW];
       for (int i = 0; i < C::S_RAW; ++i) last_issued[i] = -1;
       bool ok = true;
@@ -246,6 +257,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
       if (!ok) {  // let the copies in flight land before the CTA exits
         for (int i = 0; i < C::S_RAW; ++i)
           if (last_issued[i] >= 0) mbar_wait(&rawFull[i], (last_issued[i] / C::S_RAW) & 1, abort_flag + 1, status);
+        if (C::RTMA) mbar_wait(rFull, 0, abort_flag + 1, status);
       }
     }
   } else if (warp == 2) {
@@ -324,12 +336,23 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
     }
     // epilogue: the NM warpgroups split the BN token columns
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(accFull, 0, abort_flag, status));
+    if (ok && C::RTMA) ok = __all_sync(0xffffffffu, mbar_wait(rFull, 0, abort_flag, status));
     if (ok) {
       tc_fence_after();
       const int row = m0 + (int)r;
       const uint32_t lane_addr = tmem_base + (((uint32_t)(warp & 3) * 32u) << 16);
       constexpr int COLS_PER_WG = BN / C::NM;
       for (int cb = g * COLS_PER_WG; cb < (g + 1) * COLS_PER_WG; cb += 16) {
+        // residual without the shared tile: issue all 16 loads before any store
+        // (Y may be R itself, so a load may not move past an earlier store)
+        float rv[16];
+        if (EPI == kEpiResidual && !C::RTMA) {
+#pragma unroll
+          for (int j2 = 0; j2 < 16; ++j2) {
+            const int t = t0 + cb + j2;
+            rv[j2] = (row < n && t < T) ? R[(size_t)t * n + row] : 0.f;
+          }
+        }
         uint32_t v[16];
         tmem_ld_32x32b_x16(lane_addr + cb, v);
         uint32_t u[16];
@@ -347,7 +370,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
                 const float up = __uint_as_float(u[j2]);
                 y = acc / (1.0f + expf(-acc)) * up;
               } else if (EPI == kEpiResidual) {
-                y = acc + R[o];
+                y = acc + (C::RTMA ? sR[(cb + j2) * BM + (int)r] : rv[j2]);
               } else {
                 y = acc;
               }
@@ -416,10 +439,10 @@ bool make_map_2d(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* map, CUtenso
   return true;
 }
 
-template <int QT, int EPI, int BN>
+template <int QT, int EPI, int BN, bool RTMA>
 int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y,
                const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len) {
-  using C = Cfg<QT, EPI, BN>;
+  using C = Cfg<QT, EPI, BN, RTMA>;
   auto fn = encode_fn(msg, msg_len);
   if (!fn) return -1;
   CUtensorMap mW, mWu, mX;
@@ -437,8 +460,14 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
   if (!make_map_2d(fn, &mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X16, (uint64_t)k, (uint64_t)T, (uint64_t)k * 2, BK,
                    BN, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
     return -1;
+  CUtensorMap mR = mX;
+  if (C::RTMA) {  // residual [T][n] f32, box 128 rows x BN tokens
+    if (!make_map_2d(fn, &mR, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, R, (uint64_t)n, (uint64_t)T, (uint64_t)n * 4, BM, BN,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, msg, msg_len))
+      return -1;
+  }
 
-  auto kern = gemm_tc_kernel<QT, EPI, BN>;
+  auto kern = gemm_tc_kernel<QT, EPI, BN, RTMA>;
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -451,7 +480,7 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
     attr_set[dev] = 1;
   }
   const dim3 grid((n + BM - 1) / BM, (T + BN - 1) / BN);
-  kern<<<grid, C::NTHREADS, C::SMEM, s>>>(mW, mWu, mX, n, k, T, Y, R, status);
+  kern<<<grid, C::NTHREADS, C::SMEM, s>>>(mW, mWu, mX, mR, n, k, T, Y, R, status);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     snprintf(msg, msg_len, "gemm_tc launch: %s", cudaGetErrorString(e));
@@ -473,14 +502,18 @@ cudaError_t launch_x_to_f16(const float* X, uint16_t* X16, size_t count, cudaStr
 int launch_gemm_tc(int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y,
                    const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len) {
   constexpr int BN = 128;
+  // The residual tile goes through TMA when a row of R is a multiple of 16 bytes.
+  const bool rtma = R && (n % 4) == 0;
   if (qtype == kQ4_0) {
-    if (Wu) return launch_cfg<kQ4_0, kEpiSwiGLU, BN>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len);
-    if (R) return launch_cfg<kQ4_0, kEpiResidual, BN>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len);
-    return launch_cfg<kQ4_0, kEpiPlain, BN>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len);
+    if (Wu) return launch_cfg<kQ4_0, kEpiSwiGLU, BN, false>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len);
+    if (rtma) return launch_cfg<kQ4_0, kEpiResidual, BN, true>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len);
+    if (R) return launch_cfg<kQ4_0, kEpiResidual, BN, false>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len);
+    return launch_cfg<kQ4_0, kEpiPlain, BN, false>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len);
   }
-  if (Wu) return launch_cfg<kQ8_0, kEpiSwiGLU, BN>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len);
-  if (R) return launch_cfg<kQ8_0, kEpiResidual, BN>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len);
-  return launch_cfg<kQ8_0, kEpiPlain, BN>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len);
+  if (Wu) return launch_cfg<kQ8_0, kEpiSwiGLU, BN, false>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len);
+  if (rtma) return launch_cfg<kQ8_0, kEpiResidual, BN, true>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len);
+  if (R) return launch_cfg<kQ8_0, kEpiResidual, BN, false>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len);
+  return launch_cfg<kQ8_0, kEpiPlain, BN, false>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len);
 }
 
 }  // namespace apr

@@ -66,7 +66,9 @@ def test_dequant_golden_blocks(q):
 # ------------------------------------------------------------------ GEMV
 @pytest.mark.parametrize("qtype", QTYPES)
 @pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8, 9, 13, 16])
-@pytest.mark.parametrize("n,k", [(300, 512), (77, 288)])   # k = 288: rows not 16-byte multiples
+# (300, 512): ragged 16-row groups; (10, 2304): one partial group and a partial
+# 2048-column chunk; (77, 288): rows not 16-byte multiples (staged kernel)
+@pytest.mark.parametrize("n,k", [(300, 512), (10, 2304), (77, 288)])
 def test_gemv_exact(q, qtype, T, n, k):
     c = synth.make_case(qtype, n, k, T, residual=True, seed=T)
     buf, Y = guarded(T, n)
