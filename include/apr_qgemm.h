@@ -174,6 +174,30 @@ int apr_qgemm_f16_in(int qtype, const void* W, const void* Wu, int n, int k, con
                      float* Y, const float* residual, apr_stream_t stream);
 
 /*
+ * apr_qgemm_noalloc: Y = X . dequant(W)^T (+ residual) on the tensor cores (the
+ * fp16 leg's GEMM path, whatever T is), allocating no device memory. The pages
+ * have no counterpart: it exists for callers that cannot allocate device
+ * memory once they run (a serving process that has reserved nearly all of HBM
+ * for weights and its KV-cache arena and treats a later allocation as a fault,
+ * or a runtime that allows allocation only at start-up). apr_qgemm takes its
+ * T*k*2-byte fp16 copy of X from a pool it grows on demand; this variant uses
+ * a fixed scratch array of APR_NOALLOC_MAX_TK fp16 values (16 MiB) that exists
+ * on every GPU that loads the library, from module load until the process
+ * exits.
+ *   - T*k > APR_NOALLOC_MAX_TK or k % 256 != 0: APR_E_INVAL with a message.
+ *   - The first call on each device looks up the scratch's device address (and
+ *     checks the device); make that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents
+ *     (each call overwrites the T*k values it reads, so nothing needs
+ *     clearing). Calls whose work overlaps on the GPU (on different streams,
+ *     or from different threads) race on it: order them on one stream.
+ * Other arguments, errors and the status word as for apr_qgemm.
+ */
+#define APR_NOALLOC_MAX_TK (8 * 1024 * 1024)
+int apr_qgemm_noalloc(int qtype, const void* W, int n, int k, const float* X, int T,
+                      float* Y, const float* residual, apr_stream_t stream);
+
+/*
  * Standalone dequant: out[n][k] f32 = f32(d) * f32(q'), bit exact (the product
  * of an fp16 scale and a code of at most 8 bits is exact in fp32). The device
  * dequant of aprender-serve gdn_prefill_ops.rs qwen35_dequant_f32 (Q8_0 and

@@ -32,6 +32,7 @@ APR_E_LAUNCH = -6
 APR_E_TIMEOUT = -7
 APR_E_NOMEM = -8
 APR_GEMV_MAX_T = 16
+APR_NOALLOC_MAX_TK = 8 * 1024 * 1024
 
 BLOCK_BYTES = {APR_Q4_0: 18, APR_Q8_0: 34}
 
@@ -44,6 +45,7 @@ EXPORTS = (
     "apr_qgemm_ex",
     "apr_convert_f32_to_f16",
     "apr_qgemm_f16_in",
+    "apr_qgemm_noalloc",
     "apr_dequant",
     "apr_stream_status",
     "apr_last_error",
@@ -87,6 +89,7 @@ def _load() -> ctypes.CDLL:
         "apr_qgemm_ex": ([ctypes.POINTER(_Args)], ci),
         "apr_convert_f32_to_f16": ([vp, ctypes.c_longlong, vp, vp], ci),
         "apr_qgemm_f16_in": ([ci, vp, vp, ci, ci, vp, ci, vp, vp, vp], ci),
+        "apr_qgemm_noalloc": ([ci, vp, ci, ci, vp, ci, vp, vp, vp], ci),
         "apr_dequant": ([ci, vp, ci, ci, vp, vp], ci),
         "apr_stream_status": ([vp], ci),
         "apr_last_error": ([], ctypes.c_char_p),
@@ -218,6 +221,16 @@ def apr_qgemm_f16_in(qtype, W, n, k, X16, T, Y, residual=None, Wu=None, stream=N
                                         _ptr(X16, "X16", dtype=torch.float16, min_bytes=xb // 2), T,
                                         _ptr(Y, "Y", dtype=f32, min_bytes=yb),
                                         _ptr(residual, "residual", dtype=f32, min_bytes=yb), _stream(stream)))
+
+
+def apr_qgemm_noalloc(qtype, W, n, k, X, T, Y, residual=None, stream=None) -> int:
+    """apr_qgemm's tensor-core GEMM without device allocation (fixed scratch)."""
+    u8, f32 = _dtypes()
+    wb, xb, yb = _sizes(qtype, n, k, T)
+    return _check(_lib.apr_qgemm_noalloc(qtype, _ptr(W, "W", dtype=u8, min_bytes=wb), n, k,
+                                         _ptr(X, "X", dtype=f32, min_bytes=xb), T,
+                                         _ptr(Y, "Y", dtype=f32, min_bytes=yb),
+                                         _ptr(residual, "residual", dtype=f32, min_bytes=yb), _stream(stream)))
 
 
 def apr_dequant(qtype, W, n, k, out, stream=None) -> int:

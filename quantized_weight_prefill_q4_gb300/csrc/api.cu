@@ -177,6 +177,29 @@ int run(const Problem& p) {
 
 }  // namespace
 
+namespace apr {
+
+int set_error(int code, const char* msg) {
+  snprintf(t_msg, sizeof t_msg, "%s", msg);
+  return code;
+}
+
+int check_gemm_args(int qtype, const void* W, int n, int k, const float* X, int T, const float* Y, const float* R) {
+  t_msg[0] = 0;
+  return check(Problem{qtype, APR_LEG_F16, APR_PATH_GEMM, W, nullptr, n, k, T, X, R, const_cast<float*>(Y), nullptr});
+}
+
+unsigned* status_word_address() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return static_cast<unsigned*>(p);
+}
+
+}  // namespace apr
+
 extern "C" {
 
 int apr_gemv_max_T(void) { return APR_GEMV_MAX_T; }

@@ -39,4 +39,12 @@ cudaError_t launch_x_to_f16(const float* X, uint16_t* X16, size_t count, cudaStr
 int launch_gemm_tc(int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T,
                    float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len);
 
+// Shared with the allocation-free entry point (api.cu): sets this thread's error
+// message and returns `code`; checks the arguments of a plain / residual GEMM
+// call (APR_OK, an error, or 1 for "nothing to do"); device address of the
+// status word of the current device (nullptr on failure). None allocates.
+int set_error(int code, const char* msg);
+int check_gemm_args(int qtype, const void* W, int n, int k, const float* X, int T, const float* Y, const float* R);
+unsigned* status_word_address();
+
 }  // namespace apr

@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(q):
     names = declared_functions()
-    assert len(names) == 10, names
+    assert len(names) == 11, names
     lib = q.library()
     for name in names:
         assert hasattr(lib, name), name

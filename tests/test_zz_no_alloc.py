@@ -1,0 +1,58 @@
+"""The allocation-free GEMM entry point, apr_qgemm_noalloc, on the GPU.
+
+Some callers cannot allocate device memory once they run (a server that has
+reserved nearly all HBM for weights and its KV-cache arena, or a runtime that
+allocates only at start-up). For them apr_qgemm_noalloc runs the same
+tensor-core GEMM as apr_qgemm, with its fp16 copy of the activations in a
+fixed scratch array instead of a pooled allocation. This file is collected
+last: it checks two calls in a row against the pooled entry point (and the
+float64 oracle), through the C ABI, and the size limit.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import assert_f16_leg, check_guards, dev, guarded
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(q, qtype, W, n, k, X, T, Y, R):
+    stream = torch.cuda.current_stream().cuda_stream
+    return q.library().apr_qgemm_noalloc(qtype, W.data_ptr(), n, k, X.data_ptr(), T, Y.data_ptr(),
+                                         R.data_ptr() if R is not None else None, stream)
+
+
+def test_noalloc_matches_pooled_entry_on_two_calls_in_a_row(q):
+    n, k, T = 384, 1024, 200
+    cases = [synth.make_case(synth.Q4_0, n, k, T, residual=True, seed=71),
+             synth.make_case(synth.Q8_0, n, k, T - 37, residual=False, seed=72)]
+    for c in cases:
+        Tc = c["T"]
+        W, X = dev(c["W"]), dev(c["X"])
+        R = dev(c["R"]) if c["R"] is not None else None
+        buf, Y = guarded(Tc, n)
+        assert _noalloc(q, c["qtype"], W, n, k, X, Tc, Y, R) == 0, q.apr_last_error()
+        q.apr_stream_status()
+        check_guards(buf, Tc, n)
+        Yp = torch.empty((Tc, n), device="cuda")
+        q.apr_qgemm_ex(c["qtype"], W, n, k, X, Tc, Yp, residual=R, path=q.APR_PATH_GEMM)
+        q.apr_stream_status()
+        y = Y.cpu().numpy()
+        assert_f16_leg(y, Yp.cpu().numpy().astype(np.float64))
+        assert_f16_leg(y, oracle.qgemm_f64(c["qtype"], c["W"], n, k, c["X"], c["R"]))
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch(q):
+    k = 4096
+    T = q.APR_NOALLOC_MAX_TK // k + 1
+    lib = q.library()
+    A = 1 << 20  # never dereferenced: the size check comes first
+    assert lib.apr_qgemm_noalloc(2, A, 64, k, 2 * A, T, 64 * A, None, None) == q.APR_E_INVAL
+    assert "fixed scratch" in q.apr_last_error()
+    assert lib.apr_qgemm_noalloc(2, A, 64, 288, 2 * A, 16, 64 * A, None, None) == q.APR_E_INVAL
