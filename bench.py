@@ -218,6 +218,43 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ GPU arm
+def capture_graph(calls):
+    """One CUDA graph replaying `calls` (each enqueues its work on the current
+    stream) back to back: the timed loops replay graphs so that the Python
+    binding's per-call host time does not starve the GPU."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=side):
+        for c in calls:
+            c()
+    torch.cuda.current_stream().wait_stream(side)
+    return g
+
+
+def timed_calls(calls, count, stream):
+    """Seconds for `count` calls cycling through `calls`, replayed from graphs,
+    measured with CUDA events on `stream` (the caller synchronises around it)."""
+    import torch
+
+    full, rest = divmod(count, len(calls))
+    g = capture_graph(calls)
+    g_rest = capture_graph(calls[:rest]) if rest else None
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(full):
+        g.replay()
+    if g_rest is not None:
+        g_rest.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3
+
+
 def run_ours(args):
     import torch
 
@@ -243,9 +280,11 @@ def run_ours(args):
                          X16=torch.empty((T, K), dtype=torch.float16, device=dev)))
     torch.cuda.synchronize()
 
+    def step_call(s):
+        return lambda: q.apr_qgemm(QTYPE, s["W"], N, K, s["X"], T, s["Y"], s["R"])
+
     def step(i):
-        s = sets[i % SETS]
-        q.apr_qgemm(QTYPE, s["W"], N, K, s["X"], T, s["Y"], s["R"], stream=stream)
+        step_call(sets[i % SETS])()
 
     if args.only == "kernel":
         for s in sets:
@@ -261,19 +300,25 @@ def run_ours(args):
         step(i)
     q.apr_stream_status(stream)
 
-    # ---- timed region: K steps, events on the launching stream
+    # ---- timed region: K steps (graph replays of the rotating sets), events
+    # on the launching stream, barrier + synchronize on both sides
     barrier(ws)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    timing = "CUDA graph replay"
     with ClockSampler(dev.index) as clk:
-        e0.record(stream)
-        for i in range(args.steps):
-            step(i)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        # keep the GPU busy while the sampler sees it (also the roofline runs below)
+        try:
+            elapsed = timed_calls([step_call(s) for s in sets], args.steps, stream)
+        except RuntimeError as exc:  # a driver that cannot capture the pooled scratch
+            timing = f"direct launches (graph capture failed: {str(exc)[:80]})"
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(args.steps):
+                step(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            elapsed = e0.elapsed_time(e1) / 1e3
     barrier(ws)
-    elapsed = e0.elapsed_time(e1) / 1e3
     q.apr_stream_status(stream)
     t_max, flop_all = reduce_over_ranks(elapsed, FLOP * args.steps, ws)
     value = flop_all / t_max / 1e12
@@ -287,18 +332,8 @@ def run_ours(args):
     for s in sets:
         q.apr_convert_f32_to_f16(s["X"], T * K, s["X16"], stream=stream)
     reps = max(200, min(args.steps, 2000))
-    for i in range(10):
-        s = sets[i % SETS]
-        q.apr_qgemm_f16_in(QTYPE, s["W"], N, K, s["X16"], T, s["Y"], s["R"], stream=stream)
-    torch.cuda.synchronize()
-    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    g0.record(stream)
-    for i in range(reps):
-        s = sets[i % SETS]
-        q.apr_qgemm_f16_in(QTYPE, s["W"], N, K, s["X16"], T, s["Y"], s["R"], stream=stream)
-    g1.record(stream)
-    torch.cuda.synchronize()
-    gemm_s = g0.elapsed_time(g1) / 1e3 / reps
+    gemm_calls = [(lambda s=s: q.apr_qgemm_f16_in(QTYPE, s["W"], N, K, s["X16"], T, s["Y"], s["R"])) for s in sets]
+    gemm_s = timed_calls(gemm_calls, reps, stream) / reps
     q.apr_stream_status(stream)
     peak_tf, peak_gbs, peak_kind = _peaks()
     achieved = FLOP / gemm_s / 1e12
@@ -347,6 +382,7 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "qtype": "Q4_0", "n": N, "k": K, "T": T, "residual": True,
                        "leg": "f16 inputs, f32 accumulate", "l2": f"{SETS} rotating input sets (277 MB > 2x L2)",
+                       "timing": timing,
                        "parallelism": f"replicas x{ws}"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                          "frac": achieved / peak_tf, "traffic": traffic,
@@ -381,14 +417,8 @@ def gemv_rate(q, synth, dev, stream, peak_gbs):
         q.apr_qgemv(QTYPE, Ws[i % nsets], n, k, X, 1, Y, stream=stream)
     torch.cuda.synchronize()
     reps = 2000
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for i in range(reps):
-        q.apr_qgemv(QTYPE, Ws[i % nsets], n, k, X, 1, Y, stream=stream)
-    b.record(stream)
-    torch.cuda.synchronize()
+    dt = timed_calls([(lambda w=w: q.apr_qgemv(QTYPE, w, n, k, X, 1, Y)) for w in Ws], reps, stream) / reps
     q.apr_stream_status(stream)
-    dt = a.elapsed_time(b) / 1e3 / reps
     byts = n * (k // 32) * 18 + k * 4 + n * 4
     gbs = byts / dt / 1e9
     return {"workload": "q4_0_gemv_n4096_k4096_t1", "GB/s": gbs, "frac_hbm": gbs / peak_gbs, "us": dt * 1e6}
