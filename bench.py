@@ -217,6 +217,30 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def kernel_hash() -> str:
+    """sha256 (16 hex) of the GEMM kernel's sources, to tie ncu counters to a kernel version."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "dev_common.cuh"):
+        with open(os.path.join(ROOT, "quantized_weight_prefill_q4_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic():
+    """DRAM bytes per launch from the committed ncu summary, or None once the
+    kernel has changed since the counters were taken."""
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(tp):
+        return None
+    with open(tp) as f:
+        rec = json.load(f).get(WORKLOAD)
+    if not rec or rec.get("kernel_hash") != kernel_hash():
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
 # ------------------------------------------------------------------ GPU arm
 def capture_graph(calls):
     """One CUDA graph replaying `calls` (each enqueues its work on the current
@@ -286,6 +310,18 @@ def run_ours(args):
     def step(i):
         step_call(sets[i % SETS])()
 
+    if args.only == "gemv":
+        n, k = 4096, 4096
+        c = synth.make_case(QTYPE, n, k, 1, seed=0)
+        Ws = [torch.from_numpy(c["W"]).to(dev) for _ in range(16)]
+        X1 = torch.from_numpy(c["X"]).to(dev)
+        Y1 = torch.empty((1, n), device=dev)
+        for i in range(args.warmup + args.steps):
+            q.apr_qgemv(QTYPE, Ws[i % 16], n, k, X1, 1, Y1, stream=stream)
+        q.apr_stream_status(stream)
+        print(json.dumps({"only": "gemv", "launches": args.warmup + args.steps}), flush=True)
+        return
+
     if args.only == "kernel":
         for s in sets:
             q.apr_convert_f32_to_f16(s["X"], T * K, s["X16"], stream=stream)
@@ -337,11 +373,7 @@ def run_ours(args):
     q.apr_stream_status(stream)
     peak_tf, peak_gbs, peak_kind = _peaks()
     achieved = FLOP / gemm_s / 1e12
-    traffic = None
-    tp = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tp):
-        with open(tp) as f:
-            traffic = json.load(f).get(WORKLOAD)
+    traffic = measured_traffic()
 
     # ---- small-T GEMV (T = 1), the other half of the metric
     gemv = None
@@ -432,9 +464,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=["all", "step", "kernel"], default="all",
-                    help="step: only the timed apr_qgemm steps; kernel: only the GEMM kernel on fp16 activations "
-                         "(small, bounded runs for profilers)")
+    ap.add_argument("--only", choices=["all", "step", "kernel", "gemv"], default="all",
+                    help="step: only the timed apr_qgemm steps; kernel: only the GEMM kernel on fp16 activations; "
+                         "gemv: only the T = 1 GEMV (small, bounded runs for profilers)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -6,27 +6,29 @@
 // This is the f16 leg of aprender-serve 0.70.2 src/cuda/executor/gdn_prefill_ops.rs
 // (qwen35_project_rows_f16: fp16 inputs, fp32 accumulation and output on the
 // tensor cores), but the weight is never written out as fp16 or f32: raw GGUF
-// blocks stream into shared memory and are decoded in registers into the
-// MMA's operand tile. The same page's f32 path dequantizes every weight to an
-// f32 scratch per chunk, and the chunked driver of
-// src/gguf/cuda/forward_qwen35_cuda_prefill.rs reports that dequant as a large
-// share of prefill time (module constants PREFILL_MAX_CHUNK_ROWS and
+// blocks stream into shared memory and are decoded in registers straight into
+// tensor memory, where the MMA reads them as its A operand. The same page's f32
+// path dequantizes every weight to an f32 scratch per chunk, and the chunked
+// driver of src/gguf/cuda/forward_qwen35_cuda_prefill.rs reports that dequant
+// as a large share of prefill time (module constants PREFILL_MAX_CHUNK_ROWS and
 // UNIFIED_PREFILL_CHUNK_ROWS); here it costs no memory traffic at all.
 //
 // One CTA computes one 128-row x BN-token output tile. Warp roles:
 //   warp 0       TMA producer of raw weight chunks: 128 rows x 256 k (8 blocks
 //                per row: 144 B for Q4_0, 272 B for Q8_0, the smallest box whose
 //                width is a multiple of 16 bytes for both formats) into a ring
-//                of S_RAW slots
+//                of S_RAW slots, with L2 prefetches PF chunks ahead
 //   warp 1       TMEM allocator and the single MMA-issuing thread
 //   warp 2       TMA producer of X tiles: BN tokens x 64 k of the fp16 copy of X,
-//                128-byte swizzled, into the B ring (S_AB stages)
+//                128-byte swizzled, into the B ring (S_B stages)
 //   warp 3       idle
-//   warps 4..    one warpgroup per weight (two for gate/up): each thread owns one
-//                of the 128 rows, decodes 2 blocks (64 k) per stage from the raw
-//                slot and writes them as fp16 into the A ring in the canonical
-//                K-major 128-byte-swizzle layout; then the same warps read the
-//                accumulators out of TMEM and run the epilogue.
+//   warps 4..    dequant warpgroups: each thread owns one of the 128 rows (its
+//                TMEM lane), decodes 2 blocks (64 k) per stage from the raw slot
+//                and stores them as 32 columns of fp16 pairs into an A stage in
+//                TMEM (S_A stages); with one weight, two warpgroups take
+//                alternate stages, with gate/up one warpgroup per weight. Then
+//                the same warps read the accumulators out of TMEM and run the
+//                epilogue.
 // Every mbarrier wait is bounded (2 s); a wait that gives up sets the device
 // status word and an abort flag in shared memory so that every role leaves its
 // loop, drains its own TMA copies and MMAs, and the CTA frees its TMEM.
@@ -45,37 +47,44 @@ namespace apr {
 namespace {
 
 constexpr int BM = 128;         // weight rows per tile (UMMA M)
-constexpr int BK = 64;          // k per operand stage: one 128-byte row of fp16
+constexpr int BK = 64;          // k per operand stage
 constexpr int CHUNK = 256;      // k per raw TMA chunk
 constexpr int SUBS = CHUNK / BK;
+constexpr int A_COLS = BK / 2;  // TMEM columns of one A stage (two fp16 per column)
+constexpr int PF = 4;           // raw chunks prefetched into L2 ahead of their TMA load
 
 template <int QT, int EPI, int BN_, bool RTMA_ = false>
 struct Cfg {
   static constexpr int BN = BN_;
   static constexpr int NM = EPI == kEpiSwiGLU ? 2 : 1;
+  static constexpr int DQ = NM == 1 ? 2 : 1;           // warpgroups per weight (alternate stages)
+  static constexpr int NWG = NM * DQ;                   // dequant / epilogue warpgroups
   // residual tile [BN tokens][128 rows] f32 fetched by TMA at kernel start
   static constexpr bool RTMA = RTMA_ && EPI == kEpiResidual;
   static constexpr int R_BYTES = RTMA ? BN * BM * 4 : 0;
   static constexpr int BB = QT == kQ4_0 ? 18 : 34;
   static constexpr int RAW_ROW = CHUNK / 32 * BB;     // 144 / 272 bytes
   static constexpr int RAW_BYTES = BM * RAW_ROW;      // one raw slot
-  static constexpr int A_BYTES = BM * BK * 2;         // 16 KB
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int S_AB = NM == 1 ? (RTMA ? (QT == kQ4_0 ? 3 : 2) : 4) : (QT == kQ4_0 ? 3 : 2);
+  static constexpr int S_A = 4;
+  static constexpr int S_B = QT == kQ4_0 ? 6 : 5;
   static constexpr int S_RAW = NM == 1 ? (QT == kQ4_0 ? 3 : 2) : (QT == kQ4_0 ? 4 : 3);
-  static constexpr int NTHREADS = 128 + 128 * NM;
-  static constexpr int TMEM_COLS = NM * BN;
+  static constexpr int NTHREADS = 128 + 128 * NWG;
+  static constexpr int ACC_COLS = NM * BN;
+  static constexpr int A_COL0 = ACC_COLS;                       // first A column
+  static constexpr int USED_COLS = ACC_COLS + NM * S_A * A_COLS;
+  static constexpr int TMEM_COLS = USED_COLS <= 128 ? 128 : USED_COLS <= 256 ? 256 : 512;
   // shared memory layout (offsets from a 1024-aligned base)
-  static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = OFF_A + S_AB * NM * A_BYTES;
-  static constexpr int OFF_RAW = OFF_B + S_AB * B_BYTES;
+  static constexpr int OFF_B = 0;
+  static constexpr int OFF_RAW = OFF_B + S_B * B_BYTES;
   static constexpr int OFF_R = OFF_RAW + S_RAW * RAW_BYTES;
   static constexpr int OFF_BAR = OFF_R + R_BYTES;
-  static constexpr int NBAR = 3 * S_AB + 2 * S_RAW + 3;
+  static constexpr int NBAR = 2 * S_A + 2 * S_B + 2 * S_RAW + 3;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;   // + alignment slack
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation");
+  static_assert(USED_COLS <= 512, "TMEM budget");
+  static_assert(BN % (16 * NWG) == 0, "epilogue split");
 };
 
 // ---------------------------------------------------------------- dequant
@@ -119,10 +128,10 @@ __device__ __forceinline__ __half2 scale2(uint32_t dbits) {
   return u32_as_h2((dbits & 0xFFFFu) | (dbits << 16));
 }
 
-// Decodes row `r`'s two blocks (64 k) at `src` (4-byte aligned) into the A
-// tile at `a_tile` (1024-aligned, 128-byte swizzle, K-major).
+// Decodes one row's two blocks (64 k) at `src` (4-byte aligned) into 32 fp16
+// pairs in k order: a[j] = (w_2j, w_2j+1), j = 0..31.
 template <int QT>
-__device__ __forceinline__ void dequant_row_stage(const uint8_t* src, uint8_t* a_tile, uint32_t r) {
+__device__ __forceinline__ void dequant_row_stage(const uint8_t* src, uint32_t (&a)[32]) {
   const uint32_t* s32 = reinterpret_cast<const uint32_t*>(src);
   if constexpr (QT == kQ4_0) {
     uint32_t w[9];
@@ -138,39 +147,30 @@ __device__ __forceinline__ void dequant_row_stage(const uint8_t* src, uint8_t* a
     const __half2 d1 = scale2(w[4] >> 16);
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
-      uint32_t o[4][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) q4_word(p[blk * 4 + i], blk ? d1 : d0, o[i]);
-      // chunk 0: elements 0..7 = low halves of words 0, 1; chunk 1: 8..15 (words 2, 3);
-      // chunk 2: 16..23 = high halves of words 0, 1; chunk 3: 24..31.
-      const uint4 c0 = make_uint4(o[0][0], o[0][1], o[1][0], o[1][1]);
-      const uint4 c1 = make_uint4(o[2][0], o[2][1], o[3][0], o[3][1]);
-      const uint4 c2 = make_uint4(o[0][2], o[0][3], o[1][2], o[1][3]);
-      const uint4 c3 = make_uint4(o[2][2], o[2][3], o[3][2], o[3][3]);
-      *reinterpret_cast<uint4*>(a_tile + sw128_offset(r, blk * 4 + 0)) = c0;
-      *reinterpret_cast<uint4*>(a_tile + sw128_offset(r, blk * 4 + 1)) = c1;
-      *reinterpret_cast<uint4*>(a_tile + sw128_offset(r, blk * 4 + 2)) = c2;
-      *reinterpret_cast<uint4*>(a_tile + sw128_offset(r, blk * 4 + 3)) = c3;
+      for (int i = 0; i < 4; ++i) {
+        uint32_t o[4];
+        q4_word(p[blk * 4 + i], blk ? d1 : d0, o);
+        a[16 * blk + 2 * i] = o[0];          // elements 4i, 4i+1
+        a[16 * blk + 2 * i + 1] = o[1];      // 4i+2, 4i+3
+        a[16 * blk + 8 + 2 * i] = o[2];      // 16+4i, 16+4i+1
+        a[16 * blk + 8 + 2 * i + 1] = o[3];  // 16+4i+2, 16+4i+3
+      }
     }
   } else {
     uint32_t w[17];
 #pragma unroll
     for (int i = 0; i < 17; ++i) w[i] = s32[i];
     // block 0: d in bytes 0-1, payload 2..33; block 1: d in 34-35, payload 36..67
-    uint32_t p[16];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) p[i] = __byte_perm(w[i], w[i + 1], 0x5432);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) p[8 + i] = w[9 + i];
     const __half2 d0 = scale2(w[0] & 0xFFFFu);
     const __half2 d1 = scale2(w[8] >> 16);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      uint32_t o0[2], o1[2];
-      const __half2 d2 = c < 4 ? d0 : d1;
-      q8_word(p[2 * c], d2, o0);
-      q8_word(p[2 * c + 1], d2, o1);
-      *reinterpret_cast<uint4*>(a_tile + sw128_offset(r, c)) = make_uint4(o0[0], o0[1], o1[0], o1[1]);
+    for (int c = 0; c < 16; ++c) {
+      const uint32_t p = c < 8 ? __byte_perm(w[c], w[c + 1], 0x5432) : w[1 + c];
+      uint32_t o[2];
+      q8_word(p, c < 8 ? d0 : d1, o);
+      a[2 * c] = o[0];
+      a[2 * c + 1] = o[1];
     }
   }
 }
@@ -184,15 +184,15 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RTMA>::NTHREADS, 1)
   using C = Cfg<QT, EPI, BN, RTMA>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem + C::OFF_A;
   uint8_t* sB = smem + C::OFF_B;
   uint8_t* sRaw = smem + C::OFF_RAW;
   const float* sR = reinterpret_cast<const float*>(smem + C::OFF_R);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* fullA = bars;
-  uint64_t* fullB = bars + C::S_AB;
-  uint64_t* empty = bars + 2 * C::S_AB;
-  uint64_t* rawFull = bars + 3 * C::S_AB;
+  uint64_t* emptyA = fullA + C::S_A;
+  uint64_t* fullB = emptyA + C::S_A;
+  uint64_t* emptyB = fullB + C::S_B;
+  uint64_t* rawFull = emptyB + C::S_B;
   uint64_t* rawEmpty = rawFull + C::S_RAW;
   uint64_t* accFull = rawEmpty + C::S_RAW;
   uint64_t* drain = accFull + 1;
@@ -208,14 +208,17 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RTMA>::NTHREADS, 1)
   const int nchunks = k / CHUNK;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::S_AB; ++i) {
+    for (int i = 0; i < C::S_A; ++i) {
       mbar_init(&fullA[i], 4 * C::NM);
+      mbar_init(&emptyA[i], 1);
+    }
+    for (int i = 0; i < C::S_B; ++i) {
       mbar_init(&fullB[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&emptyB[i], 1);
     }
     for (int i = 0; i < C::S_RAW; ++i) {
       mbar_init(&rawFull[i], 1);
-      mbar_init(&rawEmpty[i], 4);
+      mbar_init(&rawEmpty[i], 4 * C::DQ);
     }
     mbar_init(accFull, 1);
     mbar_init(drain, 1);
@@ -239,6 +242,9 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RTMA>::NTHREADS, 1)
         mbar_arrive_expect_tx(rFull, C::R_BYTES);
         tma_load_2d(smem + C::OFF_R, &tmR, m0, t0, rFull);
       }
+      for (int c = 0; c < PF && c < nchunks; ++c)
+        for (int m = 0; m < C::NM; ++m)
+          tma_prefetch_l2_2d(m ? (const void*)&tmWu : (const void*)&tmW, c * (C::RAW_ROW / 2), m0);
       int last_issued[C::S_RAW];
       for (int i = 0; i < C::S_RAW; ++i) last_issued[i] = -1;
       bool ok = true;
@@ -248,9 +254,10 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RTMA>::NTHREADS, 1)
           const int slot = j % C::S_RAW;
           ok = mbar_wait(&rawEmpty[slot], ((j / C::S_RAW) & 1) ^ 1, abort_flag, status);
           if (!ok) break;
+          const void* map = m ? (const void*)&tmWu : (const void*)&tmW;
           mbar_arrive_expect_tx(&rawFull[slot], C::RAW_BYTES);
-          tma_load_2d(sRaw + slot * C::RAW_BYTES, m ? (const void*)&tmWu : (const void*)&tmW,
-                      c * (C::RAW_ROW / 2), m0, &rawFull[slot]);
+          tma_load_2d(sRaw + slot * C::RAW_BYTES, map, c * (C::RAW_ROW / 2), m0, &rawFull[slot]);
+          if (c + PF < nchunks) tma_prefetch_l2_2d(map, (c + PF) * (C::RAW_ROW / 2), m0);
           last_issued[slot] = j;
         }
       }
@@ -264,20 +271,20 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RTMA>::NTHREADS, 1)
     // ------------------------------------------------ activation producer
     if (lane == 0) {
       tma_prefetch_desc(&tmX);
-      int last_issued[C::S_AB];
-      for (int i = 0; i < C::S_AB; ++i) last_issued[i] = -1;
+      int last_issued[C::S_B];
+      for (int i = 0; i < C::S_B; ++i) last_issued[i] = -1;
       bool ok = true;
       for (int i = 0; i < nk; ++i) {
-        const int st = i % C::S_AB;
-        ok = mbar_wait(&empty[st], ((i / C::S_AB) & 1) ^ 1, abort_flag, status);
+        const int sb = i % C::S_B;
+        ok = mbar_wait(&emptyB[sb], ((i / C::S_B) & 1) ^ 1, abort_flag, status);
         if (!ok) break;
-        mbar_arrive_expect_tx(&fullB[st], C::B_BYTES);
-        tma_load_2d(sB + st * C::B_BYTES, &tmX, i * BK, t0, &fullB[st]);
-        last_issued[st] = i;
+        mbar_arrive_expect_tx(&fullB[sb], C::B_BYTES);
+        tma_load_2d(sB + sb * C::B_BYTES, &tmX, i * BK, t0, &fullB[sb]);
+        last_issued[sb] = i;
       }
       if (!ok) {
-        for (int i = 0; i < C::S_AB; ++i)
-          if (last_issued[i] >= 0) mbar_wait(&fullB[i], (last_issued[i] / C::S_AB) & 1, abort_flag + 1, status);
+        for (int i = 0; i < C::S_B; ++i)
+          if (last_issued[i] >= 0) mbar_wait(&fullB[i], (last_issued[i] / C::S_B) & 1, abort_flag + 1, status);
       }
     }
   } else if (warp == 1) {
@@ -286,22 +293,23 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RTMA>::NTHREADS, 1)
       constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
       bool ok = true;
       for (int i = 0; i < nk && ok; ++i) {
-        const int st = i % C::S_AB;
-        const uint32_t ph = (i / C::S_AB) & 1;
-        ok = mbar_wait(&fullA[st], ph, abort_flag, status) && mbar_wait(&fullB[st], ph, abort_flag, status);
+        const int sa = i % C::S_A, sb = i % C::S_B;
+        ok = mbar_wait(&fullA[sa], (i / C::S_A) & 1, abort_flag, status) &&
+             mbar_wait(&fullB[sb], (i / C::S_B) & 1, abort_flag, status);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t bdesc = smem_desc_sw128(sB + st * C::B_BYTES);
+        const uint64_t bdesc = smem_desc_sw128(sB + sb * C::B_BYTES);
 #pragma unroll
         for (int m = 0; m < C::NM; ++m) {
-          const uint64_t adesc = smem_desc_sw128(sA + (st * C::NM + m) * C::A_BYTES);
+          const uint32_t a_tmem = tmem_base + C::A_COL0 + (m * C::S_A + sa) * A_COLS;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            // +32 bytes per 16-element k step inside the swizzle atom
-            mma_f16(tmem_base + m * BN, adesc + 2 * kk, bdesc + 2 * kk, idesc, (i | kk) != 0);
+            // 16 k = 8 TMEM columns of A, +32 bytes of B inside its swizzle atom
+            mma_f16_ts(tmem_base + m * BN, a_tmem + kk * 8, bdesc + 2 * kk, idesc, (i | kk) != 0);
           }
         }
-        mma_commit(&empty[st]);
+        mma_commit(&emptyA[sa]);
+        mma_commit(&emptyB[sb]);
       }
       if (ok) {
         mma_commit(accFull);
@@ -312,8 +320,12 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RTMA>::NTHREADS, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------ dequant, then epilogue
-    const int g = (warp - 4) >> 2;              // which weight (0: W / gate, 1: up)
-    const uint32_t r = (uint32_t)((warp & 3) * 32 + lane);  // tile row == TMEM lane
+    const int wg = (warp - 4) >> 2;                  // dequant warpgroup
+    const int g = wg % C::NM;                        // which weight (0: W / gate, 1: up)
+    const int par = wg / C::NM;                      // which stages: i % DQ == par
+    const uint32_t q = (uint32_t)(warp & 3);         // lane quarter of TMEM this warp may access
+    const uint32_t r = q * 32 + lane;                // tile row == TMEM lane
+    const uint32_t lane_base = tmem_base + ((q * 32u) << 16);
     bool ok = true;
     for (int c = 0; c < nchunks && ok; ++c) {
       const int j = c * C::NM + g;
@@ -321,28 +333,31 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RTMA>::NTHREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&rawFull[slot], (j / C::S_RAW) & 1, abort_flag, status));
       if (!ok) break;
       const uint8_t* raw_row = sRaw + slot * C::RAW_BYTES + r * C::RAW_ROW;
-      for (int s = 0; s < SUBS; ++s) {
+      for (int s = par; s < SUBS; s += C::DQ) {
         const int i = c * SUBS + s;
-        const int st = i % C::S_AB;
-        ok = __all_sync(0xffffffffu, mbar_wait(&empty[st], ((i / C::S_AB) & 1) ^ 1, abort_flag, status));
+        const int sa = i % C::S_A;
+        uint32_t a[32];
+        dequant_row_stage<QT>(raw_row + s * 2 * C::BB, a);  // overlaps the wait below
+        ok = __all_sync(0xffffffffu, mbar_wait(&emptyA[sa], ((i / C::S_A) & 1) ^ 1, abort_flag, status));
         if (!ok) break;
-        dequant_row_stage<QT>(raw_row + s * 2 * C::BB, sA + (st * C::NM + g) * C::A_BYTES, r);
-        fence_proxy_async_smem();
+        tc_fence_after();
+        tmem_st_32x32b_x32(lane_base + C::A_COL0 + (g * C::S_A + sa) * A_COLS, a);
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&fullA[st]);
+        if (lane == 0) mbar_arrive(&fullA[sa]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&rawEmpty[slot]);
     }
-    // epilogue: the NM warpgroups split the BN token columns
+    // epilogue: the warpgroups split the BN token columns
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(accFull, 0, abort_flag, status));
     if (ok && C::RTMA) ok = __all_sync(0xffffffffu, mbar_wait(rFull, 0, abort_flag, status));
     if (ok) {
       tc_fence_after();
       const int row = m0 + (int)r;
-      const uint32_t lane_addr = tmem_base + (((uint32_t)(warp & 3) * 32u) << 16);
-      constexpr int COLS_PER_WG = BN / C::NM;
-      for (int cb = g * COLS_PER_WG; cb < (g + 1) * COLS_PER_WG; cb += 16) {
+      constexpr int COLS_PER_WG = BN / C::NWG;
+      for (int cb = wg * COLS_PER_WG; cb < (wg + 1) * COLS_PER_WG; cb += 16) {
         // residual without the shared tile: issue all 16 loads before any store
         // (Y may be R itself, so a load may not move past an earlier store)
         float rv[16];
@@ -354,9 +369,9 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RTMA>::NTHREADS, 1)
           }
         }
         uint32_t v[16];
-        tmem_ld_32x32b_x16(lane_addr + cb, v);
+        tmem_ld_32x32b_x16(lane_base + cb, v);
         uint32_t u[16];
-        if (C::NM == 2) tmem_ld_32x32b_x16(lane_addr + BN + cb, u);
+        if (C::NM == 2) tmem_ld_32x32b_x16(lane_base + BN + cb, u);
         tmem_ld_wait();
         if (row < n) {
 #pragma unroll

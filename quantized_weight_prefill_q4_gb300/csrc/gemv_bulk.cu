@@ -54,15 +54,20 @@ __host__ __device__ constexpr int q4_shift(int slot) {
                                                                                     : slot == 6 ? 12 : 16;
 }
 
-// Table slot j (0..63) of a block pair -> element offset in the pair, scale 2^-s.
+// Table layout of one block pair (64 floats + pad): Q4_0 slot 32 blk + 8 word +
+// 2 m + hi holds element 32 blk + 16 hi + 4 word + m (byte m of payload word
+// `word`, low or high nibble), scaled by 2^-s with s = q4_shift(2 m + hi), in
+// the order q4_word_dot consumes them; Q8_0 slot e holds element e.
+// Maps element offset e (0..63) to its slot and scale exponent.
 template <int QT>
-__device__ __forceinline__ void slot_info(int j, int& elem, int& s) {
+__device__ __forceinline__ void elem_slot(int e, int& slot, int& s) {
   if (QT == kQ4_0) {
-    const int blk = j >> 5, jj = j & 31, word = jj >> 3, q = jj & 7, m = q >> 1, hi = q & 1;
-    elem = 32 * blk + (hi ? 16 : 0) + 4 * word + m;
+    const int blk = e >> 5, ee = e & 31, hi = ee >> 4, within = ee & 15, word = within >> 2, m = within & 3;
+    const int q = 2 * m + hi;
+    slot = 32 * blk + 8 * word + q;
     s = q4_shift(q);
   } else {
-    elem = j;
+    slot = e;
     s = 0;
   }
 }
@@ -165,12 +170,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 
   // ------------------------------------------------ consumers: X table first
-  for (int idx = threadIdx.x; idx < T * npk * 64; idx += NCW * 32) {
-    const int t = idx / (npk * 64), rem = idx - t * (npk * 64), p = rem >> 6, j = rem & 63;
-    int elem, s;
-    slot_info<QT>(j, elem, s);
-    const float x = X[(size_t)t * k + 64 * p + elem];
-    xt[(t * npk + p) * XPAIR + j] = x * __uint_as_float((uint32_t)(127 - s) << 23);  // exact 2^-s
+  // Coalesced float4 loads, eight per thread in flight before any store.
+  {
+    const int k4 = k / 4;
+    const int total4 = T * k4;
+    const float4* X4 = reinterpret_cast<const float4*>(X);
+    constexpr int NT = NCW * 32, U = 8;
+    for (int base = threadIdx.x; base < total4; base += U * NT) {
+      float4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i4 = base + u * NT;
+        v[u] = i4 < total4 ? __ldg(X4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i4 = base + u * NT;
+        if (i4 < total4) {
+          const int t = i4 / k4;
+          const int e0 = (i4 - t * k4) * 4;
+          float* dst = xt + (t * npk + (e0 >> 6)) * XPAIR;
+          const float vv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            int slot, sh;
+            elem_slot<QT>((e0 & 63) + c, slot, sh);
+            dst[slot] = vv[c] * __uint_as_float((uint32_t)(127 - sh) << 23);  // exact 2^-sh
+          }
+        }
+      }
+    }
   }
   named_sync(1, NCW * 32);
 
