@@ -34,10 +34,29 @@ cudaError_t launch_gemm_simt(int qtype, const void* W, const void* Wu, int n, in
 // fp16 copy of X, round to nearest even (gemm_tc.cu).
 cudaError_t launch_x_to_f16(const float* X, uint16_t* X16, size_t count, cudaStream_t s);
 
+// Shape of a tensor-core GEMM launch: token-tile width, split over k (1 or 2)
+// and, with a split, the bytes of workspace it needs (fp32 partial tiles and
+// per-tile tickets; it needs no clearing).
+struct GemmPlan {
+  int bn = 128;
+  int nsplit = 1;
+  size_t ws_bytes = 0;
+};
+GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu, bool allow_split);
+
+// Exact-leg operands: hi = x with 13 low mantissa bits cleared, lo = x - hi.
+cudaError_t launch_x_split(const float* X, float* hi, float* lo, size_t count, cudaStream_t s);
+
+// tcgen05 exact leg (3 x tf32 per product); needs k % 256 == 0 and the split X.
+int launch_gemm_tc_exact(int qtype, const void* W, const void* Wu, int n, int k, const float* Xhi, const float* Xlo,
+                         int T, float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg,
+                         size_t msg_len);
+
 // tcgen05 fp16-input GEMM; needs k % 256 == 0 and X16 = fp16(X) (gemm_tc.cu).
 // `status` is the device status word.
-int launch_gemm_tc(int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T,
-                   float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len);
+int launch_gemm_tc(const GemmPlan& plan, int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16,
+                   int T, float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len,
+                   void* ws = nullptr);
 
 // Shared with the allocation-free entry point (api.cu): sets this thread's error
 // message and returns `code`; checks the arguments of a plain / residual GEMM

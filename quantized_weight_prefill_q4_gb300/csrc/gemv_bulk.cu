@@ -114,7 +114,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                      const float* __restrict__ X, int T, float* Y, const float* R, unsigned* status) {
   using C = BCfg<QT, SWI>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, by pointer arithmetic on the shared array so that
+  // the compiler keeps the shared address space (shared loads, not generic)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int npk = k / 64;                                  // block pairs per row
   float* xt = reinterpret_cast<float*>(smem + C::RING);
   const int xt_floats = T * npk * XPAIR;

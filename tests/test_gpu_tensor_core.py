@@ -164,3 +164,52 @@ def test_auto_rule_large_T_takes_the_fp16_gemm(q):
     ref = oracle.qgemm_f64(synth.Q8_0, c["W"], n, k, c["X"])
     rel, _ = assert_f16_leg(Y.cpu().numpy(), ref)
     assert rel > 1e-5
+
+
+# ------------------------------------------------------------------ 256-token tiles
+# The GEMM takes 256-token tiles when they still give every SM a tile (here
+# 37 x 5 = 185 tiles); ragged rows and tokens, residual through the operand
+# ring (n % 4 == 0) and straight from memory (n % 4 != 0).
+@pytest.mark.parametrize("qtype", QTYPES)
+@pytest.mark.parametrize("n,res", [(4736, False), (4736, True), (4738, True)])
+def test_wide_tiles(q, qtype, n, res):
+    k, T = 512, 1030
+    c = synth.make_case(qtype, n, k, T, residual=res, seed=n + qtype)
+    buf, Y = guarded(T, n)
+    gemm(q, qtype, dev(c["W"]), n, k, dev(c["X"]), T, Y, dev(c["R"]) if res else None)
+    check_guards(buf, T, n)
+    assert_f16_leg(Y.cpu().numpy(), oracle.qgemm_f64(qtype, c["W"], n, k, c["X"], c["R"]))
+
+
+# ------------------------------------------------------------------ tile plans
+# Small grids run 256-token tiles split over k between two CTAs (the second to
+# finish adds the first one's parked partial); 80 row tiles of 256 tokens are
+# too many to split and too few for 256-token tiles, so they take 128-token
+# tiles. Both with and without a residual, and with rows that are not a
+# multiple of 4 (residual read straight from memory).
+@pytest.mark.parametrize("qtype", QTYPES)
+@pytest.mark.parametrize("n,k,T,res", [(298, 512, 100, True), (512, 2048, 300, True), (10240, 256, 200, False),
+                                       (10240, 256, 200, True), (10238, 256, 130, True)])
+def test_tile_plans(q, qtype, n, k, T, res):
+    c = synth.make_case(qtype, n, k, T, residual=res, seed=3 * n + T)
+    buf, Y = guarded(T, n)
+    gemm(q, qtype, dev(c["W"]), n, k, dev(c["X"]), T, Y, dev(c["R"]) if res else None)
+    check_guards(buf, T, n)
+    y = Y.cpu().numpy()
+    assert_f16_leg(y, oracle.qgemm_f64(qtype, c["W"], n, k, c["X"], c["R"]))
+    rel, _, _ = errors(y, oracle.qgemm_f16_inputs_f64(qtype, c["W"], n, k, c["X"], c["R"]))
+    assert rel <= 2e-5, rel
+
+
+def test_split_k_is_deterministic(q):
+    # the split partials are added in split order whichever CTA finishes first
+    n, k, T = 512, 4096, 512
+    c = synth.make_case(synth.Q4_0, n, k, T, residual=True, seed=77)
+    W, X, R = dev(c["W"]), dev(c["X"]), dev(c["R"])
+    outs = []
+    for _ in range(3):
+        Y = torch.empty((T, n), device="cuda")
+        gemm(q, synth.Q4_0, W, n, k, X, T, Y, R)
+        outs.append(Y.cpu().numpy())
+    np.testing.assert_array_equal(outs[0], outs[1])
+    np.testing.assert_array_equal(outs[0], outs[2])
