@@ -155,31 +155,12 @@ int run(const Problem& p) {
     return launched(launch_gemv(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, p.R, st->status, p.s), "gemv");
   // GEMM: the tensor-core kernels need every raw 256-column chunk of a weight
   // row to start on a 16-byte boundary (k % 256 == 0); other k run the FFMA
-  // kernel (exact fp32, whatever the leg).
-  // The exact leg runs the FFMA kernel too: its tensor-core form (three tf32
-  // products per term) drifts past 1e-5 relative error at k = 4096 because
-  // the tensor core's fp32 accumulator is not rounded like FFMA.
+  // kernel (exact fp32, whatever the leg). The exact leg runs the FFMA kernel
+  // too: a tensor-core form of it (three tf32 products per term) drifts past
+  // 1e-5 relative error at k = 4096, because the tensor core's fp32
+  // accumulator is not rounded like FFMA.
   if (p.k % 256 != 0 || p.leg == APR_LEG_EXACT_F32)
     return launched(launch_gemm_simt(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, p.R, p.s), "gemm_simt");
-  if (p.leg == APR_LEG_EXACT_F32) {
-    const size_t count = (size_t)p.T * (size_t)p.k;
-    void* xs = nullptr;  // hi then lo, 4 bytes each
-    cudaError_t e = cudaMallocFromPoolAsync(&xs, count * 8, st->pool, p.s);
-    if (e != cudaSuccess)
-      return fail(APR_E_NOMEM, "scratch for the split X (%zu bytes): %s", count * 8, cudaGetErrorString(e));
-    float* hi = static_cast<float*>(xs);
-    float* lo = hi + count;
-    rc = launched(launch_x_split(p.X, hi, lo, count, p.s), "x_split");
-    if (rc == APR_OK) {
-      char msg[256] = "";
-      if (launch_gemm_tc_exact(p.qtype, p.W, p.Wu, p.n, p.k, hi, lo, p.T, p.Y, p.R, st->status, p.s, msg,
-                               sizeof msg) != 0)
-        rc = fail(APR_E_LAUNCH, "%s", msg);
-    }
-    e = cudaFreeAsync(xs, p.s);
-    if (rc == APR_OK && e != cudaSuccess) rc = fail(APR_E_LAUNCH, "cudaFreeAsync: %s", cudaGetErrorString(e));
-    return rc;
-  }
 
   // one pooled scratch: the fp16 copy of X, then the split-K workspace if any
   const GemmPlan plan = plan_gemm_tc(p.n, p.k, p.T, p.Wu != nullptr, true);

@@ -31,12 +31,14 @@ cudaError_t launch_gemv_bulk(int qtype, const void* W, const void* Wu, int n, in
 cudaError_t launch_gemm_simt(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
                              float* Y, const float* R, cudaStream_t s);
 
-// fp16 copy of X, round to nearest even (gemm_tc.cu).
+// fp16 copy of X, round to nearest even (gemm_tc.cu). Launched with
+// programmatic stream serialization; it waits for the preceding kernel before
+// it reads X or writes X16.
 cudaError_t launch_x_to_f16(const float* X, uint16_t* X16, size_t count, cudaStream_t s);
 
 // Shape of a tensor-core GEMM launch: token-tile width, split over k (1 or 2)
-// and, with a split, the bytes of workspace it needs (fp32 partial tiles and
-// per-tile tickets; it needs no clearing).
+// and, with a split, the bytes of workspace it needs (fp32 half tiles and
+// per-tile flags; it needs no clearing).
 struct GemmPlan {
   int bn = 128;
   int nsplit = 1;
@@ -44,16 +46,10 @@ struct GemmPlan {
 };
 GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu, bool allow_split);
 
-// Exact-leg operands: hi = x with 13 low mantissa bits cleared, lo = x - hi.
-cudaError_t launch_x_split(const float* X, float* hi, float* lo, size_t count, cudaStream_t s);
-
-// tcgen05 exact leg (3 x tf32 per product); needs k % 256 == 0 and the split X.
-int launch_gemm_tc_exact(int qtype, const void* W, const void* Wu, int n, int k, const float* Xhi, const float* Xlo,
-                         int T, float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg,
-                         size_t msg_len);
-
 // tcgen05 fp16-input GEMM; needs k % 256 == 0 and X16 = fp16(X) (gemm_tc.cu).
-// `status` is the device status word.
+// `status` is the device status word. Launched with programmatic stream
+// serialization: it waits for the preceding kernel before it touches X16, W,
+// R, Y or the workspace.
 int launch_gemm_tc(const GemmPlan& plan, int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16,
                    int T, float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len,
                    void* ws = nullptr);

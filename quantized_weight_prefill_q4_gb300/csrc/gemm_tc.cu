@@ -13,25 +13,42 @@
 // as a large share of prefill time (module constants PREFILL_MAX_CHUNK_ROWS and
 // UNIFIED_PREFILL_CHUNK_ROWS); here it costs no memory traffic at all.
 //
-// One CTA computes one 128-row x BN-token output tile. Warp roles:
+// One CTA computes one 128-row x BN-token output tile (BN = 128 or 256), or,
+// split over k, half of the k range of one 256-token tile. Warp roles:
 //   warp 0       TMA producer of raw weight chunks: 128 rows x 256 k (8 blocks
 //                per row: 144 B for Q4_0, 272 B for Q8_0, the smallest box whose
 //                width is a multiple of 16 bytes for both formats) into a ring
-//                of S_RAW slots, with L2 prefetches PF chunks ahead
-//   warp 1       TMEM allocator and the single MMA-issuing thread
+//                of S_RAW slots, with L2 prefetches PF chunks ahead; with a
+//                128-token tile it also fetches the residual tile early
+//   warp 1       TMEM allocator and MMA issuer: the whole warp runs the loop,
+//                one elected lane issues (four K = 16 MMAs per 64-k stage)
 //   warp 2       TMA producer of X tiles: BN tokens x 64 k of the fp16 copy of X,
-//                128-byte swizzled, into the B ring
+//                128-byte swizzled, into the B ring; with a 256-token tile it
+//                then fetches the residual into the ring slots as they free up
 //   warp 3       idle
 //   warps 4..    dequant warpgroups: each thread owns one of the 128 rows (its
 //                TMEM lane), decodes 2 blocks (64 k) per stage from the raw slot
 //                and stores them as 32 columns of fp16 pairs into an A stage in
-//                TMEM; A and B stages advance together (S of them); with one weight, two warpgroups take
-//                alternate stages, with gate/up one warpgroup per weight. Then
-//                the same warps read the accumulators out of TMEM and run the
-//                epilogue.
+//                TMEM; A and B stages advance together (S of them); with one
+//                weight, two warpgroups take alternate stages, with gate/up one
+//                warpgroup per weight. Then the same warps run the epilogue.
+// Epilogue: the tile's token columns go out in pieces of 64. A warpgroup reads
+// a piece's accumulators out of TMEM (two 32-column loads, one wait), adds the
+// residual (or applies the SiLU gate), writes the piece into shared memory and
+// one thread stores it with a TMA tensor store; when a row of Y is not a
+// multiple of 16 bytes the threads store Y directly instead.
+// Split over k (two CTAs per tile, blockIdx.z = 0, 1): CTA z finalizes token
+// columns [128 z, 128 z + 128) of the tile and parks the other half of its fp32
+// accumulator in a workspace for its partner; each waits (bounded) for the
+// partner's half and adds p0 + p1 in split order, so the result does not depend
+// on which CTA finishes first.
 // Every mbarrier wait is bounded (2 s); a wait that gives up sets the device
 // status word and an abort flag in shared memory so that every role leaves its
 // loop, drains its own TMA copies and MMAs, and the CTA frees its TMEM.
+// Programmatic dependent launch: the kernel lets the next kernel of the stream
+// launch early, and itself reads and writes global memory only after
+// griddepcontrol.wait (the X producer, the weight producer and the epilogue
+// each wait; only L2 prefetches of the weight go before).
 
 #include <cstdint>
 #include <cstdio>
@@ -49,42 +66,36 @@ namespace {
 
 constexpr int BM = 128;         // weight rows per tile (UMMA M)
 constexpr int CHUNK = 256;      // k per raw TMA chunk
+constexpr int BK = 64;          // k per operand stage (128 B of fp16 B per token row)
+constexpr int SUBS = CHUNK / BK;
 constexpr int PF = 4;           // raw chunks prefetched into L2 ahead of their TMA load
+constexpr int PIECE = 64;                      // token columns per epilogue piece
+constexpr int PIECE_BYTES = PIECE * BM * 4;    // one fp32 piece, [64 tokens][128 rows]
 
-// Residual handling: kRNone (no residual, or loads straight from R), kREarly
-// (the residual tile is fetched by TMA into its own shared buffer at kernel
-// start), kRLate (prefetched into L2 at kernel start, then fetched by TMA into
-// the operand ring once the mainloop has finished with it).
-enum RMode { kRNone = 0, kREarly = 1, kRLate = 2 };
-
-// Two arithmetic legs share the kernel:
-//   f16 leg:   a stage is 64 k; A = fp16(d * q') (two per TMEM column), B = fp16(X);
-//              kind::f16, four K = 16 MMAs per stage.
-//   exact leg: a stage is one 32-k block; A = d * q' exactly in fp32, split into
-//              tf32 hi + lo (the product has at most 19 significant bits, so hi
-//              + lo is exact), one per TMEM column (32 hi columns, 32 lo); B = X
-//              split the same way (hi has the top 11 bits, lo the rest); per
-//              K = 8 step three kind::tf32 MMAs accumulate hi.hi + hi.lo + lo.hi.
-template <int QT, int EPI, int BN_, int RM_ = kRNone, bool EX_ = false>
+// TIO: R and Y rows are multiples of 16 bytes (n % 4 == 0), so the residual is
+// fetched and Y stored by TMA through shared memory; otherwise both go through
+// direct loads and stores.
+template <int QT, int EPI, int BN_, bool TIO_>
 struct Cfg {
   static constexpr int BN = BN_;
-  static constexpr bool EX = EX_;
-  static constexpr int BK = EX ? 32 : 64;               // k per operand stage (128 B of B per row)
-  static constexpr int SUBS = CHUNK / BK;               // stages per raw chunk
-  static constexpr int A_COLS = EX ? 64 : 32;           // TMEM columns of one A stage of one weight
-  static constexpr int B_TILE = BN * 128;               // one 128-B-swizzled B tile
-  static constexpr int NB = EX ? 2 : 1;                 // B tiles per stage (hi, lo)
+  static constexpr bool TIO = TIO_;
+  static constexpr int A_COLS = 32;                     // TMEM columns of one A stage of one weight
+  static constexpr int B_BYTES = BN * 128;              // one 128-B-swizzled B stage
   static constexpr int NM = EPI == kEpiSwiGLU ? 2 : 1;
   static constexpr int DQ = NM == 1 ? 2 : 1;           // warpgroups per weight (alternate stages)
   static constexpr int NWG = NM * DQ;                   // dequant / epilogue warpgroups
-  static constexpr int RM = EPI == kEpiResidual ? RM_ : kRNone;
   static constexpr int BB = QT == kQ4_0 ? 18 : 34;
   static constexpr int RAW_ROW = CHUNK / 32 * BB;     // 144 / 272 bytes
   static constexpr int RAW_BYTES = BM * RAW_ROW;      // one raw slot
-  static constexpr int B_BYTES = NB * B_TILE;
-  static constexpr int R_BYTES = BN * BM * 4;          // residual tile
+  static constexpr int NPIECE = BN / PIECE;
+  // residual through TMA: early into its own buffer (128-token tiles), or late
+  // into the operand ring slots as the last MMAs free them (256-token tiles,
+  // where a ring slot is exactly one piece)
+  static constexpr bool R_EARLY = EPI == kEpiResidual && TIO && BN == 128;
+  static constexpr bool R_LATE = EPI == kEpiResidual && TIO && BN == 256;
+  static constexpr int R_BYTES = R_EARLY ? NPIECE * PIECE_BYTES : 0;
   // operand stages (A in TMEM and B in shared memory advance together)
-  static constexpr int S = EX ? (NM == 2 ? 2 : 4) : (NM == 2 ? 4 : (BN == 256 ? 4 : (QT == kQ4_0 ? 6 : 5)));
+  static constexpr int S = NM == 2 ? 4 : (BN == 256 ? 4 : (QT == kQ4_0 ? 6 : 5));
   static constexpr int S_RAW = NM == 1 ? (QT == kQ4_0 ? 3 : 2) : (QT == kQ4_0 ? 4 : 3);
   static constexpr int NTHREADS = 128 + 128 * NWG;
   static constexpr int ACC_COLS = NM * BN;
@@ -95,14 +106,18 @@ struct Cfg {
   static constexpr int OFF_B = 0;
   static constexpr int OFF_RAW = OFF_B + S * B_BYTES;
   static constexpr int OFF_R = OFF_RAW + S_RAW * RAW_BYTES;
-  static constexpr int OFF_BAR = OFF_R + (RM == kREarly ? R_BYTES : 0);
-  static constexpr int NBAR = 2 * S + 2 * S_RAW + 3;
+  static constexpr int OFF_BAR = OFF_R + R_BYTES;
+  static constexpr int NBAR = 2 * S + 2 * S_RAW + 2 + 4;  // + accFull, drain, 4 residual pieces
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 32 + 1024;   // + alignment slack
+  // staging of the output pieces: the residual buffer, else the operand ring
+  // (free once every MMA has completed)
+  static constexpr int OFF_STAGE = R_EARLY ? OFF_R : OFF_B;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(USED_COLS <= 512, "TMEM budget");
-  static_assert(BN % (16 * NWG) == 0, "epilogue split");
-  static_assert(RM != kRLate || R_BYTES <= S * B_BYTES, "late residual tile fits the operand ring");
+  static_assert(NPIECE % NWG == 0, "epilogue pieces per warpgroup");
+  static_assert(R_EARLY || NPIECE * PIECE_BYTES <= S * B_BYTES, "output pieces fit the operand ring");
+  static_assert(!R_LATE || B_BYTES == PIECE_BYTES, "a late residual piece is one ring slot");
 };
 
 // ---------------------------------------------------------------- dequant
@@ -193,77 +208,22 @@ __device__ __forceinline__ void dequant_row_stage(const uint8_t* src, uint32_t (
   }
 }
 
-// Exact leg: decodes one row's block b of the raw chunk at `chunk_row` (the
-// row's 144 / 272 bytes, 4-byte aligned; the block starts 2 bytes off a word
-// boundary when b is odd) into w = d * q' in fp32, split into tf32 hi (top 11
-// significant bits: 13 low mantissa bits cleared) and lo = w - hi, element j in
-// column j.
-template <int QT>
-__device__ __forceinline__ void dequant_block_exact(const uint8_t* chunk_row, int b, uint32_t (&hi)[32],
-                                                    uint32_t (&lo)[32]) {
-  constexpr int BB = QT == kQ4_0 ? 18 : 34;
-  constexpr int NW = QT == kQ4_0 ? 5 : 9;  // words covering the block from its aligned start
-  const int off = b * BB;
-  const uint32_t* s32 = reinterpret_cast<const uint32_t*>(chunk_row + (off & ~3));
-  uint32_t w[NW];
-#pragma unroll
-  for (int i = 0; i < NW; ++i) w[i] = s32[i];
-  const bool odd = (off & 3) != 0;  // block starts at byte 2 of w[0]
-  // realigned block words: x[i] = bytes 4i..4i+3 of the block (the last one
-  // only partly inside the block)
-  const uint32_t sel = odd ? 0x5432u : 0x3210u;
-  uint32_t x[NW];
-#pragma unroll
-  for (int i = 0; i < NW - 1; ++i) x[i] = __byte_perm(w[i], w[i + 1], sel);
-  x[NW - 1] = __byte_perm(w[NW - 1], 0u, sel);
-  const float d = __half2float(__ushort_as_half((unsigned short)(x[0] & 0xFFFFu)));
-  // payload words: bytes 2..BB-1 of the block
-  float v[32];
-  if constexpr (QT == kQ4_0) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t p = __byte_perm(x[i], x[i + 1], 0x5432);  // payload bytes 4i..4i+3
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const uint32_t byte = (p >> (8 * m)) & 0xFFu;
-        v[4 * i + m] = __uint_as_float(0x4B000000u | (byte & 0xFu)) - 8388616.0f;          // low nibble
-        v[16 + 4 * i + m] = __uint_as_float(0x4B000000u | (byte >> 4)) - 8388616.0f;       // high nibble
-      }
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t q = __byte_perm(x[i], x[i + 1], 0x5432) ^ 0x80808080u;  // int8 + 128
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        v[4 * i + m] = __uint_as_float(__byte_perm(q, 0x4B000000u, 0x7540 + m)) - 8388736.0f;
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const float wv = v[j] * d;  // exact: <= 8 x 11 significant bits
-    const uint32_t h = __float_as_uint(wv) & 0xFFFFE000u;
-    hi[j] = h;
-    lo[j] = __float_as_uint(wv - __uint_as_float(h));  // exact
-  }
-}
 
 // ---------------------------------------------------------------- kernel
-template <int QT, int EPI, int BN, int RM, bool EX>
-__global__ void __launch_bounds__(Cfg<QT, EPI, BN, RM, EX>::NTHREADS, 1)
+template <int QT, int EPI, int BN, bool TIO>
+__global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWu,
-                   const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmX2,
-                   const __grid_constant__ CUtensorMap tmR, int n, int k, int T, float* Y, const float* R,
-                   unsigned* status, float* ws, unsigned long long* tickets, unsigned epoch) {
-  using C = Cfg<QT, EPI, BN, RM, EX>;
-  constexpr int BK = C::BK, SUBS = C::SUBS, A_COLS = C::A_COLS;
+                   const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmR,
+                   const __grid_constant__ CUtensorMap tmY, int n, int k, int T, float* Y, const float* R,
+                   unsigned* status, float* ws, unsigned* flags, unsigned epoch) {
+  using C = Cfg<QT, EPI, BN, TIO>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, by pointer arithmetic on the shared array so that
   // the compiler keeps the shared address space (shared loads, not generic)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sB = smem + C::OFF_B;
   uint8_t* sRaw = smem + C::OFF_RAW;
-  const float* sR = reinterpret_cast<const float*>(smem + (C::RM == kRLate ? C::OFF_B : C::OFF_R));
+  float* sStage = reinterpret_cast<float*>(smem + C::OFF_STAGE);  // output pieces (and residual)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* full = bars;              // stage ready: B landed and every A writer arrived
   uint64_t* empty = full + C::S;      // stage free: its MMAs completed
@@ -271,9 +231,10 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RM, EX>::NTHREADS, 1)
   uint64_t* rawEmpty = rawFull + C::S_RAW;
   uint64_t* accFull = rawEmpty + C::S_RAW;
   uint64_t* drain = accFull + 1;
-  uint64_t* rFull = drain + 1;
+  uint64_t* rPiece = drain + 1;       // residual piece p landed
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  unsigned* parked = reinterpret_cast<unsigned*>(smem + C::OFF_MISC + 16);  // split: warps done parking
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -285,6 +246,10 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RM, EX>::NTHREADS, 1)
   const int c0 = (int)((long)z * nchunks_all / nsplit), c1 = (int)((long)(z + 1) * nchunks_all / nsplit);
   const int nchunks = c1 - c0;
   const int nk = nchunks * SUBS;
+  // piece p (token columns t0 + 64 p ..) holds a token; with a split, CTA z
+  // writes pieces 2 z and 2 z + 1
+  auto live = [&](int p) { return t0 + p * PIECE < T; };
+  auto kept = [&](int p) { return nsplit == 1 || (p >> 1) == z; };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::S; ++i) {
@@ -297,11 +262,12 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RM, EX>::NTHREADS, 1)
     }
     mbar_init(accFull, 1);
     mbar_init(drain, 1);
-    mbar_init(rFull, 1);
+    for (int p = 0; p < 4; ++p) mbar_init(&rPiece[p], 1);
     abort_flag[0] = 0;   // set by a wait that gives up
     abort_flag[1] = 0;   // never set: drain waits ignore the abort
-    *reinterpret_cast<unsigned*>(smem + C::OFF_MISC + 16) = 0;  // split-K epilogue arrivals
+    *parked = 0;
     fence_mbar_init();
+    grid_launch_dependents();
   }
   if (warp == 1) tmem_alloc(tmem_holder, C::TMEM_COLS);
   tc_fence_before();
@@ -314,18 +280,14 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RM, EX>::NTHREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmW);
       if (C::NM == 2) tma_prefetch_desc(&tmWu);
-      if (C::RM == kREarly) {  // the residual tile is needed only by the epilogue: fetch it first
-        mbar_arrive_expect_tx(rFull, C::R_BYTES);
-        tma_load_2d(smem + C::OFF_R, &tmR, m0, t0, rFull);
-      } else if (C::RM == kRLate) {
-        tma_prefetch_l2_2d(&tmR, m0, t0);
-      }
+      // an L2 prefetch changes no data, so it may run before the wait
       for (int c = 0; c < PF && c < nchunks; ++c)
         for (int m = 0; m < C::NM; ++m)
           tma_prefetch_l2_2d(m ? (const void*)&tmWu : (const void*)&tmW, (c0 + c) * (C::RAW_ROW / 2), m0);
+      grid_dependency_wait();
       int last_issued[C::S_RAW];
       for (int i = 0; i < C::S_RAW; ++i) last_issued[i] = -1;
-      bool ok = true;
+      bool ok = true, r_issued = false;
       for (int c = 0; c < nchunks && ok; ++c) {
         for (int m = 0; m < C::NM && ok; ++m) {
           const int j = c * C::NM + m;
@@ -338,22 +300,33 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RM, EX>::NTHREADS, 1)
           if (c + PF < nchunks) tma_prefetch_l2_2d(map, (c0 + c + PF) * (C::RAW_ROW / 2), m0);
           last_issued[slot] = j;
         }
+        // the residual tile, needed only by the epilogue, once the raw ring is full
+        if (C::R_EARLY && ok && !r_issued && (c == C::S_RAW - 1 || c == nchunks - 1)) {
+          for (int p = 0; p < C::NPIECE; ++p) {
+            if (!live(p)) continue;
+            mbar_arrive_expect_tx(&rPiece[p], PIECE_BYTES);
+            tma_load_2d(sStage + p * (PIECE_BYTES / 4), &tmR, m0, t0 + p * PIECE, &rPiece[p]);
+          }
+          r_issued = true;
+        }
       }
       if (!ok) {  // let the copies in flight land before the CTA exits
         for (int i = 0; i < C::S_RAW; ++i)
           if (last_issued[i] >= 0) mbar_wait(&rawFull[i], (last_issued[i] / C::S_RAW) & 1, abort_flag + 1, status);
-        if (C::RM == kREarly) mbar_wait(rFull, 0, abort_flag + 1, status);
+        if (r_issued)
+          for (int p = 0; p < C::NPIECE; ++p)
+            if (live(p)) mbar_wait(&rPiece[p], 0, abort_flag + 1, status);
       }
     }
   } else if (warp == 2) {
     // ------------------------------------------------ activation producer
     if (lane == 0) {
       tma_prefetch_desc(&tmX);
-      if (C::EX) tma_prefetch_desc(&tmX2);
-      // X (fp16 or split) is written by the conversion kernel that may still be
-      // running when this grid starts (programmatic dependent launch); nothing
-      // else this kernel reads or writes is touched by that kernel
+      // X is written by the conversion kernel, which may still be running
       grid_dependency_wait();
+      if (C::R_LATE)
+        for (int p = 0; p < C::NPIECE; ++p)
+          if (kept(p) && live(p)) tma_prefetch_l2_2d(&tmR, m0, t0 + p * PIECE);
       bool ok = true;
       int last = -1;
       for (int i = 0; i < nk; ++i) {
@@ -361,64 +334,65 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RM, EX>::NTHREADS, 1)
         ok = mbar_wait(&empty[st], ((i / C::S) & 1) ^ 1, abort_flag, status);
         if (!ok) break;
         mbar_arrive_expect_tx(&full[st], C::B_BYTES);
-        const int kx = (c0 * SUBS + i) * BK;
-        tma_load_2d(sB + st * C::B_BYTES, &tmX, kx, t0, &full[st]);
-        if (C::EX) tma_load_2d(sB + st * C::B_BYTES + C::B_TILE, &tmX2, kx, t0, &full[st]);
+        tma_load_2d(sB + st * C::B_BYTES, &tmX, (c0 * SUBS + i) * BK, t0, &full[st]);
         last = i;
       }
-      // After a give-up, wait (bounded) on the last stage issued: its phase
-      // also needs the dequant warps, so it may never complete, but by the
-      // time the bounded wait ends every copy issued has landed.
-      if (!ok && last >= 0) mbar_wait(&full[last % C::S], (last / C::S) & 1, abort_flag + 1, status);
+      // residual pieces into the ring slots as the last MMAs free them (slot
+      // p holds piece p)
+      unsigned r_issued = 0;
+      if (C::R_LATE && ok) {
+        for (int v = nk; v < nk + C::S; ++v) {
+          const int p = v % C::S;
+          if (!kept(p) || !live(p)) continue;
+          ok = mbar_wait(&empty[p], ((v / C::S) & 1) ^ 1, abort_flag, status);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&rPiece[p], PIECE_BYTES);
+          tma_load_2d(sB + p * C::B_BYTES, &tmR, m0, t0 + p * PIECE, &rPiece[p]);
+          r_issued |= 1u << p;
+        }
+      }
+      if (!ok) {
+        // After a give-up, wait (bounded) on the last stage issued: its phase
+        // also needs the dequant warps, so it may never complete, but by the
+        // time the bounded wait ends every copy issued has landed.
+        if (last >= 0) mbar_wait(&full[last % C::S], (last / C::S) & 1, abort_flag + 1, status);
+        for (int p = 0; p < 4; ++p)
+          if (r_issued & (1u << p)) mbar_wait(&rPiece[p], 0, abort_flag + 1, status);
+      }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = C::EX ? idesc_tf32_f32(BM, BN) : idesc_f16_f32(BM, BN);
-      const uint64_t bdesc0 = smem_desc_sw128(sB);
-      bool ok = true;
-      int st = 0;
-      uint32_t ph = 0;
-      for (int i = 0; i < nk && ok; ++i) {
-        ok = mbar_wait(&full[st], ph, abort_flag, status);
-        if (!ok) break;
-        tc_fence_after();
-        // stage st of B starts st * B_BYTES later: (B_BYTES >> 4) descriptor units
-        const uint64_t bdesc = bdesc0 + (uint64_t)((st * C::B_BYTES) >> 4);
+    // ------------------------------------------------ MMA issuer (whole warp)
+    constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+    const uint64_t bdesc0 = smem_desc_sw128(sB);
+    bool ok = true;
+    int st = 0;
+    uint32_t ph = 0;
+    for (int i = 0; i < nk; ++i) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&full[st], ph, abort_flag, status));
+      if (!ok) break;
+      tc_fence_after();
+      // stage st of B starts st * B_BYTES later: (B_BYTES >> 4) descriptor units
+      const uint64_t bdesc = bdesc0 + (uint64_t)((st * C::B_BYTES) >> 4);
 #pragma unroll
-        for (int m = 0; m < C::NM; ++m) {
-          const uint32_t a_tmem = tmem_base + C::A_COL0 + (m * C::S + st) * A_COLS;
-          if constexpr (C::EX) {
-            constexpr uint64_t lo_b = (uint64_t)(C::B_TILE >> 4);  // X lo tile follows X hi
+      for (int m = 0; m < C::NM; ++m) {
+        const uint32_t a_tmem = tmem_base + C::A_COL0 + (m * C::S + st) * C::A_COLS;
 #pragma unroll
-            for (int kk = 0; kk < BK / 8; ++kk) {
-              // 8 k = 8 TMEM columns of A (hi at +0, lo at +32), +32 bytes of B
-              const uint32_t ah = a_tmem + kk * 8, al = ah + 32;
-              const uint64_t bh = bdesc + 2 * kk, bl = bh + lo_b;
-              mma_tf32_ts(tmem_base + m * BN, ah, bh, idesc, (i | kk) != 0);
-              mma_tf32_ts(tmem_base + m * BN, ah, bl, idesc, 1);
-              mma_tf32_ts(tmem_base + m * BN, al, bh, idesc, 1);
-            }
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              // 16 k = 8 TMEM columns of A, +32 bytes of B inside its swizzle atom
-              mma_f16_ts(tmem_base + m * BN, a_tmem + kk * 8, bdesc + 2 * kk, idesc, (i | kk) != 0);
-            }
-          }
-        }
-        mma_commit(&empty[st]);
-        if (++st == C::S) {
-          st = 0;
-          ph ^= 1u;
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          // 16 k = 8 TMEM columns of A, +32 bytes of B inside its swizzle atom
+          mma_f16_ts_elect(tmem_base + m * BN, a_tmem + kk * 8, bdesc + 2 * kk, idesc, (i | kk) != 0);
         }
       }
-      if (ok) {
-        mma_commit(accFull);
-      } else {  // wait until the MMAs already issued have finished
-        mma_commit(drain);
-        mbar_wait(drain, 0, abort_flag + 1, status);
+      mma_commit_elect(&empty[st]);
+      if (++st == C::S) {
+        st = 0;
+        ph ^= 1u;
       }
+    }
+    if (ok) {
+      mma_commit_elect(accFull);
+    } else {  // wait until the MMAs already issued have finished
+      mma_commit_elect(drain);
+      __all_sync(0xffffffffu, mbar_wait(drain, 0, abort_flag + 1, status));
     }
   } else if (warp >= 4) {
     // ------------------------------------------------ dequant, then epilogue
@@ -438,16 +412,12 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RM, EX>::NTHREADS, 1)
       for (int s = par; s < SUBS; s += C::DQ) {
         const int i = c * SUBS + s;
         const int st = i % C::S;
-        uint32_t a[32], a_lo[32];
-        if constexpr (C::EX)
-          dequant_block_exact<QT>(raw_row, s, a, a_lo);          // overlaps the wait below
-        else
-          dequant_row_stage<QT>(raw_row + s * 2 * C::BB, a);     // overlaps the wait below
+        uint32_t a[32];
+        dequant_row_stage<QT>(raw_row + s * 2 * C::BB, a);  // overlaps the wait below
         ok = __all_sync(0xffffffffu, mbar_wait(&empty[st], ((i / C::S) & 1) ^ 1, abort_flag, status));
         if (!ok) break;
         tc_fence_after();
-        tmem_st_32x32b_x32(lane_base + C::A_COL0 + (g * C::S + st) * A_COLS, a);
-        if constexpr (C::EX) tmem_st_32x32b_x32(lane_base + C::A_COL0 + (g * C::S + st) * A_COLS + 32, a_lo);
+        tmem_st_32x32b_x32(lane_base + C::A_COL0 + (g * C::S + st) * C::A_COLS, a);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -456,142 +426,136 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RM, EX>::NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&rawEmpty[slot]);
     }
-    // epilogue: the warpgroups split the BN token columns
+
+    // ---------------------------------------------- epilogue
+    // Y, R and the workspace may still be in use by the preceding kernel
+    grid_dependency_wait();
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(accFull, 0, abort_flag, status));
+    tc_fence_after();
     const int row = m0 + (int)r;
-    constexpr int COLS_PER_WG = BN / C::NWG;
-    const int cb0 = wg * COLS_PER_WG, cb1 = cb0 + COLS_PER_WG;
+    const bool lead = (warp & 3) == 0 && lane == 0;  // issues its warpgroup's TMA stores
+    bool stored = false;
     const size_t tile = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
-    float* partial = ws + tile * (size_t)(BN * BM);  // [BN tokens][128 rows]
-    bool writer = true;  // this CTA writes Y
+    // split: half h of a tile (token columns 128 h ..) in the workspace,
+    // [128 tokens][128 rows] fp32, parked by CTA 1 - h for CTA h
+    float* half_mine = ws + (tile * 2 + (size_t)z) * (size_t)(128 * BM);
+    float* half_theirs = ws + (tile * 2 + (size_t)(1 - z)) * (size_t)(128 * BM);
+
     if (nsplit == 2) {
-      // split-K over two CTAs: the first to get here parks its fp32 partial in
-      // the workspace and raises the tile's flag; the second waits for the
-      // flag (the first is already in its epilogue), then writes Y = p0 + p1
-      // (+ R) in split order, whichever CTA got here first
-      // tile word: (epoch << 32) | arrivals this call; flag: epoch once the
-      // partial is parked. Workspace memory is not cleared between calls: a
-      // word from an earlier call (another epoch) counts as no arrival yet.
-      volatile int* role = abort_flag + 2;
-      unsigned* epi_done = reinterpret_cast<unsigned*>(smem + C::OFF_MISC + 16);  // zeroed at start
-      unsigned long long* ticket = tickets + 2 * tile;
-      unsigned* flag = reinterpret_cast<unsigned*>(tickets + 2 * tile + 1);
-      if (threadIdx.x == 128) {
-        int got = -1;
-        if (ok) {
-          unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ticket);
-          for (;;) {
-            const unsigned long long next =
-                (unsigned)(old >> 32) == epoch ? old + 1 : ((unsigned long long)epoch << 32) | 1ull;
-            const unsigned long long seen = atomicCAS(ticket, old, next);
-            if (seen == old) {
-              got = (int)(next & 0xFFFFFFFFull) - 1;
-              break;
-            }
-            old = seen;
-          }
-        }
-        *role = got;
-      }
-      named_sync(1, 128 * C::NWG);
-      const int my_role = *role;
-      writer = my_role == 1;
-      if (my_role == 0) {
-        if (ok) {
-          tc_fence_after();
-          for (int cb = cb0; cb < cb1; cb += 16) {
-            uint32_t v[16];
-            tmem_ld_32x32b_x16(lane_base + cb, v);
-            tmem_ld_wait();
+      // park piece 2 (1 - z) + wg for the partner
+      const int pg = 2 * (1 - z) + wg;
+      if (ok && live(pg)) {
+        uint32_t v[64];
+        tmem_ld_32x32b_x32(lane_base + pg * PIECE, v);
+        tmem_ld_32x32b_x32(lane_base + pg * PIECE + 32, v + 32);
+        tmem_ld_wait_regs(v);
+        regs_after_wait(v + 32);
+        float* dst = half_theirs + (size_t)wg * PIECE * BM + r;
 #pragma unroll
-            for (int j2 = 0; j2 < 16; ++j2) partial[(cb + j2) * BM + (int)r] = __uint_as_float(v[j2]);
-          }
-        }
-        // no barrier here (a warp that gave up must not be waited for): each
-        // warp counts itself in, the last one publishes the partial
+        for (int j = 0; j < PIECE; ++j) __stcg(dst + j * BM, __uint_as_float(v[j]));
+      }
+      // no barrier here (a warp that gave up must not be waited for): each
+      // warp counts itself in, the last one publishes the half
+      __threadfence();
+      __syncwarp();
+      if (lane == 0 && atomicAdd(parked, 1u) == 4u * C::NWG - 1u) {
         __threadfence();
-        __syncwarp();
-        if (lane == 0 && atomicAdd(epi_done, 1u) == 4u * C::NWG - 1u) atomicExch(flag, epoch);
-      } else if (my_role == 1 && ok) {
-        // bounded wait for the first CTA's partial
+        atomicExch(flags + tile * 2 + z, epoch);
+      }
+      // bounded wait for the partner's half
+      if (ok) {
+        int got = 1;
         if (lane == 0) {
+          const unsigned* f = flags + tile * 2 + (1 - z);
           const unsigned long long t_start = global_ns();
-          while (atomicAdd(flag, 0u) != epoch) {
+          while (atomicAdd(const_cast<unsigned*>(f), 0u) != epoch) {
             if (global_ns() - t_start > kWaitLimitNs) {
               atomicOr(status, kStatusTimeout);
               abort_flag[0] = 1;
+              got = 0;
               break;
             }
             __nanosleep(64);
           }
         }
-        __syncwarp();
-        ok = abort_flag[0] == 0;
+        ok = __shfl_sync(0xffffffffu, got, 0) != 0;
         __threadfence();
-      } else {
-        writer = false;
       }
     }
-    if (ok && writer && C::RM == kRLate && threadIdx.x == 128) {
-      // every MMA has completed, so the operand ring is free: fetch the
-      // residual tile (prefetched into L2 at kernel start) into it
-      mbar_arrive_expect_tx(rFull, C::R_BYTES);
-      tma_load_2d(smem + C::OFF_B, &tmR, m0, t0, rFull);
-    }
-    if (ok && writer && C::RM != kRNone) ok = __all_sync(0xffffffffu, mbar_wait(rFull, 0, abort_flag, status));
-    if (ok && writer) {
-      tc_fence_after();
-      const bool first_is_z0 = z == 1;  // with a split, the parked partial belongs to the other CTA
-      constexpr int CB_BATCH = COLS_PER_WG < 64 ? COLS_PER_WG : 64;
-      for (int cbb = cb0; cbb < cb1; cbb += CB_BATCH) {
-        // the other CTA's parked partial: all CB_BATCH loads in flight at once
-        float other[CB_BATCH];
-        if (nsplit == 2) {
+
+    // finalize this warpgroup's pieces: all of the tile's pieces, split evenly,
+    // or with a split piece 2 z + wg
+    constexpr int PPW = C::NPIECE / C::NWG;
+    const int npw = nsplit == 2 ? 1 : PPW;
+    for (int pp = 0; pp < npw; ++pp) {
+      const int p = nsplit == 2 ? 2 * z + wg : wg * PPW + pp;
+      if (!live(p)) continue;  // the same for the whole warpgroup
+      float* sp = sStage + p * (PIECE_BYTES / 4);
+      uint32_t v[64];
+      if (ok) {
+        tmem_ld_32x32b_x32(lane_base + p * PIECE, v);
+        tmem_ld_32x32b_x32(lane_base + p * PIECE + 32, v + 32);
+        tmem_ld_wait_regs(v);
+        regs_after_wait(v + 32);
+        if (C::NM == 2) {  // y = silu(gate) * up
+          uint32_t u[64];
+          tmem_ld_32x32b_x32(lane_base + BN + p * PIECE, u);
+          tmem_ld_32x32b_x32(lane_base + BN + p * PIECE + 32, u + 32);
+          tmem_ld_wait_regs(u);
+          regs_after_wait(u + 32);
 #pragma unroll
-          for (int q2 = 0; q2 < CB_BATCH; ++q2) other[q2] = __ldcg(partial + (cbb + q2) * BM + (int)r);
+          for (int j = 0; j < PIECE; ++j) {
+            const float gt = __uint_as_float(v[j]);
+            v[j] = __float_as_uint(gt / (1.0f + expf(-gt)) * __uint_as_float(u[j]));
+          }
         }
+        if (nsplit == 2) {  // p0 + p1, in split order
+          const float* src = half_mine + (size_t)wg * PIECE * BM + r;
 #pragma unroll
-        for (int sub = 0; sub < CB_BATCH; sub += 16) {
-          const int cb = cbb + sub;
-          // residual without the shared tile: issue all 16 loads before any store
-          // (Y may be R itself, so a load may not move past an earlier store)
+          for (int j = 0; j < PIECE; ++j) {
+            const float o = __ldcg(src + j * BM);
+            const float mine = __uint_as_float(v[j]);
+            v[j] = __float_as_uint(z == 0 ? mine + o : o + mine);
+          }
+        }
+        if (EPI == kEpiResidual && TIO)
+          ok = __all_sync(0xffffffffu, mbar_wait(&rPiece[p], 0, abort_flag, status));
+      }
+      if constexpr (TIO) {
+        if (ok) {
+#pragma unroll
+          for (int j = 0; j < PIECE; ++j) {
+            float y = __uint_as_float(v[j]);
+            if (EPI == kEpiResidual) y += sp[j * BM + r];
+            sp[j * BM + r] = y;
+          }
+          fence_proxy_async_smem();
+        }
+        named_sync(1 + wg, 128);  // every warp of the warpgroup reaches it
+        if (lead && abort_flag[0] == 0) {
+          tma_store_2d(&tmY, sp, m0, t0 + p * PIECE);
+          bulk_commit_group();
+          stored = true;
+        }
+      } else if (ok && row < n) {
+        // direct: R row t is read before Y row t is written (Y may be R)
+#pragma unroll
+        for (int j0 = 0; j0 < PIECE; j0 += 16) {
           float rv[16];
-          if (EPI == kEpiResidual && C::RM == kRNone) {
 #pragma unroll
-            for (int j2 = 0; j2 < 16; ++j2) {
-              const int t = t0 + cb + j2;
-              rv[j2] = (row < n && t < T) ? R[(size_t)t * n + row] : 0.f;
-            }
+          for (int j = 0; j < 16; ++j) {
+            const int t = t0 + p * PIECE + j0 + j;
+            rv[j] = (EPI == kEpiResidual && t < T) ? R[(size_t)t * n + row] : 0.f;
           }
-          uint32_t v[16];
-          tmem_ld_32x32b_x16(lane_base + cb, v);
-          uint32_t u[16];
-          if (C::NM == 2) tmem_ld_32x32b_x16(lane_base + BN + cb, u);
-          tmem_ld_wait();
-          if (row < n) {
 #pragma unroll
-            for (int j2 = 0; j2 < 16; ++j2) {
-              const int t = t0 + cb + j2;
-              if (t < T) {
-                const size_t o = (size_t)t * n + row;
-                float acc = __uint_as_float(v[j2]);
-                if (nsplit == 2) acc = first_is_z0 ? other[sub + j2] + acc : acc + other[sub + j2];  // p0 + p1
-                float y;
-                if (EPI == kEpiSwiGLU) {
-                  const float up = __uint_as_float(u[j2]);
-                  y = acc / (1.0f + expf(-acc)) * up;
-                } else if (EPI == kEpiResidual) {
-                  y = acc + (C::RM != kRNone ? sR[(cb + j2) * BM + (int)r] : rv[j2]);
-                } else {
-                  y = acc;
-                }
-                Y[o] = y;
-              }
-            }
+          for (int j = 0; j < 16; ++j) {
+            const int t = t0 + p * PIECE + j0 + j;
+            if (t < T) Y[(size_t)t * n + row] = __uint_as_float(v[j0 + j]) + rv[j];
           }
         }
       }
     }
+    if (stored) bulk_wait_read_all();  // the pieces stay in shared memory until read
     tc_fence_before();
   }
 
@@ -603,8 +567,11 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, RM, EX>::NTHREADS, 1)
 }
 
 // ---------------------------------------------------------------- X -> fp16
+// Launched with programmatic stream serialization: X may be written, and X16
+// still read, by the preceding kernel, so it waits for that kernel first.
 __global__ void __launch_bounds__(256) x_to_f16_kernel(const float* __restrict__ X, uint16_t* __restrict__ X16,
                                                        size_t count) {
+  grid_dependency_wait();
   grid_launch_dependents();
   const size_t n8 = count / 8;
   const float4* X4 = reinterpret_cast<const float4*>(X);
@@ -618,20 +585,6 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const float* __restrict__
     Y4[i] = make_uint4(h2_as_u32(h0), h2_as_u32(h1), h2_as_u32(h2), h2_as_u32(h3));
   }
   for (size_t i = n8 * 8 + tid; i < count; i += stride) X16[i] = __half_as_ushort(__float2half_rn(X[i]));
-}
-
-// ---------------------------------------------------------------- X -> tf32 hi, lo
-// hi = x with its 13 low mantissa bits cleared, lo = x - hi (exact).
-__global__ void __launch_bounds__(256) x_split_kernel(const float* __restrict__ X, float* __restrict__ hi,
-                                                      float* __restrict__ lo, size_t count) {
-  grid_launch_dependents();
-  const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += stride) {
-    const float x = X[i];
-    const float h = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-    hi[i] = h;
-    lo[i] = x - h;
-  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -666,11 +619,20 @@ bool make_map_2d(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* map, CUtenso
   return true;
 }
 
-template <int QT, int EPI, int BN, int RM, bool EX = false>
-int launch_cfg(const void* W, const void* Wu, int n, int k, const void* Xa, const void* Xb, int T, float* Y,
-               const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit = 1,
-               float* ws = nullptr, unsigned long long* tickets = nullptr, unsigned epoch = 0) {
-  using C = Cfg<QT, EPI, BN, RM, EX>;
+// Launch attribute that lets the kernel start before the preceding kernel of
+// the stream has finished (it waits with griddepcontrol.wait where it must).
+cudaLaunchAttribute pdl_attr() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
+template <int QT, int EPI, int BN, bool TIO>
+int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y, const float* R,
+               unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, float* ws, unsigned* flags,
+               unsigned epoch) {
+  using C = Cfg<QT, EPI, BN, TIO>;
   auto fn = encode_fn(msg, msg_len);
   if (!fn) return -1;
   CUtensorMap mW, mWu;
@@ -685,26 +647,25 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const void* Xa, cons
   } else {
     mWu = mW;
   }
-  // B operand: fp16 X (f16 leg) or the fp32 hi and lo parts of X (exact leg),
-  // 128-byte rows of a BK-column stage, swizzled
-  CUtensorMap mX, mX2;
-  const CUtensorMapDataType xt = C::EX ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const uint64_t xrow = (uint64_t)k * (C::EX ? 4 : 2);
-  if (!make_map_2d(fn, &mX, xt, Xa, (uint64_t)k, (uint64_t)T, xrow, C::BK, BN, CU_TENSOR_MAP_SWIZZLE_128B, msg,
-                   msg_len))
+  // B operand: fp16 X, 128-byte rows of a 64-column stage, swizzled
+  CUtensorMap mX;
+  if (!make_map_2d(fn, &mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X16, (uint64_t)k, (uint64_t)T, (uint64_t)k * 2, BK, BN,
+                   CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
     return -1;
-  mX2 = mX;
-  if (C::EX && !make_map_2d(fn, &mX2, xt, Xb, (uint64_t)k, (uint64_t)T, xrow, C::BK, BN, CU_TENSOR_MAP_SWIZZLE_128B,
-                            msg, msg_len))
-    return -1;
-  CUtensorMap mR = mX;
-  if (C::RM != kRNone) {  // residual [T][n] f32, box 128 rows x BN tokens
-    if (!make_map_2d(fn, &mR, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, R, (uint64_t)n, (uint64_t)T, (uint64_t)n * 4, BM, BN,
-                     CU_TENSOR_MAP_SWIZZLE_NONE, msg, msg_len))
+  // residual and output pieces: [T][n] fp32, box 128 rows x 64 tokens
+  CUtensorMap mR = mX, mY = mX;
+  if (C::R_EARLY || C::R_LATE) {
+    if (!make_map_2d(fn, &mR, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, R, (uint64_t)n, (uint64_t)T, (uint64_t)n * 4, BM,
+                     PIECE, CU_TENSOR_MAP_SWIZZLE_NONE, msg, msg_len))
+      return -1;
+  }
+  if (C::TIO) {
+    if (!make_map_2d(fn, &mY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, Y, (uint64_t)n, (uint64_t)T, (uint64_t)n * 4, BM,
+                     PIECE, CU_TENSOR_MAP_SWIZZLE_NONE, msg, msg_len))
       return -1;
   }
 
-  auto kern = gemm_tc_kernel<QT, EPI, BN, RM, EX>;
+  auto kern = gemm_tc_kernel<QT, EPI, BN, TIO>;
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -721,14 +682,10 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const void* Xa, cons
   cfg.blockDim = dim3(C::NTHREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
-  // may start while the preceding kernel (the conversion of X) finishes; only
-  // the X producer waits for it
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mW, mWu, mX, mX2, mR, n, k, T, Y, R, status, ws, tickets, epoch);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mW, mWu, mX, mR, mY, n, k, T, Y, R, status, ws, flags, epoch);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     snprintf(msg, msg_len, "gemm_tc launch: %s", cudaGetErrorString(e));
@@ -746,27 +703,41 @@ int num_sms() {
   return sms[dev] > 0 ? sms[dev] : 148;
 }
 
+template <int QT, int EPI, int BN>
+int launch_io(bool tio, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y,
+              const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, float* ws,
+              unsigned* flags, unsigned epoch) {
+  return tio ? launch_cfg<QT, EPI, BN, true>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, nsplit, ws, flags,
+                                             epoch)
+             : launch_cfg<QT, EPI, BN, false>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, nsplit, ws, flags,
+                                              epoch);
+}
+
 template <int QT>
 int launch_q(const GemmPlan& pl, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y,
-             const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, float* ws,
-             unsigned long long* tickets, unsigned epoch) {
-  if (Wu) return launch_cfg<QT, kEpiSwiGLU, 128, kRNone>(W, Wu, n, k, X16, nullptr, T, Y, R, status, s, msg, msg_len);
-  // The residual tile goes through TMA when a row of R is a multiple of 16 bytes.
-  const bool rtma = R && (n % 4) == 0;
+             const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, float* ws, unsigned* flags,
+             unsigned epoch) {
+  // TMA for the residual and the output when a row of them is a multiple of 16 bytes
+  const bool tio = (n % 4) == 0;
+  if (Wu)
+    return launch_io<QT, kEpiSwiGLU, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1, ws, flags,
+                                          epoch);
   if (pl.bn == 256) {
-    if (rtma)
-      return launch_cfg<QT, kEpiResidual, 256, kRLate>(W, Wu, n, k, X16, nullptr, T, Y, R, status, s, msg, msg_len,
-                                                       pl.nsplit, ws, tickets, epoch);
     if (R)
-      return launch_cfg<QT, kEpiResidual, 256, kRNone>(W, Wu, n, k, X16, nullptr, T, Y, R, status, s, msg, msg_len,
-                                                       pl.nsplit, ws, tickets, epoch);
-    return launch_cfg<QT, kEpiPlain, 256, kRNone>(W, Wu, n, k, X16, nullptr, T, Y, R, status, s, msg, msg_len,
-                                                  pl.nsplit, ws, tickets, epoch);
+      return launch_io<QT, kEpiResidual, 256>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, pl.nsplit,
+                                              ws, flags, epoch);
+    return launch_io<QT, kEpiPlain, 256>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, pl.nsplit, ws,
+                                         flags, epoch);
   }
-  if (rtma) return launch_cfg<QT, kEpiResidual, 128, kREarly>(W, Wu, n, k, X16, nullptr, T, Y, R, status, s, msg, msg_len);
-  if (R) return launch_cfg<QT, kEpiResidual, 128, kRNone>(W, Wu, n, k, X16, nullptr, T, Y, R, status, s, msg, msg_len);
-  return launch_cfg<QT, kEpiPlain, 128, kRNone>(W, Wu, n, k, X16, nullptr, T, Y, R, status, s, msg, msg_len);
+  if (R)
+    return launch_io<QT, kEpiResidual, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1, ws, flags,
+                                            epoch);
+  return launch_io<QT, kEpiPlain, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1, ws, flags, epoch);
 }
+
+// workspace of a split: per 256-token tile two fp32 halves of 128 x 128, then
+// per tile two epoch flags
+constexpr size_t kSplitTileBytes = 2ull * 128 * BM * 4;
 
 }  // namespace
 
@@ -774,19 +745,16 @@ cudaError_t launch_x_to_f16(const float* X, uint16_t* X16, size_t count, cudaStr
   size_t blocks = (count / 8 + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks == 0) blocks = 1;
-  x_to_f16_kernel<<<(unsigned)blocks, 256, 0, s>>>(X, X16, count);
-  return cudaGetLastError();
-}
-
-template <int QT>
-int launch_q_exact(const void* W, const void* Wu, int n, int k, const float* Xhi, const float* Xlo, int T, float* Y,
-                   const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len) {
-  if (Wu)
-    return launch_cfg<QT, kEpiSwiGLU, 128, kRNone, true>(W, Wu, n, k, Xhi, Xlo, T, Y, R, status, s, msg, msg_len);
-  if (R && (n % 4) == 0)
-    return launch_cfg<QT, kEpiResidual, 128, kRLate, true>(W, Wu, n, k, Xhi, Xlo, T, Y, R, status, s, msg, msg_len);
-  if (R) return launch_cfg<QT, kEpiResidual, 128, kRNone, true>(W, Wu, n, k, Xhi, Xlo, T, Y, R, status, s, msg, msg_len);
-  return launch_cfg<QT, kEpiPlain, 128, kRNone, true>(W, Wu, n, k, Xhi, Xlo, T, Y, R, status, s, msg, msg_len);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, x_to_f16_kernel, X, X16, count);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return e;
 }
 
 GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu, bool allow_split) {
@@ -794,16 +762,14 @@ GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu, bool allow_split) {
   if (swiglu) return pl;  // 128-token tiles, two accumulators fill TMEM
   const int sms = num_sms();
   const long tiles256 = (long)((n + BM - 1) / BM) * ((T + 255) / 256);
-  // 256-token tiles halve the MMA instructions per flop (the single issuing
-  // thread, not the tensor core, limits 128-token tiles): taken when they
+  // 256-token tiles halve the MMA instructions per flop: taken when they
   // still keep most SMs busy, or, split over k in two, fit in one wave
   if (10 * tiles256 >= 6L * sms) {
     pl.bn = 256;
   } else if (allow_split && 2 * tiles256 <= sms && k / CHUNK >= 2) {
     pl.bn = 256;
     pl.nsplit = 2;
-    // fp32 partial tiles, then per tile a ticket word and a ready flag
-    pl.ws_bytes = (size_t)tiles256 * 256 * BM * 4 + (size_t)tiles256 * 16;
+    pl.ws_bytes = (size_t)tiles256 * (kSplitTileBytes + 2 * sizeof(unsigned));
   }
   return pl;
 }
@@ -813,37 +779,23 @@ int launch_gemm_tc(const GemmPlan& pl, int qtype, const void* W, const void* Wu,
                    void* ws) {
   static std::atomic<unsigned> next_epoch{1};
   unsigned epoch = 0;
-  float* partials = nullptr;
-  unsigned long long* tickets = nullptr;
+  float* halves = nullptr;
+  unsigned* flags = nullptr;
   if (pl.nsplit > 1) {
     if (!ws) {
       snprintf(msg, msg_len, "split-K GEMM without a workspace");
       return -1;
     }
+    // a flag word left by an earlier call holds another epoch, so the
+    // workspace needs no clearing
     epoch = next_epoch.fetch_add(1);
     if (epoch == 0) epoch = next_epoch.fetch_add(1);
-    const size_t ntiles = pl.ws_bytes / ((size_t)pl.bn * BM * 4 + 16);
-    partials = static_cast<float*>(ws);
-    tickets = reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + ntiles * (size_t)pl.bn * BM * 4);
+    const size_t ntiles = (size_t)((n + BM - 1) / BM) * ((T + 255) / 256);
+    halves = static_cast<float*>(ws);
+    flags = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + ntiles * kSplitTileBytes);
   }
-  return qtype == kQ4_0
-             ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, partials, tickets, epoch)
-             : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, partials, tickets, epoch);
-}
-
-int launch_gemm_tc_exact(int qtype, const void* W, const void* Wu, int n, int k, const float* Xhi, const float* Xlo,
-                         int T, float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg,
-                         size_t msg_len) {
-  return qtype == kQ4_0 ? launch_q_exact<kQ4_0>(W, Wu, n, k, Xhi, Xlo, T, Y, R, status, s, msg, msg_len)
-                        : launch_q_exact<kQ8_0>(W, Wu, n, k, Xhi, Xlo, T, Y, R, status, s, msg, msg_len);
-}
-
-cudaError_t launch_x_split(const float* X, float* hi, float* lo, size_t count, cudaStream_t s) {
-  size_t blocks = (count + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  if (blocks == 0) blocks = 1;
-  x_split_kernel<<<(unsigned)blocks, 256, 0, s>>>(X, hi, lo, count);
-  return cudaGetLastError();
+  return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, halves, flags, epoch)
+                        : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, halves, flags, epoch);
 }
 
 }  // namespace apr
