@@ -162,20 +162,18 @@ int run(const Problem& p) {
   if (p.k % 256 != 0 || p.leg == APR_LEG_EXACT_F32)
     return launched(launch_gemm_simt(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, p.R, p.s), "gemm_simt");
 
-  // one pooled scratch: the fp16 copy of X, then the split-K workspace if any
-  const GemmPlan plan = plan_gemm_tc(p.n, p.k, p.T, p.Wu != nullptr, true);
+  // pooled scratch: the fp16 copy of X
+  const GemmPlan plan = plan_gemm_tc(p.n, p.k, p.T, p.Wu != nullptr);
   const size_t count = (size_t)p.T * (size_t)p.k;
-  const size_t x16_bytes = (count * 2 + 255) & ~(size_t)255;
   void* x16 = nullptr;
-  cudaError_t e = cudaMallocFromPoolAsync(&x16, x16_bytes + plan.ws_bytes, st->pool, p.s);
+  cudaError_t e = cudaMallocFromPoolAsync(&x16, count * 2, st->pool, p.s);
   if (e != cudaSuccess)
-    return fail(APR_E_NOMEM, "scratch for fp16 X (%zu bytes): %s", x16_bytes + plan.ws_bytes, cudaGetErrorString(e));
+    return fail(APR_E_NOMEM, "scratch for fp16 X (%zu bytes): %s", count * 2, cudaGetErrorString(e));
   rc = launched(launch_x_to_f16(p.X, static_cast<uint16_t*>(x16), count, p.s), "x_to_f16");
   if (rc == APR_OK) {
     char msg[256] = "";
-    void* ws = plan.ws_bytes ? static_cast<char*>(x16) + x16_bytes : nullptr;
     if (launch_gemm_tc(plan, p.qtype, p.W, p.Wu, p.n, p.k, static_cast<const uint16_t*>(x16), p.T, p.Y, p.R,
-                       st->status, p.s, msg, sizeof msg, ws) != 0)
+                       st->status, p.s, msg, sizeof msg) != 0)
       rc = fail(APR_E_LAUNCH, "%s", msg);
   }
   e = cudaFreeAsync(x16, p.s);
@@ -268,23 +266,12 @@ int apr_qgemm_f16_in(int qtype, const void* W, const void* Wu, int n, int k, con
   DeviceState* st = nullptr;
   rc = device_state(&st);
   if (rc != APR_OK) return rc;
-  const GemmPlan plan = plan_gemm_tc(n, k, T, Wu != nullptr, true);
-  void* ws = nullptr;
-  if (plan.ws_bytes) {
-    const cudaError_t e = cudaMallocFromPoolAsync(&ws, plan.ws_bytes, st->pool, (cudaStream_t)stream);
-    if (e != cudaSuccess)
-      return fail(APR_E_NOMEM, "split-K workspace (%zu bytes): %s", plan.ws_bytes, cudaGetErrorString(e));
-  }
+  const GemmPlan plan = plan_gemm_tc(n, k, T, Wu != nullptr);
   char msg[256] = "";
-  rc = APR_OK;
   if (launch_gemm_tc(plan, qtype, W, Wu, n, k, static_cast<const uint16_t*>(X16), T, Y, residual, st->status,
-                     (cudaStream_t)stream, msg, sizeof msg, ws) != 0)
-    rc = fail(APR_E_LAUNCH, "%s", msg);
-  if (ws) {
-    const cudaError_t e = cudaFreeAsync(ws, (cudaStream_t)stream);
-    if (rc == APR_OK && e != cudaSuccess) rc = fail(APR_E_LAUNCH, "cudaFreeAsync: %s", cudaGetErrorString(e));
-  }
-  return rc;
+                     (cudaStream_t)stream, msg, sizeof msg) != 0)
+    return fail(APR_E_LAUNCH, "%s", msg);
+  return APR_OK;
 }
 
 int apr_dequant(int qtype, const void* W, int n, int k, float* out, apr_stream_t stream) {

@@ -36,23 +36,21 @@ cudaError_t launch_gemm_simt(int qtype, const void* W, const void* Wu, int n, in
 // it reads X or writes X16.
 cudaError_t launch_x_to_f16(const float* X, uint16_t* X16, size_t count, cudaStream_t s);
 
-// Shape of a tensor-core GEMM launch: token-tile width, split over k (1 or 2)
-// and, with a split, the bytes of workspace it needs (fp32 half tiles and
-// per-tile flags; it needs no clearing).
+// Shape of a tensor-core GEMM launch: token-tile width (128 or 256) and split
+// over k (1, or 2 CTAs per tile as a cluster that combines its halves in
+// distributed shared memory; no workspace either way).
 struct GemmPlan {
   int bn = 128;
   int nsplit = 1;
-  size_t ws_bytes = 0;
 };
-GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu, bool allow_split);
+GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu);
 
 // tcgen05 fp16-input GEMM; needs k % 256 == 0 and X16 = fp16(X) (gemm_tc.cu).
 // `status` is the device status word. Launched with programmatic stream
 // serialization: it waits for the preceding kernel before it touches X16, W,
-// R, Y or the workspace.
+// R or Y.
 int launch_gemm_tc(const GemmPlan& plan, int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16,
-                   int T, float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len,
-                   void* ws = nullptr);
+                   int T, float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len);
 
 // Shared with the allocation-free entry point (api.cu): sets this thread's error
 // message and returns `code`; checks the arguments of a plain / residual GEMM

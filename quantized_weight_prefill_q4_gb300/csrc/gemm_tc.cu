@@ -37,11 +37,13 @@
 // residual (or applies the SiLU gate), writes the piece into shared memory and
 // one thread stores it with a TMA tensor store; when a row of Y is not a
 // multiple of 16 bytes the threads store Y directly instead.
-// Split over k (two CTAs per tile, blockIdx.z = 0, 1): CTA z finalizes token
-// columns [128 z, 128 z + 128) of the tile and parks the other half of its fp32
-// accumulator in a workspace for its partner; each waits (bounded) for the
-// partner's half and adds p0 + p1 in split order, so the result does not depend
-// on which CTA finishes first.
+// Split over k (two CTAs per tile, blockIdx.z = 0, 1, launched as a cluster
+// (1, 1, 2)): CTA z finalizes token columns [128 z, 128 z + 128) of the tile.
+// Once both have finished their MMAs, each writes the other half of its fp32
+// accumulator into a free operand-ring slot of its partner (distributed shared
+// memory), then adds p0 + p1 in split order, so the result does not depend on
+// which CTA finishes first. A cluster barrier at the end keeps both CTAs alive
+// until neither touches the other's shared memory.
 // Every mbarrier wait is bounded (2 s); a wait that gives up sets the device
 // status word and an abort flag in shared memory so that every role leaves its
 // loop, drains its own TMA copies and MMAs, and the CTA frees its TMEM.
@@ -107,7 +109,7 @@ struct Cfg {
   static constexpr int OFF_RAW = OFF_B + S * B_BYTES;
   static constexpr int OFF_R = OFF_RAW + S_RAW * RAW_BYTES;
   static constexpr int OFF_BAR = OFF_R + R_BYTES;
-  static constexpr int NBAR = 2 * S + 2 * S_RAW + 2 + 4;  // + accFull, drain, 4 residual pieces
+  static constexpr int NBAR = 2 * S + 2 * S_RAW + 2 + 4 + 2;  // + accFull, drain, 4 residual pieces, 2 split
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 32 + 1024;   // + alignment slack
   // staging of the output pieces: the residual buffer, else the operand ring
@@ -215,7 +217,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWu,
                    const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmR,
                    const __grid_constant__ CUtensorMap tmY, int n, int k, int T, float* Y, const float* R,
-                   unsigned* status, float* ws, unsigned* flags, unsigned epoch) {
+                   unsigned* status) {
   using C = Cfg<QT, EPI, BN, TIO>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, by pointer arithmetic on the shared array so that
@@ -232,9 +234,10 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
   uint64_t* accFull = rawEmpty + C::S_RAW;
   uint64_t* drain = accFull + 1;
   uint64_t* rPiece = drain + 1;       // residual piece p landed
+  uint64_t* peerFree = rPiece + 4;    // split: the partner may write into this CTA's receive slots
+  uint64_t* xferFull = peerFree + 1;  // split: the partner's half has landed in them
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  unsigned* parked = reinterpret_cast<unsigned*>(smem + C::OFF_MISC + 16);  // split: warps done parking
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
   const int nchunks = c1 - c0;
   const int nk = nchunks * SUBS;
   // piece p (token columns t0 + 64 p ..) holds a token; with a split, CTA z
-  // writes pieces 2 z and 2 z + 1
+  // (its rank in the cluster) writes pieces 2 z and 2 z + 1
   auto live = [&](int p) { return t0 + p * PIECE < T; };
   auto kept = [&](int p) { return nsplit == 1 || (p >> 1) == z; };
 
@@ -263,12 +266,17 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
     mbar_init(accFull, 1);
     mbar_init(drain, 1);
     for (int p = 0; p < 4; ++p) mbar_init(&rPiece[p], 1);
+    mbar_init(peerFree, 1);
+    mbar_init(xferFull, 128 * C::NWG);
     abort_flag[0] = 0;   // set by a wait that gives up
     abort_flag[1] = 0;   // never set: drain waits ignore the abort
-    *parked = 0;
     fence_mbar_init();
     grid_launch_dependents();
   }
+  // split: the partner's barriers must be initialized before the first remote
+  // access (the matching wait comes just before it)
+  bool cluster_started = nsplit == 1;
+  if (nsplit == 2) cluster_arrive_relaxed();
   if (warp == 1) tmem_alloc(tmem_holder, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -428,59 +436,38 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
     }
 
     // ---------------------------------------------- epilogue
-    // Y, R and the workspace may still be in use by the preceding kernel
+    // Y and R may still be in use by the preceding kernel
     grid_dependency_wait();
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(accFull, 0, abort_flag, status));
     tc_fence_after();
     const int row = m0 + (int)r;
     const bool lead = (warp & 3) == 0 && lane == 0;  // issues its warpgroup's TMA stores
     bool stored = false;
-    const size_t tile = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
-    // split: half h of a tile (token columns 128 h ..) in the workspace,
-    // [128 tokens][128 rows] fp32, parked by CTA 1 - h for CTA h
-    float* half_mine = ws + (tile * 2 + (size_t)z) * (size_t)(128 * BM);
-    float* half_theirs = ws + (tile * 2 + (size_t)(1 - z)) * (size_t)(128 * BM);
 
     if (nsplit == 2) {
-      // park piece 2 (1 - z) + wg for the partner
-      const int pg = 2 * (1 - z) + wg;
+      // Receive slots: the ring slots of the pieces this CTA gives away (no
+      // residual goes there). The partner's partial of piece p lands in this
+      // CTA's slot p ^ 2.
+      const uint32_t peer = (uint32_t)(1 - z);
+      cluster_wait();
+      cluster_started = true;
+      // every MMA has completed: this CTA's receive slots are free
+      if (ok && threadIdx.x == 128) mbar_arrive_remote(mapa_shared(smem_u32(peerFree), peer));
+      const int pg = 2 * (1 - z) + wg;  // the piece the partner keeps
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(peerFree, 0, abort_flag, status));
       if (ok && live(pg)) {
         uint32_t v[64];
         tmem_ld_32x32b_x32(lane_base + pg * PIECE, v);
         tmem_ld_32x32b_x32(lane_base + pg * PIECE + 32, v + 32);
         tmem_ld_wait_regs(v);
         regs_after_wait(v + 32);
-        float* dst = half_theirs + (size_t)wg * PIECE * BM + r;
+        const uint32_t dst = mapa_shared(smem_u32(sB + (pg ^ 2) * C::B_BYTES) + r * 4u, peer);
 #pragma unroll
-        for (int j = 0; j < PIECE; ++j) __stcg(dst + j * BM, __uint_as_float(v[j]));
+        for (int j = 0; j < PIECE; ++j) st_cluster_f32(dst + (uint32_t)(j * BM * 4), __uint_as_float(v[j]));
       }
-      // no barrier here (a warp that gave up must not be waited for): each
-      // warp counts itself in, the last one publishes the half
-      __threadfence();
-      __syncwarp();
-      if (lane == 0 && atomicAdd(parked, 1u) == 4u * C::NWG - 1u) {
-        __threadfence();
-        atomicExch(flags + tile * 2 + z, epoch);
-      }
-      // bounded wait for the partner's half
-      if (ok) {
-        int got = 1;
-        if (lane == 0) {
-          const unsigned* f = flags + tile * 2 + (1 - z);
-          const unsigned long long t_start = global_ns();
-          while (atomicAdd(const_cast<unsigned*>(f), 0u) != epoch) {
-            if (global_ns() - t_start > kWaitLimitNs) {
-              atomicOr(status, kStatusTimeout);
-              abort_flag[0] = 1;
-              got = 0;
-              break;
-            }
-            __nanosleep(64);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, got, 0) != 0;
-        __threadfence();
-      }
+      // each thread releases its own stores (an arrival per thread)
+      if (ok) mbar_arrive_remote(mapa_shared(smem_u32(xferFull), peer));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(xferFull, 0, abort_flag, status));
     }
 
     // finalize this warpgroup's pieces: all of the tile's pieces, split evenly,
@@ -510,10 +497,10 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
           }
         }
         if (nsplit == 2) {  // p0 + p1, in split order
-          const float* src = half_mine + (size_t)wg * PIECE * BM + r;
+          const float* src = reinterpret_cast<const float*>(sB + (p ^ 2) * C::B_BYTES) + r;
 #pragma unroll
           for (int j = 0; j < PIECE; ++j) {
-            const float o = __ldcg(src + j * BM);
+            const float o = src[j * BM];
             const float mine = __uint_as_float(v[j]);
             v[j] = __float_as_uint(z == 0 ? mine + o : o + mine);
           }
@@ -559,6 +546,11 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
     tc_fence_before();
   }
 
+  if (nsplit == 2) {  // neither CTA exits while the other may still access its shared memory
+    if (!cluster_started) cluster_wait();
+    cluster_arrive();
+    cluster_wait();
+  }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -630,8 +622,7 @@ cudaLaunchAttribute pdl_attr() {
 
 template <int QT, int EPI, int BN, bool TIO>
 int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y, const float* R,
-               unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, float* ws, unsigned* flags,
-               unsigned epoch) {
+               unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit) {
   using C = Cfg<QT, EPI, BN, TIO>;
   auto fn = encode_fn(msg, msg_len);
   if (!fn) return -1;
@@ -682,10 +673,17 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
   cfg.blockDim = dim3(C::NTHREADS);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1] = {pdl_attr()};
-  cfg.attrs = attr;
+  cudaLaunchAttribute attr[2] = {pdl_attr(), pdl_attr()};
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mW, mWu, mX, mR, mY, n, k, T, Y, R, status, ws, flags, epoch);
+  if (nsplit == 2) {  // the two k halves of a tile form a cluster
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 2;
+    cfg.numAttrs = 2;
+  }
+  cfg.attrs = attr;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mW, mWu, mX, mR, mY, n, k, T, Y, R, status);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     snprintf(msg, msg_len, "gemm_tc launch: %s", cudaGetErrorString(e));
@@ -705,39 +703,25 @@ int num_sms() {
 
 template <int QT, int EPI, int BN>
 int launch_io(bool tio, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y,
-              const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, float* ws,
-              unsigned* flags, unsigned epoch) {
-  return tio ? launch_cfg<QT, EPI, BN, true>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, nsplit, ws, flags,
-                                             epoch)
-             : launch_cfg<QT, EPI, BN, false>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, nsplit, ws, flags,
-                                              epoch);
+              const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit) {
+  return tio ? launch_cfg<QT, EPI, BN, true>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, nsplit)
+             : launch_cfg<QT, EPI, BN, false>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, nsplit);
 }
 
 template <int QT>
 int launch_q(const GemmPlan& pl, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y,
-             const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, float* ws, unsigned* flags,
-             unsigned epoch) {
+             const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len) {
   // TMA for the residual and the output when a row of them is a multiple of 16 bytes
   const bool tio = (n % 4) == 0;
-  if (Wu)
-    return launch_io<QT, kEpiSwiGLU, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1, ws, flags,
-                                          epoch);
+  if (Wu) return launch_io<QT, kEpiSwiGLU, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1);
   if (pl.bn == 256) {
     if (R)
-      return launch_io<QT, kEpiResidual, 256>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, pl.nsplit,
-                                              ws, flags, epoch);
-    return launch_io<QT, kEpiPlain, 256>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, pl.nsplit, ws,
-                                         flags, epoch);
+      return launch_io<QT, kEpiResidual, 256>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, pl.nsplit);
+    return launch_io<QT, kEpiPlain, 256>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, pl.nsplit);
   }
-  if (R)
-    return launch_io<QT, kEpiResidual, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1, ws, flags,
-                                            epoch);
-  return launch_io<QT, kEpiPlain, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1, ws, flags, epoch);
+  if (R) return launch_io<QT, kEpiResidual, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1);
+  return launch_io<QT, kEpiPlain, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1);
 }
-
-// workspace of a split: per 256-token tile two fp32 halves of 128 x 128, then
-// per tile two epoch flags
-constexpr size_t kSplitTileBytes = 2ull * 128 * BM * 4;
 
 }  // namespace
 
@@ -757,7 +741,7 @@ cudaError_t launch_x_to_f16(const float* X, uint16_t* X16, size_t count, cudaStr
   return e;
 }
 
-GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu, bool allow_split) {
+GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu) {
   GemmPlan pl;
   if (swiglu) return pl;  // 128-token tiles, two accumulators fill TMEM
   const int sms = num_sms();
@@ -766,36 +750,17 @@ GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu, bool allow_split) {
   // still keep most SMs busy, or, split over k in two, fit in one wave
   if (10 * tiles256 >= 6L * sms) {
     pl.bn = 256;
-  } else if (allow_split && 2 * tiles256 <= sms && k / CHUNK >= 2) {
+  } else if (2 * tiles256 <= sms && k / CHUNK >= 2) {
     pl.bn = 256;
     pl.nsplit = 2;
-    pl.ws_bytes = (size_t)tiles256 * (kSplitTileBytes + 2 * sizeof(unsigned));
   }
   return pl;
 }
 
 int launch_gemm_tc(const GemmPlan& pl, int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16,
-                   int T, float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len,
-                   void* ws) {
-  static std::atomic<unsigned> next_epoch{1};
-  unsigned epoch = 0;
-  float* halves = nullptr;
-  unsigned* flags = nullptr;
-  if (pl.nsplit > 1) {
-    if (!ws) {
-      snprintf(msg, msg_len, "split-K GEMM without a workspace");
-      return -1;
-    }
-    // a flag word left by an earlier call holds another epoch, so the
-    // workspace needs no clearing
-    epoch = next_epoch.fetch_add(1);
-    if (epoch == 0) epoch = next_epoch.fetch_add(1);
-    const size_t ntiles = (size_t)((n + BM - 1) / BM) * ((T + 255) / 256);
-    halves = static_cast<float*>(ws);
-    flags = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + ntiles * kSplitTileBytes);
-  }
-  return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, halves, flags, epoch)
-                        : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, halves, flags, epoch);
+                   int T, float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len) {
+  return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len)
+                        : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len);
 }
 
 }  // namespace apr

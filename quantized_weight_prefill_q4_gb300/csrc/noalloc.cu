@@ -94,7 +94,7 @@ extern "C" int apr_qgemm_noalloc(int qtype, const void* W, int n, int k, const f
   cudaError_t e = launch_x_to_f16(X, st->scratch, (size_t)T * (size_t)k, s);
   if (e != cudaSuccess) return set_error(APR_E_LAUNCH, cudaGetErrorString(e));
   char msg[256] = "";
-  const GemmPlan plan = plan_gemm_tc(n, k, T, false, false);  // no split: it would need a workspace
+  const GemmPlan plan = plan_gemm_tc(n, k, T, false);
   if (launch_gemm_tc(plan, qtype, W, nullptr, n, k, st->scratch, T, Y, residual, st->status, s, msg, sizeof msg) != 0)
     return set_error(APR_E_LAUNCH, msg);
   return APR_OK;

@@ -182,13 +182,15 @@ def test_wide_tiles(q, qtype, n, res):
 
 
 # ------------------------------------------------------------------ tile plans
-# Small grids run 256-token tiles split over k between two CTAs (the second to
-# finish adds the first one's parked partial); 80 row tiles of 256 tokens are
-# too many to split and too few for 256-token tiles, so they take 128-token
-# tiles. Both with and without a residual, and with rows that are not a
-# multiple of 4 (residual read straight from memory).
+# Small grids run 256-token tiles split over k between the two CTAs of a
+# cluster (each finalizes half the tile's tokens); with T = 100 or 300 some of
+# a CTA's 64-token pieces hold no token. 80 row tiles of 256 tokens are too
+# many to split and too few for 256-token tiles, so they take 128-token tiles.
+# Both with and without a residual, and with rows that are not a multiple of 4
+# (residual and output through direct loads and stores instead of TMA).
 @pytest.mark.parametrize("qtype", QTYPES)
-@pytest.mark.parametrize("n,k,T,res", [(298, 512, 100, True), (512, 2048, 300, True), (10240, 256, 200, False),
+@pytest.mark.parametrize("n,k,T,res", [(298, 512, 100, True), (296, 512, 100, True), (296, 512, 100, False),
+                                       (512, 2048, 300, True), (512, 2048, 300, False), (10240, 256, 200, False),
                                        (10240, 256, 200, True), (10238, 256, 130, True)])
 def test_tile_plans(q, qtype, n, k, T, res):
     c = synth.make_case(qtype, n, k, T, residual=res, seed=3 * n + T)
