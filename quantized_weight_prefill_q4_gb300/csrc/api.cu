@@ -173,7 +173,7 @@ int run(const Problem& p) {
   if (rc == APR_OK) {
     char msg[256] = "";
     if (launch_gemm_tc(plan, p.qtype, p.W, p.Wu, p.n, p.k, static_cast<const uint16_t*>(x16), p.T, p.Y, p.R,
-                       st->status, p.s, msg, sizeof msg) != 0)
+                       st->status, p.s, msg, sizeof msg, true) != 0)
       rc = fail(APR_E_LAUNCH, "%s", msg);
   }
   e = cudaFreeAsync(x16, p.s);
@@ -269,7 +269,7 @@ int apr_qgemm_f16_in(int qtype, const void* W, const void* Wu, int n, int k, con
   const GemmPlan plan = plan_gemm_tc(n, k, T, Wu != nullptr);
   char msg[256] = "";
   if (launch_gemm_tc(plan, qtype, W, Wu, n, k, static_cast<const uint16_t*>(X16), T, Y, residual, st->status,
-                     (cudaStream_t)stream, msg, sizeof msg) != 0)
+                     (cudaStream_t)stream, msg, sizeof msg, false) != 0)
     return fail(APR_E_LAUNCH, "%s", msg);
   return APR_OK;
 }

@@ -48,9 +48,11 @@ GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu);
 // tcgen05 fp16-input GEMM; needs k % 256 == 0 and X16 = fp16(X) (gemm_tc.cu).
 // `status` is the device status word. Launched with programmatic stream
 // serialization: it waits for the preceding kernel before it touches X16, W,
-// R or Y.
+// R or Y, except that with `after_conversion` (launched right after
+// launch_x_to_f16 on the same stream) it reads W and R without waiting.
 int launch_gemm_tc(const GemmPlan& plan, int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16,
-                   int T, float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len);
+                   int T, float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len,
+                   bool after_conversion);
 
 // Shared with the allocation-free entry point (api.cu): sets this thread's error
 // message and returns `code`; checks the arguments of a plain / residual GEMM

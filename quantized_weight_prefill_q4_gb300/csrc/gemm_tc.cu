@@ -39,18 +39,24 @@
 // multiple of 16 bytes the threads store Y directly instead.
 // Split over k (two CTAs per tile, blockIdx.z = 0, 1, launched as a cluster
 // (1, 1, 2)): CTA z finalizes token columns [128 z, 128 z + 128) of the tile.
-// Once both have finished their MMAs, each writes the other half of its fp32
-// accumulator into a free operand-ring slot of its partner (distributed shared
-// memory), then adds p0 + p1 in split order, so the result does not depend on
-// which CTA finishes first. A cluster barrier at the end keeps both CTAs alive
-// until neither touches the other's shared memory.
+// Its weight producer tells the partner when the raw ring is free (the last
+// chunk decoded, a little before the last MMAs finish); after its MMAs each CTA
+// stages the other half of its fp32 accumulator in its own operand ring and
+// sends it with one bulk copy per piece into the partner's raw ring
+// (distributed shared memory), then adds p0 + p1 in split order, so the result
+// does not depend on which CTA finishes first. A cluster barrier at the end
+// keeps both CTAs resident until neither touches the other's shared memory.
 // Every mbarrier wait is bounded (2 s); a wait that gives up sets the device
 // status word and an abort flag in shared memory so that every role leaves its
 // loop, drains its own TMA copies and MMAs, and the CTA frees its TMEM.
 // Programmatic dependent launch: the kernel lets the next kernel of the stream
 // launch early, and itself reads and writes global memory only after
 // griddepcontrol.wait (the X producer, the weight producer and the epilogue
-// each wait; only L2 prefetches of the weight go before).
+// each wait; only L2 prefetches of the weight go before). Launched right after
+// the library's own X conversion (w_early), the weight producer does not wait:
+// that kernel writes only X16, and it lets the GEMM launch only after every
+// kernel before it has completed, so the weight and residual loads overlap the
+// conversion.
 
 #include <cstdint>
 #include <cstdio>
@@ -98,7 +104,8 @@ struct Cfg {
   static constexpr int R_BYTES = R_EARLY ? NPIECE * PIECE_BYTES : 0;
   // operand stages (A in TMEM and B in shared memory advance together)
   static constexpr int S = NM == 2 ? 4 : (BN == 256 ? 4 : (QT == kQ4_0 ? 6 : 5));
-  static constexpr int S_RAW = NM == 1 ? (QT == kQ4_0 ? 3 : 2) : (QT == kQ4_0 ? 4 : 3);
+  // (with 256-token tiles the raw ring also receives the partner's half of a split)
+  static constexpr int S_RAW = NM == 1 ? (QT == kQ4_0 ? (BN == 256 ? 4 : 3) : 2) : (QT == kQ4_0 ? 4 : 3);
   static constexpr int NTHREADS = 128 + 128 * NWG;
   static constexpr int ACC_COLS = NM * BN;
   static constexpr int A_COL0 = ACC_COLS;                       // first A column
@@ -120,6 +127,8 @@ struct Cfg {
   static_assert(NPIECE % NWG == 0, "epilogue pieces per warpgroup");
   static_assert(R_EARLY || NPIECE * PIECE_BYTES <= S * B_BYTES, "output pieces fit the operand ring");
   static_assert(!R_LATE || B_BYTES == PIECE_BYTES, "a late residual piece is one ring slot");
+  static_assert(BN != 256 || (B_BYTES == PIECE_BYTES && S_RAW * RAW_BYTES >= 2 * PIECE_BYTES),
+                "split: a piece is one ring slot, the raw ring holds the partner's two pieces");
 };
 
 // ---------------------------------------------------------------- dequant
@@ -217,7 +226,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWu,
                    const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmR,
                    const __grid_constant__ CUtensorMap tmY, int n, int k, int T, float* Y, const float* R,
-                   unsigned* status) {
+                   unsigned* status, int w_early) {
   using C = Cfg<QT, EPI, BN, TIO>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, by pointer arithmetic on the shared array so that
@@ -234,8 +243,8 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
   uint64_t* accFull = rawEmpty + C::S_RAW;
   uint64_t* drain = accFull + 1;
   uint64_t* rPiece = drain + 1;       // residual piece p landed
-  uint64_t* peerFree = rPiece + 4;    // split: the partner may write into this CTA's receive slots
-  uint64_t* xferFull = peerFree + 1;  // split: the partner's half has landed in them
+  uint64_t* peerFree = rPiece + 4;    // split: the partner's raw ring is free to receive
+  uint64_t* xferFull = peerFree + 1;  // split: the partner's half has landed in this raw ring
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -267,15 +276,16 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
     mbar_init(drain, 1);
     for (int p = 0; p < 4; ++p) mbar_init(&rPiece[p], 1);
     mbar_init(peerFree, 1);
-    mbar_init(xferFull, 128 * C::NWG);
+    mbar_init(xferFull, 1);
     abort_flag[0] = 0;   // set by a wait that gives up
     abort_flag[1] = 0;   // never set: drain waits ignore the abort
     fence_mbar_init();
     grid_launch_dependents();
   }
   // split: the partner's barriers must be initialized before the first remote
-  // access (the matching wait comes just before it)
-  bool cluster_started = nsplit == 1;
+  // access (the matching wait comes just before it); a thread arrives at the
+  // closing barrier once it touches the partner's shared memory no more
+  bool cl_started = false, cl_done = false;
   if (nsplit == 2) cluster_arrive_relaxed();
   if (warp == 1) tmem_alloc(tmem_holder, C::TMEM_COLS);
   tc_fence_before();
@@ -292,7 +302,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
       for (int c = 0; c < PF && c < nchunks; ++c)
         for (int m = 0; m < C::NM; ++m)
           tma_prefetch_l2_2d(m ? (const void*)&tmWu : (const void*)&tmW, (c0 + c) * (C::RAW_ROW / 2), m0);
-      grid_dependency_wait();
+      if (!w_early) grid_dependency_wait();
       int last_issued[C::S_RAW];
       for (int i = 0; i < C::S_RAW; ++i) last_issued[i] = -1;
       bool ok = true, r_issued = false;
@@ -317,6 +327,17 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
           }
           r_issued = true;
         }
+      }
+      if (ok && nsplit == 2) {
+        // every raw slot read for the last time: the partner may send into the ring
+        const int total = nchunks * C::NM;
+        for (int v = total; v < total + C::S_RAW && ok; ++v)
+          ok = mbar_wait(&rawEmpty[v % C::S_RAW], ((v / C::S_RAW) & 1) ^ 1, abort_flag, status);
+        cluster_wait();
+        cl_started = true;
+        if (ok) mbar_arrive_remote(mapa_shared(smem_u32(peerFree), (uint32_t)(1 - z)));
+        cluster_arrive();
+        cl_done = true;
       }
       if (!ok) {  // let the copies in flight land before the CTA exits
         for (int i = 0; i < C::S_RAW; ++i)
@@ -445,29 +466,40 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
     bool stored = false;
 
     if (nsplit == 2) {
-      // Receive slots: the ring slots of the pieces this CTA gives away (no
-      // residual goes there). The partner's partial of piece p lands in this
-      // CTA's slot p ^ 2.
+      // stage the piece the partner keeps in this CTA's (now idle) ring slot
+      // pg, [64 tokens][128 rows], and send it to the partner's raw ring, at
+      // 32 KB x wg; the partner's copy of piece pk lands in this raw ring the
+      // same way
       const uint32_t peer = (uint32_t)(1 - z);
-      cluster_wait();
-      cluster_started = true;
-      // every MMA has completed: this CTA's receive slots are free
-      if (ok && threadIdx.x == 128) mbar_arrive_remote(mapa_shared(smem_u32(peerFree), peer));
-      const int pg = 2 * (1 - z) + wg;  // the piece the partner keeps
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(peerFree, 0, abort_flag, status));
+      const int pg = 2 * (1 - z) + wg, pk = 2 * z + wg;
+      float* stage = reinterpret_cast<float*>(sB + pg * C::B_BYTES);
       if (ok && live(pg)) {
         uint32_t v[64];
         tmem_ld_32x32b_x32(lane_base + pg * PIECE, v);
         tmem_ld_32x32b_x32(lane_base + pg * PIECE + 32, v + 32);
         tmem_ld_wait_regs(v);
         regs_after_wait(v + 32);
-        const uint32_t dst = mapa_shared(smem_u32(sB + (pg ^ 2) * C::B_BYTES) + r * 4u, peer);
 #pragma unroll
-        for (int j = 0; j < PIECE; ++j) st_cluster_f32(dst + (uint32_t)(j * BM * 4), __uint_as_float(v[j]));
+        for (int j = 0; j < PIECE; ++j) stage[j * BM + r] = __uint_as_float(v[j]);
+        fence_proxy_async_smem();
       }
-      // each thread releases its own stores (an arrival per thread)
-      if (ok) mbar_arrive_remote(mapa_shared(smem_u32(xferFull), peer));
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(xferFull, 0, abort_flag, status));
+      cluster_wait();
+      cl_started = true;
+      if (threadIdx.x == 128)  // the bytes of this CTA's live kept pieces
+        mbar_arrive_expect_tx(xferFull, PIECE_BYTES * ((live(2 * z) ? 1 : 0) + (live(2 * z + 1) ? 1 : 0)));
+      named_sync(1 + wg, 128);  // the warpgroup's piece is staged
+      if (lead && live(pg)) {
+        bool go = abort_flag[0] == 0;
+        if (go) go = mbar_wait_cluster(peerFree, 0, abort_flag, status);
+        if (go)
+          bulk_copy_to_peer(mapa_shared(smem_u32(sRaw + wg * PIECE_BYTES), peer), stage, PIECE_BYTES,
+                            mapa_shared(smem_u32(xferFull), peer));
+      }
+      if (ok && live(pk)) ok = __all_sync(0xffffffffu, mbar_wait_cluster(xferFull, 0, abort_flag, status));
+      // the partner's copy has landed: once the partner has seen this CTA's
+      // copy land as well, neither touches the other's shared memory again
+      cluster_arrive();
+      cl_done = true;
     }
 
     // finalize this warpgroup's pieces: all of the tile's pieces, split evenly,
@@ -497,7 +529,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
           }
         }
         if (nsplit == 2) {  // p0 + p1, in split order
-          const float* src = reinterpret_cast<const float*>(sB + (p ^ 2) * C::B_BYTES) + r;
+          const float* src = reinterpret_cast<const float*>(sRaw + wg * PIECE_BYTES) + r;
 #pragma unroll
           for (int j = 0; j < PIECE; ++j) {
             const float o = src[j * BM];
@@ -546,9 +578,10 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
     tc_fence_before();
   }
 
-  if (nsplit == 2) {  // neither CTA exits while the other may still access its shared memory
-    if (!cluster_started) cluster_wait();
-    cluster_arrive();
+  // split: neither CTA exits while the other may still access its shared memory
+  if (nsplit == 2) {
+    if (!cl_started) cluster_wait();
+    if (!cl_done) cluster_arrive();
     cluster_wait();
   }
   __syncthreads();
@@ -560,8 +593,11 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
 
 // ---------------------------------------------------------------- X -> fp16
 // Launched with programmatic stream serialization: X may be written, and X16
-// still read, by the preceding kernel, so it waits for that kernel first.
-__global__ void __launch_bounds__(256) x_to_f16_kernel(const float* __restrict__ X, uint16_t* __restrict__ X16,
+// still read, by the preceding kernel, so it waits for that kernel first. One
+// CTA per SM, at most 64 registers a thread (so that a GEMM CTA of up to 128
+// registers a thread fits beside it); each thread converts four groups of 8
+// per pass, all loads issued before the stores.
+__global__ void __launch_bounds__(256, 4) x_to_f16_kernel(const float* __restrict__ X, uint16_t* __restrict__ X16,
                                                        size_t count) {
   grid_dependency_wait();
   grid_launch_dependents();
@@ -570,11 +606,25 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const float* __restrict__
   uint4* Y4 = reinterpret_cast<uint4*>(X16);
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (size_t i = tid; i < n8; i += stride) {
-    const float4 a = X4[2 * i], b = X4[2 * i + 1];
-    const __half2 h0 = __floats2half2_rn(a.x, a.y), h1 = __floats2half2_rn(a.z, a.w);
-    const __half2 h2 = __floats2half2_rn(b.x, b.y), h3 = __floats2half2_rn(b.z, b.w);
-    Y4[i] = make_uint4(h2_as_u32(h0), h2_as_u32(h1), h2_as_u32(h2), h2_as_u32(h3));
+  for (size_t i0 = tid; i0 < n8; i0 += 4 * stride) {
+    float4 a[4], b[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const size_t i = i0 + u * stride;
+      if (i < n8) {
+        a[u] = X4[2 * i];
+        b[u] = X4[2 * i + 1];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const size_t i = i0 + u * stride;
+      if (i < n8) {
+        const __half2 h0 = __floats2half2_rn(a[u].x, a[u].y), h1 = __floats2half2_rn(a[u].z, a[u].w);
+        const __half2 h2 = __floats2half2_rn(b[u].x, b[u].y), h3 = __floats2half2_rn(b[u].z, b[u].w);
+        Y4[i] = make_uint4(h2_as_u32(h0), h2_as_u32(h1), h2_as_u32(h2), h2_as_u32(h3));
+      }
+    }
   }
   for (size_t i = n8 * 8 + tid; i < count; i += stride) X16[i] = __half_as_ushort(__float2half_rn(X[i]));
 }
@@ -622,7 +672,7 @@ cudaLaunchAttribute pdl_attr() {
 
 template <int QT, int EPI, int BN, bool TIO>
 int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y, const float* R,
-               unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit) {
+               unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, int w_early) {
   using C = Cfg<QT, EPI, BN, TIO>;
   auto fn = encode_fn(msg, msg_len);
   if (!fn) return -1;
@@ -683,7 +733,7 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
     cfg.numAttrs = 2;
   }
   cfg.attrs = attr;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mW, mWu, mX, mR, mY, n, k, T, Y, R, status);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mW, mWu, mX, mR, mY, n, k, T, Y, R, status, w_early);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     snprintf(msg, msg_len, "gemm_tc launch: %s", cudaGetErrorString(e));
@@ -703,31 +753,31 @@ int num_sms() {
 
 template <int QT, int EPI, int BN>
 int launch_io(bool tio, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y,
-              const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit) {
-  return tio ? launch_cfg<QT, EPI, BN, true>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, nsplit)
-             : launch_cfg<QT, EPI, BN, false>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, nsplit);
+              const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, int w_early) {
+  return tio ? launch_cfg<QT, EPI, BN, true>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, nsplit, w_early)
+             : launch_cfg<QT, EPI, BN, false>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, nsplit, w_early);
 }
 
 template <int QT>
 int launch_q(const GemmPlan& pl, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y,
-             const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len) {
+             const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int w) {
   // TMA for the residual and the output when a row of them is a multiple of 16 bytes
   const bool tio = (n % 4) == 0;
-  if (Wu) return launch_io<QT, kEpiSwiGLU, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1);
+  if (Wu) return launch_io<QT, kEpiSwiGLU, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1, w);
   if (pl.bn == 256) {
     if (R)
-      return launch_io<QT, kEpiResidual, 256>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, pl.nsplit);
-    return launch_io<QT, kEpiPlain, 256>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, pl.nsplit);
+      return launch_io<QT, kEpiResidual, 256>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, pl.nsplit, w);
+    return launch_io<QT, kEpiPlain, 256>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, pl.nsplit, w);
   }
-  if (R) return launch_io<QT, kEpiResidual, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1);
-  return launch_io<QT, kEpiPlain, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1);
+  if (R) return launch_io<QT, kEpiResidual, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1, w);
+  return launch_io<QT, kEpiPlain, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1, w);
 }
 
 }  // namespace
 
 cudaError_t launch_x_to_f16(const float* X, uint16_t* X16, size_t count, cudaStream_t s) {
   size_t blocks = (count / 8 + 255) / 256;
-  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks > (size_t)num_sms()) blocks = (size_t)num_sms();
   if (blocks == 0) blocks = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
@@ -758,9 +808,11 @@ GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu) {
 }
 
 int launch_gemm_tc(const GemmPlan& pl, int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16,
-                   int T, float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len) {
-  return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len)
-                        : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len);
+                   int T, float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len,
+                   bool after_conversion) {
+  const int w = after_conversion ? 1 : 0;
+  return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, w)
+                        : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, w);
 }
 
 }  // namespace apr
