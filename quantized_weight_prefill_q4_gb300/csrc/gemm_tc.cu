@@ -776,6 +776,17 @@ int launch_q(const GemmPlan& pl, const void* W, const void* Wu, int n, int k, co
 }  // namespace
 
 cudaError_t launch_x_to_f16(const float* X, uint16_t* X16, size_t count, cudaStream_t s) {
+  // the GEMM's shared-memory carveout, so that its CTAs may start on an SM
+  // that still runs a conversion CTA
+  static int carveout_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !carveout_set[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(x_to_f16_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                               (int)cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    carveout_set[dev] = 1;
+  }
   size_t blocks = (count / 8 + 255) / 256;
   if (blocks > (size_t)num_sms()) blocks = (size_t)num_sms();
   if (blocks == 0) blocks = 1;
