@@ -18,10 +18,17 @@ enum Epilogue { kEpiPlain = 0, kEpiResidual = 1, kEpiSwiGLU = 2 };
 // Standalone dequant (dequant.cu).
 cudaError_t launch_dequant(int qtype, const void* W, int n, int k, float* out, cudaStream_t s);
 
-// Small-T GEMV, exact fp32. Wu != nullptr: gate/up SwiGLU. Takes the bulk-copy
-// kernel (gemv_bulk.cu) when it applies, else the staged kernel (gemv.cu).
+// Small-T GEMV, exact fp32. Wu != nullptr: gate/up SwiGLU. Takes the
+// whole-row streaming kernel (gemv_rows.cu) when a stage holds a row, else the
+// chunked bulk-copy kernel (gemv_bulk.cu), else the staged kernel (gemv.cu).
+// The first two read W before the preceding kernel on the stream has
+// finished (it must not be that kernel's output).
 cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
                         float* Y, const float* R, unsigned* status, cudaStream_t s);
+size_t gemv_rows_smem(int qtype, int k, int T);
+bool gemv_rows_fits(int qtype, int n, int k, int T, bool swiglu);
+cudaError_t launch_gemv_rows(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
+                             float* Y, const float* R, unsigned* status, cudaStream_t s);
 size_t gemv_bulk_smem(int qtype, int k, int T, bool swiglu);
 bool gemv_bulk_fits(int qtype, int k, int T, bool swiglu);
 cudaError_t launch_gemv_bulk(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,

@@ -104,8 +104,14 @@ struct Cfg {
   static constexpr int R_BYTES = R_EARLY ? NPIECE * PIECE_BYTES : 0;
   // operand stages (A in TMEM and B in shared memory advance together)
   static constexpr int S = NM == 2 ? 4 : (BN == 256 ? 4 : (QT == kQ4_0 ? 6 : 5));
-  // (with 256-token tiles the raw ring also receives the partner's half of a split)
-  static constexpr int S_RAW = NM == 1 ? (QT == kQ4_0 ? (BN == 256 ? 4 : 3) : 2) : (QT == kQ4_0 ? 4 : 3);
+  // (with 256-token tiles the raw ring also receives the partner's half of a
+  // split). With gate/up the chunks of the two weights alternate through the
+  // ring, chunk j in slot j % S_RAW; S_RAW must be even so that a slot always
+  // holds the same weight: each slot's phases are then awaited in order by one
+  // warpgroup. With an odd ring a warpgroup would wait on phase p + 2 of a slot
+  // whose phase p + 1 belongs to the other warpgroup, and a parity wait cannot
+  // tell phase p + 2 from phase p.
+  static constexpr int S_RAW = NM == 1 ? (QT == kQ4_0 ? (BN == 256 ? 4 : 3) : 2) : 4;
   static constexpr int NTHREADS = 128 + 128 * NWG;
   static constexpr int ACC_COLS = NM * BN;
   static constexpr int A_COL0 = ACC_COLS;                       // first A column
@@ -123,6 +129,7 @@ struct Cfg {
   // (free once every MMA has completed)
   static constexpr int OFF_STAGE = R_EARLY ? OFF_R : OFF_B;
   static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(NM == 1 || S_RAW % 2 == 0, "gate/up: each raw slot keeps one weight");
   static_assert(USED_COLS <= 512, "TMEM budget");
   static_assert(NPIECE % NWG == 0, "epilogue pieces per warpgroup");
   static_assert(R_EARLY || NPIECE * PIECE_BYTES <= S * B_BYTES, "output pieces fit the operand ring");

@@ -228,6 +228,7 @@ cudaError_t launch_q(const void* W, const void* Wu, int n, int k, const float* X
 cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
                         float* Y, const float* R, unsigned* status, cudaStream_t s) {
   const bool swi = Wu != nullptr;
+  if (gemv_rows_fits(qtype, n, k, T, swi)) return launch_gemv_rows(qtype, W, Wu, n, k, X, T, Y, R, status, s);
   if (gemv_bulk_fits(qtype, k, T, swi)) return launch_gemv_bulk(qtype, W, Wu, n, k, X, T, Y, R, status, s);
   if (qtype == kQ4_0)
     return swi ? launch_q<kQ4_0, true>(W, Wu, n, k, X, T, Y, R, s)

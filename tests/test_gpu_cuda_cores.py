@@ -90,6 +90,46 @@ def test_gemv_swiglu_exact(q, qtype, T):
     assert_exact_leg(Y.cpu().numpy(), oracle.gate_up_swiglu_f64(qtype, c["W"], c["Wu"], n, k, c["X"]))
 
 
+# Rows longer than a 16 KB stage of the row-streaming kernel (Q8_0 k = 16384,
+# and gate/up pairs of Q4_0 rows at k = 16384) go to the chunked bulk kernel.
+@pytest.mark.parametrize("qtype", QTYPES)
+@pytest.mark.parametrize("T", [1, 5])
+@pytest.mark.parametrize("swiglu", [False, True])
+def test_gemv_long_rows(q, qtype, T, swiglu):
+    n, k = 40, 16384
+    c = synth.make_case(qtype, n, k, T, residual=not swiglu, gate_up=swiglu, seed=90 + T)
+    buf, Y = guarded(T, n)
+    if swiglu:
+        q.apr_qgemm_ex(qtype, dev(c["W"]), n, k, dev(c["X"]), T, Y, Wu=dev(c["Wu"]), path=q.APR_PATH_GEMV)
+        ref = oracle.gate_up_swiglu_f64(qtype, c["W"], c["Wu"], n, k, c["X"])
+    else:
+        q.apr_qgemv(qtype, dev(c["W"]), n, k, dev(c["X"]), T, Y, dev(c["R"]))
+        ref = oracle.qgemm_f64(qtype, c["W"], n, k, c["X"], c["R"])
+    q.apr_stream_status()
+    check_guards(buf, T, n)
+    assert_exact_leg(Y.cpu().numpy(), ref)
+
+
+# Back-to-back GEMVs on one stream, each reading the previous output as X and
+# as its residual: the next call starts before the previous one finishes and
+# streams its weight early, but must read X and R only after it.
+@pytest.mark.parametrize("qtype", QTYPES)
+@pytest.mark.parametrize("T", [1, 2])
+def test_gemv_chain_reads_previous_output(q, qtype, T):
+    n = k = 1024
+    steps = 6
+    cases = [synth.make_case(qtype, n, k, T, seed=300 + i) for i in range(steps)]
+    Ws = [dev(c["W"]) for c in cases]
+    Ys = [dev(cases[0]["X"])] + [torch.empty((T, n), device="cuda") for _ in range(steps)]
+    for i in range(steps):
+        q.apr_qgemv(qtype, Ws[i], n, k, Ys[i], T, Ys[i + 1], Ys[i])
+    q.apr_stream_status()
+    ys = [y.cpu().numpy() for y in Ys]
+    for i in range(steps):
+        ref = oracle.qgemm_f64(qtype, cases[i]["W"], n, k, ys[i], ys[i])
+        assert_exact_leg(ys[i + 1], ref)
+
+
 def test_gemv_residual_alias_accumulates(q):
     n, k, T = 256, 512, 4
     c = synth.make_case(synth.Q8_0, n, k, T, residual=True, seed=5)

@@ -203,6 +203,28 @@ def test_tile_plans(q, qtype, n, k, T, res):
     assert rel <= 2e-5, rel
 
 
+# Gate/up at a size with several waves of CTAs: the output must repeat bit for
+# bit. (An odd raw ring once let a warpgroup read the other weight's chunk
+# now and then: a race that only repetition shows.)
+@pytest.mark.parametrize("qtype", QTYPES)
+def test_gate_up_repeats_bitwise(q, qtype):
+    n, k, T = 12288, 4096, 512
+    c = synth.make_case(qtype, n, k, T, gate_up=True, seed=61)
+    W, Wu, X = dev(c["W"]), dev(c["Wu"]), dev(c["X"])
+    Y0 = torch.empty((T, n), device="cuda")
+    q.apr_qgemm_ex(qtype, W, n, k, X, T, Y0, Wu=Wu, path=q.APR_PATH_GEMM)
+    q.apr_stream_status()
+    Y = torch.empty((T, n), device="cuda")
+    for _ in range(24):
+        q.apr_qgemm_ex(qtype, W, n, k, X, T, Y, Wu=Wu, path=q.APR_PATH_GEMM)
+        q.apr_stream_status()
+        assert torch.equal(Y, Y0)
+    # and one row block against the oracle
+    rows = slice(0, 256)
+    ref = oracle.gate_up_swiglu_f64(qtype, c["W"][rows], c["Wu"][rows], 256, k, c["X"])
+    assert_f16_leg(Y0[:, rows].cpu().numpy(), ref)
+
+
 def test_split_k_is_deterministic(q):
     # the split partials are added in split order whichever CTA finishes first
     n, k, T = 512, 4096, 512
