@@ -51,6 +51,15 @@
  * try_cuda_prefill_q_std returns at once for an empty batch). On any error Y
  * is unspecified and must be discarded.
  *
+ * Stream order: every call is ordered after the work before it on its stream,
+ * with one relaxation. The library's kernels start while the preceding kernel
+ * of the library on the same stream finishes, and read the weights (W, Wg,
+ * Wu) before it has finished; X, residual and Y are touched only after it has.
+ * So a call's weights must not be an output (Y, or the X16 of
+ * apr_convert_f32_to_f16) of the immediately preceding call of this library
+ * on that stream. Kernels of other code on the stream are always complete
+ * first.
+ *
  * Limits: n, T <= 2^24, k <= 2^20, n*k/32 blocks <= 2^31.
  */
 #ifndef APR_QGEMM_H
@@ -125,11 +134,11 @@ int apr_qgemm_gate_up_swiglu(int qtype, const void* Wg, const void* Wu, int n, i
                              const float* X, int T, float* Y, apr_stream_t stream);
 
 /*
- * Small-T GEMV, 1 <= T <= APR_GEMV_MAX_T (T == 0 is a no-op): one warp per W
- * row, coalesced 16-byte block loads, T fp32 accumulators, exact fp32
- * arithmetic, optional residual (gemv_q4_0_pf / gemv_q8_0_pf of
- * oxibonsai-kernels, used for the last-token lm_head in
- * try_cuda_prefill_q_std). T > APR_GEMV_MAX_T gives APR_E_INVAL.
+ * Small-T GEMV, 1 <= T <= APR_GEMV_MAX_T (T == 0 is a no-op): weight rows
+ * streamed by bulk copies, T fp32 accumulators, exact fp32 arithmetic,
+ * optional residual (gemv_q4_0_pf / gemv_q8_0_pf of oxibonsai-kernels, used
+ * for the last-token lm_head in try_cuda_prefill_q_std). T > APR_GEMV_MAX_T
+ * gives APR_E_INVAL. The weights are read early (see stream order above).
  */
 int apr_qgemv(int qtype, const void* W, int n, int k, const float* X, int T,
               float* Y, const float* residual, apr_stream_t stream);
