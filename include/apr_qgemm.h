@@ -147,6 +147,14 @@ int apr_qgemv(int qtype, const void* W, int n, int k, const float* X, int T,
  * Full form. Wu != NULL selects the gate/up SwiGLU product (W is the gate;
  * residual must be NULL). leg and path as above; APR_PATH_GEMV needs
  * T <= APR_GEMV_MAX_T. The exact leg on the GEMM path runs fp32 FFMA.
+ * ldy: strided output. Row t of Y starts at Y + t * ldy (and row t of
+ * residual at residual + t * ldy), so Y can be a slice of a wider buffer, such
+ * as the rows of a KV cache (aprender-serve writes attn_v straight into the
+ * cache this way: forward_qwen35_cuda_prefill.rs). 0 means n (dense); else
+ * n <= ldy <= 2^28 (APR_E_INVAL otherwise). Only the n floats of each row are
+ * written. With residual == Y it accumulates into the strided rows. The
+ * tensor-core path stores by TMA when n and ldy are multiples of 4, else
+ * with plain stores. X stays dense [T][k].
  */
 typedef struct apr_qgemm_args {
   int qtype;
@@ -161,6 +169,7 @@ typedef struct apr_qgemm_args {
   const float* residual;
   float* Y;
   apr_stream_t stream;
+  int ldy;  /* floats from one row of Y (and of residual) to the next; 0: n */
 } apr_qgemm_args;
 int apr_qgemm_ex(const apr_qgemm_args* args);
 

@@ -72,6 +72,7 @@ class _Args(ctypes.Structure):
         ("residual", ctypes.c_void_p),
         ("Y", ctypes.c_void_p),
         ("stream", ctypes.c_void_p),
+        ("ldy", ctypes.c_int),
     ]
 
 
@@ -136,6 +137,24 @@ def _ptr(x, name: str, *, dtype=None, min_bytes: int = 0):
     return x.data_ptr()
 
 
+def _rows_ptr(x, name: str, rows: int, cols: int, ld: int):
+    """Device pointer of f32 rows `ld` apart (a 2-D view with strides (ld, 1),
+    or any contiguous tensor), checked to hold (rows - 1) * ld + cols floats."""
+    if x is None or isinstance(x, int):
+        return x
+    import torch
+
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.float32:
+        raise ValueError(f"{name}: expected a float32 CUDA tensor")
+    if not x.is_contiguous() and not (x.dim() == 2 and x.stride() == (ld, 1)):
+        raise ValueError(f"{name}: expected a contiguous tensor or a 2-D view with strides ({ld}, 1)")
+    need = ((rows - 1) * ld + cols) * 4 if rows > 0 else 0
+    have = x.untyped_storage().nbytes() - x.storage_offset() * 4
+    if have < need:
+        raise ValueError(f"{name}: holds {have} bytes from its start, the call addresses {need}")
+    return x.data_ptr()
+
+
 def _stream(stream):
     if stream is None:
         import torch
@@ -194,12 +213,20 @@ def apr_qgemv(qtype, W, n, k, X, T, Y, residual=None, stream=None) -> int:
 
 
 def apr_qgemm_ex(qtype, W, n, k, X, T, Y, *, residual=None, Wu=None, leg=APR_LEG_F16, path=APR_PATH_AUTO,
-                 stream=None) -> int:
+                 stream=None, ldy=0) -> int:
+    """Full form; ldy > 0 writes row t of Y at Y + t * ldy (and reads the
+    residual's rows the same way): Y and residual may then be 2-D views with
+    strides (ldy, 1)."""
     u8, f32 = _dtypes()
     wb, xb, yb = _sizes(qtype, n, k, T)
+    if ldy:
+        rp = _rows_ptr(residual, "residual", T, n, ldy)
+        yp = _rows_ptr(Y, "Y", T, n, ldy)
+    else:
+        rp = _ptr(residual, "residual", dtype=f32, min_bytes=yb)
+        yp = _ptr(Y, "Y", dtype=f32, min_bytes=yb)
     a = _Args(qtype, leg, path, _ptr(W, "W", dtype=u8, min_bytes=wb), _ptr(Wu, "Wu", dtype=u8, min_bytes=wb),
-              n, k, T, _ptr(X, "X", dtype=f32, min_bytes=xb), _ptr(residual, "residual", dtype=f32, min_bytes=yb),
-              _ptr(Y, "Y", dtype=f32, min_bytes=yb), _stream(stream))
+              n, k, T, _ptr(X, "X", dtype=f32, min_bytes=xb), rp, yp, _stream(stream), ldy)
     return _check(_lib.apr_qgemm_ex(ctypes.byref(a)))
 
 

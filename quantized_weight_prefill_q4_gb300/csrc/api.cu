@@ -103,7 +103,10 @@ struct Problem {
   const float* R;
   float* Y;
   cudaStream_t s;
+  int ldy = 0;  // floats between rows of Y and R; 0: n
 };
+
+int ldy_of(const Problem& p) { return p.ldy > 0 ? p.ldy : p.n; }
 
 // Host-side checks; returns APR_OK, an error, or 1 for "nothing to do".
 int check(const Problem& p, size_t x_elem_bytes = 4) {
@@ -115,6 +118,8 @@ int check(const Problem& p, size_t x_elem_bytes = 4) {
     return fail(APR_E_INVAL, "bad sizes n=%d k=%d T=%d (need n >= 0, T >= 0, k > 0, k %% 32 == 0)", p.n, p.k, p.T);
   if (p.n > (1 << 24) || p.T > (1 << 24) || p.k > (1 << 20) || (int64_t)p.n * (p.k / 32) > (int64_t)1 << 31)
     return fail(APR_E_INVAL, "sizes beyond the supported limits");
+  if (p.ldy < 0 || (p.ldy > 0 && p.ldy < p.n) || p.ldy > (1 << 28))
+    return fail(APR_E_INVAL, "bad ldy %d (need 0, or n <= ldy <= 2^28; n = %d)", p.ldy, p.n);
   if (p.path == APR_PATH_GEMV && p.T > APR_GEMV_MAX_T)
     return fail(APR_E_INVAL, "the GEMV path takes T <= %d (got %d)", APR_GEMV_MAX_T, p.T);
   if (p.n == 0 || p.T == 0) return 1;
@@ -124,7 +129,7 @@ int check(const Problem& p, size_t x_elem_bytes = 4) {
     if (q && !aligned16(q)) return fail(APR_E_ALIGN, "pointer %p is not 16-byte aligned", q);
   const size_t wbytes = (size_t)p.n * (size_t)(p.k / 32) * (size_t)block_bytes(p.qtype);
   const size_t xbytes = (size_t)p.T * (size_t)p.k * x_elem_bytes;
-  const size_t ybytes = (size_t)p.T * (size_t)p.n * 4;
+  const size_t ybytes = ((size_t)(p.T - 1) * (size_t)ldy_of(p) + (size_t)p.n) * 4;  // first to last element
   if (overlap(p.Y, ybytes, p.X, xbytes)) return fail(APR_E_ALIAS, "Y overlaps X");
   if (overlap(p.Y, ybytes, p.W, wbytes)) return fail(APR_E_ALIAS, "Y overlaps W");
   if (p.Wu && overlap(p.Y, ybytes, p.Wu, wbytes)) return fail(APR_E_ALIAS, "Y overlaps Wu");
@@ -152,7 +157,7 @@ int run(const Problem& p) {
   int path = p.path;
   if (path == APR_PATH_AUTO) path = p.T <= APR_GEMV_MAX_T ? APR_PATH_GEMV : APR_PATH_GEMM;
   if (path == APR_PATH_GEMV)
-    return launched(launch_gemv(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, p.R, st->status, p.s), "gemv");
+    return launched(launch_gemv(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, ldy_of(p), p.R, st->status, p.s), "gemv");
   // GEMM: the tensor-core kernels need every raw 256-column chunk of a weight
   // row to start on a 16-byte boundary (k % 256 == 0); other k run the FFMA
   // kernel (exact fp32, whatever the leg). The exact leg runs the FFMA kernel
@@ -160,7 +165,7 @@ int run(const Problem& p) {
   // 1e-5 relative error at k = 4096, because the tensor core's fp32
   // accumulator is not rounded like FFMA.
   if (p.k % 256 != 0 || p.leg == APR_LEG_EXACT_F32)
-    return launched(launch_gemm_simt(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, p.R, p.s), "gemm_simt");
+    return launched(launch_gemm_simt(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, ldy_of(p), p.R, p.s), "gemm_simt");
 
   // pooled scratch: the fp16 copy of X
   const GemmPlan plan = plan_gemm_tc(p.n, p.k, p.T, p.Wu != nullptr);
@@ -172,7 +177,7 @@ int run(const Problem& p) {
   rc = launched(launch_x_to_f16(p.X, static_cast<uint16_t*>(x16), count, p.s), "x_to_f16");
   if (rc == APR_OK) {
     char msg[256] = "";
-    if (launch_gemm_tc(plan, p.qtype, p.W, p.Wu, p.n, p.k, static_cast<const uint16_t*>(x16), p.T, p.Y, p.R,
+    if (launch_gemm_tc(plan, p.qtype, p.W, p.Wu, p.n, p.k, static_cast<const uint16_t*>(x16), p.T, p.Y, ldy_of(p), p.R,
                        st->status, p.s, msg, sizeof msg, true) != 0)
       rc = fail(APR_E_LAUNCH, "%s", msg);
   }
@@ -236,7 +241,7 @@ int apr_qgemm_ex(const apr_qgemm_args* a) {
   t_msg[0] = 0;
   if (!a) return fail(APR_E_INVAL, "null argument struct");
   return run(Problem{a->qtype, a->leg, a->path, a->W, a->Wu, a->n, a->k, a->T, a->X, a->residual, a->Y,
-                     (cudaStream_t)a->stream});
+                     (cudaStream_t)a->stream, a->ldy});
 }
 
 int apr_convert_f32_to_f16(const float* X, long long count, void* X16, apr_stream_t stream) {
@@ -268,7 +273,7 @@ int apr_qgemm_f16_in(int qtype, const void* W, const void* Wu, int n, int k, con
   if (rc != APR_OK) return rc;
   const GemmPlan plan = plan_gemm_tc(n, k, T, Wu != nullptr);
   char msg[256] = "";
-  if (launch_gemm_tc(plan, qtype, W, Wu, n, k, static_cast<const uint16_t*>(X16), T, Y, residual, st->status,
+  if (launch_gemm_tc(plan, qtype, W, Wu, n, k, static_cast<const uint16_t*>(X16), T, Y, n, residual, st->status,
                      (cudaStream_t)stream, msg, sizeof msg, false) != 0)
     return fail(APR_E_LAUNCH, "%s", msg);
   return APR_OK;

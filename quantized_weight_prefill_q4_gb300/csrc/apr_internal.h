@@ -1,4 +1,5 @@
 // Launchers shared between the C ABI (api.cu) and the kernel files. Host only.
+// Y (and the residual R) hold T rows of n floats, ldy floats apart (ldy >= n).
 #pragma once
 
 #include <cstddef>
@@ -24,7 +25,7 @@ cudaError_t launch_dequant(int qtype, const void* W, int n, int k, float* out, c
 // The first two read W before the preceding kernel on the stream has
 // finished (it must not be that kernel's output).
 cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
-                        float* Y, const float* R, unsigned* status, cudaStream_t s);
+                        float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s);
 size_t gemv_rows_smem(int qtype, int k, int T);
 bool gemv_rows_fits(int qtype, int n, int k, int T, bool swiglu);
 cudaError_t launch_gemv_rows(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
@@ -32,11 +33,11 @@ cudaError_t launch_gemv_rows(int qtype, const void* W, const void* Wu, int n, in
 size_t gemv_bulk_smem(int qtype, int k, int T, bool swiglu);
 bool gemv_bulk_fits(int qtype, int k, int T, bool swiglu);
 cudaError_t launch_gemv_bulk(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
-                             float* Y, const float* R, unsigned* status, cudaStream_t s);
+                             float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s);
 
 // Exact-fp32 FFMA GEMM for any k % 32 == 0 (gemm_simt.cu).
 cudaError_t launch_gemm_simt(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
-                             float* Y, const float* R, cudaStream_t s);
+                             float* Y, int ldy, const float* R, cudaStream_t s);
 
 // fp16 copy of X, round to nearest even (gemm_tc.cu). Launched with
 // programmatic stream serialization; it waits for the preceding kernel before
@@ -58,8 +59,8 @@ GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu);
 // R or Y, except that with `after_conversion` (launched right after
 // launch_x_to_f16 on the same stream) it reads W and R without waiting.
 int launch_gemm_tc(const GemmPlan& plan, int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16,
-                   int T, float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len,
-                   bool after_conversion);
+                   int T, float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg,
+                   size_t msg_len, bool after_conversion);
 
 // Shared with the allocation-free entry point (api.cu): sets this thread's error
 // message and returns `code`; checks the arguments of a plain / residual GEMM

@@ -44,7 +44,7 @@ template <int QT, int EPI>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const uint8_t* __restrict__ W,
                                                         const uint8_t* __restrict__ Wu, int n, int k,
                                                         const float* __restrict__ X, int T,
-                                                        float* Y,
+                                                        float* Y, int ldy,
                                                         const float* R) {
   constexpr int BB = QT == kQ4_0 ? 18 : 34;
   constexpr int NM = EPI == kEpiSwiGLU ? 2 : 1;
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const uint8_t* __restric
     for (int i = 0; i < 4; ++i) {
       const int row = m0 + ty * 4 + i;
       if (row >= n) continue;
-      const size_t o = (size_t)tok * n + row;
+      const size_t o = (size_t)tok * ldy + row;
       float v;
       if (EPI == kEpiSwiGLU) {
         const float g = acc[0][i][j], u = acc[NM - 1][i][j];
@@ -140,26 +140,26 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const uint8_t* __restric
 }
 
 template <int QT>
-cudaError_t launch_q(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y,
+cudaError_t launch_q(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
                      const float* R, cudaStream_t s) {
   const dim3 grid((n + BM - 1) / BM, (T + BN - 1) / BN);
   const uint8_t* w = (const uint8_t*)W;
   const uint8_t* wu = (const uint8_t*)Wu;
   if (Wu)
-    gemm_simt_kernel<QT, kEpiSwiGLU><<<grid, 256, 0, s>>>(w, wu, n, k, X, T, Y, R);
+    gemm_simt_kernel<QT, kEpiSwiGLU><<<grid, 256, 0, s>>>(w, wu, n, k, X, T, Y, ldy, R);
   else if (R)
-    gemm_simt_kernel<QT, kEpiResidual><<<grid, 256, 0, s>>>(w, wu, n, k, X, T, Y, R);
+    gemm_simt_kernel<QT, kEpiResidual><<<grid, 256, 0, s>>>(w, wu, n, k, X, T, Y, ldy, R);
   else
-    gemm_simt_kernel<QT, kEpiPlain><<<grid, 256, 0, s>>>(w, wu, n, k, X, T, Y, R);
+    gemm_simt_kernel<QT, kEpiPlain><<<grid, 256, 0, s>>>(w, wu, n, k, X, T, Y, ldy, R);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_simt(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
-                             float* Y, const float* R, cudaStream_t s) {
-  return qtype == kQ4_0 ? launch_q<kQ4_0>(W, Wu, n, k, X, T, Y, R, s)
-                        : launch_q<kQ8_0>(W, Wu, n, k, X, T, Y, R, s);
+                             float* Y, int ldy, const float* R, cudaStream_t s) {
+  return qtype == kQ4_0 ? launch_q<kQ4_0>(W, Wu, n, k, X, T, Y, ldy, R, s)
+                        : launch_q<kQ8_0>(W, Wu, n, k, X, T, Y, ldy, R, s);
 }
 
 }  // namespace apr

@@ -232,7 +232,7 @@ template <int QT, int EPI, int BN, bool TIO>
 __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWu,
                    const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmR,
-                   const __grid_constant__ CUtensorMap tmY, int n, int k, int T, float* Y, const float* R,
+                   const __grid_constant__ CUtensorMap tmY, int n, int k, int T, float* Y, int ldy, const float* R,
                    unsigned* status, int w_early) {
   using C = Cfg<QT, EPI, BN, TIO>;
   extern __shared__ uint8_t smem_raw[];
@@ -571,12 +571,12 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int t = t0 + p * PIECE + j0 + j;
-            rv[j] = (EPI == kEpiResidual && t < T) ? R[(size_t)t * n + row] : 0.f;
+            rv[j] = (EPI == kEpiResidual && t < T) ? R[(size_t)t * ldy + row] : 0.f;
           }
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int t = t0 + p * PIECE + j0 + j;
-            if (t < T) Y[(size_t)t * n + row] = __uint_as_float(v[j0 + j]) + rv[j];
+            if (t < T) Y[(size_t)t * ldy + row] = __uint_as_float(v[j0 + j]) + rv[j];
           }
         }
       }
@@ -678,8 +678,8 @@ cudaLaunchAttribute pdl_attr() {
 }
 
 template <int QT, int EPI, int BN, bool TIO>
-int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y, const float* R,
-               unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, int w_early) {
+int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y, int ldy,
+               const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, int w_early) {
   using C = Cfg<QT, EPI, BN, TIO>;
   auto fn = encode_fn(msg, msg_len);
   if (!fn) return -1;
@@ -700,15 +700,16 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
   if (!make_map_2d(fn, &mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X16, (uint64_t)k, (uint64_t)T, (uint64_t)k * 2, BK, BN,
                    CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
     return -1;
-  // residual and output pieces: [T][n] fp32, box 128 rows x 64 tokens
+  // residual and output pieces: [T] rows of n fp32, ldy apart, box 128 rows x
+  // 64 tokens
   CUtensorMap mR = mX, mY = mX;
   if (C::R_EARLY || C::R_LATE) {
-    if (!make_map_2d(fn, &mR, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, R, (uint64_t)n, (uint64_t)T, (uint64_t)n * 4, BM,
+    if (!make_map_2d(fn, &mR, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, R, (uint64_t)n, (uint64_t)T, (uint64_t)ldy * 4, BM,
                      PIECE, CU_TENSOR_MAP_SWIZZLE_NONE, msg, msg_len))
       return -1;
   }
   if (C::TIO) {
-    if (!make_map_2d(fn, &mY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, Y, (uint64_t)n, (uint64_t)T, (uint64_t)n * 4, BM,
+    if (!make_map_2d(fn, &mY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, Y, (uint64_t)n, (uint64_t)T, (uint64_t)ldy * 4, BM,
                      PIECE, CU_TENSOR_MAP_SWIZZLE_NONE, msg, msg_len))
       return -1;
   }
@@ -740,7 +741,7 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
     cfg.numAttrs = 2;
   }
   cfg.attrs = attr;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mW, mWu, mX, mR, mY, n, k, T, Y, R, status, w_early);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mW, mWu, mX, mR, mY, n, k, T, Y, ldy, R, status, w_early);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     snprintf(msg, msg_len, "gemm_tc launch: %s", cudaGetErrorString(e));
@@ -759,25 +760,29 @@ int num_sms() {
 }
 
 template <int QT, int EPI, int BN>
-int launch_io(bool tio, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y,
+int launch_io(bool tio, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y, int ldy,
               const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, int w_early) {
-  return tio ? launch_cfg<QT, EPI, BN, true>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, nsplit, w_early)
-             : launch_cfg<QT, EPI, BN, false>(W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, nsplit, w_early);
+  return tio ? launch_cfg<QT, EPI, BN, true>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, nsplit, w_early)
+             : launch_cfg<QT, EPI, BN, false>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, nsplit,
+                                              w_early);
 }
 
 template <int QT>
 int launch_q(const GemmPlan& pl, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y,
-             const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int w) {
-  // TMA for the residual and the output when a row of them is a multiple of 16 bytes
-  const bool tio = (n % 4) == 0;
-  if (Wu) return launch_io<QT, kEpiSwiGLU, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1, w);
+             int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int w) {
+  // TMA for the residual and the output when a row of them is a multiple of
+  // 16 bytes long and starts on one (n and ldy multiples of 4)
+  const bool tio = (n % 4) == 0 && (ldy % 4) == 0;
+  if (Wu) return launch_io<QT, kEpiSwiGLU, 128>(tio, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w);
   if (pl.bn == 256) {
     if (R)
-      return launch_io<QT, kEpiResidual, 256>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, pl.nsplit, w);
-    return launch_io<QT, kEpiPlain, 256>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, pl.nsplit, w);
+      return launch_io<QT, kEpiResidual, 256>(tio, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len,
+                                              pl.nsplit, w);
+    return launch_io<QT, kEpiPlain, 256>(tio, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, pl.nsplit,
+                                         w);
   }
-  if (R) return launch_io<QT, kEpiResidual, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1, w);
-  return launch_io<QT, kEpiPlain, 128>(tio, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, 1, w);
+  if (R) return launch_io<QT, kEpiResidual, 128>(tio, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w);
+  return launch_io<QT, kEpiPlain, 128>(tio, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w);
 }
 
 }  // namespace
@@ -826,11 +831,11 @@ GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu) {
 }
 
 int launch_gemm_tc(const GemmPlan& pl, int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16,
-                   int T, float* Y, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len,
-                   bool after_conversion) {
+                   int T, float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg,
+                   size_t msg_len, bool after_conversion) {
   const int w = after_conversion ? 1 : 0;
-  return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, w)
-                        : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, R, status, s, msg, msg_len, w);
+  return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w)
+                        : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w);
 }
 
 }  // namespace apr

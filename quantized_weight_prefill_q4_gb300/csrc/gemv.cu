@@ -40,7 +40,7 @@ template <int QT, int TMAX, int RW, bool VEC, bool SWI>
 __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const uint8_t* __restrict__ W,
                                                            const uint8_t* __restrict__ Wu, int n, int k,
                                                            const float* __restrict__ X, int T,
-                                                           float* Y,
+                                                           float* Y, int ldy,
                                                            const float* R) {
   constexpr int BB = QT == kQ4_0 ? 18 : 34;
   constexpr int SEG = 32 * BB;
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const uint8_t* __rest
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) {
         if (lane == t && t < T && row < n) {
-          const size_t o = (size_t)t * n + row;
+          const size_t o = (size_t)t * ldy + row;
           float v;
           if (SWI)
             v = silu_mul(acc[0][r][t], acc[NM - 1][r][t]);
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const uint8_t* __rest
 }
 
 template <int QT, int TMAX, bool SWI>
-cudaError_t launch_t(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y,
+cudaError_t launch_t(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
                      const float* R, cudaStream_t s) {
   constexpr int RW = (TMAX >= 8 || SWI) ? 1 : 2;
   const int ngroups = (n + RW - 1) / RW;
@@ -206,35 +206,37 @@ cudaError_t launch_t(const void* W, const void* Wu, int n, int k, const float* X
   const bool vec = (k % 256) == 0;
   if (vec)
     gemv_kernel<QT, TMAX, RW, true, SWI><<<blocks, kWarps * 32, 0, s>>>(
-        (const uint8_t*)W, (const uint8_t*)Wu, n, k, X, T, Y, R);
+        (const uint8_t*)W, (const uint8_t*)Wu, n, k, X, T, Y, ldy, R);
   else
     gemv_kernel<QT, TMAX, RW, false, SWI><<<blocks, kWarps * 32, 0, s>>>(
-        (const uint8_t*)W, (const uint8_t*)Wu, n, k, X, T, Y, R);
+        (const uint8_t*)W, (const uint8_t*)Wu, n, k, X, T, Y, ldy, R);
   return cudaGetLastError();
 }
 
 template <int QT, bool SWI>
-cudaError_t launch_q(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y,
+cudaError_t launch_q(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
                      const float* R, cudaStream_t s) {
-  if (T <= 1) return launch_t<QT, 1, SWI>(W, Wu, n, k, X, T, Y, R, s);
-  if (T <= 2) return launch_t<QT, 2, SWI>(W, Wu, n, k, X, T, Y, R, s);
-  if (T <= 4) return launch_t<QT, 4, SWI>(W, Wu, n, k, X, T, Y, R, s);
-  if (T <= 8) return launch_t<QT, 8, SWI>(W, Wu, n, k, X, T, Y, R, s);
-  return launch_t<QT, 16, SWI>(W, Wu, n, k, X, T, Y, R, s);
+  if (T <= 1) return launch_t<QT, 1, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 2) return launch_t<QT, 2, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 4) return launch_t<QT, 4, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 8) return launch_t<QT, 8, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  return launch_t<QT, 16, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
 }
 
 }  // namespace
 
 cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
-                        float* Y, const float* R, unsigned* status, cudaStream_t s) {
+                        float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s) {
   const bool swi = Wu != nullptr;
+  // one token: one row of Y, so the row kernel needs no stride
+  // one token only: its single output row starts at Y whatever ldy is
   if (gemv_rows_fits(qtype, n, k, T, swi)) return launch_gemv_rows(qtype, W, Wu, n, k, X, T, Y, R, status, s);
-  if (gemv_bulk_fits(qtype, k, T, swi)) return launch_gemv_bulk(qtype, W, Wu, n, k, X, T, Y, R, status, s);
+  if (gemv_bulk_fits(qtype, k, T, swi)) return launch_gemv_bulk(qtype, W, Wu, n, k, X, T, Y, ldy, R, status, s);
   if (qtype == kQ4_0)
-    return swi ? launch_q<kQ4_0, true>(W, Wu, n, k, X, T, Y, R, s)
-               : launch_q<kQ4_0, false>(W, Wu, n, k, X, T, Y, R, s);
-  return swi ? launch_q<kQ8_0, true>(W, Wu, n, k, X, T, Y, R, s)
-             : launch_q<kQ8_0, false>(W, Wu, n, k, X, T, Y, R, s);
+    return swi ? launch_q<kQ4_0, true>(W, Wu, n, k, X, T, Y, ldy, R, s)
+               : launch_q<kQ4_0, false>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  return swi ? launch_q<kQ8_0, true>(W, Wu, n, k, X, T, Y, ldy, R, s)
+             : launch_q<kQ8_0, false>(W, Wu, n, k, X, T, Y, ldy, R, s);
 }
 
 }  // namespace apr

@@ -41,7 +41,7 @@ struct BCfg {
 template <int QT, int TMAX, bool SWI>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemv_bulk_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ Wu, int n, int k,
-                     const float* __restrict__ X, int T, float* Y, const float* R, unsigned* status) {
+                     const float* __restrict__ X, int T, float* Y, int ldy, const float* R, unsigned* status) {
   using C = BCfg<QT, SWI>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, by pointer arithmetic on the shared array so that
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) {
         if (lane == t && t < T && row < n) {
-          const size_t o = (size_t)t * n + row;
+          const size_t o = (size_t)t * ldy + row;
           float y;
           if (SWI) {
             const float gt = acc[0][r][t];
@@ -177,8 +177,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 int g_num_sms[64] = {0};
 
 template <int QT, int TMAX, bool SWI>
-cudaError_t launch_t(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, const float* R,
-                     unsigned* status, cudaStream_t s) {
+cudaError_t launch_t(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
+                     const float* R, unsigned* status, cudaStream_t s) {
   using C = BCfg<QT, SWI>;
   const size_t smem = gemv_bulk_smem(QT, k, T, SWI);
   auto kern = gemv_bulk_kernel<QT, TMAX, SWI>;
@@ -198,17 +198,17 @@ cudaError_t launch_t(const void* W, const void* Wu, int n, int k, const float* X
   const int ngroups = (n + G - 1) / G;
   const int grid = ngroups < sms ? ngroups : sms;
   (void)C::RING;
-  kern<<<grid, NTHREADS, smem, s>>>((const uint8_t*)W, (const uint8_t*)Wu, n, k, X, T, Y, R, status);
+  kern<<<grid, NTHREADS, smem, s>>>((const uint8_t*)W, (const uint8_t*)Wu, n, k, X, T, Y, ldy, R, status);
   return cudaGetLastError();
 }
 
 template <int QT, bool SWI>
-cudaError_t launch_q(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, const float* R,
-                     unsigned* status, cudaStream_t s) {
-  if (T <= 1) return launch_t<QT, 1, SWI>(W, Wu, n, k, X, T, Y, R, status, s);
-  if (T <= 2) return launch_t<QT, 2, SWI>(W, Wu, n, k, X, T, Y, R, status, s);
-  if (T <= 4) return launch_t<QT, 4, SWI>(W, Wu, n, k, X, T, Y, R, status, s);
-  return launch_t<QT, 8, SWI>(W, Wu, n, k, X, T, Y, R, status, s);
+cudaError_t launch_q(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
+                     const float* R, unsigned* status, cudaStream_t s) {
+  if (T <= 1) return launch_t<QT, 1, SWI>(W, Wu, n, k, X, T, Y, ldy, R, status, s);
+  if (T <= 2) return launch_t<QT, 2, SWI>(W, Wu, n, k, X, T, Y, ldy, R, status, s);
+  if (T <= 4) return launch_t<QT, 4, SWI>(W, Wu, n, k, X, T, Y, ldy, R, status, s);
+  return launch_t<QT, 8, SWI>(W, Wu, n, k, X, T, Y, ldy, R, status, s);
 }
 
 }  // namespace
@@ -229,13 +229,13 @@ bool gemv_bulk_fits(int qtype, int k, int T, bool swiglu) {
 }
 
 cudaError_t launch_gemv_bulk(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y,
-                             const float* R, unsigned* status, cudaStream_t s) {
+                             int ldy, const float* R, unsigned* status, cudaStream_t s) {
   const bool swi = Wu != nullptr;
   if (qtype == kQ4_0)
-    return swi ? launch_q<kQ4_0, true>(W, Wu, n, k, X, T, Y, R, status, s)
-               : launch_q<kQ4_0, false>(W, Wu, n, k, X, T, Y, R, status, s);
-  return swi ? launch_q<kQ8_0, true>(W, Wu, n, k, X, T, Y, R, status, s)
-             : launch_q<kQ8_0, false>(W, Wu, n, k, X, T, Y, R, status, s);
+    return swi ? launch_q<kQ4_0, true>(W, Wu, n, k, X, T, Y, ldy, R, status, s)
+               : launch_q<kQ4_0, false>(W, Wu, n, k, X, T, Y, ldy, R, status, s);
+  return swi ? launch_q<kQ8_0, true>(W, Wu, n, k, X, T, Y, ldy, R, status, s)
+             : launch_q<kQ8_0, false>(W, Wu, n, k, X, T, Y, ldy, R, status, s);
 }
 
 }  // namespace apr

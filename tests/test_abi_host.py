@@ -96,6 +96,13 @@ def test_swiglu_and_gemv_specific_errors(q):
     args = q.capi._Args(2, 0, 9, A, None, 64, 64, 8, 2 * A, None, 3 * A, None)
     assert lib.apr_qgemm_ex(ctypes.byref(args)) == -1       # unknown path
     assert lib.apr_qgemm_ex(None) == -1
+    for ldy in (-1, 63, (1 << 28) + 1):                      # strided output: 0 or n <= ldy <= 2^28
+        args = q.capi._Args(2, 0, 0, A, None, 64, 64, 8, 2 * A, None, 3 * A, None, ldy)
+        assert lib.apr_qgemm_ex(ctypes.byref(args)) == -1, ldy
+        assert "ldy" in q.apr_last_error()
+    # a strided Y reaching over X is an alias even when its first rows are not
+    args = q.capi._Args(2, 0, 0, A, None, 64, 64, 8, 3 * A, None, A + 4096, None, 1 << 20)
+    assert lib.apr_qgemm_ex(ctypes.byref(args)) == -4
     assert lib.apr_dequant(3, A, 4, 64, 2 * A, None) == -2
     assert lib.apr_dequant(2, A, 4, 48, 2 * A, None) == -1
     assert lib.apr_dequant(2, A, 4, 64, A + 16, None) == -4
