@@ -28,10 +28,20 @@
  * given stream (NULL = the legacy default stream): a return of APR_OK means the
  * work was enqueued. X, residual, Y and out are float32, row major, densely
  * packed (row stride = number of columns). Device pointers must be 16-byte
- * aligned. The GEMM path takes a stream-ordered scratch of T*k*2 bytes (the
- * fp16 copy of X) from a memory pool the library owns per device; it is
- * released on the same stream when the call's work is done. Weights are
- * never dequantized to memory: blocks are decoded in registers.
+ * aligned. Weights are never dequantized to memory: blocks are decoded in
+ * registers.
+ *
+ * Scratch. The library owns device scratch per (device, stream): the fp16
+ * copy of X for the GEMM path (T*k*2 bytes), and, for the tensor-core GEMV
+ * (T = 3 or 4, or T = 2 on weights of 2^25 or more elements), ticket counters
+ * and partial sums (64 KiB plus 2 KiB per 128 weight rows and per SM, at
+ * most). Calls on one stream share their stream's buffers, which are ordered
+ * by the stream. A buffer grows on demand with cudaMalloc (also during a
+ * stream capture: the calling thread's capture mode is relaxed for that
+ * call) and is never freed while the process runs; a grown buffer replaces
+ * the old one for later calls and the old one is kept. A graph captured from
+ * a stream uses that stream's buffers: replay it ordered with the other
+ * library calls on that stream, not concurrently with them.
  *
  * Errors. Arguments are checked on the host before anything is enqueued:
  *   APR_E_INVAL   null pointer with nonzero sizes, n < 0, T < 0, k <= 0,
@@ -43,7 +53,7 @@
  *                 exactly the same buffer (Y == residual is allowed: it gives
  *                 Y += X.W^T, the accumulate form of the pages' batch kernels)
  *   APR_E_DEVICE  no CUDA device, or the device is not compute capability 10.3
- *   APR_E_NOMEM   the scratch pool could not provide the fp16 copy of X
+ *   APR_E_NOMEM   the scratch could not be allocated
  *   APR_E_LAUNCH  a CUDA launch or API call failed (see apr_last_error)
  *   APR_E_TIMEOUT reported by apr_stream_status: a bounded device-side wait
  *                 expired and the kernel gave up (results are garbage)
@@ -197,8 +207,8 @@ int apr_qgemm_f16_in(int qtype, const void* W, const void* Wu, int n, int k, con
  * have no counterpart: it exists for callers that cannot allocate device
  * memory once they run (a serving process that has reserved nearly all of HBM
  * for weights and its KV-cache arena and treats a later allocation as a fault,
- * or a runtime that allows allocation only at start-up). apr_qgemm takes its
- * T*k*2-byte fp16 copy of X from a pool it grows on demand; this variant uses
+ * or a runtime that allows allocation only at start-up). apr_qgemm keeps its
+ * T*k*2-byte fp16 copy of X in scratch it grows on demand; this variant uses
  * a fixed scratch array of APR_NOALLOC_MAX_TK fp16 values (16 MiB) that exists
  * on every GPU that loads the library, from module load until the process
  * exits.

@@ -11,6 +11,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -39,9 +40,9 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceState {
   std::once_flag once;
+  int dev = -1;
   int checked = 0;          // APR_OK or APR_E_DEVICE
   unsigned* status = nullptr;
-  cudaMemPool_t pool = nullptr;
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -54,6 +55,7 @@ int device_state(DeviceState** out) {
   }
   DeviceState& st = g_dev[dev];
   std::call_once(st.once, [&st, dev] {
+    st.dev = dev;
     cudaDeviceProp prop;
     if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess || prop.major != 10 || prop.minor != 3) {
       cudaGetLastError();
@@ -67,24 +69,83 @@ int device_state(DeviceState** out) {
       return;
     }
     st.status = static_cast<unsigned*>(p);
-    cudaMemPoolProps props;
-    memset(&props, 0, sizeof props);
-    props.allocType = cudaMemAllocationTypePinned;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = dev;
-    if (cudaMemPoolCreate(&st.pool, &props) != cudaSuccess) {
-      cudaGetLastError();
-      st.checked = APR_E_DEVICE;
-      return;
-    }
-    uint64_t keep = UINT64_MAX;  // keep freed scratch in the pool
-    cudaMemPoolSetAttribute(st.pool, cudaMemPoolAttrReleaseThreshold, &keep);
     st.checked = APR_OK;
   });
   if (st.checked != APR_OK)
     return fail(APR_E_DEVICE, "device %d is not a compute capability 10.3 GPU (GB300) or failed to initialise", dev);
   *out = &st;
   return APR_OK;
+}
+
+// Scratch owned by the library, one buffer per (device, stream, use): the
+// fp16 copy of X for the GEMM, the ticket counters and partial sums of the
+// GEMV. Calls on one stream are ordered by it, and every kernel touches
+// scratch only after waiting for the kernel before it (griddepcontrol.wait),
+// so one buffer serves every call on the stream and successive kernels still
+// overlap (no allocation between them). A buffer only grows: a larger one
+// replaces it and the old one is kept, so graphs captured with it stay valid.
+// Growth uses cudaMalloc with the calling thread's capture mode relaxed for
+// the call, so that it also works while the stream is being captured. A graph
+// captured from a stream uses that stream's buffers: replay it ordered with
+// the stream's other library calls, not concurrently with them.
+// The GEMV's buffer starts zeroed (cudaMemsetAsync on the stream) and every
+// completed call leaves its counters zero; after a device-side timeout the
+// buffers are cleared again before their next use.
+enum ScratchUse { kScratchX16 = 0, kScratchGemv = 1 };
+struct StreamScratch {
+  int dev;
+  cudaStream_t s;
+  int use;
+  void* p;
+  size_t bytes;
+  bool dirty;
+};
+std::mutex g_scratch_mu;
+std::vector<StreamScratch> g_scratch;   // current buffers
+std::vector<void*> g_scratch_retired;   // replaced buffers, never freed
+
+int stream_scratch(int dev, cudaStream_t s, int use, size_t bytes, void** out) {
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  const bool zeroed = use == kScratchGemv;
+  StreamScratch* cur = nullptr;
+  for (auto& e : g_scratch)
+    if (e.dev == dev && e.s == s && e.use == use) cur = &e;
+  if (!cur || cur->bytes < bytes) {
+    size_t want = (size_t)1 << 20;
+    while (want < bytes) want <<= 1;
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    void* p = nullptr;
+    const cudaError_t e = cudaMalloc(&p, want);
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(APR_E_NOMEM, "scratch of %zu bytes: %s", want, cudaGetErrorString(e));
+    }
+    if (cur) {
+      g_scratch_retired.push_back(cur->p);
+      cur->p = p;
+      cur->bytes = want;
+    } else {
+      g_scratch.push_back(StreamScratch{dev, s, use, p, want, false});
+      cur = &g_scratch.back();
+    }
+    cur->dirty = zeroed;
+  }
+  if (cur->dirty) {
+    const cudaError_t e = cudaMemsetAsync(cur->p, 0, cur->bytes, s);
+    if (e != cudaSuccess) return fail(APR_E_LAUNCH, "scratch clear: %s", cudaGetErrorString(e));
+    cur->dirty = false;
+  }
+  *out = cur->p;
+  return APR_OK;
+}
+
+// After a device-side timeout some counters may be left nonzero.
+void scratch_mark_dirty(int dev) {
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  for (auto& e : g_scratch)
+    if (e.dev == dev && e.use == kScratchGemv) e.dirty = true;
 }
 
 bool overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -156,8 +217,21 @@ int run(const Problem& p) {
 
   int path = p.path;
   if (path == APR_PATH_AUTO) path = p.T <= APR_GEMV_MAX_T ? APR_PATH_GEMV : APR_PATH_GEMM;
-  if (path == APR_PATH_GEMV)
-    return launched(launch_gemv(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, ldy_of(p), p.R, st->status, p.s), "gemv");
+  if (path == APR_PATH_GEMV) {
+    if (!gemv_tc_takes(p.n, p.k, p.T, p.Wu != nullptr))
+      return launched(launch_gemv(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, ldy_of(p), p.R, st->status, p.s),
+                      "gemv");
+    // tensor-core GEMV: the stream's scratch holds its split X, scales and
+    // partial sums
+    void* scratch = nullptr;
+    rc = stream_scratch(st->dev, p.s, kScratchGemv, gemv_tc_scratch_bytes(p.n, p.k, p.T), &scratch);
+    if (rc != APR_OK) return rc;
+    char msg[256] = "";
+    if (launch_gemv_tc(p.qtype, p.W, p.n, p.k, p.X, p.T, p.Y, ldy_of(p), p.R, scratch, st->status, p.s, msg,
+                       sizeof msg) != 0)
+      return fail(APR_E_LAUNCH, "%s", msg);
+    return APR_OK;
+  }
   // GEMM: the tensor-core kernels need every raw 256-column chunk of a weight
   // row to start on a 16-byte boundary (k % 256 == 0); other k run the FFMA
   // kernel (exact fp32, whatever the leg). The exact leg runs the FFMA kernel
@@ -167,23 +241,19 @@ int run(const Problem& p) {
   if (p.k % 256 != 0 || p.leg == APR_LEG_EXACT_F32)
     return launched(launch_gemm_simt(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, ldy_of(p), p.R, p.s), "gemm_simt");
 
-  // pooled scratch: the fp16 copy of X
+  // the stream's scratch holds the fp16 copy of X
   const GemmPlan plan = plan_gemm_tc(p.n, p.k, p.T, p.Wu != nullptr);
   const size_t count = (size_t)p.T * (size_t)p.k;
   void* x16 = nullptr;
-  cudaError_t e = cudaMallocFromPoolAsync(&x16, count * 2, st->pool, p.s);
-  if (e != cudaSuccess)
-    return fail(APR_E_NOMEM, "scratch for fp16 X (%zu bytes): %s", count * 2, cudaGetErrorString(e));
+  rc = stream_scratch(st->dev, p.s, kScratchX16, count * 2, &x16);
+  if (rc != APR_OK) return rc;
   rc = launched(launch_x_to_f16(p.X, static_cast<uint16_t*>(x16), count, p.s), "x_to_f16");
-  if (rc == APR_OK) {
-    char msg[256] = "";
-    if (launch_gemm_tc(plan, p.qtype, p.W, p.Wu, p.n, p.k, static_cast<const uint16_t*>(x16), p.T, p.Y, ldy_of(p), p.R,
-                       st->status, p.s, msg, sizeof msg, true) != 0)
-      rc = fail(APR_E_LAUNCH, "%s", msg);
-  }
-  e = cudaFreeAsync(x16, p.s);
-  if (rc == APR_OK && e != cudaSuccess) rc = fail(APR_E_LAUNCH, "cudaFreeAsync: %s", cudaGetErrorString(e));
-  return rc;
+  if (rc != APR_OK) return rc;
+  char msg[256] = "";
+  if (launch_gemm_tc(plan, p.qtype, p.W, p.Wu, p.n, p.k, static_cast<const uint16_t*>(x16), p.T, p.Y, ldy_of(p), p.R,
+                     st->status, p.s, msg, sizeof msg, true) != 0)
+    return fail(APR_E_LAUNCH, "%s", msg);
+  return APR_OK;
 }
 
 }  // namespace
@@ -308,6 +378,7 @@ int apr_stream_status(apr_stream_t stream) {
   if (v) {
     const unsigned zero = 0;
     cudaMemcpy(st->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    scratch_mark_dirty(st->dev);
     return fail(APR_E_TIMEOUT, "a kernel's bounded wait gave up (status 0x%x)", v);
   }
   return APR_OK;

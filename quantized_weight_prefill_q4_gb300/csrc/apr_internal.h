@@ -35,13 +35,27 @@ bool gemv_bulk_fits(int qtype, int k, int T, bool swiglu);
 cudaError_t launch_gemv_bulk(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
                              float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s);
 
+// Tensor-core GEMV (gemv_tc.cu): fp16 integer codes x three fp16 pieces of X
+// (every product exact), block scales applied in fp32. gemv_tc_takes() is the
+// dispatch rule: T <= kGemvTcMaxT, k % 256 == 0, n <= 2097152, no gate/up,
+// and T large enough that it beats the CUDA-core kernels. Needs
+// gemv_tc_scratch_bytes() of device scratch whose first bytes (the ticket
+// counters) are zero; each completed launch leaves them zero, so successive
+// launches on one stream may share it. The kernel reads W before the
+// preceding kernel on the stream has finished (it must not be that kernel's
+// output). Returns 0, or -1 with a message in msg.
+constexpr int kGemvTcMaxT = 4;
+bool gemv_tc_takes(int n, int k, int T, bool swiglu);
+size_t gemv_tc_scratch_bytes(int n, int k, int T);
+int launch_gemv_tc(int qtype, const void* W, int n, int k, const float* X, int T, float* Y, int ldy, const float* R,
+                   void* scratch, unsigned* status, cudaStream_t s, char* msg, size_t msg_len);
+
 // Exact-fp32 FFMA GEMM for any k % 32 == 0 (gemm_simt.cu).
 cudaError_t launch_gemm_simt(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
                              float* Y, int ldy, const float* R, cudaStream_t s);
 
-// fp16 copy of X, round to nearest even (gemm_tc.cu). Launched with
-// programmatic stream serialization; it waits for the preceding kernel before
-// it reads X or writes X16.
+// fp16 copy of X, round to nearest even (gemm_tc.cu). Launched in plain
+// stream order, so it starts after the preceding kernel has completed.
 cudaError_t launch_x_to_f16(const float* X, uint16_t* X16, size_t count, cudaStream_t s);
 
 // Shape of a tensor-core GEMM launch: token-tile width (128 or 256) and split

@@ -63,11 +63,10 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
-#include <atomic>
-#include <mutex>
 
 #include "apr_internal.h"
 #include "dev_common.cuh"
+#include "host_common.h"
 
 namespace apr {
 namespace {
@@ -599,8 +598,8 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
 }
 
 // ---------------------------------------------------------------- X -> fp16
-// Launched with programmatic stream serialization: X may be written, and X16
-// still read, by the preceding kernel, so it waits for that kernel first. One
+// Launched in plain stream order (its griddepcontrol.wait then returns at
+// once); it lets the GEMM after it launch as soon as it starts. One
 // CTA per SM, at most 64 registers a thread (so that a GEMM CTA of up to 128
 // registers a thread fits beside it); each thread converts four groups of 8
 // per pass, all loads issued before the stores.
@@ -637,46 +636,6 @@ __global__ void __launch_bounds__(256, 4) x_to_f16_kernel(const float* __restric
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn(char* msg, size_t msg_len) {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  if (!fn) snprintf(msg, msg_len, "cuTensorMapEncodeTiled is not available from the driver");
-  return fn;
-}
-
-bool make_map_2d(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* map, CUtensorMapDataType dt,
-                 const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes, uint32_t box_inner,
-                 uint32_t box_outer, CUtensorMapSwizzle swz, char* msg, size_t msg_len) {
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    snprintf(msg, msg_len, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-    return false;
-  }
-  return true;
-}
-
-// Launch attribute that lets the kernel start before the preceding kernel of
-// the stream has finished (it waits with griddepcontrol.wait where it must).
-cudaLaunchAttribute pdl_attr() {
-  cudaLaunchAttribute a;
-  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  a.val.programmaticStreamSerializationAllowed = 1;
-  return a;
-}
-
 template <int QT, int EPI, int BN, bool TIO>
 int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y, int ldy,
                const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, int w_early) {
@@ -750,15 +709,6 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
   return 0;
 }
 
-int num_sms() {
-  static int sms[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return 148;
-  if (!sms[dev]) cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
-  return sms[dev] > 0 ? sms[dev] : 148;
-}
-
 template <int QT, int EPI, int BN>
 int launch_io(bool tio, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y, int ldy,
               const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, int w_early) {
@@ -802,16 +752,12 @@ cudaError_t launch_x_to_f16(const float* X, uint16_t* X16, size_t count, cudaStr
   size_t blocks = (count / 8 + 255) / 256;
   if (blocks > (size_t)num_sms()) blocks = (size_t)num_sms();
   if (blocks == 0) blocks = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)blocks);
-  cfg.blockDim = dim3(256);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1] = {pdl_attr()};
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, x_to_f16_kernel, X, X16, count);
-  if (e == cudaSuccess) e = cudaGetLastError();
-  return e;
+  // plain stream order: launched programmatically after a GEMM, its CTAs
+  // would sit beside that GEMM's for the GEMM's whole run (the GEMM lets the
+  // next kernel launch at its start), which measured about 2 us slower per
+  // call on GB300
+  x_to_f16_kernel<<<(unsigned)blocks, 256, 0, s>>>(X, X16, count);
+  return cudaGetLastError();
 }
 
 GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu) {
