@@ -325,13 +325,13 @@ def run_ours(args):
         step_call(sets[i % SETS])()
 
     if args.only == "gemv":
-        n, k = 4096, 4096
-        c = synth.make_case(QTYPE, n, k, 1, seed=0)
+        n, k, tg = args.gemv_rows, 4096, args.gemv_tokens
+        c = synth.make_case(QTYPE, n, k, tg, seed=0)
         Ws = [torch.from_numpy(c["W"]).to(dev) for _ in range(16)]
         X1 = torch.from_numpy(c["X"]).to(dev)
-        Y1 = torch.empty((1, n), device=dev)
+        Y1 = torch.empty((tg, n), device=dev)
         for i in range(args.warmup + args.steps):
-            q.apr_qgemv(QTYPE, Ws[i % 16], n, k, X1, 1, Y1, stream=stream)
+            q.apr_qgemv(QTYPE, Ws[i % 16], n, k, X1, tg, Y1, stream=stream)
         q.apr_stream_status(stream)
         print(json.dumps({"only": "gemv", "launches": args.warmup + args.steps}), flush=True)
         return
@@ -484,6 +484,8 @@ def main(argv=None):
     ap.add_argument("--only", choices=["all", "step", "kernel", "gemv"], default="all",
                     help="step: only the timed apr_qgemm steps; kernel: only the GEMM kernel on fp16 activations; "
                          "gemv: only the T = 1 GEMV (small, bounded runs for profilers)")
+    ap.add_argument("--gemv-tokens", type=int, default=1, help="tokens of the --only gemv run (1..16)")
+    ap.add_argument("--gemv-rows", type=int, default=4096, help="weight rows of the --only gemv run (k = 4096)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -74,37 +74,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// As mbar_try_wait, but the hardware may suspend the thread for up to hint_ns
-// nanoseconds while the phase is incomplete, so that a waiting warp takes no
-// issue slots from the warps that work (it resumes when the phase completes).
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
-// mbar_wait with suspension (each try may sleep up to 20 us; same bounds).
-__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                unsigned* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
-    if ((it & 15u) == 0) {
-      if (*abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
-        *abort = 1;
-        atomicOr(status, kStatusTimeout);
-        return false;
-      }
-    }
-  }
-}
-
 // ---------------------------------------------------------------- cluster
 // A CTA pair of a cluster (1, 1, 2): distributed shared memory, remote
 // mbarrier arrivals and the cluster barrier.
