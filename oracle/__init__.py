@@ -19,4 +19,6 @@ from .qref import (  # noqa: F401
     gate_up_swiglu,
     qgemm_f16_inputs_f64,
     gate_up_swiglu_f16_inputs_f64,
+    rmsnorm_f64,
+    ffn_sublayer_f64,
 )

@@ -28,6 +28,15 @@ What is computed, and where the pages define it:
   step 2; the unfused twin gate GEMM, up GEMM, ``fused_swiglu_into`` in
   ``prefill_ffn_rows``).
 
+* The FFN sublayer of a prefill layer over a chunk of rows (oxibonsai-kernels
+  0.1.4, doc of ``encode_q_std_ffn_phase``: batched RMSNorm of the input rows,
+  the fused gate/up SwiGLU GEMM, the down GEMM whose result is added back into
+  the input rows; aprender-serve src/gguf/cuda/forward_qwen35_cuda_prefill.rs,
+  ``prefill_ffn_rows``: the same steps with ``batched_rmsnorm_into`` over
+  ``hidden_dim`` with ``d.eps``). The pages call the norm without printing it;
+  this module reads it as the usual RMSNorm of a row,
+  ``y = x / sqrt(mean(x^2) + eps) * w``, ``w`` the norm weight per column.
+
 Every product is accumulated in float64 and the result is rounded to float32
 once. The f16-input mode rounds ``X`` and the dequantized ``W`` to fp16 first
 (the fp16 leg of ``qwen35_project_rows_f16``: fp16 in, fp32 accumulate), then
@@ -165,3 +174,25 @@ def gate_up_swiglu_f16_inputs_f64(qtype: int, Wg, Wu, n: int, k: int, X) -> np.n
     g = qgemm_f16_inputs_f64(qtype, Wg, n, k, X)
     u = qgemm_f16_inputs_f64(qtype, Wu, n, k, X)
     return silu_f64(g) * u
+
+
+# --------------------------------------------------------------------------
+# FFN sublayer (the norm, then SwiGLU, then down + residual)
+# --------------------------------------------------------------------------
+def rmsnorm_f64(X, weight, eps: float) -> np.ndarray:
+    """Row-wise ``x / sqrt(mean(x^2) + eps) * w`` in float64, shape of ``X``."""
+    X64 = _as_f64(X)
+    w64 = _as_f64(weight).reshape(1, -1)
+    ms = np.mean(X64 * X64, axis=-1, keepdims=True)
+    return X64 / np.sqrt(ms + float(eps)) * w64
+
+
+def ffn_sublayer_f64(qtype: int, X, weight, eps: float, Wg, Wu, Wd, hidden: int, inter: int) -> np.ndarray:
+    """``X + down(silu(h . Wg^T) * (h . Wu^T))`` with ``h = rmsnorm(X)``:
+    Wg, Wu are ``[inter][hidden]`` blocks, Wd ``[hidden][inter]``; float64."""
+    X64 = _as_f64(X).reshape(-1, hidden)
+    h = rmsnorm_f64(X64, weight, eps)  # kept in float64, as every intermediate
+    g = h @ dequant_f64(qtype, Wg, inter, hidden).T
+    u = h @ dequant_f64(qtype, Wu, inter, hidden).T
+    act = silu_f64(g) * u
+    return X64 + act @ dequant_f64(qtype, Wd, hidden, inter).T

@@ -284,3 +284,89 @@ def test_q4_0_encoder_maps_signed_extreme_to_nibble_zero():
     d_bits, codes = oracle.block_scales_and_codes(synth.Q4_0, W, 1, 32)
     assert oracle.fp16_bits_to_f64(d_bits)[0, 0] == float(np.float16(-0.1))
     assert codes[0, 0, 5] == -8 and codes[0, 0, 9] == 4 and codes[0, 0, 0] == 0
+
+
+# ------------------------------------------------------------------ FFN sublayer
+# The pages run a batched RMSNorm (weight, eps) before the gate/up GEMM and add
+# the down projection back into the rows (oxibonsai-kernels 0.1.4,
+# encode_q_std_ffn_phase); the norm is read as x / sqrt(mean(x^2) + eps) * w.
+def test_rmsnorm_hand_values():
+    # [3, 4]: mean of squares 12.5, so 3 / sqrt(12.5) and 4 / sqrt(12.5), weights 1 and 2
+    y = oracle.rmsnorm_f64(np.array([[3.0, 4.0]]), np.array([1.0, 2.0]), 0.0)
+    np.testing.assert_allclose(y, [[0.8485281374238571, 2.2627416997969525]], rtol=1e-15)
+    # a constant row c with eps: c / sqrt(c^2 + eps); 2 / sqrt(4 + 5) = 2 / 3
+    y = oracle.rmsnorm_f64(np.full((1, 4), 2.0), np.ones(4), 5.0)
+    np.testing.assert_allclose(y, np.full((1, 4), 2.0 / 3.0), rtol=1e-15)
+    # rows are normalised one by one: [1, 1] and [10, 10] both give [1, 1]
+    y = oracle.rmsnorm_f64(np.array([[1.0, 1.0], [-10.0, -10.0]]), np.array([1.0, 0.5]), 0.0)
+    np.testing.assert_array_equal(y, [[1.0, 0.5], [-1.0, -0.5]])
+
+
+def test_rmsnorm_scale_invariance():
+    X = synth.activations(3, 64, 5).astype(np.float64)
+    w = synth.activations(1, 64, 6)[0]
+    # scaling a row by 8 (a power of 4 times 2) leaves x / rms(x) unchanged
+    # exactly: sqrt(64 m) = 8 sqrt(m) in floating point
+    np.testing.assert_array_equal(oracle.rmsnorm_f64(8.0 * X, w, 0.0), oracle.rmsnorm_f64(X, w, 0.0))
+
+
+def test_ffn_sublayer_special_cases():
+    hidden, inter, T = 64, 96, 3
+    X = synth.activations(T, hidden, 1)
+    w = np.ones(hidden, np.float32)
+    Wg = synth.quantize_q8_0(synth.weight_f32(inter, hidden, 2))
+    Wu = synth.quantize_q8_0(synth.weight_f32(inter, hidden, 3))
+    Wd = synth.quantize_q8_0(synth.weight_f32(hidden, inter, 4))
+    # zero norm weight: the normed rows are zero, so is SwiGLU, and X comes back
+    y = oracle.ffn_sublayer_f64(synth.Q8_0, X, np.zeros(hidden), 1e-6, Wg, Wu, Wd, hidden, inter)
+    np.testing.assert_array_equal(y, X.astype(np.float64))
+    # a down weight with every code zero adds nothing
+    Wz = np.zeros((hidden, inter // 32, 34), np.uint8)
+    Wz[..., 1] = 0x3C
+    y = oracle.ffn_sublayer_f64(synth.Q8_0, X, w, 1e-6, Wg, Wu, Wz.reshape(hidden, -1), hidden, inter)
+    np.testing.assert_array_equal(y, X.astype(np.float64))
+
+
+def _block_values(raw, qtype, n, k):
+    """Dequantized weight from the raw bytes, by the block rules (struct parse)."""
+    bb = 18 if qtype == synth.Q4_0 else 34
+    out = np.zeros((n, k))
+    for i in range(n):
+        for b in range(k // 32):
+            blk = bytes(raw[i, b * bb:(b + 1) * bb])
+            d = struct.unpack("<e", blk[:2])[0]
+            for j in range(32):
+                if qtype == synth.Q4_0:
+                    byte = blk[2 + (j % 16)]
+                    q = (byte & 0xF if j < 16 else byte >> 4) - 8
+                else:
+                    q = struct.unpack("<b", blk[2 + j:3 + j])[0]
+                out[i, 32 * b + j] = d * q
+    return out
+
+
+@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
+def test_ffn_sublayer_brute_force(qtype):
+    """Element-by-element loops (struct block parsing, math.sqrt, math.exp)
+    against the oracle's array form."""
+    hidden, inter, T, eps = 32, 64, 2, 1e-5
+    X = synth.activations(T, hidden, 7).astype(np.float64)
+    w = synth.activations(1, hidden, 8)[0].astype(np.float64)
+    raw = {}
+    for name, (rows, cols, seed) in {"g": (inter, hidden, 9), "u": (inter, hidden, 10), "d": (hidden, inter, 11)}.items():
+        raw[name] = synth.quantize(qtype, synth.weight_f32(rows, cols, seed))
+    Wg, Wu, Wd = (_block_values(raw[n_], qtype, *s) for n_, s in
+                  (("g", (inter, hidden)), ("u", (inter, hidden)), ("d", (hidden, inter))))
+    want = np.zeros((T, hidden))
+    for t in range(T):
+        ms = sum(X[t, c] * X[t, c] for c in range(hidden)) / hidden
+        h = [X[t, c] / math.sqrt(ms + eps) * w[c] for c in range(hidden)]
+        act = []
+        for i in range(inter):
+            g = sum(h[c] * Wg[i, c] for c in range(hidden))
+            u = sum(h[c] * Wu[i, c] for c in range(hidden))
+            act.append(g / (1.0 + math.exp(-g)) * u)
+        for o in range(hidden):
+            want[t, o] = X[t, o] + sum(act[i] * Wd[o, i] for i in range(inter))
+    got = oracle.ffn_sublayer_f64(qtype, X, w, eps, raw["g"], raw["u"], raw["d"], hidden, inter)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
