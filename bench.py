@@ -394,6 +394,7 @@ def run_ours(args):
     if rank == 0:
         gemv = gemv_rate(q, synth, dev, stream, peak_gbs)
         gemv_big = gemv_rate(q, synth, dev, stream, peak_gbs, n=12288, k=4096)
+        ffn = ffn_rate(q, synth, dev, stream)
 
     # ---- end to end: host buffers, copies inside the timed region
     e2e_steps = max(20, min(args.steps, 200))
@@ -442,6 +443,7 @@ def run_ours(args):
             "clocks": clk.summary(),
             "gemv": gemv,
             "gemv_12288": gemv_big,
+            "ffn_sublayer": ffn,
         }
         if not args.no_cpu:
             line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -450,6 +452,34 @@ def run_ours(args):
         import torch.distributed as dist
 
         dist.destroy_process_group()
+
+
+def ffn_rate(q, synth, dev, stream, hidden=4096, inter=12288, T=512):
+    """The FFN sublayer of a 9B-class layer (RMSNorm, fused gate/up SwiGLU,
+    down + residual, Q4_0, fp16 leg) on T rows, two rotating weight sets
+    (170 MB, more than L2); TFLOP/s counts the three projections."""
+    import torch
+
+    sets = []
+    for j in range(2):
+        W = [torch.from_numpy(synth.quantize(QTYPE, synth.weight_f32(r, c, 50 + 3 * j + i))).to(dev)
+             for i, (r, c) in enumerate(((inter, hidden), (inter, hidden), (hidden, inter)))]
+        sets.append((W, torch.from_numpy(synth.activations(T, hidden, 60 + j)).to(dev)))
+    w = torch.ones(hidden, device=dev)
+
+    def call(s):
+        W, X = s
+        return lambda: q.apr_ffn_sublayer(QTYPE, W[0], W[1], W[2], hidden, inter, T, w, 1e-6, X)
+
+    for s in sets:
+        call(s)()
+    torch.cuda.synchronize()
+    reps = 200
+    dt = timed_calls([call(s) for s in sets], reps, stream) / reps
+    q.apr_stream_status(stream)
+    flop = 2.0 * T * 3 * hidden * inter
+    return {"workload": f"q4_0_ffn_hidden{hidden}_inter{inter}_t{T}", "TFLOP/s": flop / dt / 1e12, "us": dt * 1e6,
+            "launches_per_call": 4}
 
 
 def gemv_rate(q, synth, dev, stream, peak_gbs, n=4096, k=4096):

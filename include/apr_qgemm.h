@@ -226,6 +226,49 @@ int apr_qgemm_noalloc(int qtype, const void* W, int n, int k, const float* X, in
                       float* Y, const float* residual, apr_stream_t stream);
 
 /*
+ * FFN sublayer of a prefill layer over T rows of the residual stream, in place:
+ *   h = RMSNorm(X) = X / sqrt(mean(X^2, per row) + eps) * norm_weight
+ *   X = X + (silu(h . Wg^T) * (h . Wu^T)) . Wd^T
+ * The pages' batched FFN phase (oxibonsai-kernels 0.1.4
+ * cuda_q_std_prefill.rs encode_q_std_ffn_phase: batched RMSNorm, fused
+ * gate/up SwiGLU GEMM, down GEMM with the residual added; aprender-serve
+ * forward_qwen35_cuda_prefill.rs prefill_ffn_rows). The norm is not printed
+ * there; this is the usual RMSNorm of a row, eps inside the square root.
+ *   qtype      APR_Q4_0 or APR_Q8_0 for all three weights
+ *   leg        APR_LEG_F16 or APR_LEG_EXACT_F32, as for apr_qgemm_ex; the f16
+ *              leg writes the normed rows straight as fp16 (norm and
+ *              conversion in one pass) for the tensor-core GEMMs
+ *   Wg, Wu     [inter][hidden] weights (rows of hidden / 32 blocks)
+ *   Wd         [hidden][inter] weight
+ *   hidden, inter  multiples of 32 (hidden also of 4); the tensor-core path
+ *              needs both multiples of 256, else the FFMA kernels run
+ *   T          rows (0: no-op); processed in chunks of up to
+ *              APR_FFN_CHUNK_ROWS rows, each chunk one norm and three
+ *              projections that follow the T rule of apr_qgemm_ex
+ *   norm_weight  [hidden] fp32; eps >= 0 and finite
+ *   X          [T][hidden] fp32, dense, read and updated in place
+ * Scratch per stream as for apr_qgemm (the normed rows and the activations of
+ * a chunk, at most APR_FFN_CHUNK_ROWS * (4 hidden + 6 inter) bytes). Errors:
+ * as for apr_qgemm_ex, and APR_E_ALIAS if X overlaps a weight or norm_weight.
+ */
+#define APR_FFN_CHUNK_ROWS 2048
+typedef struct apr_ffn_args {
+  int qtype;
+  int leg;
+  const void* Wg;
+  const void* Wu;
+  const void* Wd;
+  int hidden;
+  int inter;
+  int T;
+  const float* norm_weight;
+  float eps;
+  float* X;
+  apr_stream_t stream;
+} apr_ffn_args;
+int apr_ffn_sublayer(const apr_ffn_args* args);
+
+/*
  * Standalone dequant: out[n][k] f32 = f32(d) * f32(q'), bit exact (the product
  * of an fp16 scale and a code of at most 8 bits is exact in fp32). The device
  * dequant of aprender-serve gdn_prefill_ops.rs qwen35_dequant_f32 (Q8_0 and

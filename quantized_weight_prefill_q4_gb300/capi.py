@@ -33,6 +33,7 @@ APR_E_TIMEOUT = -7
 APR_E_NOMEM = -8
 APR_GEMV_MAX_T = 16
 APR_NOALLOC_MAX_TK = 8 * 1024 * 1024
+APR_FFN_CHUNK_ROWS = 2048
 
 BLOCK_BYTES = {APR_Q4_0: 18, APR_Q8_0: 34}
 
@@ -46,6 +47,7 @@ EXPORTS = (
     "apr_convert_f32_to_f16",
     "apr_qgemm_f16_in",
     "apr_qgemm_noalloc",
+    "apr_ffn_sublayer",
     "apr_dequant",
     "apr_stream_status",
     "apr_last_error",
@@ -76,6 +78,23 @@ class _Args(ctypes.Structure):
     ]
 
 
+class _FfnArgs(ctypes.Structure):
+    _fields_ = [
+        ("qtype", ctypes.c_int),
+        ("leg", ctypes.c_int),
+        ("Wg", ctypes.c_void_p),
+        ("Wu", ctypes.c_void_p),
+        ("Wd", ctypes.c_void_p),
+        ("hidden", ctypes.c_int),
+        ("inter", ctypes.c_int),
+        ("T", ctypes.c_int),
+        ("norm_weight", ctypes.c_void_p),
+        ("eps", ctypes.c_float),
+        ("X", ctypes.c_void_p),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -91,6 +110,7 @@ def _load() -> ctypes.CDLL:
         "apr_convert_f32_to_f16": ([vp, ctypes.c_longlong, vp, vp], ci),
         "apr_qgemm_f16_in": ([ci, vp, vp, ci, ci, vp, ci, vp, vp, vp], ci),
         "apr_qgemm_noalloc": ([ci, vp, ci, ci, vp, ci, vp, vp, vp], ci),
+        "apr_ffn_sublayer": ([ctypes.POINTER(_FfnArgs)], ci),
         "apr_dequant": ([ci, vp, ci, ci, vp, vp], ci),
         "apr_stream_status": ([vp], ci),
         "apr_last_error": ([], ctypes.c_char_p),
@@ -258,6 +278,21 @@ def apr_qgemm_noalloc(qtype, W, n, k, X, T, Y, residual=None, stream=None) -> in
                                          _ptr(X, "X", dtype=f32, min_bytes=xb), T,
                                          _ptr(Y, "Y", dtype=f32, min_bytes=yb),
                                          _ptr(residual, "residual", dtype=f32, min_bytes=yb), _stream(stream)))
+
+
+def apr_ffn_sublayer(qtype, Wg, Wu, Wd, hidden, inter, T, norm_weight, eps, X, leg=APR_LEG_F16, stream=None) -> int:
+    """X[T][hidden] += down(silu(h . Wg^T) * (h . Wu^T)), h = RMSNorm(X) with
+    norm_weight and eps; X is updated in place."""
+    u8, f32 = _dtypes()
+    bb = BLOCK_BYTES.get(qtype, 0)
+    h_, i_, t_ = max(hidden, 0), max(inter, 0), max(T, 0)
+    wgu = i_ * (h_ // 32) * bb
+    wd = h_ * (i_ // 32) * bb
+    a = _FfnArgs(qtype, leg, _ptr(Wg, "Wg", dtype=u8, min_bytes=wgu), _ptr(Wu, "Wu", dtype=u8, min_bytes=wgu),
+                 _ptr(Wd, "Wd", dtype=u8, min_bytes=wd), hidden, inter, T,
+                 _ptr(norm_weight, "norm_weight", dtype=f32, min_bytes=h_ * 4), float(eps),
+                 _ptr(X, "X", dtype=f32, min_bytes=t_ * h_ * 4), _stream(stream))
+    return _check(_lib.apr_ffn_sublayer(ctypes.byref(a)))
 
 
 def apr_dequant(qtype, W, n, k, out, stream=None) -> int:

@@ -91,7 +91,7 @@ int device_state(DeviceState** out) {
 // The GEMV's buffer starts zeroed (cudaMemsetAsync on the stream) and every
 // completed call leaves its counters zero; after a device-side timeout the
 // buffers are cleared again before their next use.
-enum ScratchUse { kScratchX16 = 0, kScratchGemv = 1 };
+enum ScratchUse { kScratchX16 = 0, kScratchGemv = 1, kScratchFfn = 2 };
 struct StreamScratch {
   int dev;
   cudaStream_t s;
@@ -256,6 +256,73 @@ int run(const Problem& p) {
   return APR_OK;
 }
 
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// FFN sublayer: per chunk of rows, the norm into scratch, then gate/up SwiGLU
+// into scratch, then down with the chunk's rows of X as residual and output.
+int run_ffn(const apr_ffn_args& a) {
+  if (a.qtype != APR_Q4_0 && a.qtype != APR_Q8_0) return fail(APR_E_QTYPE, "unsupported qtype %d", a.qtype);
+  if (a.leg != APR_LEG_F16 && a.leg != APR_LEG_EXACT_F32) return fail(APR_E_INVAL, "unknown leg %d", a.leg);
+  if (a.hidden <= 0 || a.inter <= 0 || a.hidden % 32 != 0 || a.inter % 32 != 0 || a.T < 0)
+    return fail(APR_E_INVAL, "bad sizes hidden=%d inter=%d T=%d (need multiples of 32, T >= 0)", a.hidden, a.inter,
+                a.T);
+  if (a.hidden > (1 << 20) || a.inter > (1 << 20) || a.T > (1 << 24) ||
+      (int64_t)a.hidden * (a.inter / 32) > (int64_t)1 << 31)
+    return fail(APR_E_INVAL, "sizes beyond the supported limits");
+  if (!(a.eps >= 0.f) || a.eps > 3.402823466e38f) return fail(APR_E_INVAL, "eps must be finite and >= 0");
+  if (a.T == 0) return APR_OK;
+  if (!a.Wg || !a.Wu || !a.Wd || !a.norm_weight || !a.X) return fail(APR_E_INVAL, "null pointer");
+  const void* ptrs[5] = {a.Wg, a.Wu, a.Wd, a.norm_weight, a.X};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return fail(APR_E_ALIGN, "pointer %p is not 16-byte aligned", q);
+  const size_t bb = (size_t)block_bytes(a.qtype);
+  const size_t wgu = (size_t)a.inter * (a.hidden / 32) * bb, wd = (size_t)a.hidden * (a.inter / 32) * bb;
+  const size_t xb = (size_t)a.T * a.hidden * 4;
+  if (overlap(a.X, xb, a.Wg, wgu) || overlap(a.X, xb, a.Wu, wgu) || overlap(a.X, xb, a.Wd, wd) ||
+      overlap(a.X, xb, a.norm_weight, (size_t)a.hidden * 4))
+    return fail(APR_E_ALIAS, "X overlaps a weight or the norm weight");
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != APR_OK) return rc;
+  const cudaStream_t s = (cudaStream_t)a.stream;
+  const int chunk = a.T < APR_FFN_CHUNK_ROWS ? a.T : APR_FFN_CHUNK_ROWS;
+  const size_t h_bytes = align256((size_t)chunk * a.hidden * 4), act_bytes = align256((size_t)chunk * a.inter * 4);
+  void* scratch = nullptr;
+  rc = stream_scratch(st->dev, s, kScratchFfn, h_bytes + act_bytes + (size_t)chunk * a.inter * 2, &scratch);
+  if (rc != APR_OK) return rc;
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  void* h = base;                                          // normed rows (fp16 or fp32)
+  float* act = reinterpret_cast<float*>(base + h_bytes);   // SwiGLU output
+  uint16_t* act16 = reinterpret_cast<uint16_t*>(base + h_bytes + act_bytes);
+  for (int t0 = 0; t0 < a.T; t0 += chunk) {
+    const int rows = a.T - t0 < chunk ? a.T - t0 : chunk;
+    float* Xc = a.X + (size_t)t0 * a.hidden;
+    const bool tc = a.leg == APR_LEG_F16 && rows > APR_GEMV_MAX_T && a.hidden % 256 == 0 && a.inter % 256 == 0;
+    rc = launched(launch_rmsnorm_rows(Xc, a.norm_weight, a.eps, rows, a.hidden, h, tc, s), "rmsnorm");
+    if (rc != APR_OK) return rc;
+    if (tc) {
+      char msg[256] = "";
+      const GemmPlan pg = plan_gemm_tc(a.inter, a.hidden, rows, true);
+      if (launch_gemm_tc(pg, a.qtype, a.Wg, a.Wu, a.inter, a.hidden, static_cast<const uint16_t*>(h), rows, act,
+                         a.inter, nullptr, st->status, s, msg, sizeof msg, true) != 0)
+        return fail(APR_E_LAUNCH, "%s", msg);
+      rc = launched(launch_x_to_f16(act, act16, (size_t)rows * a.inter, s), "x_to_f16");
+      if (rc != APR_OK) return rc;
+      const GemmPlan pd = plan_gemm_tc(a.hidden, a.inter, rows, false);
+      if (launch_gemm_tc(pd, a.qtype, a.Wd, nullptr, a.hidden, a.inter, act16, rows, Xc, a.hidden, Xc, st->status, s,
+                         msg, sizeof msg, true) != 0)
+        return fail(APR_E_LAUNCH, "%s", msg);
+    } else {
+      rc = run(Problem{a.qtype, a.leg, APR_PATH_AUTO, a.Wg, a.Wu, a.inter, a.hidden, rows,
+                       static_cast<const float*>(h), nullptr, act, s});
+      if (rc != APR_OK) return rc;
+      rc = run(Problem{a.qtype, a.leg, APR_PATH_AUTO, a.Wd, nullptr, a.hidden, a.inter, rows, act, Xc, Xc, s});
+      if (rc != APR_OK) return rc;
+    }
+  }
+  return APR_OK;
+}
+
 }  // namespace
 
 namespace apr {
@@ -312,6 +379,12 @@ int apr_qgemm_ex(const apr_qgemm_args* a) {
   if (!a) return fail(APR_E_INVAL, "null argument struct");
   return run(Problem{a->qtype, a->leg, a->path, a->W, a->Wu, a->n, a->k, a->T, a->X, a->residual, a->Y,
                      (cudaStream_t)a->stream, a->ldy});
+}
+
+int apr_ffn_sublayer(const apr_ffn_args* a) {
+  t_msg[0] = 0;
+  if (!a) return fail(APR_E_INVAL, "null argument struct");
+  return run_ffn(*a);
 }
 
 int apr_convert_f32_to_f16(const float* X, long long count, void* X16, apr_stream_t stream) {

@@ -50,6 +50,12 @@ size_t gemv_tc_scratch_bytes(int n, int k, int T);
 int launch_gemv_tc(int qtype, const void* W, int n, int k, const float* X, int T, float* Y, int ldy, const float* R,
                    void* scratch, unsigned* status, cudaStream_t s, char* msg, size_t msg_len);
 
+// Row RMSNorm y = x / sqrt(mean(x^2) + eps) * w over T rows of k floats
+// (k % 4 == 0), into fp16 (f16) or fp32 rows of k (rmsnorm.cu). Plain stream
+// order; it lets the next kernel launch at its start.
+cudaError_t launch_rmsnorm_rows(const float* X, const float* w, float eps, int T, int k, void* out, bool f16,
+                                cudaStream_t s);
+
 // Exact-fp32 FFMA GEMM for any k % 32 == 0 (gemm_simt.cu).
 cudaError_t launch_gemm_simt(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
                              float* Y, int ldy, const float* R, cudaStream_t s);

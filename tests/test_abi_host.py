@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(q):
     names = declared_functions()
-    assert len(names) == 11, names
+    assert len(names) == 12, names
     lib = q.library()
     for name in names:
         assert hasattr(lib, name), name
@@ -42,6 +42,8 @@ def test_header_constants_match_binding(q):
         assert m, name
         assert int(m.group(1)) == getattr(q, name), name
     assert q.library().apr_gemv_max_T() == q.APR_GEMV_MAX_T == 16
+    m = re.search(r"#define APR_FFN_CHUNK_ROWS (\d+)", text)
+    assert m and int(m.group(1)) == q.APR_FFN_CHUNK_ROWS
 
 
 # Raw calls through ctypes with fake (never dereferenced) addresses: every
@@ -127,3 +129,35 @@ def test_binding_rejects_host_tensors(q):
     Y = torch.zeros(8, 64)
     with pytest.raises(ValueError, match="device memory"):
         q.apr_qgemm(q.APR_Q4_0, W, 64, 64, X, 8, Y, stream=0)
+
+
+def test_ffn_sublayer_argument_errors(q):
+    """Every argument fault of apr_ffn_sublayer is caught on the host, before
+    any device work (fake, never dereferenced, aligned addresses)."""
+    lib = q.library()
+    B = 1 << 24
+
+    def args(**kw):
+        a = dict(qtype=2, leg=0, Wg=B, Wu=2 * B, Wd=3 * B, hidden=256, inter=512, T=4, norm_weight=4 * B, eps=1e-5,
+                 X=5 * B, stream=None)
+        a.update(kw)
+        return q.capi._FfnArgs(*[a[f] for f, _ in q.capi._FfnArgs._fields_])
+
+    def rc(**kw):
+        return lib.apr_ffn_sublayer(ctypes.byref(args(**kw)))
+
+    assert lib.apr_ffn_sublayer(None) == -1
+    assert rc(qtype=3) == -2
+    assert rc(leg=7) == -1
+    assert rc(hidden=100) == -1 and "hidden" in q.apr_last_error()
+    assert rc(inter=48) == -1
+    assert rc(T=-1) == -1
+    assert rc(eps=-1.0) == -1 and "eps" in q.apr_last_error()
+    assert rc(eps=float("nan")) == -1
+    assert rc(eps=float("inf")) == -1
+    assert rc(T=0) == 0                      # no-op, nothing checked further
+    assert rc(Wd=None) == -1
+    assert rc(norm_weight=None) == -1
+    assert rc(X=5 * B + 4) == -3             # misaligned
+    assert rc(X=B + 64) == -4                # X over the gate weight
+    assert rc(X=4 * B - 256) == -4           # X over the norm weight
