@@ -395,6 +395,7 @@ def run_ours(args):
         gemv = gemv_rate(q, synth, dev, stream, peak_gbs)
         gemv_big = gemv_rate(q, synth, dev, stream, peak_gbs, n=12288, k=4096)
         ffn = ffn_rate(q, synth, dev, stream)
+        big = gemm_kernel_rate(q, synth, dev, stream, peak_tf, T=2048)
 
     # ---- end to end: host buffers, copies inside the timed region
     e2e_steps = max(20, min(args.steps, 200))
@@ -444,6 +445,7 @@ def run_ours(args):
             "gemv": gemv,
             "gemv_12288": gemv_big,
             "ffn_sublayer": ffn,
+            "gemm_t2048": big,
         }
         if not args.no_cpu:
             line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -452,6 +454,32 @@ def run_ours(args):
         import torch.distributed as dist
 
         dist.destroy_process_group()
+
+
+def gemm_kernel_rate(q, synth, dev, stream, peak_tf, n=4096, k=4096, T=2048):
+    """The GEMM kernel alone (fp16 X in, + residual) at a larger chunk of
+    tokens, four rotating input sets (more than L2)."""
+    import torch
+
+    sets = []
+    for j in range(4):
+        c = synth.make_case(QTYPE, n, k, T, residual=True, seed=70 + j)
+        d = {key: torch.from_numpy(c[key]).to(dev) for key in ("W", "R")}
+        d["X16"] = torch.from_numpy(c["X"]).to(dev).half()
+        d["Y"] = torch.empty((T, n), device=dev)
+        sets.append(d)
+
+    def call(s):
+        return lambda: q.apr_qgemm_f16_in(QTYPE, s["W"], n, k, s["X16"], T, s["Y"], s["R"])
+
+    for s in sets:
+        call(s)()
+    torch.cuda.synchronize()
+    reps = 200
+    dt = timed_calls([call(s) for s in sets], reps, stream) / reps
+    q.apr_stream_status(stream)
+    tf = 2.0 * n * k * T / dt / 1e12
+    return {"workload": f"q4_0_gemm_residual_n{n}_k{k}_t{T}", "TFLOP/s": tf, "frac": tf / peak_tf, "us": dt * 1e6}
 
 
 def ffn_rate(q, synth, dev, stream, hidden=4096, inter=12288, T=512):
