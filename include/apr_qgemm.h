@@ -226,6 +226,22 @@ int apr_qgemm_noalloc(int qtype, const void* W, int n, int k, const float* X, in
                       float* Y, const float* residual, apr_stream_t stream);
 
 /*
+ * Normed projection: apr_qgemm_ex with X replaced by its row RMSNorm,
+ *   h = X / sqrt(mean(X^2, per row) + eps) * norm_weight,
+ * so Y = h . W^T (+ residual), or silu(h . Wg^T) * (h . Wu^T) with Wu. The
+ * pages' prefill layer runs the norm and then the projection as two steps
+ * (aprender-serve forward_qwen35_cuda_prefill.rs: batched_rmsnorm_into with
+ * attn_norm, then attn_qkv; post_attention_norm, then gate and up). Here, on
+ * the fp16 leg's tensor-core path, the norm writes the fp16 rows the GEMM
+ * reads, in one pass. args as for apr_qgemm_ex (ldy included; X is the
+ * un-normed input, read only); norm_weight [k] fp32, 16-byte aligned; eps >= 0
+ * and finite. Rows are processed in chunks of APR_FFN_CHUNK_ROWS; scratch per
+ * stream (the normed rows of a chunk). Errors as for apr_qgemm_ex, and
+ * APR_E_ALIAS if Y overlaps norm_weight.
+ */
+int apr_qgemm_rmsnorm(const apr_qgemm_args* args, const float* norm_weight, float eps);
+
+/*
  * FFN sublayer of a prefill layer over T rows of the residual stream, in place:
  *   h = RMSNorm(X) = X / sqrt(mean(X^2, per row) + eps) * norm_weight
  *   X = X + (silu(h . Wg^T) * (h . Wu^T)) . Wd^T

@@ -21,4 +21,5 @@ from .qref import (  # noqa: F401
     gate_up_swiglu_f16_inputs_f64,
     rmsnorm_f64,
     ffn_sublayer_f64,
+    normed_qgemm_f64,
 )

@@ -196,3 +196,16 @@ def ffn_sublayer_f64(qtype: int, X, weight, eps: float, Wg, Wu, Wd, hidden: int,
     u = h @ dequant_f64(qtype, Wu, inter, hidden).T
     act = silu_f64(g) * u
     return X64 + act @ dequant_f64(qtype, Wd, hidden, inter).T
+
+
+def normed_qgemm_f64(qtype: int, W, n: int, k: int, X, weight, eps: float, residual=None, Wu=None) -> np.ndarray:
+    """``h . W^T (+ R)``, or ``silu(h . W^T) * (h . Wu^T)`` with ``Wu``, where
+    ``h = rmsnorm(X)`` (the norm before a projection: rms_norm(x, attn_norm)
+    then attn_qkv in the pages' prefill layer); float64 throughout."""
+    h = rmsnorm_f64(_as_f64(X).reshape(-1, k), weight, eps)
+    g = h @ dequant_f64(qtype, W, n, k).T
+    if Wu is not None:
+        return silu_f64(g) * (h @ dequant_f64(qtype, Wu, n, k).T)
+    if residual is not None:
+        g = g + _as_f64(residual).reshape(g.shape)
+    return g

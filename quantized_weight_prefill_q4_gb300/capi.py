@@ -48,6 +48,7 @@ EXPORTS = (
     "apr_qgemm_f16_in",
     "apr_qgemm_noalloc",
     "apr_ffn_sublayer",
+    "apr_qgemm_rmsnorm",
     "apr_dequant",
     "apr_stream_status",
     "apr_last_error",
@@ -111,6 +112,7 @@ def _load() -> ctypes.CDLL:
         "apr_qgemm_f16_in": ([ci, vp, vp, ci, ci, vp, ci, vp, vp, vp], ci),
         "apr_qgemm_noalloc": ([ci, vp, ci, ci, vp, ci, vp, vp, vp], ci),
         "apr_ffn_sublayer": ([ctypes.POINTER(_FfnArgs)], ci),
+        "apr_qgemm_rmsnorm": ([ctypes.POINTER(_Args), vp, ctypes.c_float], ci),
         "apr_dequant": ([ci, vp, ci, ci, vp, vp], ci),
         "apr_stream_status": ([vp], ci),
         "apr_last_error": ([], ctypes.c_char_p),
@@ -278,6 +280,24 @@ def apr_qgemm_noalloc(qtype, W, n, k, X, T, Y, residual=None, stream=None) -> in
                                          _ptr(X, "X", dtype=f32, min_bytes=xb), T,
                                          _ptr(Y, "Y", dtype=f32, min_bytes=yb),
                                          _ptr(residual, "residual", dtype=f32, min_bytes=yb), _stream(stream)))
+
+
+def apr_qgemm_rmsnorm(qtype, W, n, k, X, T, Y, norm_weight, eps, *, residual=None, Wu=None, leg=APR_LEG_F16,
+                      path=APR_PATH_AUTO, stream=None, ldy=0) -> int:
+    """apr_qgemm_ex on RMSNorm(X) (norm_weight, eps): Y = h . W^T (+ residual),
+    or the gate/up SwiGLU of h with Wu."""
+    u8, f32 = _dtypes()
+    wb, xb, yb = _sizes(qtype, n, k, T)
+    if ldy:
+        rp = _rows_ptr(residual, "residual", T, n, ldy)
+        yp = _rows_ptr(Y, "Y", T, n, ldy)
+    else:
+        rp = _ptr(residual, "residual", dtype=f32, min_bytes=yb)
+        yp = _ptr(Y, "Y", dtype=f32, min_bytes=yb)
+    a = _Args(qtype, leg, path, _ptr(W, "W", dtype=u8, min_bytes=wb), _ptr(Wu, "Wu", dtype=u8, min_bytes=wb),
+              n, k, T, _ptr(X, "X", dtype=f32, min_bytes=xb), rp, yp, _stream(stream), ldy)
+    return _check(_lib.apr_qgemm_rmsnorm(ctypes.byref(a), _ptr(norm_weight, "norm_weight", dtype=f32,
+                                                               min_bytes=max(k, 0) * 4), float(eps)))
 
 
 def apr_ffn_sublayer(qtype, Wg, Wu, Wd, hidden, inter, T, norm_weight, eps, X, leg=APR_LEG_F16, stream=None) -> int:

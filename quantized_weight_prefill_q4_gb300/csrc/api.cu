@@ -91,7 +91,7 @@ int device_state(DeviceState** out) {
 // The GEMV's buffer starts zeroed (cudaMemsetAsync on the stream) and every
 // completed call leaves its counters zero; after a device-side timeout the
 // buffers are cleared again before their next use.
-enum ScratchUse { kScratchX16 = 0, kScratchGemv = 1, kScratchFfn = 2 };
+enum ScratchUse { kScratchX16 = 0, kScratchGemv = 1, kScratchFfn = 2, kScratchNorm = 3 };
 struct StreamScratch {
   int dev;
   cudaStream_t s;
@@ -323,6 +323,50 @@ int run_ffn(const apr_ffn_args& a) {
   return APR_OK;
 }
 
+// Normed projection: per chunk of rows, the norm into scratch (fp16 for the
+// fp16 leg's tensor-core path, else fp32), then the projection.
+int run_normed(const Problem& p, const float* w, float eps) {
+  int rc = check(p);
+  if (rc == 1) return APR_OK;
+  if (rc != APR_OK) return rc;
+  if (!(eps >= 0.f) || eps > 3.402823466e38f) return fail(APR_E_INVAL, "eps must be finite and >= 0");
+  if (!w) return fail(APR_E_INVAL, "null norm weight");
+  if (!aligned16(w)) return fail(APR_E_ALIGN, "pointer %p is not 16-byte aligned", (const void*)w);
+  const size_t ybytes = ((size_t)(p.T - 1) * (size_t)ldy_of(p) + (size_t)p.n) * 4;
+  if (overlap(p.Y, ybytes, w, (size_t)p.k * 4)) return fail(APR_E_ALIAS, "Y overlaps the norm weight");
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc != APR_OK) return rc;
+  int path = p.path;
+  if (path == APR_PATH_AUTO) path = p.T <= APR_GEMV_MAX_T ? APR_PATH_GEMV : APR_PATH_GEMM;
+  const bool tc = p.leg == APR_LEG_F16 && path == APR_PATH_GEMM && p.k % 256 == 0;
+  const int chunk = p.T < APR_FFN_CHUNK_ROWS ? p.T : APR_FFN_CHUNK_ROWS;
+  void* h = nullptr;
+  rc = stream_scratch(st->dev, p.s, kScratchNorm, (size_t)chunk * p.k * (tc ? 2 : 4), &h);
+  if (rc != APR_OK) return rc;
+  const int ldy = ldy_of(p);
+  for (int t0 = 0; t0 < p.T; t0 += chunk) {
+    const int rows = p.T - t0 < chunk ? p.T - t0 : chunk;
+    const float* Xc = p.X + (size_t)t0 * p.k;
+    float* Yc = p.Y + (size_t)t0 * ldy;
+    const float* Rc = p.R ? p.R + (size_t)t0 * ldy : nullptr;
+    rc = launched(launch_rmsnorm_rows(Xc, w, eps, rows, p.k, h, tc, p.s), "rmsnorm");
+    if (rc != APR_OK) return rc;
+    if (tc) {
+      char msg[256] = "";
+      const GemmPlan plan = plan_gemm_tc(p.n, p.k, rows, p.Wu != nullptr);
+      if (launch_gemm_tc(plan, p.qtype, p.W, p.Wu, p.n, p.k, static_cast<const uint16_t*>(h), rows, Yc, ldy, Rc,
+                         st->status, p.s, msg, sizeof msg, true) != 0)
+        return fail(APR_E_LAUNCH, "%s", msg);
+    } else {
+      rc = run(Problem{p.qtype, p.leg, path, p.W, p.Wu, p.n, p.k, rows, static_cast<const float*>(h), Rc, Yc, p.s,
+                       p.ldy});
+      if (rc != APR_OK) return rc;
+    }
+  }
+  return APR_OK;
+}
+
 }  // namespace
 
 namespace apr {
@@ -379,6 +423,14 @@ int apr_qgemm_ex(const apr_qgemm_args* a) {
   if (!a) return fail(APR_E_INVAL, "null argument struct");
   return run(Problem{a->qtype, a->leg, a->path, a->W, a->Wu, a->n, a->k, a->T, a->X, a->residual, a->Y,
                      (cudaStream_t)a->stream, a->ldy});
+}
+
+int apr_qgemm_rmsnorm(const apr_qgemm_args* a, const float* norm_weight, float eps) {
+  t_msg[0] = 0;
+  if (!a) return fail(APR_E_INVAL, "null argument struct");
+  return run_normed(Problem{a->qtype, a->leg, a->path, a->W, a->Wu, a->n, a->k, a->T, a->X, a->residual, a->Y,
+                            (cudaStream_t)a->stream, a->ldy},
+                    norm_weight, eps);
 }
 
 int apr_ffn_sublayer(const apr_ffn_args* a) {

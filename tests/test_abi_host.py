@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(q):
     names = declared_functions()
-    assert len(names) == 12, names
+    assert len(names) == 13, names
     lib = q.library()
     for name in names:
         assert hasattr(lib, name), name
@@ -161,3 +161,20 @@ def test_ffn_sublayer_argument_errors(q):
     assert rc(X=5 * B + 4) == -3             # misaligned
     assert rc(X=B + 64) == -4                # X over the gate weight
     assert rc(X=4 * B - 256) == -4           # X over the norm weight
+
+
+def test_normed_projection_argument_errors(q):
+    lib = q.library()
+    B = 1 << 24
+    args = q.capi._Args(2, 0, 0, B, None, 256, 512, 8, 2 * B, None, 3 * B, None, 0)
+    w = 4 * B
+    assert lib.apr_qgemm_rmsnorm(None, w, 1e-5) == -1
+    assert lib.apr_qgemm_rmsnorm(ctypes.byref(args), None, 1e-5) == -1
+    assert lib.apr_qgemm_rmsnorm(ctypes.byref(args), w, -1.0) == -1
+    assert lib.apr_qgemm_rmsnorm(ctypes.byref(args), w, float("nan")) == -1
+    assert lib.apr_qgemm_rmsnorm(ctypes.byref(args), w + 4, 1e-5) == -3
+    assert lib.apr_qgemm_rmsnorm(ctypes.byref(args), 3 * B + 64, 1e-5) == -4   # Y over the norm weight
+    bad = q.capi._Args(3, 0, 0, B, None, 256, 512, 8, 2 * B, None, 3 * B, None, 0)
+    assert lib.apr_qgemm_rmsnorm(ctypes.byref(bad), w, 1e-5) == -2            # the projection's own checks
+    empty = q.capi._Args(2, 0, 0, B, None, 256, 512, 0, 2 * B, None, 3 * B, None, 0)
+    assert lib.apr_qgemm_rmsnorm(ctypes.byref(empty), None, -1.0) == 0        # T == 0: nothing to do

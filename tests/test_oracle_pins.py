@@ -370,3 +370,21 @@ def test_ffn_sublayer_brute_force(qtype):
             want[t, o] = X[t, o] + sum(act[i] * Wd[o, i] for i in range(inter))
     got = oracle.ffn_sublayer_f64(qtype, X, w, eps, raw["g"], raw["u"], raw["d"], hidden, inter)
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
+def test_normed_projection_reduces_to_projection(qtype):
+    """Rows of +-1 have mean square 1, so with eps = 0 and unit weight the norm
+    is the identity and the normed projection is the plain one (pinned above
+    by brute force); a weight of 2 doubles it."""
+    n, k, T = 40, 96, 5
+    c = synth.make_case(qtype, n, k, T, residual=True, seed=12)
+    X = np.where(synth.activations(T, k, 13) >= 0, 1.0, -1.0).astype(np.float32)
+    ones = np.ones(k, np.float32)
+    np.testing.assert_array_equal(oracle.normed_qgemm_f64(qtype, c["W"], n, k, X, ones, 0.0, c["R"]),
+                                  oracle.qgemm_f64(qtype, c["W"], n, k, X, c["R"]))
+    np.testing.assert_array_equal(oracle.normed_qgemm_f64(qtype, c["W"], n, k, X, 2 * ones, 0.0),
+                                  2 * oracle.qgemm_f64(qtype, c["W"], n, k, X))
+    Wu = synth.quantize(qtype, synth.weight_f32(n, k, 14))
+    np.testing.assert_array_equal(oracle.normed_qgemm_f64(qtype, c["W"], n, k, X, ones, 0.0, Wu=Wu),
+                                  oracle.gate_up_swiglu_f64(qtype, c["W"], Wu, n, k, X))
