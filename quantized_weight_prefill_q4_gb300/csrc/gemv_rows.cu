@@ -23,11 +23,12 @@
 // of the row's warps to finish (a shared-memory counter) adds the PW partials
 // in a fixed order, so the result does not depend on timing.
 //
-// Programmatic dependent launch: the kernel lets the next kernel of the stream
-// launch as soon as it starts, and its producer streams W without waiting for
+// Programmatic dependent launch: the producer streams W without waiting for
 // the preceding kernel (so W must not be an output of the preceding call of
 // this library on the stream); X, R and Y are read or written only after
-// griddepcontrol.wait.
+// griddepcontrol.wait, and the kernel lets the next kernel of the stream
+// launch only after that wait, so at most the one kernel before it runs
+// beside it.
 
 #include <cstdint>
 #include <cuda_fp16.h>
@@ -87,7 +88,6 @@ __global__ void __launch_bounds__(RNTHREADS, 1)
     abort_flag[0] = 0;
     abort_flag[1] = 0;
     fence_mbar_init();
-    grid_launch_dependents();
   }
   for (int i = threadIdx.x; i < RMAXROWS; i += RNTHREADS) done[i] = 0;
   __syncthreads();
@@ -122,8 +122,10 @@ __global__ void __launch_bounds__(RNTHREADS, 1)
   const int pa = wi * 64 + lane, pb = pa + 32;  // this thread's block pairs
   const bool act_a = g < RG && pa < npk, act_b = g < RG && pb < npk;
 
-  // X, R and Y may belong to the preceding kernel until it completes
+  // X, R and Y may belong to the preceding kernel until it completes; once it
+  // has, the next kernel may launch (so only this kernel runs beside it)
   grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
   build_x_table<QT>(X, 1, k, xt, threadIdx.x, RNCW * 32);
   if (!SWI && R)
     for (int i = threadIdx.x; i < r1 - r0; i += RNCW * 32) rres[i] = R[r0 + i];
