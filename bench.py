@@ -32,6 +32,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -93,6 +94,9 @@ def barrier(world):
 
 
 # ------------------------------------------------------------------ clocks
+CLOCKS_DIR = tempfile.gettempdir()
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -101,7 +105,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        # the raw samples go to --clocks-dir (default: the system's temporary
+        # directory); the JSON line carries their summary
+        self.path = os.path.join(CLOCKS_DIR, f"clocks_bench_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
@@ -572,8 +578,12 @@ def main(argv=None):
                     help="step: only the timed apr_qgemm steps; kernel: only the GEMM kernel on fp16 activations; "
                          "gemv: only the T = 1 GEMV (small, bounded runs for profilers)")
     ap.add_argument("--gemv-tokens", type=int, default=1, help="tokens of the --only gemv run (1..16)")
+    ap.add_argument("--clocks-dir", default=None, help="where the raw nvidia-smi clock samples are written")
     ap.add_argument("--gemv-rows", type=int, default=4096, help="weight rows of the --only gemv run (k = 4096)")
     args = ap.parse_args(argv)
+    if args.clocks_dir:
+        global CLOCKS_DIR
+        CLOCKS_DIR = args.clocks_dir
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
