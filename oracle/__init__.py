@@ -22,4 +22,6 @@ from .qref import (  # noqa: F401
     rmsnorm_f64,
     ffn_sublayer_f64,
     normed_qgemm_f64,
+    prefill_attention_f64,
+    prefill_attention_f16_inputs_f64,
 )

@@ -37,6 +37,15 @@ What is computed, and where the pages define it:
   this module reads it as the usual RMSNorm of a row,
   ``y = x / sqrt(mean(x^2) + eps) * w``, ``w`` the norm weight per column.
 
+* Causal prefill attention over a KV cache (aprender-serve 0.70.2
+  src/cuda/executor/gdn_prefill_ops.rs, docs of ``qwen35_prefill_attention``
+  and ``qwen35_attention_pass``, and ``qwen35_flash_prefill_attention`` for the
+  fused form): query row ``t`` of a chunk sits at position ``pos0 + t`` and
+  attends to the cache rows ``0 .. pos0 + t``; scores are ``q . k / sqrt(d)``,
+  softmax over those keys, output ``sum_j p_j v_j``; query head ``h`` reads KV
+  head ``h / (num_heads / num_kv_heads)``. ``q`` is ``[rows][num_heads * d]``,
+  the caches ``[>= pos0 + rows][num_kv_heads * d]``, the output like ``q``.
+
 Every product is accumulated in float64 and the result is rounded to float32
 once. The f16-input mode rounds ``X`` and the dequantized ``W`` to fp16 first
 (the fp16 leg of ``qwen35_project_rows_f16``: fp16 in, fp32 accumulate), then
@@ -209,3 +218,44 @@ def normed_qgemm_f64(qtype: int, W, n: int, k: int, X, weight, eps: float, resid
     if residual is not None:
         g = g + _as_f64(residual).reshape(g.shape)
     return g
+
+
+# --------------------------------------------------------------------------
+# Causal prefill attention over a KV cache
+# --------------------------------------------------------------------------
+def prefill_attention_f64(Q, K_cache, V_cache, T: int, pos0: int, num_heads: int, num_kv_heads: int,
+                          head_dim: int, rows=None) -> np.ndarray:
+    """``out[t, h] = sum_{j <= pos0+t} softmax_j(q_{t,h} . k_{j,g} / sqrt(d)) v_{j,g}``
+    with ``g = h // (num_heads // num_kv_heads)``; float64, shape
+    ``[len(rows)][num_heads * head_dim]`` (``rows`` defaults to all ``T``)."""
+    d = head_dim
+    hpk = num_heads // num_kv_heads
+    rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
+    Q64 = _as_f64(Q).reshape(T, num_heads * d)[rows]
+    nk = pos0 + int(rows.max()) + 1 if len(rows) else 0
+    K64 = _as_f64(K_cache).reshape(-1, num_kv_heads * d)[:nk]
+    V64 = _as_f64(V_cache).reshape(-1, num_kv_heads * d)[:nk]
+    out = np.zeros((len(rows), num_heads * d), dtype=np.float64)
+    if not len(rows):
+        return out
+    # key j is visible to row t when j <= pos0 + t
+    visible = np.arange(nk)[None, :] <= (pos0 + rows)[:, None]
+    for h in range(num_heads):
+        g = h // hpk
+        q = Q64[:, h * d:(h + 1) * d]
+        k = K64[:, g * d:(g + 1) * d]
+        v = V64[:, g * d:(g + 1) * d]
+        s = (q @ k.T) / np.sqrt(d)
+        s = np.where(visible, s, -np.inf)
+        e = np.exp(s - s.max(axis=1, keepdims=True))
+        out[:, h * d:(h + 1) * d] = (e @ v) / e.sum(axis=1, keepdims=True)
+    return out
+
+
+def prefill_attention_f16_inputs_f64(Q, K_cache, V_cache, T: int, pos0: int, num_heads: int,
+                                     num_kv_heads: int, head_dim: int, rows=None) -> np.ndarray:
+    """The same attention after rounding ``q``, ``k`` and ``v`` to fp16 (the
+    flash form's tensor-core inputs), then in float64."""
+    r16 = lambda a: np.asarray(a, dtype=np.float32).astype(np.float16).astype(np.float64)  # noqa: E731
+    return prefill_attention_f64(r16(Q), r16(K_cache), r16(V_cache), T, pos0, num_heads, num_kv_heads,
+                                 head_dim, rows=rows)

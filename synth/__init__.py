@@ -19,5 +19,6 @@ from .gen import (  # noqa: F401
     weight_f32,
     activations,
     make_case,
+    attention_case,
     WORKLOADS,
 )

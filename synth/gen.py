@@ -21,6 +21,10 @@ Recipe (the same for every workload):
   rounded to fp16 (round to nearest even) for storage, and an all-zero block
   gets ``d = 0`` with ``q = 8`` (Q4_0) or ``q = 0`` (Q8_0).
 
+Prefill attention (``attention_case``): the query rows ``Q`` and the K and V
+caches are ``N(0, 1)`` float32 draws with seeds ``seed``, ``seed+1`` and
+``seed+2`` (rows of unit RMS, as the pages' per-head QK norm leaves them).
+
 This is the inverse direction of what the prefill path computes; the decoding
 and the products are not here.
 """
@@ -119,6 +123,20 @@ def make_case(qtype: int, n: int, k: int, T: int, *, residual: bool = False,
     case["X"] = activations(T, k, seed + 1)
     case["R"] = activations(T, n, seed + 2) if residual else None
     return case
+
+
+def attention_case(T: int, pos0: int, num_heads: int, num_kv_heads: int, head_dim: int = 256,
+                   seed: int = 0, cache_rows: int | None = None) -> dict:
+    """One seeded prefill-attention problem: ``Q`` f32 ``[T][num_heads * d]``
+    (seed), the K and V caches f32 ``[cache_rows][num_kv_heads * d]`` (seed+1,
+    seed+2), all ``N(0, 1)``; ``cache_rows`` defaults to ``pos0 + T``."""
+    rows = pos0 + T if cache_rows is None else cache_rows
+    return {
+        "T": T, "pos0": pos0, "num_heads": num_heads, "num_kv_heads": num_kv_heads, "head_dim": head_dim,
+        "Q": activations(T, num_heads * head_dim, seed),
+        "K": activations(rows, num_kv_heads * head_dim, seed + 1),
+        "V": activations(rows, num_kv_heads * head_dim, seed + 2),
+    }
 
 
 # Named workloads: shapes of the prefill projections the pages run, at their

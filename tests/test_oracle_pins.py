@@ -388,3 +388,131 @@ def test_normed_projection_reduces_to_projection(qtype):
     Wu = synth.quantize(qtype, synth.weight_f32(n, k, 14))
     np.testing.assert_array_equal(oracle.normed_qgemm_f64(qtype, c["W"], n, k, X, ones, 0.0, Wu=Wu),
                                   oracle.gate_up_swiglu_f64(qtype, c["W"], Wu, n, k, X))
+
+
+# ---------------------------------------------------------------- attention
+# Causal prefill attention (aprender-serve 0.70.2
+# src/cuda/executor/gdn_prefill_ops.rs, qwen35_prefill_attention and
+# qwen35_attention_pass): each pin fixes a part of the definition, the
+# 1/sqrt(d) scale, the mask j <= pos0 + t, the head grouping
+# h / (heads / kv_heads) and the softmax normalisation, from facts the
+# definition implies.
+def _attn(c, rows=None, **over):
+    a = dict(c)
+    a.update(over)
+    return oracle.prefill_attention_f64(a["Q"], a["K"], a["V"], a["T"], a["pos0"], a["num_heads"],
+                                        a["num_kv_heads"], a["head_dim"], rows=rows)
+
+
+def test_attention_first_position_sees_only_its_own_key():
+    # row 0 at position 0 attends to key 0 alone: its weight is exactly 1
+    c = synth.attention_case(3, 0, 4, 2, 16, seed=5)
+    out = _attn(c)
+    V = c["V"].astype(np.float64)
+    for h in range(4):
+        g = h // 2
+        assert np.array_equal(out[0, h * 16:(h + 1) * 16], V[0, g * 16:(g + 1) * 16])
+
+
+def test_attention_zero_query_is_the_running_mean_of_values():
+    # q = 0: every visible score is 0, the weights uniform, the output the mean
+    # of the values at positions 0 .. pos0 + t
+    T, pos0, d = 6, 5, 8
+    c = synth.attention_case(T, pos0, 2, 1, d, seed=6)
+    c["Q"] = np.zeros_like(c["Q"])
+    out = _attn(c)
+    V = c["V"].astype(np.float64)
+    running = np.cumsum(V, axis=0) / np.arange(1, len(V) + 1)[:, None]
+    for t in range(T):
+        for h in range(2):
+            np.testing.assert_allclose(out[t, h * d:(h + 1) * d], running[pos0 + t], rtol=0, atol=1e-14)
+
+
+def test_attention_two_keys_hand_value():
+    # d = 4, one head, query at position 1: q = (2,0,0,0), k0 = (1,0,0,0),
+    # k1 = 0, so the scores are 2 * 1 / sqrt(4) = 1 and 0, the weights
+    # e / (e + 1) and 1 / (e + 1); v0 = (1,2,0,0), v1 = (0,0,3,0)
+    e = math.e
+    Q = np.array([[2.0, 0, 0, 0]], dtype=np.float32)
+    K = np.array([[1.0, 0, 0, 0], [0, 0, 0, 0]], dtype=np.float32)
+    V = np.array([[1.0, 2, 0, 0], [0, 0, 3, 0]], dtype=np.float32)
+    out = oracle.prefill_attention_f64(Q, K, V, 1, 1, 1, 1, 4)
+    want = [e / (e + 1), 2 * e / (e + 1), 3 / (e + 1), 0.0]
+    np.testing.assert_allclose(out[0], want, rtol=1e-15, atol=0)
+
+
+def test_attention_mask_hides_later_positions():
+    T, pos0, d = 5, 3, 8
+    c = synth.attention_case(T, pos0, 2, 2, d, seed=7)
+    base = _attn(c)
+    for t in range(T):
+        # change every cache row after position pos0 + t: rows <= t keep their output
+        K2, V2 = c["K"].copy(), c["V"].copy()
+        K2[pos0 + t + 1:] += 1.5
+        V2[pos0 + t + 1:] -= 2.0
+        out = _attn(c, K=K2, V=V2)
+        np.testing.assert_array_equal(out[:t + 1], base[:t + 1])
+        if t + 1 < T:
+            assert np.abs(out[t + 1:] - base[t + 1:]).max() > 1e-3
+        # and the row's own position is visible to it
+        V3 = c["V"].copy()
+        V3[pos0 + t] += 1.0
+        assert np.abs(_attn(c, V=V3)[t] - base[t]).max() > 1e-6
+
+
+def test_attention_query_heads_share_kv_heads_in_consecutive_groups():
+    # 4 query heads over 2 KV heads: heads 0, 1 read KV head 0 and heads 2, 3
+    # read KV head 1 (h / 2, not h % 2)
+    T, pos0, d = 4, 2, 8
+    c = synth.attention_case(T, pos0, 4, 2, d, seed=8)
+    base = _attn(c)
+    V2 = c["V"].copy()
+    V2[:, d:2 * d] *= 2.0  # KV head 1 only (exact in f32: the weights stay, the sums double)
+    out = _attn(c, V=V2)
+    np.testing.assert_array_equal(out[:, :2 * d], base[:, :2 * d])
+    np.testing.assert_array_equal(out[:, 2 * d:], 2.0 * base[:, 2 * d:])
+
+
+def test_attention_chunk_split_gives_the_same_rows():
+    # rows 4..6 of a chunk at pos0 = 2 are the chunk of 3 rows at pos0 = 6 over
+    # the same cache: the output of a row depends on its position, not on the chunk
+    c = synth.attention_case(7, 2, 2, 1, 16, seed=9)
+    whole = _attn(c)
+    part = oracle.prefill_attention_f64(c["Q"][4:], c["K"], c["V"], 3, 6, 2, 1, 16)
+    np.testing.assert_allclose(part, whole[4:], rtol=0, atol=1e-14)
+
+
+def test_attention_is_invariant_to_a_shift_of_all_keys_and_to_key_order():
+    # adding one vector to every key shifts all scores of a row by the same
+    # amount; permuting the visible keys with their values changes nothing
+    T, pos0, d = 1, 9, 8
+    c = synth.attention_case(T, pos0, 1, 1, d, seed=10)
+    # keys on a 1/64 grid and a shift of whole 1/64 steps, so that the shifted
+    # keys are exact in f32
+    c["K"] = (np.round(c["K"] * 64) / 64).astype(np.float32)
+    base = _attn(c)
+    shift = (np.arange(d, dtype=np.float32) - 3) / 64
+    shifted = _attn(c, K=c["K"] + shift[None, :])
+    assert np.array_equal((c["K"] + shift).astype(np.float64), c["K"].astype(np.float64) + shift)
+    np.testing.assert_allclose(shifted, base, rtol=1e-12, atol=1e-13)
+    perm = np.random.default_rng(0).permutation(pos0 + T)
+    np.testing.assert_allclose(_attn(c, K=c["K"][perm], V=c["V"][perm]), base, rtol=1e-12, atol=1e-13)
+
+
+def test_attention_dominant_key_takes_all_the_weight():
+    # one key aligned with the query and far longer than the others: its
+    # weight is 1 - O(exp(-200)), so the output is its value
+    T, pos0, d = 1, 7, 16
+    c = synth.attention_case(T, pos0, 1, 1, d, seed=11)
+    K = c["K"] * 0.01
+    K[3] = c["Q"][0] / np.linalg.norm(c["Q"][0]) * (200.0 * 4 / np.linalg.norm(c["Q"][0]))
+    out = _attn(c, K=K)
+    np.testing.assert_allclose(out[0], c["V"][3].astype(np.float64), rtol=0, atol=1e-12)
+
+
+def test_attention_f16_input_mode_rounds_q_k_and_v():
+    c = synth.attention_case(3, 1, 2, 1, 8, seed=12)
+    r = lambda a: a.astype(np.float16).astype(np.float32)  # noqa: E731
+    np.testing.assert_array_equal(
+        oracle.prefill_attention_f16_inputs_f64(c["Q"], c["K"], c["V"], 3, 1, 2, 1, 8),
+        oracle.prefill_attention_f64(r(c["Q"]), r(c["K"]), r(c["V"]), 3, 1, 2, 1, 8))
