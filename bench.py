@@ -115,13 +115,15 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "25"], stdout=self.f, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
+            self.t0 = time.time()
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
 
     def __exit__(self, *a):
+        self.window_s = time.time() - self.t0 if self.proc else None
         if self.proc:
             time.sleep(0.15)
             self.proc.terminate()
@@ -150,7 +152,7 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[4]) if v.lower() == "active"})
         return {"sm_mhz": float(np.median([r[0] for r in loaded])), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(loaded)}
+                "reasons": reasons, "samples": len(loaded), "window_s": round(self.window_s, 3)}
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -402,6 +404,7 @@ def run_ours(args):
         gemv_big = gemv_rate(q, synth, dev, stream, peak_gbs, n=12288, k=4096)
         ffn = ffn_rate(q, synth, dev, stream)
         big = gemm_kernel_rate(q, synth, dev, stream, peak_tf, T=2048)
+        attn = {f"t{t}": attention_rate(q, synth, dev, stream, peak_tf, T=t) for t in (512, 2048)}
 
     # ---- end to end: host buffers, copies inside the timed region
     e2e_steps = max(20, min(args.steps, 200))
@@ -481,6 +484,7 @@ def run_ours(args):
             "gemv_12288": gemv_big,
             "ffn_sublayer": ffn,
             "gemm_t2048": big,
+            "attention": attn,
         }
         if not args.no_cpu:
             line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -543,6 +547,38 @@ def ffn_rate(q, synth, dev, stream, hidden=4096, inter=12288, T=512):
     flop = 2.0 * T * 3 * hidden * inter
     return {"workload": f"q4_0_ffn_hidden{hidden}_inter{inter}_t{T}", "TFLOP/s": flop / dt / 1e12, "us": dt * 1e6,
             "launches_per_call": 4}
+
+
+def attention_rate(q, synth, dev, stream, peak_tf, T=2048, pos0=0, nh=16, nkv=4):
+    """Causal prefill attention of a 9B-class layer (16 query heads over 4 KV
+    heads, head_dim 256) on a chunk of T rows at pos0, rotating input sets
+    (more than L2 in all). TFLOP/s counts the two products over the visible
+    (row, key) pairs only: 4 * 256 * heads * sum_t (pos0 + t + 1)."""
+    import torch
+
+    d = 256
+    per_set = 4 * (T * nh * d + 2 * (pos0 + T) * nkv * d)
+    nsets = max(2, -(-160 * 2**20 // per_set))
+    sets = []
+    for j in range(nsets):
+        c = synth.attention_case(T, pos0, nh, nkv, d, seed=80 + j)
+        x = {key: torch.from_numpy(c[key]).to(dev) for key in ("Q", "K", "V")}
+        x["O"] = torch.empty((T, nh * d), device=dev)
+        sets.append(x)
+
+    def call(x):
+        return lambda: q.apr_prefill_attention(x["Q"], x["K"], x["V"], x["O"], T, pos0, nh, nkv, d)
+
+    for x in sets:
+        call(x)()
+    torch.cuda.synchronize()
+    reps = 200
+    dt = timed_calls([call(x) for x in sets], reps, stream) / reps
+    q.apr_stream_status(stream)
+    flop = 4.0 * d * nh * (T * (T + 1) / 2 + pos0 * T)
+    tf = flop / dt / 1e12
+    return {"workload": f"attention_h{nh}_kv{nkv}_d{d}_t{T}_pos{pos0}", "TFLOP/s": tf, "frac": tf / peak_tf,
+            "us": dt * 1e6}
 
 
 def gemv_rate(q, synth, dev, stream, peak_gbs, n=4096, k=4096):

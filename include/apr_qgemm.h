@@ -285,6 +285,37 @@ typedef struct apr_ffn_args {
 int apr_ffn_sublayer(const apr_ffn_args* args);
 
 /*
+ * Causal prefill attention over a KV cache, the step between the attention
+ * sublayer's qkv projection and its output projection (aprender-serve 0.70.2
+ * gdn_prefill_ops.rs: qwen35_prefill_attention / qwen35_attention_pass define
+ * the layouts, the mask and the head grouping; qwen35_flash_prefill_attention
+ * the fused form taken here, fp16 tensor-core inputs with fp32 accumulation
+ * and an fp32 online softmax, no score matrix in memory). For query row t
+ * (position pos0 + t) and query head h,
+ *   out[t][h] = sum_{j <= pos0 + t} softmax_j(Q[t][h] . K[j][g] / sqrt(d)) V[j][g]
+ * with g = h / (num_heads / num_kv_heads) and d = head_dim.
+ *   Q          [T][num_heads * head_dim] fp32 query rows (normed and rotated
+ *              by the caller), dense
+ *   K_cache, V_cache  [>= pos0 + T][num_kv_heads * head_dim] fp32 rows, with
+ *              this chunk's rows already written; rows at or past pos0 + T are
+ *              never read
+ *   out        [T][num_heads * head_dim] fp32, overwritten
+ *   T          query rows (0: no-op); pos0 >= 0 their first position
+ *   num_heads  a multiple of num_kv_heads (grouped-query attention)
+ *   head_dim   256 (the only size the fused form takes)
+ * q, k and v enter the products rounded to fp16; the result is within fp16
+ * input rounding of the exact attention (the tests bound it). All pointers
+ * 16-byte aligned, caller owned; no scratch, no allocation. Errors:
+ * APR_E_INVAL for negative sizes, num_heads not a multiple of num_kv_heads,
+ * head_dim != 256, sizes past 2^30 positions, or a null pointer with T > 0;
+ * APR_E_ALIGN; APR_E_ALIAS if out overlaps Q or a cache; APR_E_DEVICE;
+ * APR_E_LAUNCH. Asynchronous on the stream; apr_stream_status reports a
+ * bounded wait that gave up (out is then unspecified).
+ */
+int apr_prefill_attention(const float* Q, const float* K_cache, const float* V_cache, float* out, int T, int pos0,
+                          int num_heads, int num_kv_heads, int head_dim, apr_stream_t stream);
+
+/*
  * Standalone dequant: out[n][k] f32 = f32(d) * f32(q'), bit exact (the product
  * of an fp16 scale and a code of at most 8 bits is exact in fp32). The device
  * dequant of aprender-serve gdn_prefill_ops.rs qwen35_dequant_f32 (Q8_0 and

@@ -49,6 +49,7 @@ EXPORTS = (
     "apr_qgemm_noalloc",
     "apr_ffn_sublayer",
     "apr_qgemm_rmsnorm",
+    "apr_prefill_attention",
     "apr_dequant",
     "apr_stream_status",
     "apr_last_error",
@@ -113,6 +114,7 @@ def _load() -> ctypes.CDLL:
         "apr_qgemm_noalloc": ([ci, vp, ci, ci, vp, ci, vp, vp, vp], ci),
         "apr_ffn_sublayer": ([ctypes.POINTER(_FfnArgs)], ci),
         "apr_qgemm_rmsnorm": ([ctypes.POINTER(_Args), vp, ctypes.c_float], ci),
+        "apr_prefill_attention": ([vp, vp, vp, vp, ci, ci, ci, ci, ci, vp], ci),
         "apr_dequant": ([ci, vp, ci, ci, vp, vp], ci),
         "apr_stream_status": ([vp], ci),
         "apr_last_error": ([], ctypes.c_char_p),
@@ -313,6 +315,21 @@ def apr_ffn_sublayer(qtype, Wg, Wu, Wd, hidden, inter, T, norm_weight, eps, X, l
                  _ptr(norm_weight, "norm_weight", dtype=f32, min_bytes=h_ * 4), float(eps),
                  _ptr(X, "X", dtype=f32, min_bytes=t_ * h_ * 4), _stream(stream))
     return _check(_lib.apr_ffn_sublayer(ctypes.byref(a)))
+
+
+def apr_prefill_attention(Q, K_cache, V_cache, out, T, pos0, num_heads, num_kv_heads, head_dim=256,
+                          stream=None) -> int:
+    """Causal attention of the T query rows at positions pos0 .. pos0 + T - 1
+    over the cache rows 0 .. pos0 + T - 1: Q and out [T][num_heads * head_dim],
+    the caches [>= pos0 + T][num_kv_heads * head_dim], all float32."""
+    _, f32 = _dtypes()
+    t_, p_ = max(T, 0), max(pos0, 0)
+    qb = t_ * max(num_heads, 0) * max(head_dim, 0) * 4
+    cb = (t_ + p_) * max(num_kv_heads, 0) * max(head_dim, 0) * 4 if t_ else 0
+    return _check(_lib.apr_prefill_attention(
+        _ptr(Q, "Q", dtype=f32, min_bytes=qb), _ptr(K_cache, "K_cache", dtype=f32, min_bytes=cb),
+        _ptr(V_cache, "V_cache", dtype=f32, min_bytes=cb), _ptr(out, "out", dtype=f32, min_bytes=qb), T, pos0,
+        num_heads, num_kv_heads, head_dim, _stream(stream)))
 
 
 def apr_dequant(qtype, W, n, k, out, stream=None) -> int:

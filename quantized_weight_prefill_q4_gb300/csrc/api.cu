@@ -474,6 +474,34 @@ int apr_qgemm_f16_in(int qtype, const void* W, const void* Wu, int n, int k, con
   return APR_OK;
 }
 
+int apr_prefill_attention(const float* Q, const float* K_cache, const float* V_cache, float* out, int T, int pos0,
+                          int num_heads, int num_kv_heads, int head_dim, apr_stream_t stream) {
+  t_msg[0] = 0;
+  if (T < 0 || pos0 < 0 || num_heads <= 0 || num_kv_heads <= 0)
+    return fail(APR_E_INVAL, "bad sizes T=%d pos0=%d num_heads=%d num_kv_heads=%d", T, pos0, num_heads,
+                num_kv_heads);
+  if (num_heads % num_kv_heads != 0)
+    return fail(APR_E_INVAL, "num_heads (%d) must be a multiple of num_kv_heads (%d)", num_heads, num_kv_heads);
+  if (head_dim != 256) return fail(APR_E_INVAL, "head_dim must be 256 (got %d)", head_dim);
+  if ((long long)pos0 + T > (1LL << 30) || (long long)num_heads * 256 > (1LL << 24) ||
+      (long long)((T + 127) / 128) * num_heads > 0x7FFFFFFFLL)
+    return fail(APR_E_INVAL, "sizes beyond the supported limits");
+  if (T == 0) return APR_OK;
+  if (!Q || !K_cache || !V_cache || !out) return fail(APR_E_INVAL, "null pointer");
+  for (const void* p : {(const void*)Q, (const void*)K_cache, (const void*)V_cache, (const void*)out})
+    if (!aligned16(p)) return fail(APR_E_ALIGN, "pointer %p is not 16-byte aligned", p);
+  const size_t qbytes = (size_t)T * num_heads * 256 * 4;
+  const size_t cbytes = ((size_t)pos0 + T) * num_kv_heads * 256 * 4;
+  if (overlap(out, qbytes, Q, qbytes) || overlap(out, qbytes, K_cache, cbytes) || overlap(out, qbytes, V_cache, cbytes))
+    return fail(APR_E_ALIAS, "out overlaps Q or the K / V cache");
+  DeviceState* st = nullptr;
+  const int rc = device_state(&st);
+  if (rc != APR_OK) return rc;
+  return launched(launch_prefill_attention(Q, K_cache, V_cache, out, T, pos0, num_heads, num_kv_heads, st->status,
+                                           (cudaStream_t)stream),
+                  "prefill_attention");
+}
+
 int apr_dequant(int qtype, const void* W, int n, int k, float* out, apr_stream_t stream) {
   t_msg[0] = 0;
   if (qtype != APR_Q4_0 && qtype != APR_Q8_0) return fail(APR_E_QTYPE, "unsupported qtype %d", qtype);

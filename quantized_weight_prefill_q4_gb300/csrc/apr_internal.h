@@ -56,6 +56,13 @@ int launch_gemv_tc(int qtype, const void* W, int n, int k, const float* X, int T
 cudaError_t launch_rmsnorm_rows(const float* X, const float* w, float eps, int T, int k, void* out, bool f16,
                                 cudaStream_t s);
 
+// Causal prefill attention, head_dim 256, fp16 tensor-core inputs, fp32
+// online softmax (attention.cu): Q and O [T][num_heads * 256], the caches
+// [>= pos0 + T][num_kv_heads * 256], all f32 and 16-byte aligned; rows of the
+// caches at or past pos0 + T are never read. Plain stream order.
+cudaError_t launch_prefill_attention(const float* Q, const float* K, const float* V, float* O, int T, int pos0,
+                                     int num_heads, int num_kv_heads, unsigned* status, cudaStream_t s);
+
 // Exact-fp32 FFMA GEMM for any k % 32 == 0 (gemm_simt.cu).
 cudaError_t launch_gemm_simt(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
                              float* Y, int ldy, const float* R, cudaStream_t s);

@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(q):
     names = declared_functions()
-    assert len(names) == 13, names
+    assert len(names) == 14, names
     lib = q.library()
     for name in names:
         assert hasattr(lib, name), name
@@ -178,3 +178,29 @@ def test_normed_projection_argument_errors(q):
     assert lib.apr_qgemm_rmsnorm(ctypes.byref(bad), w, 1e-5) == -2            # the projection's own checks
     empty = q.capi._Args(2, 0, 0, B, None, 256, 512, 0, 2 * B, None, 3 * B, None, 0)
     assert lib.apr_qgemm_rmsnorm(ctypes.byref(empty), None, -1.0) == 0        # T == 0: nothing to do
+
+
+def test_prefill_attention_argument_errors(q):
+    lib = q.library()
+    B = 1 << 26
+    Qp, Kp, Vp, Op = B, 2 * B, 3 * B, 4 * B   # 64 MB apart: no overlap at these sizes
+
+    def rc(Q=Qp, K=Kp, V=Vp, O=Op, T=8, pos0=16, nh=16, nkv=4, d=256):
+        return lib.apr_prefill_attention(Q, K, V, O, T, pos0, nh, nkv, d, None)
+
+    assert rc(T=-1) == -1
+    assert rc(pos0=-1) == -1
+    assert rc(nh=0) == -1
+    assert rc(nkv=0) == -1
+    assert rc(nh=6, nkv=4) == -1             # not a multiple
+    assert rc(d=128) == -1                   # the fused form takes head_dim 256
+    assert rc(pos0=(1 << 30)) == -1          # past the supported positions
+    assert rc(Q=None) == -1
+    assert rc(O=None) == -1
+    assert rc(K=Kp + 4) == -3                # misaligned
+    assert rc(O=Qp + 256) == -4              # out over Q
+    assert rc(O=Vp + 1024) == -4             # out over the V cache
+    assert rc(O=Kp - 4096) == -4             # out runs into the K cache
+    assert rc(T=0, Q=None, K=None, V=None, O=None) == 0   # T == 0: nothing to do
+    assert "head_dim" in (lib.apr_prefill_attention(Qp, Kp, Vp, Op, 1, 0, 1, 1, 64, None),
+                          q.apr_last_error())[1]
