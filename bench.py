@@ -344,6 +344,17 @@ def run_ours(args):
         print(json.dumps({"only": "gemv", "launches": args.warmup + args.steps}), flush=True)
         return
 
+    if args.only == "attention":
+        Ta = args.attn_tokens
+        c = synth.attention_case(Ta, 0, 16, 4, seed=80)
+        x = {key: torch.from_numpy(c[key]).to(dev) for key in ("Q", "K", "V")}
+        Oa = torch.empty((Ta, 16 * 256), device=dev)
+        for i in range(args.warmup + args.steps):
+            q.apr_prefill_attention(x["Q"], x["K"], x["V"], Oa, Ta, 0, 16, 4, 256, stream=stream)
+        q.apr_stream_status(stream)
+        print(json.dumps({"only": "attention", "launches": args.warmup + args.steps}), flush=True)
+        return
+
     if args.only == "kernel":
         for s in sets:
             q.apr_convert_f32_to_f16(s["X"], T * K, s["X16"], stream=stream)
@@ -610,9 +621,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=["all", "step", "kernel", "gemv"], default="all",
+    ap.add_argument("--only", choices=["all", "step", "kernel", "gemv", "attention"], default="all",
                     help="step: only the timed apr_qgemm steps; kernel: only the GEMM kernel on fp16 activations; "
-                         "gemv: only the T = 1 GEMV (small, bounded runs for profilers)")
+                         "gemv: only the T = 1 GEMV; attention: only the prefill attention (16 query heads, 4 KV "
+                         "heads, --attn-tokens rows at position 0) (small, bounded runs for profilers)")
+    ap.add_argument("--attn-tokens", type=int, default=2048, help="query rows of the --only attention run")
     ap.add_argument("--gemv-tokens", type=int, default=1, help="tokens of the --only gemv run (1..16)")
     ap.add_argument("--clocks-dir", default=None, help="where the raw nvidia-smi clock samples are written")
     ap.add_argument("--gemv-rows", type=int, default=4096, help="weight rows of the --only gemv run (k = 4096)")

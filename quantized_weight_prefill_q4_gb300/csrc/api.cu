@@ -91,7 +91,7 @@ int device_state(DeviceState** out) {
 // The GEMV's buffer starts zeroed (cudaMemsetAsync on the stream) and every
 // completed call leaves its counters zero; after a device-side timeout the
 // buffers are cleared again before their next use.
-enum ScratchUse { kScratchX16 = 0, kScratchGemv = 1, kScratchFfn = 2, kScratchNorm = 3 };
+enum ScratchUse { kScratchX16 = 0, kScratchGemv = 1, kScratchFfn = 2, kScratchNorm = 3, kScratchAttn = 4 };
 struct StreamScratch {
   int dev;
   cudaStream_t s;
@@ -495,11 +495,18 @@ int apr_prefill_attention(const float* Q, const float* K_cache, const float* V_c
   if (overlap(out, qbytes, Q, qbytes) || overlap(out, qbytes, K_cache, cbytes) || overlap(out, qbytes, V_cache, cbytes))
     return fail(APR_E_ALIAS, "out overlaps Q or the K / V cache");
   DeviceState* st = nullptr;
-  const int rc = device_state(&st);
+  int rc = device_state(&st);
   if (rc != APR_OK) return rc;
-  return launched(launch_prefill_attention(Q, K_cache, V_cache, out, T, pos0, num_heads, num_kv_heads, st->status,
-                                           (cudaStream_t)stream),
-                  "prefill_attention");
+  // the stream's scratch holds the fp16 copies of K and of V transposed
+  void* scratch = nullptr;
+  rc = stream_scratch(st->dev, (cudaStream_t)stream, kScratchAttn,
+                      prefill_attention_scratch_bytes(T, pos0, num_kv_heads), &scratch);
+  if (rc != APR_OK) return rc;
+  char msg[256] = "";
+  if (launch_prefill_attention(Q, K_cache, V_cache, out, T, pos0, num_heads, num_kv_heads, scratch, st->status,
+                               (cudaStream_t)stream, msg, sizeof msg) != 0)
+    return fail(APR_E_LAUNCH, "%s", msg);
+  return APR_OK;
 }
 
 int apr_dequant(int qtype, const void* W, int n, int k, float* out, apr_stream_t stream) {

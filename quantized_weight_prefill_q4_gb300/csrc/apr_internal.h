@@ -59,9 +59,14 @@ cudaError_t launch_rmsnorm_rows(const float* X, const float* w, float eps, int T
 // Causal prefill attention, head_dim 256, fp16 tensor-core inputs, fp32
 // online softmax (attention.cu): Q and O [T][num_heads * 256], the caches
 // [>= pos0 + T][num_kv_heads * 256], all f32 and 16-byte aligned; rows of the
-// caches at or past pos0 + T are never read. Plain stream order.
-cudaError_t launch_prefill_attention(const float* Q, const float* K, const float* V, float* O, int T, int pos0,
-                                     int num_heads, int num_kv_heads, unsigned* status, cudaStream_t s);
+// caches at or past pos0 + T are never read. Three plain launches in stream
+// order: K and V (transposed) to fp16 into `scratch`
+// (prefill_attention_scratch_bytes, 256-byte aligned), then the attention.
+// Returns 0, or -1 with a message.
+size_t prefill_attention_scratch_bytes(int T, int pos0, int num_kv_heads);
+int launch_prefill_attention(const float* Q, const float* K, const float* V, float* O, int T, int pos0,
+                             int num_heads, int num_kv_heads, void* scratch, unsigned* status, cudaStream_t s,
+                             char* msg, size_t msg_len);
 
 // Exact-fp32 FFMA GEMM for any k % 32 == 0 (gemm_simt.cu).
 cudaError_t launch_gemm_simt(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,

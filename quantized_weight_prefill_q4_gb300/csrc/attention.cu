@@ -10,36 +10,35 @@
 // qwen35_attention_pass: scores GEMM, causal mask and softmax, value GEMM per
 // KV group) fixes the layouts, the mask and the head grouping.
 //
+// Before the kernel, the K and V rows 0 .. pos0 + T - 1 of the KV head pairs
+// are converted to fp16 into the stream's scratch: K as it is
+// ([positions][num_kv_heads * 256]), V transposed ([num_kv_heads * 256]
+// [positions]), so that both operands of the two products are K-major tiles
+// that TMA copies straight into the 128-byte-swizzled MMA layout.
+//
 // One CTA per (128 query rows, query head); the CTAs of the last query rows,
 // which see the most keys, are launched first. Keys go in tiles of 64:
 //   warps 0-3   own the 128 query rows (one row per thread, TMEM lane = row):
 //               they put fp16 Q into tensor memory once, then per key tile read
 //               the 64 scores, update the running max and sum, write the fp16
 //               weights P into tensor memory, and at the end scale O by 1 / sum
-//   warps 4-11  convert K and V tiles from the f32 cache to fp16 in shared
-//               memory, 128-byte swizzled and K-major for the MMAs (V
-//               transposed), two tiles ahead in a ring of three; keys past the
-//               chunk's last position are written as zeros, never read
-//   warp 4      also issues the MMAs (one elected lane): S = Q . K^T (M = 128,
+//   warp 4      issues the MMAs (one elected lane): S = Q . K^T (M = 128,
 //               N = 64, 16 steps of K = 16 over the head dim) and O += P . V
 //               (M = 128, N = 256, 4 steps of K = 16 over the keys), with Q
 //               and P read from tensor memory
-// Tensor memory (512 columns): O fp32 [0, 256), S fp32 [256, 320), P fp16
-// pairs [320, 352), Q fp16 pairs [384, 512).
-// The softmax works in base 2 (scores times log2(e) / 16). The weights are
-// taken against a reference max m_ref that is moved (rescaling O and the sum)
-// only when the running max exceeds it by more than 8, so a weight is at most
-// 2^8 and O is rewritten only when the max jumps; the sum adds the weights
-// as rounded to fp16, the values the MMA multiplies.
-// Every mbarrier wait is bounded (2 s); a wait that gives up sets the device
-// status word, the CTA leaves its loop at the next block-wide barrier, waits
-// (bounded) for its MMAs in flight and frees its tensor memory.
-
+//   warp 5      TMA producer: per tile four K boxes [64 keys][64 dims] and one
+//               V box [256 dims][64 keys] into a ring of three buffers, two
+//               tiles ahead; positions past pos0 + T lie outside the tensor
+//               maps and arrive as zeros
 #include <cstdint>
+#include <cstdio>
+#include <cuda.h>
 #include <cuda_fp16.h>
+#include <cudaTypedefs.h>
 
 #include "apr_internal.h"
 #include "dev_common.cuh"
+#include "host_common.h"
 
 namespace apr {
 namespace {
@@ -49,9 +48,9 @@ constexpr int AQ = 128;                          // query rows per CTA (MMA M, T
 constexpr int AKEY = 64;                         // keys per tile
 constexpr int ANBUF = 3;                         // K/V tile ring
 constexpr int SOFT_WARPS = 4;
-constexpr int LOAD_WARPS = 8;
-constexpr int LOAD_THREADS = 32 * LOAD_WARPS;
-constexpr int A_THREADS = 32 * (SOFT_WARPS + LOAD_WARPS);
+constexpr int MMA_WARP = 4;
+constexpr int TMA_WARP = 5;
+constexpr int A_THREADS = 32 * 6;
 constexpr int K_PANEL = AKEY * 128;              // [64 keys][64 dims] fp16, 8 KB
 constexpr int K_BYTES = (AD / 64) * K_PANEL;     // four panels, 32 KB
 constexpr int V_BYTES = AD * 128;                // [256 dims][64 keys] fp16, 32 KB
@@ -62,57 +61,41 @@ constexpr uint32_t COL_O = 0, COL_S = 256, COL_P = 320, COL_Q = 384;
 constexpr uint32_t A_TMEM_COLS = 512;
 constexpr float kRescaleAbove = 8.0f;            // log2 of the largest weight kept unscaled
 static_assert(A_SMEM <= 232448, "shared memory budget");
-static_assert(AKEY * (AD / 8) == 8 * LOAD_THREADS && AD * (AKEY / 8) == 8 * LOAD_THREADS, "8 chunks a thread");
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Keys [kb, kb + 64) of KV head g into a ring buffer. K: four panels [64 keys]
-// [64 dims], one 128-byte row per key; V transposed: [256 dims][64 keys], one
-// 128-byte row per dim; 16-byte chunk c of row r sits at chunk c ^ (r & 7)
-// (the 128-byte swizzle). Keys >= nkeys are zeros.
-__device__ __forceinline__ void load_kv_tile(const float* __restrict__ Kc, const float* __restrict__ Vc,
-                                             size_t kv_dim, int g, int kb, int nkeys, uint8_t* buf, int ltid) {
-  const float* kbase = Kc + (size_t)g * AD;
-  const float* vbase = Vc + (size_t)g * AD;
-#pragma unroll 4
-  for (int i = 0; i < 8; ++i) {
-    const int c = ltid + LOAD_THREADS * i;
-    const int key = c >> 5, dc = c & 31;         // 32 chunks of 8 dims per key
-    uint4 o = make_uint4(0u, 0u, 0u, 0u);
-    if (kb + key < nkeys) {
-      const float4* src = reinterpret_cast<const float4*>(kbase + (size_t)(kb + key) * kv_dim + dc * 8);
-      const float4 a = __ldg(src), b = __ldg(src + 1);
-      o = make_uint4(pack_half2(a.x, a.y), pack_half2(a.z, a.w), pack_half2(b.x, b.y), pack_half2(b.z, b.w));
+// V rows [rows][cols] f32 -> VT [cols][ldv] fp16 (round to nearest), 64 x 64
+// tiles through shared memory; grid (ceil(rows / 64), cols / 64), block
+// (32, 8). Columns rows .. ldv - 1 of VT are not written.
+__global__ void __launch_bounds__(256) v_to_f16t_kernel(const float* __restrict__ V, int rows, int cols,
+                                                        uint16_t* __restrict__ VT, int ldv) {
+  __shared__ float tile[64][65];
+  const int r0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
+  for (int i = threadIdx.y; i < 64; i += 8)
+    for (int jj = threadIdx.x; jj < 64; jj += 32) {
+      const int r = r0 + i, c = c0 + jj;
+      tile[i][jj] = r < rows && c < cols ? V[(size_t)r * cols + c] : 0.f;
     }
-    *reinterpret_cast<uint4*>(buf + (dc >> 3) * K_PANEL + key * 128 + (((dc & 7) ^ (key & 7)) << 4)) = o;
-  }
-  uint8_t* vt = buf + K_BYTES;
-#pragma unroll 2
-  for (int i = 0; i < 8; ++i) {
-    const int c = ltid + LOAD_THREADS * i;
-    const int d = c & (AD - 1), kg = c >> 8;     // dim d, keys 8 kg .. 8 kg + 7
-    float x[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int key = kb + kg * 8 + e;
-      x[e] = key < nkeys ? __ldg(vbase + (size_t)key * kv_dim + d) : 0.f;
+  __syncthreads();
+  for (int i = threadIdx.y; i < 64; i += 8)
+    for (int jj = threadIdx.x; jj < 64; jj += 32) {
+      const int c = c0 + i, r = r0 + jj;
+      if (c < cols && r < rows) VT[(size_t)c * ldv + r] = __half_as_ushort(__float2half_rn(tile[jj][i]));
     }
-    *reinterpret_cast<uint4*>(vt + d * 128 + ((kg ^ (d & 7)) << 4)) =
-        make_uint4(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]), pack_half2(x[6], x[7]));
-  }
 }
 
 __global__ void __launch_bounds__(A_THREADS, 1)
-    prefill_attention_kernel(const float* __restrict__ Q, const float* __restrict__ Kc, const float* __restrict__ Vc,
-                             float* __restrict__ O, int T, int pos0, int num_heads, int num_kv_heads,
-                             unsigned* status) {
+    prefill_attention_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                             const float* __restrict__ Q, float* __restrict__ O, int T, int pos0, int num_heads,
+                             int num_kv_heads, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* barS = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint64_t* barO = barS + 1;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);   // [ANBUF]: a tile has landed
+  uint64_t* barS = full + ANBUF;                                  // S_j computed (and every MMA before it)
+  uint64_t* barO = barS + 1;                                      // the last O product done
   uint64_t* drain = barS + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(barS + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(barS + 4);
@@ -122,16 +105,17 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   const int h = blockIdx.x % num_heads;
   const int t0 = (nqt - 1 - (int)(blockIdx.x / num_heads)) * AQ;
   const int g = h / (num_heads / num_kv_heads);
-  const size_t q_dim = (size_t)num_heads * AD, kv_dim = (size_t)num_kv_heads * AD;
+  const size_t q_dim = (size_t)num_heads * AD;
   const int nkeys = pos0 + min(t0 + AQ, T);      // keys this CTA's rows see
   const int nkt = (nkeys + AKEY - 1) / AKEY;
 
   if (threadIdx.x == 0) {
+    for (int i = 0; i < ANBUF; ++i) mbar_init(&full[i], 1);
     mbar_init(barS, 1);
     mbar_init(barO, 1);
     mbar_init(drain, 1);
     abort_flag[0] = 0;
-    abort_flag[1] = 0;   // never set: the drain wait ignores the abort
+    abort_flag[1] = 0;   // never set: the drain waits ignore the abort
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tmem_holder, A_TMEM_COLS);
@@ -144,9 +128,19 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   const int r = threadIdx.x;
   const int t = t0 + r;
   const uint32_t lane_addr = tmem_base + ((uint32_t)(warp * 32) << 16);
-  const int ltid = threadIdx.x - SOFT_WARPS * 32;
+  const bool producer = warp == TMA_WARP && (threadIdx.x & 31) == 0;
+  int last[ANBUF] = {-1, -1, -1};   // producer: last tile sent into each buffer
+  auto send_tile = [&](int ti) {
+    const int b = ti % ANBUF;
+    uint8_t* buf = smem + b * BUF_BYTES;
+    mbar_arrive_expect_tx(&full[b], BUF_BYTES);
+#pragma unroll
+    for (int p = 0; p < AD / 64; ++p) tma_load_2d(buf + p * K_PANEL, &tmK, g * AD + 64 * p, ti * AKEY, &full[b]);
+    tma_load_2d(buf + K_BYTES, &tmV, ti * AKEY, g * AD, &full[b]);
+    last[b] = ti;
+  };
 
-  // ---- prologue: Q into tensor memory, K/V tiles 0 and 1 into the ring
+  // ---- prologue: Q into tensor memory, K/V tiles 0 and 1 on their way
   if (warp < SOFT_WARPS) {
     const float* qrow = Q + (size_t)t * q_dim + (size_t)h * AD;
 #pragma unroll 1
@@ -163,10 +157,11 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     }
     tmem_st_wait();
     tc_fence_before();
-  } else {
-    load_kv_tile(Kc, Vc, kv_dim, g, 0, nkeys, smem, ltid);
-    if (nkt > 1) load_kv_tile(Kc, Vc, kv_dim, g, AKEY, nkeys, smem + BUF_BYTES, ltid);
-    fence_proxy_async_smem();
+  } else if (producer) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    send_tile(0);
+    if (nkt > 1) send_tile(1);
   }
   __syncthreads();
 
@@ -179,19 +174,22 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 
 #pragma unroll 1
   for (int j = 0; j < nkt; ++j) {
-    uint8_t* buf = smem + (j % ANBUF) * BUF_BYTES;
-    // (1) S = Q . K_j^T
-    if (warp == SOFT_WARPS) {
-      tc_fence_after();
-      const uint64_t kdesc = smem_desc_sw128(buf);
-#pragma unroll
-      for (int kk = 0; kk < AD / 16; ++kk)
-        mma_f16_ts_elect(tmem_base + COL_S, tmem_base + COL_Q + 8 * kk,
-                         kdesc + (uint64_t)(((kk >> 2) * K_PANEL) >> 4) + 2 * (kk & 3), IDESC_S, kk != 0);
-      mma_commit_elect(barS);
-    }
+    const int b = j % ANBUF;
+    uint8_t* buf = smem + b * BUF_BYTES;
     bool ok = true;
-    if (warp < SOFT_WARPS) {
+    // (1) S = Q . K_j^T once tile j has landed
+    if (warp == MMA_WARP) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&full[b], (uint32_t)((j / ANBUF) & 1), abort_flag, status));
+      if (ok) {
+        tc_fence_after();
+        const uint64_t kdesc = smem_desc_sw128(buf);
+#pragma unroll
+        for (int kk = 0; kk < AD / 16; ++kk)
+          mma_f16_ts_elect(tmem_base + COL_S, tmem_base + COL_Q + 8 * kk,
+                           kdesc + (uint64_t)(((kk >> 2) * K_PANEL) >> 4) + 2 * (kk & 3), IDESC_S, kk != 0);
+        mma_commit_elect(barS);
+      }
+    } else if (warp < SOFT_WARPS) {
       // (2) softmax of tile j (its completion also means O += P . V_{j-1} is done)
       ok = __all_sync(0xffffffffu, mbar_wait(barS, (uint32_t)(j & 1), abort_flag, status));
       if (ok) {
@@ -242,20 +240,17 @@ __global__ void __launch_bounds__(A_THREADS, 1)
         tmem_st_wait();
         tc_fence_before();
       }
-    } else if (j + 2 < nkt) {
+    } else if (producer && j + 2 < nkt) {
       // (2') tile j + 2 into the buffer of tile j - 1, whose MMAs are done once S_j is
-      ok = __all_sync(0xffffffffu, mbar_wait(barS, (uint32_t)(j & 1), abort_flag, status));
-      if (ok) {
-        load_kv_tile(Kc, Vc, kv_dim, g, (j + 2) * AKEY, nkeys, smem + ((j + 2) % ANBUF) * BUF_BYTES, ltid);
-        fence_proxy_async_smem();
-      }
+      ok = mbar_wait(barS, (uint32_t)(j & 1), abort_flag, status);
+      if (ok) send_tile(j + 2);
     }
     if (__syncthreads_or(!ok)) {
       aborted = true;
       break;
     }
     // (3) O += P_j . V_j
-    if (warp == SOFT_WARPS) {
+    if (warp == MMA_WARP) {
       tc_fence_after();
       const uint64_t vdesc = smem_desc_sw128(buf + K_BYTES);
 #pragma unroll
@@ -287,10 +282,16 @@ __global__ void __launch_bounds__(A_THREADS, 1)
       }
     }
   }
-  if (aborted && warp == SOFT_WARPS) {
-    // wait until the MMAs already issued have finished
-    mma_commit_elect(drain);
-    __all_sync(0xffffffffu, mbar_wait(drain, 0, abort_flag + 1, status));
+  if (aborted) {
+    if (warp == MMA_WARP) {
+      // wait until the MMAs already issued have finished
+      mma_commit_elect(drain);
+      __all_sync(0xffffffffu, mbar_wait(drain, 0, abort_flag + 1, status));
+    } else if (producer) {
+      // and the copies in flight have landed
+      for (int i = 0; i < ANBUF; ++i)
+        if (last[i] >= 0) mbar_wait(&full[i], (uint32_t)((last[i] / ANBUF) & 1), abort_flag + 1, status);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -300,22 +301,56 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 
 }  // namespace
 
-cudaError_t launch_prefill_attention(const float* Q, const float* K, const float* V, float* O, int T, int pos0,
-                                     int num_heads, int num_kv_heads, unsigned* status, cudaStream_t s) {
-  if (T <= 0) return cudaSuccess;
+size_t prefill_attention_scratch_bytes(int T, int pos0, int num_kv_heads) {
+  const size_t rows = (size_t)pos0 + (size_t)T, kv_dim = (size_t)num_kv_heads * AD;
+  const size_t ldv = (rows + 7) & ~(size_t)7;
+  return ((rows * kv_dim * 2 + 255) & ~(size_t)255) + kv_dim * ldv * 2;
+}
+
+int launch_prefill_attention(const float* Q, const float* K, const float* V, float* O, int T, int pos0,
+                             int num_heads, int num_kv_heads, void* scratch, unsigned* status, cudaStream_t s,
+                             char* msg, size_t msg_len) {
+  if (T <= 0) return 0;
+  const size_t rows = (size_t)pos0 + (size_t)T, kv_dim = (size_t)num_kv_heads * AD;
+  const size_t ldv = (rows + 7) & ~(size_t)7;
+  uint16_t* K16 = static_cast<uint16_t*>(scratch);
+  uint16_t* VT16 = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(scratch) + ((rows * kv_dim * 2 + 255) & ~(size_t)255));
+  auto cuda_fail = [&](cudaError_t e, const char* what) {
+    snprintf(msg, msg_len, "%s: %s", what, cudaGetErrorString(e));
+    return -1;
+  };
+  // the fp16 copies of the cache rows 0 .. pos0 + T - 1
+  cudaError_t e = launch_x_to_f16(K, K16, rows * kv_dim, s);
+  if (e != cudaSuccess) return cuda_fail(e, "K to fp16");
+  v_to_f16t_kernel<<<dim3((unsigned)((rows + 63) / 64), (unsigned)(kv_dim / 64)), dim3(32, 8), 0, s>>>(
+      V, (int)rows, (int)kv_dim, VT16, (int)ldv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "V to fp16 (transposed)");
+
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn(msg, msg_len);
+  if (!fn) return -1;
+  CUtensorMap mK, mV;
+  if (!make_map_2d(fn, &mK, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K16, kv_dim, rows, kv_dim * 2, 64, AKEY,
+                   CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
+    return -1;
+  if (!make_map_2d(fn, &mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, VT16, rows, kv_dim, ldv * 2, AKEY, AD,
+                   CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
+    return -1;
+
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(prefill_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, A_SMEM);
-    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(prefill_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, A_SMEM);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill attention attributes");
     attr_set[dev] = 1;
   }
   const long long grid = (long long)((T + AQ - 1) / AQ) * num_heads;
-  prefill_attention_kernel<<<(unsigned)grid, A_THREADS, A_SMEM, s>>>(Q, K, V, O, T, pos0, num_heads, num_kv_heads,
+  prefill_attention_kernel<<<(unsigned)grid, A_THREADS, A_SMEM, s>>>(mK, mV, Q, O, T, pos0, num_heads, num_kv_heads,
                                                                      status);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "prefill attention");
+  return 0;
 }
 
 }  // namespace apr
