@@ -17,19 +17,37 @@
 // that TMA copies straight into the 128-byte-swizzled MMA layout.
 //
 // One CTA per (128 query rows, query head); the CTAs of the last query rows,
-// which see the most keys, are launched first. Keys go in tiles of 64:
+// which see the most keys, are launched first. Keys go in tiles of 64. The
+// roles hand work to each other through mbarriers, so that the tensor cores
+// compute the scores of tile j + 1 while the softmax of tile j runs:
 //   warps 0-3   own the 128 query rows (one row per thread, TMEM lane = row):
-//               they put fp16 Q into tensor memory once, then per key tile read
-//               the 64 scores, update the running max and sum, write the fp16
-//               weights P into tensor memory, and at the end scale O by 1 / sum
-//   warp 4      issues the MMAs (one elected lane): S = Q . K^T (M = 128,
-//               N = 64, 16 steps of K = 16 over the head dim) and O += P . V
-//               (M = 128, N = 256, 4 steps of K = 16 over the keys), with Q
-//               and P read from tensor memory
+//               they write fp16 Q into shared memory once (128-byte swizzled,
+//               K-major), then per key tile read the 64 scores, update the
+//               running max and sum, write the fp16 weights P into tensor
+//               memory, and at the end scale O by 1 / sum
+//   warp 4      issues the MMAs (one elected lane), in the order S_0, then per
+//               tile j: S_{j+1} = Q . K_{j+1}^T (M = 128, N = 64, 16 steps of
+//               K = 16 over the head dim, both operands in shared memory) and,
+//               once P_j is written, O += P_j . V_j (M = 128, N = 256, 4 steps
+//               of K = 16 over the keys, P read from tensor memory)
 //   warp 5      TMA producer: per tile four K boxes [64 keys][64 dims] and one
-//               V box [256 dims][64 keys] into a ring of three buffers, two
-//               tiles ahead; positions past pos0 + T lie outside the tensor
-//               maps and arrive as zeros
+//               V box [256 dims][64 keys] into a ring of two buffers, a buffer
+//               refilled once the MMAs of its previous tile are done;
+//               positions past pos0 + T lie outside the tensor maps and arrive
+//               as zeros
+// Tensor memory (512 columns allocated): O fp32 [0, 256), S fp32 two buffers
+// [256, 384), P fp16 pairs two buffers [384, 448).
+// The softmax works in base 2 (scores times log2(e) / 16). The weights are
+// taken against a reference max m_ref that is moved (rescaling O and the sum,
+// after the previous O product is done) only when the running max exceeds it
+// by more than 8, so a weight is at most 2^8 and O is rewritten only when the
+// max jumps; the sum adds the weights as rounded to fp16, the values the MMA
+// multiplies.
+// Every mbarrier wait is bounded (2 s); a wait that gives up sets the device
+// status word and an abort flag that ends every role's waits; the MMA warp
+// then waits (bounded) for its MMAs in flight, the producer for its copies,
+// and the CTA frees its tensor memory.
+
 #include <cstdint>
 #include <cstdio>
 #include <cuda.h>
@@ -46,18 +64,21 @@ namespace {
 constexpr int AD = 256;                          // head dim
 constexpr int AQ = 128;                          // query rows per CTA (MMA M, TMEM lanes)
 constexpr int AKEY = 64;                         // keys per tile
-constexpr int ANBUF = 3;                         // K/V tile ring
+constexpr int ANBUF = 2;                         // K/V tile ring
 constexpr int SOFT_WARPS = 4;
 constexpr int MMA_WARP = 4;
 constexpr int TMA_WARP = 5;
 constexpr int A_THREADS = 32 * 6;
+constexpr int Q_PANEL = AQ * 128;                // [128 rows][64 dims] fp16, 16 KB
+constexpr int Q_BYTES = (AD / 64) * Q_PANEL;     // 64 KB
 constexpr int K_PANEL = AKEY * 128;              // [64 keys][64 dims] fp16, 8 KB
 constexpr int K_BYTES = (AD / 64) * K_PANEL;     // four panels, 32 KB
 constexpr int V_BYTES = AD * 128;                // [256 dims][64 keys] fp16, 32 KB
 constexpr int BUF_BYTES = K_BYTES + V_BYTES;
-constexpr int OFF_BAR = ANBUF * BUF_BYTES;
-constexpr int A_SMEM = OFF_BAR + 64 + 1024;      // barriers, TMEM holder, flags; alignment slack
-constexpr uint32_t COL_O = 0, COL_S = 256, COL_P = 320, COL_Q = 384;
+constexpr int OFF_RING = Q_BYTES;
+constexpr int OFF_BAR = OFF_RING + ANBUF * BUF_BYTES;
+constexpr int A_SMEM = OFF_BAR + 128 + 1024;     // barriers, TMEM holder, flags; alignment slack
+constexpr uint32_t COL_O = 0, COL_S = 256, COL_P = 384;
 constexpr uint32_t A_TMEM_COLS = 512;
 constexpr float kRescaleAbove = 8.0f;            // log2 of the largest weight kept unscaled
 static_assert(A_SMEM <= 232448, "shared memory budget");
@@ -93,14 +114,19 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                              int num_kv_heads, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);   // [ANBUF]: a tile has landed
-  uint64_t* barS = full + ANBUF;                                  // S_j computed (and every MMA before it)
-  uint64_t* barO = barS + 1;                                      // the last O product done
-  uint64_t* drain = barS + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(barS + 3);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(barS + 4);
+  uint8_t* sQ = smem;
+  uint8_t* ring = smem + OFF_RING;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);  // [2] a tile has landed
+  uint64_t* kvEmpty = full + 2;                                   // [2] the MMAs of a buffer's tile are done
+  uint64_t* sFull = full + 4;                                     // [2] S_j computed (and every MMA before it)
+  uint64_t* pFull = full + 6;                                     // [2] P_j written (one arrival per softmax warp)
+  uint64_t* oDone = full + 8;                                     // O += P_j . V_j done
+  uint64_t* oLast = full + 9;                                     // the last O product done (one phase)
+  uint64_t* drain = full + 10;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full + 11);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 12);
 
-  const int warp = threadIdx.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqt = (T + AQ - 1) / AQ;
   const int h = blockIdx.x % num_heads;
   const int t0 = (nqt - 1 - (int)(blockIdx.x / num_heads)) * AQ;
@@ -110,9 +136,14 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   const int nkt = (nkeys + AKEY - 1) / AKEY;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < ANBUF; ++i) mbar_init(&full[i], 1);
-    mbar_init(barS, 1);
-    mbar_init(barO, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&kvEmpty[i], 1);
+      mbar_init(&sFull[i], 1);
+      mbar_init(&pFull[i], SOFT_WARPS);
+    }
+    mbar_init(oDone, 1);
+    mbar_init(oLast, 1);
     mbar_init(drain, 1);
     abort_flag[0] = 0;
     abort_flag[1] = 0;   // never set: the drain waits ignore the abort
@@ -123,16 +154,11 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-
-  // softmax rows: thread r = query row t0 + r = TMEM lane r
-  const int r = threadIdx.x;
-  const int t = t0 + r;
-  const uint32_t lane_addr = tmem_base + ((uint32_t)(warp * 32) << 16);
-  const bool producer = warp == TMA_WARP && (threadIdx.x & 31) == 0;
-  int last[ANBUF] = {-1, -1, -1};   // producer: last tile sent into each buffer
+  const bool producer = warp == TMA_WARP && lane == 0;
+  int last[ANBUF] = {-1, -1};   // producer: last tile sent into each buffer
   auto send_tile = [&](int ti) {
-    const int b = ti % ANBUF;
-    uint8_t* buf = smem + b * BUF_BYTES;
+    const int b = ti & 1;
+    uint8_t* buf = ring + b * BUF_BYTES;
     mbar_arrive_expect_tx(&full[b], BUF_BYTES);
 #pragma unroll
     for (int p = 0; p < AD / 64; ++p) tma_load_2d(buf + p * K_PANEL, &tmK, g * AD + 64 * p, ti * AKEY, &full[b]);
@@ -140,129 +166,161 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     last[b] = ti;
   };
 
-  // ---- prologue: Q into tensor memory, K/V tiles 0 and 1 on their way
-  if (warp < SOFT_WARPS) {
-    const float* qrow = Q + (size_t)t * q_dim + (size_t)h * AD;
-#pragma unroll 1
-    for (int cb = 0; cb < AD / 64; ++cb) {
-      uint32_t a[32];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (t < T) v = __ldg(reinterpret_cast<const float4*>(qrow + cb * 64) + i);
-        a[2 * i] = pack_half2(v.x, v.y);
-        a[2 * i + 1] = pack_half2(v.z, v.w);
-      }
-      tmem_st_32x32b_x32(lane_addr + COL_Q + cb * 32, a);
-    }
-    tmem_st_wait();
-    tc_fence_before();
-  } else if (producer) {
+  // softmax rows: thread r = query row t0 + r = TMEM lane r
+  const int r = threadIdx.x;
+  const int t = t0 + r;
+  const uint32_t lane_addr = tmem_base + ((uint32_t)(warp * 32) << 16);
+
+  // ---- prologue: tiles 0 and 1 on their way, Q into shared memory
+  if (producer) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     send_tile(0);
     if (nkt > 1) send_tile(1);
+  } else if (warp < SOFT_WARPS) {
+    // row r of the four Q panels; 16-byte chunk c of a row sits at c ^ (r & 7)
+    const float4* qrow = reinterpret_cast<const float4*>(Q + (size_t)t * q_dim + (size_t)h * AD);
+#pragma unroll 4
+    for (int c = 0; c < AD / 8; ++c) {
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
+      if (t < T) {
+        a = __ldg(qrow + 2 * c);
+        b = __ldg(qrow + 2 * c + 1);
+      }
+      *reinterpret_cast<uint4*>(sQ + (c >> 3) * Q_PANEL + r * 128 + (((c & 7) ^ (r & 7)) << 4)) =
+          make_uint4(pack_half2(a.x, a.y), pack_half2(a.z, a.w), pack_half2(b.x, b.y), pack_half2(b.z, b.w));
+    }
+    fence_proxy_async_smem();
   }
   __syncthreads();
 
-  constexpr uint32_t IDESC_S = idesc_f16_f32(AQ, AKEY);
-  constexpr uint32_t IDESC_O = idesc_f16_f32(AQ, AD);
-  const float sl2 = 1.4426950408889634f / 16.0f;   // log2(e) / sqrt(256)
-  const int plim = pos0 + min(t, T - 1);            // last key row t sees (rows past T: the last row's)
-  float m_run = -INFINITY, m_ref = 0.f, l = 0.f;
-  bool aborted = false;
-
-#pragma unroll 1
-  for (int j = 0; j < nkt; ++j) {
-    const int b = j % ANBUF;
-    uint8_t* buf = smem + b * BUF_BYTES;
-    bool ok = true;
-    // (1) S = Q . K_j^T once tile j has landed
-    if (warp == MMA_WARP) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&full[b], (uint32_t)((j / ANBUF) & 1), abort_flag, status));
-      if (ok) {
-        tc_fence_after();
-        const uint64_t kdesc = smem_desc_sw128(buf);
+  if (warp == MMA_WARP) {
+    // ------------------------------------------------ MMA issuer (whole warp)
+    constexpr uint32_t IDESC_S = idesc_f16_f32(AQ, AKEY);
+    constexpr uint32_t IDESC_O = idesc_f16_f32(AQ, AD);
+    const uint64_t qdesc = smem_desc_sw128(sQ);
+    auto issue_S = [&](int ti) {
+      const uint64_t kdesc = smem_desc_sw128(ring + (ti & 1) * BUF_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < AD / 16; ++kk)
-          mma_f16_ts_elect(tmem_base + COL_S, tmem_base + COL_Q + 8 * kk,
-                           kdesc + (uint64_t)(((kk >> 2) * K_PANEL) >> 4) + 2 * (kk & 3), IDESC_S, kk != 0);
-        mma_commit_elect(barS);
+      for (int kk = 0; kk < AD / 16; ++kk) {
+        const uint64_t step = 2 * (kk & 3);   // +32 bytes inside the 128-byte swizzle atom
+        mma_f16_ss_elect(tmem_base + COL_S + 64 * (ti & 1), qdesc + (uint64_t)(((kk >> 2) * Q_PANEL) >> 4) + step,
+                         kdesc + (uint64_t)(((kk >> 2) * K_PANEL) >> 4) + step, IDESC_S, kk != 0);
       }
-    } else if (warp < SOFT_WARPS) {
-      // (2) softmax of tile j (its completion also means O += P . V_{j-1} is done)
-      ok = __all_sync(0xffffffffu, mbar_wait(barS, (uint32_t)(j & 1), abort_flag, status));
-      if (ok) {
-        tc_fence_after();
-        uint32_t sv[64];
-        tmem_ld_32x32b_x32(lane_addr + COL_S, sv);
-        tmem_ld_32x32b_x32(lane_addr + COL_S + 32, sv + 32);
-        tmem_ld_wait_regs(sv);
-        regs_after_wait(sv + 32);
-        const int kb = j * AKEY;
-        float s[64];
-        float m_tile = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          s[c] = kb + c <= plim ? __uint_as_float(sv[c]) * sl2 : -INFINITY;
-          m_tile = fmaxf(m_tile, s[c]);
-        }
-        const float m_new = fmaxf(m_run, m_tile);
-        if (j == 0) {
-          m_ref = m_new;   // key 0 is visible to every row: finite
-        } else if (__any_sync(0xffffffffu, m_new > m_ref + kRescaleAbove)) {
-          // the whole warp moves its reference (tensor-memory access is per warp)
-          const float f = exp2f(m_ref - m_new);
-          l *= f;
-#pragma unroll 1
-          for (int cb = 0; cb < AD / 32; ++cb) {
-            uint32_t ov[32];
-            tmem_ld_32x32b_x32(lane_addr + COL_O + cb * 32, ov);
-            tmem_ld_wait_regs(ov);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
-            tmem_st_32x32b_x32(lane_addr + COL_O + cb * 32, ov);
-          }
-          m_ref = m_new;
-        }
-        m_run = m_new;
-        uint32_t pv[32];
-        float lsum = 0.f;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const __half2 p = __floats2half2_rn(exp2f(s[2 * c] - m_ref), exp2f(s[2 * c + 1] - m_ref));
-          const float2 pf = __half22float2(p);
-          lsum += pf.x + pf.y;
-          pv[c] = *reinterpret_cast<const uint32_t*>(&p);
-        }
-        l += lsum;
-        tmem_st_32x32b_x32(lane_addr + COL_P, pv);
-        tmem_st_wait();
-        tc_fence_before();
-      }
-    } else if (producer && j + 2 < nkt) {
-      // (2') tile j + 2 into the buffer of tile j - 1, whose MMAs are done once S_j is
-      ok = mbar_wait(barS, (uint32_t)(j & 1), abort_flag, status);
-      if (ok) send_tile(j + 2);
-    }
-    if (__syncthreads_or(!ok)) {
-      aborted = true;
-      break;
-    }
-    // (3) O += P_j . V_j
-    if (warp == MMA_WARP) {
+    };
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&full[0], 0, abort_flag, status));
+    if (ok) {
       tc_fence_after();
-      const uint64_t vdesc = smem_desc_sw128(buf + K_BYTES);
+      issue_S(0);
+      mma_commit_elect(&sFull[0]);
+    }
+#pragma unroll 1
+    for (int j = 0; j < nkt && ok; ++j) {
+      if (j + 1 < nkt) {
+        // S_{j+1} into the S buffer that S_{j-1} used: read before P_{j-1} was
+        // handed over, which came before O_{j-1} was issued
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[(j + 1) & 1], (uint32_t)(((j + 1) >> 1) & 1), abort_flag, status));
+        if (!ok) break;
+        tc_fence_after();
+        issue_S(j + 1);
+        mma_commit_elect(&sFull[(j + 1) & 1]);
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(&pFull[j & 1], (uint32_t)((j >> 1) & 1), abort_flag, status));
+      if (!ok) break;
+      tc_fence_after();
+      const uint64_t vdesc = smem_desc_sw128(ring + (j & 1) * BUF_BYTES + K_BYTES);
 #pragma unroll
       for (int kk = 0; kk < AKEY / 16; ++kk)
-        mma_f16_ts_elect(tmem_base + COL_O, tmem_base + COL_P + 8 * kk, vdesc + 2 * kk, IDESC_O, (j | kk) != 0);
-      if (j == nkt - 1) mma_commit_elect(barO);
+        mma_f16_ts_elect(tmem_base + COL_O, tmem_base + COL_P + 32 * (j & 1) + 8 * kk, vdesc + 2 * kk, IDESC_O,
+                         (j | kk) != 0);
+      mma_commit_elect(&kvEmpty[j & 1]);
+      mma_commit_elect(oDone);
+      if (j == nkt - 1) mma_commit_elect(oLast);
     }
-  }
-
-  // ---- epilogue: O / l to global memory
-  if (!aborted && warp < SOFT_WARPS) {
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(barO, 0, abort_flag, status));
+    if (!ok) {  // wait until the MMAs already issued have finished
+      mma_commit_elect(drain);
+      __all_sync(0xffffffffu, mbar_wait(drain, 0, abort_flag + 1, status));
+    }
+  } else if (warp == TMA_WARP) {
+    // ------------------------------------------------ TMA producer
+    if (producer) {
+#pragma unroll 1
+      for (int ti = 2; ti < nkt; ++ti)
+        if (mbar_wait(&kvEmpty[ti & 1], (uint32_t)(((ti >> 1) - 1) & 1), abort_flag, status))
+          send_tile(ti);
+        else
+          break;
+      // every copy sent has landed before the CTA ends (at once unless a wait gave up)
+      for (int i = 0; i < ANBUF; ++i)
+        if (last[i] >= 0) mbar_wait(&full[i], (uint32_t)((last[i] >> 1) & 1), abort_flag + 1, status);
+    }
+  } else {
+    // ------------------------------------------------ softmax rows, then the output
+    const float sl2 = 1.4426950408889634f / 16.0f;   // log2(e) / sqrt(256)
+    const int plim = pos0 + min(t, T - 1);            // last key row t sees (rows past T: the last row's)
+    float m_run = -INFINITY, m_ref = 0.f, l = 0.f;
+    bool ok = true;
+#pragma unroll 1
+    for (int j = 0; j < nkt; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&sFull[j & 1], (uint32_t)((j >> 1) & 1), abort_flag, status));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sv[64];
+      tmem_ld_32x32b_x32(lane_addr + COL_S + 64 * (j & 1), sv);
+      tmem_ld_32x32b_x32(lane_addr + COL_S + 64 * (j & 1) + 32, sv + 32);
+      tmem_ld_wait_regs(sv);
+      regs_after_wait(sv + 32);
+      const int kb = j * AKEY;
+      float s[64];
+      float m_tile = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        s[c] = kb + c <= plim ? __uint_as_float(sv[c]) * sl2 : -INFINITY;
+        m_tile = fmaxf(m_tile, s[c]);
+      }
+      const float m_new = fmaxf(m_run, m_tile);
+      if (j == 0) {
+        m_ref = m_new;   // key 0 is visible to every row: finite
+      } else if (__any_sync(0xffffffffu, m_new > m_ref + kRescaleAbove)) {
+        // the whole warp moves its reference (tensor-memory access is per
+        // warp), once O += P_{j-1} . V_{j-1} is done (S_j's completion already
+        // covers O_{j-2}, so the parity wait cannot be a phase behind)
+        ok = __all_sync(0xffffffffu, mbar_wait(oDone, (uint32_t)((j - 1) & 1), abort_flag, status));
+        if (!ok) break;
+        tc_fence_after();
+        const float f = exp2f(m_ref - m_new);
+        l *= f;
+#pragma unroll 1
+        for (int cb = 0; cb < AD / 32; ++cb) {
+          uint32_t ov[32];
+          tmem_ld_32x32b_x32(lane_addr + COL_O + cb * 32, ov);
+          tmem_ld_wait_regs(ov);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
+          tmem_st_32x32b_x32(lane_addr + COL_O + cb * 32, ov);
+        }
+        m_ref = m_new;
+      }
+      m_run = m_new;
+      uint32_t pv[32];
+      float lsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const __half2 p = __floats2half2_rn(exp2f(s[2 * c] - m_ref), exp2f(s[2 * c + 1] - m_ref));
+        const float2 pf = __half22float2(p);
+        lsum += pf.x + pf.y;
+        pv[c] = *reinterpret_cast<const uint32_t*>(&p);
+      }
+      l += lsum;
+      // P_j into the P buffer of P_{j-2}, whose O product S_j's completion covers
+      tmem_st_32x32b_x32(lane_addr + COL_P + 32 * (j & 1), pv);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pFull[j & 1]);
+    }
+    // ---- O / l to global memory, after the last O product
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(oLast, 0, abort_flag, status));
     if (ok) {
       tc_fence_after();
       const float inv = 1.0f / l;
@@ -280,17 +338,6 @@ __global__ void __launch_bounds__(A_THREADS, 1)
                                  __uint_as_float(ov[4 * i + 2]) * inv, __uint_as_float(ov[4 * i + 3]) * inv);
         }
       }
-    }
-  }
-  if (aborted) {
-    if (warp == MMA_WARP) {
-      // wait until the MMAs already issued have finished
-      mma_commit_elect(drain);
-      __all_sync(0xffffffffu, mbar_wait(drain, 0, abort_flag + 1, status));
-    } else if (producer) {
-      // and the copies in flight have landed
-      for (int i = 0; i < ANBUF; ++i)
-        if (last[i] >= 0) mbar_wait(&full[i], (uint32_t)((last[i] / ANBUF) & 1), abort_flag + 1, status);
     }
   }
   tc_fence_before();
