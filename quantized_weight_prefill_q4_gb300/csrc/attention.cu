@@ -30,11 +30,12 @@
 //               K = 16 over the head dim, both operands in shared memory) and,
 //               once P_j is written, O += P_j . V_j (M = 128, N = 256, 4 steps
 //               of K = 16 over the keys, P read from tensor memory)
-//   warp 5      TMA producer: per tile four K boxes [64 keys][64 dims] and one
-//               V box [256 dims][64 keys] into a ring of two buffers, a buffer
-//               refilled once the MMAs of its previous tile are done;
-//               positions past pos0 + T lie outside the tensor maps and arrive
-//               as zeros
+//   warp 5      TMA producer: per tile four K boxes [64 keys][64 dims] into a
+//               ring of three K buffers, each refilled once the scores of its
+//               previous tile are computed, and one V box [256 dims][64 keys]
+//               into a ring of two V buffers, each refilled once the O product
+//               of its previous tile is done; positions past pos0 + T lie
+//               outside the tensor maps and arrive as zeros
 // Tensor memory (512 columns allocated): O fp32 [0, 256), S fp32 two buffers
 // [256, 384), P fp16 pairs two buffers [384, 448).
 // The softmax works in base 2 (scores times log2(e) / 16). The weights are
@@ -64,7 +65,8 @@ namespace {
 constexpr int AD = 256;                          // head dim
 constexpr int AQ = 128;                          // query rows per CTA (MMA M, TMEM lanes)
 constexpr int AKEY = 64;                         // keys per tile
-constexpr int ANBUF = 2;                         // K/V tile ring
+constexpr int KBUF = 3;                          // K tile ring
+constexpr int VBUF = 2;                          // V tile ring
 constexpr int SOFT_WARPS = 4;
 constexpr int MMA_WARP = 4;
 constexpr int TMA_WARP = 5;
@@ -74,10 +76,10 @@ constexpr int Q_BYTES = (AD / 64) * Q_PANEL;     // 64 KB
 constexpr int K_PANEL = AKEY * 128;              // [64 keys][64 dims] fp16, 8 KB
 constexpr int K_BYTES = (AD / 64) * K_PANEL;     // four panels, 32 KB
 constexpr int V_BYTES = AD * 128;                // [256 dims][64 keys] fp16, 32 KB
-constexpr int BUF_BYTES = K_BYTES + V_BYTES;
-constexpr int OFF_RING = Q_BYTES;
-constexpr int OFF_BAR = OFF_RING + ANBUF * BUF_BYTES;
-constexpr int A_SMEM = OFF_BAR + 128 + 1024;     // barriers, TMEM holder, flags; alignment slack
+constexpr int OFF_K = Q_BYTES;
+constexpr int OFF_V = OFF_K + KBUF * K_BYTES;
+constexpr int OFF_BAR = OFF_V + VBUF * V_BYTES;
+constexpr int A_SMEM = OFF_BAR + 192 + 1024;     // barriers, TMEM holder, flags; alignment slack
 constexpr uint32_t COL_O = 0, COL_S = 256, COL_P = 384;
 constexpr uint32_t A_TMEM_COLS = 512;
 constexpr float kRescaleAbove = 8.0f;            // log2 of the largest weight kept unscaled
@@ -115,16 +117,19 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = smem;
-  uint8_t* ring = smem + OFF_RING;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + OFF_BAR);  // [2] a tile has landed
-  uint64_t* kvEmpty = full + 2;                                   // [2] the MMAs of a buffer's tile are done
-  uint64_t* sFull = full + 4;                                     // [2] S_j computed (and every MMA before it)
-  uint64_t* pFull = full + 6;                                     // [2] P_j written (one arrival per softmax warp)
-  uint64_t* oDone = full + 8;                                     // O += P_j . V_j done
-  uint64_t* oLast = full + 9;                                     // the last O product done (one phase)
-  uint64_t* drain = full + 10;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(full + 11);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 12);
+  uint8_t* sK = smem + OFF_K;
+  uint8_t* sV = smem + OFF_V;
+  uint64_t* kFull = reinterpret_cast<uint64_t*>(smem + OFF_BAR);  // [3] a K tile has landed
+  uint64_t* kEmpty = kFull + 3;                                   // [3] the scores of a K buffer's tile are done
+  uint64_t* vFull = kFull + 6;                                    // [2] a V tile has landed
+  uint64_t* vEmpty = kFull + 8;                                   // [2] the O product of a V buffer's tile is done
+  uint64_t* sFull = kFull + 10;                                   // [2] S_j computed (and every MMA before it)
+  uint64_t* pFull = kFull + 12;                                   // [2] P_j written (one arrival per softmax warp)
+  uint64_t* oDone = kFull + 14;                                   // O += P_j . V_j done
+  uint64_t* oLast = kFull + 15;                                   // the last O product done (one phase)
+  uint64_t* drain = kFull + 16;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(kFull + 17);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(kFull + 18);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqt = (T + AQ - 1) / AQ;
@@ -136,9 +141,13 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   const int nkt = (nkeys + AKEY - 1) / AKEY;
 
   if (threadIdx.x == 0) {
+    for (int i = 0; i < KBUF; ++i) {
+      mbar_init(&kFull[i], 1);
+      mbar_init(&kEmpty[i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&kvEmpty[i], 1);
+      mbar_init(&vFull[i], 1);
+      mbar_init(&vEmpty[i], 1);
       mbar_init(&sFull[i], 1);
       mbar_init(&pFull[i], SOFT_WARPS);
     }
@@ -155,15 +164,20 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const bool producer = warp == TMA_WARP && lane == 0;
-  int last[ANBUF] = {-1, -1};   // producer: last tile sent into each buffer
-  auto send_tile = [&](int ti) {
-    const int b = ti & 1;
-    uint8_t* buf = ring + b * BUF_BYTES;
-    mbar_arrive_expect_tx(&full[b], BUF_BYTES);
+  int last_k = -1, last_v = -1;   // producer: last K and V tiles sent
+  auto send_k = [&](int ti) {
+    const int b = ti % KBUF;
+    mbar_arrive_expect_tx(&kFull[b], K_BYTES);
 #pragma unroll
-    for (int p = 0; p < AD / 64; ++p) tma_load_2d(buf + p * K_PANEL, &tmK, g * AD + 64 * p, ti * AKEY, &full[b]);
-    tma_load_2d(buf + K_BYTES, &tmV, ti * AKEY, g * AD, &full[b]);
-    last[b] = ti;
+    for (int p = 0; p < AD / 64; ++p)
+      tma_load_2d(sK + b * K_BYTES + p * K_PANEL, &tmK, g * AD + 64 * p, ti * AKEY, &kFull[b]);
+    last_k = ti;
+  };
+  auto send_v = [&](int ti) {
+    const int b = ti & 1;
+    mbar_arrive_expect_tx(&vFull[b], V_BYTES);
+    tma_load_2d(sV + b * V_BYTES, &tmV, ti * AKEY, g * AD, &vFull[b]);
+    last_v = ti;
   };
 
   // softmax rows: thread r = query row t0 + r = TMEM lane r
@@ -175,8 +189,11 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   if (producer) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    send_tile(0);
-    if (nkt > 1) send_tile(1);
+    for (int ti = 0; ti < 2 && ti < nkt; ++ti) {
+      send_k(ti);
+      send_v(ti);
+    }
+    if (nkt > 2) send_k(2);
   } else if (warp < SOFT_WARPS) {
     // row r of the four Q panels; 16-byte chunk c of a row sits at c ^ (r & 7)
     const float4* qrow = reinterpret_cast<const float4*>(Q + (size_t)t * q_dim + (size_t)h * AD);
@@ -200,40 +217,42 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     constexpr uint32_t IDESC_O = idesc_f16_f32(AQ, AD);
     const uint64_t qdesc = smem_desc_sw128(sQ);
     auto issue_S = [&](int ti) {
-      const uint64_t kdesc = smem_desc_sw128(ring + (ti & 1) * BUF_BYTES);
+      const uint64_t kdesc = smem_desc_sw128(sK + (ti % KBUF) * K_BYTES);
 #pragma unroll
       for (int kk = 0; kk < AD / 16; ++kk) {
         const uint64_t step = 2 * (kk & 3);   // +32 bytes inside the 128-byte swizzle atom
         mma_f16_ss_elect(tmem_base + COL_S + 64 * (ti & 1), qdesc + (uint64_t)(((kk >> 2) * Q_PANEL) >> 4) + step,
                          kdesc + (uint64_t)(((kk >> 2) * K_PANEL) >> 4) + step, IDESC_S, kk != 0);
       }
+      mma_commit_elect(&sFull[ti & 1]);
+      mma_commit_elect(&kEmpty[ti % KBUF]);
     };
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&full[0], 0, abort_flag, status));
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&kFull[0], 0, abort_flag, status));
     if (ok) {
       tc_fence_after();
       issue_S(0);
-      mma_commit_elect(&sFull[0]);
     }
 #pragma unroll 1
     for (int j = 0; j < nkt && ok; ++j) {
       if (j + 1 < nkt) {
         // S_{j+1} into the S buffer that S_{j-1} used: read before P_{j-1} was
         // handed over, which came before O_{j-1} was issued
-        ok = __all_sync(0xffffffffu, mbar_wait(&full[(j + 1) & 1], (uint32_t)(((j + 1) >> 1) & 1), abort_flag, status));
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&kFull[(j + 1) % KBUF], (uint32_t)(((j + 1) / KBUF) & 1), abort_flag, status));
         if (!ok) break;
         tc_fence_after();
         issue_S(j + 1);
-        mma_commit_elect(&sFull[(j + 1) & 1]);
       }
-      ok = __all_sync(0xffffffffu, mbar_wait(&pFull[j & 1], (uint32_t)((j >> 1) & 1), abort_flag, status));
+      ok = __all_sync(0xffffffffu, mbar_wait(&pFull[j & 1], (uint32_t)((j >> 1) & 1), abort_flag, status) &&
+                                       mbar_wait(&vFull[j & 1], (uint32_t)((j >> 1) & 1), abort_flag, status));
       if (!ok) break;
       tc_fence_after();
-      const uint64_t vdesc = smem_desc_sw128(ring + (j & 1) * BUF_BYTES + K_BYTES);
+      const uint64_t vdesc = smem_desc_sw128(sV + (j & 1) * V_BYTES);
 #pragma unroll
       for (int kk = 0; kk < AKEY / 16; ++kk)
         mma_f16_ts_elect(tmem_base + COL_O, tmem_base + COL_P + 32 * (j & 1) + 8 * kk, vdesc + 2 * kk, IDESC_O,
                          (j | kk) != 0);
-      mma_commit_elect(&kvEmpty[j & 1]);
+      mma_commit_elect(&vEmpty[j & 1]);
       mma_commit_elect(oDone);
       if (j == nkt - 1) mma_commit_elect(oLast);
     }
@@ -244,15 +263,25 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   } else if (warp == TMA_WARP) {
     // ------------------------------------------------ TMA producer
     if (producer) {
+      // K_{n+1} once S_{n-2} is done, then V_n once O_{n-2} is (the scores of
+      // a tile are computed well before its O product, so K runs further ahead)
+      bool ok = true;
 #pragma unroll 1
-      for (int ti = 2; ti < nkt; ++ti)
-        if (mbar_wait(&kvEmpty[ti & 1], (uint32_t)(((ti >> 1) - 1) & 1), abort_flag, status))
-          send_tile(ti);
-        else
-          break;
-      // every copy sent has landed before the CTA ends (at once unless a wait gave up)
-      for (int i = 0; i < ANBUF; ++i)
-        if (last[i] >= 0) mbar_wait(&full[i], (uint32_t)((last[i] >> 1) & 1), abort_flag + 1, status);
+      for (int n = 2; n < nkt && ok; ++n) {
+        if (n + 1 < nkt) {
+          ok = mbar_wait(&kEmpty[(n + 1) % KBUF], (uint32_t)((((n + 1) / KBUF) - 1) & 1), abort_flag, status);
+          if (!ok) break;
+          send_k(n + 1);
+        }
+        ok = mbar_wait(&vEmpty[n & 1], (uint32_t)(((n >> 1) - 1) & 1), abort_flag, status);
+        if (ok) send_v(n);
+      }
+      // every copy sent has landed before the CTA ends (at once unless a wait
+      // gave up); the last tile of a ring slot is the only one that can be pending
+      for (int ti = max(0, last_k - KBUF + 1); ti <= last_k; ++ti)
+        mbar_wait(&kFull[ti % KBUF], (uint32_t)((ti / KBUF) & 1), abort_flag + 1, status);
+      for (int ti = max(0, last_v - 1); ti <= last_v; ++ti)
+        mbar_wait(&vFull[ti & 1], (uint32_t)((ti >> 1) & 1), abort_flag + 1, status);
     }
   } else {
     // ------------------------------------------------ softmax rows, then the output
