@@ -91,23 +91,37 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 }
 
 // V rows [rows][cols] f32 -> VT [cols][ldv] fp16 (round to nearest), 64 x 64
-// tiles through shared memory; grid (ceil(rows / 64), cols / 64), block
-// (32, 8). Columns rows .. ldv - 1 of VT are not written.
+// tiles through shared memory; grid (ceil(rows / 64), cols / 64), 256
+// threads. Reads are float4 along a row of V; each write is 16 bytes, eight
+// positions of one row of VT (ldv is a multiple of 8, so a chunk never passes
+// the row's end; positions past rows are written as zeros).
 __global__ void __launch_bounds__(256) v_to_f16t_kernel(const float* __restrict__ V, int rows, int cols,
                                                         uint16_t* __restrict__ VT, int ldv) {
   __shared__ float tile[64][65];
   const int r0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
-  for (int i = threadIdx.y; i < 64; i += 8)
-    for (int jj = threadIdx.x; jj < 64; jj += 32) {
-      const int r = r0 + i, c = c0 + jj;
-      tile[i][jj] = r < rows && c < cols ? V[(size_t)r * cols + c] : 0.f;
-    }
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int rr = (tid >> 4) + 16 * i, cc = 4 * (tid & 15);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r0 + rr < rows) v = __ldg(reinterpret_cast<const float4*>(V + (size_t)(r0 + rr) * cols + c0 + cc));
+    tile[rr][cc] = v.x;
+    tile[rr][cc + 1] = v.y;
+    tile[rr][cc + 2] = v.z;
+    tile[rr][cc + 3] = v.w;
+  }
   __syncthreads();
-  for (int i = threadIdx.y; i < 64; i += 8)
-    for (int jj = threadIdx.x; jj < 64; jj += 32) {
-      const int c = c0 + i, r = r0 + jj;
-      if (c < cols && r < rows) VT[(size_t)c * ldv + r] = __half_as_ushort(__float2half_rn(tile[jj][i]));
-    }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int cc = (tid >> 3) + 32 * i, rc = 8 * (tid & 7);
+    if (r0 + rc >= rows) continue;
+    uint4 o;
+    o.x = pack_half2(tile[rc][cc], tile[rc + 1][cc]);
+    o.y = pack_half2(tile[rc + 2][cc], tile[rc + 3][cc]);
+    o.z = pack_half2(tile[rc + 4][cc], tile[rc + 5][cc]);
+    o.w = pack_half2(tile[rc + 6][cc], tile[rc + 7][cc]);
+    *reinterpret_cast<uint4*>(VT + (size_t)(c0 + cc) * ldv + r0 + rc) = o;
+  }
 }
 
 __global__ void __launch_bounds__(A_THREADS, 1)
@@ -398,7 +412,7 @@ int launch_prefill_attention(const float* Q, const float* K, const float* V, flo
   // the fp16 copies of the cache rows 0 .. pos0 + T - 1
   cudaError_t e = launch_x_to_f16(K, K16, rows * kv_dim, s);
   if (e != cudaSuccess) return cuda_fail(e, "K to fp16");
-  v_to_f16t_kernel<<<dim3((unsigned)((rows + 63) / 64), (unsigned)(kv_dim / 64)), dim3(32, 8), 0, s>>>(
+  v_to_f16t_kernel<<<dim3((unsigned)((rows + 63) / 64), (unsigned)(kv_dim / 64)), 256, 0, s>>>(
       V, (int)rows, (int)kv_dim, VT16, (int)ldv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "V to fp16 (transposed)");
