@@ -35,8 +35,9 @@
  * copy of X for the GEMM path (T*k*2 bytes), and, for the tensor-core GEMV
  * (T = 3 or 4, or T = 2 on weights of 2^25 or more elements), ticket counters
  * and partial sums (64 KiB plus 2 KiB per 128 weight rows and per SM, at
- * most). Calls on one stream share their stream's buffers, which are ordered
- * by the stream. A buffer grows on demand with cudaMalloc (also during a
+ * most), and, for apr_prefill_attention, the fp16 copies of the K and V
+ * cache rows it reads. Calls on one stream share their stream's buffers,
+ * which are ordered by the stream. A buffer grows on demand with cudaMalloc (also during a
  * stream capture: the calling thread's capture mode is relaxed for that
  * call) and is never freed while the process runs; a grown buffer replaces
  * the old one for later calls and the old one is kept. A graph captured from
@@ -305,11 +306,13 @@ int apr_ffn_sublayer(const apr_ffn_args* args);
  *   head_dim   256 (the only size the fused form takes)
  * q, k and v enter the products rounded to fp16; the result is within fp16
  * input rounding of the exact attention (the tests bound it). All pointers
- * 16-byte aligned, caller owned; no scratch, no allocation. Errors:
- * APR_E_INVAL for negative sizes, num_heads not a multiple of num_kv_heads,
- * head_dim != 256, sizes past 2^30 positions, or a null pointer with T > 0;
- * APR_E_ALIGN; APR_E_ALIAS if out overlaps Q or a cache; APR_E_DEVICE;
- * APR_E_LAUNCH. Asynchronous on the stream; apr_stream_status reports a
+ * 16-byte aligned, caller owned. Scratch per stream as for apr_qgemm: the
+ * fp16 copies of the cache rows 0 .. pos0 + T - 1 that the call makes, K as
+ * it is and V transposed (4 * (pos0 + T) * num_kv_heads * 256 bytes, plus
+ * padding). Errors: APR_E_INVAL for negative sizes, num_heads not a multiple
+ * of num_kv_heads, head_dim != 256, sizes past 2^30 positions, or a null
+ * pointer with T > 0; APR_E_ALIGN; APR_E_ALIAS if out overlaps Q or a cache;
+ * APR_E_NOMEM; APR_E_DEVICE; APR_E_LAUNCH. Asynchronous on the stream; apr_stream_status reports a
  * bounded wait that gave up (out is then unspecified).
  */
 int apr_prefill_attention(const float* Q, const float* K_cache, const float* V_cache, float* out, int T, int pos0,
