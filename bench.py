@@ -13,7 +13,9 @@ step), the roofline of the dominant kernel (the GEMM, timed alone with CUDA
 events through ``apr_qgemm_f16_in``), the end-to-end throughput through the
 same public call with host buffers (pinned X and R copied in, Y copied out,
 every step), the CPU oracle's throughput on the host cores, and the SM clocks
-sampled during the timed region.
+sampled during the timed region. Beside them, for the rest of the path: the
+T = 1 GEMV (GB/s), the FFN sublayer, the GEMM at 2048 rows, and the causal
+prefill attention of the 9B layer at 512 and 2048 rows (TFLOP/s).
 
 ``--impl reference`` times the CPU oracle (there is no other implementation
 of this path to run) on the same workload, a bounded sample of W rows per

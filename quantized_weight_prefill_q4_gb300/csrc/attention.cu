@@ -10,10 +10,10 @@
 // qwen35_attention_pass: scores GEMM, causal mask and softmax, value GEMM per
 // KV group) fixes the layouts, the mask and the head grouping.
 //
-// Before the kernel, the K and V rows 0 .. pos0 + T - 1 of the KV head pairs
+// Before the kernel, the K and V cache rows 0 .. pos0 + T - 1 (every KV head)
 // are converted to fp16 into the stream's scratch: K as it is
 // ([positions][num_kv_heads * 256]), V transposed ([num_kv_heads * 256]
-// [positions]), so that both operands of the two products are K-major tiles
+// [positions, rounded up to 8]), so that both operands of the two products are K-major tiles
 // that TMA copies straight into the 128-byte-swizzled MMA layout.
 //
 // One CTA per (128 query rows, query head); the CTAs of the last query rows,
