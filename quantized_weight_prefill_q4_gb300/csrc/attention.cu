@@ -85,6 +85,17 @@ constexpr uint32_t A_TMEM_COLS = 512;
 constexpr float kRescaleAbove = 8.0f;            // log2 of the largest weight kept unscaled
 static_assert(A_SMEM <= 232448, "shared memory budget");
 
+// D[tmem] (+)= A[smem] . B[smem]^T: both operands K-major in shared memory
+// (128-byte swizzle descriptors, smem_desc_sw128), fp32 accumulate.
+__device__ __forceinline__ void mma_f16_ss_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

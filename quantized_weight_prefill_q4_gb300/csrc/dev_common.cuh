@@ -237,17 +237,6 @@ __device__ __forceinline__ void mma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tme
       : "memory");
 }
 
-// D[tmem] (+)= A[smem] . B[smem]^T: both operands K-major in shared memory
-// (descriptors as for B above), fp32 accumulate.
-__device__ __forceinline__ void mma_f16_ss_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                                 uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Arrives once on `bar` when every tcgen05.mma issued so far by the elected
 // lane has completed (elect.sync picks the same lane of a converged warp).
 __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
