@@ -302,7 +302,8 @@ int apr_ffn_sublayer(const apr_ffn_args* args);
  *              never read
  *   out        [T][num_heads * head_dim] fp32, overwritten
  *   T          query rows (0: no-op); pos0 >= 0 their first position
- *   num_heads  a multiple of num_kv_heads (grouped-query attention)
+ *   num_heads  a multiple of num_kv_heads (grouped-query attention);
+ *              num_heads <= 65536, num_kv_heads <= 16383
  *   head_dim   256 (the only size the fused form takes)
  * q, k and v enter the products rounded to fp16; the result is within fp16
  * input rounding of the exact attention (the tests bound it). All pointers

@@ -483,8 +483,10 @@ int apr_prefill_attention(const float* Q, const float* K_cache, const float* V_c
   if (num_heads % num_kv_heads != 0)
     return fail(APR_E_INVAL, "num_heads (%d) must be a multiple of num_kv_heads (%d)", num_heads, num_kv_heads);
   if (head_dim != 256) return fail(APR_E_INVAL, "head_dim must be 256 (got %d)", head_dim);
+  // positions, the widths of Q and of the caches (the V transpose runs one
+  // grid row per 64 cache columns), and the attention grid
   if ((long long)pos0 + T > (1LL << 30) || (long long)num_heads * 256 > (1LL << 24) ||
-      (long long)((T + 127) / 128) * num_heads > 0x7FFFFFFFLL)
+      (long long)num_kv_heads * 256 / 64 > 65535 || (long long)((T + 127) / 128) * num_heads > 0x7FFFFFFFLL)
     return fail(APR_E_INVAL, "sizes beyond the supported limits");
   if (T == 0) return APR_OK;
   if (!Q || !K_cache || !V_cache || !out) return fail(APR_E_INVAL, "null pointer");

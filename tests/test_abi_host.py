@@ -195,6 +195,7 @@ def test_prefill_attention_argument_errors(q):
     assert rc(nh=6, nkv=4) == -1             # not a multiple
     assert rc(d=128) == -1                   # the fused form takes head_dim 256
     assert rc(pos0=(1 << 30)) == -1          # past the supported positions
+    assert rc(T=1, nh=16384, nkv=16384) == -1  # cache rows wider than the transpose grid takes
     assert rc(Q=None) == -1
     assert rc(O=None) == -1
     assert rc(K=Kp + 4) == -3                # misaligned
