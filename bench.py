@@ -417,7 +417,7 @@ def run_ours(args):
         gemv_big = gemv_rate(q, synth, dev, stream, peak_gbs, n=12288, k=4096)
         ffn = ffn_rate(q, synth, dev, stream)
         big = gemm_kernel_rate(q, synth, dev, stream, peak_tf, T=2048)
-        attn = {f"t{t}": attention_rate(q, synth, dev, stream, peak_tf, T=t) for t in (512, 2048)}
+        attn = {f"t{t}": attention_rate(q, synth, dev, stream, peak_tf, peak_gbs, T=t) for t in (512, 2048)}
 
     # ---- end to end: host buffers, copies inside the timed region
     e2e_steps = max(20, min(args.steps, 200))
@@ -562,11 +562,22 @@ def ffn_rate(q, synth, dev, stream, hidden=4096, inter=12288, T=512):
             "launches_per_call": 4}
 
 
-def attention_rate(q, synth, dev, stream, peak_tf, T=2048, pos0=0, nh=16, nkv=4):
+def attention_work(T, pos0, nh, nkv, d=256):
+    """Algorithmic work of one prefill-attention call: the two products over
+    the visible (row, key) pairs, 4 * d * heads * sum_t (pos0 + t + 1) flops,
+    and the bytes the method must move, Q in and O out ([T][heads * d] f32)
+    and the K and V cache rows 0 .. pos0 + T - 1 ([.][kv_heads * d] f32)."""
+    flop = 4.0 * d * nh * (T * (T + 1) / 2 + pos0 * T)
+    byts = 4 * (2 * T * nh * d + 2 * (pos0 + T) * nkv * d)
+    return flop, byts
+
+
+def attention_rate(q, synth, dev, stream, peak_tf, peak_gbs, T=2048, pos0=0, nh=16, nkv=4):
     """Causal prefill attention of a 9B-class layer (16 query heads over 4 KV
     heads, head_dim 256) on a chunk of T rows at pos0, rotating input sets
     (more than L2 in all). TFLOP/s counts the two products over the visible
-    (row, key) pairs only: 4 * 256 * heads * sum_t (pos0 + t + 1)."""
+    (row, key) pairs only; frac_roofline = the larger of the flop time at the
+    tensor peak and the byte time at the HBM rate, over the measured time."""
     import torch
 
     d = 256
@@ -588,9 +599,11 @@ def attention_rate(q, synth, dev, stream, peak_tf, T=2048, pos0=0, nh=16, nkv=4)
     reps = 200
     dt = timed_calls([call(x) for x in sets], reps, stream) / reps
     q.apr_stream_status(stream)
-    flop = 4.0 * d * nh * (T * (T + 1) / 2 + pos0 * T)
+    flop, byts = attention_work(T, pos0, nh, nkv, d)
     tf = flop / dt / 1e12
+    t_flop, t_byte = flop / (peak_tf * 1e12), byts / (peak_gbs * 1e9)
     return {"workload": f"attention_h{nh}_kv{nkv}_d{d}_t{T}_pos{pos0}", "TFLOP/s": tf, "frac": tf / peak_tf,
+            "bound": "tensor" if t_flop >= t_byte else "hbm", "frac_roofline": max(t_flop, t_byte) / dt,
             "us": dt * 1e6}
 
 

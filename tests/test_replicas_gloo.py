@@ -56,3 +56,18 @@ def test_reference_arm_runs_on_cpu(capsys):
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_attention_work_counts_visible_pairs():
+    import bench
+
+    # brute force: every (row, key) pair with key <= pos0 + row, two products of
+    # d multiply-adds each per head
+    T, pos0, nh, nkv, d = 5, 3, 4, 2, 8
+    pairs = sum(1 for t in range(T) for j in range(pos0 + T) if j <= pos0 + t)
+    flop, byts = bench.attention_work(T, pos0, nh, nkv, d)
+    assert flop == 2 * 2 * d * nh * pairs
+    assert byts == 4 * (T * nh * d * 2 + (pos0 + T) * nkv * d * 2)
+    # the 9B chunk of 2048 rows: 34.4 GFLOP against 83.9 MB
+    flop, byts = bench.attention_work(2048, 0, 16, 4)
+    assert round(flop / 1e9, 1) == 34.4 and round(byts / 1e6, 1) == 83.9
