@@ -516,3 +516,12 @@ def test_attention_f16_input_mode_rounds_q_k_and_v():
     np.testing.assert_array_equal(
         oracle.prefill_attention_f16_inputs_f64(c["Q"], c["K"], c["V"], 3, 1, 2, 1, 8),
         oracle.prefill_attention_f64(r(c["Q"]), r(c["K"]), r(c["V"]), 3, 1, 2, 1, 8))
+
+
+def test_attention_sampled_rows_equal_the_full_result():
+    # the full-size GPU tests compare sampled rows: computing only those rows
+    # (fewer keys gathered) must give exactly the full computation's rows
+    c = synth.attention_case(9, 4, 4, 2, 8, seed=13)
+    full = _attn(c)
+    rows = np.array([8, 0, 3, 3, 5])
+    np.testing.assert_allclose(_attn(c, rows=rows), full[rows], rtol=1e-13, atol=1e-15)
