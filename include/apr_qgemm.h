@@ -215,7 +215,9 @@ int apr_qgemm_f16_in(int qtype, const void* W, const void* Wu, int n, int k, con
  * exits.
  *   - T*k > APR_NOALLOC_MAX_TK or k % 256 != 0: APR_E_INVAL with a message.
  *   - The first call on each device looks up the scratch's device address (and
- *     checks the device); make that first call before any stream capture.
+ *     checks the device); make that first call before any stream capture. A
+ *     lookup that fails returns APR_E_DEVICE and is tried again by the next
+ *     call; once it has succeeded it is kept for the process.
  *   - Every call shares the one array, which keeps the last call's contents
  *     (each call overwrites the T*k values it reads, so nothing needs
  *     clearing). Calls whose work overlaps on the GPU (on different streams,
@@ -334,6 +336,19 @@ int apr_dequant(int qtype, const void* W, int n, int k, float* out, apr_stream_t
  * call, or APR_E_LAUNCH if the stream reported a CUDA error.
  */
 int apr_stream_status(apr_stream_t stream);
+
+/*
+ * Test of the failure detection (the pages have no counterpart): enqueues one
+ * kernel that waits on an mbarrier nothing arrives on, through the same
+ * bounded wait every kernel of the library uses, with a limit of limit_us
+ * microseconds (1 .. 1000000; APR_E_INVAL otherwise) instead of the library's
+ * 2 s. The wait runs out, the kernel records the timeout in the device status
+ * word and returns: no trap, no fault, the context stays usable. After it,
+ * apr_stream_status on the stream returns APR_E_TIMEOUT (and clears the
+ * word), and the library's calls on that stream work as before. Errors:
+ * APR_E_INVAL, APR_E_DEVICE, APR_E_LAUNCH.
+ */
+int apr_test_bounded_wait(unsigned limit_us, apr_stream_t stream);
 
 /* Message of the last failed call on this thread ("" if none). */
 const char* apr_last_error(void);

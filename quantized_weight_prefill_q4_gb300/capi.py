@@ -52,6 +52,7 @@ EXPORTS = (
     "apr_prefill_attention",
     "apr_dequant",
     "apr_stream_status",
+    "apr_test_bounded_wait",
     "apr_last_error",
 )
 
@@ -117,6 +118,7 @@ def _load() -> ctypes.CDLL:
         "apr_prefill_attention": ([vp, vp, vp, vp, ci, ci, ci, ci, ci, vp], ci),
         "apr_dequant": ([ci, vp, ci, ci, vp, vp], ci),
         "apr_stream_status": ([vp], ci),
+        "apr_test_bounded_wait": ([ctypes.c_uint, vp], ci),
         "apr_last_error": ([], ctypes.c_char_p),
     }
     for name, (args, res) in sig.items():
@@ -342,3 +344,10 @@ def apr_dequant(qtype, W, n, k, out, stream=None) -> int:
 
 def apr_stream_status(stream=None) -> int:
     return _check(_lib.apr_stream_status(_stream(stream)))
+
+
+def apr_test_bounded_wait(limit_us, stream=None) -> int:
+    """Enqueues the failure-detection test kernel (a bounded wait that runs
+    out after limit_us microseconds); apr_stream_status then reports the
+    timeout."""
+    return _check(_lib.apr_test_bounded_wait(int(limit_us), _stream(stream)))

@@ -527,6 +527,15 @@ int apr_dequant(int qtype, const void* W, int n, int k, float* out, apr_stream_t
   return launched(launch_dequant(qtype, W, n, k, out, (cudaStream_t)stream), "dequant");
 }
 
+int apr_test_bounded_wait(unsigned limit_us, apr_stream_t stream) {
+  t_msg[0] = 0;
+  if (limit_us < 1 || limit_us > 1000000) return fail(APR_E_INVAL, "limit_us must be in [1, 1000000] (got %u)", limit_us);
+  DeviceState* st = nullptr;
+  const int rc = device_state(&st);
+  if (rc != APR_OK) return rc;
+  return launched(launch_bounded_wait(1000ull * limit_us, st->status, (cudaStream_t)stream), "bounded_wait");
+}
+
 int apr_stream_status(apr_stream_t stream) {
   t_msg[0] = 0;
   DeviceState* st = nullptr;

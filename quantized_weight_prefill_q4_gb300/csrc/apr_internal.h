@@ -94,6 +94,10 @@ int launch_gemm_tc(const GemmPlan& plan, int qtype, const void* W, const void* W
                    int T, float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg,
                    size_t msg_len, bool after_conversion);
 
+// A kernel that waits (bounded, limit_ns) on an mbarrier nothing arrives on,
+// then records the timeout in the status word and returns (selftest.cu).
+cudaError_t launch_bounded_wait(unsigned long long limit_ns, unsigned* status, cudaStream_t s);
+
 // Shared with the allocation-free entry point (api.cu): sets this thread's error
 // message and returns `code`; checks the arguments of a plain / residual GEMM
 // call (APR_OK, an error, or 1 for "nothing to do"); device address of the

@@ -55,23 +55,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity of `bar` has completed. Gives up
-// when *abort becomes nonzero (another role gave up) or after kWaitLimitNs, in
+// when *abort becomes nonzero (another role gave up) or after limit_ns, in
 // which case it sets the status bit and *abort. Returns false if it gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          unsigned* status) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              unsigned* status, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (global_ns() - t0 > limit_ns) {
         *abort = 1;
         atomicOr(status, kStatusTimeout);
         return false;
       }
     }
   }
+}
+
+// The kernels' bounded wait: mbar_wait_for with the library's limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          unsigned* status) {
+  return mbar_wait_for(bar, parity, abort, status, kWaitLimitNs);
 }
 
 // ---------------------------------------------------------------- cluster

@@ -12,6 +12,7 @@
 // loaded on a device and lives until the process exits, and no call here
 // allocates or frees device memory.
 
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -31,17 +32,19 @@ constexpr size_t kNoAllocScratchElems = size_t(APR_NOALLOC_MAX_TK);
 __device__ __align__(256) uint16_t g_noalloc_x16[kNoAllocScratchElems];
 
 struct NoAllocDevice {
-  std::once_flag once;
-  int rc = APR_E_DEVICE;
+  std::atomic<bool> ready{false};
   uint16_t* scratch = nullptr;  // device address of g_noalloc_x16
   unsigned* status = nullptr;   // device address of the library's status word
 };
 NoAllocDevice g_na[64];
+std::mutex g_na_mu;
 
-// Once per device, with that device current: check it, then look up the device
+// Per device, with that device current: check it, then look up the device
 // addresses of the scratch array and of the status word. In host code the
 // array's name only stands in for the symbol; the kernels need the address
-// cudaGetSymbolAddress returns.
+// cudaGetSymbolAddress returns. Only a successful lookup is kept: a failed
+// one (for instance made during a stream capture, which the header warns
+// against) is tried again on the next call.
 int setup(NoAllocDevice** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
@@ -49,24 +52,27 @@ int setup(NoAllocDevice** out) {
     return set_error(APR_E_DEVICE, "no usable CUDA device");
   }
   NoAllocDevice& st = g_na[dev];
-  std::call_once(st.once, [&st, dev] {
-    cudaDeviceProp prop;
-    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess || prop.major != 10 || prop.minor != 3) {
-      cudaGetLastError();
-      return;
+  if (!st.ready.load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_na_mu);
+    if (!st.ready.load(std::memory_order_relaxed)) {
+      cudaDeviceProp prop;
+      if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess || prop.major != 10 || prop.minor != 3) {
+        cudaGetLastError();
+        return set_error(APR_E_DEVICE, "device is not a compute capability 10.3 GPU (GB300)");
+      }
+      void* p = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_x16);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        return set_error(APR_E_DEVICE, "looking up the fixed scratch failed (retried on the next call)");
+      }
+      unsigned* status = status_word_address();
+      if (!status) return set_error(APR_E_DEVICE, "looking up the status word failed (retried on the next call)");
+      st.scratch = static_cast<uint16_t*>(p);
+      st.status = status;
+      st.ready.store(true, std::memory_order_release);
     }
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_x16) != cudaSuccess) {
-      cudaGetLastError();
-      return;
-    }
-    st.scratch = static_cast<uint16_t*>(p);
-    st.status = status_word_address();
-    if (!st.status) return;
-    st.rc = APR_OK;
-  });
-  if (st.rc != APR_OK)
-    return set_error(APR_E_DEVICE, "device is not a compute capability 10.3 GPU, or its scratch symbol failed");
+  }
   *out = &st;
   return APR_OK;
 }

@@ -21,4 +21,6 @@ from .gen import (  # noqa: F401
     make_case,
     attention_case,
     WORKLOADS,
+    SCALE_CLASSES,
+    random_blocks,
 )

@@ -110,6 +110,45 @@ def activations(rows: int, cols: int, seed: int, sigma: float = 1.0) -> np.ndarr
     return (rng.standard_normal((rows, cols)) * sigma).astype(np.float32)
 
 
+# Scale classes of ``random_blocks``: ranges of the fp16 exponent field of d
+# (0 = subnormal). Every class draws both signs and random mantissas.
+SCALE_CLASSES = {
+    "subnormal": (0, 0),      # |d| in [2^-24, 2^-14)
+    "small": (1, 5),          # [2^-14, 2^-9)
+    "typical": (6, 12),       # [2^-9, 2^-2), where quantized model weights sit
+    "large": (16, 30),        # [2, 65504], capped by fp16_range below
+    "mixed": (0, 30),         # every finite exponent, block by block
+}
+
+
+def random_blocks(qtype: int, n: int, k: int, seed: int, scale_class: str = "mixed",
+                  fp16_range: bool = False) -> np.ndarray:
+    """Arbitrary GGUF blocks ``[n][k/32*bytes]``: uniformly random payload bytes
+    (every Q4_0 nibble 0..15, every Q8_0 code -128..127) and fp16 scales of both
+    signs whose exponent field is uniform over the class's range (random
+    mantissa; the subnormal class has a nonzero mantissa). Scales are finite.
+
+    ``fp16_range``: cap |d| so that |d * q| stays within fp16's largest finite
+    value 65504 for every code (|q| <= 8 for Q4_0, 128 for Q8_0): the scale's
+    exponent field is at most 27 (Q4_0) or 23 (Q8_0), which with any mantissa
+    gives |d| <= 8188 or 511.75.
+    """
+    lo, hi = SCALE_CLASSES[scale_class]
+    if fp16_range:
+        hi = min(hi, 27 if qtype == Q4_0 else 23)
+    rng = np.random.default_rng(seed)
+    bb = block_bytes(qtype)
+    raw = rng.integers(0, 256, size=(n, k // BLOCK_ELEMS, bb), dtype=np.uint8)
+    exp = rng.integers(lo, hi + 1, size=(n, k // BLOCK_ELEMS)).astype(np.uint16)
+    man = rng.integers(0, 1024, size=(n, k // BLOCK_ELEMS)).astype(np.uint16)
+    man = np.where(exp == 0, np.maximum(man, 1), man)
+    sign = rng.integers(0, 2, size=(n, k // BLOCK_ELEMS)).astype(np.uint16)
+    bits = (sign << 15) | (exp << 10) | man
+    raw[..., 0] = (bits & 0xFF).astype(np.uint8)
+    raw[..., 1] = (bits >> 8).astype(np.uint8)
+    return raw.reshape(n, -1)
+
+
 def make_case(qtype: int, n: int, k: int, T: int, *, residual: bool = False,
               gate_up: bool = False, seed: int = 0) -> dict:
     """One seeded problem: quantized ``W`` (and ``Wu`` for a gate/up pair), ``X``, ``R``.

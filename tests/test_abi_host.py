@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(q):
     names = declared_functions()
-    assert len(names) == 14, names
+    assert len(names) == 15, names
     lib = q.library()
     for name in names:
         assert hasattr(lib, name), name
@@ -119,6 +119,17 @@ def test_valid_call_without_gpu_reports_device(q):
     assert call(q, 2, A, 64, 64, 2 * A, 8, 3 * A, 3 * A, None) == -5
     assert "device" in q.apr_last_error()
     assert q.library().apr_stream_status(None) == -5
+
+
+def test_bounded_wait_test_entry_checks_its_limit(q):
+    import torch
+
+    lib = q.library()
+    assert lib.apr_test_bounded_wait(0, None) == q.APR_E_INVAL
+    assert lib.apr_test_bounded_wait(1000001, None) == q.APR_E_INVAL
+    assert "limit_us" in q.apr_last_error()
+    if not torch.cuda.is_available():
+        assert lib.apr_test_bounded_wait(1000, None) == q.APR_E_DEVICE
 
 
 def test_binding_rejects_host_tensors(q):

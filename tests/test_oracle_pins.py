@@ -525,3 +525,119 @@ def test_attention_sampled_rows_equal_the_full_result():
     full = _attn(c)
     rows = np.array([8, 0, 3, 3, 5])
     np.testing.assert_allclose(_attn(c, rows=rows), full[rows], rtol=1e-13, atol=1e-15)
+
+
+# ---------------------------------------------------------------- fp16-input modes
+# The fp16-input modes round X (or q, k, v) and the decoded weight to fp16,
+# round to nearest even, then compute exactly. Pinned by hand-rounded values
+# (which fix fp16 rather than bf16, and nearest-even rather than truncation),
+# and by equality with the float64 oracle when every operand is already an
+# fp16 value (the modes may then change nothing).
+def _q4_block(d_bits, nibbles):
+    """One Q4_0 block, element j's nibble nibbles[j] (j < 32)."""
+    b = bytearray(struct.pack("<H", d_bits))
+    b += bytes((nibbles[j] & 0xF) | ((nibbles[j + 16] & 0xF) << 4) for j in range(16))
+    return np.frombuffer(bytes(b), dtype=np.uint8).reshape(1, 18)
+
+
+ONE_PLUS = 1.0 + 2.0 ** -11 + 2.0 ** -20   # fp16: 1 + 2^-10 (bf16 and truncation give 1)
+
+
+@pytest.mark.parametrize("x,want", [
+    (ONE_PLUS, 1.0 + 2.0 ** -10),
+    (1.0 + 2.0 ** -11, 1.0),                  # tie, the even neighbour is 1
+    (1.0 + 3 * 2.0 ** -11, 1.0 + 2.0 ** -9),  # tie, the even neighbour is above
+    (-ONE_PLUS, -(1.0 + 2.0 ** -10)),
+])
+def test_f16_mode_rounds_x_to_nearest_even_fp16(x, want):
+    W = _q4_block(0x3C00, [9] + [8] * 31)     # d = 1, w_0 = 1, the rest 0
+    X = np.zeros((1, 32), np.float32)
+    X[0, 0] = x
+    assert oracle.qgemm_f16_inputs_f64(synth.Q4_0, W, 1, 32, X)[0, 0] == want
+
+
+def test_f16_mode_rounds_the_decoded_weight():
+    # d = 1 + 2^-10 (0x3C01), nibble 11 (q' = 3): w = 3 + 3 * 2^-10 lies halfway
+    # between the fp16 values 3 + 2^-9 (odd mantissa 513) and 3 + 2^-8 (even,
+    # 514); nearest even gives 3 + 2^-8. The residual is added unrounded.
+    W = _q4_block(0x3C01, [11] + [8] * 31)
+    X = np.zeros((1, 32), np.float32)
+    X[0, 0] = 1.0
+    R = np.array([[2.0 ** -30]], np.float32)
+    assert oracle.qgemm_f16_inputs_f64(synth.Q4_0, W, 1, 32, X)[0, 0] == 3.0 + 2.0 ** -8
+    assert oracle.qgemm_f64(synth.Q4_0, W, 1, 32, X)[0, 0] == 3.0 + 3 * 2.0 ** -10
+    assert oracle.qgemm_f16_inputs_f64(synth.Q4_0, W, 1, 32, X, R)[0, 0] == 3.0 + 2.0 ** -8 + 2.0 ** -30
+
+
+def _fp16_exact_case(seed, n, k, T):
+    """Q4_0 weights whose decoded values are fp16 values (scales with at most 7
+    significant bits times codes of at most 4) and fp16-valued activations."""
+    rng = np.random.default_rng(seed)
+    raw = rng.integers(0, 256, size=(n, k // 32, 18), dtype=np.uint8)
+    man = (rng.integers(0, 8, size=(n, k // 32)) << 7).astype(np.uint16)  # 3 fraction bits
+    exp = rng.integers(5, 20, size=(n, k // 32)).astype(np.uint16)
+    sign = rng.integers(0, 2, size=(n, k // 32)).astype(np.uint16)
+    bits = (sign << 15) | (exp << 10) | man
+    raw[..., 0] = (bits & 0xFF).astype(np.uint8)
+    raw[..., 1] = (bits >> 8).astype(np.uint8)
+    X = synth.activations(T, k, seed + 1).astype(np.float16).astype(np.float32)
+    return raw.reshape(n, -1), X
+
+
+def test_f16_mode_equals_the_exact_oracle_on_fp16_operands():
+    n, k, T = 6, 128, 4
+    W, X = _fp16_exact_case(31, n, k, T)
+    Wf = oracle.dequant_f64(synth.Q4_0, W, n, k)
+    assert np.array_equal(Wf, Wf.astype(np.float16).astype(np.float64))  # the case is what it claims
+    R = synth.activations(T, n, 33)
+    np.testing.assert_array_equal(oracle.qgemm_f16_inputs_f64(synth.Q4_0, W, n, k, X, R),
+                                  oracle.qgemm_f64(synth.Q4_0, W, n, k, X, R))
+    W2, _ = _fp16_exact_case(32, n, k, T)
+    np.testing.assert_array_equal(oracle.gate_up_swiglu_f16_inputs_f64(synth.Q4_0, W, W2, n, k, X),
+                                  oracle.gate_up_swiglu_f64(synth.Q4_0, W, W2, n, k, X))
+    # and a perturbation below fp16's resolution changes nothing in the mode
+    Xp = (X.astype(np.float64) * (1.0 + 2.0 ** -14)).astype(np.float32)
+    np.testing.assert_array_equal(oracle.qgemm_f16_inputs_f64(synth.Q4_0, W, n, k, Xp),
+                                  oracle.qgemm_f64(synth.Q4_0, W, n, k, X))
+
+
+def test_f16_swiglu_mode_hand_value():
+    # gate and up both w_0 = 1; x_0 rounds to g = u = 1 + 2^-10 in fp16
+    W = _q4_block(0x3C00, [9] + [8] * 31)
+    X = np.zeros((1, 32), np.float32)
+    X[0, 0] = ONE_PLUS
+    g = 1.0 + 2.0 ** -10
+    want = g / (1.0 + math.exp(-g)) * g
+    got = oracle.gate_up_swiglu_f16_inputs_f64(synth.Q4_0, W, W, 1, 32, X)[0, 0]
+    assert abs(got - want) <= 1e-15 * want
+    x = float(np.float32(ONE_PLUS))
+    unrounded = x / (1.0 + math.exp(-x)) * x
+    assert abs(got - unrounded) > 1e-4  # the rounding is visible
+
+
+def test_f16_attention_mode_hand_values():
+    d = 4
+    # one visible key (position 0): the output is fp16(v_0)
+    Q = np.array([[ONE_PLUS, 0, 0, 0]], np.float32)
+    K = np.array([[0.5, 0, 0, 0]], np.float32)
+    V = np.array([[ONE_PLUS, -ONE_PLUS, 1.0 + 2.0 ** -11, 2.0]], np.float32)
+    out = oracle.prefill_attention_f16_inputs_f64(Q, K, V, 1, 0, 1, 1, d)
+    np.testing.assert_array_equal(out[0], [1.0 + 2.0 ** -10, -(1.0 + 2.0 ** -10), 1.0, 2.0])
+    # two keys: k_0 = 0, k_1 = (2, 0, 0, 0); the score of key 1 is
+    # fp16(q_0) * 2 / sqrt(4) = 1 + 2^-10, of key 0 zero; v_0 = 0 and
+    # v_1 = (1 + 3 * 2^-11) -> 1 + 2^-9
+    Q = np.array([[ONE_PLUS, 0, 0, 0]], np.float32)
+    K = np.array([[0, 0, 0, 0], [2, 0, 0, 0]], np.float32)
+    V = np.array([[0, 0, 0, 0], [1.0 + 3 * 2.0 ** -11, 0, 0, 0]], np.float32)
+    out = oracle.prefill_attention_f16_inputs_f64(Q, K, V, 1, 1, 1, 1, d)
+    s = 1.0 + 2.0 ** -10
+    want = math.exp(s) / (1.0 + math.exp(s)) * (1.0 + 2.0 ** -9)
+    assert abs(out[0, 0] - want) <= 1e-15 * want
+    np.testing.assert_array_equal(out[0, 1:], [0.0, 0.0, 0.0])
+
+
+def test_f16_attention_mode_equals_the_exact_oracle_on_fp16_operands():
+    c = synth.attention_case(5, 3, 4, 2, 8, seed=14)
+    r = {key: c[key].astype(np.float16).astype(np.float32) for key in ("Q", "K", "V")}
+    np.testing.assert_array_equal(oracle.prefill_attention_f16_inputs_f64(r["Q"], r["K"], r["V"], 5, 3, 4, 2, 8),
+                                  oracle.prefill_attention_f64(r["Q"], r["K"], r["V"], 5, 3, 4, 2, 8))

@@ -48,6 +48,52 @@ def test_noalloc_matches_pooled_entry_on_two_calls_in_a_row(q):
         assert_f16_leg(y, oracle.qgemm_f64(c["qtype"], c["W"], n, k, c["X"], c["R"]))
 
 
+def test_noalloc_allocates_nothing_on_a_new_stream(q):
+    """On a stream the library has not seen, a call of the pooled entry point
+    allocates its fp16 scratch (free device memory drops: the measurement
+    sees an allocation), while apr_qgemm_noalloc leaves free memory as it
+    was, on its first call on that stream and on the next."""
+    n, k, T = 256, 1024, 200
+    c = synth.make_case(synth.Q4_0, n, k, T, residual=True, seed=73)
+    W, X, R = dev(c["W"]), dev(c["X"]), dev(c["R"])
+    Y = torch.empty((T, n), device="cuda")
+    # the kernels' modules are loaded by a first call (lazy module loading)
+    assert _noalloc(q, synth.Q4_0, W, n, k, X, T, Y, R) == 0, q.apr_last_error()
+    q.apr_stream_status()
+    s_pooled, s_fixed = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    with torch.cuda.stream(s_pooled):
+        q.apr_qgemm(synth.Q4_0, W, n, k, X, T, Y, R, stream=s_pooled)
+    q.apr_stream_status(s_pooled)
+    free1 = torch.cuda.mem_get_info()[0]
+    assert free1 < free0, "the pooled call on a new stream should have allocated its scratch"
+    with torch.cuda.stream(s_fixed):
+        for _ in range(2):
+            assert _noalloc(q, synth.Q4_0, W, n, k, X, T, Y, R) == 0, q.apr_last_error()
+    q.apr_stream_status(s_fixed)
+    assert torch.cuda.mem_get_info()[0] == free1
+    assert_f16_leg(Y.cpu().numpy(), oracle.qgemm_f64(synth.Q4_0, c["W"], n, k, c["X"], c["R"]))
+
+
+def test_noalloc_at_its_size_limit(q):
+    """T * k exactly APR_NOALLOC_MAX_TK: every element of the fixed array is used."""
+    n, k = 256, 4096
+    T = q.APR_NOALLOC_MAX_TK // k
+    c = synth.make_case(synth.Q4_0, n, k, T, residual=True, seed=74)
+    W, X, R = dev(c["W"]), dev(c["X"]), dev(c["R"])
+    buf, Y = guarded(T, n)
+    assert _noalloc(q, synth.Q4_0, W, n, k, X, T, Y, R) == 0, q.apr_last_error()
+    q.apr_stream_status()
+    check_guards(buf, T, n)
+    Yp = torch.empty((T, n), device="cuda")
+    q.apr_qgemm_ex(synth.Q4_0, W, n, k, X, T, Yp, residual=R, path=q.APR_PATH_GEMM)
+    q.apr_stream_status()
+    y = Y.cpu().numpy()
+    assert_f16_leg(y, Yp.cpu().numpy().astype(np.float64))
+    assert_f16_leg(y, oracle.qgemm_f64(synth.Q4_0, c["W"], n, k, c["X"], c["R"]))
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch(q):
     k = 4096
     T = q.APR_NOALLOC_MAX_TK // k + 1
