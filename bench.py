@@ -49,6 +49,7 @@ os.environ.setdefault("OMP_NUM_THREADS", str(_CORES))
 import numpy as np  # noqa: E402
 
 METRIC = "Q4_0/Q8_0 prefill GEMM TFLOP/s at T=512 (% tensor peak); GEMV GB/s (% HBM)"
+REPEATS = 5  # timed regions of --steps steps; the headline is their median
 WORKLOAD = "q4_0_gemm_residual_n4096_k4096_t512"
 QTYPE, N, K, T = 2, 4096, 4096, 512
 SETS = 8
@@ -376,9 +377,13 @@ def run_ours(args):
     barrier(ws)
     torch.cuda.synchronize()
     timing = "CUDA graph replay"
+    region_s = []
     with ClockSampler(dev.index) as clk:
         try:
-            elapsed = timed_calls([step_call(s) for s in sets], args.steps, stream)
+            # the same K-step region timed REPEATS times; value = the median
+            for _ in range(REPEATS):
+                region_s.append(timed_calls([step_call(s) for s in sets], args.steps, stream))
+            elapsed = float(np.median(region_s))
         except RuntimeError as exc:  # a driver that cannot capture the pooled scratch
             timing = f"direct launches (graph capture failed: {str(exc)[:80]})"
             torch.cuda.synchronize()
@@ -418,6 +423,7 @@ def run_ours(args):
         ffn = ffn_rate(q, synth, dev, stream)
         big = gemm_kernel_rate(q, synth, dev, stream, peak_tf, T=2048)
         attn = {f"t{t}": attention_rate(q, synth, dev, stream, peak_tf, peak_gbs, T=t) for t in (512, 2048)}
+        workloads = {} if args.no_configs else every_workload(q, dev, stream, peak_tf, peak_gbs)
 
     # ---- end to end: host buffers, copies inside the timed region
     e2e_steps = max(20, min(args.steps, 200))
@@ -492,12 +498,16 @@ def run_ours(args):
                     "overlap": "copies in, apr_qgemm and copies out on three streams, 8 device sets",
                     "h2d_bytes_per_step": 2 * T * N * 4, "d2h_bytes_per_step": T * N * 4},
             "gpu_launches": 2 * args.steps,
+            "repeats": {"regions": len(region_s) or 1, "steps_each": args.steps,
+                        "TFLOP/s": [FLOP * args.steps / t / 1e12 for t in region_s],
+                        "note": "value is the median region; gpu_launches counts one region"},
             "clocks": clk.summary(),
             "gemv": gemv,
             "gemv_12288": gemv_big,
             "ffn_sublayer": ffn,
             "gemm_t2048": big,
             "attention": attn,
+            "workloads": workloads,
         }
         if not args.no_cpu:
             line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -506,6 +516,137 @@ def run_ours(args):
         import torch.distributed as dist
 
         dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ every workload
+_HOST = {}
+
+
+def host_weight(qtype, n, k, seed):
+    """Seeded GGUF bytes of an n x k weight (the f32 draw shared by both formats)."""
+    import synth
+
+    key = ("w", qtype, n, k, seed)
+    if key not in _HOST:
+        fk = ("f", n, k, seed)
+        if fk not in _HOST:
+            _HOST[fk] = synth.weight_f32(n, k, seed)
+        _HOST[key] = synth.quantize(qtype, _HOST[fk])
+    return _HOST[key]
+
+
+def host_acts(rows, cols, seed):
+    import synth
+
+    key = ("x", rows, cols, seed)
+    if key not in _HOST:
+        _HOST[key] = synth.activations(rows, cols, seed)
+    return _HOST[key]
+
+
+L2_BYTES = 129 * 2**20
+
+
+def time_per_call(calls, stream, budget_s=0.04, max_reps=2000):
+    """Seconds per call: one graph replay of the rotating calls to estimate,
+    then enough replays for about budget_s of device time."""
+    import torch
+
+    for c in calls:
+        c()
+    torch.cuda.synchronize()
+    est = timed_calls(calls, len(calls), stream) / len(calls)
+    reps = int(min(max_reps, max(2 * len(calls), budget_s / max(est, 1e-7))))
+    return timed_calls(calls, reps, stream) / reps
+
+
+def projection_rate(q, dev, stream, peak_tf, peak_gbs, *, qtype, n, k, T, residual=False, gate_up=False,
+                    leg=0, path=0, seed=0):
+    """One projection through apr_qgemm_ex, timed over rotating input sets whose
+    bytes exceed 2.5x L2 (copies of one seeded set). Algorithmic work: flops
+    2 T n k (x2 for gate/up), bytes = the quantized weight(s) + X + Y (+ R)."""
+    import torch
+
+    bb = 18 if qtype == 2 else 34
+    wbytes = n * (k // 32) * bb * (2 if gate_up else 1)
+    byts = wbytes + 4 * T * k + 4 * T * n * (2 if residual else 1)
+    nsets = int(min(16, max(2, -(-2.5 * L2_BYTES // byts))))
+    W0 = torch.from_numpy(host_weight(qtype, n, k, seed)).to(dev)
+    Wu0 = torch.from_numpy(host_weight(qtype, n, k, seed + 3)).to(dev) if gate_up else None
+    X0 = torch.from_numpy(host_acts(T, k, seed + 1)).to(dev)
+    R0 = torch.from_numpy(host_acts(T, n, seed + 2)).to(dev) if residual else None
+    sets = []
+    for j in range(nsets):
+        sets.append(dict(W=W0 if j == 0 else W0.clone(), Wu=None if Wu0 is None else (Wu0 if j == 0 else Wu0.clone()),
+                         X=X0 if j == 0 else X0.clone(), R=None if R0 is None else (R0 if j == 0 else R0.clone()),
+                         Y=torch.empty((T, n), device=dev)))
+
+    def call(st):
+        return lambda: q.apr_qgemm_ex(qtype, st["W"], n, k, st["X"], T, st["Y"], residual=st["R"], Wu=st["Wu"],
+                                      leg=leg, path=path)
+
+    dt = time_per_call([call(st) for st in sets], stream)
+    q.apr_stream_status(stream)
+    assert bool(torch.isfinite(sets[0]["Y"]).all())
+    flop = 2.0 * T * n * k * (2 if gate_up else 1)
+    t_flop, t_byte = flop / (peak_tf * 1e12), byts / (peak_gbs * 1e9)
+    del sets
+    return {"us": dt * 1e6, "TFLOP/s": flop / dt / 1e12, "GB/s": byts / dt / 1e9,
+            "frac_tensor": t_flop / dt, "frac_hbm": t_byte / dt,
+            "bound": "tensor" if t_flop >= t_byte else "hbm", "frac_roofline": max(t_flop, t_byte) / dt}
+
+
+def every_workload(q, dev, stream, peak_tf, peak_gbs):
+    """Every seeded workload of the path, each through the public entry point
+    (input sets rotating past L2, CUDA graph replay, CUDA events):
+    * the Q8_0 256 x 512 problem with 16 tokens (by the T rule the GEMV; also
+      forced onto the tensor-core GEMM);
+    * fused gate/up SwiGLU 12288 x 4096 then down 4096 x 12288 + residual, 512
+      tokens, Q4_0 and Q8_0;
+    * the small-T GEMV sweep: T in {1, 2, 4, 8, 16} over 4096 x 4096 and
+      12288 x 4096, Q4_0 and Q8_0 (GB/s against the HBM rate);
+    * the T rule: the GEMV against the forced tensor-core GEMM at T = 4..16
+      (Q4_0, both weights), and the GEMM at 24 and 32;
+    * a 9B-class layer's projections (qkv 6144 x 4096, out 4096 x 4096 + R,
+      gate/up 12288 x 4096, down 4096 x 12288 + R, Q4_0) at 512 and 2048 rows
+      on the fp16 leg and the exact-fp32 leg."""
+    import torch
+
+    Q4, Q8 = 2, 8
+    P = lambda **kw: projection_rate(q, dev, stream, peak_tf, peak_gbs, **kw)  # noqa: E731
+    out = {}
+    out["q8_0_n256_k512_t16"] = {"auto (GEMV)": P(qtype=Q8, n=256, k=512, T=16),
+                                 "forced GEMM": P(qtype=Q8, n=256, k=512, T=16, path=2)}
+    for qt, name in ((Q4, "q4_0"), (Q8, "q8_0")):
+        out[f"swiglu_{name}_n12288_k4096_t512"] = P(qtype=qt, n=12288, k=4096, T=512, gate_up=True)
+        out[f"down_{name}_n4096_k12288_t512_res"] = P(qtype=qt, n=4096, k=12288, T=512, residual=True, seed=4)
+    sweep = {}
+    for qt, name in ((Q4, "q4_0"), (Q8, "q8_0")):
+        for n, k in ((4096, 4096), (12288, 4096)):
+            for T in (1, 2, 4, 8, 16):
+                r = P(qtype=qt, n=n, k=k, T=T)
+                sweep[f"{name}_n{n}_k{k}_t{T}"] = {key: r[key] for key in ("us", "GB/s", "frac_hbm", "TFLOP/s")}
+    out["gemv_sweep"] = sweep
+    rule = {}
+    for n in (4096, 12288):
+        for T in (4, 8, 12, 16, 24, 32):
+            row = {"gemm_us": P(qtype=Q4, n=n, k=4096, T=T, path=2)["us"]}
+            if T <= 16:
+                row["gemv_us"] = P(qtype=Q4, n=n, k=4096, T=T, path=1)["us"]
+            rule[f"q4_0_n{n}_k4096_t{T}"] = row
+    out["t_rule"] = rule
+    layer = {}
+    for T in (512, 2048):
+        for leg, lname in ((0, "f16"), (1, "exact_f32")):
+            layer[f"t{T}_{lname}"] = {
+                "qkv_n6144_k4096": P(qtype=Q4, n=6144, k=4096, T=T, leg=leg, seed=10),
+                "out_n4096_k4096_res": P(qtype=Q4, n=4096, k=4096, T=T, residual=True, leg=leg, seed=11),
+                "gate_up_n12288_k4096": P(qtype=Q4, n=12288, k=4096, T=T, gate_up=True, leg=leg, seed=12),
+                "down_n4096_k12288_res": P(qtype=Q4, n=4096, k=12288, T=T, residual=True, leg=leg, seed=13),
+            }
+    out["layer_9b_q4_0"] = layer
+    torch.cuda.empty_cache()
+    return out
 
 
 def gemm_kernel_rate(q, synth, dev, stream, peak_tf, n=4096, k=4096, T=2048):
@@ -635,6 +776,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload fields (every configuration)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only", choices=["all", "step", "kernel", "gemv", "attention"], default="all",
                     help="step: only the timed apr_qgemm steps; kernel: only the GEMM kernel on fp16 activations; "
