@@ -24,4 +24,5 @@ from .qref import (  # noqa: F401
     normed_qgemm_f64,
     prefill_attention_f64,
     prefill_attention_f16_inputs_f64,
+    prefill_layer_f64,
 )

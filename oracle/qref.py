@@ -46,6 +46,17 @@ What is computed, and where the pages define it:
   head ``h / (num_heads / num_kv_heads)``. ``q`` is ``[rows][num_heads * d]``,
   the caches ``[>= pos0 + rows][num_kv_heads * d]``, the output like ``q``.
 
+* One prefill layer over a chunk of rows (oxibonsai-kernels 0.1.4
+  ``encode_q_std_prefill_layer``: batched RMSNorm, the qkv projection, the
+  causal attention over the KV cache, the attention output projection with the
+  residual added, then the FFN phase; aprender-serve
+  src/gguf/cuda/forward_qwen35_cuda_prefill.rs, ``prefill_chunk``: the chunk's
+  k and v rows are written into the cache at positions ``pos0 ..`` before the
+  attention reads it). The fused qkv weight holds the q rows, then the k rows,
+  then the v rows. RoPE and the per-head q/k norm, which the pages apply
+  between the qkv projection and the attention, are model plumbing and are
+  not part of this layer.
+
 Every product is accumulated in float64 and the result is rounded to float32
 once. The f16-input mode rounds ``X`` and the dequantized ``W`` to fp16 first
 (the fp16 leg of ``qwen35_project_rows_f16``: fp16 in, fp32 accumulate), then
@@ -228,13 +239,19 @@ def prefill_attention_f64(Q, K_cache, V_cache, T: int, pos0: int, num_heads: int
     """``out[t, h] = sum_{j <= pos0+t} softmax_j(q_{t,h} . k_{j,g} / sqrt(d)) v_{j,g}``
     with ``g = h // (num_heads // num_kv_heads)``; float64, shape
     ``[len(rows)][num_heads * head_dim]`` (``rows`` defaults to all ``T``)."""
+    return _attention_f64(_as_f64(Q), _as_f64(K_cache), _as_f64(V_cache), T, pos0, num_heads, num_kv_heads,
+                          head_dim, rows)
+
+
+def _attention_f64(Q64, K64, V64, T, pos0, num_heads, num_kv_heads, head_dim, rows=None):
+    """The attention on float64 operands (see prefill_attention_f64)."""
     d = head_dim
     hpk = num_heads // num_kv_heads
     rows = np.arange(T) if rows is None else np.asarray(rows, dtype=np.int64)
-    Q64 = _as_f64(Q).reshape(T, num_heads * d)[rows]
+    Q64 = np.asarray(Q64, dtype=np.float64).reshape(T, num_heads * d)[rows]
     nk = pos0 + int(rows.max()) + 1 if len(rows) else 0
-    K64 = _as_f64(K_cache).reshape(-1, num_kv_heads * d)[:nk]
-    V64 = _as_f64(V_cache).reshape(-1, num_kv_heads * d)[:nk]
+    K64 = np.asarray(K64, dtype=np.float64).reshape(-1, num_kv_heads * d)[:nk]
+    V64 = np.asarray(V64, dtype=np.float64).reshape(-1, num_kv_heads * d)[:nk]
     out = np.zeros((len(rows), num_heads * d), dtype=np.float64)
     if not len(rows):
         return out
@@ -259,3 +276,50 @@ def prefill_attention_f16_inputs_f64(Q, K_cache, V_cache, T: int, pos0: int, num
     r16 = lambda a: np.asarray(a, dtype=np.float32).astype(np.float16).astype(np.float64)  # noqa: E731
     return prefill_attention_f64(r16(Q), r16(K_cache), r16(V_cache), T, pos0, num_heads, num_kv_heads,
                                  head_dim, rows=rows)
+
+
+# --------------------------------------------------------------------------
+# One prefill layer over a chunk: norm -> qkv (k, v into the cache) ->
+# attention -> output projection + residual -> FFN sublayer
+# --------------------------------------------------------------------------
+def prefill_layer_f64(qtype: int, X, attn_norm, ffn_norm, eps: float, Wqkv, Wo, Wg, Wu, Wd, hidden: int,
+                      inter: int, num_heads: int, num_kv_heads: int, head_dim: int, K_cache, V_cache,
+                      pos0: int):
+    """The layer on the T rows of ``X`` (positions ``pos0 .. pos0 + T - 1``):
+
+    * ``h = rmsnorm(X) * attn_norm``; ``q, k, v = h . Wq^T, h . Wk^T, h . Wv^T``
+      with ``Wqkv`` = the ``H d`` q rows, then the ``KV d`` k rows, then the v rows;
+    * the cache rows ``pos0 .. pos0 + T - 1`` become ``k`` and ``v``;
+    * ``a = attention(q, caches)`` (causal, grouped KV heads);
+    * ``X1 = X + a . Wo^T`` (``Wo`` is ``[hidden][H d]``);
+    * ``X2 = X1 + down(silu(h2 . Wg^T) * (h2 . Wu^T))``, ``h2 = rmsnorm(X1) * ffn_norm``.
+
+    Returns ``(X2, K, V)`` in float64; ``K`` and ``V`` are the updated caches
+    (copies; rows outside the chunk as given)."""
+    def norm(rows, w):  # float64 in, float64 out (no float32 round trip)
+        w64 = _as_f64(w).reshape(1, -1)
+        return rows / np.sqrt(np.mean(rows * rows, axis=-1, keepdims=True) + float(eps)) * w64
+
+    X64 = _as_f64(X).reshape(-1, hidden)
+    T = X64.shape[0]
+    qd, kvd = num_heads * head_dim, num_kv_heads * head_dim
+    bb = _BLOCK_BYTES[qtype]
+    row_bytes = hidden // _QK * bb
+    Wqkv_b = np.ascontiguousarray(Wqkv, dtype=np.uint8).reshape(-1)
+    Wq = Wqkv_b[:qd * row_bytes]
+    Wk = Wqkv_b[qd * row_bytes:(qd + kvd) * row_bytes]
+    Wv = Wqkv_b[(qd + kvd) * row_bytes:(qd + 2 * kvd) * row_bytes]
+    h = norm(X64, attn_norm)
+    q = h @ dequant_f64(qtype, Wq, qd, hidden).T
+    k = h @ dequant_f64(qtype, Wk, kvd, hidden).T
+    v = h @ dequant_f64(qtype, Wv, kvd, hidden).T
+    K = np.array(K_cache, dtype=np.float64).reshape(-1, kvd)
+    V = np.array(V_cache, dtype=np.float64).reshape(-1, kvd)
+    K[pos0:pos0 + T] = k
+    V[pos0:pos0 + T] = v
+    a = _attention_f64(q, K, V, T, pos0, num_heads, num_kv_heads, head_dim)
+    X1 = X64 + a @ dequant_f64(qtype, Wo, hidden, qd).T
+    h2 = norm(X1, ffn_norm)
+    act = silu_f64(h2 @ dequant_f64(qtype, Wg, inter, hidden).T) * (h2 @ dequant_f64(qtype, Wu, inter, hidden).T)
+    X2 = X1 + act @ dequant_f64(qtype, Wd, hidden, inter).T
+    return X2, K, V

@@ -641,3 +641,86 @@ def test_f16_attention_mode_equals_the_exact_oracle_on_fp16_operands():
     r = {key: c[key].astype(np.float16).astype(np.float32) for key in ("Q", "K", "V")}
     np.testing.assert_array_equal(oracle.prefill_attention_f16_inputs_f64(r["Q"], r["K"], r["V"], 5, 3, 4, 2, 8),
                                   oracle.prefill_attention_f64(r["Q"], r["K"], r["V"], 5, 3, 4, 2, 8))
+
+
+# ---------------------------------------------------------------- prefill layer
+# Pinned by composition identities (zero output or down weights leave one
+# sublayer), by the cache rows it must write, and by chunk splitting (a layer
+# over T rows equals the same layer over two consecutive chunks, the second
+# reading the cache rows the first wrote): a property of causal attention.
+_LD = dict(hidden=64, inter=96, num_heads=4, num_kv_heads=2, head_dim=8)
+
+
+def _layer_case(seed, T, pos0, zero_o=False, zero_d=False, qtype=synth.Q4_0):
+    h, i, H, KV, d = (_LD[k] for k in ("hidden", "inter", "num_heads", "num_kv_heads", "head_dim"))
+    w = lambda r, c, s, z: synth.quantize(qtype, np.zeros((r, c), np.float32) if z else  # noqa: E731
+                                          synth.weight_f32(r, c, s, sigma=0.1))
+    c = dict(
+        X=synth.activations(T, h, seed), an=(1 + 0.3 * synth.activations(1, h, seed + 1)[0]).astype(np.float32),
+        fn=(1 + 0.3 * synth.activations(1, h, seed + 2)[0]).astype(np.float32),
+        Wqkv=w((H + 2 * KV) * d, h, seed + 3, False), Wo=w(h, H * d, seed + 4, zero_o),
+        Wg=w(i, h, seed + 5, False), Wu=w(i, h, seed + 6, False), Wd=w(h, i, seed + 7, zero_d),
+        K=synth.activations(pos0 + T + 2, KV * d, seed + 8), V=synth.activations(pos0 + T + 2, KV * d, seed + 9))
+    return c
+
+
+def _layer(qtype, c, pos0, X=None, K=None, V=None):
+    return oracle.prefill_layer_f64(qtype, c["X"] if X is None else X, c["an"], c["fn"], 1e-5, c["Wqkv"], c["Wo"],
+                                    c["Wg"], c["Wu"], c["Wd"], _LD["hidden"], _LD["inter"], _LD["num_heads"],
+                                    _LD["num_kv_heads"], _LD["head_dim"], c["K"] if K is None else K,
+                                    c["V"] if V is None else V, pos0)
+
+
+def test_layer_with_zero_output_and_down_weights_leaves_x_and_writes_the_cache():
+    T, pos0 = 5, 3
+    c = _layer_case(1, T, pos0, zero_o=True, zero_d=True)
+    X2, K, V = _layer(synth.Q4_0, c, pos0)
+    np.testing.assert_array_equal(X2, c["X"].astype(np.float64))
+    h, H, KV, d = _LD["hidden"], _LD["num_heads"], _LD["num_kv_heads"], _LD["head_dim"]
+    rb = h // 32 * 18
+    Wk = c["Wqkv"].reshape(-1)[H * d * rb:(H + KV) * d * rb]
+    Wv = c["Wqkv"].reshape(-1)[(H + KV) * d * rb:(H + 2 * KV) * d * rb]
+    k = oracle.normed_qgemm_f64(synth.Q4_0, Wk, KV * d, h, c["X"], c["an"], 1e-5)
+    v = oracle.normed_qgemm_f64(synth.Q4_0, Wv, KV * d, h, c["X"], c["an"], 1e-5)
+    np.testing.assert_allclose(K[pos0:pos0 + T], k, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(V[pos0:pos0 + T], v, rtol=1e-12, atol=1e-12)
+    # rows outside the chunk stay as they were
+    np.testing.assert_array_equal(K[:pos0], c["K"][:pos0].astype(np.float64))
+    np.testing.assert_array_equal(K[pos0 + T:], c["K"][pos0 + T:].astype(np.float64))
+    np.testing.assert_array_equal(V[pos0 + T:], c["V"][pos0 + T:].astype(np.float64))
+
+
+def test_layer_with_zero_output_weight_is_the_ffn_sublayer():
+    T, pos0 = 6, 2
+    c = _layer_case(2, T, pos0, zero_o=True)
+    X2, _, _ = _layer(synth.Q4_0, c, pos0)
+    ffn = oracle.ffn_sublayer_f64(synth.Q4_0, c["X"], c["fn"], 1e-5, c["Wg"], c["Wu"], c["Wd"], _LD["hidden"],
+                                  _LD["inter"])
+    np.testing.assert_allclose(X2, ffn, rtol=1e-12, atol=1e-12)
+
+
+def test_layer_with_zero_down_weight_is_the_attention_sublayer():
+    T, pos0 = 4, 5
+    c = _layer_case(3, T, pos0, zero_d=True)
+    X2, K, V = _layer(synth.Q4_0, c, pos0)
+    h, H, KV, d = _LD["hidden"], _LD["num_heads"], _LD["num_kv_heads"], _LD["head_dim"]
+    rb = h // 32 * 18
+    q = oracle.normed_qgemm_f64(synth.Q4_0, c["Wqkv"].reshape(-1)[:H * d * rb], H * d, h, c["X"], c["an"], 1e-5)
+    a = oracle.prefill_attention_f64(q, K, V, T, pos0, H, KV, d)
+    want = c["X"].astype(np.float64) + a @ oracle.dequant_f64(synth.Q4_0, c["Wo"], h, H * d).T
+    # prefill_attention_f64 rounds its inputs to float32 first: agreement to float32 level
+    np.testing.assert_allclose(X2, want, rtol=1e-6, atol=1e-6)
+
+
+def test_layer_over_two_chunks_equals_one_chunk():
+    T, pos0, T1 = 7, 2, 3
+    c = _layer_case(4, T, pos0)
+    X_all, K_all, V_all = _layer(synth.Q4_0, c, pos0)
+    X_a, K_a, V_a = _layer(synth.Q4_0, c, pos0, X=c["X"][:T1])
+    X_b, K_b, V_b = _layer(synth.Q4_0, c, pos0 + T1, X=c["X"][T1:], K=K_a, V=V_a)
+    np.testing.assert_allclose(np.concatenate([X_a, X_b]), X_all, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(K_b, K_all, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(V_b, V_all, rtol=1e-12, atol=1e-12)
+    # and the order matters: the second chunk first (it would see stale cache rows) differs
+    X_w, _, _ = _layer(synth.Q4_0, c, pos0 + T1, X=c["X"][T1:])
+    assert np.max(np.abs(X_w - X_all[T1:])) > 1e-3
