@@ -424,6 +424,7 @@ def run_ours(args):
         big = gemm_kernel_rate(q, synth, dev, stream, peak_tf, T=2048)
         attn = {f"t{t}": attention_rate(q, synth, dev, stream, peak_tf, peak_gbs, T=t) for t in (512, 2048)}
         workloads = {} if args.no_configs else every_workload(q, dev, stream, peak_tf, peak_gbs)
+        layer = {f"t{t}": layer_rate(q, dev, stream, peak_tf, T=t, chunk=min(t, 2048)) for t in (512, 2048)}
 
     # ---- end to end: host buffers, copies inside the timed region
     e2e_steps = max(20, min(args.steps, 200))
@@ -508,6 +509,7 @@ def run_ours(args):
             "gemm_t2048": big,
             "attention": attn,
             "workloads": workloads,
+            "prefill_layer": layer,
         }
         if not args.no_cpu:
             line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -647,6 +649,39 @@ def every_workload(q, dev, stream, peak_tf, peak_gbs):
     out["layer_9b_q4_0"] = layer
     torch.cuda.empty_cache()
     return out
+
+
+def layer_rate(q, dev, stream, peak_tf, T=512, chunk=512, hidden=4096, inter=12288, nh=16, nkv=4):
+    """apr_prefill_layer on a 9B-class layer (Q4_0, fp16 leg, 16 query heads
+    over 4 KV heads, head_dim 256) over T rows at position 0 in chunks of
+    `chunk` rows, three rotating weight sets (325 MB, more than L2). TFLOP/s
+    counts the projections (2 T n k each, gate/up twice) and the attention's
+    two products over the visible (row, key) pairs."""
+    import torch
+
+    d = 256
+    qd, kvd = nh * d, nkv * d
+    shapes = (((qd + 2 * kvd), hidden), (hidden, qd), (inter, hidden), (inter, hidden), (hidden, inter))
+    sets = []
+    for j in range(3):
+        W = [torch.from_numpy(host_weight(2, r, c, 20 + i)).to(dev) for i, (r, c) in enumerate(shapes)]
+        X = torch.from_numpy(host_acts(T, hidden, 30)).to(dev)
+        K = torch.zeros((T, kvd), device=dev)
+        V = torch.zeros((T, kvd), device=dev)
+        sets.append((W, X, K, V))
+    an = torch.ones(hidden, device=dev)
+
+    def call(st):
+        W, X, K, V = st
+        return lambda: q.apr_prefill_layer(2, *W, hidden, inter, nh, nkv, T, 0, an, an, 1e-6, X, K, V, chunk=chunk)
+
+    dt = time_per_call([call(st) for st in sets], stream, budget_s=0.05)
+    q.apr_stream_status(stream)
+    flop = 2.0 * T * hidden * (qd + 2 * kvd + qd + 3 * inter)
+    aflop, _ = attention_work(T, 0, nh, nkv, d)
+    tf = (flop + aflop) / dt / 1e12
+    return {"workload": f"layer_q4_0_hidden{hidden}_inter{inter}_h{nh}_kv{nkv}_t{T}_chunk{chunk}", "us": dt * 1e6,
+            "TFLOP/s": tf, "frac_tensor": tf / peak_tf}
 
 
 def gemm_kernel_rate(q, synth, dev, stream, peak_tf, n=4096, k=4096, T=2048):

@@ -322,6 +322,68 @@ int apr_prefill_attention(const float* Q, const float* K_cache, const float* V_c
                           int num_heads, int num_kv_heads, int head_dim, apr_stream_t stream);
 
 /*
+ * One prefill layer over T rows of the residual stream, chunk by chunk (the
+ * pages' chunked prefill: oxibonsai-kernels 0.1.4 cuda_q_std_prefill.rs
+ * encode_q_std_prefill_layer runs batched RMSNorm, the qkv projection, the
+ * causal attention over the KV cache, the attention output projection with the
+ * residual added and then the FFN phase for every chunk; aprender-serve 0.70.2
+ * forward_qwen35_cuda_prefill.rs prefill_chunk, chunks of 512 rows by default,
+ * writes the chunk's k and v rows into the cache before the attention). For
+ * the chunk's rows of X at positions p = pos0 + t:
+ *   h = RMSNorm(X) * attn_norm
+ *   q = h . Wq^T;  K_cache[p] = h . Wk^T;  V_cache[p] = h . Wv^T
+ *   X += attention(q, K_cache, V_cache) . Wo^T      (as apr_prefill_attention)
+ *   X += down(silu(h2 . Wg^T) * (h2 . Wu^T)),  h2 = RMSNorm(X) * ffn_norm
+ * RoPE and the per-head q/k norm, which the pages apply between the qkv
+ * projection and the attention, are not part of this call (a caller that needs
+ * them runs the steps one by one with apr_qgemm_rmsnorm, apr_qgemm_ex with
+ * ldy, apr_prefill_attention, apr_qgemm and apr_ffn_sublayer).
+ *   qtype, leg  as for apr_qgemm_ex, for every projection (the attention takes
+ *               fp16 inputs on both legs)
+ *   Wqkv     [(num_heads + 2 num_kv_heads) * 256][hidden]: the q rows, then the
+ *            k rows, then the v rows (the pages' fused qkv weight)
+ *   Wo       [hidden][num_heads * 256];  Wg, Wu [inter][hidden];  Wd [hidden][inter]
+ *   hidden, inter  multiples of 32 (256 for the tensor-core routes)
+ *   num_heads, num_kv_heads, head_dim  as for apr_prefill_attention (256)
+ *   T, pos0  rows of X and the position of the first; T == 0 is a no-op
+ *   attn_norm, ffn_norm  [hidden] fp32;  eps >= 0 and finite
+ *   X        [T][hidden] fp32, dense, updated in place
+ *   K_cache, V_cache  [>= pos0 + T][num_kv_heads * 256] fp32; rows pos0 ..
+ *            pos0 + T - 1 are written, rows before are read, rows after untouched
+ *   chunk    rows per chunk (0: 512)
+ * All pointers device, 16-byte aligned, caller owned; X and the caches must not
+ * overlap each other, a weight or a norm weight (APR_E_ALIAS). Scratch per
+ * stream as for apr_qgemm (the chunk's normed rows, q and attention output,
+ * and what the steps take). Errors as for apr_qgemm_ex and
+ * apr_prefill_attention. Asynchronous on the stream.
+ */
+typedef struct apr_layer_args {
+  int qtype;
+  int leg;
+  const void* Wqkv;
+  const void* Wo;
+  const void* Wg;
+  const void* Wu;
+  const void* Wd;
+  int hidden;
+  int inter;
+  int num_heads;
+  int num_kv_heads;
+  int head_dim;
+  int T;
+  int pos0;
+  const float* attn_norm;
+  const float* ffn_norm;
+  float eps;
+  float* X;
+  float* K_cache;
+  float* V_cache;
+  int chunk;
+  apr_stream_t stream;
+} apr_layer_args;
+int apr_prefill_layer(const apr_layer_args* args);
+
+/*
  * Standalone dequant: out[n][k] f32 = f32(d) * f32(q'), bit exact (the product
  * of an fp16 scale and a code of at most 8 bits is exact in fp32). The device
  * dequant of aprender-serve gdn_prefill_ops.rs qwen35_dequant_f32 (Q8_0 and

@@ -50,6 +50,7 @@ EXPORTS = (
     "apr_ffn_sublayer",
     "apr_qgemm_rmsnorm",
     "apr_prefill_attention",
+    "apr_prefill_layer",
     "apr_dequant",
     "apr_stream_status",
     "apr_test_bounded_wait",
@@ -98,6 +99,33 @@ class _FfnArgs(ctypes.Structure):
     ]
 
 
+class _LayerArgs(ctypes.Structure):
+    _fields_ = [
+        ("qtype", ctypes.c_int),
+        ("leg", ctypes.c_int),
+        ("Wqkv", ctypes.c_void_p),
+        ("Wo", ctypes.c_void_p),
+        ("Wg", ctypes.c_void_p),
+        ("Wu", ctypes.c_void_p),
+        ("Wd", ctypes.c_void_p),
+        ("hidden", ctypes.c_int),
+        ("inter", ctypes.c_int),
+        ("num_heads", ctypes.c_int),
+        ("num_kv_heads", ctypes.c_int),
+        ("head_dim", ctypes.c_int),
+        ("T", ctypes.c_int),
+        ("pos0", ctypes.c_int),
+        ("attn_norm", ctypes.c_void_p),
+        ("ffn_norm", ctypes.c_void_p),
+        ("eps", ctypes.c_float),
+        ("X", ctypes.c_void_p),
+        ("K_cache", ctypes.c_void_p),
+        ("V_cache", ctypes.c_void_p),
+        ("chunk", ctypes.c_int),
+        ("stream", ctypes.c_void_p),
+    ]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -116,6 +144,7 @@ def _load() -> ctypes.CDLL:
         "apr_ffn_sublayer": ([ctypes.POINTER(_FfnArgs)], ci),
         "apr_qgemm_rmsnorm": ([ctypes.POINTER(_Args), vp, ctypes.c_float], ci),
         "apr_prefill_attention": ([vp, vp, vp, vp, ci, ci, ci, ci, ci, vp], ci),
+        "apr_prefill_layer": ([ctypes.POINTER(_LayerArgs)], ci),
         "apr_dequant": ([ci, vp, ci, ci, vp, vp], ci),
         "apr_stream_status": ([vp], ci),
         "apr_test_bounded_wait": ([ctypes.c_uint, vp], ci),
@@ -351,3 +380,27 @@ def apr_test_bounded_wait(limit_us, stream=None) -> int:
     out after limit_us microseconds); apr_stream_status then reports the
     timeout."""
     return _check(_lib.apr_test_bounded_wait(int(limit_us), _stream(stream)))
+
+
+def apr_prefill_layer(qtype, Wqkv, Wo, Wg, Wu, Wd, hidden, inter, num_heads, num_kv_heads, T, pos0, attn_norm,
+                      ffn_norm, eps, X, K_cache, V_cache, *, leg=APR_LEG_F16, chunk=0, head_dim=256,
+                      stream=None) -> int:
+    """One prefill layer over X[T][hidden] in place (attention sublayer with k
+    and v written into the cache rows pos0 .., then the FFN sublayer), in
+    chunks of `chunk` rows."""
+    u8, f32 = _dtypes()
+    bb = BLOCK_BYTES.get(qtype, 0)
+    h_, i_, t_ = max(hidden, 0), max(inter, 0), max(T, 0)
+    qd, kvd = max(num_heads, 0) * max(head_dim, 0), max(num_kv_heads, 0) * max(head_dim, 0)
+    crow = max(pos0, 0) + t_
+    a = _LayerArgs(qtype, leg, _ptr(Wqkv, "Wqkv", dtype=u8, min_bytes=(qd + 2 * kvd) * (h_ // 32) * bb),
+                   _ptr(Wo, "Wo", dtype=u8, min_bytes=h_ * (qd // 32) * bb),
+                   _ptr(Wg, "Wg", dtype=u8, min_bytes=i_ * (h_ // 32) * bb),
+                   _ptr(Wu, "Wu", dtype=u8, min_bytes=i_ * (h_ // 32) * bb),
+                   _ptr(Wd, "Wd", dtype=u8, min_bytes=h_ * (i_ // 32) * bb), hidden, inter, num_heads,
+                   num_kv_heads, head_dim, T, pos0, _ptr(attn_norm, "attn_norm", dtype=f32, min_bytes=h_ * 4),
+                   _ptr(ffn_norm, "ffn_norm", dtype=f32, min_bytes=h_ * 4), float(eps),
+                   _ptr(X, "X", dtype=f32, min_bytes=t_ * h_ * 4),
+                   _ptr(K_cache, "K_cache", dtype=f32, min_bytes=crow * kvd * 4),
+                   _ptr(V_cache, "V_cache", dtype=f32, min_bytes=crow * kvd * 4), chunk, _stream(stream))
+    return _check(_lib.apr_prefill_layer(ctypes.byref(a)))

@@ -91,7 +91,14 @@ int device_state(DeviceState** out) {
 // The GEMV's buffer starts zeroed (cudaMemsetAsync on the stream) and every
 // completed call leaves its counters zero; after a device-side timeout the
 // buffers are cleared again before their next use.
-enum ScratchUse { kScratchX16 = 0, kScratchGemv = 1, kScratchFfn = 2, kScratchNorm = 3, kScratchAttn = 4 };
+enum ScratchUse {
+  kScratchX16 = 0,
+  kScratchGemv = 1,
+  kScratchFfn = 2,
+  kScratchNorm = 3,
+  kScratchAttn = 4,
+  kScratchLayer = 5
+};
 struct StreamScratch {
   int dev;
   cudaStream_t s;
@@ -367,6 +374,110 @@ int run_normed(const Problem& p, const float* w, float eps) {
   return APR_OK;
 }
 
+// One prefill layer, chunk by chunk: the attention sublayer (norm, q/k/v
+// projections with k and v written into the cache rows of the chunk, the
+// causal attention, the output projection added into X), then the FFN
+// sublayer on the chunk's rows of X.
+int run_layer(const apr_layer_args& a) {
+  if (a.qtype != APR_Q4_0 && a.qtype != APR_Q8_0) return fail(APR_E_QTYPE, "unsupported qtype %d", a.qtype);
+  if (a.leg != APR_LEG_F16 && a.leg != APR_LEG_EXACT_F32) return fail(APR_E_INVAL, "unknown leg %d", a.leg);
+  if (a.head_dim != 256) return fail(APR_E_INVAL, "head_dim must be 256 (got %d)", a.head_dim);
+  if (a.hidden <= 0 || a.inter <= 0 || a.hidden % 32 != 0 || a.inter % 32 != 0 || a.T < 0 || a.pos0 < 0 ||
+      a.num_heads <= 0 || a.num_kv_heads <= 0 || a.chunk < 0)
+    return fail(APR_E_INVAL, "bad sizes hidden=%d inter=%d T=%d pos0=%d heads=%d kv_heads=%d chunk=%d", a.hidden,
+                a.inter, a.T, a.pos0, a.num_heads, a.num_kv_heads, a.chunk);
+  if (a.num_heads % a.num_kv_heads != 0)
+    return fail(APR_E_INVAL, "num_heads (%d) must be a multiple of num_kv_heads (%d)", a.num_heads, a.num_kv_heads);
+  const long long qd = (long long)a.num_heads * 256, kvd = (long long)a.num_kv_heads * 256;
+  if (a.hidden > (1 << 20) || a.inter > (1 << 20) || a.T > (1 << 24) || a.chunk > (1 << 20) ||
+      qd + 2 * kvd > (1 << 24) || (long long)a.pos0 + a.T > (1LL << 30) || kvd / 64 > 65535 ||
+      (long long)a.hidden * (a.inter / 32) > (1LL << 31) || (qd + 2 * kvd) * (a.hidden / 32) > (1LL << 31) ||
+      (long long)a.hidden * (qd / 32) > (1LL << 31))
+    return fail(APR_E_INVAL, "sizes beyond the supported limits");
+  if (!(a.eps >= 0.f) || a.eps > 3.402823466e38f) return fail(APR_E_INVAL, "eps must be finite and >= 0");
+  if (a.T == 0) return APR_OK;
+  const void* ptrs[10] = {a.Wqkv, a.Wo, a.Wg, a.Wu, a.Wd, a.attn_norm, a.ffn_norm, a.X, a.K_cache, a.V_cache};
+  for (const void* q : ptrs) {
+    if (!q) return fail(APR_E_INVAL, "null pointer");
+    if (!aligned16(q)) return fail(APR_E_ALIGN, "pointer %p is not 16-byte aligned", q);
+  }
+  const size_t bb = (size_t)block_bytes(a.qtype);
+  const size_t hrow = (size_t)(a.hidden / 32) * bb;  // bytes of a weight row over hidden columns
+  const size_t wqkv = (size_t)(qd + 2 * kvd) * hrow, wo = (size_t)a.hidden * (size_t)(qd / 32) * bb;
+  const size_t wgu = (size_t)a.inter * hrow, wd = (size_t)a.hidden * (size_t)(a.inter / 32) * bb;
+  const size_t xb = (size_t)a.T * a.hidden * 4, cb = ((size_t)a.pos0 + a.T) * (size_t)kvd * 4;
+  const void* wts[7] = {a.Wqkv, a.Wo, a.Wg, a.Wu, a.Wd, a.attn_norm, a.ffn_norm};
+  const size_t wsz[7] = {wqkv, wo, wgu, wgu, wd, (size_t)a.hidden * 4, (size_t)a.hidden * 4};
+  for (int i = 0; i < 7; ++i)
+    if (overlap(a.X, xb, wts[i], wsz[i]) || overlap(a.K_cache, cb, wts[i], wsz[i]) ||
+        overlap(a.V_cache, cb, wts[i], wsz[i]))
+      return fail(APR_E_ALIAS, "X or a cache overlaps a weight or a norm weight");
+  if (overlap(a.X, xb, a.K_cache, cb) || overlap(a.X, xb, a.V_cache, cb) || overlap(a.K_cache, cb, a.V_cache, cb))
+    return fail(APR_E_ALIAS, "X, K_cache and V_cache must not overlap");
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc != APR_OK) return rc;
+  const cudaStream_t s = (cudaStream_t)a.stream;
+  const int chunk = a.chunk > 0 ? a.chunk : 512;
+  const int rmax = a.T < chunk ? a.T : chunk;
+  // the chunk's normed rows (fp32 at most), q and the attention output
+  const size_t h_bytes = align256((size_t)rmax * a.hidden * 4), q_bytes = align256((size_t)rmax * qd * 4);
+  void* scratch = nullptr;
+  rc = stream_scratch(st->dev, s, kScratchLayer, h_bytes + 2 * q_bytes, &scratch);
+  if (rc != APR_OK) return rc;
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  void* h = base;
+  float* qbuf = reinterpret_cast<float*>(base + h_bytes);
+  float* abuf = reinterpret_cast<float*>(base + h_bytes + q_bytes);
+  // the attention's fp16 copies of the cache rows, sized for the last chunk
+  void* ascratch = nullptr;
+  rc = stream_scratch(st->dev, s, kScratchAttn, prefill_attention_scratch_bytes(rmax, a.pos0 + a.T - rmax,
+                                                                                a.num_kv_heads),
+                      &ascratch);
+  if (rc != APR_OK) return rc;
+  const uint8_t* Wq = static_cast<const uint8_t*>(a.Wqkv);
+  const uint8_t* Wk = Wq + (size_t)qd * hrow;
+  const uint8_t* Wv = Wk + (size_t)kvd * hrow;
+  for (int t0 = 0; t0 < a.T; t0 += chunk) {
+    const int rows = a.T - t0 < chunk ? a.T - t0 : chunk;
+    const int pos = a.pos0 + t0;
+    float* Xc = a.X + (size_t)t0 * a.hidden;
+    // 1. norm, then q, k, v: k and v straight into the cache rows pos ..
+    const bool tc = a.leg == APR_LEG_F16 && rows > APR_GEMV_MAX_T && a.hidden % 256 == 0;
+    rc = launched(launch_rmsnorm_rows(Xc, a.attn_norm, a.eps, rows, a.hidden, h, tc, s), "rmsnorm");
+    if (rc != APR_OK) return rc;
+    const void* Wp[3] = {Wq, Wk, Wv};
+    float* Yp[3] = {qbuf, a.K_cache + (size_t)pos * kvd, a.V_cache + (size_t)pos * kvd};
+    const int np[3] = {(int)qd, (int)kvd, (int)kvd};
+    for (int j = 0; j < 3; ++j) {
+      if (tc) {
+        char msg[256] = "";
+        const GemmPlan plan = plan_gemm_tc(np[j], a.hidden, rows, false);
+        if (launch_gemm_tc(plan, a.qtype, Wp[j], nullptr, np[j], a.hidden, static_cast<const uint16_t*>(h), rows,
+                           Yp[j], np[j], nullptr, st->status, s, msg, sizeof msg, true) != 0)
+          return fail(APR_E_LAUNCH, "%s", msg);
+      } else {
+        rc = run(Problem{a.qtype, a.leg, APR_PATH_AUTO, Wp[j], nullptr, np[j], a.hidden, rows,
+                         static_cast<const float*>(h), nullptr, Yp[j], s});
+        if (rc != APR_OK) return rc;
+      }
+    }
+    // 2. causal attention of the chunk's rows over the cache rows 0 .. pos + rows - 1
+    char msg[256] = "";
+    if (launch_prefill_attention(qbuf, a.K_cache, a.V_cache, abuf, rows, pos, a.num_heads, a.num_kv_heads, ascratch,
+                                 st->status, s, msg, sizeof msg) != 0)
+      return fail(APR_E_LAUNCH, "%s", msg);
+    // 3. output projection added into the chunk's rows of X
+    rc = run(Problem{a.qtype, a.leg, APR_PATH_AUTO, a.Wo, nullptr, a.hidden, (int)qd, rows, abuf, Xc, Xc, s});
+    if (rc != APR_OK) return rc;
+    // 4. the FFN sublayer on the same rows
+    apr_ffn_args f{a.qtype, a.leg, a.Wg, a.Wu, a.Wd, a.hidden, a.inter, rows, a.ffn_norm, a.eps, Xc, a.stream};
+    rc = run_ffn(f);
+    if (rc != APR_OK) return rc;
+  }
+  return APR_OK;
+}
+
 }  // namespace
 
 namespace apr {
@@ -437,6 +548,12 @@ int apr_ffn_sublayer(const apr_ffn_args* a) {
   t_msg[0] = 0;
   if (!a) return fail(APR_E_INVAL, "null argument struct");
   return run_ffn(*a);
+}
+
+int apr_prefill_layer(const apr_layer_args* a) {
+  t_msg[0] = 0;
+  if (!a) return fail(APR_E_INVAL, "null argument struct");
+  return run_layer(*a);
 }
 
 int apr_convert_f32_to_f16(const float* X, long long count, void* X16, apr_stream_t stream) {

@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(q):
     names = declared_functions()
-    assert len(names) == 15, names
+    assert len(names) == 16, names
     lib = q.library()
     for name in names:
         assert hasattr(lib, name), name
@@ -216,3 +216,30 @@ def test_prefill_attention_argument_errors(q):
     assert rc(T=0, Q=None, K=None, V=None, O=None) == 0   # T == 0: nothing to do
     assert "head_dim" in (lib.apr_prefill_attention(Qp, Kp, Vp, Op, 1, 0, 1, 1, 64, None),
                           q.apr_last_error())[1]
+
+
+def test_prefill_layer_argument_errors(q):
+    import ctypes
+
+    lib = q.library()
+
+    def args(**kw):
+        base = dict(qtype=2, leg=0, Wqkv=A, Wo=2 * A, Wg=3 * A, Wu=4 * A, Wd=5 * A, hidden=256, inter=512,
+                    num_heads=2, num_kv_heads=1, head_dim=256, T=8, pos0=0, attn_norm=6 * A, ffn_norm=7 * A,
+                    eps=1e-6, X=8 * A, K_cache=9 * A, V_cache=10 * A, chunk=0, stream=None)
+        base.update(kw)
+        return q.capi._LayerArgs(*[base[f] for f, _ in q.capi._LayerArgs._fields_])
+
+    assert lib.apr_prefill_layer(None) == q.APR_E_INVAL
+    assert lib.apr_prefill_layer(ctypes.byref(args(qtype=3))) == q.APR_E_QTYPE
+    assert lib.apr_prefill_layer(ctypes.byref(args(head_dim=128))) == q.APR_E_INVAL
+    assert lib.apr_prefill_layer(ctypes.byref(args(num_heads=3, num_kv_heads=2))) == q.APR_E_INVAL
+    assert lib.apr_prefill_layer(ctypes.byref(args(hidden=100))) == q.APR_E_INVAL
+    assert lib.apr_prefill_layer(ctypes.byref(args(eps=-1.0))) == q.APR_E_INVAL
+    assert lib.apr_prefill_layer(ctypes.byref(args(chunk=-1))) == q.APR_E_INVAL
+    assert lib.apr_prefill_layer(ctypes.byref(args(Wo=None))) == q.APR_E_INVAL
+    assert lib.apr_prefill_layer(ctypes.byref(args(X=8 * A + 4))) == q.APR_E_ALIGN
+    # X overlapping the K cache, and a cache overlapping a weight
+    assert lib.apr_prefill_layer(ctypes.byref(args(K_cache=8 * A + 4096))) == q.APR_E_ALIAS
+    assert lib.apr_prefill_layer(ctypes.byref(args(V_cache=A + 4096))) == q.APR_E_ALIAS
+    assert lib.apr_prefill_layer(ctypes.byref(args(T=0))) == q.APR_OK
