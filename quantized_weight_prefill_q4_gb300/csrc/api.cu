@@ -258,7 +258,7 @@ int run(const Problem& p) {
   if (rc != APR_OK) return rc;
   char msg[256] = "";
   if (launch_gemm_tc(plan, p.qtype, p.W, p.Wu, p.n, p.k, static_cast<const uint16_t*>(x16), p.T, p.Y, ldy_of(p), p.R,
-                     st->status, p.s, msg, sizeof msg, true) != 0)
+                     st->status, p.s, msg, sizeof msg, kEarlyWR) != 0)
     return fail(APR_E_LAUNCH, "%s", msg);
   return APR_OK;
 }
@@ -311,13 +311,13 @@ int run_ffn(const apr_ffn_args& a) {
       char msg[256] = "";
       const GemmPlan pg = plan_gemm_tc(a.inter, a.hidden, rows, true);
       if (launch_gemm_tc(pg, a.qtype, a.Wg, a.Wu, a.inter, a.hidden, static_cast<const uint16_t*>(h), rows, act,
-                         a.inter, nullptr, st->status, s, msg, sizeof msg, true) != 0)
+                         a.inter, nullptr, st->status, s, msg, sizeof msg, kEarlyWR) != 0)
         return fail(APR_E_LAUNCH, "%s", msg);
       rc = launched(launch_x_to_f16(act, act16, (size_t)rows * a.inter, s), "x_to_f16");
       if (rc != APR_OK) return rc;
       const GemmPlan pd = plan_gemm_tc(a.hidden, a.inter, rows, false);
       if (launch_gemm_tc(pd, a.qtype, a.Wd, nullptr, a.hidden, a.inter, act16, rows, Xc, a.hidden, Xc, st->status, s,
-                         msg, sizeof msg, true) != 0)
+                         msg, sizeof msg, kEarlyWR) != 0)
         return fail(APR_E_LAUNCH, "%s", msg);
     } else {
       rc = run(Problem{a.qtype, a.leg, APR_PATH_AUTO, a.Wg, a.Wu, a.inter, a.hidden, rows,
@@ -363,7 +363,7 @@ int run_normed(const Problem& p, const float* w, float eps) {
       char msg[256] = "";
       const GemmPlan plan = plan_gemm_tc(p.n, p.k, rows, p.Wu != nullptr);
       if (launch_gemm_tc(plan, p.qtype, p.W, p.Wu, p.n, p.k, static_cast<const uint16_t*>(h), rows, Yc, ldy, Rc,
-                         st->status, p.s, msg, sizeof msg, true) != 0)
+                         st->status, p.s, msg, sizeof msg, kEarlyWR) != 0)
         return fail(APR_E_LAUNCH, "%s", msg);
     } else {
       rc = run(Problem{p.qtype, p.leg, path, p.W, p.Wu, p.n, p.k, rows, static_cast<const float*>(h), Rc, Yc, p.s,
@@ -454,7 +454,7 @@ int run_layer(const apr_layer_args& a) {
         char msg[256] = "";
         const GemmPlan plan = plan_gemm_tc(np[j], a.hidden, rows, false);
         if (launch_gemm_tc(plan, a.qtype, Wp[j], nullptr, np[j], a.hidden, static_cast<const uint16_t*>(h), rows,
-                           Yp[j], np[j], nullptr, st->status, s, msg, sizeof msg, true) != 0)
+                           Yp[j], np[j], nullptr, st->status, s, msg, sizeof msg, j == 0 ? kEarlyWR : kEarlyW) != 0)
           return fail(APR_E_LAUNCH, "%s", msg);
       } else {
         rc = run(Problem{a.qtype, a.leg, APR_PATH_AUTO, Wp[j], nullptr, np[j], a.hidden, rows,
@@ -586,7 +586,7 @@ int apr_qgemm_f16_in(int qtype, const void* W, const void* Wu, int n, int k, con
   const GemmPlan plan = plan_gemm_tc(n, k, T, Wu != nullptr);
   char msg[256] = "";
   if (launch_gemm_tc(plan, qtype, W, Wu, n, k, static_cast<const uint16_t*>(X16), T, Y, n, residual, st->status,
-                     (cudaStream_t)stream, msg, sizeof msg, false) != 0)
+                     (cudaStream_t)stream, msg, sizeof msg, kEarlyW) != 0)
     return fail(APR_E_LAUNCH, "%s", msg);
   return APR_OK;
 }

@@ -87,12 +87,16 @@ GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu);
 
 // tcgen05 fp16-input GEMM; needs k % 256 == 0 and X16 = fp16(X) (gemm_tc.cu).
 // `status` is the device status word. Launched with programmatic stream
-// serialization: it waits for the preceding kernel before it touches X16, W,
-// R or Y, except that with `after_conversion` (launched right after
-// launch_x_to_f16 on the same stream) it reads W and R without waiting.
+// serialization: it waits for the preceding kernel before it touches X16 and
+// Y. `early` says what it reads before that: kEarlyW the weights (never the
+// preceding kernel's output: the header's stream-order rule), kEarlyWR the
+// weights and the residual (launched right after the library's own
+// conversion or norm kernel, which starts only once everything before it has
+// completed), kEarlyNone nothing.
+enum { kEarlyNone = 0, kEarlyWR = 1, kEarlyW = 2 };
 int launch_gemm_tc(const GemmPlan& plan, int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16,
                    int T, float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg,
-                   size_t msg_len, bool after_conversion);
+                   size_t msg_len, int early);
 
 // A kernel that waits (bounded, limit_ns) on an mbarrier nothing arrives on,
 // then records the timeout in the status word and returns (selftest.cu).

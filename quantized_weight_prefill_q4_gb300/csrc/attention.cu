@@ -352,6 +352,9 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
           tmem_st_32x32b_x32(lane_addr + COL_O + cb * 32, ov);
+          // the store reads its source registers asynchronously: the next
+          // load must not overwrite them before it has completed
+          tmem_st_wait();
         }
         m_ref = m_new;
       }

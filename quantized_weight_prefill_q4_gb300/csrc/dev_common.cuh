@@ -98,6 +98,11 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void* src,
                "r"(smem_u32(src)), "r"(bytes), "r"(remote_bar)
                : "memory");
 }
+// Stores one float at `addr`, a shared::cluster address in another CTA of the
+// cluster (distributed shared memory).
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
 // Arrives once on the mbarrier at `remote_bar` (a shared::cluster address),
 // releasing this thread's earlier writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
@@ -253,7 +258,8 @@ __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp writes lane
-// (base lane + i), columns col..col+31, from v[0..31].
+// (base lane + i), columns col..col+31, from v[0..31]. The store is
+// asynchronous: keep v[] unchanged until tmem_st_wait().
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "

@@ -18,13 +18,12 @@
 //   warp 0       TMA producer of raw weight chunks: 128 rows x 256 k (8 blocks
 //                per row: 144 B for Q4_0, 272 B for Q8_0, the smallest box whose
 //                width is a multiple of 16 bytes for both formats) into a ring
-//                of S_RAW slots, with L2 prefetches PF chunks ahead; with a
-//                128-token tile it also fetches the residual tile early
+//                of S_RAW slots, with L2 prefetches PF chunks ahead
 //   warp 1       TMEM allocator and MMA issuer: the whole warp runs the loop,
 //                one elected lane issues (four K = 16 MMAs per 64-k stage)
 //   warp 2       TMA producer of X tiles: BN tokens x 64 k of the fp16 copy of X,
-//                128-byte swizzled, into the B ring; with a 256-token tile it
-//                then fetches the residual into the ring slots as they free up
+//                128-byte swizzled, into the B ring; a few stages before the
+//                end it prefetches the residual pieces the CTA finalizes into L2
 //   warp 3       idle
 //   warps 4..    dequant warpgroups: each thread owns one of the 128 rows (its
 //                TMEM lane), decodes 2 blocks (64 k) per stage from the raw slot
@@ -34,29 +33,33 @@
 //                warpgroup per weight. Then the same warps run the epilogue.
 // Epilogue: the tile's token columns go out in pieces of 64. A warpgroup reads
 // a piece's accumulators out of TMEM (two 32-column loads, one wait), adds the
-// residual (or applies the SiLU gate), writes the piece into shared memory and
-// one thread stores it with a TMA tensor store; when a row of Y is not a
-// multiple of 16 bytes the threads store Y directly instead.
+// residual (or applies the SiLU gate) in registers and stores Y straight from
+// registers: thread r owns weight row r, so each store of a warp writes 32
+// consecutive floats of one token's row. The residual of the warpgroup's
+// first piece is loaded into registers while the last chunks are still in the
+// MMA pipe (after the X producer prefetched it into L2). Nothing of the
+// epilogue passes through shared memory except the split partner's half: the
+// shared-memory round trips of a TMA residual load and a TMA store of Y cost
+// more (the SM's shared-memory bandwidth) than the stores they replace.
 // Split over k (two CTAs per tile, blockIdx.z = 0, 1, launched as a cluster
 // (1, 1, 2)): CTA z finalizes token columns [128 z, 128 z + 128) of the tile.
 // Its weight producer tells the partner when the raw ring is free (the last
-// chunk decoded, a little before the last MMAs finish); after its MMAs each CTA
-// stages the other half of its fp32 accumulator in its own operand ring and
-// sends it with one bulk copy per piece into the partner's raw ring
-// (distributed shared memory), then adds p0 + p1 in split order, so the result
-// does not depend on which CTA finishes first. A cluster barrier at the end
-// keeps both CTAs resident until neither touches the other's shared memory.
+// chunk decoded, a little before the last MMAs finish); after its MMAs each
+// thread writes its row of the half the partner keeps straight from registers
+// into the partner's raw ring (distributed shared memory stores) and arrives
+// on the partner's barrier with release semantics; each CTA then adds p0 + p1
+// in split order, so the result does not depend on which CTA finishes first.
+// A cluster barrier at the end keeps both CTAs resident until neither touches
+// the other's shared memory.
 // Every mbarrier wait is bounded (2 s); a wait that gives up sets the device
 // status word and an abort flag in shared memory so that every role leaves its
 // loop, drains its own TMA copies and MMAs, and the CTA frees its TMEM.
 // Programmatic dependent launch: the kernel lets the next kernel of the stream
-// launch early, and itself reads and writes global memory only after
-// griddepcontrol.wait (the X producer, the weight producer and the epilogue
-// each wait; only L2 prefetches of the weight go before). Launched right after
-// the library's own X conversion (w_early), the weight producer does not wait:
-// that kernel writes only X16, and it lets the GEMM launch only after every
-// kernel before it has completed, so the weight and residual loads overlap the
-// conversion.
+// launch early. X16, Y and the residual are touched only after
+// griddepcontrol.wait. The weights are read before it (`early` != kEarlyNone):
+// the library's weights are never the output of the kernel just before (the
+// header's stream-order rule), so the first weight chunks stream and decode
+// while the preceding kernel finishes. With kEarlyNone everything waits.
 
 #include <cstdint>
 #include <cstdio>
@@ -79,13 +82,9 @@ constexpr int PF = 4;           // raw chunks prefetched into L2 ahead of their 
 constexpr int PIECE = 64;                      // token columns per epilogue piece
 constexpr int PIECE_BYTES = PIECE * BM * 4;    // one fp32 piece, [64 tokens][128 rows]
 
-// TIO: R and Y rows are multiples of 16 bytes (n % 4 == 0), so the residual is
-// fetched and Y stored by TMA through shared memory; otherwise both go through
-// direct loads and stores.
-template <int QT, int EPI, int BN_, bool TIO_>
+template <int QT, int EPI, int BN_>
 struct Cfg {
   static constexpr int BN = BN_;
-  static constexpr bool TIO = TIO_;
   static constexpr int A_COLS = 32;                     // TMEM columns of one A stage of one weight
   static constexpr int B_BYTES = BN * 128;              // one 128-B-swizzled B stage
   static constexpr int NM = EPI == kEpiSwiGLU ? 2 : 1;
@@ -95,12 +94,6 @@ struct Cfg {
   static constexpr int RAW_ROW = CHUNK / 32 * BB;     // 144 / 272 bytes
   static constexpr int RAW_BYTES = BM * RAW_ROW;      // one raw slot
   static constexpr int NPIECE = BN / PIECE;
-  // residual through TMA: early into its own buffer (128-token tiles), or late
-  // into the operand ring slots as the last MMAs free them (256-token tiles,
-  // where a ring slot is exactly one piece)
-  static constexpr bool R_EARLY = EPI == kEpiResidual && TIO && BN == 128;
-  static constexpr bool R_LATE = EPI == kEpiResidual && TIO && BN == 256;
-  static constexpr int R_BYTES = R_EARLY ? NPIECE * PIECE_BYTES : 0;
   // operand stages (A in TMEM and B in shared memory advance together)
   static constexpr int S = NM == 2 ? 4 : (BN == 256 ? 4 : (QT == kQ4_0 ? 6 : 5));
   // (with 256-token tiles the raw ring also receives the partner's half of a
@@ -119,22 +112,15 @@ struct Cfg {
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int OFF_B = 0;
   static constexpr int OFF_RAW = OFF_B + S * B_BYTES;
-  static constexpr int OFF_R = OFF_RAW + S_RAW * RAW_BYTES;
-  static constexpr int OFF_BAR = OFF_R + R_BYTES;
-  static constexpr int NBAR = 2 * S + 2 * S_RAW + 2 + 4 + 2;  // + accFull, drain, 4 residual pieces, 2 split
+  static constexpr int OFF_BAR = OFF_RAW + S_RAW * RAW_BYTES;
+  static constexpr int NBAR = 2 * S + 2 * S_RAW + 2 + 1 + 2;  // + accFull, drain, peerFree, 2 xferFull
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 32 + 1024;   // + alignment slack
-  // staging of the output pieces: the residual buffer, else the operand ring
-  // (free once every MMA has completed)
-  static constexpr int OFF_STAGE = R_EARLY ? OFF_R : OFF_B;
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(NM == 1 || S_RAW % 2 == 0, "gate/up: each raw slot keeps one weight");
   static_assert(USED_COLS <= 512, "TMEM budget");
   static_assert(NPIECE % NWG == 0, "epilogue pieces per warpgroup");
-  static_assert(R_EARLY || NPIECE * PIECE_BYTES <= S * B_BYTES, "output pieces fit the operand ring");
-  static_assert(!R_LATE || B_BYTES == PIECE_BYTES, "a late residual piece is one ring slot");
-  static_assert(BN != 256 || (B_BYTES == PIECE_BYTES && S_RAW * RAW_BYTES >= 2 * PIECE_BYTES),
-                "split: a piece is one ring slot, the raw ring holds the partner's two pieces");
+  static_assert(BN != 256 || S_RAW * RAW_BYTES >= 2 * PIECE_BYTES, "split: the raw ring holds the partner's two pieces");
 };
 
 // ---------------------------------------------------------------- dequant
@@ -178,15 +164,11 @@ __device__ __forceinline__ __half2 scale2(uint32_t dbits) {
   return u32_as_h2((dbits & 0xFFFFu) | (dbits << 16));
 }
 
-// Decodes one row's two blocks (64 k) at `src` (4-byte aligned) into 32 fp16
-// pairs in k order: a[j] = (w_2j, w_2j+1), j = 0..31.
+// Decodes one row's two blocks (64 k), held as the words w[0 .. 2 BB / 4),
+// into 32 fp16 pairs in k order: a[j] = (w_2j, w_2j+1), j = 0..31.
 template <int QT>
-__device__ __forceinline__ void dequant_row_stage(const uint8_t* src, uint32_t (&a)[32]) {
-  const uint32_t* s32 = reinterpret_cast<const uint32_t*>(src);
+__device__ __forceinline__ void dequant_row_stage(const uint32_t* w, uint32_t (&a)[32]) {
   if constexpr (QT == kQ4_0) {
-    uint32_t w[9];
-#pragma unroll
-    for (int i = 0; i < 9; ++i) w[i] = s32[i];
     // block 0: d in bytes 0-1, payload in bytes 2..17; block 1: d in 18-19, payload 20..35
     uint32_t p[8];
 #pragma unroll
@@ -208,9 +190,6 @@ __device__ __forceinline__ void dequant_row_stage(const uint8_t* src, uint32_t (
       }
     }
   } else {
-    uint32_t w[17];
-#pragma unroll
-    for (int i = 0; i < 17; ++i) w[i] = s32[i];
     // block 0: d in bytes 0-1, payload 2..33; block 1: d in 34-35, payload 36..67
     const __half2 d0 = scale2(w[0] & 0xFFFFu);
     const __half2 d1 = scale2(w[8] >> 16);
@@ -227,20 +206,20 @@ __device__ __forceinline__ void dequant_row_stage(const uint8_t* src, uint32_t (
 
 
 // ---------------------------------------------------------------- kernel
-template <int QT, int EPI, int BN, bool TIO>
-__global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
+template <int QT, int EPI, int BN>
+__global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWu,
-                   const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmR,
-                   const __grid_constant__ CUtensorMap tmY, int n, int k, int T, float* Y, int ldy, const float* R,
-                   unsigned* status, int w_early) {
-  using C = Cfg<QT, EPI, BN, TIO>;
+                   const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmR, int n, int k,
+                   int T, float* Y, int ldy, const float* R, unsigned* status, int early) {
+  // early: bits 0-3 what may be read before the dependency wait (kEarly*),
+  // bit 4 set when tmR describes the residual (L2 prefetches of it)
+  using C = Cfg<QT, EPI, BN>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, by pointer arithmetic on the shared array so that
   // the compiler keeps the shared address space (shared loads, not generic)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sB = smem + C::OFF_B;
   uint8_t* sRaw = smem + C::OFF_RAW;
-  float* sStage = reinterpret_cast<float*>(smem + C::OFF_STAGE);  // output pieces (and residual)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* full = bars;              // stage ready: B landed and every A writer arrived
   uint64_t* empty = full + C::S;      // stage free: its MMAs completed
@@ -248,9 +227,8 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
   uint64_t* rawEmpty = rawFull + C::S_RAW;
   uint64_t* accFull = rawEmpty + C::S_RAW;
   uint64_t* drain = accFull + 1;
-  uint64_t* rPiece = drain + 1;       // residual piece p landed
-  uint64_t* peerFree = rPiece + 4;    // split: the partner's raw ring is free to receive
-  uint64_t* xferFull = peerFree + 1;  // split: the partner's half has landed in this raw ring
+  uint64_t* peerFree = drain + 1;     // split: the partner's raw ring is free to receive
+  uint64_t* xferFull = peerFree + 1;  // split: [wg] the partner's piece for warpgroup wg has landed
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -276,13 +254,13 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
     }
     for (int i = 0; i < C::S_RAW; ++i) {
       mbar_init(&rawFull[i], 1);
-      mbar_init(&rawEmpty[i], 4 * C::DQ);
+      mbar_init(&rawEmpty[i], 4 * C::DQ);  // every warpgroup of the weight reads the chunk
     }
     mbar_init(accFull, 1);
     mbar_init(drain, 1);
-    for (int p = 0; p < 4; ++p) mbar_init(&rPiece[p], 1);
     mbar_init(peerFree, 1);
-    mbar_init(xferFull, 1);
+    // one arrival per thread of the partner's sending warpgroup
+    for (int w = 0; w < 2; ++w) mbar_init(&xferFull[w], 128);
     abort_flag[0] = 0;   // set by a wait that gives up
     abort_flag[1] = 0;   // never set: drain waits ignore the abort
     fence_mbar_init();
@@ -308,10 +286,10 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
       for (int c = 0; c < PF && c < nchunks; ++c)
         for (int m = 0; m < C::NM; ++m)
           tma_prefetch_l2_2d(m ? (const void*)&tmWu : (const void*)&tmW, (c0 + c) * (C::RAW_ROW / 2), m0);
-      if (!w_early) grid_dependency_wait();
+      if ((early & 15) == kEarlyNone) grid_dependency_wait();
       int last_issued[C::S_RAW];
       for (int i = 0; i < C::S_RAW; ++i) last_issued[i] = -1;
-      bool ok = true, r_issued = false;
+      bool ok = true;
       for (int c = 0; c < nchunks && ok; ++c) {
         for (int m = 0; m < C::NM && ok; ++m) {
           const int j = c * C::NM + m;
@@ -323,15 +301,6 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
           tma_load_2d(sRaw + slot * C::RAW_BYTES, map, (c0 + c) * (C::RAW_ROW / 2), m0, &rawFull[slot]);
           if (c + PF < nchunks) tma_prefetch_l2_2d(map, (c0 + c + PF) * (C::RAW_ROW / 2), m0);
           last_issued[slot] = j;
-        }
-        // the residual tile, needed only by the epilogue, once the raw ring is full
-        if (C::R_EARLY && ok && !r_issued && (c == C::S_RAW - 1 || c == nchunks - 1)) {
-          for (int p = 0; p < C::NPIECE; ++p) {
-            if (!live(p)) continue;
-            mbar_arrive_expect_tx(&rPiece[p], PIECE_BYTES);
-            tma_load_2d(sStage + p * (PIECE_BYTES / 4), &tmR, m0, t0 + p * PIECE, &rPiece[p]);
-          }
-          r_issued = true;
         }
       }
       if (ok && nsplit == 2) {
@@ -345,13 +314,9 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
         cluster_arrive();
         cl_done = true;
       }
-      if (!ok) {  // let the copies in flight land before the CTA exits
+      if (!ok)  // let the copies in flight land before the CTA exits
         for (int i = 0; i < C::S_RAW; ++i)
           if (last_issued[i] >= 0) mbar_wait(&rawFull[i], (last_issued[i] / C::S_RAW) & 1, abort_flag + 1, status);
-        if (r_issued)
-          for (int p = 0; p < C::NPIECE; ++p)
-            if (live(p)) mbar_wait(&rPiece[p], 0, abort_flag + 1, status);
-      }
     }
   } else if (warp == 2) {
     // ------------------------------------------------ activation producer
@@ -359,9 +324,6 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
       tma_prefetch_desc(&tmX);
       // X is written by the conversion kernel, which may still be running
       grid_dependency_wait();
-      if (C::R_LATE)
-        for (int p = 0; p < C::NPIECE; ++p)
-          if (kept(p) && live(p)) tma_prefetch_l2_2d(&tmR, m0, t0 + p * PIECE);
       bool ok = true;
       int last = -1;
       for (int i = 0; i < nk; ++i) {
@@ -371,29 +333,16 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
         mbar_arrive_expect_tx(&full[st], C::B_BYTES);
         tma_load_2d(sB + st * C::B_BYTES, &tmX, (c0 * SUBS + i) * BK, t0, &full[st]);
         last = i;
+        // the residual pieces this CTA finalizes, into L2 a few stages before
+        // the end (the epilogue threads load them into registers)
+        if (EPI == kEpiResidual && (early & 16) && i == (nk > 2 * C::S ? nk - 2 * C::S : 0))
+          for (int p = 0; p < C::NPIECE; ++p)
+            if (kept(p) && live(p)) tma_prefetch_l2_2d(&tmR, m0, t0 + p * PIECE);
       }
-      // residual pieces into the ring slots as the last MMAs free them (slot
-      // p holds piece p)
-      unsigned r_issued = 0;
-      if (C::R_LATE && ok) {
-        for (int v = nk; v < nk + C::S; ++v) {
-          const int p = v % C::S;
-          if (!kept(p) || !live(p)) continue;
-          ok = mbar_wait(&empty[p], ((v / C::S) & 1) ^ 1, abort_flag, status);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&rPiece[p], PIECE_BYTES);
-          tma_load_2d(sB + p * C::B_BYTES, &tmR, m0, t0 + p * PIECE, &rPiece[p]);
-          r_issued |= 1u << p;
-        }
-      }
-      if (!ok) {
-        // After a give-up, wait (bounded) on the last stage issued: its phase
-        // also needs the dequant warps, so it may never complete, but by the
-        // time the bounded wait ends every copy issued has landed.
-        if (last >= 0) mbar_wait(&full[last % C::S], (last / C::S) & 1, abort_flag + 1, status);
-        for (int p = 0; p < 4; ++p)
-          if (r_issued & (1u << p)) mbar_wait(&rPiece[p], 0, abort_flag + 1, status);
-      }
+      // After a give-up, wait (bounded) on the last stage issued: its phase
+      // also needs the dequant warps, so it may never complete, but by the time
+      // the bounded wait ends every copy issued has landed.
+      if (!ok && last >= 0) mbar_wait(&full[last % C::S], (last / C::S) & 1, abort_flag + 1, status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (whole warp)
@@ -443,15 +392,19 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
       const int slot = j % C::S_RAW;
       ok = __all_sync(0xffffffffu, mbar_wait(&rawFull[slot], (j / C::S_RAW) & 1, abort_flag, status));
       if (!ok) break;
-      const uint8_t* raw_row = sRaw + slot * C::RAW_BYTES + r * C::RAW_ROW;
+      const uint32_t* raw_row = reinterpret_cast<const uint32_t*>(sRaw + slot * C::RAW_BYTES + r * C::RAW_ROW);
       for (int s = par; s < SUBS; s += C::DQ) {
         const int i = c * SUBS + s;
         const int st = i % C::S;
-        uint32_t a[32];
-        dequant_row_stage<QT>(raw_row + s * 2 * C::BB, a);  // overlaps the wait below
+        uint32_t w[2 * C::BB / 4], a[32];
+#pragma unroll
+        for (int v = 0; v < 2 * C::BB / 4; ++v) w[v] = raw_row[s * (2 * C::BB / 4) + v];
+        dequant_row_stage<QT>(w, a);  // overlaps the wait below
         ok = __all_sync(0xffffffffu, mbar_wait(&empty[st], ((i / C::S) & 1) ^ 1, abort_flag, status));
         if (!ok) break;
         tc_fence_after();
+        // tcgen05.st reads its source registers asynchronously: a[] stays
+        // untouched until the wait
         tmem_st_32x32b_x32(lane_base + C::A_COL0 + (g * C::S + st) * C::A_COLS, a);
         tmem_st_wait();
         tc_fence_before();
@@ -465,122 +418,99 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, TIO>::NTHREADS, 1)
     // ---------------------------------------------- epilogue
     // Y and R may still be in use by the preceding kernel
     grid_dependency_wait();
+    const int row = m0 + (int)r;
+    constexpr int PPW = C::NPIECE / C::NWG;
+    const int npw = nsplit == 2 ? 1 : PPW;
+    // the pieces this warpgroup finalizes: all of the tile's pieces split
+    // evenly, or with a split piece 2 z + wg
+    auto piece = [&](int pp) { return nsplit == 2 ? 2 * z + wg : wg * PPW + pp; };
+    // residual of piece p into registers (coalesced: the warp's lanes read 32
+    // consecutive floats of one token's row)
+    float rv[PIECE];
+    auto load_r = [&](int p) {
+#pragma unroll
+      for (int j = 0; j < PIECE; ++j) {
+        const int t = t0 + p * PIECE + j;
+        rv[j] = (EPI == kEpiResidual && t < T && row < n) ? R[(size_t)t * ldy + row] : 0.f;
+      }
+    };
+    if (EPI == kEpiResidual && ok && live(piece(0))) load_r(piece(0));
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(accFull, 0, abort_flag, status));
     tc_fence_after();
-    const int row = m0 + (int)r;
-    const bool lead = (warp & 3) == 0 && lane == 0;  // issues its warpgroup's TMA stores
-    bool stored = false;
 
     if (nsplit == 2) {
-      // stage the piece the partner keeps in this CTA's (now idle) ring slot
-      // pg, [64 tokens][128 rows], and send it to the partner's raw ring, at
-      // 32 KB x wg; the partner's copy of piece pk lands in this raw ring the
-      // same way
+      // the piece the partner keeps, pg, goes from registers straight into the
+      // partner's raw ring at 32 KB x wg ([64 tokens][128 rows]); the
+      // partner's copy of piece pk lands in this raw ring the same way
       const uint32_t peer = (uint32_t)(1 - z);
-      const int pg = 2 * (1 - z) + wg, pk = 2 * z + wg;
-      float* stage = reinterpret_cast<float*>(sB + pg * C::B_BYTES);
+      const int pg = 2 * (1 - z) + wg;
+      cluster_wait();  // the partner has started: its barriers exist
+      cl_started = true;
       if (ok && live(pg)) {
         uint32_t v[64];
         tmem_ld_32x32b_x32(lane_base + pg * PIECE, v);
         tmem_ld_32x32b_x32(lane_base + pg * PIECE + 32, v + 32);
         tmem_ld_wait_regs(v);
         regs_after_wait(v + 32);
+        // the partner's raw ring is free once it has decoded its last chunk
+        bool go = __all_sync(0xffffffffu, mbar_wait_cluster(peerFree, 0, abort_flag, status));
+        if (go) {
+          const uint32_t dst = mapa_shared(smem_u32(sRaw + wg * PIECE_BYTES), peer) + r * 4;
 #pragma unroll
-        for (int j = 0; j < PIECE; ++j) stage[j * BM + r] = __uint_as_float(v[j]);
-        fence_proxy_async_smem();
+          for (int j = 0; j < PIECE; ++j) st_cluster_f32(dst + (uint32_t)(j * BM * 4), __uint_as_float(v[j]));
+          // release: the stores above before the arrival the partner waits on
+          mbar_arrive_remote(mapa_shared(smem_u32(&xferFull[wg]), peer));
+        }
       }
-      cluster_wait();
-      cl_started = true;
-      if (threadIdx.x == 128)  // the bytes of this CTA's live kept pieces
-        mbar_arrive_expect_tx(xferFull, PIECE_BYTES * ((live(2 * z) ? 1 : 0) + (live(2 * z + 1) ? 1 : 0)));
-      named_sync(1 + wg, 128);  // the warpgroup's piece is staged
-      if (lead && live(pg)) {
-        bool go = abort_flag[0] == 0;
-        if (go) go = mbar_wait_cluster(peerFree, 0, abort_flag, status);
-        if (go)
-          bulk_copy_to_peer(mapa_shared(smem_u32(sRaw + wg * PIECE_BYTES), peer), stage, PIECE_BYTES,
-                            mapa_shared(smem_u32(xferFull), peer));
-      }
-      if (ok && live(pk)) ok = __all_sync(0xffffffffu, mbar_wait_cluster(xferFull, 0, abort_flag, status));
-      // the partner's copy has landed: once the partner has seen this CTA's
-      // copy land as well, neither touches the other's shared memory again
+      // this CTA no longer touches the partner's shared memory
       cluster_arrive();
       cl_done = true;
     }
 
-    // finalize this warpgroup's pieces: all of the tile's pieces, split evenly,
-    // or with a split piece 2 z + wg
-    constexpr int PPW = C::NPIECE / C::NWG;
-    const int npw = nsplit == 2 ? 1 : PPW;
     for (int pp = 0; pp < npw; ++pp) {
-      const int p = nsplit == 2 ? 2 * z + wg : wg * PPW + pp;
+      const int p = piece(pp);
       if (!live(p)) continue;  // the same for the whole warpgroup
-      float* sp = sStage + p * (PIECE_BYTES / 4);
+      if (pp > 0 && EPI == kEpiResidual && ok) load_r(p);
       uint32_t v[64];
-      if (ok) {
-        tmem_ld_32x32b_x32(lane_base + p * PIECE, v);
-        tmem_ld_32x32b_x32(lane_base + p * PIECE + 32, v + 32);
-        tmem_ld_wait_regs(v);
-        regs_after_wait(v + 32);
-        if (C::NM == 2) {  // y = silu(gate) * up
-          uint32_t u[64];
-          tmem_ld_32x32b_x32(lane_base + BN + p * PIECE, u);
-          tmem_ld_32x32b_x32(lane_base + BN + p * PIECE + 32, u + 32);
-          tmem_ld_wait_regs(u);
-          regs_after_wait(u + 32);
+      if (ok && nsplit == 2)  // the partner's half of this piece has landed
+        ok = __all_sync(0xffffffffu, mbar_wait_cluster(&xferFull[wg], 0, abort_flag, status));
+      if (!ok) continue;
+      tmem_ld_32x32b_x32(lane_base + p * PIECE, v);
+      tmem_ld_32x32b_x32(lane_base + p * PIECE + 32, v + 32);
+      tmem_ld_wait_regs(v);
+      regs_after_wait(v + 32);
+      if (C::NM == 2) {  // y = silu(gate) * up
+        uint32_t u[64];
+        tmem_ld_32x32b_x32(lane_base + BN + p * PIECE, u);
+        tmem_ld_32x32b_x32(lane_base + BN + p * PIECE + 32, u + 32);
+        tmem_ld_wait_regs(u);
+        regs_after_wait(u + 32);
 #pragma unroll
-          for (int j = 0; j < PIECE; ++j) {
-            const float gt = __uint_as_float(v[j]);
-            v[j] = __float_as_uint(gt / (1.0f + expf(-gt)) * __uint_as_float(u[j]));
-          }
+        for (int j = 0; j < PIECE; ++j) {
+          const float gt = __uint_as_float(v[j]);
+          v[j] = __float_as_uint(gt / (1.0f + expf(-gt)) * __uint_as_float(u[j]));
         }
-        if (nsplit == 2) {  // p0 + p1, in split order
-          const float* src = reinterpret_cast<const float*>(sRaw + wg * PIECE_BYTES) + r;
-#pragma unroll
-          for (int j = 0; j < PIECE; ++j) {
-            const float o = src[j * BM];
-            const float mine = __uint_as_float(v[j]);
-            v[j] = __float_as_uint(z == 0 ? mine + o : o + mine);
-          }
-        }
-        if (EPI == kEpiResidual && TIO)
-          ok = __all_sync(0xffffffffu, mbar_wait(&rPiece[p], 0, abort_flag, status));
       }
-      if constexpr (TIO) {
-        if (ok) {
+      if (nsplit == 2) {  // p0 + p1, in split order
+        const float* src = reinterpret_cast<const float*>(sRaw + wg * PIECE_BYTES) + r;
 #pragma unroll
-          for (int j = 0; j < PIECE; ++j) {
-            float y = __uint_as_float(v[j]);
-            if (EPI == kEpiResidual) y += sp[j * BM + r];
-            sp[j * BM + r] = y;
-          }
-          fence_proxy_async_smem();
+        for (int j = 0; j < PIECE; ++j) {
+          const float o = src[j * BM];
+          const float mine = __uint_as_float(v[j]);
+          v[j] = __float_as_uint(z == 0 ? mine + o : o + mine);
         }
-        named_sync(1 + wg, 128);  // every warp of the warpgroup reaches it
-        if (lead && abort_flag[0] == 0) {
-          tma_store_2d(&tmY, sp, m0, t0 + p * PIECE);
-          bulk_commit_group();
-          stored = true;
-        }
-      } else if (ok && row < n) {
-        // direct: R row t is read before Y row t is written (Y may be R)
+      }
+      if (row < n) {
+        // R row t was read before Y row t is written (Y may be R), by this thread
 #pragma unroll
-        for (int j0 = 0; j0 < PIECE; j0 += 16) {
-          float rv[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int t = t0 + p * PIECE + j0 + j;
-            rv[j] = (EPI == kEpiResidual && t < T) ? R[(size_t)t * ldy + row] : 0.f;
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int t = t0 + p * PIECE + j0 + j;
-            if (t < T) Y[(size_t)t * ldy + row] = __uint_as_float(v[j0 + j]) + rv[j];
-          }
+        for (int j = 0; j < PIECE; ++j) {
+          const int t = t0 + p * PIECE + j;
+          float y = __uint_as_float(v[j]);
+          if (EPI == kEpiResidual) y += rv[j];
+          if (t < T) Y[(size_t)t * ldy + row] = y;
         }
       }
     }
-    if (stored) bulk_wait_read_all();  // the pieces stay in shared memory until read
     tc_fence_before();
   }
 
@@ -636,10 +566,10 @@ __global__ void __launch_bounds__(256, 4) x_to_f16_kernel(const float* __restric
 }
 
 // ---------------------------------------------------------------- host side
-template <int QT, int EPI, int BN, bool TIO>
+template <int QT, int EPI, int BN>
 int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y, int ldy,
-               const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, int w_early) {
-  using C = Cfg<QT, EPI, BN, TIO>;
+               const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, int early) {
+  using C = Cfg<QT, EPI, BN>;
   auto fn = encode_fn(msg, msg_len);
   if (!fn) return -1;
   CUtensorMap mW, mWu;
@@ -659,21 +589,19 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
   if (!make_map_2d(fn, &mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X16, (uint64_t)k, (uint64_t)T, (uint64_t)k * 2, BK, BN,
                    CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
     return -1;
-  // residual and output pieces: [T] rows of n fp32, ldy apart, box 128 rows x
-  // 64 tokens
-  CUtensorMap mR = mX, mY = mX;
-  if (C::R_EARLY || C::R_LATE) {
+  // the residual, [T] rows of n fp32 ldy apart, only for L2 prefetches of
+  // 128-row x 64-token boxes: a row stride that is not a multiple of 16
+  // bytes cannot be described, and then nothing is prefetched
+  CUtensorMap mR = mX;
+  int r_pf = 0;
+  if (EPI == kEpiResidual && (ldy % 4) == 0 && ((uintptr_t)R & 15) == 0) {
     if (!make_map_2d(fn, &mR, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, R, (uint64_t)n, (uint64_t)T, (uint64_t)ldy * 4, BM,
                      PIECE, CU_TENSOR_MAP_SWIZZLE_NONE, msg, msg_len))
       return -1;
-  }
-  if (C::TIO) {
-    if (!make_map_2d(fn, &mY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, Y, (uint64_t)n, (uint64_t)T, (uint64_t)ldy * 4, BM,
-                     PIECE, CU_TENSOR_MAP_SWIZZLE_NONE, msg, msg_len))
-      return -1;
+    r_pf = 1;
   }
 
-  auto kern = gemm_tc_kernel<QT, EPI, BN, TIO>;
+  auto kern = gemm_tc_kernel<QT, EPI, BN>;
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -700,7 +628,7 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
     cfg.numAttrs = 2;
   }
   cfg.attrs = attr;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mW, mWu, mX, mR, mY, n, k, T, Y, ldy, R, status, w_early);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mW, mWu, mX, mR, n, k, T, Y, ldy, R, status, early | (r_pf << 4));
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     snprintf(msg, msg_len, "gemm_tc launch: %s", cudaGetErrorString(e));
@@ -709,30 +637,16 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
   return 0;
 }
 
-template <int QT, int EPI, int BN>
-int launch_io(bool tio, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y, int ldy,
-              const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, int w_early) {
-  return tio ? launch_cfg<QT, EPI, BN, true>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, nsplit, w_early)
-             : launch_cfg<QT, EPI, BN, false>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, nsplit,
-                                              w_early);
-}
-
 template <int QT>
 int launch_q(const GemmPlan& pl, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y,
              int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int w) {
-  // TMA for the residual and the output when a row of them is a multiple of
-  // 16 bytes long and starts on one (n and ldy multiples of 4)
-  const bool tio = (n % 4) == 0 && (ldy % 4) == 0;
-  if (Wu) return launch_io<QT, kEpiSwiGLU, 128>(tio, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w);
+  if (Wu) return launch_cfg<QT, kEpiSwiGLU, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w);
   if (pl.bn == 256) {
-    if (R)
-      return launch_io<QT, kEpiResidual, 256>(tio, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len,
-                                              pl.nsplit, w);
-    return launch_io<QT, kEpiPlain, 256>(tio, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, pl.nsplit,
-                                         w);
+    if (R) return launch_cfg<QT, kEpiResidual, 256>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, pl.nsplit, w);
+    return launch_cfg<QT, kEpiPlain, 256>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, pl.nsplit, w);
   }
-  if (R) return launch_io<QT, kEpiResidual, 128>(tio, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w);
-  return launch_io<QT, kEpiPlain, 128>(tio, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w);
+  if (R) return launch_cfg<QT, kEpiResidual, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w);
+  return launch_cfg<QT, kEpiPlain, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w);
 }
 
 }  // namespace
@@ -778,8 +692,8 @@ GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu) {
 
 int launch_gemm_tc(const GemmPlan& pl, int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16,
                    int T, float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg,
-                   size_t msg_len, bool after_conversion) {
-  const int w = after_conversion ? 1 : 0;
+                   size_t msg_len, int early) {
+  const int w = early;
   return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w)
                         : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w);
 }

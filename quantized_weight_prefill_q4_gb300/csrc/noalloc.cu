@@ -102,7 +102,7 @@ extern "C" int apr_qgemm_noalloc(int qtype, const void* W, int n, int k, const f
   char msg[256] = "";
   const GemmPlan plan = plan_gemm_tc(n, k, T, false);
   if (launch_gemm_tc(plan, qtype, W, nullptr, n, k, st->scratch, T, Y, n, residual, st->status, s, msg, sizeof msg,
-                     true) != 0)
+                     kEarlyWR) != 0)
     return set_error(APR_E_LAUNCH, msg);
   return APR_OK;
 }
