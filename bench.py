@@ -607,8 +607,9 @@ def every_workload(q, dev, stream, peak_tf, peak_gbs):
       tokens, Q4_0 and Q8_0;
     * the small-T GEMV sweep: T in {1, 2, 4, 8, 16} over 4096 x 4096 and
       12288 x 4096, Q4_0 and Q8_0 (GB/s against the HBM rate);
-    * the T rule: the GEMV against the forced tensor-core GEMM at T = 4..16
-      (Q4_0, both weights), and the GEMM at 24 and 32;
+    * the T rule: the GEMV (exact) against the forced tensor-core GEMM on the
+      fp16 leg and on the exact leg at T = 4..16 (Q4_0, both weights), and the
+      GEMMs at 24 and 32;
     * a 9B-class layer's projections (qkv 6144 x 4096, out 4096 x 4096 + R,
       gate/up 12288 x 4096, down 4096 x 12288 + R, Q4_0) at 512 and 2048 rows
       on the fp16 leg and the exact-fp32 leg."""
@@ -632,7 +633,8 @@ def every_workload(q, dev, stream, peak_tf, peak_gbs):
     rule = {}
     for n in (4096, 12288):
         for T in (4, 8, 12, 16, 24, 32):
-            row = {"gemm_us": P(qtype=Q4, n=n, k=4096, T=T, path=2)["us"]}
+            row = {"gemm_us": P(qtype=Q4, n=n, k=4096, T=T, path=2)["us"],
+                   "exact_gemm_us": P(qtype=Q4, n=n, k=4096, T=T, path=2, leg=1)["us"]}
             if T <= 16:
                 row["gemv_us"] = P(qtype=Q4, n=n, k=4096, T=T, path=1)["us"]
             rule[f"q4_0_n{n}_k4096_t{T}"] = row

@@ -113,9 +113,16 @@ enum {
 };
 
 /*
- * The T rule: with APR_PATH_AUTO, 1 <= T <= apr_gemv_max_T() runs the small-T
- * GEMV (exact fp32 arithmetic whatever the leg), T above it runs the GEMM.
+ * The T rule, fixed and measured on GB300 (Q4_0, 4096 x 4096 and 12288 x 4096
+ * weights): with APR_PATH_AUTO, 1 <= T <= APR_AUTO_GEMV_MAX_T runs the small-T
+ * GEMV (exact fp32 arithmetic whatever the leg), larger T runs the GEMM of
+ * the call's leg. At T = 4 the GEMV takes 15-26 us against 32-68 us for the
+ * tensor-core GEMM; from T = 8 the fp16-leg GEMM is faster (19 against 32 us,
+ * 57 against 80 us), because the CUDA-core GEMV's work grows with T.
+ * APR_GEMV_MAX_T (apr_gemv_max_T()) is the largest T the GEMV path itself
+ * takes (APR_PATH_GEMV, apr_qgemv).
  */
+#define APR_AUTO_GEMV_MAX_T 7
 #define APR_GEMV_MAX_T 16
 int apr_gemv_max_T(void);
 
@@ -145,11 +152,15 @@ int apr_qgemm_gate_up_swiglu(int qtype, const void* Wg, const void* Wu, int n, i
                              const float* X, int T, float* Y, apr_stream_t stream);
 
 /*
- * Small-T GEMV, 1 <= T <= APR_GEMV_MAX_T (T == 0 is a no-op): weight rows
- * streamed by bulk copies, T fp32 accumulators, exact fp32 arithmetic,
- * optional residual (gemv_q4_0_pf / gemv_q8_0_pf of oxibonsai-kernels, used
- * for the last-token lm_head in try_cuda_prefill_q_std). T > APR_GEMV_MAX_T
- * gives APR_E_INVAL. The weights are read early (see stream order above).
+ * Small-T GEMV, 1 <= T <= APR_GEMV_MAX_T (T == 0 is a no-op), exact fp32
+ * arithmetic, optional residual (gemv_q4_0_pf / gemv_q8_0_pf of
+ * oxibonsai-kernels, used for the last-token lm_head in
+ * try_cuda_prefill_q_std). For T <= 8 weight rows stream by bulk copies into
+ * T fp32 accumulators (tensor cores for T = 3, 4); for 9 <= T <= 16 (k % 256
+ * == 0) the exact leg's tensor-core GEMM runs instead (50 us against 200 to
+ * 700 us for the CUDA-core kernels at 4096 x 4096 and 12288 x 4096, T = 12
+ * and 16). T > APR_GEMV_MAX_T gives APR_E_INVAL. The weights are read early
+ * (see stream order above).
  */
 int apr_qgemv(int qtype, const void* W, int n, int k, const float* X, int T,
               float* Y, const float* residual, apr_stream_t stream);
@@ -157,7 +168,13 @@ int apr_qgemv(int qtype, const void* W, int n, int k, const float* X, int T,
 /*
  * Full form. Wu != NULL selects the gate/up SwiGLU product (W is the gate;
  * residual must be NULL). leg and path as above; APR_PATH_GEMV needs
- * T <= APR_GEMV_MAX_T. The exact leg on the GEMM path runs fp32 FFMA.
+ * T <= APR_GEMV_MAX_T. The exact leg on the GEMM path runs on the tensor
+ * cores when k % 256 == 0: the weight (times a power of two per row) and X
+ * (per token) split into two fp16 pieces each, three products per term
+ * (W1.X1 + W1.X2 + W2.X1), fp32 accumulation restarted every 256 k and the
+ * partial sums added in fp32 (relative error about 1e-6 at k = 4096 and
+ * 12288); gate/up takes two such products and an elementwise SwiGLU. Other
+ * k run fp32 FFMA.
  * ldy: strided output. Row t of Y starts at Y + t * ldy (and row t of
  * residual at residual + t * ldy), so Y can be a slice of a wider buffer, such
  * as the rows of a KV cache (aprender-serve writes attn_v straight into the

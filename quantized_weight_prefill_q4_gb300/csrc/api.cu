@@ -97,7 +97,8 @@ enum ScratchUse {
   kScratchFfn = 2,
   kScratchNorm = 3,
   kScratchAttn = 4,
-  kScratchLayer = 5
+  kScratchLayer = 5,
+  kScratchExact = 6
 };
 struct StreamScratch {
   int dev;
@@ -223,7 +224,14 @@ int run(const Problem& p) {
   if (rc != APR_OK) return rc;
 
   int path = p.path;
-  if (path == APR_PATH_AUTO) path = p.T <= APR_GEMV_MAX_T ? APR_PATH_GEMV : APR_PATH_GEMM;
+  if (path == APR_PATH_AUTO) path = p.T <= APR_AUTO_GEMV_MAX_T ? APR_PATH_GEMV : APR_PATH_GEMM;
+  // from T = 9 the exact leg's tensor-core GEMM beats the CUDA-core GEMVs
+  // (their FFMA work grows with T): the GEMV path takes it there
+  int leg = p.leg;
+  if (path == APR_PATH_GEMV && p.T > 8 && p.k % 256 == 0) {
+    path = APR_PATH_GEMM;
+    leg = APR_LEG_EXACT_F32;
+  }
   if (path == APR_PATH_GEMV) {
     if (!gemv_tc_takes(p.n, p.k, p.T, p.Wu != nullptr))
       return launched(launch_gemv(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, ldy_of(p), p.R, st->status, p.s),
@@ -241,12 +249,35 @@ int run(const Problem& p) {
   }
   // GEMM: the tensor-core kernels need every raw 256-column chunk of a weight
   // row to start on a 16-byte boundary (k % 256 == 0); other k run the FFMA
-  // kernel (exact fp32, whatever the leg). The exact leg runs the FFMA kernel
-  // too: a tensor-core form of it (three tf32 products per term) drifts past
-  // 1e-5 relative error at k = 4096, because the tensor core's fp32
-  // accumulator is not rounded like FFMA.
-  if (p.k % 256 != 0 || p.leg == APR_LEG_EXACT_F32)
+  // kernel (exact fp32, whatever the leg).
+  if (p.k % 256 != 0)
     return launched(launch_gemm_simt(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, ldy_of(p), p.R, p.s), "gemm_simt");
+  if (leg == APR_LEG_EXACT_F32) {
+    // the exact leg on the tensor cores: three fp16 products per term of the
+    // split operands; the stream's scratch holds the split X, its token
+    // exponents and the weight rows' exponents (and, for gate/up, the two
+    // products before the SwiGLU)
+    const size_t xs = (gemm_xs_scratch_bytes(p.n, p.k, p.T, false) + 255) & ~(size_t)255;
+    const size_t gu = p.Wu ? 2 * (((size_t)p.T * p.n * 4 + 255) & ~(size_t)255) : 0;
+    void* scratch = nullptr;
+    rc = stream_scratch(st->dev, p.s, kScratchExact, xs + gu, &scratch);
+    if (rc != APR_OK) return rc;
+    char msg[256] = "";
+    if (!p.Wu) {
+      if (launch_gemm_xs(p.qtype, p.W, nullptr, p.n, p.k, p.X, p.T, p.Y, ldy_of(p), p.R, scratch, st->status, p.s,
+                         msg, sizeof msg) != 0)
+        return fail(APR_E_LAUNCH, "%s", msg);
+      return APR_OK;
+    }
+    float* G = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + xs);
+    float* U = G + (((size_t)p.T * p.n * 4 + 255) & ~(size_t)255) / 4;
+    if (launch_gemm_xs(p.qtype, p.W, nullptr, p.n, p.k, p.X, p.T, G, p.n, nullptr, scratch, st->status, p.s, msg,
+                       sizeof msg) != 0 ||
+        launch_gemm_xs(p.qtype, p.Wu, nullptr, p.n, p.k, p.X, p.T, U, p.n, nullptr, scratch, st->status, p.s, msg,
+                       sizeof msg) != 0)
+      return fail(APR_E_LAUNCH, "%s", msg);
+    return launched(launch_swiglu_rows(G, U, p.T, p.n, p.Y, ldy_of(p), p.s), "swiglu_rows");
+  }
 
   // the stream's scratch holds the fp16 copy of X
   const GemmPlan plan = plan_gemm_tc(p.n, p.k, p.T, p.Wu != nullptr);
@@ -304,7 +335,7 @@ int run_ffn(const apr_ffn_args& a) {
   for (int t0 = 0; t0 < a.T; t0 += chunk) {
     const int rows = a.T - t0 < chunk ? a.T - t0 : chunk;
     float* Xc = a.X + (size_t)t0 * a.hidden;
-    const bool tc = a.leg == APR_LEG_F16 && rows > APR_GEMV_MAX_T && a.hidden % 256 == 0 && a.inter % 256 == 0;
+    const bool tc = a.leg == APR_LEG_F16 && rows > APR_AUTO_GEMV_MAX_T && a.hidden % 256 == 0 && a.inter % 256 == 0;
     rc = launched(launch_rmsnorm_rows(Xc, a.norm_weight, a.eps, rows, a.hidden, h, tc, s), "rmsnorm");
     if (rc != APR_OK) return rc;
     if (tc) {
@@ -345,7 +376,7 @@ int run_normed(const Problem& p, const float* w, float eps) {
   rc = device_state(&st);
   if (rc != APR_OK) return rc;
   int path = p.path;
-  if (path == APR_PATH_AUTO) path = p.T <= APR_GEMV_MAX_T ? APR_PATH_GEMV : APR_PATH_GEMM;
+  if (path == APR_PATH_AUTO) path = p.T <= APR_AUTO_GEMV_MAX_T ? APR_PATH_GEMV : APR_PATH_GEMM;
   const bool tc = p.leg == APR_LEG_F16 && path == APR_PATH_GEMM && p.k % 256 == 0;
   const int chunk = p.T < APR_FFN_CHUNK_ROWS ? p.T : APR_FFN_CHUNK_ROWS;
   void* h = nullptr;
@@ -443,7 +474,7 @@ int run_layer(const apr_layer_args& a) {
     const int pos = a.pos0 + t0;
     float* Xc = a.X + (size_t)t0 * a.hidden;
     // 1. norm, then q, k, v: k and v straight into the cache rows pos ..
-    const bool tc = a.leg == APR_LEG_F16 && rows > APR_GEMV_MAX_T && a.hidden % 256 == 0;
+    const bool tc = a.leg == APR_LEG_F16 && rows > APR_AUTO_GEMV_MAX_T && a.hidden % 256 == 0;
     rc = launched(launch_rmsnorm_rows(Xc, a.attn_norm, a.eps, rows, a.hidden, h, tc, s), "rmsnorm");
     if (rc != APR_OK) return rc;
     const void* Wp[3] = {Wq, Wk, Wv};

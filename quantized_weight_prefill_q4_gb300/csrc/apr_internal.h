@@ -102,6 +102,20 @@ int launch_gemm_tc(const GemmPlan& plan, int qtype, const void* W, const void* W
 // then records the timeout in the status word and returns (selftest.cu).
 cudaError_t launch_bounded_wait(unsigned long long limit_ns, unsigned* status, cudaStream_t s);
 
+// Exact leg on the tensor cores (gemm_tc.cu), k % 256 == 0, one weight (Wu
+// must be null): per weight row an exponent e (max |d| * max |q'| * 2^e in
+// [2^14, 2^15)), X split per token into two fp16 pieces of X * 2^e', then
+// W1.X1 + W1.X2 + W2.X1 per 16-k step with W * 2^e = W1 + W2, fp32
+// accumulation restarted every 256 k and summed in fp32, the powers of two
+// undone in the epilogue. Two plain launches (row exponents, the X split)
+// and the GEMM; `scratch` holds gemm_xs_scratch_bytes(). Returns 0, or -1
+// with a message.
+size_t gemm_xs_scratch_bytes(int n, int k, int T, bool swiglu);
+// y = silu(g) * u over T rows of n (G, U dense; rows of Y ldy apart).
+cudaError_t launch_swiglu_rows(const float* G, const float* U, int T, int n, float* Y, int ldy, cudaStream_t s);
+int launch_gemm_xs(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
+                   const float* R, void* scratch, unsigned* status, cudaStream_t s, char* msg, size_t msg_len);
+
 // Shared with the allocation-free entry point (api.cu): sets this thread's error
 // message and returns `code`; checks the arguments of a plain / residual GEMM
 // call (APR_OK, an error, or 1 for "nothing to do"); device address of the

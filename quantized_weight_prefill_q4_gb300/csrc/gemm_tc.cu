@@ -82,11 +82,22 @@ constexpr int PF = 4;           // raw chunks prefetched into L2 ahead of their 
 constexpr int PIECE = 64;                      // token columns per epilogue piece
 constexpr int PIECE_BYTES = PIECE * BM * 4;    // one fp32 piece, [64 tokens][128 rows]
 
-template <int QT, int EPI, int BN_>
+// XS: the exact leg. The weight is split W = W1 + W2 and X = X1 + X2 into
+// fp16 pieces (scaled by powers of two per weight row and per token), and
+// each 16-k step runs three MMAs, W1.X1 + W1.X2 + W2.X1: NP = 2 pieces of A
+// and of B per stage. The tensor core's fp32 accumulator loses about 2e-8 of
+// its magnitude per update (measured: 1.35e-5 relative after the 768 updates
+// of k = 4096), so each 256-k chunk accumulates afresh, alternately into two
+// accumulators, and a decode warpgroup adds every finished chunk into a
+// running sum in TMEM with fp32 round-to-nearest additions (acc0, acc1 and
+// the sum: three accumulator regions).
+template <int QT, int EPI, int BN_, bool XS_ = false>
 struct Cfg {
   static constexpr int BN = BN_;
-  static constexpr int A_COLS = 32;                     // TMEM columns of one A stage of one weight
-  static constexpr int B_BYTES = BN * 128;              // one 128-B-swizzled B stage
+  static constexpr bool XS = XS_;
+  static constexpr int NP = XS ? 2 : 1;                 // operand pieces
+  static constexpr int A_COLS = 32;                     // TMEM columns of one A piece of one stage of one weight
+  static constexpr int B_BYTES = BN * 128;              // one 128-B-swizzled B piece of a stage
   static constexpr int NM = EPI == kEpiSwiGLU ? 2 : 1;
   static constexpr int DQ = NM == 1 ? 2 : 1;           // warpgroups per weight (alternate stages)
   static constexpr int NWG = NM * DQ;                   // dequant / epilogue warpgroups
@@ -95,7 +106,7 @@ struct Cfg {
   static constexpr int RAW_BYTES = BM * RAW_ROW;      // one raw slot
   static constexpr int NPIECE = BN / PIECE;
   // operand stages (A in TMEM and B in shared memory advance together)
-  static constexpr int S = NM == 2 ? 4 : (BN == 256 ? 4 : (QT == kQ4_0 ? 6 : 5));
+  static constexpr int S = XS ? 2 : (NM == 2 ? 4 : (BN == 256 ? 4 : (QT == kQ4_0 ? 6 : 5)));
   // (with 256-token tiles the raw ring also receives the partner's half of a
   // split). With gate/up the chunks of the two weights alternate through the
   // ring, chunk j in slot j % S_RAW; S_RAW must be even so that a slot always
@@ -105,15 +116,15 @@ struct Cfg {
   // tell phase p + 2 from phase p.
   static constexpr int S_RAW = NM == 1 ? (QT == kQ4_0 ? (BN == 256 ? 4 : 3) : 2) : 4;
   static constexpr int NTHREADS = 128 + 128 * NWG;
-  static constexpr int ACC_COLS = NM * BN;
+  static constexpr int ACC_COLS = (XS ? 3 : NM) * BN;
   static constexpr int A_COL0 = ACC_COLS;                       // first A column
-  static constexpr int USED_COLS = ACC_COLS + NM * S * A_COLS;
+  static constexpr int USED_COLS = ACC_COLS + NM * S * NP * A_COLS;
   static constexpr int TMEM_COLS = USED_COLS <= 128 ? 128 : USED_COLS <= 256 ? 256 : 512;
   // shared memory layout (offsets from a 1024-aligned base)
   static constexpr int OFF_B = 0;
-  static constexpr int OFF_RAW = OFF_B + S * B_BYTES;
+  static constexpr int OFF_RAW = OFF_B + S * NP * B_BYTES;
   static constexpr int OFF_BAR = OFF_RAW + S_RAW * RAW_BYTES;
-  static constexpr int NBAR = 2 * S + 2 * S_RAW + 2 + 1 + 2;  // + accFull, drain, peerFree, 2 xferFull
+  static constexpr int NBAR = 2 * S + 2 * S_RAW + 2 + 1 + 2 + 4;  // + accFull, drain, peerFree, 2 xferFull, 4 chunk
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 32 + 1024;   // + alignment slack
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -121,6 +132,7 @@ struct Cfg {
   static_assert(USED_COLS <= 512, "TMEM budget");
   static_assert(NPIECE % NWG == 0, "epilogue pieces per warpgroup");
   static_assert(BN != 256 || S_RAW * RAW_BYTES >= 2 * PIECE_BYTES, "split: the raw ring holds the partner's two pieces");
+  static_assert(!XS || (BN == 128 && NM == 1), "the exact leg takes 128-token tiles of one weight");
 };
 
 // ---------------------------------------------------------------- dequant
@@ -205,15 +217,80 @@ __device__ __forceinline__ void dequant_row_stage(const uint32_t* w, uint32_t (&
 }
 
 
+// Exact leg: one row's two blocks (64 k), words w[0 .. 2 BB / 4), into the
+// fp16 pieces of W * 2^e: a1[j] = fp16(v_2j, v_2j+1) and a2[j] = fp16 of the
+// remainders, v = d * q' * 2^e computed exactly in fp32 (an fp16 scale times a
+// code of at most 8 bits, times a power of two). sw = 2^e.
+//   code to float: a code c at bit offset 0 of a word OR-ed into the exponent
+//   of 2^23 is the float 2^23 + c; minus 2^23 + 8 (Q4_0) or 2^23 + 128 (Q8_0,
+//   the byte XOR 0x80) leaves q' exactly.
+__device__ __forceinline__ void split2(float x, float y, uint32_t& h1, uint32_t& h2) {
+  const __half2 a = __floats2half2_rn(x, y);
+  const float2 b = __half22float2(a);
+  const __half2 c = __floats2half2_rn(x - b.x, y - b.y);
+  h1 = h2_as_u32(a);
+  h2 = h2_as_u32(c);
+}
+
+template <int QT>
+__device__ __forceinline__ void dequant_row_stage_xs(const uint32_t* w, float sw, uint32_t (&a1)[32],
+                                                     uint32_t (&a2)[32]) {
+  auto code = [](uint32_t c) { return __uint_as_float(c | 0x4B000000u); };
+  if constexpr (QT == kQ4_0) {
+    uint32_t p[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = __byte_perm(w[i], w[i + 1], 0x5432);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[4 + i] = w[5 + i];
+    const float d0 = __half2float(__ushort_as_half((unsigned short)(w[0] & 0xFFFFu))) * sw;
+    const float d1 = __half2float(__ushort_as_half((unsigned short)(w[4] >> 16))) * sw;
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+      const float d = blk ? d1 : d0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t x = p[blk * 4 + i];  // bytes m = 0..3: elements 4i + m (low), 16 + 4i + m (high)
+        float lo[4], hi[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          lo[m] = (code((x >> (8 * m)) & 0xFu) - 8388616.0f) * d;
+          hi[m] = (code((x >> (8 * m + 4)) & 0xFu) - 8388616.0f) * d;
+        }
+        split2(lo[0], lo[1], a1[16 * blk + 2 * i], a2[16 * blk + 2 * i]);
+        split2(lo[2], lo[3], a1[16 * blk + 2 * i + 1], a2[16 * blk + 2 * i + 1]);
+        split2(hi[0], hi[1], a1[16 * blk + 8 + 2 * i], a2[16 * blk + 8 + 2 * i]);
+        split2(hi[2], hi[3], a1[16 * blk + 8 + 2 * i + 1], a2[16 * blk + 8 + 2 * i + 1]);
+      }
+    }
+  } else {
+    const float d0 = __half2float(__ushort_as_half((unsigned short)(w[0] & 0xFFFFu))) * sw;
+    const float d1 = __half2float(__ushort_as_half((unsigned short)(w[8] >> 16))) * sw;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint32_t x = (c < 8 ? __byte_perm(w[c], w[c + 1], 0x5432) : w[1 + c]) ^ 0x80808080u;
+      const float d = c < 8 ? d0 : d1;
+      float v[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) v[m] = (code((x >> (8 * m)) & 0xFFu) - 8388736.0f) * d;
+      split2(v[0], v[1], a1[2 * c], a2[2 * c]);
+      split2(v[2], v[3], a1[2 * c + 1], a2[2 * c + 1]);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- kernel
-template <int QT, int EPI, int BN>
-__global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
+template <int QT, int EPI, int BN, bool XS>
+__global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWu,
-                   const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmR, int n, int k,
-                   int T, float* Y, int ldy, const float* R, unsigned* status, int early) {
+                   const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmX2,
+                   const __grid_constant__ CUtensorMap tmR, int n, int k, int T, float* Y, int ldy, const float* R,
+                   const int* erow, const int* etok, unsigned* status, int early) {
   // early: bits 0-3 what may be read before the dependency wait (kEarly*),
-  // bit 4 set when tmR describes the residual (L2 prefetches of it)
-  using C = Cfg<QT, EPI, BN>;
+  // bit 4 set when tmR describes the residual (L2 prefetches of it).
+  // Exact leg (XS): X and X2 are the two fp16 pieces of X * 2^etok[t];
+  // erow[i] (erow[n + i] for the up weight) is the exponent e of the
+  // row's scale 2^e (computed before the launch, see row_exp_kernel).
+  using C = Cfg<QT, EPI, BN, XS>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, by pointer arithmetic on the shared array so that
   // the compiler keeps the shared address space (shared loads, not generic)
@@ -229,6 +306,8 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
   uint64_t* drain = accFull + 1;
   uint64_t* peerFree = drain + 1;     // split: the partner's raw ring is free to receive
   uint64_t* xferFull = peerFree + 1;  // split: [wg] the partner's piece for warpgroup wg has landed
+  uint64_t* chunkFull = xferFull + 2;   // exact leg: [b] the chunk in accumulator b is complete
+  uint64_t* chunkEmpty = chunkFull + 2; // exact leg: [b] accumulator b has been added into the sum
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -261,6 +340,10 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
     mbar_init(peerFree, 1);
     // one arrival per thread of the partner's sending warpgroup
     for (int w = 0; w < 2; ++w) mbar_init(&xferFull[w], 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&chunkFull[b], 1);
+      mbar_init(&chunkEmpty[b], 4);  // the warps of the summing warpgroup
+    }
     abort_flag[0] = 0;   // set by a wait that gives up
     abort_flag[1] = 0;   // never set: drain waits ignore the abort
     fence_mbar_init();
@@ -322,6 +405,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
     // ------------------------------------------------ activation producer
     if (lane == 0) {
       tma_prefetch_desc(&tmX);
+      if (XS) tma_prefetch_desc(&tmX2);
       // X is written by the conversion kernel, which may still be running
       grid_dependency_wait();
       bool ok = true;
@@ -330,8 +414,9 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
         const int st = i % C::S;
         ok = mbar_wait(&empty[st], ((i / C::S) & 1) ^ 1, abort_flag, status);
         if (!ok) break;
-        mbar_arrive_expect_tx(&full[st], C::B_BYTES);
-        tma_load_2d(sB + st * C::B_BYTES, &tmX, (c0 * SUBS + i) * BK, t0, &full[st]);
+        mbar_arrive_expect_tx(&full[st], C::NP * C::B_BYTES);
+        tma_load_2d(sB + st * C::NP * C::B_BYTES, &tmX, (c0 * SUBS + i) * BK, t0, &full[st]);
+        if (XS) tma_load_2d(sB + (st * C::NP + 1) * C::B_BYTES, &tmX2, (c0 * SUBS + i) * BK, t0, &full[st]);
         last = i;
         // the residual pieces this CTA finalizes, into L2 a few stages before
         // the end (the epilogue threads load them into registers)
@@ -352,21 +437,34 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
     int st = 0;
     uint32_t ph = 0;
     for (int i = 0; i < nk; ++i) {
+      const int cc = i / SUBS, ss = i % SUBS;  // local chunk, stage within it
+      if (XS && ss == 0 && cc >= 2) {  // accumulator cc & 1 has been added into the sum
+        ok = __all_sync(0xffffffffu, mbar_wait(&chunkEmpty[cc & 1], ((cc - 2) >> 1) & 1, abort_flag, status));
+        if (!ok) break;
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(&full[st], ph, abort_flag, status));
       if (!ok) break;
       tc_fence_after();
-      // stage st of B starts st * B_BYTES later: (B_BYTES >> 4) descriptor units
-      const uint64_t bdesc = bdesc0 + (uint64_t)((st * C::B_BYTES) >> 4);
+      // stage st of B starts st * NP * B_BYTES later: (bytes >> 4) descriptor units
+      const uint64_t bdesc = bdesc0 + (uint64_t)((st * C::NP * C::B_BYTES) >> 4);
 #pragma unroll
       for (int m = 0; m < C::NM; ++m) {
-        const uint32_t a_tmem = tmem_base + C::A_COL0 + (m * C::S + st) * C::A_COLS;
+        const uint32_t a_tmem = tmem_base + C::A_COL0 + (m * C::S + st) * C::NP * C::A_COLS;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
           // 16 k = 8 TMEM columns of A, +32 bytes of B inside its swizzle atom
-          mma_f16_ts_elect(tmem_base + m * BN, a_tmem + kk * 8, bdesc + 2 * kk, idesc, (i | kk) != 0);
+          if (XS) {  // W1 . X1 + W1 . X2 + W2 . X1 into the chunk's accumulator
+            const uint32_t d = tmem_base + (uint32_t)(cc & 1) * BN;
+            mma_f16_ts_elect(d, a_tmem + kk * 8, bdesc + 2 * kk, idesc, (ss | kk) != 0);
+            mma_f16_ts_elect(d, a_tmem + kk * 8, bdesc + (C::B_BYTES >> 4) + 2 * kk, idesc, 1);
+            mma_f16_ts_elect(d, a_tmem + C::A_COLS + kk * 8, bdesc + 2 * kk, idesc, 1);
+          } else {
+            mma_f16_ts_elect(tmem_base + m * BN, a_tmem + kk * 8, bdesc + 2 * kk, idesc, (i | kk) != 0);
+          }
         }
       }
       mma_commit_elect(&empty[st]);
+      if (XS && ss == SUBS - 1) mma_commit_elect(&chunkFull[cc & 1]);
       if (++st == C::S) {
         st = 0;
         ph ^= 1u;
@@ -386,8 +484,48 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
     const uint32_t q = (uint32_t)(warp & 3);         // lane quarter of TMEM this warp may access
     const uint32_t r = q * 32 + lane;                // tile row == TMEM lane
     const uint32_t lane_base = tmem_base + ((q * 32u) << 16);
+    // exact leg: 2^e of this thread's weight row (erow is written by a kernel
+    // launched in plain stream order before this one)
+    float sw = 1.f;
+    if (XS) {
+      grid_dependency_wait();
+      const int ri = m0 + (int)r;
+      sw = __int_as_float((127 + (ri < n ? erow[(size_t)g * n + ri] : 0)) << 23);
+    }
     bool ok = true;
+    // exact leg: add the finished chunk cs in accumulator cs & 1 into the sum
+    // (chunk 0 starts it); warpgroup 0, 128 token columns a thread
+    auto fold = [&](int cs) {
+      bool okf = __all_sync(0xffffffffu, mbar_wait(&chunkFull[cs & 1], (cs >> 1) & 1, abort_flag, status));
+      if (okf) {
+        tc_fence_after();
+        const uint32_t src = lane_base + (uint32_t)(cs & 1) * BN, sum = lane_base + 2 * BN;
+#pragma unroll 1
+        for (int cb = 0; cb < BN / 32; ++cb) {
+          uint32_t va[32], vs[32];
+          tmem_ld_32x32b_x32(src + cb * 32, va);
+          if (cs > 0) tmem_ld_32x32b_x32(sum + cb * 32, vs);
+          tmem_ld_wait_regs(va);
+          if (cs > 0) {
+            regs_after_wait(vs);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) vs[jj] = __float_as_uint(__uint_as_float(vs[jj]) + __uint_as_float(va[jj]));
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) vs[jj] = va[jj];
+          }
+          tmem_st_32x32b_x32(sum + cb * 32, vs);
+          tmem_st_wait();
+        }
+        tc_fence_before();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&chunkEmpty[cs & 1]);
+      return okf;
+    };
     for (int c = 0; c < nchunks && ok; ++c) {
+      if (XS && par == 0 && c >= 2) ok = fold(c - 2);
+      if (!ok) break;
       const int j = c * C::NM + g;
       const int slot = j % C::S_RAW;
       ok = __all_sync(0xffffffffu, mbar_wait(&rawFull[slot], (j / C::S_RAW) & 1, abort_flag, status));
@@ -396,16 +534,21 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
       for (int s = par; s < SUBS; s += C::DQ) {
         const int i = c * SUBS + s;
         const int st = i % C::S;
-        uint32_t w[2 * C::BB / 4], a[32];
+        uint32_t w[2 * C::BB / 4], a[32], a2[XS ? 32 : 1];
 #pragma unroll
         for (int v = 0; v < 2 * C::BB / 4; ++v) w[v] = raw_row[s * (2 * C::BB / 4) + v];
-        dequant_row_stage<QT>(w, a);  // overlaps the wait below
+        if constexpr (XS)
+          dequant_row_stage_xs<QT>(w, sw, a, a2);  // overlaps the wait below
+        else
+          dequant_row_stage<QT>(w, a);
         ok = __all_sync(0xffffffffu, mbar_wait(&empty[st], ((i / C::S) & 1) ^ 1, abort_flag, status));
         if (!ok) break;
         tc_fence_after();
         // tcgen05.st reads its source registers asynchronously: a[] stays
         // untouched until the wait
-        tmem_st_32x32b_x32(lane_base + C::A_COL0 + (g * C::S + st) * C::A_COLS, a);
+        const uint32_t acol = lane_base + C::A_COL0 + (g * C::S + st) * C::NP * C::A_COLS;
+        tmem_st_32x32b_x32(acol, a);
+        if constexpr (XS) tmem_st_32x32b_x32(acol + C::A_COLS, a2);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -437,6 +580,11 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
     if (EPI == kEpiResidual && ok && live(piece(0))) load_r(piece(0));
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(accFull, 0, abort_flag, status));
     tc_fence_after();
+    if (XS) {  // warpgroup 0's last fold is in TMEM before either reads the sum
+      tc_fence_before();
+      named_sync(3, 256);
+      tc_fence_after();
+    }
 
     if (nsplit == 2) {
       // the piece the partner keeps, pg, goes from registers straight into the
@@ -475,11 +623,39 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
       if (ok && nsplit == 2)  // the partner's half of this piece has landed
         ok = __all_sync(0xffffffffu, mbar_wait_cluster(&xferFull[wg], 0, abort_flag, status));
       if (!ok) continue;
-      tmem_ld_32x32b_x32(lane_base + p * PIECE, v);
-      tmem_ld_32x32b_x32(lane_base + p * PIECE + 32, v + 32);
-      tmem_ld_wait_regs(v);
-      regs_after_wait(v + 32);
-      if (C::NM == 2) {  // y = silu(gate) * up
+      if constexpr (XS) {
+        // y = ((sum + acc of chunk nc - 2) + acc of chunk nc - 1), the sum
+        // holding chunks 0 .. nc - 3
+        const int nc = nchunks;
+        bool first = true;
+        for (int part = 0; part < 3; ++part) {
+          uint32_t col;
+          if (part == 0) {
+            if (nc < 3) continue;
+            col = 2 * BN;
+          } else {
+            const int cs = nc - 3 + part;  // nc - 2, nc - 1
+            if (cs < 0) continue;
+            col = (uint32_t)(cs & 1) * BN;
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t t[32];
+            tmem_ld_32x32b_x32(lane_base + col + p * PIECE + 32 * h, t);
+            tmem_ld_wait_regs(t);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj)
+              v[32 * h + jj] = first ? t[jj] : __float_as_uint(__uint_as_float(v[32 * h + jj]) + __uint_as_float(t[jj]));
+          }
+          first = false;
+        }
+      } else {
+        tmem_ld_32x32b_x32(lane_base + p * PIECE, v);
+        tmem_ld_32x32b_x32(lane_base + p * PIECE + 32, v + 32);
+        tmem_ld_wait_regs(v);
+        regs_after_wait(v + 32);
+      }
+      if (C::NM == 2 && !XS) {  // y = silu(gate) * up
         uint32_t u[64];
         tmem_ld_32x32b_x32(lane_base + BN + p * PIECE, u);
         tmem_ld_32x32b_x32(lane_base + BN + p * PIECE + 32, u + 32);
@@ -498,6 +674,16 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN>::NTHREADS, 1)
           const float o = src[j * BM];
           const float mine = __uint_as_float(v[j]);
           v[j] = __float_as_uint(z == 0 ? mine + o : o + mine);
+        }
+      }
+      if constexpr (XS) {
+        // undo the scales: y = acc * 2^-erow * 2^-etok (exact, two steps)
+        const float sr = __int_as_float((127 - erow[row < n ? row : 0]) << 23);
+#pragma unroll
+        for (int j = 0; j < PIECE; ++j) {
+          const int t = t0 + p * PIECE + j;
+          const float stk = __int_as_float((127 - etok[t < T ? t : 0]) << 23);
+          v[j] = __float_as_uint(__uint_as_float(v[j]) * sr * stk);
         }
       }
       if (row < n) {
@@ -566,10 +752,11 @@ __global__ void __launch_bounds__(256, 4) x_to_f16_kernel(const float* __restric
 }
 
 // ---------------------------------------------------------------- host side
-template <int QT, int EPI, int BN>
+template <int QT, int EPI, int BN, bool XS = false>
 int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y, int ldy,
-               const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, int early) {
-  using C = Cfg<QT, EPI, BN>;
+               const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, int early,
+               const uint16_t* X16b = nullptr, const int* erow = nullptr, const int* etok = nullptr) {
+  using C = Cfg<QT, EPI, BN, XS>;
   auto fn = encode_fn(msg, msg_len);
   if (!fn) return -1;
   CUtensorMap mW, mWu;
@@ -589,6 +776,10 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
   if (!make_map_2d(fn, &mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X16, (uint64_t)k, (uint64_t)T, (uint64_t)k * 2, BK, BN,
                    CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
     return -1;
+  CUtensorMap mX2 = mX;
+  if (XS && !make_map_2d(fn, &mX2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X16b, (uint64_t)k, (uint64_t)T, (uint64_t)k * 2, BK,
+                         BN, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
+    return -1;
   // the residual, [T] rows of n fp32 ldy apart, only for L2 prefetches of
   // 128-row x 64-token boxes: a row stride that is not a multiple of 16
   // bytes cannot be described, and then nothing is prefetched
@@ -601,7 +792,7 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
     r_pf = 1;
   }
 
-  auto kern = gemm_tc_kernel<QT, EPI, BN>;
+  auto kern = gemm_tc_kernel<QT, EPI, BN, XS>;
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -628,7 +819,8 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
     cfg.numAttrs = 2;
   }
   cfg.attrs = attr;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mW, mWu, mX, mR, n, k, T, Y, ldy, R, status, early | (r_pf << 4));
+  cudaError_t e =
+      cudaLaunchKernelEx(&cfg, kern, mW, mWu, mX, mX2, mR, n, k, T, Y, ldy, R, erow, etok, status, early | (r_pf << 4));
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     snprintf(msg, msg_len, "gemm_tc launch: %s", cudaGetErrorString(e));
@@ -649,7 +841,141 @@ int launch_q(const GemmPlan& pl, const void* W, const void* Wu, int n, int k, co
   return launch_cfg<QT, kEpiPlain, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w);
 }
 
+// ---------------------------------------------------------------- exact-leg splits
+// Per weight row: the exponent e with max_b |d_b| * qmax * 2^e in [2^14, 2^15)
+// (qmax = 8 for Q4_0, 128 for Q8_0, the largest |q'|), so that every d * q' of
+// the row times 2^e lies below 2^15 and its remainder after fp16 rounding
+// stays an fp16 normal number unless it is far below the row's largest. One
+// warp per row; 0 for a row of zero scales.
+__global__ void row_exp_kernel(const uint8_t* __restrict__ W, int n, int nblk, int bb, float qmax,
+                               int* __restrict__ erow) {
+  const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= n) return;
+  const uint8_t* base = W + (size_t)row * nblk * bb;
+  float m = 0.f;
+  for (int b = lane; b < nblk; b += 32) {
+    const unsigned short bits = *reinterpret_cast<const unsigned short*>(base + (size_t)b * bb);
+    m = fmaxf(m, fabsf(__half2float(__ushort_as_half(bits))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) {
+    int e = 0;
+    if (m > 0.f) e = 14 - ((int)((__float_as_uint(m * qmax) >> 23) & 0xFFu) - 127);
+    erow[row] = e;
+  }
+}
+
+// Per token row of X: the exponent e with max_j |x_j| 2^e in [2^14, 2^15)
+// (clamped to [-126, 126]; 0 for a zero row), then X1 = fp16(x 2^e) and
+// X2 = fp16(x 2^e - X1), both round to nearest even: X1 + X2 carries 22 of
+// x's 24 bits. One CTA per row.
+__global__ void __launch_bounds__(256) x_split_kernel(const float* __restrict__ X, int k, uint16_t* __restrict__ X1,
+                                                      uint16_t* __restrict__ X2, int* __restrict__ etok) {
+  // launched in plain stream order; the GEMM after it may start streaming
+  // its weights at once
+  grid_launch_dependents();
+  const size_t row = blockIdx.x;
+  const float4* x4 = reinterpret_cast<const float4*>(X + row * (size_t)k);
+  const int k4 = k / 4;
+  float m = 0.f;
+  for (int i = threadIdx.x; i < k4; i += blockDim.x) {
+    const float4 v = x4[i];
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float wm[8];
+  __shared__ int se;
+  if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) t = fmaxf(t, wm[i]);
+    int e = 0;
+    if (t > 0.f) e = 14 - ((int)((__float_as_uint(t) >> 23) & 0xFFu) - 127);
+    e = e < -126 ? -126 : (e > 126 ? 126 : e);
+    se = e;
+    etok[row] = e;
+  }
+  __syncthreads();
+  const float sc = __int_as_float((127 + se) << 23);
+  uint2* y1 = reinterpret_cast<uint2*>(X1 + row * (size_t)k);
+  uint2* y2 = reinterpret_cast<uint2*>(X2 + row * (size_t)k);
+  for (int i = threadIdx.x; i < k4; i += blockDim.x) {
+    const float4 v = x4[i];
+    uint32_t a0, b0, a1, b1;
+    split2(v.x * sc, v.y * sc, a0, b0);
+    split2(v.z * sc, v.w * sc, a1, b1);
+    y1[i] = make_uint2(a0, a1);
+    y2[i] = make_uint2(b0, b1);
+  }
+}
+
+template <int QT>
+int launch_xs(const void* W, const void* Wu, int n, int k, const uint16_t* X1, const uint16_t* X2, const int* erow,
+              const int* etok, int T, float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg,
+              size_t msg_len) {
+  (void)Wu;
+  if (R)
+    return launch_cfg<QT, kEpiResidual, 128, true>(W, Wu, n, k, X1, T, Y, ldy, R, status, s, msg, msg_len, 1, kEarlyW,
+                                                    X2, erow, etok);
+  return launch_cfg<QT, kEpiPlain, 128, true>(W, Wu, n, k, X1, T, Y, ldy, R, status, s, msg, msg_len, 1, kEarlyW, X2,
+                                               erow, etok);
+}
+
+// y = silu(g) * u, silu(g) = g / (1 + e^-g), for T rows of n (rows of Y ldy
+// apart; G and U dense); the exact leg's gate/up product from its two GEMMs.
+__global__ void swiglu_rows_kernel(const float* __restrict__ G, const float* __restrict__ U, int T, int n, float* Y,
+                                   int ldy) {
+  const size_t total = (size_t)T * n;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t t = i / n, c = i - t * n;
+    const float g = G[i];
+    Y[t * ldy + c] = g / (1.0f + expf(-g)) * U[i];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_swiglu_rows(const float* G, const float* U, int T, int n, float* Y, int ldy, cudaStream_t s) {
+  const size_t total = (size_t)T * n;
+  size_t blocks = (total + 255) / 256;
+  const size_t cap = (size_t)num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks == 0) blocks = 1;
+  swiglu_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(G, U, T, n, Y, ldy);
+  return cudaGetLastError();
+}
+
+size_t gemm_xs_scratch_bytes(int n, int k, int T, bool swiglu) {
+  const size_t xb = ((size_t)T * k * 2 + 255) & ~(size_t)255;
+  return 2 * xb + (((size_t)T * 4 + 255) & ~(size_t)255) + (size_t)(swiglu ? 2 : 1) * n * 4;
+}
+
+int launch_gemm_xs(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
+                   const float* R, void* scratch, unsigned* status, cudaStream_t s, char* msg, size_t msg_len) {
+  const size_t xb = ((size_t)T * k * 2 + 255) & ~(size_t)255;
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  uint16_t* X1 = reinterpret_cast<uint16_t*>(base);
+  uint16_t* X2 = reinterpret_cast<uint16_t*>(base + xb);
+  int* etok = reinterpret_cast<int*>(base + 2 * xb);
+  int* erow = reinterpret_cast<int*>(base + 2 * xb + (((size_t)T * 4 + 255) & ~(size_t)255));
+  const int bb = qtype == kQ4_0 ? 18 : 34;
+  const float qmax = qtype == kQ4_0 ? 8.f : 128.f;
+  // plain stream order: the splits start once everything before is complete
+  const unsigned rblocks = (unsigned)((n + 7) / 8);
+  row_exp_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(W), n, k / 32, bb, qmax, erow);
+  if (Wu) row_exp_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(Wu), n, k / 32, bb, qmax, erow + n);
+  x_split_kernel<<<(unsigned)T, 256, 0, s>>>(X, k, X1, X2, etok);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    snprintf(msg, msg_len, "exact-leg splits: %s", cudaGetErrorString(e));
+    return -1;
+  }
+  return qtype == kQ4_0 ? launch_xs<kQ4_0>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len)
+                        : launch_xs<kQ8_0>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
+}
 
 cudaError_t launch_x_to_f16(const float* X, uint16_t* X16, size_t count, cudaStream_t s) {
   // the GEMM's shared-memory carveout, so that its CTAs may start on an SM

@@ -34,7 +34,8 @@ def run(q, case, *, leg=0, path=0, Wu=None):
 def test_q8_0_256x512_t16(q):
     c = synth.make_case(synth.Q8_0, 256, 512, 16, seed=0)
     ref = oracle.qgemm_f64(synth.Q8_0, c["W"], 256, 512, c["X"])
-    assert_exact_leg(run(q, c).cpu().numpy(), ref)                       # T rule: GEMV
+    assert_f16_leg(run(q, c).cpu().numpy(), ref)                         # T rule: the fp16 GEMM from T = 8
+    assert_exact_leg(run(q, c, path=q.APR_PATH_GEMV).cpu().numpy(), ref)  # the GEMV path (exact)
     assert_f16_leg(run(q, c, path=q.APR_PATH_GEMM).cpu().numpy(), ref)     # forced tcgen05 GEMM
     assert_exact_leg(run(q, c, leg=q.APR_LEG_EXACT_F32, path=q.APR_PATH_GEMM).cpu().numpy(), ref)
 

@@ -30,7 +30,7 @@ def test_normed_projection(q, qtype, n, k, T, leg):
     q.apr_qgemm_rmsnorm(qtype, dev(c["W"]), n, k, dev(c["X"]), T, Y, dev(w), EPS, residual=dev(c["R"]), leg=leg)
     q.apr_stream_status()
     ref = oracle.normed_qgemm_f64(qtype, c["W"], n, k, c["X"], w, EPS, c["R"])
-    if leg == 0 and T > q.APR_GEMV_MAX_T:
+    if leg == 0 and T > q.APR_AUTO_GEMV_MAX_T:
         assert_f16_leg(Y.cpu().numpy(), ref)
     else:
         assert_exact_leg(Y.cpu().numpy(), ref)

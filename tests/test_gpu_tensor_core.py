@@ -154,9 +154,10 @@ def test_gemv_and_gemm_agree_for_small_T(q, qtype):
         assert_f16_leg(Ym.cpu().numpy(), Yv.cpu().numpy().astype(np.float64))
 
 
-def test_auto_rule_large_T_takes_the_fp16_gemm(q):
-    # T = 17 is above the GEMV limit: the fp16 leg's error shows (it is not fp32-exact)
-    n, k, T = 256, 512, 17
+@pytest.mark.parametrize("T", [8, 17])
+def test_auto_rule_large_T_takes_the_fp16_gemm(q, T):
+    # T >= 8 is above the GEMV limit: the fp16 leg's error shows (it is not fp32-exact)
+    n, k = 256, 512
     c = synth.make_case(synth.Q8_0, n, k, T, seed=0)
     Y = torch.empty((T, n), device="cuda")
     q.apr_qgemm(synth.Q8_0, dev(c["W"]), n, k, dev(c["X"]), T, Y)
