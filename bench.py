@@ -803,7 +803,13 @@ def gemv_rate(q, synth, dev, stream, peak_gbs, n=4096, k=4096):
     q.apr_stream_status(stream)
     byts = n * (k // 32) * 18 + k * 4 + n * 4
     gbs = byts / dt / 1e9
-    return {"workload": f"q4_0_gemv_n{n}_k{k}_t1", "GB/s": gbs, "frac_hbm": gbs / peak_gbs, "us": dt * 1e6}
+    # the same weights only streamed (the GEMV's data movement, no compute):
+    # what a launch of this size can reach on this GPU
+    wb = n * (k // 32) * 18
+    fl = timed_calls([(lambda w=w: q.apr_read_stream(w, wb)) for w in Ws], reps, stream) / reps
+    q.apr_stream_status(stream)
+    return {"workload": f"q4_0_gemv_n{n}_k{k}_t1", "GB/s": gbs, "frac_hbm": gbs / peak_gbs, "us": dt * 1e6,
+            "stream_floor_us": fl * 1e6, "frac_stream_floor": fl / dt}
 
 
 def main(argv=None):

@@ -417,6 +417,18 @@ int apr_dequant(int qtype, const void* W, int n, int k, float* out, apr_stream_t
 int apr_stream_status(apr_stream_t stream);
 
 /*
+ * Measurement reference (the pages have no counterpart): streams `bytes`
+ * bytes from the device buffer src into shared memory exactly as the T = 1
+ * GEMV streams its weight (one CTA per SM, a contiguous share each, bulk
+ * copies of 16 KB into a ring of 5 stages, programmatic dependent launch) and
+ * computes nothing. Timing it beside apr_qgemv on the same number of bytes
+ * separates the GEMV's own cost from the cost of moving its weight. bytes a
+ * multiple of 16 (0: no-op), src 16-byte aligned, only read. Errors:
+ * APR_E_INVAL, APR_E_ALIGN, APR_E_DEVICE, APR_E_LAUNCH.
+ */
+int apr_read_stream(const void* src, long long bytes, apr_stream_t stream);
+
+/*
  * Test of the failure detection (the pages have no counterpart): enqueues one
  * kernel that waits on an mbarrier nothing arrives on, through the same
  * bounded wait every kernel of the library uses, with a limit of limit_us

@@ -54,6 +54,7 @@ EXPORTS = (
     "apr_prefill_layer",
     "apr_dequant",
     "apr_stream_status",
+    "apr_read_stream",
     "apr_test_bounded_wait",
     "apr_last_error",
 )
@@ -149,6 +150,7 @@ def _load() -> ctypes.CDLL:
         "apr_dequant": ([ci, vp, ci, ci, vp, vp], ci),
         "apr_stream_status": ([vp], ci),
         "apr_test_bounded_wait": ([ctypes.c_uint, vp], ci),
+        "apr_read_stream": ([vp, ctypes.c_longlong, vp], ci),
         "apr_last_error": ([], ctypes.c_char_p),
     }
     for name, (args, res) in sig.items():
@@ -405,3 +407,9 @@ def apr_prefill_layer(qtype, Wqkv, Wo, Wg, Wu, Wd, hidden, inter, num_heads, num
                    _ptr(K_cache, "K_cache", dtype=f32, min_bytes=crow * kvd * 4),
                    _ptr(V_cache, "V_cache", dtype=f32, min_bytes=crow * kvd * 4), chunk, _stream(stream))
     return _check(_lib.apr_prefill_layer(ctypes.byref(a)))
+
+
+def apr_read_stream(src, nbytes, stream=None) -> int:
+    """Streams nbytes of the device tensor src as the T = 1 GEMV streams its
+    weight, computing nothing (a measurement reference)."""
+    return _check(_lib.apr_read_stream(_ptr(src, "src", min_bytes=int(nbytes)), int(nbytes), _stream(stream)))

@@ -675,6 +675,18 @@ int apr_dequant(int qtype, const void* W, int n, int k, float* out, apr_stream_t
   return launched(launch_dequant(qtype, W, n, k, out, (cudaStream_t)stream), "dequant");
 }
 
+int apr_read_stream(const void* src, long long bytes, apr_stream_t stream) {
+  t_msg[0] = 0;
+  if (bytes < 0 || bytes % 16 != 0) return fail(APR_E_INVAL, "bytes must be a non-negative multiple of 16");
+  if (bytes == 0) return APR_OK;
+  if (!src) return fail(APR_E_INVAL, "null pointer");
+  if (!aligned16(src)) return fail(APR_E_ALIGN, "pointer %p is not 16-byte aligned", src);
+  DeviceState* st = nullptr;
+  const int rc = device_state(&st);
+  if (rc != APR_OK) return rc;
+  return launched(launch_read_stream(src, bytes, st->status, (cudaStream_t)stream), "read_stream");
+}
+
 int apr_test_bounded_wait(unsigned limit_us, apr_stream_t stream) {
   t_msg[0] = 0;
   if (limit_us < 1 || limit_us > 1000000) return fail(APR_E_INVAL, "limit_us must be in [1, 1000000] (got %u)", limit_us);

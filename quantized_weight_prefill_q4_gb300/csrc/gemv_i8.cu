@@ -1,0 +1,474 @@
+// Single-token GEMV (T = 1) over Q4_0 / Q8_0 blocks with integer dot
+// products, exact to fp32 level (the single-token GEMVs gemv_q4_0_pf /
+// gemv_q8_0_pf of oxibonsai-kernels 0.1.4 src/gpu_backend/cuda_q_std_prefill.rs,
+// HBM-bound form).
+//
+// X in fixed point per 32-block: for block b, e_b makes max_j |x_j| 2^e_b lie
+// in [2^21, 2^22), and X_j = rint(x_j 2^e_b) (a 23-bit integer, off by at most
+// 1/2: 2^-22 of the block's largest |x|) is written with three signed byte
+// digits, X_j = 2^16 p2 + 2^8 p1 + p0. A block's code-times-X sum is then
+//   sum_j q'_j X_j = 2^16 A2 + 2^8 A1 + A0,   A_k = sum_j q'_j p_kj,
+// each A_k an exact int32 of at most 2^17, accumulated four products at a
+// time by dp4a. Q4_0 multiplies the unsigned nibbles n_j (dp4a.u32.s32) and
+// starts A_k at -8 sum_j p_kj, so that A_k sums (n_j - 8) p_kj; Q8_0 multiplies
+// the signed codes directly. The three A_k become one float (rounded once at
+// fp32 level) and the row accumulates d_b 2^-e_b times it in fp32. Per weight
+// element this is 3/4 dp4a and about 3/8 of an instruction to unpack the
+// codes, against about two and a half for a decode to fp32 and an FMA.
+//
+// Work and data movement as the whole-row GEMV (gemv_rows.cu): persistent
+// CTAs, one per SM, each a contiguous range of rows; a producer warp streams
+// whole rows (the W rows then the Wu rows for gate/up) into a ring of
+// 16 KB stages with one bulk copy per stage; consumer warps take the rows
+// round-robin, each lane one block pair of a row, its X digits held in
+// registers for the whole kernel. A warp decodes two rows at a time and
+// reduces their lane partials with interleaved shuffles, and the partials of
+// a row's warps are parked in shared memory and added once, after the last
+// stage, in a fixed order: no per-row fence or atomic. Measured on GB300, a
+// kernel that only streams the bytes reads 7.5 MB in 4.2 us and 27 MB in
+// 8.2 us (1.8 and 3.3 TB/s: the launch's ramp-up and tail, not the HBM rate,
+// bound weights of this size), and a deeper ring does not change that. So
+// the CTA keeps to half an SM when it can (5 stages of 16 KB, the X table,
+// 8 consumer warps at under 113 registers): the next launch's CTA then
+// starts beside it and streams its weights while this one finishes. Rows of
+// k above about 8192 (a larger X table) take a whole SM and a ring of up to
+// 13 stages.
+//
+// Programmatic dependent launch: the producer streams W before the preceding
+// kernel has finished (W must not be its output); X, R and Y are touched only
+// after griddepcontrol.wait, and the kernel lets the next kernel launch once
+// that wait has returned.
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "apr_internal.h"
+#include "dev_common.cuh"
+#include "host_common.h"
+
+namespace apr {
+namespace {
+
+constexpr int ICW = 8;                         // consumer warps
+constexpr int ITHREADS = 32 * (ICW + 1);
+constexpr int ISTAGE = 16384;                  // bytes of one stage
+constexpr int INS_MAX = 13;                    // stages at most (as many as shared memory holds)
+constexpr int IMAXROWS = 128;                  // rows a CTA may take
+constexpr int XBW = 28;                        // table words per block: 3 x 8 digit words, 3 starts, scale
+
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_ss(uint32_t a, int b, int c) {
+  int d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// One block's table entry, built by 8 consecutive lanes (u = lane % 8), each
+// from its 4 values of X (elements 4u .. 4u + 3 of the block): the block's
+// largest |x| and the digit sums by shuffles within the 8 lanes.
+template <int QT>
+__device__ __forceinline__ void block_digits8(float4 x, int u, uint32_t* out) {
+  float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  int e = 0;
+  if (m > 0.f) e = 21 - ((int)((__float_as_uint(m) >> 23) & 0xFFu) - 127);
+  e = e < -126 ? -126 : (e > 126 ? 126 : e);
+  const float sc = __int_as_float((127 + e) << 23);
+  const float xv[4] = {x.x, x.y, x.z, x.w};
+  uint32_t dig[3] = {0u, 0u, 0u};
+  int psum[3] = {0, 0, 0};
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const int X = __float2int_rn(xv[b] * sc);
+    const int p0 = (X << 24) >> 24;
+    const int x1 = (X - p0) >> 8;
+    const int p1 = (x1 << 24) >> 24;
+    const int p2 = (x1 - p1) >> 8;
+    dig[0] |= (uint32_t)(p0 & 0xFF) << (8 * b);
+    dig[1] |= (uint32_t)(p1 & 0xFF) << (8 * b);
+    dig[2] |= (uint32_t)(p2 & 0xFF) << (8 * b);
+    psum[0] += p0;
+    psum[1] += p1;
+    psum[2] += p2;
+  }
+#pragma unroll
+  for (int kd = 0; kd < 3; ++kd) {
+    out[8 * kd + u] = dig[kd];
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) psum[kd] += __shfl_xor_sync(0xffffffffu, psum[kd], o);
+  }
+  if (u == 0) {
+#pragma unroll
+    for (int kd = 0; kd < 3; ++kd) out[24 + kd] = (uint32_t)(QT == kQ4_0 ? -8 * psum[kd] : 0);
+    out[27] = __float_as_uint(__int_as_float((127 - e) << 23));  // 2^-e
+  }
+}
+
+// sum over one block of q'_j x_j, times d: t = the block's table entry
+// (registers), p = its 4 (Q4_0: 16 bytes of nibbles) or 8 (Q8_0) payload words.
+template <int QT>
+__device__ __forceinline__ float block_dot(const uint32_t* p, const uint32_t (&t)[XBW], float d) {
+  int a0 = (int)t[24], a1 = (int)t[25], a2 = (int)t[26];
+  if constexpr (QT == kQ4_0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = p[i] & 0x0F0F0F0Fu;          // elements 4i .. 4i + 3
+      const uint32_t hi = (p[i] >> 4) & 0x0F0F0F0Fu;   // elements 16 + 4i ..
+      a0 = dp4a_us(lo, (int)t[i], a0);
+      a1 = dp4a_us(lo, (int)t[8 + i], a1);
+      a2 = dp4a_us(lo, (int)t[16 + i], a2);
+      a0 = dp4a_us(hi, (int)t[4 + i], a0);
+      a1 = dp4a_us(hi, (int)t[12 + i], a1);
+      a2 = dp4a_us(hi, (int)t[20 + i], a2);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      a0 = dp4a_ss(p[i], (int)t[i], a0);
+      a1 = dp4a_ss(p[i], (int)t[8 + i], a1);
+      a2 = dp4a_ss(p[i], (int)t[16 + i], a2);
+    }
+  }
+  const float v = fmaf((float)a2, 65536.f, fmaf((float)a1, 256.f, (float)a0));
+  return v * (d * __uint_as_float(t[27]));
+}
+
+int rows_per_stage(int qtype, int k, bool swiglu) {
+  const long row_bytes = (long)(k / 32) * block_bytes(qtype);
+  return (int)(ISTAGE / ((swiglu ? 2 : 1) * row_bytes));
+}
+
+template <int QT, bool SWI>
+__global__ void __launch_bounds__(ITHREADS, 2)
+    gemv_i8_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ Wu, int n, int k,
+                   const float* __restrict__ X, float* Y, const float* R, unsigned* status, int rs, int ns) {
+  constexpr int NM = SWI ? 2 : 1;
+  constexpr int BB = QT == kQ4_0 ? 18 : 34;
+  constexpr int PW_WORDS = 2 * BB / 4;  // words of one block pair
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+  const int nblk = k / 32, npk = nblk / 2;
+  const int PW = (npk + 31) / 32;  // warps per row
+  uint32_t* xt = reinterpret_cast<uint32_t*>(smem + (size_t)ns * ISTAGE);  // X table, [nblk][XBW]
+  float* part = reinterpret_cast<float*>(xt + (size_t)nblk * XBW);     // [row slot][NM][PW]
+  float* rres = part + IMAXROWS * NM * 8;                              // residual of the CTA's rows
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rres + IMAXROWS);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + INS_MAX;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * INS_MAX);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t row_bytes = (size_t)nblk * BB;
+  const int r0 = (int)((long)n * blockIdx.x / gridDim.x);
+  const int r1 = (int)((long)n * (blockIdx.x + 1) / gridDim.x);
+  const int nst = (r1 - r0 + rs - 1) / rs;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < ns; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], ICW);
+    }
+    abort_flag[0] = 0;
+    abort_flag[1] = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == ICW) {
+    // ------------------------------------------------ producer
+    if (lane == 0) {
+      int last[INS_MAX];
+      for (int i = 0; i < INS_MAX; ++i) last[i] = -1;
+      bool ok = true;
+      for (int s = 0; s < nst && ok; ++s) {
+        const int st = s % ns;
+        ok = mbar_wait(&empty[st], ((s / ns) & 1) ^ 1, abort_flag, status);
+        if (!ok) break;
+        const int rb = r0 + s * rs, rows = min(rs, r1 - rb);
+        const uint32_t bytes = (uint32_t)(rows * row_bytes);
+        mbar_arrive_expect_tx(&full[st], bytes * NM);
+        bulk_load_1d(smem + st * ISTAGE, W + (size_t)rb * row_bytes, bytes, &full[st]);
+        if (SWI) bulk_load_1d(smem + st * ISTAGE + rs * row_bytes, Wu + (size_t)rb * row_bytes, bytes, &full[st]);
+        last[st] = s;
+      }
+      if (!ok)  // let the copies in flight land before the CTA exits
+        for (int i = 0; i < ns; ++i)
+          if (last[i] >= 0) mbar_wait(&full[i], (last[i] / ns) & 1, abort_flag + 1, status);
+    }
+    return;
+  }
+
+  // ------------------------------------------------ consumers
+  const int RG = ICW / PW;          // row groups
+  const int g = warp / PW, wi = warp % PW;
+  const int P = wi * 32 + lane;     // this lane's block pair
+  const bool act = g < RG && P < npk;
+
+  // X, R and Y may belong to the preceding kernel until it completes; once it
+  // has, the next kernel may launch
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
+  // 8 lanes a block, 32 blocks a pass of the consumers (nblk is a multiple of
+  // 8, so a warp's 4 blocks of a pass are all present or all absent); the X
+  // loads of four passes are issued before any is used
+  for (int base = (int)threadIdx.x / 8; base < nblk; base += 4 * (ICW * 32 / 8)) {
+    float4 xv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int b0 = base + u * (ICW * 32 / 8);
+      if (b0 < nblk) xv[u] = __ldg(reinterpret_cast<const float4*>(X) + (size_t)b0 * 8 + (threadIdx.x & 7));
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int b0 = base + u * (ICW * 32 / 8);
+      if (b0 < nblk) block_digits8<QT>(xv[u], threadIdx.x & 7, xt + (size_t)b0 * XBW);
+    }
+  }
+  if (!SWI && R)
+    for (int i = threadIdx.x; i < r1 - r0; i += ICW * 32) rres[i] = R[r0 + i];
+  named_sync(1, ICW * 32);
+  uint32_t ta[XBW], tb[XBW];
+  if (act) {
+    const uint4* src = reinterpret_cast<const uint4*>(xt + (size_t)2 * P * XBW);
+#pragma unroll
+    for (int v = 0; v < XBW / 4; ++v) {
+      const uint4 a = src[v], b = src[XBW / 4 + v];
+      ta[4 * v] = a.x; ta[4 * v + 1] = a.y; ta[4 * v + 2] = a.z; ta[4 * v + 3] = a.w;
+      tb[4 * v] = b.x; tb[4 * v + 1] = b.y; tb[4 * v + 2] = b.z; tb[4 * v + 3] = b.w;
+    }
+  }
+
+  // one row's partial of this lane (its block pair), weight m
+  auto row_part = [&](int st, int m, int rr) -> float {
+    if (!act) return 0.f;
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(smem + st * ISTAGE + (size_t)(m * rs + rr) * row_bytes) +
+                        P * PW_WORDS;
+    uint32_t wr[PW_WORDS];
+#pragma unroll
+    for (int i = 0; i < PW_WORDS; ++i) wr[i] = w[i];
+    uint32_t pa[QT == kQ4_0 ? 4 : 8];
+    if constexpr (QT == kQ4_0) {
+      // block A: d in bytes 0-1, nibbles 2..17; block B: d in 18-19, nibbles 20..35
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pa[i] = __byte_perm(wr[i], wr[i + 1], 0x5432);
+      const float dA = __half2float(__ushort_as_half((unsigned short)(wr[0] & 0xFFFFu)));
+      const float dB = __half2float(__ushort_as_half((unsigned short)(wr[4] >> 16)));
+      return block_dot<QT>(pa, ta, dA) + block_dot<QT>(wr + 5, tb, dB);
+    } else {
+      // block A: d in bytes 0-1, codes 2..33; block B: d in 34-35, codes 36..67
+#pragma unroll
+      for (int i = 0; i < 8; ++i) pa[i] = __byte_perm(wr[i], wr[i + 1], 0x5432);
+      const float dA = __half2float(__ushort_as_half((unsigned short)(wr[0] & 0xFFFFu)));
+      const float dB = __half2float(__ushort_as_half((unsigned short)(wr[8] >> 16)));
+      return block_dot<QT>(pa, ta, dA) + block_dot<QT>(wr + 9, tb, dB);
+    }
+  };
+
+  bool ok = true;
+  for (int s = 0; s < nst; ++s) {
+    const int st = s % ns;
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (s / ns) & 1, abort_flag, status));
+    if (!ok) break;
+    const int rb = r0 + s * rs, rows = min(rs, r1 - rb);
+    if (g < RG) {
+      // the stage's rows whose index within the CTA is g modulo RG, two at a time
+      for (int rr = ((g - (rb - r0)) % RG + RG) % RG; rr < rows; rr += 2 * RG) {
+        const bool two = rr + RG < rows;
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+          float a = row_part(st, m, rr);
+          float b = two ? row_part(st, m, rr + RG) : 0.f;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            a += __shfl_xor_sync(0xffffffffu, a, o);
+            b += __shfl_xor_sync(0xffffffffu, b, o);
+          }
+          // the warp's share of the row, added with the others' after the
+          // last stage
+          if (lane == 0) {
+            part[((rb + rr - r0) * NM + m) * 8 + wi] = a;
+            if (two) part[((rb + rr + RG - r0) * NM + m) * 8 + wi] = b;
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage's rows
+  }
+  // every row's warp shares are in shared memory: add them in warp order
+  named_sync(1, ICW * 32);
+  if (ok)
+    for (int slot = threadIdx.x; slot < r1 - r0; slot += ICW * 32) {
+      float acc[NM];
+#pragma unroll
+      for (int m = 0; m < NM; ++m) {
+        float v = 0.f;
+        for (int w2 = 0; w2 < PW; ++w2) v += part[(slot * NM + m) * 8 + w2];
+        acc[m] = v;
+      }
+      float y;
+      if (SWI) {
+        y = acc[0] / (1.0f + expf(-acc[0])) * acc[NM - 1];
+      } else {
+        y = acc[0] + (R ? rres[slot] : 0.f);
+      }
+      Y[r0 + slot] = y;
+    }
+}
+
+// shared memory besides the ring, and the stages that fit beside it
+size_t i8_fixed_smem(int k) {
+  return 128 + (size_t)(k / 32) * XBW * 4 + (size_t)IMAXROWS * (2 * 8 + 1) * 4 + 2 * INS_MAX * 8 + 16;
+}
+int i8_stages(int k) {
+  // two CTAs an SM (228 KB of shared memory, 1 KB reserved per CTA) when 5
+  // stages fit beside the X table, else one with as many as fit
+  const long half = 232448L / 2 - 1024 - (long)i8_fixed_smem(k);
+  if (half / ISTAGE >= 5) return 5;
+  const long ns = (232448L - (long)i8_fixed_smem(k)) / ISTAGE;
+  return (int)(ns < INS_MAX ? ns : INS_MAX);
+}
+size_t i8_smem(int k) { return i8_fixed_smem(k) + (size_t)i8_stages(k) * ISTAGE; }
+
+template <int QT, bool SWI>
+cudaError_t launch_i8(const void* W, const void* Wu, int n, int k, const float* X, float* Y, const float* R,
+                      unsigned* status, cudaStream_t s) {
+  const size_t smem = i8_smem(k);
+  auto kern = gemv_i8_kernel<QT, SWI>;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = 1;
+  }
+  const int nsm = num_sms();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(n < nsm ? n : nsm));
+  cfg.blockDim = dim3(ITHREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e =
+      cudaLaunchKernelEx(&cfg, kern, (const uint8_t*)W, (const uint8_t*)Wu, n, k, X, Y, R, status,
+                         rows_per_stage(QT, k, SWI), i8_stages(k));
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return e;
+}
+
+// The GEMV's data movement alone: each CTA streams its contiguous share of
+// `bytes` into a ring of 16 KB stages by bulk copies, exactly as the GEMV's
+// producer does, and the consumer warps only release the stages. A measured
+// reference for the GEMV's roofline; nothing is computed or written.
+__global__ void __launch_bounds__(ITHREADS, 2) read_stream_kernel(const uint8_t* __restrict__ src, long long bytes,
+                                                                  unsigned* status, int ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)ns * ISTAGE);
+  uint64_t* empty = full + INS_MAX;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + INS_MAX);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long units = bytes / 16;  // 16-byte units, split evenly over the CTAs
+  const long long u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
+  const long long my = (u1 - u0) * 16;
+  const int nst = (int)((my + ISTAGE - 1) / ISTAGE);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < ns; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], ICW);
+    }
+    abort_flag[0] = 0;
+    abort_flag[1] = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == ICW) {
+    if (lane == 0) {
+      int last[INS_MAX];
+      for (int i = 0; i < INS_MAX; ++i) last[i] = -1;
+      bool ok = true;
+      for (int s = 0; s < nst && ok; ++s) {
+        const int st = s % ns;
+        ok = mbar_wait(&empty[st], ((s / ns) & 1) ^ 1, abort_flag, status);
+        if (!ok) break;
+        const long long off = (long long)s * ISTAGE;
+        const uint32_t b = (uint32_t)(my - off < ISTAGE ? my - off : ISTAGE);
+        mbar_arrive_expect_tx(&full[st], b);
+        bulk_load_1d(smem + st * ISTAGE, src + u0 * 16 + off, b, &full[st]);
+        last[st] = s;
+      }
+      if (!ok)
+        for (int i = 0; i < ns; ++i)
+          if (last[i] >= 0) mbar_wait(&full[i], (last[i] / ns) & 1, abort_flag + 1, status);
+    }
+    return;
+  }
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
+  bool ok = true;
+  for (int s = 0; s < nst; ++s) {
+    const int st = s % ns;
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (s / ns) & 1, abort_flag, status));
+    if (!ok) break;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_read_stream(const void* src, long long bytes, unsigned* status, cudaStream_t s) {
+  const int ns = 5;
+  const size_t smem = 128 + (size_t)ns * ISTAGE + 2 * INS_MAX * 8 + 16;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(read_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)num_sms());
+  cfg.blockDim = dim3(ITHREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, read_stream_kernel, (const uint8_t*)src, bytes, status, ns);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return e;
+}
+
+bool gemv_i8_fits(int qtype, int n, int k, int T, bool swiglu) {
+  // one token; k % 256 == 0 (whole rows 16-byte aligned in a stage); a row's
+  // warps within the consumer warps; at most IMAXROWS rows a CTA
+  if (T != 1 || k % 256 != 0 || (k / 64 + 31) / 32 > 8) return false;
+  if ((n + num_sms() - 1) / num_sms() > IMAXROWS) return false;
+  return rows_per_stage(qtype, k, swiglu) >= 1 && i8_stages(k) >= 4;
+}
+
+cudaError_t launch_gemv_i8(int qtype, const void* W, const void* Wu, int n, int k, const float* X, float* Y,
+                           const float* R, unsigned* status, cudaStream_t s) {
+  const bool swi = Wu != nullptr;
+  if (qtype == kQ4_0)
+    return swi ? launch_i8<kQ4_0, true>(W, Wu, n, k, X, Y, R, status, s)
+               : launch_i8<kQ4_0, false>(W, Wu, n, k, X, Y, R, status, s);
+  return swi ? launch_i8<kQ8_0, true>(W, Wu, n, k, X, Y, R, status, s)
+             : launch_i8<kQ8_0, false>(W, Wu, n, k, X, Y, R, status, s);
+}
+
+}  // namespace apr

@@ -26,7 +26,7 @@ def declared_functions():
 
 def test_every_declared_symbol_is_exported(q):
     names = declared_functions()
-    assert len(names) == 16, names
+    assert len(names) == 17, names
     lib = q.library()
     for name in names:
         assert hasattr(lib, name), name
@@ -245,3 +245,16 @@ def test_prefill_layer_argument_errors(q):
     assert lib.apr_prefill_layer(ctypes.byref(args(K_cache=8 * A + 4096))) == q.APR_E_ALIAS
     assert lib.apr_prefill_layer(ctypes.byref(args(V_cache=A + 4096))) == q.APR_E_ALIAS
     assert lib.apr_prefill_layer(ctypes.byref(args(T=0))) == q.APR_OK
+
+
+def test_read_stream_argument_errors(q):
+    import torch
+
+    lib = q.library()
+    assert lib.apr_read_stream(A, 24, None) == q.APR_E_INVAL
+    assert lib.apr_read_stream(A, -16, None) == q.APR_E_INVAL
+    assert lib.apr_read_stream(None, 32, None) == q.APR_E_INVAL
+    assert lib.apr_read_stream(A + 8, 32, None) == q.APR_E_ALIGN
+    assert lib.apr_read_stream(A, 0, None) == q.APR_OK
+    if not torch.cuda.is_available():
+        assert lib.apr_read_stream(A, 32, None) == q.APR_E_DEVICE

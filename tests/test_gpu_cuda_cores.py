@@ -192,3 +192,13 @@ def test_empty_batch_leaves_output(q):
     q.apr_qgemm(synth.Q4_0, dev(c["W"]), 0, k, dev(c["X"]), 1, Y)
     q.apr_stream_status()
     assert torch.all(Y == 7.0)
+
+
+@pytest.mark.parametrize("nbytes", [16, 16400, 9437184, 28311552 + 48])
+def test_read_stream_reads_and_changes_nothing(q, nbytes):
+    # the GEMV's data movement alone: it runs to completion and writes nothing
+    src = torch.arange(nbytes // 4, dtype=torch.int32, device="cuda")
+    before = src.clone()
+    q.apr_read_stream(src, nbytes)
+    assert q.apr_stream_status() == q.APR_OK
+    assert torch.equal(src, before)
