@@ -1,4 +1,4 @@
-"""CPU oracle (float64) for the Q4_0 / Q8_0 prefill projections.
+"""CPU oracle (float64) for the Q4_0 / Q8_0 / F16 prefill projections.
 
 TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and
 ``bench.py``'s CPU-baseline legs use it. It shares no code with the CUDA
@@ -6,6 +6,7 @@ library and never imports it.
 """
 
 from .qref import (  # noqa: F401
+    F16,
     Q4_0,
     Q8_0,
     fp16_bits_to_f64,

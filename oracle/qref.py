@@ -1,4 +1,4 @@
-"""Plain CPU oracle for the Q4_0 / Q8_0 prefill projections (float64).
+"""Plain CPU oracle for the Q4_0 / Q8_0 / F16 prefill projections (float64).
 
 TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import or call
@@ -16,7 +16,14 @@ What is computed, and where the pages define it:
   size (18 bytes), the position of ``d`` and the fp16 encoding of 1.0
   (``0x00, 0x3C``). Q8_0 = fp16 ``d`` + 32 int8, ``w = d * q`` (32 elements per
   block, the ``k.div_ceil(32)`` dequant grid of aprender-serve 0.70.2
-  src/cuda/executor/gdn_prefill_ops.rs, ``qwen35_dequant_f32``).
+  src/cuda/executor/gdn_prefill_ops.rs, ``qwen35_dequant_f32``). F16 = each
+  element its own IEEE binary16 value, two little-endian bytes, row after row
+  (the F16 arm of that dispatch, with the same ``(n, k.div_ceil(32))`` grid,
+  and its test ``f16_weight_dequantizes_on_the_device``, which writes the
+  weight as ``f16::from_f32(v).to_le_bytes()`` per element and expects the
+  values back unchanged). Here a "block" of F16 is 32 consecutive elements
+  (64 bytes), so that every format is addressed the same way; ``k`` is a
+  multiple of 32 for every format.
 * Projection ``Y[T][n] = X[T][k] . W[n][k]^T`` (aprender-serve 0.70.2
   src/cuda/executor/gdn_prefill_ops.rs, doc of ``qwen35_project_rows``),
   optionally ``+ R[T][n]`` (the residual add that follows the down / output
@@ -67,10 +74,11 @@ from __future__ import annotations
 
 import numpy as np
 
+F16 = 1
 Q4_0 = 2
 Q8_0 = 8
 _QK = 32
-_BLOCK_BYTES = {Q4_0: 18, Q8_0: 34}
+_BLOCK_BYTES = {F16: 64, Q4_0: 18, Q8_0: 34}
 
 
 # --------------------------------------------------------------------------
@@ -111,6 +119,8 @@ def block_scales_and_codes(qtype: int, W: np.ndarray, n: int, k: int):
     ``q'`` is ``nibble - 8`` for Q4_0 and the int8 value for Q8_0, shape
     ``[n][k/32][32]`` (int64), element order as stored.
     """
+    if qtype == F16:
+        raise ValueError("F16 weights have no block scales")
     blk = _blocks(qtype, W, n, k)
     d_bits = blk[..., 0].astype(np.uint16) | (blk[..., 1].astype(np.uint16) << 8)
     payload = blk[..., 2:]
@@ -124,19 +134,25 @@ def block_scales_and_codes(qtype: int, W: np.ndarray, n: int, k: int):
 
 
 def dequant_f64(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
-    """``Wf[i][j] = fp16(d_{i, j/32}) * q'_{i,j}`` in float64, shape ``[n][k]``."""
+    """``Wf[i][j] = fp16(d_{i, j/32}) * q'_{i,j}`` in float64, shape ``[n][k]``;
+    for F16 the binary16 value of element ``(i, j)``."""
+    if qtype == F16:
+        raw = _blocks(qtype, W, n, k).reshape(n, k, 2)
+        bits = raw[..., 0].astype(np.uint16) | (raw[..., 1].astype(np.uint16) << 8)
+        return fp16_bits_to_f64(bits)
     d_bits, codes = block_scales_and_codes(qtype, W, n, k)
     d = fp16_bits_to_f64(d_bits)
     return (d[..., None] * codes.astype(np.float64)).reshape(n, k)
 
 
 def dequant_f32(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
-    """The standalone dequant export: ``f32(d) * f32(q')``.
+    """The standalone dequant export: ``f32(d) * f32(q')`` (F16: ``f32(w)``).
 
     ``d`` has at most 11 significant bits and ``|q'| <= 128`` at most 8, so the
     float64 product is exact and so is its conversion to float32 (the range of
     an fp16 scale times 128 is well inside float32's normal range, and fp16
-    subnormal scales times small integers stay exact in float32).
+    subnormal scales times small integers stay exact in float32). Every fp16
+    value, subnormals included, is a float32 value.
     """
     return dequant_f64(qtype, W, n, k).astype(np.float32)
 

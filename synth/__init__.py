@@ -2,13 +2,14 @@
 
 This package is shared by the CUDA path's tests and benchmark and by the CPU
 oracle's tests. It only *makes* inputs: seeded normal draws and the GGUF block
-encoder that turns an f32 weight into Q4_0 / Q8_0 bytes. It holds none of the
+encoders that turn an f32 weight into Q4_0 / Q8_0 / F16 bytes. It holds none of the
 arithmetic the prefill path computes (block decoding, the products, the
 epilogues): that lives, twice and independently, in ``oracle/`` and in the
 CUDA library.
 """
 
 from .gen import (  # noqa: F401
+    F16,
     Q4_0,
     Q8_0,
     BLOCK_ELEMS,
@@ -16,6 +17,7 @@ from .gen import (  # noqa: F401
     quantize,
     quantize_q4_0,
     quantize_q8_0,
+    quantize_f16,
     weight_f32,
     activations,
     make_case,

@@ -1,4 +1,4 @@
-"""Seeded generators and the GGUF Q4_0 / Q8_0 block encoder.
+"""Seeded generators and the GGUF Q4_0 / Q8_0 / F16 weight encoders.
 
 Recipe (the same for every workload):
 
@@ -20,6 +20,8 @@ Recipe (the same for every workload):
   ``round`` is half away from zero, ``w / d`` uses the f32 ``d`` before it is
   rounded to fp16 (round to nearest even) for storage, and an all-zero block
   gets ``d = 0`` with ``q = 8`` (Q4_0) or ``q = 0`` (Q8_0).
+* or stored as F16: every element rounded to its nearest binary16 value (ties
+  to even), two little-endian bytes each, ``[n][2k]`` bytes.
 
 Prefill attention (``attention_case``): the query rows ``Q`` and the K and V
 caches are ``N(0, 1)`` float32 draws with seeds ``seed``, ``seed+1`` and
@@ -33,14 +35,15 @@ from __future__ import annotations
 
 import numpy as np
 
+F16 = 1   # GGUF type id
 Q4_0 = 2  # GGUF type id
 Q8_0 = 8  # GGUF type id
 BLOCK_ELEMS = 32
-_BLOCK_BYTES = {Q4_0: 18, Q8_0: 34}
+_BLOCK_BYTES = {F16: 64, Q4_0: 18, Q8_0: 34}
 
 
 def block_bytes(qtype: int) -> int:
-    """Bytes of one 32-element block of ``qtype``."""
+    """Bytes of 32 elements of ``qtype`` (one block; 64 bytes of F16)."""
     return _BLOCK_BYTES[qtype]
 
 
@@ -92,7 +95,16 @@ def quantize_q8_0(w: np.ndarray) -> np.ndarray:
     return out.reshape(n, -1)
 
 
+def quantize_f16(w: np.ndarray) -> np.ndarray:
+    """Store an f32 ``[n][k]`` weight as F16 bytes ``[n][2k]`` (RNE, little endian)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n, k = w.shape
+    return np.ascontiguousarray(w.astype("<f2")).view(np.uint8).reshape(n, 2 * k)
+
+
 def quantize(qtype: int, w: np.ndarray) -> np.ndarray:
+    if qtype == F16:
+        return quantize_f16(w)
     if qtype == Q4_0:
         return quantize_q4_0(w)
     if qtype == Q8_0:
@@ -127,6 +139,7 @@ def random_blocks(qtype: int, n: int, k: int, seed: int, scale_class: str = "mix
     (every Q4_0 nibble 0..15, every Q8_0 code -128..127) and fp16 scales of both
     signs whose exponent field is uniform over the class's range (random
     mantissa; the subnormal class has a nonzero mantissa). Scales are finite.
+    For F16 the elements themselves are drawn that way.
 
     ``fp16_range``: cap |d| so that |d * q| stays within fp16's largest finite
     value 65504 for every code (|q| <= 8 for Q4_0, 128 for Q8_0): the scale's
@@ -134,6 +147,16 @@ def random_blocks(qtype: int, n: int, k: int, seed: int, scale_class: str = "mix
     gives |d| <= 8188 or 511.75.
     """
     lo, hi = SCALE_CLASSES[scale_class]
+    if qtype == F16:
+        # every element an fp16 value of both signs, exponent field uniform over
+        # the class (nonzero mantissa in the subnormal class)
+        rng = np.random.default_rng(seed)
+        exp = rng.integers(lo, hi + 1, size=(n, k)).astype(np.uint16)
+        man = rng.integers(0, 1024, size=(n, k)).astype(np.uint16)
+        man = np.where(exp == 0, np.maximum(man, 1), man)
+        sign = rng.integers(0, 2, size=(n, k)).astype(np.uint16)
+        bits = ((sign << 15) | (exp << 10) | man).astype("<u2")
+        return np.ascontiguousarray(bits).view(np.uint8).reshape(n, 2 * k)
     if fp16_range:
         hi = min(hi, 27 if qtype == Q4_0 else 23)
     rng = np.random.default_rng(seed)

@@ -23,6 +23,7 @@ import oracle
 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+QTYPES = [synth.Q4_0, synth.Q8_0, synth.F16]
 
 
 def load_golden(name):
@@ -54,7 +55,61 @@ def test_golden_block_dequant(name):
 
 def test_golden_files_present():
     assert {"q4_0_zero_block.txt", "q4_0_nibble_order.txt", "q8_0_half_scale.txt",
-            "q8_0_subnormal_scale.txt", "q4_0_negative_scale.txt"} <= set(GOLDEN_FILES)
+            "q8_0_subnormal_scale.txt", "q4_0_negative_scale.txt", "f16_exact_values.txt"} <= set(GOLDEN_FILES)
+
+
+# ---------------------------------------------------------------- F16 weights
+def test_f16_weight_page_values_come_back_unchanged():
+    # aprender-serve 0.70.2 src/cuda/executor/gdn_prefill_ops.rs,
+    # f16_weight_dequantizes_on_the_device: n = 2, k = 64, w = i * 0.5 - 16 for
+    # element i in row-major order, stored as little-endian halves
+    n, k = 2, 64
+    want = np.array([i * 0.5 - 16.0 for i in range(n * k)]).reshape(n, k)
+    raw = np.frombuffer(b"".join(struct.pack("<e", v) for v in want.reshape(-1)), np.uint8).reshape(n, 2 * k)
+    np.testing.assert_array_equal(oracle.dequant_f64(synth.F16, raw, n, k), want)
+    got32 = oracle.dequant_f32(synth.F16, raw, n, k)
+    assert got32.dtype == np.float32
+    np.testing.assert_array_equal(got32.astype(np.float64), want)
+    # the encoder writes exactly those bytes
+    np.testing.assert_array_equal(synth.quantize(synth.F16, want.astype(np.float32)), raw)
+
+
+def test_f16_weight_equals_a_q8_0_weight_with_the_same_values():
+    # a Q8_0 block whose values d * q are fp16 values (d = 2^-3, |q| <= 127:
+    # at most 7 significant bits), written as F16: every product is the same
+    n, k, T = 3, 64, 2
+    rng = np.random.default_rng(5)
+    blk = np.zeros((n, k // 32, 34), np.uint8)
+    blk[..., 0], blk[..., 1] = 0x00, 0x30                    # d = 0x3000 = 2^-3
+    codes = rng.integers(-127, 128, size=(n, k // 32, 32)).astype(np.int8)
+    blk[..., 2:] = codes.view(np.uint8)
+    W8 = blk.reshape(n, -1)
+    vals = codes.reshape(n, k).astype(np.float64) / 8.0
+    W16 = np.frombuffer(b"".join(struct.pack("<e", v) for v in vals.reshape(-1)), np.uint8).reshape(n, 2 * k)
+    X = synth.activations(T, k, 6)
+    R = synth.activations(T, n, 7)
+    np.testing.assert_array_equal(oracle.qgemm_f64(synth.F16, W16, n, k, X, R), oracle.qgemm_f64(synth.Q8_0, W8, n, k, X, R))
+    np.testing.assert_array_equal(oracle.dequant_f32(synth.F16, W16, n, k), oracle.dequant_f32(synth.Q8_0, W8, n, k))
+
+
+def test_f16_weight_has_no_block_scales_and_needs_its_byte_count():
+    raw = np.zeros((2, 128), np.uint8)
+    with pytest.raises(ValueError):
+        oracle.block_scales_and_codes(synth.F16, raw, 2, 64)
+    with pytest.raises(ValueError):
+        oracle.dequant_f64(synth.F16, raw[:, :96], 2, 64)
+    with pytest.raises(ValueError):
+        oracle.dequant_f64(synth.F16, raw.reshape(-1)[:96], 1, 48)  # k % 32 != 0
+
+
+def test_f16_weights_reach_every_finite_half():
+    # the random F16 generator draws every exponent field 0..30 and no inf/NaN;
+    # the oracle decodes each element to its binary16 value
+    W = synth.random_blocks(synth.F16, 16, 256, seed=3)
+    bits = W.view("<u2")
+    exp = (bits >> 10) & 0x1F
+    assert set(np.unique(exp)) == set(range(31))
+    np.testing.assert_array_equal(oracle.dequant_f64(synth.F16, W, 16, 256), bits.view(np.float16).astype(np.float64))
 
 
 # ---------------------------------------------------------------- fp16 decode
@@ -101,6 +156,8 @@ def test_fp16_decode_landmarks():
 # ---------------------------------------------------------------- brute force
 def _parse_block_independent(qtype, blk: bytes):
     """(Fraction d, list of 32 int codes) via struct, not the oracle's decoder."""
+    if qtype == synth.F16:  # 32 binary16 values, no scale
+        return Fraction(1), [Fraction(v) for v in struct.unpack("<32e", blk)]
     d = Fraction(struct.unpack("<e", blk[0:2])[0])
     if qtype == synth.Q4_0:
         lo = [(b & 0xF) - 8 for b in blk[2:18]]
@@ -110,11 +167,16 @@ def _parse_block_independent(qtype, blk: bytes):
 
 
 def _random_blocks(rng, qtype, n, k):
-    """Random raw bytes with finite scales (exponent field kept below 31)."""
+    """Random raw bytes with finite scales (exponent field kept below 31); for
+    F16 every element is such a half."""
     bb = synth.block_bytes(qtype)
     raw = rng.integers(0, 256, size=(n, k // 32, bb), dtype=np.uint8)
-    hi = raw[..., 1]
-    raw[..., 1] = np.where((hi & 0x7C) == 0x7C, hi & 0xBF, hi)  # clear one exp bit
+    hi = raw[..., 1::2] if qtype == synth.F16 else raw[..., 1]
+    hi = np.where((hi & 0x7C) == 0x7C, hi & 0xBF, hi)  # clear one exp bit
+    if qtype == synth.F16:
+        raw[..., 1::2] = hi
+    else:
+        raw[..., 1] = hi
     return raw.reshape(n, -1)
 
 
@@ -145,7 +207,7 @@ def _ulp32(x):
     return float(np.spacing(x)) if x != 0 else float(np.spacing(np.float32(0)))
 
 
-@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
+@pytest.mark.parametrize("qtype", QTYPES)
 @pytest.mark.parametrize("n,k,T,res", [(3, 32, 2, False), (5, 64, 3, True), (2, 96, 1, True)])
 def test_brute_force_exact_rationals(qtype, n, k, T, res):
     rng = np.random.default_rng(1234 + n + k + T + qtype)
@@ -166,7 +228,7 @@ def test_brute_force_exact_rationals(qtype, n, k, T, res):
     assert n_equal >= T * n - 1
 
 
-@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
+@pytest.mark.parametrize("qtype", QTYPES)
 def test_brute_force_dequant_exact(qtype):
     rng = np.random.default_rng(77 + qtype)
     n, k = 4, 64
@@ -178,7 +240,7 @@ def test_brute_force_dequant_exact(qtype):
             assert Fraction(float(got[i, j])) == rows[i][j]
 
 
-@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
+@pytest.mark.parametrize("qtype", QTYPES)
 def test_brute_force_swiglu(qtype):
     rng = np.random.default_rng(99 + qtype)
     n, k, T = 4, 64, 3
@@ -196,7 +258,7 @@ def test_brute_force_swiglu(qtype):
 
 
 # ---------------------------------------------------------------- invariants
-@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
+@pytest.mark.parametrize("qtype", QTYPES)
 def test_identity_x_returns_dequantized_weight(qtype):
     n, k = 8, 64
     W = synth.quantize(qtype, synth.weight_f32(n, k, seed=5))
@@ -205,7 +267,7 @@ def test_identity_x_returns_dequantized_weight(qtype):
     np.testing.assert_array_equal(Y, oracle.dequant_f32(qtype, W, n, k).T)
 
 
-@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
+@pytest.mark.parametrize("qtype", QTYPES)
 def test_scaling_and_permutation(qtype):
     n, k, T = 16, 128, 7
     case = synth.make_case(qtype, n, k, T, seed=3)
@@ -329,6 +391,8 @@ def test_ffn_sublayer_special_cases():
 
 def _block_values(raw, qtype, n, k):
     """Dequantized weight from the raw bytes, by the block rules (struct parse)."""
+    if qtype == synth.F16:
+        return np.array([struct.unpack("<%de" % k, bytes(raw[i])) for i in range(n)], dtype=np.float64)
     bb = 18 if qtype == synth.Q4_0 else 34
     out = np.zeros((n, k))
     for i in range(n):
@@ -345,7 +409,7 @@ def _block_values(raw, qtype, n, k):
     return out
 
 
-@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
+@pytest.mark.parametrize("qtype", QTYPES)
 def test_ffn_sublayer_brute_force(qtype):
     """Element-by-element loops (struct block parsing, math.sqrt, math.exp)
     against the oracle's array form."""
@@ -372,7 +436,7 @@ def test_ffn_sublayer_brute_force(qtype):
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
 
 
-@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q8_0])
+@pytest.mark.parametrize("qtype", QTYPES)
 def test_normed_projection_reduces_to_projection(qtype):
     """Rows of +-1 have mean square 1, so with eps = 0 and unit weight the norm
     is the identity and the normed projection is the plain one (pinned above
