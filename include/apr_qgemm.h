@@ -1,6 +1,6 @@
 /*
  * apr_qgemm.h — C ABI of the GB300 (sm_103a) prefill projections over GGUF
- * Q4_0 / Q8_0 block-quantized weights.
+ * Q4_0 / Q8_0 block-quantized weights and F16 weights.
  *
  * Every projection of a batched (chunked) prompt prefill is ONE product over
  * the chunk's T token rows, instead of T per-token GEMVs:
@@ -20,6 +20,12 @@
  *                    element j in its low nibble and element j+16 in its high
  *                    nibble; w = d * (nibble - 8).
  *   Q8_0 (34 bytes): fp16 d then 32 int8 q; w = d * q.
+ *   F16  (64 bytes per 32 weights): each weight its own IEEE binary16 value,
+ *                    little endian (the F16 arm of aprender-serve
+ *                    qwen35_dequant_f32, and its test
+ *                    f16_weight_dequantizes_on_the_device). Every F16 call
+ *                    takes k % 32 == 0 like the block formats; on the fp16
+ *                    leg the weights enter the tensor cores unrounded.
  * Row i of W is the k/32 consecutive blocks starting at byte i*(k/32)*bytes.
  *
  * Memory and streams. Every pointer argument named W, Wu, X, residual, Y or
@@ -48,7 +54,7 @@
  *   APR_E_INVAL   null pointer with nonzero sizes, n < 0, T < 0, k <= 0,
  *                 k % 32 != 0, a size beyond the documented limits, or an
  *                 unknown leg / path
- *   APR_E_QTYPE   qtype is not APR_Q4_0 or APR_Q8_0
+ *   APR_E_QTYPE   qtype is not APR_Q4_0, APR_Q8_0 or APR_F16
  *   APR_E_ALIGN   a pointer is not 16-byte aligned
  *   APR_E_ALIAS   Y overlaps X, W or Wu, or overlaps residual without being
  *                 exactly the same buffer (Y == residual is allowed: it gives
@@ -84,7 +90,7 @@ extern "C" {
 typedef struct CUstream_st* apr_stream_t;
 
 /* GGUF tensor type ids. */
-enum { APR_Q4_0 = 2, APR_Q8_0 = 8 };
+enum { APR_F16 = 1, APR_Q4_0 = 2, APR_Q8_0 = 8 };
 
 /*
  * Arithmetic legs (aprender-serve gdn_prefill_ops.rs, module doc, group 1):
@@ -128,7 +134,7 @@ int apr_gemv_max_T(void);
 
 /*
  * Y = X . dequant(W)^T (+ residual), fp16 leg, T rule.
- *   qtype     APR_Q4_0 or APR_Q8_0
+ *   qtype     APR_Q4_0, APR_Q8_0 or APR_F16
  *   W         [n rows][k/32 blocks] GGUF blocks
  *   X         [T][k] f32;  Y [T][n] f32, overwritten
  *   residual  [T][n] f32 or NULL; may be Y itself (accumulate)
@@ -156,7 +162,8 @@ int apr_qgemm_gate_up_swiglu(int qtype, const void* Wg, const void* Wu, int n, i
  * arithmetic, optional residual (gemv_q4_0_pf / gemv_q8_0_pf of
  * oxibonsai-kernels, used for the last-token lm_head in
  * try_cuda_prefill_q_std). For T <= 8 weight rows stream by bulk copies into
- * T fp32 accumulators (tensor cores for T = 3, 4); for 9 <= T <= 16 (k % 256
+ * T fp32 accumulators (tensor cores for T = 3, 4 with block formats; F16
+ * weights always on the CUDA cores); for 9 <= T <= 16 (k % 256
  * == 0) the exact leg's tensor-core GEMM runs instead (50 us against 200 to
  * 700 us for the CUDA-core kernels at 4096 x 4096 and 12288 x 4096, T = 12
  * and 16). T > APR_GEMV_MAX_T gives APR_E_INVAL. The weights are read early
@@ -270,7 +277,7 @@ int apr_qgemm_rmsnorm(const apr_qgemm_args* args, const float* norm_weight, floa
  * gate/up SwiGLU GEMM, down GEMM with the residual added; aprender-serve
  * forward_qwen35_cuda_prefill.rs prefill_ffn_rows). The norm is not printed
  * there; this is the usual RMSNorm of a row, eps inside the square root.
- *   qtype      APR_Q4_0 or APR_Q8_0 for all three weights
+ *   qtype      APR_Q4_0, APR_Q8_0 or APR_F16 for all three weights
  *   leg        APR_LEG_F16 or APR_LEG_EXACT_F32, as for apr_qgemm_ex; the f16
  *              leg writes the normed rows straight as fp16 (norm and
  *              conversion in one pass) for the tensor-core GEMMs
@@ -402,10 +409,12 @@ int apr_prefill_layer(const apr_layer_args* args);
 
 /*
  * Standalone dequant: out[n][k] f32 = f32(d) * f32(q'), bit exact (the product
- * of an fp16 scale and a code of at most 8 bits is exact in fp32). The device
- * dequant of aprender-serve gdn_prefill_ops.rs qwen35_dequant_f32 (Q8_0 and
- * the other formats it dispatches), here for Q4_0 and Q8_0 and meant for
- * tests: the projections never write decoded weights to memory.
+ * of an fp16 scale and a code of at most 8 bits is exact in fp32); for F16
+ * out = f32(w), also exact. The device dequant of aprender-serve
+ * gdn_prefill_ops.rs qwen35_dequant_f32 (Q8_0, F16 and the other formats it
+ * dispatches), here for Q4_0, Q8_0 and F16 and meant for tests: the
+ * projections never write decoded weights to memory. An F16 W needs only
+ * 2-byte alignment here (APR_E_ALIGN otherwise).
  */
 int apr_dequant(int qtype, const void* W, int n, int k, float* out, apr_stream_t stream);
 

@@ -15,6 +15,7 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libapr_qgemm.so")
 
+APR_F16 = 1
 APR_Q4_0 = 2
 APR_Q8_0 = 8
 APR_LEG_F16 = 0
@@ -36,7 +37,7 @@ APR_AUTO_GEMV_MAX_T = 7
 APR_NOALLOC_MAX_TK = 8 * 1024 * 1024
 APR_FFN_CHUNK_ROWS = 2048
 
-BLOCK_BYTES = {APR_Q4_0: 18, APR_Q8_0: 34}
+BLOCK_BYTES = {APR_F16: 64, APR_Q4_0: 18, APR_Q8_0: 34}  # bytes per 32 weights
 
 # Every symbol include/apr_qgemm.h declares.
 EXPORTS = (

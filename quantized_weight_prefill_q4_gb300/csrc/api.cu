@@ -177,9 +177,11 @@ struct Problem {
 
 int ldy_of(const Problem& p) { return p.ldy > 0 ? p.ldy : p.n; }
 
+bool known_qtype(int q) { return q == APR_Q4_0 || q == APR_Q8_0 || q == APR_F16; }
+
 // Host-side checks; returns APR_OK, an error, or 1 for "nothing to do".
 int check(const Problem& p, size_t x_elem_bytes = 4) {
-  if (p.qtype != APR_Q4_0 && p.qtype != APR_Q8_0) return fail(APR_E_QTYPE, "unsupported qtype %d", p.qtype);
+  if (!known_qtype(p.qtype)) return fail(APR_E_QTYPE, "unsupported qtype %d", p.qtype);
   if (p.leg != APR_LEG_F16 && p.leg != APR_LEG_EXACT_F32) return fail(APR_E_INVAL, "unknown leg %d", p.leg);
   if (p.path != APR_PATH_AUTO && p.path != APR_PATH_GEMV && p.path != APR_PATH_GEMM)
     return fail(APR_E_INVAL, "unknown path %d", p.path);
@@ -233,7 +235,8 @@ int run(const Problem& p) {
     leg = APR_LEG_EXACT_F32;
   }
   if (path == APR_PATH_GEMV) {
-    if (!gemv_tc_takes(p.n, p.k, p.T, p.Wu != nullptr))
+    // the tensor-core GEMV multiplies integer codes: block formats only
+    if (p.qtype == APR_F16 || !gemv_tc_takes(p.n, p.k, p.T, p.Wu != nullptr))
       return launched(launch_gemv(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, ldy_of(p), p.R, st->status, p.s),
                       "gemv");
     // tensor-core GEMV: the stream's scratch holds its split X, scales and
@@ -299,7 +302,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // FFN sublayer: per chunk of rows, the norm into scratch, then gate/up SwiGLU
 // into scratch, then down with the chunk's rows of X as residual and output.
 int run_ffn(const apr_ffn_args& a) {
-  if (a.qtype != APR_Q4_0 && a.qtype != APR_Q8_0) return fail(APR_E_QTYPE, "unsupported qtype %d", a.qtype);
+  if (!known_qtype(a.qtype)) return fail(APR_E_QTYPE, "unsupported qtype %d", a.qtype);
   if (a.leg != APR_LEG_F16 && a.leg != APR_LEG_EXACT_F32) return fail(APR_E_INVAL, "unknown leg %d", a.leg);
   if (a.hidden <= 0 || a.inter <= 0 || a.hidden % 32 != 0 || a.inter % 32 != 0 || a.T < 0)
     return fail(APR_E_INVAL, "bad sizes hidden=%d inter=%d T=%d (need multiples of 32, T >= 0)", a.hidden, a.inter,
@@ -410,7 +413,7 @@ int run_normed(const Problem& p, const float* w, float eps) {
 // causal attention, the output projection added into X), then the FFN
 // sublayer on the chunk's rows of X.
 int run_layer(const apr_layer_args& a) {
-  if (a.qtype != APR_Q4_0 && a.qtype != APR_Q8_0) return fail(APR_E_QTYPE, "unsupported qtype %d", a.qtype);
+  if (!known_qtype(a.qtype)) return fail(APR_E_QTYPE, "unsupported qtype %d", a.qtype);
   if (a.leg != APR_LEG_F16 && a.leg != APR_LEG_EXACT_F32) return fail(APR_E_INVAL, "unknown leg %d", a.leg);
   if (a.head_dim != 256) return fail(APR_E_INVAL, "head_dim must be 256 (got %d)", a.head_dim);
   if (a.hidden <= 0 || a.inter <= 0 || a.hidden % 32 != 0 || a.inter % 32 != 0 || a.T < 0 || a.pos0 < 0 ||
@@ -661,12 +664,13 @@ int apr_prefill_attention(const float* Q, const float* K_cache, const float* V_c
 
 int apr_dequant(int qtype, const void* W, int n, int k, float* out, apr_stream_t stream) {
   t_msg[0] = 0;
-  if (qtype != APR_Q4_0 && qtype != APR_Q8_0) return fail(APR_E_QTYPE, "unsupported qtype %d", qtype);
+  if (!known_qtype(qtype)) return fail(APR_E_QTYPE, "unsupported qtype %d", qtype);
   if (n < 0 || k <= 0 || k % 32 != 0) return fail(APR_E_INVAL, "bad sizes n=%d k=%d", n, k);
   if (n > (1 << 24) || k > (1 << 20) || (int64_t)n * (k / 32) > (int64_t)1 << 31)
     return fail(APR_E_INVAL, "sizes beyond the supported limits");
   if (n == 0) return APR_OK;
   if (!W || !out) return fail(APR_E_INVAL, "null pointer");
+  if (qtype == APR_F16 && ((uintptr_t)W & 1) != 0) return fail(APR_E_ALIGN, "an F16 weight must be 2-byte aligned");
   const size_t wbytes = (size_t)n * (size_t)(k / 32) * (size_t)block_bytes(qtype);
   if (overlap(out, (size_t)n * k * 4, W, wbytes)) return fail(APR_E_ALIAS, "out overlaps W");
   DeviceState* st = nullptr;

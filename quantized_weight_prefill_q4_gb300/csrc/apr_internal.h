@@ -8,10 +8,12 @@
 
 namespace apr {
 
+constexpr int kF16 = 1;
 constexpr int kQ4_0 = 2;
 constexpr int kQ8_0 = 8;
 
-inline int block_bytes(int qtype) { return qtype == kQ4_0 ? 18 : 34; }
+// bytes of 32 consecutive elements of a weight row (one block; 64 for F16)
+inline int block_bytes(int qtype) { return qtype == kQ4_0 ? 18 : (qtype == kQ8_0 ? 34 : 64); }
 
 // Epilogue of a projection.
 enum Epilogue { kEpiPlain = 0, kEpiResidual = 1, kEpiSwiGLU = 2 };

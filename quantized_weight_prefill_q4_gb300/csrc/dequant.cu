@@ -1,4 +1,4 @@
-// Standalone block dequant: out[n][k] = f32(d) * f32(q'), bit exact.
+// Standalone dequant: out[n][k] = f32(d) * f32(q') (F16: f32(w)), bit exact.
 //
 // The device dequant of aprender-serve 0.70.2 src/cuda/executor/gdn_prefill_ops.rs
 // (qwen35_dequant_f32: one 32-element block per warp, one element per lane),
@@ -20,6 +20,10 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
   const size_t nb_row = (size_t)(k / 32);
   for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (size_t)gridDim.x * blockDim.x) {
+    if constexpr (QT == kF16) {  // each element its own half: widening is exact
+      out[idx] = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t*>(W)[idx]));
+      continue;
+    }
     const size_t row = idx / (size_t)k;
     const uint32_t col = (uint32_t)(idx - row * (size_t)k);
     const uint8_t* blk = W + (row * nb_row + col / 32) * BB;
@@ -43,7 +47,9 @@ cudaError_t launch_dequant(int qtype, const void* W, int n, int k, float* out, c
   const size_t total = (size_t)n * (size_t)k;
   size_t blocks = (total + 255) / 256;
   if (blocks > 152 * 64) blocks = 152 * 64;
-  if (qtype == kQ4_0)
+  if (qtype == kF16)
+    dequant_kernel<kF16><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);
+  else if (qtype == kQ4_0)
     dequant_kernel<kQ4_0><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);
   else
     dequant_kernel<kQ8_0><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);

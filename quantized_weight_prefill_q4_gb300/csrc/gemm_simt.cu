@@ -1,10 +1,10 @@
-// Exact-fp32 GEMM over Q4_0 / Q8_0 blocks on the CUDA cores (FFMA).
+// Exact-fp32 GEMM over Q4_0 / Q8_0 blocks (or F16 weights) on the CUDA cores (FFMA).
 //
 // The f32 leg of aprender-serve 0.70.2 src/cuda/executor/gdn_prefill_ops.rs
 // (qwen35_project_rows: fp32 in and out, no TF32, because these projections
 // feed a recurrence that compounds low-precision error), without the f32
 // dequant scratch: each 64-row x 32-column weight tile is decoded exactly
-// (fp16 d times a code of at most 8 bits is exact in fp32) straight into
+// (fp16 d times a code of at most 8 bits, or a half, is exact in fp32) straight into
 // shared memory, next to a 64-token x 32-column tile of X, and 256 threads
 // each accumulate a 4 x 4 block of outputs. Works for any k % 32 == 0.
 //
@@ -26,6 +26,12 @@ constexpr int PAD = 4;
 template <int QT>
 __device__ __forceinline__ void decode8(const uint8_t* __restrict__ blk, int part, float (&w)[8]) {
   // part 0..3 -> elements 8*part .. 8*part+7 of the block
+  if constexpr (QT == kF16) {  // 32 halves, 2-byte aligned
+    const __half* h = reinterpret_cast<const __half*>(blk) + part * 8;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e] = __half2float(h[e]);
+    return;
+  }
   const uint16_t db = (uint16_t)blk[0] | ((uint16_t)blk[1] << 8);
   const float d = __half2float(__ushort_as_half(db));
   if (QT == kQ4_0) {
@@ -46,7 +52,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const uint8_t* __restric
                                                         const float* __restrict__ X, int T,
                                                         float* Y, int ldy,
                                                         const float* R) {
-  constexpr int BB = QT == kQ4_0 ? 18 : 34;
+  constexpr int BB = QT == kQ4_0 ? 18 : (QT == kQ8_0 ? 34 : 64);
   constexpr int NM = EPI == kEpiSwiGLU ? 2 : 1;
   __shared__ float Ws[NM][BK][BM + PAD];
   __shared__ float Xs[BK][BN + PAD];
@@ -158,6 +164,7 @@ cudaError_t launch_q(const void* W, const void* Wu, int n, int k, const float* X
 
 cudaError_t launch_gemm_simt(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
                              float* Y, int ldy, const float* R, cudaStream_t s) {
+  if (qtype == kF16) return launch_q<kF16>(W, Wu, n, k, X, T, Y, ldy, R, s);
   return qtype == kQ4_0 ? launch_q<kQ4_0>(W, Wu, n, k, X, T, Y, ldy, R, s)
                         : launch_q<kQ8_0>(W, Wu, n, k, X, T, Y, ldy, R, s);
 }

@@ -101,12 +101,21 @@ struct Cfg {
   static constexpr int NM = EPI == kEpiSwiGLU ? 2 : 1;
   static constexpr int DQ = NM == 1 ? 2 : 1;           // warpgroups per weight (alternate stages)
   static constexpr int NWG = NM * DQ;                   // dequant / epilogue warpgroups
-  static constexpr int BB = QT == kQ4_0 ? 18 : 34;
-  static constexpr int RAW_ROW = CHUNK / 32 * BB;     // 144 / 272 bytes
+  static constexpr bool F16W = QT == kF16;
+  static constexpr int BB = QT == kQ4_0 ? 18 : (QT == kQ8_0 ? 34 : 64);  // bytes per 32 k
+  // k per raw slot: a chunk, or half of one for an F16 gate/up pair (four
+  // slots of 32 KB keep each weight double-buffered)
+  static constexpr int RAW_K = F16W && NM == 2 ? CHUNK / 2 : CHUNK;
+  static constexpr int RAW_SUBS = RAW_K / BK;         // operand stages per raw slot
+  static constexpr int RAW_ROW = RAW_K / 32 * BB;     // 144 / 272 / 512 (or 256) bytes
   static constexpr int RAW_BYTES = BM * RAW_ROW;      // one raw slot
+  // F16 rows arrive as 64-column boxes of [128 rows][128 B], 128-byte
+  // swizzled (conflict-free row reads); block formats as one unswizzled box
+  static constexpr int RAW_LOADS = F16W ? RAW_SUBS : 1;
+  static constexpr int RAW_BOX = F16W ? BK : RAW_ROW / 2;  // 16-bit elements across a box
   static constexpr int NPIECE = BN / PIECE;
   // operand stages (A in TMEM and B in shared memory advance together)
-  static constexpr int S = XS ? 2 : (NM == 2 ? 4 : (BN == 256 ? 4 : (QT == kQ4_0 ? 6 : 5)));
+  static constexpr int S = XS ? 2 : (NM == 2 ? 4 : (BN == 256 ? 4 : (QT == kQ4_0 ? 6 : (F16W ? 4 : 5))));
   // (with 256-token tiles the raw ring also receives the partner's half of a
   // split). With gate/up the chunks of the two weights alternate through the
   // ring, chunk j in slot j % S_RAW; S_RAW must be even so that a slot always
@@ -115,6 +124,8 @@ struct Cfg {
   // whose phase p + 1 belongs to the other warpgroup, and a parity wait cannot
   // tell phase p + 2 from phase p.
   static constexpr int S_RAW = NM == 1 ? (QT == kQ4_0 ? (BN == 256 ? 4 : 3) : 2) : 4;
+  static_assert(!XS || RAW_K == CHUNK, "the exact leg folds one raw slot per accumulation chunk");
+  static_assert(!F16W || BN == 128, "F16 tiles take 128 tokens");
   static constexpr int NTHREADS = 128 + 128 * NWG;
   static constexpr int ACC_COLS = (XS ? 3 : NM) * BN;
   static constexpr int A_COL0 = ACC_COLS;                       // first A column
@@ -217,6 +228,20 @@ __device__ __forceinline__ void dequant_row_stage(const uint32_t* w, uint32_t (&
 }
 
 
+// F16: the 64 k of one row in one 128-byte-swizzled box row: 16-byte unit u
+// of row r sits at unit u ^ (r mod 8) (the box starts 1024-byte aligned).
+__device__ __forceinline__ void f16_row_stage(const uint8_t* box, uint32_t r, uint32_t (&a)[32]) {
+  const uint8_t* row = box + r * 128u;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + ((u ^ (r & 7u)) << 4));
+    a[4 * u] = v.x;
+    a[4 * u + 1] = v.y;
+    a[4 * u + 2] = v.z;
+    a[4 * u + 3] = v.w;
+  }
+}
+
 // Exact leg: one row's two blocks (64 k), words w[0 .. 2 BB / 4), into the
 // fp16 pieces of W * 2^e: a1[j] = fp16(v_2j, v_2j+1) and a2[j] = fp16 of the
 // remainders, v = d * q' * 2^e computed exactly in fp32 (an fp16 scale times a
@@ -236,7 +261,14 @@ template <int QT>
 __device__ __forceinline__ void dequant_row_stage_xs(const uint32_t* w, float sw, uint32_t (&a1)[32],
                                                      uint32_t (&a2)[32]) {
   auto code = [](uint32_t c) { return __uint_as_float(c | 0x4B000000u); };
-  if constexpr (QT == kQ4_0) {
+  if constexpr (QT == kF16) {
+    // w holds the 64 halves themselves (f16_row_stage); v = w * 2^e is exact
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float2 f = __half22float2(u32_as_h2(w[j]));
+      split2(f.x * sw, f.y * sw, a1[j], a2[j]);
+    }
+  } else if constexpr (QT == kQ4_0) {
     uint32_t p[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) p[i] = __byte_perm(w[i], w[i + 1], 0x5432);
@@ -321,6 +353,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
   const int c0 = (int)((long)z * nchunks_all / nsplit), c1 = (int)((long)(z + 1) * nchunks_all / nsplit);
   const int nchunks = c1 - c0;
   const int nk = nchunks * SUBS;
+  const int nunits = nk / C::RAW_SUBS;  // raw slots' worth of k
   // piece p (token columns t0 + 64 p ..) holds a token; with a split, CTA z
   // (its rank in the cluster) writes pieces 2 z and 2 z + 1
   auto live = [&](int p) { return t0 + p * PIECE < T; };
@@ -365,30 +398,39 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmW);
       if (C::NM == 2) tma_prefetch_desc(&tmWu);
+      // x of box b of raw slot u (16-bit elements): the raw row bytes of block
+      // formats, the k index itself for F16
+      auto raw_x = [&](int u, int b) {
+        return C::F16W ? c0 * CHUNK + u * C::RAW_K + b * BK : (c0 + u) * (C::RAW_ROW / 2);
+      };
       // an L2 prefetch changes no data, so it may run before the wait
-      for (int c = 0; c < PF && c < nchunks; ++c)
+      for (int u = 0; u < PF && u < nunits; ++u)
         for (int m = 0; m < C::NM; ++m)
-          tma_prefetch_l2_2d(m ? (const void*)&tmWu : (const void*)&tmW, (c0 + c) * (C::RAW_ROW / 2), m0);
+          for (int b = 0; b < C::RAW_LOADS; ++b)
+            tma_prefetch_l2_2d(m ? (const void*)&tmWu : (const void*)&tmW, raw_x(u, b), m0);
       if ((early & 15) == kEarlyNone) grid_dependency_wait();
       int last_issued[C::S_RAW];
       for (int i = 0; i < C::S_RAW; ++i) last_issued[i] = -1;
       bool ok = true;
-      for (int c = 0; c < nchunks && ok; ++c) {
+      for (int u = 0; u < nunits && ok; ++u) {
         for (int m = 0; m < C::NM && ok; ++m) {
-          const int j = c * C::NM + m;
+          const int j = u * C::NM + m;
           const int slot = j % C::S_RAW;
           ok = mbar_wait(&rawEmpty[slot], ((j / C::S_RAW) & 1) ^ 1, abort_flag, status);
           if (!ok) break;
           const void* map = m ? (const void*)&tmWu : (const void*)&tmW;
           mbar_arrive_expect_tx(&rawFull[slot], C::RAW_BYTES);
-          tma_load_2d(sRaw + slot * C::RAW_BYTES, map, (c0 + c) * (C::RAW_ROW / 2), m0, &rawFull[slot]);
-          if (c + PF < nchunks) tma_prefetch_l2_2d(map, (c0 + c + PF) * (C::RAW_ROW / 2), m0);
+          for (int b = 0; b < C::RAW_LOADS; ++b)
+            tma_load_2d(sRaw + slot * C::RAW_BYTES + b * (C::RAW_BYTES / C::RAW_LOADS), map, raw_x(u, b), m0,
+                        &rawFull[slot]);
+          if (u + PF < nunits)
+            for (int b = 0; b < C::RAW_LOADS; ++b) tma_prefetch_l2_2d(map, raw_x(u + PF, b), m0);
           last_issued[slot] = j;
         }
       }
       if (ok && nsplit == 2) {
         // every raw slot read for the last time: the partner may send into the ring
-        const int total = nchunks * C::NM;
+        const int total = nunits * C::NM;
         for (int v = total; v < total + C::S_RAW && ok; ++v)
           ok = mbar_wait(&rawEmpty[v % C::S_RAW], ((v / C::S_RAW) & 1) ^ 1, abort_flag, status);
         cluster_wait();
@@ -523,22 +565,30 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
       if (lane == 0) mbar_arrive(&chunkEmpty[cs & 1]);
       return okf;
     };
-    for (int c = 0; c < nchunks && ok; ++c) {
-      if (XS && par == 0 && c >= 2) ok = fold(c - 2);
+    for (int c = 0; c < nunits && ok; ++c) {
+      if (XS && par == 0 && c >= 2) ok = fold(c - 2);  // exact leg: a raw slot is a chunk
       if (!ok) break;
       const int j = c * C::NM + g;
       const int slot = j % C::S_RAW;
       ok = __all_sync(0xffffffffu, mbar_wait(&rawFull[slot], (j / C::S_RAW) & 1, abort_flag, status));
       if (!ok) break;
-      const uint32_t* raw_row = reinterpret_cast<const uint32_t*>(sRaw + slot * C::RAW_BYTES + r * C::RAW_ROW);
-      for (int s = par; s < SUBS; s += C::DQ) {
-        const int i = c * SUBS + s;
+      const uint8_t* raw_slot = sRaw + slot * C::RAW_BYTES;
+      const uint32_t* raw_row = reinterpret_cast<const uint32_t*>(raw_slot + r * C::RAW_ROW);
+      for (int s = par; s < C::RAW_SUBS; s += C::DQ) {
+        const int i = c * C::RAW_SUBS + s;
         const int st = i % C::S;
         uint32_t w[2 * C::BB / 4], a[32], a2[XS ? 32 : 1];
+        if constexpr (C::F16W) {
+          f16_row_stage(raw_slot + s * (C::RAW_BYTES / C::RAW_LOADS), r, w);
+        } else {
 #pragma unroll
-        for (int v = 0; v < 2 * C::BB / 4; ++v) w[v] = raw_row[s * (2 * C::BB / 4) + v];
+          for (int v = 0; v < 2 * C::BB / 4; ++v) w[v] = raw_row[s * (2 * C::BB / 4) + v];
+        }
         if constexpr (XS)
           dequant_row_stage_xs<QT>(w, sw, a, a2);  // overlaps the wait below
+        else if constexpr (C::F16W)
+#pragma unroll
+          for (int v = 0; v < 32; ++v) a[v] = w[v];  // already the fp16 operand
         else
           dequant_row_stage<QT>(w, a);
         ok = __all_sync(0xffffffffu, mbar_wait(&empty[st], ((i / C::S) & 1) ^ 1, abort_flag, status));
@@ -761,12 +811,13 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
   if (!fn) return -1;
   CUtensorMap mW, mWu;
   const uint64_t row_bytes = (uint64_t)(k / 32) * C::BB;
-  if (!make_map_2d(fn, &mW, CU_TENSOR_MAP_DATA_TYPE_UINT16, W, row_bytes / 2, (uint64_t)n, row_bytes,
-                   C::RAW_ROW / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE, msg, msg_len))
+  const CUtensorMapSwizzle wswz = C::F16W ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (!make_map_2d(fn, &mW, CU_TENSOR_MAP_DATA_TYPE_UINT16, W, row_bytes / 2, (uint64_t)n, row_bytes, C::RAW_BOX,
+                   BM, wswz, msg, msg_len))
     return -1;
   if (C::NM == 2) {
-    if (!make_map_2d(fn, &mWu, CU_TENSOR_MAP_DATA_TYPE_UINT16, Wu, row_bytes / 2, (uint64_t)n, row_bytes,
-                     C::RAW_ROW / 2, BM, CU_TENSOR_MAP_SWIZZLE_NONE, msg, msg_len))
+    if (!make_map_2d(fn, &mWu, CU_TENSOR_MAP_DATA_TYPE_UINT16, Wu, row_bytes / 2, (uint64_t)n, row_bytes, C::RAW_BOX,
+                     BM, wswz, msg, msg_len))
       return -1;
   } else {
     mWu = mW;
@@ -833,7 +884,10 @@ template <int QT>
 int launch_q(const GemmPlan& pl, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y,
              int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int w) {
   if (Wu) return launch_cfg<QT, kEpiSwiGLU, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w);
-  if (pl.bn == 256) {
+  if constexpr (QT == kF16) {
+    // an F16 raw slot is four times a Q4_0 one: 256-token tiles do not fit
+    (void)pl;
+  } else if (pl.bn == 256) {
     if (R) return launch_cfg<QT, kEpiResidual, 256>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, pl.nsplit, w);
     return launch_cfg<QT, kEpiPlain, 256>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, pl.nsplit, w);
   }
@@ -862,6 +916,33 @@ __global__ void row_exp_kernel(const uint8_t* __restrict__ W, int n, int nblk, i
   if (lane == 0) {
     int e = 0;
     if (m > 0.f) e = 14 - ((int)((__float_as_uint(m * qmax) >> 23) & 0xFFu) - 127);
+    erow[row] = e;
+  }
+}
+
+// F16: the same exponent from the row's largest |w| (qmax = 1): every w * 2^e
+// is again an fp16 value while it stays above 2^-14, so W2 is zero there.
+// One warp per row, 16-byte loads (k % 256 == 0); the largest magnitude is
+// the largest of the bit patterns with the sign cleared (finite halves).
+__global__ void row_exp_f16_kernel(const uint16_t* __restrict__ W, int n, int k, int* __restrict__ erow) {
+  const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= n) return;
+  const uint4* base = reinterpret_cast<const uint4*>(W + (size_t)row * k);
+  uint32_t m = 0;
+  for (int i = lane; i < k / 8; i += 32) {
+    const uint4 v = base[i];
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) m = max(m, max(w4[q] & 0x7FFFu, (w4[q] >> 16) & 0x7FFFu));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) {
+    int e = 0;
+    if (m > 0u) {
+      const float f = __half2float(__ushort_as_half((unsigned short)m));
+      e = 14 - ((int)((__float_as_uint(f) >> 23) & 0xFFu) - 127);
+    }
     erow[row] = e;
   }
 }
@@ -961,18 +1042,24 @@ int launch_gemm_xs(int qtype, const void* W, const void* Wu, int n, int k, const
   uint16_t* X2 = reinterpret_cast<uint16_t*>(base + xb);
   int* etok = reinterpret_cast<int*>(base + 2 * xb);
   int* erow = reinterpret_cast<int*>(base + 2 * xb + (((size_t)T * 4 + 255) & ~(size_t)255));
-  const int bb = qtype == kQ4_0 ? 18 : 34;
+  const int bb = block_bytes(qtype);
   const float qmax = qtype == kQ4_0 ? 8.f : 128.f;
   // plain stream order: the splits start once everything before is complete
   const unsigned rblocks = (unsigned)((n + 7) / 8);
-  row_exp_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(W), n, k / 32, bb, qmax, erow);
-  if (Wu) row_exp_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(Wu), n, k / 32, bb, qmax, erow + n);
+  if (qtype == kF16) {
+    row_exp_f16_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint16_t*>(W), n, k, erow);
+    if (Wu) row_exp_f16_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint16_t*>(Wu), n, k, erow + n);
+  } else {
+    row_exp_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(W), n, k / 32, bb, qmax, erow);
+    if (Wu) row_exp_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(Wu), n, k / 32, bb, qmax, erow + n);
+  }
   x_split_kernel<<<(unsigned)T, 256, 0, s>>>(X, k, X1, X2, etok);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {
     snprintf(msg, msg_len, "exact-leg splits: %s", cudaGetErrorString(e));
     return -1;
   }
+  if (qtype == kF16) return launch_xs<kF16>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
   return qtype == kQ4_0 ? launch_xs<kQ4_0>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len)
                         : launch_xs<kQ8_0>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
 }
@@ -1020,6 +1107,7 @@ int launch_gemm_tc(const GemmPlan& pl, int qtype, const void* W, const void* Wu,
                    int T, float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg,
                    size_t msg_len, int early) {
   const int w = early;
+  if (qtype == kF16) return launch_q<kF16>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w);
   return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w)
                         : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w);
 }

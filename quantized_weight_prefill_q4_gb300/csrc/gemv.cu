@@ -1,4 +1,4 @@
-// Small-T GEMV over Q4_0 / Q8_0 blocks, exact fp32 arithmetic.
+// Small-T GEMV over Q4_0 / Q8_0 blocks or F16 weights, exact fp32 arithmetic.
 //
 // Y[t][i] = sum_j X[t][j] * d_{i,j/32} * q'_{i,j} (+ R[t][i]) for T <= 16 token
 // rows, or silu(g) * u for a gate/up pair. The single-token GEMVs of
@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const uint8_t* __rest
                                                            const float* __restrict__ X, int T,
                                                            float* Y, int ldy,
                                                            const float* R) {
-  constexpr int BB = QT == kQ4_0 ? 18 : 34;
+  constexpr int BB = QT == kQ4_0 ? 18 : (QT == kQ8_0 ? 34 : 64);
   constexpr int SEG = 32 * BB;
   constexpr int NM = SWI ? 2 : 1;
   __shared__ __align__(16) uint8_t stage[kWarps][NM * RW][SEG];
@@ -94,14 +94,18 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const uint8_t* __rest
 #pragma unroll
           for (int r = 0; r < RW; ++r) {
             const uint8_t* blk = stage[warp][m * RW + r] + lane * BB;
-            const uint16_t db = *reinterpret_cast<const uint16_t*>(blk);
-            dsc[m][r] = __half2float(__ushort_as_half(db));
+            if constexpr (QT == kF16) {
+              dsc[m][r] = 1.f;  // the elements are the weights
+            } else {
+              const uint16_t db = *reinterpret_cast<const uint16_t*>(blk);
+              dsc[m][r] = __half2float(__ushort_as_half(db));
+            }
 #pragma unroll
             for (int t = 0; t < TMAX; ++t) part[m][r][t] = 0.f;
           }
         // Q4_0: half h covers payload bytes 8h..8h+7, i.e. elements 8h..8h+7
         // (low nibbles) and 16+8h..16+8h+7 (high nibbles).
-        // Q8_0: quarter h covers elements 8h..8h+7.
+        // Q8_0 and F16: quarter h covers elements 8h..8h+7.
         constexpr int NPART = QT == kQ4_0 ? 2 : 4;
         constexpr int NE = QT == kQ4_0 ? 16 : 8;  // elements per part
 #pragma unroll
@@ -111,8 +115,15 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const uint8_t* __rest
           for (int m = 0; m < NM; ++m)
 #pragma unroll
             for (int r = 0; r < RW; ++r) {
-              const uint8_t* pay = stage[warp][m * RW + r] + lane * BB + 2;
-              if constexpr (QT == kQ4_0) {
+              const uint8_t* pay = stage[warp][m * RW + r] + lane * BB + (QT == kF16 ? 0 : 2);
+              if constexpr (QT == kF16) {
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(pay + 16 * h + 2 * e));
+                  wq[m][r][e] = f.x;
+                  wq[m][r][e + 1] = f.y;
+                }
+              } else if constexpr (QT == kQ4_0) {
 #pragma unroll
                 for (int e = 0; e < 8; e += 2) {
                   const uint32_t two = *reinterpret_cast<const uint16_t*>(pay + 8 * h + e);
@@ -232,6 +243,9 @@ cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, 
   if (gemv_i8_fits(qtype, n, k, T, swi)) return launch_gemv_i8(qtype, W, Wu, n, k, X, Y, R, status, s);
   if (gemv_rows_fits(qtype, n, k, T, swi)) return launch_gemv_rows(qtype, W, Wu, n, k, X, T, Y, R, status, s);
   if (gemv_bulk_fits(qtype, k, T, swi)) return launch_gemv_bulk(qtype, W, Wu, n, k, X, T, Y, ldy, R, status, s);
+  if (qtype == kF16)
+    return swi ? launch_q<kF16, true>(W, Wu, n, k, X, T, Y, ldy, R, s)
+               : launch_q<kF16, false>(W, Wu, n, k, X, T, Y, ldy, R, s);
   if (qtype == kQ4_0)
     return swi ? launch_q<kQ4_0, true>(W, Wu, n, k, X, T, Y, ldy, R, s)
                : launch_q<kQ4_0, false>(W, Wu, n, k, X, T, Y, ldy, R, s);

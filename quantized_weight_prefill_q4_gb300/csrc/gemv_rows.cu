@@ -239,10 +239,10 @@ size_t gemv_rows_smem(int qtype, int k, int T) {
 }
 
 bool gemv_rows_fits(int qtype, int n, int k, int T, bool swiglu) {
-  // one token; a row's warps within the consumer warps; whole rows in a
+  // block formats, one token; a row's warps within the consumer warps; whole rows in a
   // stage, each starting on a 16-byte boundary (k % 256 == 0); at most
   // RMAXROWS rows a CTA
-  if (T != 1 || k % 256 != 0 || (k / 64 + 63) / 64 > RNCW) return false;
+  if (qtype == kF16 || T != 1 || k % 256 != 0 || (k / 64 + 63) / 64 > RNCW) return false;
   if ((n + device_sms() - 1) / device_sms() > RMAXROWS) return false;
   return rows_per_stage(qtype, k, swiglu) >= 1 && gemv_rows_smem(qtype, k, T) <= 232448;
 }

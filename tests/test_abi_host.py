@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(q):
 
 def test_header_constants_match_binding(q):
     text = open(HEADER).read()
-    for name in ["APR_Q4_0", "APR_Q8_0", "APR_LEG_F16", "APR_LEG_EXACT_F32", "APR_PATH_AUTO", "APR_PATH_GEMV",
+    for name in ["APR_F16", "APR_Q4_0", "APR_Q8_0", "APR_LEG_F16", "APR_LEG_EXACT_F32", "APR_PATH_AUTO", "APR_PATH_GEMV",
                  "APR_PATH_GEMM", "APR_OK", "APR_E_INVAL", "APR_E_QTYPE", "APR_E_ALIGN", "APR_E_ALIAS",
                  "APR_E_DEVICE", "APR_E_LAUNCH", "APR_E_TIMEOUT", "APR_E_NOMEM"]:
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
@@ -74,6 +74,11 @@ def call(q, *args):
     ((2, A, 64, 64, 2 * A, 8, 2 * A + 16, None, None), -4, "X"),
     ((2, A, 64, 64, 2 * A, 8, A + 32, None, None), -4, "W"),
     ((2, A, 64, 64, 2 * A, 8, 3 * A, 3 * A + 16, None), -4, "residual"),
+    ((0, A, 64, 64, 2 * A, 8, 3 * A, None, None), -2, "qtype"),
+    ((3, A, 64, 64, 2 * A, 8, 3 * A, None, None), -2, "qtype"),
+    ((1, A, 64, 48, 2 * A, 8, 3 * A, None, None), -1, "k"),
+    # an F16 weight spans 2 bytes a weight: 64 x 64 -> 8192 bytes from A
+    ((1, A, 64, 64, 2 * A, 8, A + 8192 - 16, None, None), -4, "W"),
     ((2, A, (1 << 24) + 1, 64, 2 * A, 8, 3 * A, None, None), -1, "limits"),
     ((2, A, 64, (1 << 20) + 32, 2 * A, 8, 3 * A, None, None), -1, "limits"),
 ])
@@ -110,6 +115,8 @@ def test_swiglu_and_gemv_specific_errors(q):
     assert lib.apr_dequant(3, A, 4, 64, 2 * A, None) == -2
     assert lib.apr_dequant(2, A, 4, 48, 2 * A, None) == -1
     assert lib.apr_dequant(2, A, 4, 64, A + 16, None) == -4
+    assert lib.apr_dequant(1, A + 1, 4, 64, 2 * A, None) == -3          # F16 needs 2-byte alignment
+    assert lib.apr_dequant(1, A, 4, 64, A + 4 * 64 * 2 - 4, None) == -4  # F16: 512 bytes of W
 
 
 def test_valid_call_without_gpu_reports_device(q):
@@ -120,6 +127,9 @@ def test_valid_call_without_gpu_reports_device(q):
     # Y == residual exactly is allowed (accumulate form)
     assert call(q, 2, A, 64, 64, 2 * A, 8, 3 * A, 3 * A, None) == -5
     assert "device" in q.apr_last_error()
+    # F16 passes the checks too; a Q4_0 weight of this shape ends before Y
+    assert call(q, 1, A, 64, 64, 2 * A, 8, 3 * A, None, None) == -5
+    assert call(q, 2, A, 64, 64, 2 * A, 8, A + 8192 - 16, None, None) == -5
     assert q.library().apr_stream_status(None) == -5
 
 
