@@ -359,13 +359,27 @@ def run_ours(args):
         return
 
     if args.only == "kernel":
+        qt = args.kernel_qtype
+        Wk = [s["W"] for s in sets]
+        if qt != QTYPE:
+            w = synth.quantize(qt, synth.weight_f32(N, K, 0))
+            Wk = [torch.from_numpy(w).to(dev) for _ in sets]
         for s in sets:
             q.apr_convert_f32_to_f16(s["X"], T * K, s["X16"], stream=stream)
         for i in range(args.warmup + args.steps):
             s = sets[i % SETS]
-            q.apr_qgemm_f16_in(QTYPE, s["W"], N, K, s["X16"], T, s["Y"], s["R"], stream=stream)
+            q.apr_qgemm_f16_in(qt, Wk[i % SETS], N, K, s["X16"], T, s["Y"], s["R"], stream=stream)
         q.apr_stream_status(stream)
-        print(json.dumps({"only": "kernel", "launches": args.warmup + args.steps}), flush=True)
+        print(json.dumps({"only": "kernel", "qtype": qt, "launches": args.warmup + args.steps}), flush=True)
+        return
+
+    if args.only == "exact":
+        for i in range(args.warmup + args.steps):
+            s = sets[i % SETS]
+            q.apr_qgemm_ex(QTYPE, s["W"], N, K, s["X"], T, s["Y"], residual=s["R"], leg=q.APR_LEG_EXACT_F32,
+                           path=q.APR_PATH_GEMM, stream=stream)
+        q.apr_stream_status(stream)
+        print(json.dumps({"only": "exact", "launches": args.warmup + args.steps}), flush=True)
         return
 
     for i in range(max(args.warmup, 3)):
@@ -569,7 +583,7 @@ def projection_rate(q, dev, stream, peak_tf, peak_gbs, *, qtype, n, k, T, residu
     2 T n k (x2 for gate/up), bytes = the quantized weight(s) + X + Y (+ R)."""
     import torch
 
-    bb = 18 if qtype == 2 else 34
+    bb = {1: 64, 2: 18, 8: 34}[qtype]  # bytes per 32 weights (F16, Q4_0, Q8_0)
     wbytes = n * (k // 32) * bb * (2 if gate_up else 1)
     byts = wbytes + 4 * T * k + 4 * T * n * (2 if residual else 1)
     nsets = int(min(16, max(2, -(-2.5 * L2_BYTES // byts))))
@@ -612,10 +626,12 @@ def every_workload(q, dev, stream, peak_tf, peak_gbs):
       GEMMs at 24 and 32;
     * a 9B-class layer's projections (qkv 6144 x 4096, out 4096 x 4096 + R,
       gate/up 12288 x 4096, down 4096 x 12288 + R, Q4_0) at 512 and 2048 rows
-      on the fp16 leg and the exact-fp32 leg."""
+      on the fp16 leg and the exact-fp32 leg;
+    * F16 weights: 4096 x 4096 + R at 512 tokens on both legs, gate/up 12288 x
+      4096 at 512 tokens, and the GEMV at T = 1 and 4."""
     import torch
 
-    Q4, Q8 = 2, 8
+    F16, Q4, Q8 = 1, 2, 8
     P = lambda **kw: projection_rate(q, dev, stream, peak_tf, peak_gbs, **kw)  # noqa: E731
     out = {}
     out["q8_0_n256_k512_t16"] = {"auto (GEMV)": P(qtype=Q8, n=256, k=512, T=16),
@@ -649,6 +665,13 @@ def every_workload(q, dev, stream, peak_tf, peak_gbs):
                 "down_n4096_k12288_res": P(qtype=Q4, n=4096, k=12288, T=T, residual=True, leg=leg, seed=13),
             }
     out["layer_9b_q4_0"] = layer
+    out["f16"] = {
+        "n4096_k4096_t512_res": P(qtype=F16, n=4096, k=4096, T=512, residual=True),
+        "n4096_k4096_t512_res_exact": P(qtype=F16, n=4096, k=4096, T=512, residual=True, leg=1),
+        "swiglu_n12288_k4096_t512": P(qtype=F16, n=12288, k=4096, T=512, gate_up=True),
+        "gemv_n4096_k4096_t1": P(qtype=F16, n=4096, k=4096, T=1),
+        "gemv_n4096_k4096_t4": P(qtype=F16, n=4096, k=4096, T=4),
+    }
     torch.cuda.empty_cache()
     return out
 
@@ -821,10 +844,13 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload fields (every configuration)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--only", choices=["all", "step", "kernel", "gemv", "attention"], default="all",
-                    help="step: only the timed apr_qgemm steps; kernel: only the GEMM kernel on fp16 activations; "
+    ap.add_argument("--only", choices=["all", "step", "kernel", "exact", "gemv", "attention"], default="all",
+                    help="step: only the timed apr_qgemm steps; kernel: only the GEMM kernel on fp16 activations "
+                         "(--kernel-qtype weights); exact: only the exact-fp32 leg's GEMM call on the same problem; "
                          "gemv: only the T = 1 GEMV; attention: only the prefill attention (16 query heads, 4 KV "
                          "heads, --attn-tokens rows at position 0) (small, bounded runs for profilers)")
+    ap.add_argument("--kernel-qtype", type=int, default=2, choices=[1, 2, 8],
+                    help="weight type of the --only kernel run (GGUF id: 1 F16, 2 Q4_0, 8 Q8_0)")
     ap.add_argument("--attn-tokens", type=int, default=2048, help="query rows of the --only attention run")
     ap.add_argument("--gemv-tokens", type=int, default=1, help="tokens of the --only gemv run (1..16)")
     ap.add_argument("--clocks-dir", default=None, help="where the raw nvidia-smi clock samples are written")
