@@ -119,16 +119,18 @@ enum {
 };
 
 /*
- * The T rule, fixed and measured on GB300 (Q4_0, 4096 x 4096 and 12288 x 4096
- * weights): with APR_PATH_AUTO, 1 <= T <= APR_AUTO_GEMV_MAX_T runs the small-T
- * GEMV (exact fp32 arithmetic whatever the leg), larger T runs the GEMM of
- * the call's leg. At T = 4 the GEMV takes 15-26 us against 32-68 us for the
- * tensor-core GEMM; from T = 8 the fp16-leg GEMM is faster (19 against 32 us,
- * 57 against 80 us), because the CUDA-core GEMV's work grows with T.
+ * The T rule, fixed and measured on GB300 (Q4_0 and Q8_0, 4096 x 4096 and
+ * 12288 x 4096 weights, each call with its fp32 X): with APR_PATH_AUTO,
+ * 1 <= T <= APR_AUTO_GEMV_MAX_T runs the small-T GEMV (exact fp32 arithmetic
+ * whatever the leg), larger T runs the GEMM of the call's leg. The fp16-leg
+ * GEMM call costs the same at every T up to its 256-token tile (15.6 us at
+ * 4096 x 4096, 23.7 us at 12288 x 4096, Q4_0); the GEMV costs 5.6, 10.0, 14.6
+ * and 15.0 us at T = 1 to 4 and 22.0 us at T = 5 (4096 x 4096), 11.3 to 26.3 us
+ * at T = 1 to 4 (12288 x 4096), because its FFMA work grows with T.
  * APR_GEMV_MAX_T (apr_gemv_max_T()) is the largest T the GEMV path itself
  * takes (APR_PATH_GEMV, apr_qgemv).
  */
-#define APR_AUTO_GEMV_MAX_T 7
+#define APR_AUTO_GEMV_MAX_T 4
 #define APR_GEMV_MAX_T 16
 int apr_gemv_max_T(void);
 
@@ -163,11 +165,12 @@ int apr_qgemm_gate_up_swiglu(int qtype, const void* Wg, const void* Wu, int n, i
  * oxibonsai-kernels, used for the last-token lm_head in
  * try_cuda_prefill_q_std). For T <= 8 weight rows stream by bulk copies into
  * T fp32 accumulators (tensor cores for T = 3, 4 with block formats; F16
- * weights always on the CUDA cores); for 9 <= T <= 16 (k % 256
- * == 0) the exact leg's tensor-core GEMM runs instead (50 us against 200 to
- * 700 us for the CUDA-core kernels at 4096 x 4096 and 12288 x 4096, T = 12
- * and 16). T > APR_GEMV_MAX_T gives APR_E_INVAL. The weights are read early
- * (see stream order above).
+ * weights always on the CUDA cores); for 9 <= T <= 16, and for smaller T
+ * where no streaming kernel takes the shape (the X table of a long row does
+ * not fit shared memory), the exact leg's tensor-core GEMM runs instead when
+ * k % 256 == 0 (49-57 us at 4096 x 4096 and 12288 x 4096, against 50 to 700
+ * us for the CUDA-core kernels at T = 12 and 16). T > APR_GEMV_MAX_T gives
+ * APR_E_INVAL. The weights are read early (see stream order above).
  */
 int apr_qgemv(int qtype, const void* W, int n, int k, const float* X, int T,
               float* Y, const float* residual, apr_stream_t stream);

@@ -33,7 +33,7 @@ APR_E_LAUNCH = -6
 APR_E_TIMEOUT = -7
 APR_E_NOMEM = -8
 APR_GEMV_MAX_T = 16
-APR_AUTO_GEMV_MAX_T = 7
+APR_AUTO_GEMV_MAX_T = 4
 APR_NOALLOC_MAX_TK = 8 * 1024 * 1024
 APR_FFN_CHUNK_ROWS = 2048
 

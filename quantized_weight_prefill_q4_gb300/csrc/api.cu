@@ -7,6 +7,7 @@
 // batch returns success without work).
 
 #include <cstdarg>
+#include <algorithm>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -179,6 +180,12 @@ int ldy_of(const Problem& p) { return p.ldy > 0 ? p.ldy : p.n; }
 
 bool known_qtype(int q) { return q == APR_Q4_0 || q == APR_Q8_0 || q == APR_F16; }
 
+// a streaming GEMV kernel (integer-dot, whole-row, bulk or tensor-core) takes the shape
+bool gemv_streams(int qtype, int n, int k, int T, bool swiglu) {
+  return gemv_i8_fits(qtype, n, k, T, swiglu) || gemv_rows_fits(qtype, n, k, T, swiglu) ||
+         gemv_bulk_fits(qtype, k, T, swiglu) || (!swiglu && qtype != APR_F16 && gemv_tc_takes(n, k, T, false));
+}
+
 // Host-side checks; returns APR_OK, an error, or 1 for "nothing to do".
 int check(const Problem& p, size_t x_elem_bytes = 4) {
   if (!known_qtype(p.qtype)) return fail(APR_E_QTYPE, "unsupported qtype %d", p.qtype);
@@ -227,10 +234,13 @@ int run(const Problem& p) {
 
   int path = p.path;
   if (path == APR_PATH_AUTO) path = p.T <= APR_AUTO_GEMV_MAX_T ? APR_PATH_GEMV : APR_PATH_GEMM;
-  // from T = 9 the exact leg's tensor-core GEMM beats the CUDA-core GEMVs
-  // (their FFMA work grows with T): the GEMV path takes it there
+  // From T = 9, and wherever no streaming GEMV kernel takes the shape (the
+  // staged fallback is several times slower), the exact leg's tensor-core
+  // GEMM beats the CUDA-core GEMVs (their FFMA work grows with T): the GEMV
+  // path takes it there. F16 weights stay on the GEMV kernels below T = 9.
   int leg = p.leg;
-  if (path == APR_PATH_GEMV && p.T > 8 && p.k % 256 == 0) {
+  if (path == APR_PATH_GEMV && p.k % 256 == 0 &&
+      (p.T > 8 || (p.qtype != APR_F16 && !gemv_streams(p.qtype, p.n, p.k, p.T, p.Wu != nullptr)))) {
     path = APR_PATH_GEMM;
     leg = APR_LEG_EXACT_F32;
   }
@@ -282,17 +292,17 @@ int run(const Problem& p) {
     return launched(launch_swiglu_rows(G, U, p.T, p.n, p.Y, ldy_of(p), p.s), "swiglu_rows");
   }
 
-  // the stream's scratch holds the fp16 copy of X
+  // the stream's scratch holds the fp16 copy of X (at least kMinXRows rows)
   const GemmPlan plan = plan_gemm_tc(p.n, p.k, p.T, p.Wu != nullptr);
   const size_t count = (size_t)p.T * (size_t)p.k;
   void* x16 = nullptr;
-  rc = stream_scratch(st->dev, p.s, kScratchX16, count * 2, &x16);
+  rc = stream_scratch(st->dev, p.s, kScratchX16, (size_t)padded_x_rows(p.T) * p.k * 2, &x16);
   if (rc != APR_OK) return rc;
   rc = launched(launch_x_to_f16(p.X, static_cast<uint16_t*>(x16), count, p.s), "x_to_f16");
   if (rc != APR_OK) return rc;
   char msg[256] = "";
   if (launch_gemm_tc(plan, p.qtype, p.W, p.Wu, p.n, p.k, static_cast<const uint16_t*>(x16), p.T, p.Y, ldy_of(p), p.R,
-                     st->status, p.s, msg, sizeof msg, kEarlyWR) != 0)
+                     st->status, p.s, msg, sizeof msg, kEarlyWR, padded_x_rows(p.T)) != 0)
     return fail(APR_E_LAUNCH, "%s", msg);
   return APR_OK;
 }
@@ -327,9 +337,12 @@ int run_ffn(const apr_ffn_args& a) {
   if (rc != APR_OK) return rc;
   const cudaStream_t s = (cudaStream_t)a.stream;
   const int chunk = a.T < APR_FFN_CHUNK_ROWS ? a.T : APR_FFN_CHUNK_ROWS;
-  const size_t h_bytes = align256((size_t)chunk * a.hidden * 4), act_bytes = align256((size_t)chunk * a.inter * 4);
+  // h: the normed rows, fp32, or fp16 padded to kMinXRows rows
+  const size_t h_bytes = align256(std::max((size_t)chunk * a.hidden * 4, (size_t)padded_x_rows(chunk) * a.hidden * 2));
+  const size_t act_bytes = align256((size_t)chunk * a.inter * 4);
   void* scratch = nullptr;
-  rc = stream_scratch(st->dev, s, kScratchFfn, h_bytes + act_bytes + (size_t)chunk * a.inter * 2, &scratch);
+  rc = stream_scratch(st->dev, s, kScratchFfn, h_bytes + act_bytes + (size_t)padded_x_rows(chunk) * a.inter * 2,
+                      &scratch);
   if (rc != APR_OK) return rc;
   uint8_t* base = static_cast<uint8_t*>(scratch);
   void* h = base;                                          // normed rows (fp16 or fp32)
@@ -345,13 +358,13 @@ int run_ffn(const apr_ffn_args& a) {
       char msg[256] = "";
       const GemmPlan pg = plan_gemm_tc(a.inter, a.hidden, rows, true);
       if (launch_gemm_tc(pg, a.qtype, a.Wg, a.Wu, a.inter, a.hidden, static_cast<const uint16_t*>(h), rows, act,
-                         a.inter, nullptr, st->status, s, msg, sizeof msg, kEarlyWR) != 0)
+                         a.inter, nullptr, st->status, s, msg, sizeof msg, kEarlyWR, padded_x_rows(rows)) != 0)
         return fail(APR_E_LAUNCH, "%s", msg);
       rc = launched(launch_x_to_f16(act, act16, (size_t)rows * a.inter, s), "x_to_f16");
       if (rc != APR_OK) return rc;
       const GemmPlan pd = plan_gemm_tc(a.hidden, a.inter, rows, false);
       if (launch_gemm_tc(pd, a.qtype, a.Wd, nullptr, a.hidden, a.inter, act16, rows, Xc, a.hidden, Xc, st->status, s,
-                         msg, sizeof msg, kEarlyWR) != 0)
+                         msg, sizeof msg, kEarlyWR, padded_x_rows(rows)) != 0)
         return fail(APR_E_LAUNCH, "%s", msg);
     } else {
       rc = run(Problem{a.qtype, a.leg, APR_PATH_AUTO, a.Wg, a.Wu, a.inter, a.hidden, rows,
@@ -383,7 +396,8 @@ int run_normed(const Problem& p, const float* w, float eps) {
   const bool tc = p.leg == APR_LEG_F16 && path == APR_PATH_GEMM && p.k % 256 == 0;
   const int chunk = p.T < APR_FFN_CHUNK_ROWS ? p.T : APR_FFN_CHUNK_ROWS;
   void* h = nullptr;
-  rc = stream_scratch(st->dev, p.s, kScratchNorm, (size_t)chunk * p.k * (tc ? 2 : 4), &h);
+  rc = stream_scratch(st->dev, p.s, kScratchNorm, tc ? (size_t)padded_x_rows(chunk) * p.k * 2 : (size_t)chunk * p.k * 4,
+                      &h);
   if (rc != APR_OK) return rc;
   const int ldy = ldy_of(p);
   for (int t0 = 0; t0 < p.T; t0 += chunk) {
@@ -397,7 +411,7 @@ int run_normed(const Problem& p, const float* w, float eps) {
       char msg[256] = "";
       const GemmPlan plan = plan_gemm_tc(p.n, p.k, rows, p.Wu != nullptr);
       if (launch_gemm_tc(plan, p.qtype, p.W, p.Wu, p.n, p.k, static_cast<const uint16_t*>(h), rows, Yc, ldy, Rc,
-                         st->status, p.s, msg, sizeof msg, kEarlyWR) != 0)
+                         st->status, p.s, msg, sizeof msg, kEarlyWR, padded_x_rows(rows)) != 0)
         return fail(APR_E_LAUNCH, "%s", msg);
     } else {
       rc = run(Problem{p.qtype, p.leg, path, p.W, p.Wu, p.n, p.k, rows, static_cast<const float*>(h), Rc, Yc, p.s,
@@ -455,7 +469,8 @@ int run_layer(const apr_layer_args& a) {
   const int chunk = a.chunk > 0 ? a.chunk : 512;
   const int rmax = a.T < chunk ? a.T : chunk;
   // the chunk's normed rows (fp32 at most), q and the attention output
-  const size_t h_bytes = align256((size_t)rmax * a.hidden * 4), q_bytes = align256((size_t)rmax * qd * 4);
+  const size_t h_bytes = align256(std::max((size_t)rmax * a.hidden * 4, (size_t)padded_x_rows(rmax) * a.hidden * 2));
+  const size_t q_bytes = align256((size_t)rmax * qd * 4);
   void* scratch = nullptr;
   rc = stream_scratch(st->dev, s, kScratchLayer, h_bytes + 2 * q_bytes, &scratch);
   if (rc != APR_OK) return rc;
@@ -488,7 +503,8 @@ int run_layer(const apr_layer_args& a) {
         char msg[256] = "";
         const GemmPlan plan = plan_gemm_tc(np[j], a.hidden, rows, false);
         if (launch_gemm_tc(plan, a.qtype, Wp[j], nullptr, np[j], a.hidden, static_cast<const uint16_t*>(h), rows,
-                           Yp[j], np[j], nullptr, st->status, s, msg, sizeof msg, j == 0 ? kEarlyWR : kEarlyW) != 0)
+                           Yp[j], np[j], nullptr, st->status, s, msg, sizeof msg, j == 0 ? kEarlyWR : kEarlyW,
+                           padded_x_rows(rows)) != 0)
           return fail(APR_E_LAUNCH, "%s", msg);
       } else {
         rc = run(Problem{a.qtype, a.leg, APR_PATH_AUTO, Wp[j], nullptr, np[j], a.hidden, rows,

@@ -805,7 +805,7 @@ __global__ void __launch_bounds__(256, 4) x_to_f16_kernel(const float* __restric
 template <int QT, int EPI, int BN, bool XS = false>
 int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y, int ldy,
                const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, int early,
-               const uint16_t* X16b = nullptr, const int* erow = nullptr, const int* etok = nullptr) {
+               int x_rows, const uint16_t* X16b = nullptr, const int* erow = nullptr, const int* etok = nullptr) {
   using C = Cfg<QT, EPI, BN, XS>;
   auto fn = encode_fn(msg, msg_len);
   if (!fn) return -1;
@@ -823,13 +823,14 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
     mWu = mW;
   }
   // B operand: fp16 X, 128-byte rows of a 64-column stage, swizzled
+  const uint64_t xr = (uint64_t)(x_rows > T ? x_rows : T);
   CUtensorMap mX;
-  if (!make_map_2d(fn, &mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X16, (uint64_t)k, (uint64_t)T, (uint64_t)k * 2, BK, BN,
+  if (!make_map_2d(fn, &mX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X16, (uint64_t)k, xr, (uint64_t)k * 2, BK, BN,
                    CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
     return -1;
   CUtensorMap mX2 = mX;
-  if (XS && !make_map_2d(fn, &mX2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X16b, (uint64_t)k, (uint64_t)T, (uint64_t)k * 2, BK,
-                         BN, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
+  if (XS && !make_map_2d(fn, &mX2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X16b, (uint64_t)k, xr, (uint64_t)k * 2, BK, BN,
+                         CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
     return -1;
   // the residual, [T] rows of n fp32 ldy apart, only for L2 prefetches of
   // 128-row x 64-token boxes: a row stride that is not a multiple of 16
@@ -882,17 +883,19 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
 
 template <int QT>
 int launch_q(const GemmPlan& pl, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y,
-             int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int w) {
-  if (Wu) return launch_cfg<QT, kEpiSwiGLU, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w);
+             int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int w, int xr) {
+  if (Wu) return launch_cfg<QT, kEpiSwiGLU, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w, xr);
   if constexpr (QT == kF16) {
     // an F16 raw slot is four times a Q4_0 one: 256-token tiles do not fit
     (void)pl;
   } else if (pl.bn == 256) {
-    if (R) return launch_cfg<QT, kEpiResidual, 256>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, pl.nsplit, w);
-    return launch_cfg<QT, kEpiPlain, 256>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, pl.nsplit, w);
+    if (R)
+      return launch_cfg<QT, kEpiResidual, 256>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, pl.nsplit, w,
+                                               xr);
+    return launch_cfg<QT, kEpiPlain, 256>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, pl.nsplit, w, xr);
   }
-  if (R) return launch_cfg<QT, kEpiResidual, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w);
-  return launch_cfg<QT, kEpiPlain, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w);
+  if (R) return launch_cfg<QT, kEpiResidual, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w, xr);
+  return launch_cfg<QT, kEpiPlain, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w, xr);
 }
 
 // ---------------------------------------------------------------- exact-leg splits
@@ -998,11 +1001,12 @@ int launch_xs(const void* W, const void* Wu, int n, int k, const uint16_t* X1, c
               const int* etok, int T, float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg,
               size_t msg_len) {
   (void)Wu;
+  const int xr = padded_x_rows(T);  // the split's scratch holds that many rows
   if (R)
     return launch_cfg<QT, kEpiResidual, 128, true>(W, Wu, n, k, X1, T, Y, ldy, R, status, s, msg, msg_len, 1, kEarlyW,
-                                                    X2, erow, etok);
-  return launch_cfg<QT, kEpiPlain, 128, true>(W, Wu, n, k, X1, T, Y, ldy, R, status, s, msg, msg_len, 1, kEarlyW, X2,
-                                               erow, etok);
+                                                    xr, X2, erow, etok);
+  return launch_cfg<QT, kEpiPlain, 128, true>(W, Wu, n, k, X1, T, Y, ldy, R, status, s, msg, msg_len, 1, kEarlyW, xr,
+                                               X2, erow, etok);
 }
 
 // y = silu(g) * u, silu(g) = g / (1 + e^-g), for T rows of n (rows of Y ldy
@@ -1030,13 +1034,13 @@ cudaError_t launch_swiglu_rows(const float* G, const float* U, int T, int n, flo
 }
 
 size_t gemm_xs_scratch_bytes(int n, int k, int T, bool swiglu) {
-  const size_t xb = ((size_t)T * k * 2 + 255) & ~(size_t)255;
+  const size_t xb = ((size_t)padded_x_rows(T) * k * 2 + 255) & ~(size_t)255;
   return 2 * xb + (((size_t)T * 4 + 255) & ~(size_t)255) + (size_t)(swiglu ? 2 : 1) * n * 4;
 }
 
 int launch_gemm_xs(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
                    const float* R, void* scratch, unsigned* status, cudaStream_t s, char* msg, size_t msg_len) {
-  const size_t xb = ((size_t)T * k * 2 + 255) & ~(size_t)255;
+  const size_t xb = ((size_t)padded_x_rows(T) * k * 2 + 255) & ~(size_t)255;
   uint8_t* base = static_cast<uint8_t*>(scratch);
   uint16_t* X1 = reinterpret_cast<uint16_t*>(base);
   uint16_t* X2 = reinterpret_cast<uint16_t*>(base + xb);
@@ -1105,11 +1109,11 @@ GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu) {
 
 int launch_gemm_tc(const GemmPlan& pl, int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16,
                    int T, float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg,
-                   size_t msg_len, int early) {
+                   size_t msg_len, int early, int x_rows) {
   const int w = early;
-  if (qtype == kF16) return launch_q<kF16>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w);
-  return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w)
-                        : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w);
+  if (qtype == kF16) return launch_q<kF16>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
+  return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows)
+                        : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
 }
 
 }  // namespace apr

@@ -28,13 +28,15 @@ constexpr int G = NCW * RW;           // rows per group
 constexpr int KC = 2048;              // columns per chunk: 32 lanes x one block pair
 constexpr int NTHREADS = 32 * (NCW + 1);
 
-template <int QT, bool SWI>
+// Ring depth: Q8_0 with eight tokens takes two stages, so that the ring and
+// the X table of k = 4096 fit shared memory.
+template <int QT, bool SWI, int TMAX>
 struct BCfg {
   static constexpr int NM = SWI ? 2 : 1;
   static constexpr int BB = QT == kQ4_0 ? 18 : 34;
   static constexpr int CB = KC / 32 * BB;            // bytes of one row's chunk
   static constexpr int STAGE = NM * G * CB;
-  static constexpr int NS = QT == kQ4_0 ? (SWI ? 3 : 4) : (SWI ? 2 : 3);
+  static constexpr int NS = QT == kQ4_0 ? (SWI ? 3 : 4) : (SWI || TMAX == 8 ? 2 : 3);
   static constexpr int RING = NS * STAGE;
 };
 
@@ -42,7 +44,7 @@ template <int QT, int TMAX, bool SWI>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemv_bulk_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ Wu, int n, int k,
                      const float* __restrict__ X, int T, float* Y, int ldy, const float* R, unsigned* status) {
-  using C = BCfg<QT, SWI>;
+  using C = BCfg<QT, SWI, TMAX>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, by pointer arithmetic on the shared array so that
   // the compiler keeps the shared address space (shared loads, not generic)
@@ -179,7 +181,7 @@ int g_num_sms[64] = {0};
 template <int QT, int TMAX, bool SWI>
 cudaError_t launch_t(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
                      const float* R, unsigned* status, cudaStream_t s) {
-  using C = BCfg<QT, SWI>;
+  using C = BCfg<QT, SWI, TMAX>;
   const size_t smem = gemv_bulk_smem(QT, k, T, SWI);
   auto kern = gemv_bulk_kernel<QT, TMAX, SWI>;
   static int attr_set[64] = {0};
@@ -211,14 +213,23 @@ cudaError_t launch_q(const void* W, const void* Wu, int n, int k, const float* X
   return launch_t<QT, 8, SWI>(W, Wu, n, k, X, T, Y, ldy, R, status, s);
 }
 
+template <int QT, int TMAX>
+size_t ring_bytes(bool swiglu) {
+  return swiglu ? BCfg<QT, true, TMAX>::RING : BCfg<QT, false, TMAX>::RING;
+}
+
+template <int QT>
+size_t ring_bytes_t(int T, bool swiglu) {  // the TMAX launch_q picks for T
+  if (T <= 1) return ring_bytes<QT, 1>(swiglu);
+  if (T <= 2) return ring_bytes<QT, 2>(swiglu);
+  if (T <= 4) return ring_bytes<QT, 4>(swiglu);
+  return ring_bytes<QT, 8>(swiglu);
+}
+
 }  // namespace
 
 size_t gemv_bulk_smem(int qtype, int k, int T, bool swiglu) {
-  size_t ring;
-  if (qtype == kQ4_0)
-    ring = swiglu ? BCfg<kQ4_0, true>::RING : BCfg<kQ4_0, false>::RING;
-  else
-    ring = swiglu ? BCfg<kQ8_0, true>::RING : BCfg<kQ8_0, false>::RING;
+  const size_t ring = qtype == kQ4_0 ? ring_bytes_t<kQ4_0>(T, swiglu) : ring_bytes_t<kQ8_0>(T, swiglu);
   const size_t xt = ((size_t)T * (k / 64) * XPAIR * 4 + 15) & ~(size_t)15;
   return 1024 + ring + xt + 2 * 8 * 4 + 16;
 }

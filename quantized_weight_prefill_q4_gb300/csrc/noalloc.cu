@@ -101,8 +101,10 @@ extern "C" int apr_qgemm_noalloc(int qtype, const void* W, int n, int k, const f
   if (e != cudaSuccess) return set_error(APR_E_LAUNCH, cudaGetErrorString(e));
   char msg[256] = "";
   const GemmPlan plan = plan_gemm_tc(n, k, T, false);
+  // the fixed array also covers kMinXRows rows of X when they fit
+  const int xr = (size_t)padded_x_rows(T) * (size_t)k <= kNoAllocScratchElems ? padded_x_rows(T) : T;
   if (launch_gemm_tc(plan, qtype, W, nullptr, n, k, st->scratch, T, Y, n, residual, st->status, s, msg, sizeof msg,
-                     kEarlyWR) != 0)
+                     kEarlyWR, xr) != 0)
     return set_error(APR_E_LAUNCH, msg);
   return APR_OK;
 }

@@ -43,7 +43,7 @@ def test_header_constants_match_binding(q):
         assert int(m.group(1)) == getattr(q, name), name
     assert q.library().apr_gemv_max_T() == q.APR_GEMV_MAX_T == 16
     m = re.search(r"#define APR_AUTO_GEMV_MAX_T (\d+)", text)
-    assert m and int(m.group(1)) == q.APR_AUTO_GEMV_MAX_T == 7
+    assert m and int(m.group(1)) == q.APR_AUTO_GEMV_MAX_T == 4
     m = re.search(r"#define APR_FFN_CHUNK_ROWS (\d+)", text)
     assert m and int(m.group(1)) == q.APR_FFN_CHUNK_ROWS
 

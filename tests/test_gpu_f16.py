@@ -226,15 +226,16 @@ def test_gemv(q, cls, n, k, T):
     _check_exact(W, n, k, X, R, Y.cpu().numpy())
 
 
-@pytest.mark.parametrize("T", [1, 3, 7])
-def test_auto_rule_small_T_and_gemv_gate_up(q, T):
+@pytest.mark.parametrize("T", [1, 3, 4, 7])
+def test_auto_rule_and_gemv_gate_up(q, T):
+    # AUTO: the exact GEMV up to APR_AUTO_GEMV_MAX_T tokens, the fp16-leg GEMM above
     n, k = 4096, 4096
     W, X, R = _synthetic(n, k, T, seed=T, residual=True)
     buf, Y = guarded(T, n)
     q.apr_qgemm(F16, dev(W), n, k, dev(X), T, Y, dev(R))
     q.apr_stream_status()
     check_guards(buf, T, n)
-    _check_exact(W, n, k, X, R, Y.cpu().numpy())
+    (_check_exact if T <= q.APR_AUTO_GEMV_MAX_T else _check_f16)(W, n, k, X, R, Y.cpu().numpy())
     Wu = synth.quantize_f16(synth.weight_f32(n, k, 100 + T))
     y = _call(q, W, n, k, X, T, leg=q.APR_LEG_EXACT_F32, path=q.APR_PATH_GEMV, Wu=Wu)
     assert_exact_leg(y, oracle.gate_up_swiglu_f64(F16, W, Wu, n, k, X))

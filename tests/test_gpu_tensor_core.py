@@ -154,9 +154,10 @@ def test_gemv_and_gemm_agree_for_small_T(q, qtype):
         assert_f16_leg(Ym.cpu().numpy(), Yv.cpu().numpy().astype(np.float64))
 
 
-@pytest.mark.parametrize("T", [8, 17])
+@pytest.mark.parametrize("T", [5, 8, 15, 17])
 def test_auto_rule_large_T_takes_the_fp16_gemm(q, T):
-    # T >= 8 is above the GEMV limit: the fp16 leg's error shows (it is not fp32-exact)
+    # T >= 5 is above the GEMV limit: the fp16 leg's error shows (it is not fp32-exact)
+    assert T > q.APR_AUTO_GEMV_MAX_T
     n, k = 256, 512
     c = synth.make_case(synth.Q8_0, n, k, T, seed=0)
     Y = torch.empty((T, n), device="cuda")
