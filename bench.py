@@ -615,8 +615,8 @@ def projection_rate(q, dev, stream, peak_tf, peak_gbs, *, qtype, n, k, T, residu
 def every_workload(q, dev, stream, peak_tf, peak_gbs):
     """Every seeded workload of the path, each through the public entry point
     (input sets rotating past L2, CUDA graph replay, CUDA events):
-    * the Q8_0 256 x 512 problem with 16 tokens (by the T rule the GEMV; also
-      forced onto the tensor-core GEMM);
+    * the Q8_0 256 x 512 problem with 16 tokens (by the T rule and forced onto
+      the tensor-core GEMM);
     * fused gate/up SwiGLU 12288 x 4096 then down 4096 x 12288 + residual, 512
       tokens, Q4_0 and Q8_0;
     * the small-T GEMV sweep: T in {1, 2, 4, 8, 16} over 4096 x 4096 and
@@ -634,7 +634,7 @@ def every_workload(q, dev, stream, peak_tf, peak_gbs):
     F16, Q4, Q8 = 1, 2, 8
     P = lambda **kw: projection_rate(q, dev, stream, peak_tf, peak_gbs, **kw)  # noqa: E731
     out = {}
-    out["q8_0_n256_k512_t16"] = {"auto (GEMV)": P(qtype=Q8, n=256, k=512, T=16),
+    out["q8_0_n256_k512_t16"] = {"auto (T rule: the GEMM)": P(qtype=Q8, n=256, k=512, T=16),
                                  "forced GEMM": P(qtype=Q8, n=256, k=512, T=16, path=2)}
     for qt, name in ((Q4, "q4_0"), (Q8, "q8_0")):
         out[f"swiglu_{name}_n12288_k4096_t512"] = P(qtype=qt, n=12288, k=4096, T=512, gate_up=True)

@@ -1,4 +1,5 @@
-// fp16-input tensor-core GEMM over Q4_0 / Q8_0 blocks, sm_103a (tcgen05 + TMA).
+// Tensor-core GEMM over Q4_0 / Q8_0 blocks and F16 weights, sm_103a (tcgen05 + TMA):
+// the fp16-input leg and, on the same skeleton, the exact-fp32 leg (XS below).
 //
 //   D[W rows][tokens] = dequant(W)[128 x k] . fp16(X)[BN x k]^T   (fp32 in TMEM)
 //   Y[t][i] = D[i][t]  (+ R[t][i])       or  silu(Dg[i][t]) * Du[i][t]
@@ -17,8 +18,10 @@
 // split over k, half of the k range of one 256-token tile. Warp roles:
 //   warp 0       TMA producer of raw weight chunks: 128 rows x 256 k (8 blocks
 //                per row: 144 B for Q4_0, 272 B for Q8_0, the smallest box whose
-//                width is a multiple of 16 bytes for both formats) into a ring
-//                of S_RAW slots, with L2 prefetches PF chunks ahead
+//                width is a multiple of 16 bytes for both formats; F16 rows as
+//                four 64-k boxes of [128 rows][128 B], 128-byte swizzled, half
+//                a chunk per slot for a gate/up pair) into a ring of S_RAW
+//                slots, with L2 prefetches PF slots ahead
 //   warp 1       TMEM allocator and MMA issuer: the whole warp runs the loop,
 //                one elected lane issues (four K = 16 MMAs per 64-k stage)
 //   warp 2       TMA producer of X tiles: BN tokens x 64 k of the fp16 copy of X,
@@ -27,8 +30,9 @@
 //   warp 3       idle
 //   warps 4..    dequant warpgroups: each thread owns one of the 128 rows (its
 //                TMEM lane), decodes 2 blocks (64 k) per stage from the raw slot
-//                and stores them as 32 columns of fp16 pairs into an A stage in
-//                TMEM; A and B stages advance together (S of them); with one
+//                (F16: copies its 128 bytes) and stores them as 32 columns of
+//                fp16 pairs into an A stage in TMEM; A and B stages advance
+//                together (S of them); with one
 //                weight, two warpgroups take alternate stages, with gate/up one
 //                warpgroup per weight. Then the same warps run the epilogue.
 // Epilogue: the tile's token columns go out in pieces of 64. A warpgroup reads
@@ -51,6 +55,8 @@
 // in split order, so the result does not depend on which CTA finishes first.
 // A cluster barrier at the end keeps both CTAs resident until neither touches
 // the other's shared memory.
+// Exact leg (XS): the pages' f32 leg (fp32 products, no reduced-precision
+// input) on the same skeleton; see the comment above Cfg.
 // Every mbarrier wait is bounded (2 s); a wait that gives up sets the device
 // status word and an abort flag in shared memory so that every role leaves its
 // loop, drains its own TMA copies and MMAs, and the CTA frees its TMEM.
