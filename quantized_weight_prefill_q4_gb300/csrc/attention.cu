@@ -66,24 +66,33 @@ constexpr int AD = 256;                          // head dim
 constexpr int AQ = 128;                          // query rows per CTA (MMA M, TMEM lanes)
 constexpr int AKEY = 64;                         // keys per tile
 constexpr int KBUF = 3;                          // K tile ring
-constexpr int VBUF = 2;                          // V tile ring
+constexpr int VBUF = 3;                          // V tile ring
+constexpr int PBUF = 2;                          // P tiles (softmax weights) in shared memory
 constexpr int SOFT_WARPS = 4;
 constexpr int MMA_WARP = 4;
 constexpr int TMA_WARP = 5;
 constexpr int A_THREADS = 32 * 6;
-constexpr int Q_PANEL = AQ * 128;                // [128 rows][64 dims] fp16, 16 KB
-constexpr int Q_BYTES = (AD / 64) * Q_PANEL;     // 64 KB
 constexpr int K_PANEL = AKEY * 128;              // [64 keys][64 dims] fp16, 8 KB
 constexpr int K_BYTES = (AD / 64) * K_PANEL;     // four panels, 32 KB
 constexpr int V_BYTES = AD * 128;                // [256 dims][64 keys] fp16, 32 KB
-constexpr int OFF_K = Q_BYTES;
+constexpr int P_BYTES = AQ * 128;                // [128 rows][64 keys] fp16, 16 KB
+constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + KBUF * K_BYTES;
-constexpr int OFF_BAR = OFF_V + VBUF * V_BYTES;
+constexpr int OFF_P = OFF_V + VBUF * V_BYTES;
+constexpr int OFF_BAR = OFF_P + PBUF * P_BYTES;
+// Q arrives as fp32 boxes of [128 rows][32 dims] (128-byte swizzled), 8 of
+// them, staged in K buffer 2 and the V ring before those receive tiles (K
+// buffers 0 and 1 fill meanwhile)
+constexpr int QBOX_BYTES = AQ * 128;
+constexpr int OFF_QST = OFF_K + 2 * K_BYTES;
+static_assert(OFF_QST + (AD / 32) * QBOX_BYTES <= OFF_P, "Q staging fits K buffer 2 and the V ring");
 constexpr int A_SMEM = OFF_BAR + 192 + 1024;     // barriers, TMEM holder, flags; alignment slack
-constexpr uint32_t COL_O = 0, COL_S = 256, COL_P = 384;
+// tensor memory: O fp32 [0, 256), Q fp16 pairs [256, 384), S fp32 two buffers [384, 512)
+constexpr uint32_t COL_O = 0, COL_Q = 256, COL_S = 384;
 constexpr uint32_t A_TMEM_COLS = 512;
 constexpr float kRescaleAbove = 8.0f;            // log2 of the largest weight kept unscaled
 static_assert(A_SMEM <= 232448, "shared memory budget");
+static_assert(COL_S + 2 * AKEY <= A_TMEM_COLS, "tensor memory budget");
 
 // D[tmem] (+)= A[smem] . B[smem]^T: both operands K-major in shared memory
 // (128-byte swizzle descriptors, smem_desc_sw128), fp32 accumulate.
@@ -94,6 +103,14 @@ __device__ __forceinline__ void mma_f16_ss_elect(uint32_t d_tmem, uint64_t adesc
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// 2^x, the hardware approximation with results below float's normal range
+// flushed to zero
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -137,24 +154,26 @@ __global__ void __launch_bounds__(256) v_to_f16t_kernel(const float* __restrict_
 
 __global__ void __launch_bounds__(A_THREADS, 1)
     prefill_attention_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                             const float* __restrict__ Q, float* __restrict__ O, int T, int pos0, int num_heads,
-                             int num_kv_heads, unsigned* status) {
+                             const __grid_constant__ CUtensorMap tmQ, float* __restrict__ O, int T, int pos0,
+                             int num_heads, int num_kv_heads, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sQ = smem;
   uint8_t* sK = smem + OFF_K;
   uint8_t* sV = smem + OFF_V;
+  uint8_t* sP = smem + OFF_P;
   uint64_t* kFull = reinterpret_cast<uint64_t*>(smem + OFF_BAR);  // [3] a K tile has landed
   uint64_t* kEmpty = kFull + 3;                                   // [3] the scores of a K buffer's tile are done
-  uint64_t* vFull = kFull + 6;                                    // [2] a V tile has landed
-  uint64_t* vEmpty = kFull + 8;                                   // [2] the O product of a V buffer's tile is done
-  uint64_t* sFull = kFull + 10;                                   // [2] S_j computed (and every MMA before it)
-  uint64_t* pFull = kFull + 12;                                   // [2] P_j written (one arrival per softmax warp)
-  uint64_t* oDone = kFull + 14;                                   // O += P_j . V_j done
-  uint64_t* oLast = kFull + 15;                                   // the last O product done (one phase)
-  uint64_t* drain = kFull + 16;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(kFull + 17);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(kFull + 18);
+  uint64_t* vFull = kFull + 6;                                    // [3] a V tile has landed
+  uint64_t* vEmpty = kFull + 9;                                   // [3] the O product of a V buffer's tile is done
+  uint64_t* sFull = kFull + 12;                                   // [2] S_j computed (and every MMA before it)
+  uint64_t* pFull = kFull + 14;                                   // [2] P_j written (one arrival per softmax warp)
+  uint64_t* oDone = kFull + 16;                                   // O += P_j . V_j done
+  uint64_t* oLast = kFull + 17;                                   // the last O product done (one phase)
+  uint64_t* drain = kFull + 18;
+  uint64_t* qFull = kFull + 19;                                   // Q's fp32 boxes have landed
+  uint64_t* qFree = kFull + 20;                                   // Q is in tensor memory: its staging is free
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(kFull + 21);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(kFull + 22);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqt = (T + AQ - 1) / AQ;
@@ -166,19 +185,21 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   const int nkt = (nkeys + AKEY - 1) / AKEY;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < KBUF; ++i) {
+    for (int i = 0; i < 3; ++i) {
       mbar_init(&kFull[i], 1);
       mbar_init(&kEmpty[i], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
       mbar_init(&vFull[i], 1);
       mbar_init(&vEmpty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&sFull[i], 1);
       mbar_init(&pFull[i], SOFT_WARPS);
     }
     mbar_init(oDone, 1);
     mbar_init(oLast, 1);
     mbar_init(drain, 1);
+    mbar_init(qFull, 1);
+    mbar_init(qFree, SOFT_WARPS);
     abort_flag[0] = 0;
     abort_flag[1] = 0;   // never set: the drain waits ignore the abort
     fence_mbar_init();
@@ -188,8 +209,10 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const bool producer = warp == TMA_WARP && lane == 0;
-  int last_k = -1, last_v = -1;   // producer: last K and V tiles sent
+  // two producer lanes, so that K and V are each refilled as soon as their own
+  // buffer is free: lane 0 the K ring, lane 1 the V ring
+  const bool kprod = warp == TMA_WARP && lane == 0, vprod = warp == TMA_WARP && lane == 1;
+  int last_k = -1, last_v = -1;   // the last K (lane 0) and V (lane 1) tiles sent
   auto send_k = [&](int ti) {
     const int b = ti % KBUF;
     mbar_arrive_expect_tx(&kFull[b], K_BYTES);
@@ -199,7 +222,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     last_k = ti;
   };
   auto send_v = [&](int ti) {
-    const int b = ti & 1;
+    const int b = ti % VBUF;
     mbar_arrive_expect_tx(&vFull[b], V_BYTES);
     tma_load_2d(sV + b * V_BYTES, &tmV, ti * AKEY, g * AD, &vFull[b]);
     last_v = ti;
@@ -210,29 +233,50 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   const int t = t0 + r;
   const uint32_t lane_addr = tmem_base + ((uint32_t)(warp * 32) << 16);
 
-  // ---- prologue: tiles 0 and 1 on their way, Q into shared memory
-  if (producer) {
+  // ---- prologue: Q's fp32 boxes and K tiles 0, 1 on their way; Q converted
+  // into tensor memory; then the rest of the K and V rings
+  bool q_sent = false;
+  if (kprod) {
+    tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
+    mbar_arrive_expect_tx(qFull, (AD / 32) * QBOX_BYTES);
+#pragma unroll
+    for (int b = 0; b < AD / 32; ++b) tma_load_2d(smem + OFF_QST + b * QBOX_BYTES, &tmQ, h * AD + 32 * b, t0, qFull);
+    q_sent = true;
+    for (int ti = 0; ti < 2 && ti < nkt; ++ti) send_k(ti);
+    if (mbar_wait(qFree, 0, abort_flag, status) && nkt > 2) send_k(2);
+  } else if (vprod) {
     tma_prefetch_desc(&tmV);
-    for (int ti = 0; ti < 2 && ti < nkt; ++ti) {
-      send_k(ti);
-      send_v(ti);
-    }
-    if (nkt > 2) send_k(2);
+    if (mbar_wait(qFree, 0, abort_flag, status))
+      for (int ti = 0; ti < VBUF && ti < nkt; ++ti) send_v(ti);
   } else if (warp < SOFT_WARPS) {
-    // row r of the four Q panels; 16-byte chunk c of a row sits at c ^ (r & 7)
-    const float4* qrow = reinterpret_cast<const float4*>(Q + (size_t)t * q_dim + (size_t)h * AD);
-#pragma unroll 4
-    for (int c = 0; c < AD / 8; ++c) {
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-      if (t < T) {
-        a = __ldg(qrow + 2 * c);
-        b = __ldg(qrow + 2 * c + 1);
+    // row r of the staged boxes (16-byte chunk c of a row at c ^ (r & 7)) as
+    // fp16 pairs into TMEM lane r, columns COL_Q + 0 .. 127 (dims in order);
+    // rows past T arrived as zeros
+    if (__all_sync(0xffffffffu, mbar_wait(qFull, 0, abort_flag, status))) {
+#pragma unroll 1
+      for (int pair = 0; pair < AD / 64; ++pair) {
+        uint32_t w[32];
+#pragma unroll
+        for (int bb = 0; bb < 2; ++bb) {
+          const uint8_t* row = smem + OFF_QST + (2 * pair + bb) * QBOX_BYTES + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float4 v = *reinterpret_cast<const float4*>(row + ((c ^ (r & 7)) << 4));
+            w[16 * bb + 2 * c] = pack_half2(v.x, v.y);
+            w[16 * bb + 2 * c + 1] = pack_half2(v.z, v.w);
+          }
+        }
+        tmem_st_32x32b_x32(lane_addr + COL_Q + 32 * pair, w);
+        // the store reads its source registers asynchronously
+        tmem_st_wait();
       }
-      *reinterpret_cast<uint4*>(sQ + (c >> 3) * Q_PANEL + r * 128 + (((c & 7) ^ (r & 7)) << 4)) =
-          make_uint4(pack_half2(a.x, a.y), pack_half2(a.z, a.w), pack_half2(b.x, b.y), pack_half2(b.z, b.w));
     }
+    tc_fence_before();
+    // the staging's generic reads before the producers' TMA writes into it
     fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(qFree);
   }
   __syncthreads();
 
@@ -240,15 +284,15 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     // ------------------------------------------------ MMA issuer (whole warp)
     constexpr uint32_t IDESC_S = idesc_f16_f32(AQ, AKEY);
     constexpr uint32_t IDESC_O = idesc_f16_f32(AQ, AD);
-    const uint64_t qdesc = smem_desc_sw128(sQ);
+    tc_fence_after();   // Q's tensor-memory stores came before the block barrier
+    // S_ti = Q . K_ti^T: A = Q from tensor memory (8 columns per 16 dims), B =
+    // the K tile in shared memory (panel per 64 dims, +32 bytes per 16)
     auto issue_S = [&](int ti) {
       const uint64_t kdesc = smem_desc_sw128(sK + (ti % KBUF) * K_BYTES);
 #pragma unroll
-      for (int kk = 0; kk < AD / 16; ++kk) {
-        const uint64_t step = 2 * (kk & 3);   // +32 bytes inside the 128-byte swizzle atom
-        mma_f16_ss_elect(tmem_base + COL_S + 64 * (ti & 1), qdesc + (uint64_t)(((kk >> 2) * Q_PANEL) >> 4) + step,
-                         kdesc + (uint64_t)(((kk >> 2) * K_PANEL) >> 4) + step, IDESC_S, kk != 0);
-      }
+      for (int kk = 0; kk < AD / 16; ++kk)
+        mma_f16_ts_elect(tmem_base + COL_S + AKEY * (ti & 1), tmem_base + COL_Q + 8 * kk,
+                         kdesc + (uint64_t)(((kk >> 2) * K_PANEL) >> 4) + 2 * (kk & 3), IDESC_S, kk != 0);
       mma_commit_elect(&sFull[ti & 1]);
       mma_commit_elect(&kEmpty[ti % KBUF]);
     };
@@ -268,16 +312,19 @@ __global__ void __launch_bounds__(A_THREADS, 1)
         tc_fence_after();
         issue_S(j + 1);
       }
-      ok = __all_sync(0xffffffffu, mbar_wait(&pFull[j & 1], (uint32_t)((j >> 1) & 1), abort_flag, status) &&
-                                       mbar_wait(&vFull[j & 1], (uint32_t)((j >> 1) & 1), abort_flag, status));
+      // V first (it is usually in), then P: one wake-up on the critical path
+      ok = __all_sync(0xffffffffu, mbar_wait(&vFull[j % VBUF], (uint32_t)((j / VBUF) & 1), abort_flag, status));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&pFull[j & 1], (uint32_t)((j >> 1) & 1), abort_flag, status));
       if (!ok) break;
       tc_fence_after();
-      const uint64_t vdesc = smem_desc_sw128(sV + (j & 1) * V_BYTES);
+      // O += P_j . V_j: A = P_j [128 rows][64 keys], B = V_j [256 dims][64
+      // keys], both K-major in shared memory (+32 bytes per 16 keys)
+      const uint64_t pdesc = smem_desc_sw128(sP + (j & 1) * P_BYTES);
+      const uint64_t vdesc = smem_desc_sw128(sV + (j % VBUF) * V_BYTES);
 #pragma unroll
       for (int kk = 0; kk < AKEY / 16; ++kk)
-        mma_f16_ts_elect(tmem_base + COL_O, tmem_base + COL_P + 32 * (j & 1) + 8 * kk, vdesc + 2 * kk, IDESC_O,
-                         (j | kk) != 0);
-      mma_commit_elect(&vEmpty[j & 1]);
+        mma_f16_ss_elect(tmem_base + COL_O, pdesc + 2 * kk, vdesc + 2 * kk, IDESC_O, (j | kk) != 0);
+      mma_commit_elect(&vEmpty[j % VBUF]);
       mma_commit_elect(oDone);
       if (j == nkt - 1) mma_commit_elect(oLast);
     }
@@ -286,27 +333,30 @@ __global__ void __launch_bounds__(A_THREADS, 1)
       __all_sync(0xffffffffu, mbar_wait(drain, 0, abort_flag + 1, status));
     }
   } else if (warp == TMA_WARP) {
-    // ------------------------------------------------ TMA producer
-    if (producer) {
-      // K_{n+1} once S_{n-2} is done, then V_n once O_{n-2} is (the scores of
-      // a tile are computed well before its O product, so K runs further ahead)
+    // ------------------------------------------------ TMA producers
+    if (kprod) {
+      // K_n once S_{n-3}, the previous tile of its buffer, is done
       bool ok = true;
 #pragma unroll 1
-      for (int n = 2; n < nkt && ok; ++n) {
-        if (n + 1 < nkt) {
-          ok = mbar_wait(&kEmpty[(n + 1) % KBUF], (uint32_t)((((n + 1) / KBUF) - 1) & 1), abort_flag, status);
-          if (!ok) break;
-          send_k(n + 1);
-        }
-        ok = mbar_wait(&vEmpty[n & 1], (uint32_t)(((n >> 1) - 1) & 1), abort_flag, status);
-        if (ok) send_v(n);
+      for (int n = KBUF; n < nkt && ok; ++n) {
+        ok = mbar_wait(&kEmpty[n % KBUF], (uint32_t)(((n / KBUF) - 1) & 1), abort_flag, status);
+        if (ok) send_k(n);
       }
       // every copy sent has landed before the CTA ends (at once unless a wait
       // gave up); the last tile of a ring slot is the only one that can be pending
       for (int ti = max(0, last_k - KBUF + 1); ti <= last_k; ++ti)
         mbar_wait(&kFull[ti % KBUF], (uint32_t)((ti / KBUF) & 1), abort_flag + 1, status);
-      for (int ti = max(0, last_v - 1); ti <= last_v; ++ti)
-        mbar_wait(&vFull[ti & 1], (uint32_t)((ti >> 1) & 1), abort_flag + 1, status);
+      if (q_sent) mbar_wait(qFull, 0, abort_flag + 1, status);
+    } else if (vprod) {
+      // V_n once O_{n-3}, the previous tile of its buffer, is done
+      bool ok = true;
+#pragma unroll 1
+      for (int n = VBUF; n < nkt && ok; ++n) {
+        ok = mbar_wait(&vEmpty[n % VBUF], (uint32_t)(((n / VBUF) - 1) & 1), abort_flag, status);
+        if (ok) send_v(n);
+      }
+      for (int ti = max(0, last_v - VBUF + 1); ti <= last_v; ++ti)
+        mbar_wait(&vFull[ti % VBUF], (uint32_t)((ti / VBUF) & 1), abort_flag + 1, status);
     }
   } else {
     // ------------------------------------------------ softmax rows, then the output
@@ -320,19 +370,23 @@ __global__ void __launch_bounds__(A_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       uint32_t sv[64];
-      tmem_ld_32x32b_x32(lane_addr + COL_S + 64 * (j & 1), sv);
-      tmem_ld_32x32b_x32(lane_addr + COL_S + 64 * (j & 1) + 32, sv + 32);
+      tmem_ld_32x32b_x32(lane_addr + COL_S + AKEY * (j & 1), sv);
+      tmem_ld_32x32b_x32(lane_addr + COL_S + AKEY * (j & 1) + 32, sv + 32);
       tmem_ld_wait_regs(sv);
       regs_after_wait(sv + 32);
       const int kb = j * AKEY;
       float s[64];
-      float m_tile = -INFINITY;
+      if (kb + AKEY - 1 <= plim) {   // every key of the tile visible to this row
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        s[c] = kb + c <= plim ? __uint_as_float(sv[c]) * sl2 : -INFINITY;
-        m_tile = fmaxf(m_tile, s[c]);
+        for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sv[c]) * sl2;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) s[c] = kb + c <= plim ? __uint_as_float(sv[c]) * sl2 : -INFINITY;
       }
-      const float m_new = fmaxf(m_run, m_tile);
+      float mq[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+      for (int c = 4; c < 64; ++c) mq[c & 3] = fmaxf(mq[c & 3], s[c]);
+      const float m_new = fmaxf(m_run, fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])));
       if (j == 0) {
         m_ref = m_new;   // key 0 is visible to every row: finite
       } else if (__any_sync(0xffffffffu, m_new > m_ref + kRescaleAbove)) {
@@ -359,19 +413,27 @@ __global__ void __launch_bounds__(A_THREADS, 1)
         m_ref = m_new;
       }
       m_run = m_new;
+      // weights 2^(s - m_ref) <= 2^8, rounded to fp16 (a result below
+      // float's normal range rounds to fp16 zero either way, so the
+      // flush-to-zero form of ex2 gives the same fp16 weights)
       uint32_t pv[32];
-      float lsum = 0.f;
+      float lq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const __half2 p = __floats2half2_rn(exp2f(s[2 * c] - m_ref), exp2f(s[2 * c + 1] - m_ref));
+        const __half2 p = __floats2half2_rn(ex2_ftz(s[2 * c] - m_ref), ex2_ftz(s[2 * c + 1] - m_ref));
         const float2 pf = __half22float2(p);
-        lsum += pf.x + pf.y;
+        lq[c & 3] += pf.x + pf.y;
         pv[c] = *reinterpret_cast<const uint32_t*>(&p);
       }
-      l += lsum;
-      // P_j into the P buffer of P_{j-2}, whose O product S_j's completion covers
-      tmem_st_32x32b_x32(lane_addr + COL_P + 32 * (j & 1), pv);
-      tmem_st_wait();
+      l += (lq[0] + lq[1]) + (lq[2] + lq[3]);
+      // P_j into shared memory, row r of the P buffer of P_{j-2} (whose O
+      // product S_j's completion covers): 16-byte chunk c at c ^ (r & 7)
+      uint8_t* prow = sP + (j & 1) * P_BYTES + r * 128;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc)
+        *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) =
+            make_uint4(pv[4 * cc], pv[4 * cc + 1], pv[4 * cc + 2], pv[4 * cc + 3]);
+      fence_proxy_async_smem();   // the MMA reads P through the async proxy
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&pFull[j & 1]);
@@ -440,6 +502,12 @@ int launch_prefill_attention(const float* Q, const float* K, const float* V, flo
   if (!make_map_2d(fn, &mV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, VT16, rows, kv_dim, ldv * 2, AKEY, AD,
                    CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
     return -1;
+  // Q as fp32 boxes of [128 rows][32 dims] (128 bytes, the swizzle span)
+  const uint64_t q_dim = (uint64_t)num_heads * AD;
+  CUtensorMap mQ;
+  if (!make_map_2d(fn, &mQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, Q, q_dim, (uint64_t)T, q_dim * 4, 32, AQ,
+                   CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
+    return -1;
 
   static int attr_set[64] = {0};
   int dev = 0;
@@ -450,8 +518,8 @@ int launch_prefill_attention(const float* Q, const float* K, const float* V, flo
     attr_set[dev] = 1;
   }
   const long long grid = (long long)((T + AQ - 1) / AQ) * num_heads;
-  prefill_attention_kernel<<<(unsigned)grid, A_THREADS, A_SMEM, s>>>(mK, mV, Q, O, T, pos0, num_heads, num_kv_heads,
-                                                                     status);
+  prefill_attention_kernel<<<(unsigned)grid, A_THREADS, A_SMEM, s>>>(mK, mV, mQ, O, T, pos0, num_heads,
+                                                                     num_kv_heads, status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prefill attention");
   return 0;
