@@ -86,6 +86,10 @@ constexpr int OFF_BAR = OFF_P + PBUF * P_BYTES;
 constexpr int QBOX_BYTES = AQ * 128;
 constexpr int OFF_QST = OFF_K + 2 * K_BYTES;
 static_assert(OFF_QST + (AD / 32) * QBOX_BYTES <= OFF_P, "Q staging fits K buffer 2 and the V ring");
+// O leaves the same way, fp32 boxes of [128 rows][32 dims] staged from offset
+// 0 once every product is done (the rings are idle then)
+constexpr int OFF_OST = 0;
+static_assert(OFF_OST + (AD / 32) * QBOX_BYTES <= OFF_P, "O staging fits the rings");
 constexpr int A_SMEM = OFF_BAR + 192 + 1024;     // barriers, TMEM holder, flags; alignment slack
 // tensor memory: O fp32 [0, 256), Q fp16 pairs [256, 384), S fp32 two buffers [384, 512)
 constexpr uint32_t COL_O = 0, COL_Q = 256, COL_S = 384;
@@ -154,8 +158,8 @@ __global__ void __launch_bounds__(256) v_to_f16t_kernel(const float* __restrict_
 
 __global__ void __launch_bounds__(A_THREADS, 1)
     prefill_attention_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                             const __grid_constant__ CUtensorMap tmQ, float* __restrict__ O, int T, int pos0,
-                             int num_heads, int num_kv_heads, unsigned* status) {
+                             const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO, int T,
+                             int pos0, int num_heads, int num_kv_heads, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sK = smem + OFF_K;
@@ -180,7 +184,6 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   const int h = blockIdx.x % num_heads;
   const int t0 = (nqt - 1 - (int)(blockIdx.x / num_heads)) * AQ;
   const int g = h / (num_heads / num_kv_heads);
-  const size_t q_dim = (size_t)num_heads * AD;
   const int nkeys = pos0 + min(t0 + AQ, T);      // keys this CTA's rows see
   const int nkt = (nkeys + AKEY - 1) / AKEY;
 
@@ -438,25 +441,35 @@ __global__ void __launch_bounds__(A_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&pFull[j & 1]);
     }
-    // ---- O / l to global memory, after the last O product
+    // ---- O / l to global memory, after the last O product: row r of box cb
+    // (dims 32 cb ..) with 16-byte chunk c at c ^ (r & 7), then TMA tensor
+    // stores (rows past T are not written). A thread writes 128 contiguous
+    // bytes of one row per box; a warp store of scattered rows would move
+    // 32 half-filled sectors instead.
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(oLast, 0, abort_flag, status));
     if (ok) {
       tc_fence_after();
       const float inv = 1.0f / l;
-      float* orow = O + (size_t)t * q_dim + (size_t)h * AD;
 #pragma unroll 1
       for (int cb = 0; cb < AD / 32; ++cb) {
         uint32_t ov[32];
         tmem_ld_32x32b_x32(lane_addr + COL_O + cb * 32, ov);
         tmem_ld_wait_regs(ov);
-        if (t < T) {
-          float4* dst = reinterpret_cast<float4*>(orow + cb * 32);
+        uint8_t* row = smem + OFF_OST + cb * QBOX_BYTES + r * 128;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(ov[4 * i]) * inv, __uint_as_float(ov[4 * i + 1]) * inv,
-                                 __uint_as_float(ov[4 * i + 2]) * inv, __uint_as_float(ov[4 * i + 3]) * inv);
-        }
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<float4*>(row + ((c ^ (r & 7)) << 4)) =
+              make_float4(__uint_as_float(ov[4 * c]) * inv, __uint_as_float(ov[4 * c + 1]) * inv,
+                          __uint_as_float(ov[4 * c + 2]) * inv, __uint_as_float(ov[4 * c + 3]) * inv);
       }
+      fence_proxy_async_smem();   // the TMA store reads the boxes through the async proxy
+    }
+    named_sync(1, 32 * SOFT_WARPS);
+    if (threadIdx.x == 0 && ok) {
+#pragma unroll
+      for (int cb = 0; cb < AD / 32; ++cb) tma_store_2d(&tmO, smem + OFF_OST + cb * QBOX_BYTES, h * AD + 32 * cb, t0);
+      bulk_commit_group();
+      bulk_wait_read_all();   // the boxes are read before the CTA's shared memory goes
     }
   }
   tc_fence_before();
@@ -504,8 +517,10 @@ int launch_prefill_attention(const float* Q, const float* K, const float* V, flo
     return -1;
   // Q as fp32 boxes of [128 rows][32 dims] (128 bytes, the swizzle span)
   const uint64_t q_dim = (uint64_t)num_heads * AD;
-  CUtensorMap mQ;
+  CUtensorMap mQ, mO;
   if (!make_map_2d(fn, &mQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, Q, q_dim, (uint64_t)T, q_dim * 4, 32, AQ,
+                   CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len) ||
+      !make_map_2d(fn, &mO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, O, q_dim, (uint64_t)T, q_dim * 4, 32, AQ,
                    CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
     return -1;
 
@@ -518,7 +533,7 @@ int launch_prefill_attention(const float* Q, const float* K, const float* V, flo
     attr_set[dev] = 1;
   }
   const long long grid = (long long)((T + AQ - 1) / AQ) * num_heads;
-  prefill_attention_kernel<<<(unsigned)grid, A_THREADS, A_SMEM, s>>>(mK, mV, mQ, O, T, pos0, num_heads,
+  prefill_attention_kernel<<<(unsigned)grid, A_THREADS, A_SMEM, s>>>(mK, mV, mQ, mO, T, pos0, num_heads,
                                                                      num_kv_heads, status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prefill attention");
