@@ -122,37 +122,42 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// V rows [rows][cols] f32 -> VT [cols][ldv] fp16 (round to nearest), 64 x 64
-// tiles through shared memory; grid (ceil(rows / 64), cols / 64), 256
-// threads. Reads are float4 along a row of V; each write is 16 bytes, eight
-// positions of one row of VT (ldv is a multiple of 8, so a chunk never passes
-// the row's end; positions past rows are written as zeros).
-__global__ void __launch_bounds__(256) v_to_f16t_kernel(const float* __restrict__ V, int rows, int cols,
+// The cache rows 0 .. rows - 1 to fp16 (round to nearest) in one launch:
+// K as it is ([rows][cols] -> K16, 8 values a thread step) and V transposed
+// ([rows][cols] -> VT [cols][ldv], ldv a multiple of 16, positions past rows
+// written as zeros). A warp transposes 16 positions x 32 columns through
+// registers: lane l reads column c0 + l of the 16 rows (every load a
+// coalesced 128-byte row segment) and writes its 16 fp16 values as 32
+// contiguous bytes of row c0 + l of VT. No shared memory, so that the
+// attention kernel, launched programmatically behind it, can take an SM
+// beside its blocks.
+__global__ void __launch_bounds__(256) kv_to_f16_kernel(const float* __restrict__ K, const float* __restrict__ V,
+                                                        int rows, int cols, uint16_t* __restrict__ K16,
                                                         uint16_t* __restrict__ VT, int ldv) {
-  __shared__ float tile[64][65];
-  const int r0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
-  const int tid = threadIdx.x;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int rr = (tid >> 4) + 16 * i, cc = 4 * (tid & 15);
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r0 + rr < rows) v = __ldg(reinterpret_cast<const float4*>(V + (size_t)(r0 + rr) * cols + c0 + cc));
-    tile[rr][cc] = v.x;
-    tile[rr][cc + 1] = v.y;
-    tile[rr][cc + 2] = v.z;
-    tile[rr][cc + 3] = v.w;
+  grid_launch_dependents();
+  const size_t nthreads = (size_t)gridDim.x * blockDim.x;
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  // K: rows * cols is a multiple of 8 (cols is a multiple of 256)
+  const size_t n8 = (size_t)rows * cols / 8;
+  const float4* k4 = reinterpret_cast<const float4*>(K);
+  uint4* o4 = reinterpret_cast<uint4*>(K16);
+  for (size_t i = tid; i < n8; i += nthreads) {
+    const float4 a = __ldg(k4 + 2 * i), b = __ldg(k4 + 2 * i + 1);
+    o4[i] = make_uint4(pack_half2(a.x, a.y), pack_half2(a.z, a.w), pack_half2(b.x, b.y), pack_half2(b.z, b.w));
   }
-  __syncthreads();
+  // V: units of 16 positions x 32 columns, one per warp step
+  const int lane = threadIdx.x & 31;
+  const size_t nwarps = nthreads / 32, wid = tid / 32;
+  const int pblocks = ldv / 16, cblocks = cols / 32;
+  for (size_t u = wid; u < (size_t)pblocks * cblocks; u += nwarps) {
+    const int p0 = (int)(u % pblocks) * 16, c = (int)(u / pblocks) * 32 + lane;
+    float v[16];
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int cc = (tid >> 3) + 32 * i, rc = 8 * (tid & 7);
-    if (r0 + rc >= rows) continue;
-    uint4 o;
-    o.x = pack_half2(tile[rc][cc], tile[rc + 1][cc]);
-    o.y = pack_half2(tile[rc + 2][cc], tile[rc + 3][cc]);
-    o.z = pack_half2(tile[rc + 4][cc], tile[rc + 5][cc]);
-    o.w = pack_half2(tile[rc + 6][cc], tile[rc + 7][cc]);
-    *reinterpret_cast<uint4*>(VT + (size_t)(c0 + cc) * ldv + r0 + rc) = o;
+    for (int i = 0; i < 16; ++i) v[i] = p0 + i < rows ? __ldg(V + (size_t)(p0 + i) * cols + c) : 0.f;
+    uint4* dst = reinterpret_cast<uint4*>(VT + (size_t)c * ldv + p0);
+    dst[0] = make_uint4(pack_half2(v[0], v[1]), pack_half2(v[2], v[3]), pack_half2(v[4], v[5]), pack_half2(v[6], v[7]));
+    dst[1] = make_uint4(pack_half2(v[8], v[9]), pack_half2(v[10], v[11]), pack_half2(v[12], v[13]),
+                        pack_half2(v[14], v[15]));
   }
 }
 
@@ -246,10 +251,12 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 #pragma unroll
     for (int b = 0; b < AD / 32; ++b) tma_load_2d(smem + OFF_QST + b * QBOX_BYTES, &tmQ, h * AD + 32 * b, t0, qFull);
     q_sent = true;
+    grid_dependency_wait();   // K16 and VT16 come from the conversion launched just before
     for (int ti = 0; ti < 2 && ti < nkt; ++ti) send_k(ti);
     if (mbar_wait(qFree, 0, abort_flag, status) && nkt > 2) send_k(2);
   } else if (vprod) {
     tma_prefetch_desc(&tmV);
+    grid_dependency_wait();
     if (mbar_wait(qFree, 0, abort_flag, status))
       for (int ti = 0; ti < VBUF && ti < nkt; ++ti) send_v(ti);
   } else if (warp < SOFT_WARPS) {
@@ -482,7 +489,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 
 size_t prefill_attention_scratch_bytes(int T, int pos0, int num_kv_heads) {
   const size_t rows = (size_t)pos0 + (size_t)T, kv_dim = (size_t)num_kv_heads * AD;
-  const size_t ldv = (rows + 7) & ~(size_t)7;
+  const size_t ldv = (rows + 15) & ~(size_t)15;
   return ((rows * kv_dim * 2 + 255) & ~(size_t)255) + kv_dim * ldv * 2;
 }
 
@@ -491,20 +498,22 @@ int launch_prefill_attention(const float* Q, const float* K, const float* V, flo
                              char* msg, size_t msg_len) {
   if (T <= 0) return 0;
   const size_t rows = (size_t)pos0 + (size_t)T, kv_dim = (size_t)num_kv_heads * AD;
-  const size_t ldv = (rows + 7) & ~(size_t)7;
+  const size_t ldv = (rows + 15) & ~(size_t)15;
   uint16_t* K16 = static_cast<uint16_t*>(scratch);
   uint16_t* VT16 = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(scratch) + ((rows * kv_dim * 2 + 255) & ~(size_t)255));
   auto cuda_fail = [&](cudaError_t e, const char* what) {
     snprintf(msg, msg_len, "%s: %s", what, cudaGetErrorString(e));
     return -1;
   };
-  // the fp16 copies of the cache rows 0 .. pos0 + T - 1
-  cudaError_t e = launch_x_to_f16(K, K16, rows * kv_dim, s);
-  if (e != cudaSuccess) return cuda_fail(e, "K to fp16");
-  v_to_f16t_kernel<<<dim3((unsigned)((rows + 63) / 64), (unsigned)(kv_dim / 64)), 256, 0, s>>>(
-      V, (int)rows, (int)kv_dim, VT16, (int)ldv);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "V to fp16 (transposed)");
+  // the fp16 copies of the cache rows 0 .. pos0 + T - 1 (plain stream order:
+  // everything before is complete when it starts)
+  {
+    const size_t units = rows * kv_dim / 8 / 256 + 1;
+    const unsigned blocks = (unsigned)(units < (size_t)num_sms() * 4 ? units : (size_t)num_sms() * 4);
+    kv_to_f16_kernel<<<blocks, 256, 0, s>>>(K, V, (int)rows, (int)kv_dim, K16, VT16, (int)ldv);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "K and V to fp16");
 
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn(msg, msg_len);
   if (!fn) return -1;
@@ -533,9 +542,18 @@ int launch_prefill_attention(const float* Q, const float* K, const float* V, flo
     attr_set[dev] = 1;
   }
   const long long grid = (long long)((T + AQ - 1) / AQ) * num_heads;
-  prefill_attention_kernel<<<(unsigned)grid, A_THREADS, A_SMEM, s>>>(mK, mV, mQ, mO, T, pos0, num_heads,
-                                                                     num_kv_heads, status);
-  e = cudaGetLastError();
+  // launched programmatically: its CTAs start (Q on its way) while the
+  // conversion finishes; the K and V producers wait for it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(A_THREADS);
+  cfg.dynamicSmemBytes = A_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, prefill_attention_kernel, mK, mV, mQ, mO, T, pos0, num_heads, num_kv_heads, status);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prefill attention");
   return 0;
 }
