@@ -20,6 +20,7 @@
 #include <cuda_fp16.h>
 
 #include "apr_internal.h"
+#include "host_common.h"
 
 namespace apr {
 namespace {
@@ -35,6 +36,8 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+__device__ __forceinline__ void grid_dependency_wait_inline() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 template <int QT, int TMAX, int RW, bool VEC, bool SWI>
 __global__ void __launch_bounds__(kWarps * 32) gemv_kernel(const uint8_t* __restrict__ W,
@@ -234,6 +237,131 @@ cudaError_t launch_q(const void* W, const void* Wu, int n, int k, const float* X
   return launch_t<QT, 16, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
 }
 
+// F16 weights, k % 256 == 0: a warp per weight row, each lane 16-byte chunks
+// (8 halves) c = lane + 32 i of the row, eight chunks' loads in flight; X
+// through the read-only cache (the same columns for every row, so it stays in
+// L1); exact fp32 products (a half widens exactly). The weights of the
+// warp's first chunks are requested before the dependency wait (they are
+// never the output of the preceding kernel); X, R and Y after it.
+constexpr int F16G = 8;  // chunks a lane loads at once
+
+template <int TMAX, bool SWI>
+__global__ void __launch_bounds__(kWarps * 32) gemv_f16_kernel(const uint16_t* __restrict__ W,
+                                                               const uint16_t* __restrict__ Wu, int n, int k,
+                                                               const float* __restrict__ X, int T, float* Y, int ldy,
+                                                               const float* R) {
+  constexpr int NM = SWI ? 2 : 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nchunk = k / 8;                 // 16-byte chunks a row
+  const int ngroup = nchunk / (32 * F16G);  // groups of F16G chunks a lane
+  const int rest = nchunk / 32 - ngroup * F16G;
+  bool waited = false;
+  for (int row = blockIdx.x * kWarps + warp; row < n; row += gridDim.x * kWarps) {
+    float acc[NM][TMAX];
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) acc[m][t] = 0.f;
+    const uint4* wr[NM];
+    wr[0] = reinterpret_cast<const uint4*>(W + (size_t)row * k);
+    if (SWI) wr[NM - 1] = reinterpret_cast<const uint4*>(Wu + (size_t)row * k);
+    auto chunk = [&](const uint4 (&w)[NM], int c) {
+      // chunk c: columns 8c .. 8c + 7
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        if (t < T) {
+          const float4* xr = reinterpret_cast<const float4*>(X + (size_t)t * k + 8 * c);
+          const float4 a = __ldg(xr), b = __ldg(xr + 1);
+#pragma unroll
+          for (int m = 0; m < NM; ++m) {
+            const float2 w0 = __half22float2(*reinterpret_cast<const __half2*>(&w[m].x));
+            const float2 w1 = __half22float2(*reinterpret_cast<const __half2*>(&w[m].y));
+            const float2 w2 = __half22float2(*reinterpret_cast<const __half2*>(&w[m].z));
+            const float2 w3 = __half22float2(*reinterpret_cast<const __half2*>(&w[m].w));
+            float v = acc[m][t];
+            v = fmaf(w0.x, a.x, v);
+            v = fmaf(w0.y, a.y, v);
+            v = fmaf(w1.x, a.z, v);
+            v = fmaf(w1.y, a.w, v);
+            v = fmaf(w2.x, b.x, v);
+            v = fmaf(w2.y, b.y, v);
+            v = fmaf(w3.x, b.z, v);
+            v = fmaf(w3.y, b.w, v);
+            acc[m][t] = v;
+          }
+        }
+      }
+    };
+    for (int gi = 0; gi < ngroup; ++gi) {
+      uint4 w[F16G][NM];
+#pragma unroll
+      for (int i = 0; i < F16G; ++i)
+#pragma unroll
+        for (int m = 0; m < NM; ++m) w[i][m] = ldg_nc_v4(wr[m] + lane + 32 * (gi * F16G + i));
+      if (!waited) {
+        grid_dependency_wait_inline();
+        waited = true;
+      }
+#pragma unroll
+      for (int i = 0; i < F16G; ++i) chunk(w[i], lane + 32 * (gi * F16G + i));
+    }
+    for (int i = 0; i < rest; ++i) {
+      uint4 w[NM];
+#pragma unroll
+      for (int m = 0; m < NM; ++m) w[m] = ldg_nc_v4(wr[m] + lane + 32 * (ngroup * F16G + i));
+      if (!waited) {
+        grid_dependency_wait_inline();
+        waited = true;
+      }
+      chunk(w, lane + 32 * (ngroup * F16G + i));
+    }
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        float v = acc[m][t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        acc[m][t] = v;
+      }
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+      if (lane == t && t < T) {
+        const size_t o = (size_t)t * ldy + row;
+        Y[o] = SWI ? silu_mul(acc[0][t], acc[NM - 1][t]) : acc[0][t] + (R ? R[o] : 0.f);
+      }
+    }
+  }
+  if (!waited) grid_dependency_wait_inline();  // a CTA without rows
+}
+
+template <int TMAX, bool SWI>
+cudaError_t launch_f16_t(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
+                         const float* R, cudaStream_t s) {
+  long blocks = (n + kWarps - 1) / kWarps;
+  const long cap = (long)num_sms() * 2;
+  if (blocks > cap) blocks = cap;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemv_f16_kernel<TMAX, SWI>, static_cast<const uint16_t*>(W),
+                            static_cast<const uint16_t*>(Wu), n, k, X, T, Y, ldy, R);
+}
+
+template <bool SWI>
+cudaError_t launch_f16(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
+                       const float* R, cudaStream_t s) {
+  if (T <= 1) return launch_f16_t<1, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 2) return launch_f16_t<2, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 4) return launch_f16_t<4, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 8) return launch_f16_t<8, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  return launch_f16_t<16, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+}
+
 }  // namespace
 
 cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
@@ -243,9 +371,12 @@ cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, 
   if (gemv_i8_fits(qtype, n, k, T, swi)) return launch_gemv_i8(qtype, W, Wu, n, k, X, Y, R, status, s);
   if (gemv_rows_fits(qtype, n, k, T, swi)) return launch_gemv_rows(qtype, W, Wu, n, k, X, T, Y, R, status, s);
   if (gemv_bulk_fits(qtype, k, T, swi)) return launch_gemv_bulk(qtype, W, Wu, n, k, X, T, Y, ldy, R, status, s);
-  if (qtype == kF16)
+  if (qtype == kF16) {
+    if (k % 256 == 0)
+      return swi ? launch_f16<true>(W, Wu, n, k, X, T, Y, ldy, R, s) : launch_f16<false>(W, Wu, n, k, X, T, Y, ldy, R, s);
     return swi ? launch_q<kF16, true>(W, Wu, n, k, X, T, Y, ldy, R, s)
                : launch_q<kF16, false>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  }
   if (qtype == kQ4_0)
     return swi ? launch_q<kQ4_0, true>(W, Wu, n, k, X, T, Y, ldy, R, s)
                : launch_q<kQ4_0, false>(W, Wu, n, k, X, T, Y, ldy, R, s);
