@@ -1,4 +1,4 @@
-"""Plain CPU oracle for the Q4_0 / Q8_0 / F16 prefill projections (float64).
+"""Plain CPU oracle for the Q4_0 / Q8_0 / F16 / Q4_K prefill projections (float64).
 
 TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import or call
@@ -24,6 +24,14 @@ What is computed, and where the pages define it:
   values back unchanged). Here a "block" of F16 is 32 consecutive elements
   (64 bytes), so that every format is addressed the same way; ``k`` is a
   multiple of 32 for every format.
+* Q4_K, a format the pages dispatch (``qwen35_dequant_f32``, grid
+  ``(n, k.div_ceil(256))``) without printing its layout; read as the GGUF
+  Q4_K superblock of 256 elements in 144 bytes: fp16 ``d`` (bytes 0-1), fp16
+  ``dmin`` (2-3), 12 bytes of packed 6-bit sub-block scales and mins
+  (``q4_k_scales_mins``), then 128 bytes of 4-bit codes: byte ``32 g + l``
+  holds element ``64 g + l`` in its low nibble and ``64 g + 32 + l`` in its
+  high nibble; element ``e`` of sub-block ``j = e / 32`` is
+  ``w = d sc_j q - dmin m_j``.
 * Projection ``Y[T][n] = X[T][k] . W[n][k]^T`` (aprender-serve 0.70.2
   src/cuda/executor/gdn_prefill_ops.rs, doc of ``qwen35_project_rows``),
   optionally ``+ R[T][n]`` (the residual add that follows the down / output
@@ -77,8 +85,11 @@ import numpy as np
 F16 = 1
 Q4_0 = 2
 Q8_0 = 8
+Q4_K = 12
 _QK = 32
+_QK_K = 256
 _BLOCK_BYTES = {F16: 64, Q4_0: 18, Q8_0: 34}
+_SUPER_BYTES = {Q4_K: 144}
 
 
 # --------------------------------------------------------------------------
@@ -101,6 +112,45 @@ def fp16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return np.where(e == 0, sub, np.where(e == 31, special, normal))
 
 
+def _superblocks(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
+    if k % _QK_K:
+        raise ValueError("k must be a multiple of 256 for a superblock format")
+    sb = _SUPER_BYTES[qtype]
+    raw = np.ascontiguousarray(W, dtype=np.uint8).reshape(-1)
+    if raw.size != n * (k // _QK_K) * sb:
+        raise ValueError("weight byte count does not match n, k")
+    return raw.reshape(n, k // _QK_K, sb)
+
+
+def q4_k_scales_mins(scales: np.ndarray):
+    """The eight 6-bit sub-block scales and mins of a Q4_K superblock from its
+    12 packed bytes ``[..., 12]`` (reading: bytes 0-3 hold scales 0-3 in their
+    low 6 bits, bytes 4-7 mins 0-3 likewise; bytes 8-11 hold scales 4-7 in
+    their low nibble and mins 4-7 in their high nibble, whose top two bits sit
+    in the top two bits of bytes 0-3 (scales) and 4-7 (mins))."""
+    s = scales.astype(np.int64)
+    sc = np.empty(s.shape[:-1] + (8,), np.int64)
+    mn = np.empty_like(sc)
+    for j in range(4):
+        sc[..., j] = s[..., j] & 63
+        mn[..., j] = s[..., j + 4] & 63
+        sc[..., j + 4] = (s[..., j + 8] & 0x0F) | ((s[..., j] >> 6) << 4)
+        mn[..., j + 4] = (s[..., j + 8] >> 4) | ((s[..., j + 4] >> 6) << 4)
+    return sc, mn
+
+
+def _dequant_q4_k(W: np.ndarray, n: int, k: int) -> np.ndarray:
+    sb = _superblocks(Q4_K, W, n, k)
+    d = fp16_bits_to_f64(sb[..., 0].astype(np.uint16) | (sb[..., 1].astype(np.uint16) << 8))
+    dmin = fp16_bits_to_f64(sb[..., 2].astype(np.uint16) | (sb[..., 3].astype(np.uint16) << 8))
+    sc, mn = q4_k_scales_mins(sb[..., 4:16])
+    qs = sb[..., 16:].reshape(n, k // _QK_K, 4, 32)     # group g: bytes 32 g .. 32 g + 31
+    q = np.concatenate([qs & 0x0F, qs >> 4], axis=-1)  # group g: 64 elements, low nibbles first
+    q = q.reshape(n, k // _QK_K, 8, 32).astype(np.float64)  # sub-block j = 2 g + (high nibble)
+    w = d[..., None, None] * sc[..., None] * q - dmin[..., None, None] * mn[..., None]
+    return w.reshape(n, k)
+
+
 def _blocks(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
     if qtype not in _BLOCK_BYTES:
         raise ValueError(f"unsupported qtype {qtype}")
@@ -119,8 +169,8 @@ def block_scales_and_codes(qtype: int, W: np.ndarray, n: int, k: int):
     ``q'`` is ``nibble - 8`` for Q4_0 and the int8 value for Q8_0, shape
     ``[n][k/32][32]`` (int64), element order as stored.
     """
-    if qtype == F16:
-        raise ValueError("F16 weights have no block scales")
+    if qtype not in _BLOCK_BYTES or qtype == F16:
+        raise ValueError("only Q4_0 and Q8_0 have one scale and codes per 32-element block")
     blk = _blocks(qtype, W, n, k)
     d_bits = blk[..., 0].astype(np.uint16) | (blk[..., 1].astype(np.uint16) << 8)
     payload = blk[..., 2:]
@@ -136,6 +186,8 @@ def block_scales_and_codes(qtype: int, W: np.ndarray, n: int, k: int):
 def dequant_f64(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
     """``Wf[i][j] = fp16(d_{i, j/32}) * q'_{i,j}`` in float64, shape ``[n][k]``;
     for F16 the binary16 value of element ``(i, j)``."""
+    if qtype == Q4_K:
+        return _dequant_q4_k(W, n, k)
     if qtype == F16:
         raw = _blocks(qtype, W, n, k).reshape(n, k, 2)
         bits = raw[..., 0].astype(np.uint16) | (raw[..., 1].astype(np.uint16) << 8)
@@ -152,7 +204,8 @@ def dequant_f32(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
     float64 product is exact and so is its conversion to float32 (the range of
     an fp16 scale times 128 is well inside float32's normal range, and fp16
     subnormal scales times small integers stay exact in float32). Every fp16
-    value, subnormals included, is a float32 value.
+    value, subnormals included, is a float32 value. Q4_K: the exact float64
+    value ``d sc q - dmin m`` rounded once to float32.
     """
     return dequant_f64(qtype, W, n, k).astype(np.float32)
 

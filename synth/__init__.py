@@ -12,12 +12,14 @@ from .gen import (  # noqa: F401
     F16,
     Q4_0,
     Q8_0,
+    Q4_K,
     BLOCK_ELEMS,
     block_bytes,
     quantize,
     quantize_q4_0,
     quantize_q8_0,
     quantize_f16,
+    quantize_q4_k,
     weight_f32,
     activations,
     make_case,

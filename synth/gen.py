@@ -38,12 +38,14 @@ import numpy as np
 F16 = 1   # GGUF type id
 Q4_0 = 2  # GGUF type id
 Q8_0 = 8  # GGUF type id
+Q4_K = 12  # GGUF type id (256-element superblocks of 144 bytes)
 BLOCK_ELEMS = 32
-_BLOCK_BYTES = {F16: 64, Q4_0: 18, Q8_0: 34}
+_BLOCK_BYTES = {F16: 64, Q4_0: 18, Q8_0: 34, Q4_K: 18}
 
 
 def block_bytes(qtype: int) -> int:
-    """Bytes of 32 elements of ``qtype`` (one block; 64 bytes of F16)."""
+    """Bytes of 32 elements of ``qtype`` (one block; 64 bytes of F16; an
+    eighth of a Q4_K superblock)."""
     return _BLOCK_BYTES[qtype]
 
 
@@ -102,9 +104,58 @@ def quantize_f16(w: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray(w.astype("<f2")).view(np.uint8).reshape(n, 2 * k)
 
 
+def _pack_q4_k_scales(sc: np.ndarray, mn: np.ndarray) -> np.ndarray:
+    """Eight 6-bit scales and mins ``[..., 8]`` into the 12 packed bytes."""
+    out = np.zeros(sc.shape[:-1] + (12,), np.uint8)
+    for j in range(4):
+        out[..., j] = (sc[..., j] & 63) | ((sc[..., j + 4] >> 4) << 6)
+        out[..., j + 4] = (mn[..., j] & 63) | ((mn[..., j + 4] >> 4) << 6)
+        out[..., j + 8] = (sc[..., j + 4] & 15) | ((mn[..., j + 4] & 15) << 4)
+    return out
+
+
+def quantize_q4_k(w: np.ndarray) -> np.ndarray:
+    """Encode an f32 ``[n][k]`` weight (k % 256 == 0) into Q4_K superblocks
+    ``[n][k/256*144]``: per 32-element sub-block the range [lo, hi] (lo <= 0 <=
+    hi widened to include 0) gives scale (hi - lo) / 15 and min -lo; d and
+    dmin are the largest of them over 63 (stored as fp16), the 6-bit
+    sub-scales round(scale / d) and round(min / dmin), and each code
+    round((w + dmin m) / (d sc)) clamped to 0..15."""
+    w = np.ascontiguousarray(w, dtype=np.float32).astype(np.float64)
+    n, k = w.shape
+    x = w.reshape(n, k // 256, 8, 32)
+    lo = np.minimum(x.min(axis=-1), 0.0)
+    hi = np.maximum(x.max(axis=-1), 0.0)
+    scale = (hi - lo) / 15.0
+    mins = -lo
+    d = scale.max(axis=-1) / 63.0
+    dmin = mins.max(axis=-1) / 63.0
+    d16 = d.astype(np.float16)
+    dmin16 = dmin.astype(np.float16)
+    df = d16.astype(np.float64)
+    dmf = dmin16.astype(np.float64)
+    sc = np.where(df[..., None] > 0, np.clip(np.rint(scale / np.where(df > 0, df, 1.0)[..., None]), 0, 63), 0)
+    mn = np.where(dmf[..., None] > 0, np.clip(np.rint(mins / np.where(dmf > 0, dmf, 1.0)[..., None]), 0, 63), 0)
+    sc = sc.astype(np.int64)
+    mn = mn.astype(np.int64)
+    step = df[..., None] * sc
+    q = np.where(step[..., None] > 0,
+                 np.rint((x + (dmf[..., None] * mn)[..., None]) / np.where(step > 0, step, 1.0)[..., None]), 0)
+    q = np.clip(q, 0, 15).astype(np.uint8).reshape(n, k // 256, 4, 2, 32)
+    qs = (q[:, :, :, 0, :] | (q[:, :, :, 1, :] << 4)).reshape(n, k // 256, 128)
+    out = np.zeros((n, k // 256, 144), np.uint8)
+    out[..., 0:2] = d16.view(np.uint16)[..., None].view(np.uint8).reshape(n, k // 256, 2)
+    out[..., 2:4] = dmin16.view(np.uint16)[..., None].view(np.uint8).reshape(n, k // 256, 2)
+    out[..., 4:16] = _pack_q4_k_scales(sc, mn)
+    out[..., 16:] = qs
+    return out.reshape(n, -1)
+
+
 def quantize(qtype: int, w: np.ndarray) -> np.ndarray:
     if qtype == F16:
         return quantize_f16(w)
+    if qtype == Q4_K:
+        return quantize_q4_k(w)
     if qtype == Q4_0:
         return quantize_q4_0(w)
     if qtype == Q8_0:
@@ -147,6 +198,21 @@ def random_blocks(qtype: int, n: int, k: int, seed: int, scale_class: str = "mix
     gives |d| <= 8188 or 511.75.
     """
     lo, hi = SCALE_CLASSES[scale_class]
+    if qtype == Q4_K:
+        # random bytes; d and dmin of both signs drawn from the class
+        rng = np.random.default_rng(seed)
+        raw = rng.integers(0, 256, size=(n, k // 256, 144), dtype=np.uint8)
+        for off in (0, 2):
+            exp = rng.integers(lo, hi + 1, size=(n, k // 256)).astype(np.uint16)
+            if fp16_range:  # |d sc q| and |dmin m| within fp16's range: |d| < 2^6 (63 x 15 x 2^6 < 65504)
+                exp = np.minimum(exp, 20)
+            man = rng.integers(0, 1024, size=(n, k // 256)).astype(np.uint16)
+            man = np.where(exp == 0, np.maximum(man, 1), man)
+            sign = rng.integers(0, 2, size=(n, k // 256)).astype(np.uint16)
+            bits = (sign << 15) | (exp << 10) | man
+            raw[..., off] = (bits & 0xFF).astype(np.uint8)
+            raw[..., off + 1] = (bits >> 8).astype(np.uint8)
+        return raw.reshape(n, -1)
     if qtype == F16:
         # every element an fp16 value of both signs, exponent field uniform over
         # the class (nonzero mantissa in the subnormal class)

@@ -23,7 +23,12 @@ import oracle
 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-QTYPES = [synth.Q4_0, synth.Q8_0, synth.F16]
+QTYPES = [synth.Q4_0, synth.Q8_0, synth.F16, synth.Q4_K]
+
+
+def _kk(qtype, k):
+    """k as given, or widened to whole 256-element superblocks for Q4_K."""
+    return max(256, k // 256 * 256) if qtype == synth.Q4_K else k
 
 
 def load_golden(name):
@@ -102,6 +107,79 @@ def test_f16_weight_has_no_block_scales_and_needs_its_byte_count():
         oracle.dequant_f64(synth.F16, raw.reshape(-1)[:96], 1, 48)  # k % 32 != 0
 
 
+# ---------------------------------------------------------------- Q4_K (layout read, not printed on the pages)
+def _q4_k_superblock(d_bits, dmin_bits, sc, mn, q):
+    """Bytes of one Q4_K superblock from d, dmin, 8 scales, 8 mins and 256
+    codes in element order, packed by hand from the layout reading."""
+    b = bytearray(144)
+    b[0:2] = struct.pack("<H", d_bits)
+    b[2:4] = struct.pack("<H", dmin_bits)
+    for j in range(4):
+        b[4 + j] = (sc[j] & 63) | ((sc[j + 4] >> 4) << 6)
+        b[8 + j] = (mn[j] & 63) | ((mn[j + 4] >> 4) << 6)
+        b[12 + j] = (sc[j + 4] & 15) | ((mn[j + 4] & 15) << 4)
+    for g in range(4):
+        for l in range(32):
+            b[16 + 32 * g + l] = q[64 * g + l] | (q[64 * g + 32 + l] << 4)
+    return bytes(b)
+
+
+def test_q4_k_equals_q4_0_blocks_with_the_same_codes():
+    # d = 2^-9, dmin = 2^-7, sub-scales 16..31 and mins 2 sc: every element is
+    # d sc (q - 8), the Q4_0 block of scale d sc with the same code. Scales and
+    # mins above 15 use the packing's top bits.
+    rng = np.random.default_rng(21)
+    n, k = 3, 512
+    W4 = np.zeros((n, k // 32, 18), np.uint8)
+    WK = bytearray()
+    for i in range(n):
+        for s_ in range(k // 256):
+            sc = [int(v) for v in rng.integers(16, 32, size=8)]
+            mn = [2 * v for v in sc]
+            q = [int(v) for v in rng.integers(0, 16, size=256)]
+            WK += _q4_k_superblock(0x1800, 0x2000, sc, mn, q)
+            for j in range(8):
+                blk = W4[i, 8 * s_ + j]
+                blk[0:2] = np.frombuffer(struct.pack("<e", 2.0 ** -9 * sc[j]), np.uint8)
+                for e in range(16):
+                    blk[2 + e] = q[32 * j + e] | (q[32 * j + 16 + e] << 4)
+    WK = np.frombuffer(bytes(WK), np.uint8).reshape(n, -1)
+    np.testing.assert_array_equal(oracle.dequant_f64(synth.Q4_K, WK, n, k),
+                                  oracle.dequant_f64(synth.Q4_0, W4.reshape(n, -1), n, k))
+
+
+def test_q4_k_sub_block_scales_and_mins_land_on_their_elements():
+    # codes 1 everywhere, d = 1, dmin = 1: element e of sub-block j is sc_j - m_j
+    sc = [1, 2, 3, 4, 17, 33, 48, 63]
+    mn = [0, 1, 2, 3, 16, 40, 5, 62]
+    raw = np.frombuffer(_q4_k_superblock(0x3C00, 0x3C00, sc, mn, [1] * 256), np.uint8).reshape(1, 144)
+    w = oracle.dequant_f64(synth.Q4_K, raw, 1, 256)[0]
+    for j in range(8):
+        np.testing.assert_array_equal(w[32 * j:32 * (j + 1)], np.full(32, float(sc[j] - mn[j])))
+    got_sc, got_mn = oracle.q4_k_scales_mins(raw[0, 4:16])
+    assert list(got_sc) == sc and list(got_mn) == mn
+
+
+def test_q4_k_codes_in_element_order():
+    # d = 1, dmin = 0, unit scales: w = q; element e gets code e mod 16
+    q = [e % 16 for e in range(256)]
+    raw = np.frombuffer(_q4_k_superblock(0x3C00, 0x0000, [1] * 8, [0] * 8, q), np.uint8).reshape(1, 144)
+    np.testing.assert_array_equal(oracle.dequant_f64(synth.Q4_K, raw, 1, 256)[0], np.array(q, np.float64))
+
+
+def test_q4_k_encoder_round_trip_and_sizes():
+    n, k = 16, 512
+    w = synth.weight_f32(n, k, seed=4)
+    W = synth.quantize(synth.Q4_K, w)
+    assert W.shape == (n, k // 256 * 144) and synth.block_bytes(synth.Q4_K) * (k // 32) == W.shape[1]
+    err = np.abs(oracle.dequant_f64(synth.Q4_K, W, n, k) - w.astype(np.float64)).reshape(n, k // 256, 8, 32)
+    rng_ = w.reshape(n, k // 256, 8, 32)
+    step = (np.maximum(rng_.max(-1), 0) - np.minimum(rng_.min(-1), 0)) / 15.0
+    assert np.all(err.max(-1) <= 0.75 * step + 0.01 * np.abs(w).max())
+    with pytest.raises(ValueError):
+        oracle.dequant_f64(synth.Q4_K, W[:, :144], n, 128)
+
+
 def test_f16_weights_reach_every_finite_half():
     # the random F16 generator draws every exponent field 0..30 and no inf/NaN;
     # the oracle decodes each element to its binary16 value
@@ -168,7 +246,12 @@ def _parse_block_independent(qtype, blk: bytes):
 
 def _random_blocks(rng, qtype, n, k):
     """Random raw bytes with finite scales (exponent field kept below 31); for
-    F16 every element is such a half."""
+    F16 every element is such a half; for Q4_K d and dmin of every superblock."""
+    if qtype == synth.Q4_K:
+        raw = rng.integers(0, 256, size=(n, k // 256, 144), dtype=np.uint8)
+        for b in (1, 3):
+            raw[..., b] = np.where((raw[..., b] & 0x7C) == 0x7C, raw[..., b] & 0xBF, raw[..., b])
+        return raw.reshape(n, -1)
     bb = synth.block_bytes(qtype)
     raw = rng.integers(0, 256, size=(n, k // 32, bb), dtype=np.uint8)
     hi = raw[..., 1::2] if qtype == synth.F16 else raw[..., 1]
@@ -180,10 +263,38 @@ def _random_blocks(rng, qtype, n, k):
     return raw.reshape(n, -1)
 
 
+def _q4_k_row_independent(raw: bytes, k):
+    """Exact values of one Q4_K row, element by element with struct (the
+    layout read in the oracle's header, written out here as plain loops)."""
+    out = []
+    for sb in range(k // 256):
+        blk = raw[144 * sb:144 * (sb + 1)]
+        d = Fraction(struct.unpack("<e", blk[0:2])[0])
+        dmin = Fraction(struct.unpack("<e", blk[2:4])[0])
+        s = blk[4:16]
+        vals = [None] * 256
+        for j in range(8):
+            if j < 4:
+                sc, m = s[j] & 63, s[j + 4] & 63
+            else:
+                sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4)
+                m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4)
+            g, hi = j // 2, j % 2
+            for l in range(32):
+                byte = blk[16 + 32 * g + l]
+                q = (byte >> 4) if hi else (byte & 15)
+                vals[64 * g + 32 * hi + l] = d * sc * q - dmin * m
+        out.extend(vals)
+    return out
+
+
 def _exact_qgemm(qtype, W, n, k, X, R):
     bb = synth.block_bytes(qtype)
     rows = []
     for i in range(n):
+        if qtype == synth.Q4_K:
+            rows.append(_q4_k_row_independent(bytes(W[i]), k))
+            continue
         wrow = []
         for b in range(k // 32):
             blk = bytes(W[i, b * bb:(b + 1) * bb])
@@ -210,6 +321,7 @@ def _ulp32(x):
 @pytest.mark.parametrize("qtype", QTYPES)
 @pytest.mark.parametrize("n,k,T,res", [(3, 32, 2, False), (5, 64, 3, True), (2, 96, 1, True)])
 def test_brute_force_exact_rationals(qtype, n, k, T, res):
+    k = _kk(qtype, k)
     rng = np.random.default_rng(1234 + n + k + T + qtype)
     W = _random_blocks(rng, qtype, n, k)
     X = rng.standard_normal((T, k)).astype(np.float32)
@@ -231,19 +343,22 @@ def test_brute_force_exact_rationals(qtype, n, k, T, res):
 @pytest.mark.parametrize("qtype", QTYPES)
 def test_brute_force_dequant_exact(qtype):
     rng = np.random.default_rng(77 + qtype)
-    n, k = 4, 64
+    n, k = 4, _kk(qtype, 64)
     W = _random_blocks(rng, qtype, n, k)
     _, rows = _exact_qgemm(qtype, W, n, k, np.zeros((1, k), np.float32), None)
     got = oracle.dequant_f32(qtype, W, n, k)
     for i in range(n):
         for j in range(k):
-            assert Fraction(float(got[i, j])) == rows[i][j]
+            if qtype == synth.Q4_K:  # d sc q - dmin m may need more than 24 bits: rounded once
+                assert abs(Fraction(float(got[i, j])) - rows[i][j]) <= Fraction(_ulp32(float(got[i, j]))) / 2
+            else:
+                assert Fraction(float(got[i, j])) == rows[i][j]
 
 
 @pytest.mark.parametrize("qtype", QTYPES)
 def test_brute_force_swiglu(qtype):
     rng = np.random.default_rng(99 + qtype)
-    n, k, T = 4, 64, 3
+    n, k, T = 4, _kk(qtype, 64), 3
     Wg = synth.quantize(qtype, (rng.standard_normal((n, k)) * 0.3).astype(np.float32))
     Wu = synth.quantize(qtype, (rng.standard_normal((n, k)) * 0.3).astype(np.float32))
     X = rng.standard_normal((T, k)).astype(np.float32)
@@ -260,7 +375,7 @@ def test_brute_force_swiglu(qtype):
 # ---------------------------------------------------------------- invariants
 @pytest.mark.parametrize("qtype", QTYPES)
 def test_identity_x_returns_dequantized_weight(qtype):
-    n, k = 8, 64
+    n, k = 8, _kk(qtype, 64)
     W = synth.quantize(qtype, synth.weight_f32(n, k, seed=5))
     X = np.eye(k, dtype=np.float32)
     Y = oracle.qgemm(qtype, W, n, k, X)
@@ -269,7 +384,7 @@ def test_identity_x_returns_dequantized_weight(qtype):
 
 @pytest.mark.parametrize("qtype", QTYPES)
 def test_scaling_and_permutation(qtype):
-    n, k, T = 16, 128, 7
+    n, k, T = 16, _kk(qtype, 128), 7
     case = synth.make_case(qtype, n, k, T, seed=3)
     Y = oracle.qgemm(qtype, case["W"], n, k, case["X"])
     np.testing.assert_array_equal(oracle.qgemm(qtype, case["W"], n, k, 2 * case["X"]), 2 * Y)
@@ -391,6 +506,8 @@ def test_ffn_sublayer_special_cases():
 
 def _block_values(raw, qtype, n, k):
     """Dequantized weight from the raw bytes, by the block rules (struct parse)."""
+    if qtype == synth.Q4_K:
+        return np.array([[float(v) for v in _q4_k_row_independent(bytes(raw[i]), k)] for i in range(n)])
     if qtype == synth.F16:
         return np.array([struct.unpack("<%de" % k, bytes(raw[i])) for i in range(n)], dtype=np.float64)
     bb = 18 if qtype == synth.Q4_0 else 34
@@ -413,7 +530,7 @@ def _block_values(raw, qtype, n, k):
 def test_ffn_sublayer_brute_force(qtype):
     """Element-by-element loops (struct block parsing, math.sqrt, math.exp)
     against the oracle's array form."""
-    hidden, inter, T, eps = 32, 64, 2, 1e-5
+    hidden, inter, T, eps = _kk(qtype, 32), _kk(qtype, 64), 2, 1e-5
     X = synth.activations(T, hidden, 7).astype(np.float64)
     w = synth.activations(1, hidden, 8)[0].astype(np.float64)
     raw = {}
@@ -441,7 +558,7 @@ def test_normed_projection_reduces_to_projection(qtype):
     """Rows of +-1 have mean square 1, so with eps = 0 and unit weight the norm
     is the identity and the normed projection is the plain one (pinned above
     by brute force); a weight of 2 doubles it."""
-    n, k, T = 40, 96, 5
+    n, k, T = 40, _kk(qtype, 96), 5
     c = synth.make_case(qtype, n, k, T, residual=True, seed=12)
     X = np.where(synth.activations(T, k, 13) >= 0, 1.0, -1.0).astype(np.float32)
     ones = np.ones(k, np.float32)
