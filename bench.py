@@ -583,7 +583,7 @@ def projection_rate(q, dev, stream, peak_tf, peak_gbs, *, qtype, n, k, T, residu
     2 T n k (x2 for gate/up), bytes = the quantized weight(s) + X + Y (+ R)."""
     import torch
 
-    bb = {1: 64, 2: 18, 8: 34}[qtype]  # bytes per 32 weights (F16, Q4_0, Q8_0)
+    bb = {1: 64, 2: 18, 8: 34, 12: 18}[qtype]  # bytes per 32 weights (F16, Q4_0, Q8_0, Q4_K)
     wbytes = n * (k // 32) * bb * (2 if gate_up else 1)
     byts = wbytes + 4 * T * k + 4 * T * n * (2 if residual else 1)
     nsets = int(min(16, max(2, -(-2.5 * L2_BYTES // byts))))
@@ -628,10 +628,11 @@ def every_workload(q, dev, stream, peak_tf, peak_gbs):
       gate/up 12288 x 4096, down 4096 x 12288 + R, Q4_0) at 512 and 2048 rows
       on the fp16 leg and the exact-fp32 leg;
     * F16 weights: 4096 x 4096 + R at 512 tokens on both legs, gate/up 12288 x
-      4096 at 512 tokens, and the GEMV at T = 1 and 4."""
+      4096 at 512 tokens, and the GEMV at T = 1 and 4;
+    * Q4_K weights: the same five workloads."""
     import torch
 
-    F16, Q4, Q8 = 1, 2, 8
+    F16, Q4, Q8, Q4K = 1, 2, 8, 12
     P = lambda **kw: projection_rate(q, dev, stream, peak_tf, peak_gbs, **kw)  # noqa: E731
     out = {}
     out["q8_0_n256_k512_t16"] = {"auto (T rule: the GEMM)": P(qtype=Q8, n=256, k=512, T=16),
@@ -665,13 +666,14 @@ def every_workload(q, dev, stream, peak_tf, peak_gbs):
                 "down_n4096_k12288_res": P(qtype=Q4, n=4096, k=12288, T=T, residual=True, leg=leg, seed=13),
             }
     out["layer_9b_q4_0"] = layer
-    out["f16"] = {
-        "n4096_k4096_t512_res": P(qtype=F16, n=4096, k=4096, T=512, residual=True),
-        "n4096_k4096_t512_res_exact": P(qtype=F16, n=4096, k=4096, T=512, residual=True, leg=1),
-        "swiglu_n12288_k4096_t512": P(qtype=F16, n=12288, k=4096, T=512, gate_up=True),
-        "gemv_n4096_k4096_t1": P(qtype=F16, n=4096, k=4096, T=1),
-        "gemv_n4096_k4096_t4": P(qtype=F16, n=4096, k=4096, T=4),
-    }
+    for qt, name in ((F16, "f16"), (Q4K, "q4_k")):
+        out[name] = {
+            "n4096_k4096_t512_res": P(qtype=qt, n=4096, k=4096, T=512, residual=True),
+            "n4096_k4096_t512_res_exact": P(qtype=qt, n=4096, k=4096, T=512, residual=True, leg=1),
+            "swiglu_n12288_k4096_t512": P(qtype=qt, n=12288, k=4096, T=512, gate_up=True),
+            "gemv_n4096_k4096_t1": P(qtype=qt, n=4096, k=4096, T=1),
+            "gemv_n4096_k4096_t4": P(qtype=qt, n=4096, k=4096, T=4),
+        }
     torch.cuda.empty_cache()
     return out
 

@@ -151,6 +151,13 @@ def _dequant_q4_k(W: np.ndarray, n: int, k: int) -> np.ndarray:
     return w.reshape(n, k)
 
 
+def _row_bytes(qtype: int, k: int) -> int:
+    """Bytes of one weight row of k elements."""
+    if qtype in _SUPER_BYTES:
+        return k // _QK_K * _SUPER_BYTES[qtype]
+    return k // _QK * _BLOCK_BYTES[qtype]
+
+
 def _blocks(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
     if qtype not in _BLOCK_BYTES:
         raise ValueError(f"unsupported qtype {qtype}")
@@ -372,8 +379,7 @@ def prefill_layer_f64(qtype: int, X, attn_norm, ffn_norm, eps: float, Wqkv, Wo, 
     X64 = _as_f64(X).reshape(-1, hidden)
     T = X64.shape[0]
     qd, kvd = num_heads * head_dim, num_kv_heads * head_dim
-    bb = _BLOCK_BYTES[qtype]
-    row_bytes = hidden // _QK * bb
+    row_bytes = _row_bytes(qtype, hidden)
     Wqkv_b = np.ascontiguousarray(Wqkv, dtype=np.uint8).reshape(-1)
     Wq = Wqkv_b[:qd * row_bytes]
     Wk = Wqkv_b[qd * row_bytes:(qd + kvd) * row_bytes]

@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libapr_qgemm.so")
 APR_F16 = 1
 APR_Q4_0 = 2
 APR_Q8_0 = 8
+APR_Q4_K = 12
 APR_LEG_F16 = 0
 APR_LEG_EXACT_F32 = 1
 APR_PATH_AUTO = 0
@@ -37,7 +38,7 @@ APR_AUTO_GEMV_MAX_T = 4
 APR_NOALLOC_MAX_TK = 8 * 1024 * 1024
 APR_FFN_CHUNK_ROWS = 2048
 
-BLOCK_BYTES = {APR_F16: 64, APR_Q4_0: 18, APR_Q8_0: 34}  # bytes per 32 weights
+BLOCK_BYTES = {APR_F16: 64, APR_Q4_0: 18, APR_Q8_0: 34, APR_Q4_K: 18}  # bytes per 32 weights
 
 # Every symbol include/apr_qgemm.h declares.
 EXPORTS = (

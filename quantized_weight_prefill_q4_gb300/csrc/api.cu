@@ -178,12 +178,14 @@ struct Problem {
 
 int ldy_of(const Problem& p) { return p.ldy > 0 ? p.ldy : p.n; }
 
-bool known_qtype(int q) { return q == APR_Q4_0 || q == APR_Q8_0 || q == APR_F16; }
+bool known_qtype(int q) { return q == APR_Q4_0 || q == APR_Q8_0 || q == APR_F16 || q == APR_Q4_K; }
+// k (the columns of every weight row) a whole number of the format's blocks
+bool k_fits(int qtype, int k) { return k > 0 && k % (qtype == APR_Q4_K ? 256 : 32) == 0; }
 
-// a streaming GEMV kernel (integer-dot, whole-row, bulk or tensor-core) takes the shape
+// a streaming GEMV kernel (integer-dot, whole-row, bulk, tensor-core or the Q4_K one) takes the shape
 bool gemv_streams(int qtype, int n, int k, int T, bool swiglu) {
-  return gemv_i8_fits(qtype, n, k, T, swiglu) || gemv_rows_fits(qtype, n, k, T, swiglu) ||
-         gemv_bulk_fits(qtype, k, T, swiglu) || (!swiglu && qtype != APR_F16 && gemv_tc_takes(n, k, T, false));
+  return qtype == APR_Q4_K || gemv_i8_fits(qtype, n, k, T, swiglu) || gemv_rows_fits(qtype, n, k, T, swiglu) ||
+         gemv_bulk_fits(qtype, k, T, swiglu) || (!swiglu && block32_format(qtype) && gemv_tc_takes(n, k, T, false));
 }
 
 // Host-side checks; returns APR_OK, an error, or 1 for "nothing to do".
@@ -192,8 +194,9 @@ int check(const Problem& p, size_t x_elem_bytes = 4) {
   if (p.leg != APR_LEG_F16 && p.leg != APR_LEG_EXACT_F32) return fail(APR_E_INVAL, "unknown leg %d", p.leg);
   if (p.path != APR_PATH_AUTO && p.path != APR_PATH_GEMV && p.path != APR_PATH_GEMM)
     return fail(APR_E_INVAL, "unknown path %d", p.path);
-  if (p.n < 0 || p.T < 0 || p.k <= 0 || p.k % 32 != 0)
-    return fail(APR_E_INVAL, "bad sizes n=%d k=%d T=%d (need n >= 0, T >= 0, k > 0, k %% 32 == 0)", p.n, p.k, p.T);
+  if (p.n < 0 || p.T < 0 || !k_fits(p.qtype, p.k))
+    return fail(APR_E_INVAL, "bad sizes n=%d k=%d T=%d (need n >= 0, T >= 0, k > 0, k a multiple of %d)", p.n, p.k,
+                p.T, p.qtype == APR_Q4_K ? 256 : 32);
   if (p.n > (1 << 24) || p.T > (1 << 24) || p.k > (1 << 20) || (int64_t)p.n * (p.k / 32) > (int64_t)1 << 31)
     return fail(APR_E_INVAL, "sizes beyond the supported limits");
   if (p.ldy < 0 || (p.ldy > 0 && p.ldy < p.n) || p.ldy > (1 << 28))
@@ -246,7 +249,7 @@ int run(const Problem& p) {
   }
   if (path == APR_PATH_GEMV) {
     // the tensor-core GEMV multiplies integer codes: block formats only
-    if (p.qtype == APR_F16 || !gemv_tc_takes(p.n, p.k, p.T, p.Wu != nullptr))
+    if (!block32_format(p.qtype) || !gemv_tc_takes(p.n, p.k, p.T, p.Wu != nullptr))
       return launched(launch_gemv(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, ldy_of(p), p.R, st->status, p.s),
                       "gemv");
     // tensor-core GEMV: the stream's scratch holds its split X, scales and
@@ -314,9 +317,9 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 int run_ffn(const apr_ffn_args& a) {
   if (!known_qtype(a.qtype)) return fail(APR_E_QTYPE, "unsupported qtype %d", a.qtype);
   if (a.leg != APR_LEG_F16 && a.leg != APR_LEG_EXACT_F32) return fail(APR_E_INVAL, "unknown leg %d", a.leg);
-  if (a.hidden <= 0 || a.inter <= 0 || a.hidden % 32 != 0 || a.inter % 32 != 0 || a.T < 0)
-    return fail(APR_E_INVAL, "bad sizes hidden=%d inter=%d T=%d (need multiples of 32, T >= 0)", a.hidden, a.inter,
-                a.T);
+  if (!k_fits(a.qtype, a.hidden) || !k_fits(a.qtype, a.inter) || a.T < 0)
+    return fail(APR_E_INVAL, "bad sizes hidden=%d inter=%d T=%d (need multiples of %d, T >= 0)", a.hidden, a.inter,
+                a.T, a.qtype == APR_Q4_K ? 256 : 32);
   if (a.hidden > (1 << 20) || a.inter > (1 << 20) || a.T > (1 << 24) ||
       (int64_t)a.hidden * (a.inter / 32) > (int64_t)1 << 31)
     return fail(APR_E_INVAL, "sizes beyond the supported limits");
@@ -430,7 +433,7 @@ int run_layer(const apr_layer_args& a) {
   if (!known_qtype(a.qtype)) return fail(APR_E_QTYPE, "unsupported qtype %d", a.qtype);
   if (a.leg != APR_LEG_F16 && a.leg != APR_LEG_EXACT_F32) return fail(APR_E_INVAL, "unknown leg %d", a.leg);
   if (a.head_dim != 256) return fail(APR_E_INVAL, "head_dim must be 256 (got %d)", a.head_dim);
-  if (a.hidden <= 0 || a.inter <= 0 || a.hidden % 32 != 0 || a.inter % 32 != 0 || a.T < 0 || a.pos0 < 0 ||
+  if (!k_fits(a.qtype, a.hidden) || !k_fits(a.qtype, a.inter) || a.T < 0 || a.pos0 < 0 ||
       a.num_heads <= 0 || a.num_kv_heads <= 0 || a.chunk < 0)
     return fail(APR_E_INVAL, "bad sizes hidden=%d inter=%d T=%d pos0=%d heads=%d kv_heads=%d chunk=%d", a.hidden,
                 a.inter, a.T, a.pos0, a.num_heads, a.num_kv_heads, a.chunk);
@@ -681,7 +684,7 @@ int apr_prefill_attention(const float* Q, const float* K_cache, const float* V_c
 int apr_dequant(int qtype, const void* W, int n, int k, float* out, apr_stream_t stream) {
   t_msg[0] = 0;
   if (!known_qtype(qtype)) return fail(APR_E_QTYPE, "unsupported qtype %d", qtype);
-  if (n < 0 || k <= 0 || k % 32 != 0) return fail(APR_E_INVAL, "bad sizes n=%d k=%d", n, k);
+  if (n < 0 || !k_fits(qtype, k)) return fail(APR_E_INVAL, "bad sizes n=%d k=%d", n, k);
   if (n > (1 << 24) || k > (1 << 20) || (int64_t)n * (k / 32) > (int64_t)1 << 31)
     return fail(APR_E_INVAL, "sizes beyond the supported limits");
   if (n == 0) return APR_OK;

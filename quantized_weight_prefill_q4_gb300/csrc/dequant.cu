@@ -1,4 +1,5 @@
-// Standalone dequant: out[n][k] = f32(d) * f32(q') (F16: f32(w)), bit exact.
+// Standalone dequant: out[n][k] = f32(d) * f32(q') (F16: f32(w); Q4_K: d sc q -
+// dmin m rounded once), bit exact against the oracle.
 //
 // The device dequant of aprender-serve 0.70.2 src/cuda/executor/gdn_prefill_ops.rs
 // (qwen35_dequant_f32: one 32-element block per warp, one element per lane),
@@ -8,6 +9,7 @@
 #include <cuda_fp16.h>
 
 #include "apr_internal.h"
+#include "q4k.cuh"
 
 namespace apr {
 namespace {
@@ -22,6 +24,20 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
        idx += (size_t)gridDim.x * blockDim.x) {
     if constexpr (QT == kF16) {  // each element its own half: widening is exact
       out[idx] = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t*>(W)[idx]));
+      continue;
+    }
+    if constexpr (QT == kQ4_K) {  // superblock of 256 in 144 bytes
+      const size_t row = idx / (size_t)k;
+      const uint32_t col = (uint32_t)(idx - row * (size_t)k);
+      const uint8_t* sb = W + (row * (size_t)(k / 256) + col / 256) * 144;
+      const uint32_t e = col & 255u, g = e >> 6, hi = (e >> 5) & 1u, l = e & 31u, j = 2 * g + hi;
+      uint32_t sc, m;
+      q4k_scale_min(sb + 4, j, sc, m);
+      const float d = __half2float(__ushort_as_half((uint16_t)(sb[0] | (sb[1] << 8))));
+      const float dmin = __half2float(__ushort_as_half((uint16_t)(sb[2] | (sb[3] << 8))));
+      const uint32_t q = (sb[16 + 32 * g + l] >> (4 * hi)) & 15u;
+      // d sc and dmin m are exact in fp32; one rounding of d sc q - dmin m
+      out[idx] = fmaf(d * (float)sc, (float)q, -(dmin * (float)m));
       continue;
     }
     const size_t row = idx / (size_t)k;
@@ -47,7 +63,9 @@ cudaError_t launch_dequant(int qtype, const void* W, int n, int k, float* out, c
   const size_t total = (size_t)n * (size_t)k;
   size_t blocks = (total + 255) / 256;
   if (blocks > 152 * 64) blocks = 152 * 64;
-  if (qtype == kF16)
+  if (qtype == kQ4_K)
+    dequant_kernel<kQ4_K><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);
+  else if (qtype == kF16)
     dequant_kernel<kF16><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);
   else if (qtype == kQ4_0)
     dequant_kernel<kQ4_0><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);

@@ -76,6 +76,7 @@
 #include "apr_internal.h"
 #include "dev_common.cuh"
 #include "host_common.h"
+#include "q4k.cuh"
 
 namespace apr {
 namespace {
@@ -108,7 +109,11 @@ struct Cfg {
   static constexpr int DQ = NM == 1 ? 2 : 1;           // warpgroups per weight (alternate stages)
   static constexpr int NWG = NM * DQ;                   // dequant / epilogue warpgroups
   static constexpr bool F16W = QT == kF16;
-  static constexpr int BB = QT == kQ4_0 ? 18 : (QT == kQ8_0 ? 34 : 64);  // bytes per 32 k
+  static constexpr bool Q4W = QT == kQ4_0 || QT == kQ4_K;  // 144 bytes per row of a 256-k chunk
+  static constexpr int BB = Q4W ? 18 : (QT == kQ8_0 ? 34 : 64);  // bytes per 32 k
+  // words a decode thread reads per stage: two blocks, or for Q4_K the
+  // superblock's header and scales (4 words) and the stage's 32 code bytes
+  static constexpr int NWORDS = QT == kQ4_K ? 12 : 2 * BB / 4;
   // k per raw slot: a chunk, or half of one for an F16 gate/up pair (four
   // slots of 32 KB keep each weight double-buffered)
   static constexpr int RAW_K = F16W && NM == 2 ? CHUNK / 2 : CHUNK;
@@ -121,7 +126,7 @@ struct Cfg {
   static constexpr int RAW_BOX = F16W ? BK : RAW_ROW / 2;  // 16-bit elements across a box
   static constexpr int NPIECE = BN / PIECE;
   // operand stages (A in TMEM and B in shared memory advance together)
-  static constexpr int S = XS ? 2 : (NM == 2 ? 4 : (BN == 256 ? 4 : (QT == kQ4_0 ? 6 : (F16W ? 4 : 5))));
+  static constexpr int S = XS ? 2 : (NM == 2 ? 4 : (BN == 256 ? 4 : (Q4W ? 6 : (F16W ? 4 : 5))));
   // (with 256-token tiles the raw ring also receives the partner's half of a
   // split). With gate/up the chunks of the two weights alternate through the
   // ring, chunk j in slot j % S_RAW; S_RAW must be even so that a slot always
@@ -129,7 +134,7 @@ struct Cfg {
   // warpgroup. With an odd ring a warpgroup would wait on phase p + 2 of a slot
   // whose phase p + 1 belongs to the other warpgroup, and a parity wait cannot
   // tell phase p + 2 from phase p.
-  static constexpr int S_RAW = NM == 1 ? (QT == kQ4_0 ? (BN == 256 ? 4 : 3) : 2) : 4;
+  static constexpr int S_RAW = NM == 1 ? (Q4W ? (BN == 256 ? 4 : 3) : 2) : 4;
   static_assert(!XS || RAW_K == CHUNK, "the exact leg folds one raw slot per accumulation chunk");
   static_assert(!F16W || BN == 128, "F16 tiles take 128 tokens");
   static constexpr int NTHREADS = 128 + 128 * NWG;
@@ -312,6 +317,46 @@ __device__ __forceinline__ void dequant_row_stage_xs(const uint32_t* w, float sw
       for (int m = 0; m < 4; ++m) v[m] = (code((x >> (8 * m)) & 0xFFu) - 8388736.0f) * d;
       split2(v[0], v[1], a1[2 * c], a2[2 * c]);
       split2(v[2], v[3], a1[2 * c + 1], a2[2 * c + 1]);
+    }
+  }
+}
+
+// Q4_K: stage g (64 k) of one row's superblock, words w[0] = d | dmin << 16,
+// w[1..3] = the packed scales, w[4..11] = code bytes 32 g .. 32 g + 31:
+// a[j] for j < 16 the low nibbles (sub-block 2 g, elements 2j, 2j + 1), for
+// j >= 16 the high nibbles (sub-block 2 g + 1). Each weight d sc q - dmin m is
+// one fma of two exact products, rounded to fp32, then to fp16 (xs = false),
+// or times sw = 2^e and split into two fp16 pieces (xs = true).
+template <bool XSP>
+__device__ __forceinline__ void q4k_row_stage(const uint32_t* w, uint32_t g, float sw, uint32_t (&a1)[32],
+                                              uint32_t (&a2)[32]) {
+  const float d = __half2float(__ushort_as_half((unsigned short)(w[0] & 0xFFFFu)));
+  const float dmin = __half2float(__ushort_as_half((unsigned short)(w[0] >> 16)));
+  float A[2], B[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t sc, m;
+    q4k_scale_min_w(w + 1, 2 * g + h, sc, m);
+    A[h] = d * (float)sc;
+    B[h] = -(dmin * (float)m);
+  }
+  auto code = [](uint32_t c) { return __uint_as_float(c | 0x4B000000u) - 8388608.0f; };  // 0..15 exactly
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    const uint32_t x = w[4 + v];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float q[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) q[b] = fmaf(A[h], code((x >> (8 * b + 4 * h)) & 15u), B[h]);
+      const int j = 16 * h + 2 * v;
+      if constexpr (XSP) {
+        split2(q[0] * sw, q[1] * sw, a1[j], a2[j]);
+        split2(q[2] * sw, q[3] * sw, a1[j + 1], a2[j + 1]);
+      } else {
+        a1[j] = h2_as_u32(__floats2half2_rn(q[0], q[1]));
+        a1[j + 1] = h2_as_u32(__floats2half2_rn(q[2], q[3]));
+      }
     }
   }
 }
@@ -583,14 +628,21 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
       for (int s = par; s < C::RAW_SUBS; s += C::DQ) {
         const int i = c * C::RAW_SUBS + s;
         const int st = i % C::S;
-        uint32_t w[2 * C::BB / 4], a[32], a2[XS ? 32 : 1];
+        uint32_t w[C::NWORDS], a[32], a2[32];
         if constexpr (C::F16W) {
           f16_row_stage(raw_slot + s * (C::RAW_BYTES / C::RAW_LOADS), r, w);
+        } else if constexpr (QT == kQ4_K) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) w[v] = raw_row[v];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) w[4 + v] = raw_row[4 + 8 * s + v];
         } else {
 #pragma unroll
-          for (int v = 0; v < 2 * C::BB / 4; ++v) w[v] = raw_row[s * (2 * C::BB / 4) + v];
+          for (int v = 0; v < C::NWORDS; ++v) w[v] = raw_row[s * C::NWORDS + v];
         }
-        if constexpr (XS)
+        if constexpr (QT == kQ4_K)
+          q4k_row_stage<XS>(w, (uint32_t)s, sw, a, a2);  // overlaps the wait below
+        else if constexpr (XS)
           dequant_row_stage_xs<QT>(w, sw, a, a2);  // overlaps the wait below
         else if constexpr (C::F16W)
 #pragma unroll
@@ -956,6 +1008,29 @@ __global__ void row_exp_f16_kernel(const uint16_t* __restrict__ W, int n, int k,
   }
 }
 
+// Q4_K: the same exponent from a bound on the row's largest |w|, the largest
+// over its superblocks of |d| 63 x 15 + |dmin| 63 (every |d sc q - dmin m| is
+// at most that). One warp per row.
+__global__ void row_exp_q4k_kernel(const uint8_t* __restrict__ W, int n, int nsb, int* __restrict__ erow) {
+  const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= n) return;
+  const uint8_t* base = W + (size_t)row * nsb * 144;
+  float m = 0.f;
+  for (int b = lane; b < nsb; b += 32) {
+    const uint32_t h = *reinterpret_cast<const uint32_t*>(base + (size_t)b * 144);
+    const float d = fabsf(__half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu))));
+    const float dmin = fabsf(__half2float(__ushort_as_half((unsigned short)(h >> 16))));
+    m = fmaxf(m, d * 945.0f + dmin * 63.0f);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) {
+    int e = 0;
+    if (m > 0.f) e = 14 - ((int)((__float_as_uint(m) >> 23) & 0xFFu) - 127);
+    erow[row] = e;
+  }
+}
+
 // Per token row of X: the exponent e with max_j |x_j| 2^e in [2^14, 2^15)
 // (clamped to [-126, 126]; 0 for a zero row), then X1 = fp16(x 2^e) and
 // X2 = fp16(x 2^e - X1), both round to nearest even: X1 + X2 carries 22 of
@@ -1059,6 +1134,9 @@ int launch_gemm_xs(int qtype, const void* W, const void* Wu, int n, int k, const
   if (qtype == kF16) {
     row_exp_f16_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint16_t*>(W), n, k, erow);
     if (Wu) row_exp_f16_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint16_t*>(Wu), n, k, erow + n);
+  } else if (qtype == kQ4_K) {
+    row_exp_q4k_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(W), n, k / 256, erow);
+    if (Wu) row_exp_q4k_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(Wu), n, k / 256, erow + n);
   } else {
     row_exp_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(W), n, k / 32, bb, qmax, erow);
     if (Wu) row_exp_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(Wu), n, k / 32, bb, qmax, erow + n);
@@ -1070,6 +1148,7 @@ int launch_gemm_xs(int qtype, const void* W, const void* Wu, int n, int k, const
     return -1;
   }
   if (qtype == kF16) return launch_xs<kF16>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
+  if (qtype == kQ4_K) return launch_xs<kQ4_K>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
   return qtype == kQ4_0 ? launch_xs<kQ4_0>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len)
                         : launch_xs<kQ8_0>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
 }
@@ -1118,6 +1197,7 @@ int launch_gemm_tc(const GemmPlan& pl, int qtype, const void* W, const void* Wu,
                    size_t msg_len, int early, int x_rows) {
   const int w = early;
   if (qtype == kF16) return launch_q<kF16>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
+  if (qtype == kQ4_K) return launch_q<kQ4_K>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
   return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows)
                         : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
 }

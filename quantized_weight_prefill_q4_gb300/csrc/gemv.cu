@@ -1,4 +1,4 @@
-// Small-T GEMV over Q4_0 / Q8_0 blocks or F16 weights, exact fp32 arithmetic.
+// Small-T GEMV over Q4_0 / Q8_0 blocks, F16 or Q4_K weights, exact fp32 arithmetic.
 //
 // Y[t][i] = sum_j X[t][j] * d_{i,j/32} * q'_{i,j} (+ R[t][i]) for T <= 16 token
 // rows, or silu(g) * u for a gate/up pair. The single-token GEMVs of
@@ -21,6 +21,7 @@
 
 #include "apr_internal.h"
 #include "host_common.h"
+#include "q4k.cuh"
 
 namespace apr {
 namespace {
@@ -362,6 +363,132 @@ cudaError_t launch_f16(const void* W, const void* Wu, int n, int k, const float*
   return launch_f16_t<16, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
 }
 
+// Q4_K weights: a warp per weight row, one 256-element superblock (144 bytes)
+// a step; lane l takes elements 8 l .. 8 l + 7 of it: group g = l / 8 (64
+// elements), low nibbles of code bytes 32 g + 8 (l mod 4) .. for l mod 8 < 4
+// (sub-block 2 g), high nibbles of the same bytes otherwise (sub-block
+// 2 g + 1). Each weight is d sc q - dmin m rounded once to fp32 (one fma of
+// two exact products), then exact fp32 products with X. The loads of two
+// superblocks are issued before either is used.
+template <int TMAX, bool SWI>
+__global__ void __launch_bounds__(kWarps * 32) gemv_q4k_kernel(const uint8_t* __restrict__ W,
+                                                               const uint8_t* __restrict__ Wu, int n, int k,
+                                                               const float* __restrict__ X, int T, float* Y, int ldy,
+                                                               const float* R) {
+  constexpr int NM = SWI ? 2 : 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nsb = k / 256;
+  const size_t row_bytes = (size_t)nsb * 144;
+  const uint32_t g = (uint32_t)lane >> 3, part = (uint32_t)lane & 7u, hi = part >> 2, j = 2 * g + hi;
+  const uint32_t qoff = 16 + 32 * g + 8 * (part & 3u);
+  bool waited = false;
+  for (int row = blockIdx.x * kWarps + warp; row < n; row += gridDim.x * kWarps) {
+    float acc[NM][TMAX];
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) acc[m][t] = 0.f;
+    const uint8_t* base[NM];
+    base[0] = W + (size_t)row * row_bytes;
+    if (SWI) base[NM - 1] = Wu + (size_t)row * row_bytes;
+    for (int sb0 = 0; sb0 < nsb; sb0 += 2) {
+      uint4 h[2][NM];
+      uint2 c[2][NM];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int m = 0; m < NM; ++m)
+          if (sb0 + u < nsb) {
+            const uint8_t* sb = base[m] + (size_t)(sb0 + u) * 144;
+            h[u][m] = ldg_nc_v4(sb);
+            c[u][m] = __ldg(reinterpret_cast<const uint2*>(sb + qoff));
+          }
+      if (!waited) {
+        grid_dependency_wait_inline();
+        waited = true;
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (sb0 + u >= nsb) break;
+        float w[NM][8];
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+          const uint32_t sw[3] = {h[u][m].y, h[u][m].z, h[u][m].w};
+          uint32_t sc, mn;
+          q4k_scale_min_w(sw, j, sc, mn);
+          const float d = __half2float(__ushort_as_half((unsigned short)(h[u][m].x & 0xFFFFu)));
+          const float dmin = __half2float(__ushort_as_half((unsigned short)(h[u][m].x >> 16)));
+          const float a = d * (float)sc, b = -(dmin * (float)mn);
+          const uint32_t cw[2] = {c[u][m].x, c[u][m].y};
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            w[m][e] = fmaf(a, (float)((cw[e >> 2] >> (8 * (e & 3) + 4 * hi)) & 15u), b);
+        }
+        const int col = (sb0 + u) * 256 + 8 * lane;
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t) {
+          if (t < T) {
+            const float4* xr = reinterpret_cast<const float4*>(X + (size_t)t * k + col);
+            const float4 xa = __ldg(xr), xb = __ldg(xr + 1);
+            const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+            for (int m = 0; m < NM; ++m) {
+              float v = acc[m][t];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v = fmaf(w[m][e], xv[e], v);
+              acc[m][t] = v;
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        float v = acc[m][t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        acc[m][t] = v;
+      }
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+      if (lane == t && t < T) {
+        const size_t o = (size_t)t * ldy + row;
+        Y[o] = SWI ? silu_mul(acc[0][t], acc[NM - 1][t]) : acc[0][t] + (R ? R[o] : 0.f);
+      }
+    }
+  }
+  if (!waited) grid_dependency_wait_inline();  // a CTA without rows
+}
+
+template <int TMAX, bool SWI>
+cudaError_t launch_q4k_t(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
+                         const float* R, cudaStream_t s) {
+  long blocks = (n + kWarps - 1) / kWarps;
+  const long cap = (long)num_sms() * 2;
+  if (blocks > cap) blocks = cap;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemv_q4k_kernel<TMAX, SWI>, static_cast<const uint8_t*>(W),
+                            static_cast<const uint8_t*>(Wu), n, k, X, T, Y, ldy, R);
+}
+
+template <bool SWI>
+cudaError_t launch_q4k(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
+                       const float* R, cudaStream_t s) {
+  if (T <= 1) return launch_q4k_t<1, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 2) return launch_q4k_t<2, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 4) return launch_q4k_t<4, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 8) return launch_q4k_t<8, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  return launch_q4k_t<16, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+}
+
 }  // namespace
 
 cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
@@ -371,6 +498,8 @@ cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, 
   if (gemv_i8_fits(qtype, n, k, T, swi)) return launch_gemv_i8(qtype, W, Wu, n, k, X, Y, R, status, s);
   if (gemv_rows_fits(qtype, n, k, T, swi)) return launch_gemv_rows(qtype, W, Wu, n, k, X, T, Y, R, status, s);
   if (gemv_bulk_fits(qtype, k, T, swi)) return launch_gemv_bulk(qtype, W, Wu, n, k, X, T, Y, ldy, R, status, s);
+  if (qtype == kQ4_K)
+    return swi ? launch_q4k<true>(W, Wu, n, k, X, T, Y, ldy, R, s) : launch_q4k<false>(W, Wu, n, k, X, T, Y, ldy, R, s);
   if (qtype == kF16) {
     if (k % 256 == 0)
       return swi ? launch_f16<true>(W, Wu, n, k, X, T, Y, ldy, R, s) : launch_f16<false>(W, Wu, n, k, X, T, Y, ldy, R, s);

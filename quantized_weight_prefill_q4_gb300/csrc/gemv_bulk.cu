@@ -235,7 +235,7 @@ size_t gemv_bulk_smem(int qtype, int k, int T, bool swiglu) {
 }
 
 bool gemv_bulk_fits(int qtype, int k, int T, bool swiglu) {
-  if (qtype == kF16 || k % 256 != 0 || T < 1 || T > (swiglu ? 4 : 8)) return false;
+  if (!block32_format(qtype) || k % 256 != 0 || T < 1 || T > (swiglu ? 4 : 8)) return false;
   return gemv_bulk_smem(qtype, k, T, swiglu) <= 232448;
 }
 

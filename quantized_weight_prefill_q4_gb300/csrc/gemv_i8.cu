@@ -456,7 +456,7 @@ cudaError_t launch_read_stream(const void* src, long long bytes, unsigned* statu
 bool gemv_i8_fits(int qtype, int n, int k, int T, bool swiglu) {
   // block formats, one token; k % 256 == 0 (whole rows 16-byte aligned in a stage); a row's
   // warps within the consumer warps; at most IMAXROWS rows a CTA
-  if (qtype == kF16 || T != 1 || k % 256 != 0 || (k / 64 + 31) / 32 > 8) return false;
+  if (!block32_format(qtype) || T != 1 || k % 256 != 0 || (k / 64 + 31) / 32 > 8) return false;
   if ((n + num_sms() - 1) / num_sms() > IMAXROWS) return false;
   return rows_per_stage(qtype, k, swiglu) >= 1 && i8_stages(k) >= 4;
 }

@@ -242,7 +242,7 @@ bool gemv_rows_fits(int qtype, int n, int k, int T, bool swiglu) {
   // block formats, one token; a row's warps within the consumer warps; whole rows in a
   // stage, each starting on a 16-byte boundary (k % 256 == 0); at most
   // RMAXROWS rows a CTA
-  if (qtype == kF16 || T != 1 || k % 256 != 0 || (k / 64 + 63) / 64 > RNCW) return false;
+  if (!block32_format(qtype) || T != 1 || k % 256 != 0 || (k / 64 + 63) / 64 > RNCW) return false;
   if ((n + device_sms() - 1) / device_sms() > RMAXROWS) return false;
   return rows_per_stage(qtype, k, swiglu) >= 1 && gemv_rows_smem(qtype, k, T) <= 232448;
 }
