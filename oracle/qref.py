@@ -1,4 +1,4 @@
-"""Plain CPU oracle for the Q4_0 / Q8_0 / F16 / Q4_K prefill projections (float64).
+"""Plain CPU oracle for the Q4_0 / Q8_0 / F16 / Q4_K / Q5_K prefill projections (float64).
 
 TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import or call
@@ -31,7 +31,10 @@ What is computed, and where the pages define it:
   (``q4_k_scales_mins``), then 128 bytes of 4-bit codes: byte ``32 g + l``
   holds element ``64 g + l`` in its low nibble and ``64 g + 32 + l`` in its
   high nibble; element ``e`` of sub-block ``j = e / 32`` is
-  ``w = d sc_j q - dmin m_j``.
+  ``w = d sc_j q - dmin m_j``. Q5_K (176 bytes) likewise, with 32 bytes of
+  fifth code bits between the scales and the codes (bit ``2 g`` of byte ``l``
+  for element ``64 g + l``, bit ``2 g + 1`` for ``64 g + 32 + l``, each worth
+  16), the codes at bytes 48-175.
 * Projection ``Y[T][n] = X[T][k] . W[n][k]^T`` (aprender-serve 0.70.2
   src/cuda/executor/gdn_prefill_ops.rs, doc of ``qwen35_project_rows``),
   optionally ``+ R[T][n]`` (the residual add that follows the down / output
@@ -86,10 +89,11 @@ F16 = 1
 Q4_0 = 2
 Q8_0 = 8
 Q4_K = 12
+Q5_K = 13
 _QK = 32
 _QK_K = 256
 _BLOCK_BYTES = {F16: 64, Q4_0: 18, Q8_0: 34}
-_SUPER_BYTES = {Q4_K: 144}
+_SUPER_BYTES = {Q4_K: 144, Q5_K: 176}
 
 
 # --------------------------------------------------------------------------
@@ -139,13 +143,22 @@ def q4_k_scales_mins(scales: np.ndarray):
     return sc, mn
 
 
-def _dequant_q4_k(W: np.ndarray, n: int, k: int) -> np.ndarray:
-    sb = _superblocks(Q4_K, W, n, k)
+def _dequant_k(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
+    """Q4_K and Q5_K (the same header, scales and code bytes; Q5_K adds 32
+    bytes of fifth bits after the scales: bit 2 g of byte l for element
+    64 g + l, bit 2 g + 1 for element 64 g + 32 + l, worth 16)."""
+    sb = _superblocks(qtype, W, n, k)
     d = fp16_bits_to_f64(sb[..., 0].astype(np.uint16) | (sb[..., 1].astype(np.uint16) << 8))
     dmin = fp16_bits_to_f64(sb[..., 2].astype(np.uint16) | (sb[..., 3].astype(np.uint16) << 8))
     sc, mn = q4_k_scales_mins(sb[..., 4:16])
-    qs = sb[..., 16:].reshape(n, k // _QK_K, 4, 32)     # group g: bytes 32 g .. 32 g + 31
+    qoff = 16 if qtype == Q4_K else 48
+    qs = sb[..., qoff:].reshape(n, k // _QK_K, 4, 32).astype(np.int64)  # group g: bytes 32 g .. 32 g + 31
     q = np.concatenate([qs & 0x0F, qs >> 4], axis=-1)  # group g: 64 elements, low nibbles first
+    if qtype == Q5_K:
+        qh = sb[..., 16:48].astype(np.int64)[:, :, None, :]      # [.., 1, 32]
+        g = np.arange(4).reshape(1, 1, 4, 1)
+        hb = np.concatenate([(qh >> (2 * g)) & 1, (qh >> (2 * g + 1)) & 1], axis=-1)
+        q = q + 16 * hb
     q = q.reshape(n, k // _QK_K, 8, 32).astype(np.float64)  # sub-block j = 2 g + (high nibble)
     w = d[..., None, None] * sc[..., None] * q - dmin[..., None, None] * mn[..., None]
     return w.reshape(n, k)
@@ -193,8 +206,8 @@ def block_scales_and_codes(qtype: int, W: np.ndarray, n: int, k: int):
 def dequant_f64(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
     """``Wf[i][j] = fp16(d_{i, j/32}) * q'_{i,j}`` in float64, shape ``[n][k]``;
     for F16 the binary16 value of element ``(i, j)``."""
-    if qtype == Q4_K:
-        return _dequant_q4_k(W, n, k)
+    if qtype in _SUPER_BYTES:
+        return _dequant_k(qtype, W, n, k)
     if qtype == F16:
         raw = _blocks(qtype, W, n, k).reshape(n, k, 2)
         bits = raw[..., 0].astype(np.uint16) | (raw[..., 1].astype(np.uint16) << 8)
@@ -211,8 +224,8 @@ def dequant_f32(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
     float64 product is exact and so is its conversion to float32 (the range of
     an fp16 scale times 128 is well inside float32's normal range, and fp16
     subnormal scales times small integers stay exact in float32). Every fp16
-    value, subnormals included, is a float32 value. Q4_K: the exact float64
-    value ``d sc q - dmin m`` rounded once to float32.
+    value, subnormals included, is a float32 value. Q4_K and Q5_K: the exact
+    float64 value ``d sc q - dmin m`` rounded once to float32.
     """
     return dequant_f64(qtype, W, n, k).astype(np.float32)
 

@@ -13,6 +13,7 @@ from .gen import (  # noqa: F401
     Q4_0,
     Q8_0,
     Q4_K,
+    Q5_K,
     BLOCK_ELEMS,
     block_bytes,
     quantize,
@@ -20,6 +21,7 @@ from .gen import (  # noqa: F401
     quantize_q8_0,
     quantize_f16,
     quantize_q4_k,
+    quantize_q5_k,
     weight_f32,
     activations,
     make_case,

@@ -39,8 +39,10 @@ F16 = 1   # GGUF type id
 Q4_0 = 2  # GGUF type id
 Q8_0 = 8  # GGUF type id
 Q4_K = 12  # GGUF type id (256-element superblocks of 144 bytes)
+Q5_K = 13  # GGUF type id (256-element superblocks of 176 bytes)
 BLOCK_ELEMS = 32
-_BLOCK_BYTES = {F16: 64, Q4_0: 18, Q8_0: 34, Q4_K: 18}
+_BLOCK_BYTES = {F16: 64, Q4_0: 18, Q8_0: 34, Q4_K: 18, Q5_K: 22}
+_SUPER_BYTES = {Q4_K: 144, Q5_K: 176}
 
 
 def block_bytes(qtype: int) -> int:
@@ -121,12 +123,24 @@ def quantize_q4_k(w: np.ndarray) -> np.ndarray:
     dmin are the largest of them over 63 (stored as fp16), the 6-bit
     sub-scales round(scale / d) and round(min / dmin), and each code
     round((w + dmin m) / (d sc)) clamped to 0..15."""
+    return _quantize_k(w, 4)
+
+
+def quantize_q5_k(w: np.ndarray) -> np.ndarray:
+    """Q5_K superblocks ``[n][k/256*176]`` the same way with codes 0..31 (scale
+    (hi - lo) / 31): the low four bits as Q4_K's code bytes, the fifth bits in
+    the 32 bytes after the scales."""
+    return _quantize_k(w, 5)
+
+
+def _quantize_k(w: np.ndarray, bits: int) -> np.ndarray:
+    top = (1 << bits) - 1
     w = np.ascontiguousarray(w, dtype=np.float32).astype(np.float64)
     n, k = w.shape
     x = w.reshape(n, k // 256, 8, 32)
     lo = np.minimum(x.min(axis=-1), 0.0)
     hi = np.maximum(x.max(axis=-1), 0.0)
-    scale = (hi - lo) / 15.0
+    scale = (hi - lo) / top
     mins = -lo
     d = scale.max(axis=-1) / 63.0
     dmin = mins.max(axis=-1) / 63.0
@@ -141,13 +155,21 @@ def quantize_q4_k(w: np.ndarray) -> np.ndarray:
     step = df[..., None] * sc
     q = np.where(step[..., None] > 0,
                  np.rint((x + (dmf[..., None] * mn)[..., None]) / np.where(step > 0, step, 1.0)[..., None]), 0)
-    q = np.clip(q, 0, 15).astype(np.uint8).reshape(n, k // 256, 4, 2, 32)
-    qs = (q[:, :, :, 0, :] | (q[:, :, :, 1, :] << 4)).reshape(n, k // 256, 128)
-    out = np.zeros((n, k // 256, 144), np.uint8)
+    q = np.clip(q, 0, top).astype(np.uint8).reshape(n, k // 256, 4, 2, 32)
+    qs = ((q[:, :, :, 0, :] & 15) | ((q[:, :, :, 1, :] & 15) << 4)).reshape(n, k // 256, 128)
+    out = np.zeros((n, k // 256, 144 if bits == 4 else 176), np.uint8)
     out[..., 0:2] = d16.view(np.uint16)[..., None].view(np.uint8).reshape(n, k // 256, 2)
     out[..., 2:4] = dmin16.view(np.uint16)[..., None].view(np.uint8).reshape(n, k // 256, 2)
     out[..., 4:16] = _pack_q4_k_scales(sc, mn)
-    out[..., 16:] = qs
+    if bits == 4:
+        out[..., 16:] = qs
+    else:
+        qh = np.zeros((n, k // 256, 32), np.uint8)
+        for g in range(4):
+            qh |= ((q[:, :, g, 0, :] >> 4) << (2 * g)).astype(np.uint8)
+            qh |= ((q[:, :, g, 1, :] >> 4) << (2 * g + 1)).astype(np.uint8)
+        out[..., 16:48] = qh
+        out[..., 48:] = qs
     return out.reshape(n, -1)
 
 
@@ -156,6 +178,8 @@ def quantize(qtype: int, w: np.ndarray) -> np.ndarray:
         return quantize_f16(w)
     if qtype == Q4_K:
         return quantize_q4_k(w)
+    if qtype == Q5_K:
+        return quantize_q5_k(w)
     if qtype == Q4_0:
         return quantize_q4_0(w)
     if qtype == Q8_0:
@@ -198,14 +222,14 @@ def random_blocks(qtype: int, n: int, k: int, seed: int, scale_class: str = "mix
     gives |d| <= 8188 or 511.75.
     """
     lo, hi = SCALE_CLASSES[scale_class]
-    if qtype == Q4_K:
+    if qtype in _SUPER_BYTES:
         # random bytes; d and dmin of both signs drawn from the class
         rng = np.random.default_rng(seed)
-        raw = rng.integers(0, 256, size=(n, k // 256, 144), dtype=np.uint8)
+        raw = rng.integers(0, 256, size=(n, k // 256, _SUPER_BYTES[qtype]), dtype=np.uint8)
         for off in (0, 2):
             exp = rng.integers(lo, hi + 1, size=(n, k // 256)).astype(np.uint16)
-            if fp16_range:  # |d sc q| and |dmin m| within fp16's range: |d| < 2^6 (63 x 15 x 2^6 < 65504)
-                exp = np.minimum(exp, 20)
+            if fp16_range:  # |d sc q| within fp16's range: |d| < 2^5 (63 x 31 x 2^5 < 65504)
+                exp = np.minimum(exp, 19)
             man = rng.integers(0, 1024, size=(n, k // 256)).astype(np.uint16)
             man = np.where(exp == 0, np.maximum(man, 1), man)
             sign = rng.integers(0, 2, size=(n, k // 256)).astype(np.uint16)

@@ -23,12 +23,13 @@ import oracle
 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-QTYPES = [synth.Q4_0, synth.Q8_0, synth.F16, synth.Q4_K]
+QTYPES = [synth.Q4_0, synth.Q8_0, synth.F16, synth.Q4_K, synth.Q5_K]
+KQ = (synth.Q4_K, synth.Q5_K)
 
 
 def _kk(qtype, k):
     """k as given, or widened to whole 256-element superblocks for Q4_K."""
-    return max(256, k // 256 * 256) if qtype == synth.Q4_K else k
+    return max(256, k // 256 * 256) if qtype in KQ else k
 
 
 def load_golden(name):
@@ -167,6 +168,52 @@ def test_q4_k_codes_in_element_order():
     np.testing.assert_array_equal(oracle.dequant_f64(synth.Q4_K, raw, 1, 256)[0], np.array(q, np.float64))
 
 
+def _q5_k_superblock(d_bits, dmin_bits, sc, mn, q):
+    """Q5_K bytes: the Q4_K header and scales, the fifth bits of the codes
+    (bit 2 g of byte l for element 64 g + l, bit 2 g + 1 for 64 g + 32 + l),
+    then the low four bits as Q4_K's code bytes."""
+    k4 = _q4_k_superblock(d_bits, dmin_bits, sc, mn, [v & 15 for v in q])
+    qh = bytearray(32)
+    for g in range(4):
+        for l in range(32):
+            qh[l] |= ((q[64 * g + l] >> 4) << (2 * g)) | ((q[64 * g + 32 + l] >> 4) << (2 * g + 1))
+    return k4[:16] + bytes(qh) + k4[16:]
+
+
+def test_q5_k_without_fifth_bits_equals_q4_k():
+    rng = np.random.default_rng(23)
+    sc = [int(v) for v in rng.integers(0, 64, size=8)]
+    mn = [int(v) for v in rng.integers(0, 64, size=8)]
+    q = [int(v) for v in rng.integers(0, 16, size=256)]
+    k4 = np.frombuffer(_q4_k_superblock(0x2C00, 0x2800, sc, mn, q), np.uint8).reshape(1, 144)
+    k5 = np.frombuffer(_q5_k_superblock(0x2C00, 0x2800, sc, mn, q), np.uint8).reshape(1, 176)
+    np.testing.assert_array_equal(oracle.dequant_f64(synth.Q5_K, k5, 1, 256), oracle.dequant_f64(synth.Q4_K, k4, 1, 256))
+
+
+def test_q5_k_fifth_bits_land_on_their_elements():
+    # d = 1, dmin = 0, unit scales, low bits zero: element e is 16 x its fifth bit
+    rng = np.random.default_rng(24)
+    hb = [int(v) for v in rng.integers(0, 2, size=256)]
+    raw = np.frombuffer(_q5_k_superblock(0x3C00, 0x0000, [1] * 8, [0] * 8, [16 * b for b in hb]), np.uint8)
+    np.testing.assert_array_equal(oracle.dequant_f64(synth.Q5_K, raw.reshape(1, 176), 1, 256)[0],
+                                  16.0 * np.array(hb, np.float64))
+    # and the codes 0 .. 31 in element order
+    q = [e % 32 for e in range(256)]
+    raw = np.frombuffer(_q5_k_superblock(0x3C00, 0x0000, [1] * 8, [0] * 8, q), np.uint8).reshape(1, 176)
+    np.testing.assert_array_equal(oracle.dequant_f64(synth.Q5_K, raw, 1, 256)[0], np.array(q, np.float64))
+
+
+def test_q5_k_encoder_round_trip():
+    n, k = 16, 512
+    w = synth.weight_f32(n, k, seed=4)
+    W = synth.quantize(synth.Q5_K, w)
+    assert W.shape == (n, k // 256 * 176) and synth.block_bytes(synth.Q5_K) * (k // 32) == W.shape[1]
+    err = np.abs(oracle.dequant_f64(synth.Q5_K, W, n, k) - w.astype(np.float64)).reshape(n, k // 256, 8, 32)
+    rng_ = w.reshape(n, k // 256, 8, 32)
+    step = (np.maximum(rng_.max(-1), 0) - np.minimum(rng_.min(-1), 0)) / 31.0
+    assert np.all(err.max(-1) <= 0.75 * step + 0.01 * np.abs(w).max())
+
+
 def test_q4_k_encoder_round_trip_and_sizes():
     n, k = 16, 512
     w = synth.weight_f32(n, k, seed=4)
@@ -247,8 +294,8 @@ def _parse_block_independent(qtype, blk: bytes):
 def _random_blocks(rng, qtype, n, k):
     """Random raw bytes with finite scales (exponent field kept below 31); for
     F16 every element is such a half; for Q4_K d and dmin of every superblock."""
-    if qtype == synth.Q4_K:
-        raw = rng.integers(0, 256, size=(n, k // 256, 144), dtype=np.uint8)
+    if qtype in KQ:
+        raw = rng.integers(0, 256, size=(n, k // 256, 144 if qtype == synth.Q4_K else 176), dtype=np.uint8)
         for b in (1, 3):
             raw[..., b] = np.where((raw[..., b] & 0x7C) == 0x7C, raw[..., b] & 0xBF, raw[..., b])
         return raw.reshape(n, -1)
@@ -263,12 +310,15 @@ def _random_blocks(rng, qtype, n, k):
     return raw.reshape(n, -1)
 
 
-def _q4_k_row_independent(raw: bytes, k):
-    """Exact values of one Q4_K row, element by element with struct (the
-    layout read in the oracle's header, written out here as plain loops)."""
+def _q4_k_row_independent(raw: bytes, k, five=False):
+    """Exact values of one Q4_K (Q5_K: five=True) row, element by element with
+    struct (the layout read in the oracle's header, written out here as plain
+    loops)."""
     out = []
+    sbb = 176 if five else 144
+    qoff = 48 if five else 16
     for sb in range(k // 256):
-        blk = raw[144 * sb:144 * (sb + 1)]
+        blk = raw[sbb * sb:sbb * (sb + 1)]
         d = Fraction(struct.unpack("<e", blk[0:2])[0])
         dmin = Fraction(struct.unpack("<e", blk[2:4])[0])
         s = blk[4:16]
@@ -281,8 +331,10 @@ def _q4_k_row_independent(raw: bytes, k):
                 m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4)
             g, hi = j // 2, j % 2
             for l in range(32):
-                byte = blk[16 + 32 * g + l]
+                byte = blk[qoff + 32 * g + l]
                 q = (byte >> 4) if hi else (byte & 15)
+                if five:
+                    q += 16 * ((blk[16 + l] >> (2 * g + hi)) & 1)
                 vals[64 * g + 32 * hi + l] = d * sc * q - dmin * m
         out.extend(vals)
     return out
@@ -292,8 +344,8 @@ def _exact_qgemm(qtype, W, n, k, X, R):
     bb = synth.block_bytes(qtype)
     rows = []
     for i in range(n):
-        if qtype == synth.Q4_K:
-            rows.append(_q4_k_row_independent(bytes(W[i]), k))
+        if qtype in KQ:
+            rows.append(_q4_k_row_independent(bytes(W[i]), k, five=qtype == synth.Q5_K))
             continue
         wrow = []
         for b in range(k // 32):
@@ -349,7 +401,7 @@ def test_brute_force_dequant_exact(qtype):
     got = oracle.dequant_f32(qtype, W, n, k)
     for i in range(n):
         for j in range(k):
-            if qtype == synth.Q4_K:  # d sc q - dmin m may need more than 24 bits: rounded once
+            if qtype in KQ:  # d sc q - dmin m may need more than 24 bits: rounded once
                 assert abs(Fraction(float(got[i, j])) - rows[i][j]) <= Fraction(_ulp32(float(got[i, j]))) / 2
             else:
                 assert Fraction(float(got[i, j])) == rows[i][j]
@@ -506,8 +558,9 @@ def test_ffn_sublayer_special_cases():
 
 def _block_values(raw, qtype, n, k):
     """Dequantized weight from the raw bytes, by the block rules (struct parse)."""
-    if qtype == synth.Q4_K:
-        return np.array([[float(v) for v in _q4_k_row_independent(bytes(raw[i]), k)] for i in range(n)])
+    if qtype in KQ:
+        return np.array([[float(v) for v in _q4_k_row_independent(bytes(raw[i]), k, five=qtype == synth.Q5_K)]
+                         for i in range(n)])
     if qtype == synth.F16:
         return np.array([struct.unpack("<%de" % k, bytes(raw[i])) for i in range(n)], dtype=np.float64)
     bb = 18 if qtype == synth.Q4_0 else 34
