@@ -1,6 +1,6 @@
 /*
  * apr_qgemm.h — C ABI of the GB300 (sm_103a) prefill projections over GGUF
- * Q4_0 / Q8_0 / Q4_K block-quantized weights and F16 weights.
+ * Q4_0 / Q8_0 / Q4_K / Q5_K block-quantized weights and F16 weights.
  *
  * Every projection of a batched (chunked) prompt prefill is ONE product over
  * the chunk's T token rows, instead of T per-token GEMVs:
@@ -37,6 +37,12 @@
  *                    then 128 code bytes: byte 32g + l holds element 64g + l
  *                    (low nibble) and 64g + 32 + l (high nibble);
  *                    w = d * sc_j * q - dmin * m_j for element e, j = e / 32.
+ *   Q5_K (176 bytes per 256 weights, k % 256 == 0): also dispatched by the
+ *                    pages without a printed layout; taken as the GGUF
+ *                    superblock: the first 16 bytes as in Q4_K, then 32 bytes
+ *                    of fifth code bits (bit 2g + h of byte l is the fifth
+ *                    bit, worth 16, of element 64g + 32h + l), then the 128
+ *                    code bytes as in Q4_K; q in 0..31, w as for Q4_K.
  * Row i of W is the k/32 consecutive blocks starting at byte i*(k/32)*bytes.
  *
  * Memory and streams. Every pointer argument named W, Wu, X, residual, Y or
@@ -63,10 +69,10 @@
  *
  * Errors. Arguments are checked on the host before anything is enqueued:
  *   APR_E_INVAL   null pointer with nonzero sizes, n < 0, T < 0, k <= 0,
- *                 k % 32 != 0 (k % 256 != 0 for Q4_K), a size beyond the
+ *                 k % 32 != 0 (k % 256 != 0 for Q4_K, Q5_K), a size beyond the
  *                 documented limits, or an
  *                 unknown leg / path
- *   APR_E_QTYPE   qtype is not APR_Q4_0, APR_Q8_0, APR_F16 or APR_Q4_K
+ *   APR_E_QTYPE   qtype is not APR_Q4_0, APR_Q8_0, APR_F16, APR_Q4_K or APR_Q5_K
  *   APR_E_ALIGN   a pointer is not 16-byte aligned
  *   APR_E_ALIAS   Y overlaps X, W or Wu, or overlaps residual without being
  *                 exactly the same buffer (Y == residual is allowed: it gives
@@ -102,7 +108,7 @@ extern "C" {
 typedef struct CUstream_st* apr_stream_t;
 
 /* GGUF tensor type ids. */
-enum { APR_F16 = 1, APR_Q4_0 = 2, APR_Q8_0 = 8, APR_Q4_K = 12 };
+enum { APR_F16 = 1, APR_Q4_0 = 2, APR_Q8_0 = 8, APR_Q4_K = 12, APR_Q5_K = 13 };
 
 /*
  * Arithmetic legs (aprender-serve gdn_prefill_ops.rs, module doc, group 1):
@@ -148,7 +154,7 @@ int apr_gemv_max_T(void);
 
 /*
  * Y = X . dequant(W)^T (+ residual), fp16 leg, T rule.
- *   qtype     APR_Q4_0, APR_Q8_0, APR_F16 or APR_Q4_K
+ *   qtype     APR_Q4_0, APR_Q8_0, APR_F16, APR_Q4_K or APR_Q5_K
  *   W         [n rows][k/32 blocks] GGUF blocks
  *   X         [T][k] f32;  Y [T][n] f32, overwritten
  *   residual  [T][n] f32 or NULL; may be Y itself (accumulate)
@@ -176,8 +182,8 @@ int apr_qgemm_gate_up_swiglu(int qtype, const void* Wg, const void* Wu, int n, i
  * arithmetic, optional residual (gemv_q4_0_pf / gemv_q8_0_pf of
  * oxibonsai-kernels, used for the last-token lm_head in
  * try_cuda_prefill_q_std). For T <= 8 weight rows stream by bulk copies into
- * T fp32 accumulators (tensor cores for T = 3, 4 with Q4_0 / Q8_0; F16 and
- * Q4_K weights always on the CUDA cores); for 9 <= T <= 16, and for smaller T
+ * T fp32 accumulators (tensor cores for T = 3, 4 with Q4_0 / Q8_0; F16,
+ * Q4_K and Q5_K weights always on the CUDA cores); for 9 <= T <= 16, and for smaller T
  * where no streaming kernel takes the shape (the X table of a long row does
  * not fit shared memory), the exact leg's tensor-core GEMM runs instead when
  * k % 256 == 0 (49-57 us at 4096 x 4096 and 12288 x 4096, against 50 to 700
@@ -292,7 +298,7 @@ int apr_qgemm_rmsnorm(const apr_qgemm_args* args, const float* norm_weight, floa
  * gate/up SwiGLU GEMM, down GEMM with the residual added; aprender-serve
  * forward_qwen35_cuda_prefill.rs prefill_ffn_rows). The norm is not printed
  * there; this is the usual RMSNorm of a row, eps inside the square root.
- *   qtype      APR_Q4_0, APR_Q8_0, APR_F16 or APR_Q4_K for all three weights
+ *   qtype      APR_Q4_0, APR_Q8_0, APR_F16, APR_Q4_K or APR_Q5_K (all three)
  *   leg        APR_LEG_F16 or APR_LEG_EXACT_F32, as for apr_qgemm_ex; the f16
  *              leg writes the normed rows straight as fp16 (norm and
  *              conversion in one pass) for the tensor-core GEMMs
@@ -425,10 +431,10 @@ int apr_prefill_layer(const apr_layer_args* args);
 /*
  * Standalone dequant: out[n][k] f32 = f32(d) * f32(q'), bit exact (the product
  * of an fp16 scale and a code of at most 8 bits is exact in fp32); for F16
- * out = f32(w), also exact; for Q4_K the exact d * sc * q - dmin * m rounded
- * once to f32. The device dequant of aprender-serve
+ * out = f32(w), also exact; for Q4_K and Q5_K the exact d * sc * q - dmin * m
+ * rounded once to f32. The device dequant of aprender-serve
  * gdn_prefill_ops.rs qwen35_dequant_f32 (Q8_0, F16 and the other formats it
- * dispatches), here for Q4_0, Q8_0 and F16 and meant for tests: the
+ * dispatches), here for Q4_0, Q8_0, F16, Q4_K and Q5_K and meant for tests: the
  * projections never write decoded weights to memory. An F16 W needs only
  * 2-byte alignment here (APR_E_ALIGN otherwise).
  */

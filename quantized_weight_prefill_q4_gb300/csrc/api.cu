@@ -178,13 +178,16 @@ struct Problem {
 
 int ldy_of(const Problem& p) { return p.ldy > 0 ? p.ldy : p.n; }
 
-bool known_qtype(int q) { return q == APR_Q4_0 || q == APR_Q8_0 || q == APR_F16 || q == APR_Q4_K; }
+bool known_qtype(int q) {
+  return q == APR_Q4_0 || q == APR_Q8_0 || q == APR_F16 || q == APR_Q4_K || q == APR_Q5_K;
+}
 // k (the columns of every weight row) a whole number of the format's blocks
-bool k_fits(int qtype, int k) { return k > 0 && k % (qtype == APR_Q4_K ? 256 : 32) == 0; }
+int k_unit(int qtype) { return kquant(qtype) ? 256 : 32; }
+bool k_fits(int qtype, int k) { return k > 0 && k % k_unit(qtype) == 0; }
 
-// a streaming GEMV kernel (integer-dot, whole-row, bulk, tensor-core or the Q4_K one) takes the shape
+// a streaming GEMV kernel (integer-dot, whole-row, bulk, tensor-core or the K-quant one) takes the shape
 bool gemv_streams(int qtype, int n, int k, int T, bool swiglu) {
-  return qtype == APR_Q4_K || gemv_i8_fits(qtype, n, k, T, swiglu) || gemv_rows_fits(qtype, n, k, T, swiglu) ||
+  return kquant(qtype) || gemv_i8_fits(qtype, n, k, T, swiglu) || gemv_rows_fits(qtype, n, k, T, swiglu) ||
          gemv_bulk_fits(qtype, k, T, swiglu) || (!swiglu && block32_format(qtype) && gemv_tc_takes(n, k, T, false));
 }
 
@@ -196,7 +199,7 @@ int check(const Problem& p, size_t x_elem_bytes = 4) {
     return fail(APR_E_INVAL, "unknown path %d", p.path);
   if (p.n < 0 || p.T < 0 || !k_fits(p.qtype, p.k))
     return fail(APR_E_INVAL, "bad sizes n=%d k=%d T=%d (need n >= 0, T >= 0, k > 0, k a multiple of %d)", p.n, p.k,
-                p.T, p.qtype == APR_Q4_K ? 256 : 32);
+                p.T, k_unit(p.qtype));
   if (p.n > (1 << 24) || p.T > (1 << 24) || p.k > (1 << 20) || (int64_t)p.n * (p.k / 32) > (int64_t)1 << 31)
     return fail(APR_E_INVAL, "sizes beyond the supported limits");
   if (p.ldy < 0 || (p.ldy > 0 && p.ldy < p.n) || p.ldy > (1 << 28))
@@ -319,7 +322,7 @@ int run_ffn(const apr_ffn_args& a) {
   if (a.leg != APR_LEG_F16 && a.leg != APR_LEG_EXACT_F32) return fail(APR_E_INVAL, "unknown leg %d", a.leg);
   if (!k_fits(a.qtype, a.hidden) || !k_fits(a.qtype, a.inter) || a.T < 0)
     return fail(APR_E_INVAL, "bad sizes hidden=%d inter=%d T=%d (need multiples of %d, T >= 0)", a.hidden, a.inter,
-                a.T, a.qtype == APR_Q4_K ? 256 : 32);
+                a.T, k_unit(a.qtype));
   if (a.hidden > (1 << 20) || a.inter > (1 << 20) || a.T > (1 << 24) ||
       (int64_t)a.hidden * (a.inter / 32) > (int64_t)1 << 31)
     return fail(APR_E_INVAL, "sizes beyond the supported limits");

@@ -12,11 +12,13 @@ constexpr int kF16 = 1;
 constexpr int kQ4_0 = 2;
 constexpr int kQ8_0 = 8;
 constexpr int kQ4_K = 12;  // 256-element superblocks of 144 bytes (k % 256 == 0)
+constexpr int kQ5_K = 13;  // 256-element superblocks of 176 bytes (k % 256 == 0)
+inline bool kquant(int qtype) { return qtype == kQ4_K || qtype == kQ5_K; }
 
 // bytes of 32 consecutive elements of a weight row (one block; 64 for F16; an
-// eighth of a Q4_K superblock)
+// eighth of a Q4_K or Q5_K superblock)
 inline int block_bytes(int qtype) {
-  return qtype == kQ4_0 || qtype == kQ4_K ? 18 : (qtype == kQ8_0 ? 34 : 64);
+  return qtype == kQ4_0 || qtype == kQ4_K ? 18 : (qtype == kQ8_0 ? 34 : (qtype == kQ5_K ? 22 : 64));
 }
 // formats of one scale and 32 codes per 32-element block (the block-GEMV kernels)
 inline bool block32_format(int qtype) { return qtype == kQ4_0 || qtype == kQ8_0; }

@@ -26,16 +26,18 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
       out[idx] = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t*>(W)[idx]));
       continue;
     }
-    if constexpr (QT == kQ4_K) {  // superblock of 256 in 144 bytes
+    if constexpr (QT == kQ4_K || QT == kQ5_K) {  // superblock of 256 in 144 or 176 bytes
+      constexpr uint32_t SBB = QT == kQ4_K ? 144 : 176, QOFF = QT == kQ4_K ? 16 : 48;
       const size_t row = idx / (size_t)k;
       const uint32_t col = (uint32_t)(idx - row * (size_t)k);
-      const uint8_t* sb = W + (row * (size_t)(k / 256) + col / 256) * 144;
+      const uint8_t* sb = W + (row * (size_t)(k / 256) + col / 256) * SBB;
       const uint32_t e = col & 255u, g = e >> 6, hi = (e >> 5) & 1u, l = e & 31u, j = 2 * g + hi;
       uint32_t sc, m;
       q4k_scale_min(sb + 4, j, sc, m);
       const float d = __half2float(__ushort_as_half((uint16_t)(sb[0] | (sb[1] << 8))));
       const float dmin = __half2float(__ushort_as_half((uint16_t)(sb[2] | (sb[3] << 8))));
-      const uint32_t q = (sb[16 + 32 * g + l] >> (4 * hi)) & 15u;
+      uint32_t q = (sb[QOFF + 32 * g + l] >> (4 * hi)) & 15u;
+      if (QT == kQ5_K) q += ((sb[16 + l] >> j) & 1u) << 4;  // the fifth bit: bit 2 g + hi of byte l
       // d sc and dmin m are exact in fp32; one rounding of d sc q - dmin m
       out[idx] = fmaf(d * (float)sc, (float)q, -(dmin * (float)m));
       continue;
@@ -63,7 +65,9 @@ cudaError_t launch_dequant(int qtype, const void* W, int n, int k, float* out, c
   const size_t total = (size_t)n * (size_t)k;
   size_t blocks = (total + 255) / 256;
   if (blocks > 152 * 64) blocks = 152 * 64;
-  if (qtype == kQ4_K)
+  if (qtype == kQ5_K)
+    dequant_kernel<kQ5_K><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);
+  else if (qtype == kQ4_K)
     dequant_kernel<kQ4_K><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);
   else if (qtype == kF16)
     dequant_kernel<kF16><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);

@@ -109,11 +109,12 @@ struct Cfg {
   static constexpr int DQ = NM == 1 ? 2 : 1;           // warpgroups per weight (alternate stages)
   static constexpr int NWG = NM * DQ;                   // dequant / epilogue warpgroups
   static constexpr bool F16W = QT == kF16;
-  static constexpr bool Q4W = QT == kQ4_0 || QT == kQ4_K;  // 144 bytes per row of a 256-k chunk
-  static constexpr int BB = Q4W ? 18 : (QT == kQ8_0 ? 34 : 64);  // bytes per 32 k
-  // words a decode thread reads per stage: two blocks, or for Q4_K the
-  // superblock's header and scales (4 words) and the stage's 32 code bytes
-  static constexpr int NWORDS = QT == kQ4_K ? 12 : 2 * BB / 4;
+  static constexpr bool Q4W = QT == kQ4_0 || QT == kQ4_K || QT == kQ5_K;  // ring depths of the short-row formats
+  static constexpr int BB = QT == kQ4_0 || QT == kQ4_K ? 18 : (QT == kQ8_0 ? 34 : (QT == kQ5_K ? 22 : 64));
+  // words a decode thread reads per stage: two blocks, or for Q4_K / Q5_K the
+  // superblock's header and scales (4 words), Q5_K's fifth-bit bytes (8
+  // words) and the stage's 32 code bytes (8 words)
+  static constexpr int NWORDS = QT == kQ4_K ? 12 : (QT == kQ5_K ? 20 : 2 * BB / 4);
   // k per raw slot: a chunk, or half of one for an F16 gate/up pair (four
   // slots of 32 KB keep each weight double-buffered)
   static constexpr int RAW_K = F16W && NM == 2 ? CHUNK / 2 : CHUNK;
@@ -321,13 +322,14 @@ __device__ __forceinline__ void dequant_row_stage_xs(const uint32_t* w, float sw
   }
 }
 
-// Q4_K: stage g (64 k) of one row's superblock, words w[0] = d | dmin << 16,
-// w[1..3] = the packed scales, w[4..11] = code bytes 32 g .. 32 g + 31:
+// Q4_K / Q5_K: stage g (64 k) of one row's superblock, words w[0] = d | dmin
+// << 16, w[1..3] = the packed scales, then (Q5_K) w[4..11] the fifth-bit
+// bytes 0 .. 31, then the code bytes 32 g .. 32 g + 31 (8 words):
 // a[j] for j < 16 the low nibbles (sub-block 2 g, elements 2j, 2j + 1), for
 // j >= 16 the high nibbles (sub-block 2 g + 1). Each weight d sc q - dmin m is
 // one fma of two exact products, rounded to fp32, then to fp16 (xs = false),
 // or times sw = 2^e and split into two fp16 pieces (xs = true).
-template <bool XSP>
+template <bool XSP, bool FIVE>
 __device__ __forceinline__ void q4k_row_stage(const uint32_t* w, uint32_t g, float sw, uint32_t (&a1)[32],
                                               uint32_t (&a2)[32]) {
   const float d = __half2float(__ushort_as_half((unsigned short)(w[0] & 0xFFFFu)));
@@ -343,12 +345,17 @@ __device__ __forceinline__ void q4k_row_stage(const uint32_t* w, uint32_t g, flo
   auto code = [](uint32_t c) { return __uint_as_float(c | 0x4B000000u) - 8388608.0f; };  // 0..15 exactly
 #pragma unroll
   for (int v = 0; v < 8; ++v) {
-    const uint32_t x = w[4 + v];
+    const uint32_t x = w[(FIVE ? 12 : 4) + v];
+    const uint32_t f = FIVE ? w[4 + v] : 0u;  // fifth bits of elements 4 v .. 4 v + 3 (and + 32)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       float q[4];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) q[b] = fmaf(A[h], code((x >> (8 * b + 4 * h)) & 15u), B[h]);
+      for (int b = 0; b < 4; ++b) {
+        uint32_t qv = (x >> (8 * b + 4 * h)) & 15u;
+        if (FIVE) qv |= ((f >> (8 * b + 2 * g + h)) & 1u) << 4;
+        q[b] = fmaf(A[h], code(qv), B[h]);
+      }
       const int j = 16 * h + 2 * v;
       if constexpr (XSP) {
         split2(q[0] * sw, q[1] * sw, a1[j], a2[j]);
@@ -631,17 +638,18 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
         uint32_t w[C::NWORDS], a[32], a2[32];
         if constexpr (C::F16W) {
           f16_row_stage(raw_slot + s * (C::RAW_BYTES / C::RAW_LOADS), r, w);
-        } else if constexpr (QT == kQ4_K) {
+        } else if constexpr (QT == kQ4_K || QT == kQ5_K) {
+          constexpr int H = QT == kQ5_K ? 12 : 4;  // words before the code bytes
 #pragma unroll
-          for (int v = 0; v < 4; ++v) w[v] = raw_row[v];
+          for (int v = 0; v < H; ++v) w[v] = raw_row[v];
 #pragma unroll
-          for (int v = 0; v < 8; ++v) w[4 + v] = raw_row[4 + 8 * s + v];
+          for (int v = 0; v < 8; ++v) w[H + v] = raw_row[H + 8 * s + v];
         } else {
 #pragma unroll
           for (int v = 0; v < C::NWORDS; ++v) w[v] = raw_row[s * C::NWORDS + v];
         }
-        if constexpr (QT == kQ4_K)
-          q4k_row_stage<XS>(w, (uint32_t)s, sw, a, a2);  // overlaps the wait below
+        if constexpr (QT == kQ4_K || QT == kQ5_K)
+          q4k_row_stage<XS, QT == kQ5_K>(w, (uint32_t)s, sw, a, a2);  // overlaps the wait below
         else if constexpr (XS)
           dequant_row_stage_xs<QT>(w, sw, a, a2);  // overlaps the wait below
         else if constexpr (C::F16W)
@@ -1008,19 +1016,20 @@ __global__ void row_exp_f16_kernel(const uint16_t* __restrict__ W, int n, int k,
   }
 }
 
-// Q4_K: the same exponent from a bound on the row's largest |w|, the largest
-// over its superblocks of |d| 63 x 15 + |dmin| 63 (every |d sc q - dmin m| is
-// at most that). One warp per row.
-__global__ void row_exp_q4k_kernel(const uint8_t* __restrict__ W, int n, int nsb, int* __restrict__ erow) {
+// Q4_K / Q5_K: the same exponent from a bound on the row's largest |w|, the
+// largest over its superblocks of |d| 63 qmax + |dmin| 63 (qmax 15 or 31: every
+// |d sc q - dmin m| is at most that). One warp per row.
+__global__ void row_exp_q4k_kernel(const uint8_t* __restrict__ W, int n, int nsb, int sbb, float qmax,
+                                   int* __restrict__ erow) {
   const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (row >= n) return;
-  const uint8_t* base = W + (size_t)row * nsb * 144;
+  const uint8_t* base = W + (size_t)row * nsb * sbb;
   float m = 0.f;
   for (int b = lane; b < nsb; b += 32) {
-    const uint32_t h = *reinterpret_cast<const uint32_t*>(base + (size_t)b * 144);
+    const uint32_t h = *reinterpret_cast<const uint32_t*>(base + (size_t)b * sbb);
     const float d = fabsf(__half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu))));
     const float dmin = fabsf(__half2float(__ushort_as_half((unsigned short)(h >> 16))));
-    m = fmaxf(m, d * 945.0f + dmin * 63.0f);
+    m = fmaxf(m, d * (63.0f * qmax) + dmin * 63.0f);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -1134,9 +1143,12 @@ int launch_gemm_xs(int qtype, const void* W, const void* Wu, int n, int k, const
   if (qtype == kF16) {
     row_exp_f16_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint16_t*>(W), n, k, erow);
     if (Wu) row_exp_f16_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint16_t*>(Wu), n, k, erow + n);
-  } else if (qtype == kQ4_K) {
-    row_exp_q4k_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(W), n, k / 256, erow);
-    if (Wu) row_exp_q4k_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(Wu), n, k / 256, erow + n);
+  } else if (kquant(qtype)) {
+    const int sbb = qtype == kQ4_K ? 144 : 176;
+    const float qm = qtype == kQ4_K ? 15.f : 31.f;
+    row_exp_q4k_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(W), n, k / 256, sbb, qm, erow);
+    if (Wu)
+      row_exp_q4k_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(Wu), n, k / 256, sbb, qm, erow + n);
   } else {
     row_exp_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(W), n, k / 32, bb, qmax, erow);
     if (Wu) row_exp_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(Wu), n, k / 32, bb, qmax, erow + n);
@@ -1149,6 +1161,7 @@ int launch_gemm_xs(int qtype, const void* W, const void* Wu, int n, int k, const
   }
   if (qtype == kF16) return launch_xs<kF16>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
   if (qtype == kQ4_K) return launch_xs<kQ4_K>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
+  if (qtype == kQ5_K) return launch_xs<kQ5_K>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
   return qtype == kQ4_0 ? launch_xs<kQ4_0>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len)
                         : launch_xs<kQ8_0>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
 }
@@ -1198,6 +1211,7 @@ int launch_gemm_tc(const GemmPlan& pl, int qtype, const void* W, const void* Wu,
   const int w = early;
   if (qtype == kF16) return launch_q<kF16>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
   if (qtype == kQ4_K) return launch_q<kQ4_K>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
+  if (qtype == kQ5_K) return launch_q<kQ5_K>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
   return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows)
                         : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
 }

@@ -1,4 +1,4 @@
-// Small-T GEMV over Q4_0 / Q8_0 blocks, F16 or Q4_K weights, exact fp32 arithmetic.
+// Small-T GEMV over Q4_0 / Q8_0 blocks, F16, Q4_K or Q5_K weights, exact fp32 arithmetic.
 //
 // Y[t][i] = sum_j X[t][j] * d_{i,j/32} * q'_{i,j} (+ R[t][i]) for T <= 16 token
 // rows, or silu(g) * u for a gate/up pair. The single-token GEMVs of
@@ -363,24 +363,27 @@ cudaError_t launch_f16(const void* W, const void* Wu, int n, int k, const float*
   return launch_f16_t<16, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
 }
 
-// Q4_K weights: a warp per weight row, one 256-element superblock (144 bytes)
-// a step; lane l takes elements 8 l .. 8 l + 7 of it: group g = l / 8 (64
-// elements), low nibbles of code bytes 32 g + 8 (l mod 4) .. for l mod 8 < 4
-// (sub-block 2 g), high nibbles of the same bytes otherwise (sub-block
-// 2 g + 1). Each weight is d sc q - dmin m rounded once to fp32 (one fma of
-// two exact products), then exact fp32 products with X. The loads of two
-// superblocks are issued before either is used.
-template <int TMAX, bool SWI>
+// Q4_K and Q5_K weights: a warp per weight row, one 256-element superblock
+// (144 or 176 bytes) a step; lane l takes elements 8 l .. 8 l + 7 of it: group
+// g = l / 8 (64 elements), low nibbles of code bytes 32 g + 8 (l mod 4) .. for
+// l mod 8 < 4 (sub-block 2 g), high nibbles of the same bytes otherwise
+// (sub-block 2 g + 1); Q5_K adds bit 2 g (or 2 g + 1) of the fifth-bit bytes
+// 8 (l mod 4) .. as 16. Each weight is d sc q - dmin m rounded once to fp32
+// (one fma of two exact products), then exact fp32 products with X. The loads
+// of two superblocks are issued before either is used.
+template <int QT, int TMAX, bool SWI>
 __global__ void __launch_bounds__(kWarps * 32) gemv_q4k_kernel(const uint8_t* __restrict__ W,
                                                                const uint8_t* __restrict__ Wu, int n, int k,
                                                                const float* __restrict__ X, int T, float* Y, int ldy,
                                                                const float* R) {
   constexpr int NM = SWI ? 2 : 1;
+  constexpr bool FIVE = QT == kQ5_K;
+  constexpr uint32_t SBB = FIVE ? 176 : 144;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nsb = k / 256;
-  const size_t row_bytes = (size_t)nsb * 144;
+  const size_t row_bytes = (size_t)nsb * SBB;
   const uint32_t g = (uint32_t)lane >> 3, part = (uint32_t)lane & 7u, hi = part >> 2, j = 2 * g + hi;
-  const uint32_t qoff = 16 + 32 * g + 8 * (part & 3u);
+  const uint32_t qoff = (FIVE ? 48 : 16) + 32 * g + 8 * (part & 3u), hoff = 16 + 8 * (part & 3u);
   bool waited = false;
   for (int row = blockIdx.x * kWarps + warp; row < n; row += gridDim.x * kWarps) {
     float acc[NM][TMAX];
@@ -393,15 +396,16 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q4k_kernel(const uint8_t* __
     if (SWI) base[NM - 1] = Wu + (size_t)row * row_bytes;
     for (int sb0 = 0; sb0 < nsb; sb0 += 2) {
       uint4 h[2][NM];
-      uint2 c[2][NM];
+      uint2 c[2][NM], f[2][NM];
 #pragma unroll
       for (int u = 0; u < 2; ++u)
 #pragma unroll
         for (int m = 0; m < NM; ++m)
           if (sb0 + u < nsb) {
-            const uint8_t* sb = base[m] + (size_t)(sb0 + u) * 144;
+            const uint8_t* sb = base[m] + (size_t)(sb0 + u) * SBB;
             h[u][m] = ldg_nc_v4(sb);
             c[u][m] = __ldg(reinterpret_cast<const uint2*>(sb + qoff));
+            if (FIVE) f[u][m] = __ldg(reinterpret_cast<const uint2*>(sb + hoff));
           }
       if (!waited) {
         grid_dependency_wait_inline();
@@ -420,9 +424,17 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q4k_kernel(const uint8_t* __
           const float dmin = __half2float(__ushort_as_half((unsigned short)(h[u][m].x >> 16)));
           const float a = d * (float)sc, b = -(dmin * (float)mn);
           const uint32_t cw[2] = {c[u][m].x, c[u][m].y};
+          uint32_t fw[2] = {0u, 0u};
+          if (FIVE) {
+            fw[0] = f[u][m].x;
+            fw[1] = f[u][m].y;
+          }
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            w[m][e] = fmaf(a, (float)((cw[e >> 2] >> (8 * (e & 3) + 4 * hi)) & 15u), b);
+          for (int e = 0; e < 8; ++e) {
+            uint32_t qv = (cw[e >> 2] >> (8 * (e & 3) + 4 * hi)) & 15u;
+            if (FIVE) qv += ((fw[e >> 2] >> (8 * (e & 3) + j)) & 1u) << 4;
+            w[m][e] = fmaf(a, (float)qv, b);
+          }
         }
         const int col = (sb0 + u) * 256 + 8 * lane;
 #pragma unroll
@@ -462,7 +474,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q4k_kernel(const uint8_t* __
   if (!waited) grid_dependency_wait_inline();  // a CTA without rows
 }
 
-template <int TMAX, bool SWI>
+template <int QT, int TMAX, bool SWI>
 cudaError_t launch_q4k_t(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
                          const float* R, cudaStream_t s) {
   long blocks = (n + kWarps - 1) / kWarps;
@@ -475,18 +487,18 @@ cudaError_t launch_q4k_t(const void* W, const void* Wu, int n, int k, const floa
   cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_q4k_kernel<TMAX, SWI>, static_cast<const uint8_t*>(W),
+  return cudaLaunchKernelEx(&cfg, gemv_q4k_kernel<QT, TMAX, SWI>, static_cast<const uint8_t*>(W),
                             static_cast<const uint8_t*>(Wu), n, k, X, T, Y, ldy, R);
 }
 
-template <bool SWI>
+template <int QT, bool SWI>
 cudaError_t launch_q4k(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
                        const float* R, cudaStream_t s) {
-  if (T <= 1) return launch_q4k_t<1, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
-  if (T <= 2) return launch_q4k_t<2, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
-  if (T <= 4) return launch_q4k_t<4, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
-  if (T <= 8) return launch_q4k_t<8, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
-  return launch_q4k_t<16, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 1) return launch_q4k_t<QT, 1, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 2) return launch_q4k_t<QT, 2, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 4) return launch_q4k_t<QT, 4, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 8) return launch_q4k_t<QT, 8, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  return launch_q4k_t<QT, 16, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
 }
 
 }  // namespace
@@ -499,7 +511,11 @@ cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, 
   if (gemv_rows_fits(qtype, n, k, T, swi)) return launch_gemv_rows(qtype, W, Wu, n, k, X, T, Y, R, status, s);
   if (gemv_bulk_fits(qtype, k, T, swi)) return launch_gemv_bulk(qtype, W, Wu, n, k, X, T, Y, ldy, R, status, s);
   if (qtype == kQ4_K)
-    return swi ? launch_q4k<true>(W, Wu, n, k, X, T, Y, ldy, R, s) : launch_q4k<false>(W, Wu, n, k, X, T, Y, ldy, R, s);
+    return swi ? launch_q4k<kQ4_K, true>(W, Wu, n, k, X, T, Y, ldy, R, s)
+               : launch_q4k<kQ4_K, false>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (qtype == kQ5_K)
+    return swi ? launch_q4k<kQ5_K, true>(W, Wu, n, k, X, T, Y, ldy, R, s)
+               : launch_q4k<kQ5_K, false>(W, Wu, n, k, X, T, Y, ldy, R, s);
   if (qtype == kF16) {
     if (k % 256 == 0)
       return swi ? launch_f16<true>(W, Wu, n, k, X, T, Y, ldy, R, s) : launch_f16<false>(W, Wu, n, k, X, T, Y, ldy, R, s);

@@ -1,6 +1,7 @@
-"""GPU parity of Q4_K weights (256-element superblocks: fp16 d and dmin, 6-bit
-sub-block scales and mins, 4-bit codes; the layout read in the oracle) on every
-route, against the float64 oracle.
+"""GPU parity of Q4_K and Q5_K weights (256-element superblocks: fp16 d and
+dmin, 6-bit sub-block scales and mins, 4-bit codes, and for Q5_K a fifth code
+bit per element; the layouts read in the oracle) on every route, against the
+float64 oracle.
 
 Bars:
 * dequant: bit exact (d sc q - dmin m rounded once to f32 on both sides);
@@ -11,7 +12,7 @@ Bars:
   fp32 value lands on an fp16 tie the exact value is not on);
 * exact routes (GEMV, the exact leg's GEMM): within 1e-5 of the sum of the
   terms' magnitudes elementwise and the exact-leg bar overall.
-Inputs: the seeded N(0, 0.02) weight encoded as Q4_K, and random superblocks
+Inputs: the seeded N(0, 0.02) weight encoded in the format, and random superblocks
 (random bytes, d and dmin of both signs from one exponent class).
 """
 
@@ -25,12 +26,17 @@ from gpu_util import assert_exact_leg, assert_f16_leg, check_guards, dev, guarde
 
 pytestmark = pytest.mark.gpu
 
-QK = synth.Q4_K
+
+
+@pytest.fixture(params=[synth.Q4_K, synth.Q5_K], ids=["q4_k", "q5_k"])
+def qk(request):
+    return request.param
+
 CLASSES = ["subnormal", "small", "typical", "large", "mixed"]
 
 
-def _scale(W, n, k, X, R=None, f16=False):
-    Wf = oracle.dequant_f64(QK, W, n, k)
+def _scale(qk, W, n, k, X, R=None, f16=False):
+    Wf = oracle.dequant_f64(qk, W, n, k)
     Xf = np.asarray(X, np.float32)
     if f16:
         Wf = Wf.astype(np.float16).astype(np.float64)
@@ -51,27 +57,27 @@ def _elementwise(y, ref, s, tol):
                              f"y={y[t, i]!r} ref={ref[t, i]!r} scale={s[t, i]!r}")
 
 
-def _check_exact(W, n, k, X, R, y):
-    ref = oracle.qgemm_f64(QK, W, n, k, X, R)
-    _elementwise(y, ref, _scale(W, n, k, X, R), 1e-5)
+def _check_exact(qk, W, n, k, X, R, y):
+    ref = oracle.qgemm_f64(qk, W, n, k, X, R)
+    _elementwise(y, ref, _scale(qk, W, n, k, X, R), 1e-5)
     assert_exact_leg(y, ref)
 
 
-def _check_f16(W, n, k, X, R, y, f64_bar=True):
-    ref16 = oracle.qgemm_f16_inputs_f64(QK, W, n, k, X, R)
-    _elementwise(y, ref16, _scale(W, n, k, X, R, f16=True), 3e-5)
+def _check_f16(qk, W, n, k, X, R, y, f64_bar=True):
+    ref16 = oracle.qgemm_f16_inputs_f64(qk, W, n, k, X, R)
+    _elementwise(y, ref16, _scale(qk, W, n, k, X, R, f16=True), 3e-5)
     if f64_bar:
-        assert_f16_leg(y, oracle.qgemm_f64(QK, W, n, k, X, R))
+        assert_f16_leg(y, oracle.qgemm_f64(qk, W, n, k, X, R))
 
 
-def _synthetic(n, k, T, seed, residual=False):
-    c = synth.make_case(QK, n, k, T, residual=residual, seed=seed)
+def _synthetic(qk, n, k, T, seed, residual=False):
+    c = synth.make_case(qk, n, k, T, residual=residual, seed=seed)
     return c["W"], c["X"], c["R"]
 
 
-def _call(q, W, n, k, X, T, R=None, leg=0, path=0, Wu=None):
+def _call(q, qk, W, n, k, X, T, R=None, leg=0, path=0, Wu=None):
     buf, Y = guarded(T, n)
-    q.apr_qgemm_ex(QK, dev(W), n, k, dev(X), T, Y, residual=None if R is None else dev(R),
+    q.apr_qgemm_ex(qk, dev(W), n, k, dev(X), T, Y, residual=None if R is None else dev(R),
                    Wu=None if Wu is None else dev(Wu), leg=leg, path=path)
     q.apr_stream_status()
     check_guards(buf, T, n)
@@ -81,162 +87,164 @@ def _call(q, W, n, k, X, T, R=None, leg=0, path=0, Wu=None):
 # ------------------------------------------------------------------ dequant
 @pytest.mark.parametrize("cls", CLASSES)
 @pytest.mark.parametrize("n,k", [(1, 256), (37, 768), (130, 4096)])
-def test_dequant_bit_exact_random_superblocks(q, cls, n, k):
-    W = synth.random_blocks(QK, n, k, seed=n + k, scale_class=cls)
+def test_dequant_bit_exact_random_superblocks(q, qk, cls, n, k):
+    W = synth.random_blocks(qk, n, k, seed=n + k, scale_class=cls)
     out = torch.full((n, k), float("nan"), device="cuda")
-    q.apr_dequant(QK, dev(W), n, k, out)
+    q.apr_dequant(qk, dev(W), n, k, out)
     q.apr_stream_status()
     np.testing.assert_array_equal(out.cpu().numpy().view(np.uint32),
-                                  oracle.dequant_f32(QK, W, n, k).view(np.uint32))
+                                  oracle.dequant_f32(qk, W, n, k).view(np.uint32))
 
 
-def test_dequant_hand_superblocks(q):
+def test_dequant_hand_superblocks(q, qk):
     import test_oracle_pins as pins
 
+    five = qk == synth.Q5_K
+    build, qmax, sbb = (pins._q5_k_superblock, 32, 176) if five else (pins._q4_k_superblock, 16, 144)
     sc = [1, 2, 3, 4, 17, 33, 48, 63]
     mn = [0, 1, 2, 3, 16, 40, 5, 62]
-    a = pins._q4_k_superblock(0x3C00, 0x3C00, sc, mn, [1] * 256)
-    b = pins._q4_k_superblock(0x3C00, 0x0000, [1] * 8, [0] * 8, [e % 16 for e in range(256)])
-    W = np.frombuffer(a + b, np.uint8).reshape(2, 144).copy()
+    a = build(0x3C00, 0x3C00, sc, mn, [1] * 256)
+    b = build(0x3C00, 0x0000, [1] * 8, [0] * 8, [e % qmax for e in range(256)])
+    W = np.frombuffer(a + b, np.uint8).reshape(2, sbb).copy()
     out = torch.empty((2, 256), device="cuda")
-    q.apr_dequant(QK, dev(W), 2, 256, out)
+    q.apr_dequant(qk, dev(W), 2, 256, out)
     q.apr_stream_status()
     got = out.cpu().numpy()
     np.testing.assert_array_equal(got[0], np.repeat(np.array(sc) - np.array(mn), 32).astype(np.float32))
-    np.testing.assert_array_equal(got[1], np.array([e % 16 for e in range(256)], np.float32))
+    np.testing.assert_array_equal(got[1], np.array([e % qmax for e in range(256)], np.float32))
 
 
 # ------------------------------------------------------------------ fp16-leg GEMM
 @pytest.mark.parametrize("n,k,T,res", [(300, 768, 200, True), (4096, 4096, 512, True), (128, 256, 9, False),
                                        (1000, 1024, 130, False), (256, 512, 100, True)])
-def test_gemm_synthetic(q, n, k, T, res):
-    W, X, R = _synthetic(n, k, T, seed=n + T, residual=res)
-    y = _call(q, W, n, k, X, T, R, leg=q.APR_LEG_F16, path=q.APR_PATH_GEMM)
-    _check_f16(W, n, k, X, R, y)
+def test_gemm_synthetic(q, qk, n, k, T, res):
+    W, X, R = _synthetic(qk, n, k, T, seed=n + T, residual=res)
+    y = _call(q, qk, W, n, k, X, T, R, leg=q.APR_LEG_F16, path=q.APR_PATH_GEMM)
+    _check_f16(qk, W, n, k, X, R, y)
 
 
 @pytest.mark.parametrize("cls", ["small", "typical", "large", "mixed"])
-def test_gemm_random_superblocks(q, cls):
+def test_gemm_random_superblocks(q, qk, cls):
     n, k, T = 300, 1024, 150
-    W = synth.random_blocks(QK, n, k, 60, cls, fp16_range=True)
+    W = synth.random_blocks(qk, n, k, 60, cls, fp16_range=True)
     X = synth.activations(T, k, 61)
     R = synth.activations(T, n, 62)
-    y = _call(q, W, n, k, X, T, R, leg=q.APR_LEG_F16, path=q.APR_PATH_GEMM)
-    _check_f16(W, n, k, X, R, y)
+    y = _call(q, qk, W, n, k, X, T, R, leg=q.APR_LEG_F16, path=q.APR_PATH_GEMM)
+    _check_f16(qk, W, n, k, X, R, y)
 
 
-def test_gate_up_swiglu(q):
+def test_gate_up_swiglu(q, qk):
     n, k, T = 384, 1024, 200
-    Wg = synth.quantize(QK, synth.weight_f32(n, k, 5))
-    Wu = synth.quantize(QK, synth.weight_f32(n, k, 6))
+    Wg = synth.quantize(qk, synth.weight_f32(n, k, 5))
+    Wu = synth.quantize(qk, synth.weight_f32(n, k, 6))
     X = synth.activations(T, k, 7)
     buf, Y = guarded(T, n)
-    q.apr_qgemm_gate_up_swiglu(QK, dev(Wg), dev(Wu), n, k, dev(X), T, Y)
+    q.apr_qgemm_gate_up_swiglu(qk, dev(Wg), dev(Wu), n, k, dev(X), T, Y)
     q.apr_stream_status()
     check_guards(buf, T, n)
     y = Y.cpu().numpy()
-    ref16 = oracle.gate_up_swiglu_f16_inputs_f64(QK, Wg, Wu, n, k, X)
+    ref16 = oracle.gate_up_swiglu_f16_inputs_f64(qk, Wg, Wu, n, k, X)
     assert float(np.linalg.norm(y - ref16) / np.linalg.norm(ref16)) <= 2e-5
-    assert_f16_leg(y, oracle.gate_up_swiglu_f64(QK, Wg, Wu, n, k, X))
+    assert_f16_leg(y, oracle.gate_up_swiglu_f64(qk, Wg, Wu, n, k, X))
 
 
-def test_f16_input_entry_and_noalloc(q):
+def test_f16_input_entry_and_noalloc(q, qk):
     n, k, T = 300, 512, 64
-    W, X, R = _synthetic(n, k, T, seed=9, residual=True)
+    W, X, R = _synthetic(qk, n, k, T, seed=9, residual=True)
     X16 = torch.empty((T, k), dtype=torch.float16, device="cuda")
     q.apr_convert_f32_to_f16(dev(X), T * k, X16)
     buf, Y = guarded(T, n)
-    q.apr_qgemm_f16_in(QK, dev(W), n, k, X16, T, Y, dev(R))
+    q.apr_qgemm_f16_in(qk, dev(W), n, k, X16, T, Y, dev(R))
     q.apr_stream_status()
     check_guards(buf, T, n)
-    _check_f16(W, n, k, X, R, Y.cpu().numpy())
+    _check_f16(qk, W, n, k, X, R, Y.cpu().numpy())
     buf, Y = guarded(T, n)
-    q.apr_qgemm_noalloc(QK, dev(W), n, k, dev(X), T, Y, dev(R))
+    q.apr_qgemm_noalloc(qk, dev(W), n, k, dev(X), T, Y, dev(R))
     q.apr_stream_status()
     check_guards(buf, T, n)
-    _check_f16(W, n, k, X, R, Y.cpu().numpy())
+    _check_f16(qk, W, n, k, X, R, Y.cpu().numpy())
 
 
 # ------------------------------------------------------------------ exact routes
 @pytest.mark.parametrize("cls", CLASSES)
 @pytest.mark.parametrize("n,k,T,res", [(130, 1024, 129, True), (200, 512, 40, False)])
-def test_exact_gemm(q, cls, n, k, T, res):
-    W = synth.random_blocks(QK, n, k, 7 * n + T, cls)
+def test_exact_gemm(q, qk, cls, n, k, T, res):
+    W = synth.random_blocks(qk, n, k, 7 * n + T, cls)
     X = synth.activations(T, k, 8)
     R = synth.activations(T, n, 9) if res else None
-    y = _call(q, W, n, k, X, T, R, leg=q.APR_LEG_EXACT_F32, path=q.APR_PATH_GEMM)
-    _check_exact(W, n, k, X, R, y)
+    y = _call(q, qk, W, n, k, X, T, R, leg=q.APR_LEG_EXACT_F32, path=q.APR_PATH_GEMM)
+    _check_exact(qk, W, n, k, X, R, y)
 
 
-def test_exact_gate_up(q):
+def test_exact_gate_up(q, qk):
     n, k, T = 200, 512, 40
-    Wg = synth.random_blocks(QK, n, k, 15, "typical")
-    Wu = synth.random_blocks(QK, n, k, 16, "typical")
+    Wg = synth.random_blocks(qk, n, k, 15, "typical")
+    Wu = synth.random_blocks(qk, n, k, 16, "typical")
     X = synth.activations(T, k, 17)
-    y = _call(q, Wg, n, k, X, T, leg=q.APR_LEG_EXACT_F32, path=q.APR_PATH_GEMM, Wu=Wu)
-    assert_exact_leg(y, oracle.gate_up_swiglu_f64(QK, Wg, Wu, n, k, X))
+    y = _call(q, qk, Wg, n, k, X, T, leg=q.APR_LEG_EXACT_F32, path=q.APR_PATH_GEMM, Wu=Wu)
+    assert_exact_leg(y, oracle.gate_up_swiglu_f64(qk, Wg, Wu, n, k, X))
 
 
 # T <= 8: the Q4_K GEMV; T = 13: the exact tensor-core GEMM
 @pytest.mark.parametrize("cls", ["subnormal", "typical", "large", "mixed"])
 @pytest.mark.parametrize("n,k,T", [(300, 512, 1), (300, 512, 2), (300, 1024, 4), (300, 512, 8), (300, 512, 13),
                                    (77, 256, 1), (64, 12288, 3)])
-def test_gemv(q, cls, n, k, T):
-    W = synth.random_blocks(QK, n, k, 3 * n + k + T, cls)
+def test_gemv(q, qk, cls, n, k, T):
+    W = synth.random_blocks(qk, n, k, 3 * n + k + T, cls)
     X = synth.activations(T, k, 5)
     R = synth.activations(T, n, 6)
     buf, Y = guarded(T, n)
-    q.apr_qgemv(QK, dev(W), n, k, dev(X), T, Y, dev(R))
+    q.apr_qgemv(qk, dev(W), n, k, dev(X), T, Y, dev(R))
     q.apr_stream_status()
     check_guards(buf, T, n)
-    _check_exact(W, n, k, X, R, Y.cpu().numpy())
+    _check_exact(qk, W, n, k, X, R, Y.cpu().numpy())
 
 
 @pytest.mark.parametrize("T", [1, 4, 7])
-def test_auto_rule_and_gemv_gate_up(q, T):
+def test_auto_rule_and_gemv_gate_up(q, qk, T):
     n, k = 4096, 4096
-    W, X, R = _synthetic(n, k, T, seed=T, residual=True)
+    W, X, R = _synthetic(qk, n, k, T, seed=T, residual=True)
     buf, Y = guarded(T, n)
-    q.apr_qgemm(QK, dev(W), n, k, dev(X), T, Y, dev(R))
+    q.apr_qgemm(qk, dev(W), n, k, dev(X), T, Y, dev(R))
     q.apr_stream_status()
     check_guards(buf, T, n)
-    (_check_exact if T <= q.APR_AUTO_GEMV_MAX_T else _check_f16)(W, n, k, X, R, Y.cpu().numpy())
-    Wu = synth.quantize(QK, synth.weight_f32(n, k, 100 + T))
-    y = _call(q, W, n, k, X, T, leg=q.APR_LEG_EXACT_F32, path=q.APR_PATH_GEMV, Wu=Wu)
-    assert_exact_leg(y, oracle.gate_up_swiglu_f64(QK, W, Wu, n, k, X))
+    (_check_exact if T <= q.APR_AUTO_GEMV_MAX_T else _check_f16)(qk, W, n, k, X, R, Y.cpu().numpy())
+    Wu = synth.quantize(qk, synth.weight_f32(n, k, 100 + T))
+    y = _call(q, qk, W, n, k, X, T, leg=q.APR_LEG_EXACT_F32, path=q.APR_PATH_GEMV, Wu=Wu)
+    assert_exact_leg(y, oracle.gate_up_swiglu_f64(qk, W, Wu, n, k, X))
 
 
 # ------------------------------------------------------------------ composites
 @pytest.mark.parametrize("leg,T", [(0, 40), (1, 40), (0, 3), (1, 3)])
-def test_ffn_sublayer(q, leg, T):
+def test_ffn_sublayer(q, qk, leg, T):
     hidden, inter = 256, 512
-    Ws = [synth.quantize(QK, synth.weight_f32(r, c, 30 + i))
+    Ws = [synth.quantize(qk, synth.weight_f32(r, c, 30 + i))
           for i, (r, c) in enumerate(((inter, hidden), (inter, hidden), (hidden, inter)))]
     X = synth.activations(T, hidden, 33)
     w = (1.0 + 0.5 * synth.activations(1, hidden, 34)[0]).astype(np.float32)
     Xd = dev(X)
-    q.apr_ffn_sublayer(QK, *[dev(Wi) for Wi in Ws], hidden, inter, T, dev(w), 1e-6, Xd, leg=leg)
+    q.apr_ffn_sublayer(qk, *[dev(Wi) for Wi in Ws], hidden, inter, T, dev(w), 1e-6, Xd, leg=leg)
     q.apr_stream_status()
-    ref = oracle.ffn_sublayer_f64(QK, X, w, 1e-6, Ws[0], Ws[1], Ws[2], hidden, inter)
+    ref = oracle.ffn_sublayer_f64(qk, X, w, 1e-6, Ws[0], Ws[1], Ws[2], hidden, inter)
     x0 = X.astype(np.float64)
     (assert_f16_leg if leg == 0 else assert_exact_leg)(Xd.cpu().numpy() - x0, ref - x0)
 
 
-def test_normed_projection(q):
+def test_normed_projection(q, qk):
     n, k, T = 300, 512, 50
-    W = synth.random_blocks(QK, n, k, 41, "typical")
+    W = synth.random_blocks(qk, n, k, 41, "typical")
     X = synth.activations(T, k, 42)
     w = (1.0 + 0.5 * synth.activations(1, k, 43)[0]).astype(np.float32)
     buf, Y = guarded(T, n)
-    q.apr_qgemm_rmsnorm(QK, dev(W), n, k, dev(X), T, Y, dev(w), 1e-6)
+    q.apr_qgemm_rmsnorm(qk, dev(W), n, k, dev(X), T, Y, dev(w), 1e-6)
     q.apr_stream_status()
     check_guards(buf, T, n)
-    assert_f16_leg(Y.cpu().numpy(), oracle.normed_qgemm_f64(QK, W, n, k, X, w, 1e-6))
+    assert_f16_leg(Y.cpu().numpy(), oracle.normed_qgemm_f64(qk, W, n, k, X, w, 1e-6))
 
 
 @pytest.mark.parametrize("leg", [0, 1])
-def test_prefill_layer(q, leg):
+def test_prefill_layer(q, qk, leg):
     import test_gpu_layer as lay
 
-    c = lay._case(QK, 512, 1024, 4, 2, 200, 37, seed=71)
+    c = lay._case(qk, 512, 1024, 4, 2, 200, 37, seed=71)
     lay._check(c, lay._run(q, c, leg=leg, chunk=128), leg)
