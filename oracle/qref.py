@@ -1,4 +1,4 @@
-"""Plain CPU oracle for the Q4_0 / Q8_0 / F16 / Q4_K / Q5_K prefill projections (float64).
+"""Plain CPU oracle for the Q4_0 / Q8_0 / F16 / Q4_K / Q5_K / Q6_K prefill projections (float64).
 
 TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import or call
@@ -35,6 +35,13 @@ What is computed, and where the pages define it:
   fifth code bits between the scales and the codes (bit ``2 g`` of byte ``l``
   for element ``64 g + l``, bit ``2 g + 1`` for ``64 g + 32 + l``, each worth
   16), the codes at bytes 48-175.
+* Q6_K, also dispatched without a printed layout; read as the GGUF Q6_K
+  superblock of 256 elements in 210 bytes: 128 bytes of low code nibbles, 64
+  bytes of high code bit pairs, 16 int8 sub-block scales (one per 16
+  elements), then fp16 ``d`` (bytes 208-209). Element ``e = 128 h + 32 c + l``
+  (half ``h``, quarter ``c``, lane ``l`` < 32) takes nibble ``c / 2`` of low
+  byte ``64 h + 32 (c % 2) + l`` and bits ``2 c .. 2 c + 1`` of high byte
+  ``32 h + l`` as its six-bit code ``q``; ``w = d sc_{e/16} (q - 32)``.
 * Projection ``Y[T][n] = X[T][k] . W[n][k]^T`` (aprender-serve 0.70.2
   src/cuda/executor/gdn_prefill_ops.rs, doc of ``qwen35_project_rows``),
   optionally ``+ R[T][n]`` (the residual add that follows the down / output
@@ -90,10 +97,11 @@ Q4_0 = 2
 Q8_0 = 8
 Q4_K = 12
 Q5_K = 13
+Q6_K = 14
 _QK = 32
 _QK_K = 256
 _BLOCK_BYTES = {F16: 64, Q4_0: 18, Q8_0: 34}
-_SUPER_BYTES = {Q4_K: 144, Q5_K: 176}
+_SUPER_BYTES = {Q4_K: 144, Q5_K: 176, Q6_K: 210}
 
 
 # --------------------------------------------------------------------------
@@ -164,6 +172,23 @@ def _dequant_k(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
     return w.reshape(n, k)
 
 
+def _dequant_q6_k(W: np.ndarray, n: int, k: int) -> np.ndarray:
+    """Q6_K: six-bit codes from a low nibble and a high bit pair, a signed
+    8-bit scale per 16 elements, ``w = d sc (q - 32)``."""
+    sb = _superblocks(Q6_K, W, n, k)
+    nsb = k // _QK_K
+    ql = sb[..., 0:128].astype(np.int64).reshape(n, nsb, 2, 2, 32)    # [half][c % 2][l]
+    qh = sb[..., 128:192].astype(np.int64).reshape(n, nsb, 2, 1, 32)  # [half][.][l]
+    sc = sb[..., 192:208].view(np.int8).astype(np.int64)               # [16]
+    d = fp16_bits_to_f64(sb[..., 208].astype(np.uint16) | (sb[..., 209].astype(np.uint16) << 8))
+    low = np.concatenate([ql & 0x0F, ql >> 4], axis=3)                 # [half][c][l], c = 0 .. 3
+    c = np.arange(4).reshape(1, 1, 1, 4, 1)
+    high = (qh >> (2 * c)) & 3
+    q = (low | (high << 4)).reshape(n, nsb, 16, 16).astype(np.float64)  # sub-block e / 16
+    w = d[..., None, None] * sc[..., None].astype(np.float64) * (q - 32.0)
+    return w.reshape(n, k)
+
+
 def _row_bytes(qtype: int, k: int) -> int:
     """Bytes of one weight row of k elements."""
     if qtype in _SUPER_BYTES:
@@ -206,6 +231,8 @@ def block_scales_and_codes(qtype: int, W: np.ndarray, n: int, k: int):
 def dequant_f64(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
     """``Wf[i][j] = fp16(d_{i, j/32}) * q'_{i,j}`` in float64, shape ``[n][k]``;
     for F16 the binary16 value of element ``(i, j)``."""
+    if qtype == Q6_K:
+        return _dequant_q6_k(W, n, k)
     if qtype in _SUPER_BYTES:
         return _dequant_k(qtype, W, n, k)
     if qtype == F16:
@@ -225,7 +252,9 @@ def dequant_f32(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
     an fp16 scale times 128 is well inside float32's normal range, and fp16
     subnormal scales times small integers stay exact in float32). Every fp16
     value, subnormals included, is a float32 value. Q4_K and Q5_K: the exact
-    float64 value ``d sc q - dmin m`` rounded once to float32.
+    float64 value ``d sc q - dmin m`` rounded once to float32. Q6_K: ``d sc
+    (q - 32)`` has at most 11 + 7 + 6 significant bits, so it is exact in
+    float32 too.
     """
     return dequant_f64(qtype, W, n, k).astype(np.float32)
 

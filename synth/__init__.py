@@ -14,6 +14,7 @@ from .gen import (  # noqa: F401
     Q8_0,
     Q4_K,
     Q5_K,
+    Q6_K,
     BLOCK_ELEMS,
     block_bytes,
     quantize,
@@ -22,6 +23,8 @@ from .gen import (  # noqa: F401
     quantize_f16,
     quantize_q4_k,
     quantize_q5_k,
+    quantize_q6_k,
+    row_bytes,
     weight_f32,
     activations,
     make_case,

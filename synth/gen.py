@@ -40,15 +40,23 @@ Q4_0 = 2  # GGUF type id
 Q8_0 = 8  # GGUF type id
 Q4_K = 12  # GGUF type id (256-element superblocks of 144 bytes)
 Q5_K = 13  # GGUF type id (256-element superblocks of 176 bytes)
+Q6_K = 14  # GGUF type id (256-element superblocks of 210 bytes)
 BLOCK_ELEMS = 32
 _BLOCK_BYTES = {F16: 64, Q4_0: 18, Q8_0: 34, Q4_K: 18, Q5_K: 22}
-_SUPER_BYTES = {Q4_K: 144, Q5_K: 176}
+_SUPER_BYTES = {Q4_K: 144, Q5_K: 176, Q6_K: 210}
 
 
 def block_bytes(qtype: int) -> int:
     """Bytes of 32 elements of ``qtype`` (one block; 64 bytes of F16; an
     eighth of a Q4_K superblock)."""
     return _BLOCK_BYTES[qtype]
+
+
+def row_bytes(qtype: int, k: int) -> int:
+    """Bytes of one weight row of ``k`` elements."""
+    if qtype in _SUPER_BYTES:
+        return k // 256 * _SUPER_BYTES[qtype]
+    return k // BLOCK_ELEMS * _BLOCK_BYTES[qtype]
 
 
 def _round_half_away(v: np.ndarray) -> np.ndarray:
@@ -133,6 +141,42 @@ def quantize_q5_k(w: np.ndarray) -> np.ndarray:
     return _quantize_k(w, 5)
 
 
+def quantize_q6_k(w: np.ndarray) -> np.ndarray:
+    """Encode an f32 ``[n][k]`` weight (k % 256 == 0) into Q6_K superblocks
+    ``[n][k/256*210]``: per 16-element sub-block the signed element m of
+    largest magnitude gives the sub-scale m / -32 (m maps to code 0); d is the
+    largest |sub-scale| over 127 (fp16), the int8 scales round(sub-scale / d),
+    and each code round(w / (d sc)) + 32 clamped to 0..63. Byte placement:
+    low nibble of element 128 h + 32 c + l in byte 64 h + 32 (c % 2) + l
+    (nibble c / 2), its top two bits at bits 2 c of byte 128 + 32 h + l, the
+    scales at bytes 192-207 and d at 208-209."""
+    w = np.ascontiguousarray(w, dtype=np.float32).astype(np.float64)
+    n, k = w.shape
+    nsb = k // 256
+    x = w.reshape(n, nsb, 16, 16)
+    idx = np.abs(x).argmax(axis=-1)
+    m = np.take_along_axis(x, idx[..., None], axis=-1)[..., 0]
+    sub = m / -32.0
+    d16 = (np.abs(sub).max(axis=-1) / 127.0).astype(np.float16)
+    df = d16.astype(np.float64)
+    sc = np.where(df[..., None] > 0, np.clip(np.rint(sub / np.where(df > 0, df, 1.0)[..., None]), -127, 127), 0)
+    sc = sc.astype(np.int64)
+    step = df[..., None] * sc
+    q = np.where(step[..., None] != 0, np.rint(x / np.where(step != 0, step, 1.0)[..., None]) + 32, 32)
+    q = np.clip(q, 0, 63).astype(np.int64).reshape(n, nsb, 2, 4, 32)  # [half][c][l]
+    out = np.zeros((n, nsb, 210), np.uint8)
+    low = q & 15
+    ql = low[:, :, :, 0:2, :] | (low[:, :, :, 2:4, :] << 4)  # [half][c % 2][l]: quarters c and c + 2
+    out[..., 0:128] = ql.reshape(n, nsb, 128).astype(np.uint8)
+    qh = np.zeros((n, nsb, 2, 32), np.int64)
+    for c in range(4):
+        qh |= (q[:, :, :, c, :] >> 4) << (2 * c)
+    out[..., 128:192] = qh.reshape(n, nsb, 64).astype(np.uint8)
+    out[..., 192:208] = sc.astype(np.int8).view(np.uint8)
+    out[..., 208:210] = d16.view(np.uint16)[..., None].view(np.uint8).reshape(n, nsb, 2)
+    return out.reshape(n, -1)
+
+
 def _quantize_k(w: np.ndarray, bits: int) -> np.ndarray:
     top = (1 << bits) - 1
     w = np.ascontiguousarray(w, dtype=np.float32).astype(np.float64)
@@ -180,6 +224,8 @@ def quantize(qtype: int, w: np.ndarray) -> np.ndarray:
         return quantize_q4_k(w)
     if qtype == Q5_K:
         return quantize_q5_k(w)
+    if qtype == Q6_K:
+        return quantize_q6_k(w)
     if qtype == Q4_0:
         return quantize_q4_0(w)
     if qtype == Q8_0:
@@ -223,13 +269,14 @@ def random_blocks(qtype: int, n: int, k: int, seed: int, scale_class: str = "mix
     """
     lo, hi = SCALE_CLASSES[scale_class]
     if qtype in _SUPER_BYTES:
-        # random bytes; d and dmin of both signs drawn from the class
+        # random bytes; d and dmin (Q6_K: d alone, at the end) of both signs
+        # drawn from the class
         rng = np.random.default_rng(seed)
         raw = rng.integers(0, 256, size=(n, k // 256, _SUPER_BYTES[qtype]), dtype=np.uint8)
-        for off in (0, 2):
+        for off in ((208,) if qtype == Q6_K else (0, 2)):
             exp = rng.integers(lo, hi + 1, size=(n, k // 256)).astype(np.uint16)
-            if fp16_range:  # |d sc q| within fp16's range: |d| < 2^5 (63 x 31 x 2^5 < 65504)
-                exp = np.minimum(exp, 19)
+            if fp16_range:  # |w| within fp16's range: |d| < 2^5 (63 x 31 x 2^5 < 65504); Q6_K |d| < 16 (128 x 32 x 16)
+                exp = np.minimum(exp, 18 if qtype == Q6_K else 19)
             man = rng.integers(0, 1024, size=(n, k // 256)).astype(np.uint16)
             man = np.where(exp == 0, np.maximum(man, 1), man)
             sign = rng.integers(0, 2, size=(n, k // 256)).astype(np.uint16)

@@ -23,12 +23,12 @@ import oracle
 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-QTYPES = [synth.Q4_0, synth.Q8_0, synth.F16, synth.Q4_K, synth.Q5_K]
-KQ = (synth.Q4_K, synth.Q5_K)
+QTYPES = [synth.Q4_0, synth.Q8_0, synth.F16, synth.Q4_K, synth.Q5_K, synth.Q6_K]
+KQ = (synth.Q4_K, synth.Q5_K, synth.Q6_K)
 
 
 def _kk(qtype, k):
-    """k as given, or widened to whole 256-element superblocks for Q4_K."""
+    """k as given, or widened to whole 256-element superblocks for the K-quants."""
     return max(256, k // 256 * 256) if qtype in KQ else k
 
 
@@ -227,6 +227,77 @@ def test_q4_k_encoder_round_trip_and_sizes():
         oracle.dequant_f64(synth.Q4_K, W[:, :144], n, 128)
 
 
+def _q6_k_superblock(d_bits, sc, q):
+    """Q6_K bytes from d's fp16 bits, 16 int8 scales and 256 six-bit codes,
+    placed one element at a time: element 128 h + 32 c + l keeps its low four
+    bits in nibble c // 2 of byte 64 h + 32 (c % 2) + l and its top two at bit
+    2 c of byte 128 + 32 h + l; the scales at bytes 192-207, d at 208-209."""
+    b = bytearray(210)
+    for e in range(256):
+        h, c, l = e // 128, (e % 128) // 32, e % 32
+        b[64 * h + 32 * (c % 2) + l] |= (q[e] & 15) << (4 * (c // 2))
+        b[128 + 32 * h + l] |= (q[e] >> 4) << (2 * c)
+    b[192:208] = struct.pack("<16b", *sc)
+    b[208:210] = struct.pack("<H", d_bits)
+    return bytes(b)
+
+
+def test_q6_k_with_unit_scales_equals_q8_0_blocks():
+    # every scale 1: element e is d (q_e - 32), the Q8_0 block of scale d with
+    # code q_e - 32 (-32 .. 31)
+    rng = np.random.default_rng(25)
+    n, k = 3, 512
+    W8 = np.zeros((n, k // 32, 34), np.uint8)
+    W6 = bytearray()
+    for i in range(n):
+        for s_ in range(k // 256):
+            d_bits = int(rng.integers(0x0400, 0x7800))
+            q = [int(v) for v in rng.integers(0, 64, size=256)]
+            W6 += _q6_k_superblock(d_bits, [1] * 16, q)
+            for j in range(8):
+                blk = W8[i, 8 * s_ + j]
+                blk[0:2] = np.frombuffer(struct.pack("<H", d_bits), np.uint8)
+                blk[2:34] = np.array([v - 32 for v in q[32 * j:32 * (j + 1)]], np.int8).view(np.uint8)
+    W6 = np.frombuffer(bytes(W6), np.uint8).reshape(n, -1)
+    np.testing.assert_array_equal(oracle.dequant_f64(synth.Q6_K, W6, n, k),
+                                  oracle.dequant_f64(synth.Q8_0, W8.reshape(n, -1), n, k))
+
+
+def test_q6_k_scales_land_on_their_sixteen_elements():
+    # d = 1, every code 33 (q - 32 = 1): element e is the int8 scale of e // 16
+    sc = [1, -1, 2, -128, 127, 0, 5, -7, 64, -64, 3, 33, -100, 99, 11, -2]
+    raw = np.frombuffer(_q6_k_superblock(0x3C00, sc, [33] * 256), np.uint8).reshape(1, 210)
+    np.testing.assert_array_equal(oracle.dequant_f64(synth.Q6_K, raw, 1, 256)[0],
+                                  np.repeat(np.array(sc, np.float64), 16))
+
+
+def test_q6_k_codes_in_element_order():
+    # d = 1, unit scales: w = q - 32; element e gets code e mod 64, then a
+    # code whose top bits alone are set
+    q = [e % 64 for e in range(256)]
+    raw = np.frombuffer(_q6_k_superblock(0x3C00, [1] * 16, q), np.uint8).reshape(1, 210)
+    np.testing.assert_array_equal(oracle.dequant_f64(synth.Q6_K, raw, 1, 256)[0], np.array(q, np.float64) - 32)
+    q = [48 if e == 201 else 32 for e in range(256)]
+    raw = np.frombuffer(_q6_k_superblock(0x4000, [1] * 16, q), np.uint8).reshape(1, 210)
+    want = np.zeros(256)
+    want[201] = 2.0 * 16
+    np.testing.assert_array_equal(oracle.dequant_f64(synth.Q6_K, raw, 1, 256)[0], want)
+
+
+def test_q6_k_encoder_round_trip_and_sizes():
+    n, k = 16, 512
+    w = synth.weight_f32(n, k, seed=4)
+    W = synth.quantize(synth.Q6_K, w)
+    assert W.shape == (n, k // 256 * 210) == (n, synth.row_bytes(synth.Q6_K, k))
+    err = np.abs(oracle.dequant_f64(synth.Q6_K, W, n, k) - w.astype(np.float64)).reshape(n, k // 256, 16, 16)
+    amax = np.abs(w.reshape(n, k // 256, 16, 16)).max(-1)
+    # a step of about amax / 32, rounded to nearest; the 8-bit scale and fp16 d
+    # add a few hundredths of the largest value
+    assert np.all(err.max(-1) <= amax / 64 * 1.1 + 0.02 * np.abs(w).max())
+    with pytest.raises(ValueError):
+        oracle.dequant_f64(synth.Q6_K, W[:, :210], n, 128)
+
+
 def test_f16_weights_reach_every_finite_half():
     # the random F16 generator draws every exponent field 0..30 and no inf/NaN;
     # the oracle decodes each element to its binary16 value
@@ -295,8 +366,9 @@ def _random_blocks(rng, qtype, n, k):
     """Random raw bytes with finite scales (exponent field kept below 31); for
     F16 every element is such a half; for Q4_K d and dmin of every superblock."""
     if qtype in KQ:
-        raw = rng.integers(0, 256, size=(n, k // 256, 144 if qtype == synth.Q4_K else 176), dtype=np.uint8)
-        for b in (1, 3):
+        sbb = {synth.Q4_K: 144, synth.Q5_K: 176, synth.Q6_K: 210}[qtype]
+        raw = rng.integers(0, 256, size=(n, k // 256, sbb), dtype=np.uint8)
+        for b in ((209,) if qtype == synth.Q6_K else (1, 3)):
             raw[..., b] = np.where((raw[..., b] & 0x7C) == 0x7C, raw[..., b] & 0xBF, raw[..., b])
         return raw.reshape(n, -1)
     bb = synth.block_bytes(qtype)
@@ -340,13 +412,42 @@ def _q4_k_row_independent(raw: bytes, k, five=False):
     return out
 
 
+def _q6_k_row_independent(raw: bytes, k):
+    """Exact values of one Q6_K row, element by element with struct: element
+    128 h + 32 c + l takes nibble c // 2 of byte 64 h + 32 (c % 2) + l, bits
+    2 c, 2 c + 1 of byte 128 + 32 h + l, scale byte 192 + (element % 256) // 16
+    (int8) and d from bytes 208-209; w = d sc (q - 32)."""
+    out = []
+    for sb in range(k // 256):
+        blk = raw[210 * sb:210 * (sb + 1)]
+        d = Fraction(struct.unpack("<e", blk[208:210])[0])
+        vals = [None] * 256
+        for h in range(2):
+            for c in range(4):
+                for l in range(32):
+                    e = 128 * h + 32 * c + l
+                    lo = blk[64 * h + 32 * (c % 2) + l]
+                    lo = (lo >> 4) if c >= 2 else (lo & 15)
+                    hi = (blk[128 + 32 * h + l] >> (2 * c)) & 3
+                    sc = struct.unpack("<b", blk[192 + e // 16:193 + e // 16])[0]
+                    vals[e] = d * sc * ((lo | (hi << 4)) - 32)
+        out.extend(vals)
+    return out
+
+
+def _kq_row_independent(qtype, raw: bytes, k):
+    if qtype == synth.Q6_K:
+        return _q6_k_row_independent(raw, k)
+    return _q4_k_row_independent(raw, k, five=qtype == synth.Q5_K)
+
+
 def _exact_qgemm(qtype, W, n, k, X, R):
-    bb = synth.block_bytes(qtype)
     rows = []
     for i in range(n):
         if qtype in KQ:
-            rows.append(_q4_k_row_independent(bytes(W[i]), k, five=qtype == synth.Q5_K))
+            rows.append(_kq_row_independent(qtype, bytes(W[i]), k))
             continue
+        bb = synth.block_bytes(qtype)
         wrow = []
         for b in range(k // 32):
             blk = bytes(W[i, b * bb:(b + 1) * bb])
@@ -401,7 +502,7 @@ def test_brute_force_dequant_exact(qtype):
     got = oracle.dequant_f32(qtype, W, n, k)
     for i in range(n):
         for j in range(k):
-            if qtype in KQ:  # d sc q - dmin m may need more than 24 bits: rounded once
+            if qtype in (synth.Q4_K, synth.Q5_K):  # d sc q - dmin m may need more than 24 bits: rounded once
                 assert abs(Fraction(float(got[i, j])) - rows[i][j]) <= Fraction(_ulp32(float(got[i, j]))) / 2
             else:
                 assert Fraction(float(got[i, j])) == rows[i][j]
@@ -559,8 +660,7 @@ def test_ffn_sublayer_special_cases():
 def _block_values(raw, qtype, n, k):
     """Dequantized weight from the raw bytes, by the block rules (struct parse)."""
     if qtype in KQ:
-        return np.array([[float(v) for v in _q4_k_row_independent(bytes(raw[i]), k, five=qtype == synth.Q5_K)]
-                         for i in range(n)])
+        return np.array([[float(v) for v in _kq_row_independent(qtype, bytes(raw[i]), k)] for i in range(n)])
     if qtype == synth.F16:
         return np.array([struct.unpack("<%de" % k, bytes(raw[i])) for i in range(n)], dtype=np.float64)
     bb = 18 if qtype == synth.Q4_0 else 34
