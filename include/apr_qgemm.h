@@ -1,6 +1,6 @@
 /*
  * apr_qgemm.h — C ABI of the GB300 (sm_103a) prefill projections over GGUF
- * Q4_0 / Q8_0 / Q4_K / Q5_K block-quantized weights and F16 weights.
+ * Q4_0 / Q8_0 / Q4_K / Q5_K / Q6_K block-quantized weights and F16 weights.
  *
  * Every projection of a batched (chunked) prompt prefill is ONE product over
  * the chunk's T token rows, instead of T per-token GEMVs:
@@ -43,6 +43,14 @@
  *                    of fifth code bits (bit 2g + h of byte l is the fifth
  *                    bit, worth 16, of element 64g + 32h + l), then the 128
  *                    code bytes as in Q4_K; q in 0..31, w as for Q4_K.
+ *   Q6_K (210 bytes per 256 weights, k % 2048 == 0 so that every row starts
+ *                    on a 16-byte boundary): also dispatched without a printed
+ *                    layout; taken as the GGUF superblock: 128 bytes of low
+ *                    code nibbles, 64 bytes of high code bit pairs, 16 int8
+ *                    scales (one per 16 weights), fp16 d in bytes 208-209.
+ *                    Element 128h + 32c + l (c < 4, l < 32) has nibble c / 2
+ *                    of byte 64h + 32(c % 2) + l and bits 2c, 2c + 1 of byte
+ *                    128 + 32h + l as its 6-bit code q; w = d * sc * (q - 32).
  * Row i of W is the k/32 consecutive blocks starting at byte i*(k/32)*bytes.
  *
  * Memory and streams. Every pointer argument named W, Wu, X, residual, Y or
@@ -69,10 +77,12 @@
  *
  * Errors. Arguments are checked on the host before anything is enqueued:
  *   APR_E_INVAL   null pointer with nonzero sizes, n < 0, T < 0, k <= 0,
- *                 k % 32 != 0 (k % 256 != 0 for Q4_K, Q5_K), a size beyond the
+ *                 k % 32 != 0 (k % 256 != 0 for Q4_K, Q5_K; k % 2048 != 0
+ *                 for Q6_K), a size beyond the
  *                 documented limits, or an
  *                 unknown leg / path
- *   APR_E_QTYPE   qtype is not APR_Q4_0, APR_Q8_0, APR_F16, APR_Q4_K or APR_Q5_K
+ *   APR_E_QTYPE   qtype is not APR_Q4_0, APR_Q8_0, APR_F16, APR_Q4_K, APR_Q5_K
+ *                 or APR_Q6_K
  *   APR_E_ALIGN   a pointer is not 16-byte aligned
  *   APR_E_ALIAS   Y overlaps X, W or Wu, or overlaps residual without being
  *                 exactly the same buffer (Y == residual is allowed: it gives
@@ -108,7 +118,7 @@ extern "C" {
 typedef struct CUstream_st* apr_stream_t;
 
 /* GGUF tensor type ids. */
-enum { APR_F16 = 1, APR_Q4_0 = 2, APR_Q8_0 = 8, APR_Q4_K = 12, APR_Q5_K = 13 };
+enum { APR_F16 = 1, APR_Q4_0 = 2, APR_Q8_0 = 8, APR_Q4_K = 12, APR_Q5_K = 13, APR_Q6_K = 14 };
 
 /*
  * Arithmetic legs (aprender-serve gdn_prefill_ops.rs, module doc, group 1):
@@ -154,7 +164,7 @@ int apr_gemv_max_T(void);
 
 /*
  * Y = X . dequant(W)^T (+ residual), fp16 leg, T rule.
- *   qtype     APR_Q4_0, APR_Q8_0, APR_F16, APR_Q4_K or APR_Q5_K
+ *   qtype     APR_Q4_0, APR_Q8_0, APR_F16, APR_Q4_K, APR_Q5_K or APR_Q6_K
  *   W         [n rows][k/32 blocks] GGUF blocks
  *   X         [T][k] f32;  Y [T][n] f32, overwritten
  *   residual  [T][n] f32 or NULL; may be Y itself (accumulate)
@@ -182,8 +192,8 @@ int apr_qgemm_gate_up_swiglu(int qtype, const void* Wg, const void* Wu, int n, i
  * arithmetic, optional residual (gemv_q4_0_pf / gemv_q8_0_pf of
  * oxibonsai-kernels, used for the last-token lm_head in
  * try_cuda_prefill_q_std). For T <= 8 weight rows stream by bulk copies into
- * T fp32 accumulators (tensor cores for T = 3, 4 with Q4_0 / Q8_0; F16,
- * Q4_K and Q5_K weights always on the CUDA cores); for 9 <= T <= 16, and for smaller T
+ * T fp32 accumulators (tensor cores for T = 3, 4 with Q4_0 / Q8_0; F16 and
+ * K-quant weights always on the CUDA cores); for 9 <= T <= 16, and for smaller T
  * where no streaming kernel takes the shape (the X table of a long row does
  * not fit shared memory), the exact leg's tensor-core GEMM runs instead when
  * k % 256 == 0 (49-57 us at 4096 x 4096 and 12288 x 4096, against 50 to 700
@@ -298,7 +308,7 @@ int apr_qgemm_rmsnorm(const apr_qgemm_args* args, const float* norm_weight, floa
  * gate/up SwiGLU GEMM, down GEMM with the residual added; aprender-serve
  * forward_qwen35_cuda_prefill.rs prefill_ffn_rows). The norm is not printed
  * there; this is the usual RMSNorm of a row, eps inside the square root.
- *   qtype      APR_Q4_0, APR_Q8_0, APR_F16, APR_Q4_K or APR_Q5_K (all three)
+ *   qtype      any qtype above, the same for all three
  *   leg        APR_LEG_F16 or APR_LEG_EXACT_F32, as for apr_qgemm_ex; the f16
  *              leg writes the normed rows straight as fp16 (norm and
  *              conversion in one pass) for the tensor-core GEMMs
@@ -388,7 +398,8 @@ int apr_prefill_attention(const float* Q, const float* K_cache, const float* V_c
  *   Wqkv     [(num_heads + 2 num_kv_heads) * 256][hidden]: the q rows, then the
  *            k rows, then the v rows (the pages' fused qkv weight)
  *   Wo       [hidden][num_heads * 256];  Wg, Wu [inter][hidden];  Wd [hidden][inter]
- *   hidden, inter  multiples of 32 (256 for the tensor-core routes)
+ *   hidden, inter  multiples of the format's unit (32; 256 for Q4_K, Q5_K;
+ *            2048 for Q6_K), and so must num_heads * 256 be (Wo's columns)
  *   num_heads, num_kv_heads, head_dim  as for apr_prefill_attention (256)
  *   T, pos0  rows of X and the position of the first; T == 0 is a no-op
  *   attn_norm, ffn_norm  [hidden] fp32;  eps >= 0 and finite
@@ -432,9 +443,9 @@ int apr_prefill_layer(const apr_layer_args* args);
  * Standalone dequant: out[n][k] f32 = f32(d) * f32(q'), bit exact (the product
  * of an fp16 scale and a code of at most 8 bits is exact in fp32); for F16
  * out = f32(w), also exact; for Q4_K and Q5_K the exact d * sc * q - dmin * m
- * rounded once to f32. The device dequant of aprender-serve
+ * rounded once to f32; for Q6_K d * sc * (q - 32), exact. The device dequant of aprender-serve
  * gdn_prefill_ops.rs qwen35_dequant_f32 (Q8_0, F16 and the other formats it
- * dispatches), here for Q4_0, Q8_0, F16, Q4_K and Q5_K and meant for tests: the
+ * dispatches), here for every qtype above and meant for tests: the
  * projections never write decoded weights to memory. An F16 W needs only
  * 2-byte alignment here (APR_E_ALIGN otherwise).
  */

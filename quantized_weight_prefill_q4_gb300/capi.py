@@ -20,6 +20,7 @@ APR_Q4_0 = 2
 APR_Q8_0 = 8
 APR_Q4_K = 12
 APR_Q5_K = 13
+APR_Q6_K = 14
 APR_LEG_F16 = 0
 APR_LEG_EXACT_F32 = 1
 APR_PATH_AUTO = 0
@@ -40,6 +41,14 @@ APR_NOALLOC_MAX_TK = 8 * 1024 * 1024
 APR_FFN_CHUNK_ROWS = 2048
 
 BLOCK_BYTES = {APR_F16: 64, APR_Q4_0: 18, APR_Q8_0: 34, APR_Q4_K: 18, APR_Q5_K: 22}  # bytes per 32 weights
+SUPERBLOCK_BYTES = {APR_Q6_K: 210}  # bytes per 256 weights, for the formats without whole bytes per 32
+
+
+def row_bytes(qtype, k):
+    """Bytes of one weight row of k elements (0 for an unknown qtype)."""
+    if qtype in SUPERBLOCK_BYTES:
+        return k // 256 * SUPERBLOCK_BYTES[qtype]
+    return k // 32 * BLOCK_BYTES.get(qtype, 0)
 
 # Every symbol include/apr_qgemm.h declares.
 EXPORTS = (
@@ -227,9 +236,8 @@ def _stream(stream):
 
 
 def _sizes(qtype, n, k, T):
-    bb = BLOCK_BYTES.get(qtype, 0)
     n_, k_, T_ = max(n, 0), max(k, 0), max(T, 0)
-    return n_ * (k_ // 32) * bb, T_ * k_ * 4, T_ * n_ * 4
+    return n_ * row_bytes(qtype, k_), T_ * k_ * 4, T_ * n_ * 4
 
 
 def _dtypes():
@@ -343,10 +351,9 @@ def apr_ffn_sublayer(qtype, Wg, Wu, Wd, hidden, inter, T, norm_weight, eps, X, l
     """X[T][hidden] += down(silu(h . Wg^T) * (h . Wu^T)), h = RMSNorm(X) with
     norm_weight and eps; X is updated in place."""
     u8, f32 = _dtypes()
-    bb = BLOCK_BYTES.get(qtype, 0)
     h_, i_, t_ = max(hidden, 0), max(inter, 0), max(T, 0)
-    wgu = i_ * (h_ // 32) * bb
-    wd = h_ * (i_ // 32) * bb
+    wgu = i_ * row_bytes(qtype, h_)
+    wd = h_ * row_bytes(qtype, i_)
     a = _FfnArgs(qtype, leg, _ptr(Wg, "Wg", dtype=u8, min_bytes=wgu), _ptr(Wu, "Wu", dtype=u8, min_bytes=wgu),
                  _ptr(Wd, "Wd", dtype=u8, min_bytes=wd), hidden, inter, T,
                  _ptr(norm_weight, "norm_weight", dtype=f32, min_bytes=h_ * 4), float(eps),
@@ -395,15 +402,15 @@ def apr_prefill_layer(qtype, Wqkv, Wo, Wg, Wu, Wd, hidden, inter, num_heads, num
     and v written into the cache rows pos0 .., then the FFN sublayer), in
     chunks of `chunk` rows."""
     u8, f32 = _dtypes()
-    bb = BLOCK_BYTES.get(qtype, 0)
     h_, i_, t_ = max(hidden, 0), max(inter, 0), max(T, 0)
     qd, kvd = max(num_heads, 0) * max(head_dim, 0), max(num_kv_heads, 0) * max(head_dim, 0)
     crow = max(pos0, 0) + t_
-    a = _LayerArgs(qtype, leg, _ptr(Wqkv, "Wqkv", dtype=u8, min_bytes=(qd + 2 * kvd) * (h_ // 32) * bb),
-                   _ptr(Wo, "Wo", dtype=u8, min_bytes=h_ * (qd // 32) * bb),
-                   _ptr(Wg, "Wg", dtype=u8, min_bytes=i_ * (h_ // 32) * bb),
-                   _ptr(Wu, "Wu", dtype=u8, min_bytes=i_ * (h_ // 32) * bb),
-                   _ptr(Wd, "Wd", dtype=u8, min_bytes=h_ * (i_ // 32) * bb), hidden, inter, num_heads,
+    hrow = row_bytes(qtype, h_)
+    a = _LayerArgs(qtype, leg, _ptr(Wqkv, "Wqkv", dtype=u8, min_bytes=(qd + 2 * kvd) * hrow),
+                   _ptr(Wo, "Wo", dtype=u8, min_bytes=h_ * row_bytes(qtype, qd)),
+                   _ptr(Wg, "Wg", dtype=u8, min_bytes=i_ * hrow),
+                   _ptr(Wu, "Wu", dtype=u8, min_bytes=i_ * hrow),
+                   _ptr(Wd, "Wd", dtype=u8, min_bytes=h_ * row_bytes(qtype, i_)), hidden, inter, num_heads,
                    num_kv_heads, head_dim, T, pos0, _ptr(attn_norm, "attn_norm", dtype=f32, min_bytes=h_ * 4),
                    _ptr(ffn_norm, "ffn_norm", dtype=f32, min_bytes=h_ * 4), float(eps),
                    _ptr(X, "X", dtype=f32, min_bytes=t_ * h_ * 4),

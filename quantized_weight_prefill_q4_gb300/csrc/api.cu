@@ -179,10 +179,12 @@ struct Problem {
 int ldy_of(const Problem& p) { return p.ldy > 0 ? p.ldy : p.n; }
 
 bool known_qtype(int q) {
-  return q == APR_Q4_0 || q == APR_Q8_0 || q == APR_F16 || q == APR_Q4_K || q == APR_Q5_K;
+  return q == APR_Q4_0 || q == APR_Q8_0 || q == APR_F16 || q == APR_Q4_K || q == APR_Q5_K || q == APR_Q6_K;
 }
-// k (the columns of every weight row) a whole number of the format's blocks
-int k_unit(int qtype) { return kquant(qtype) ? 256 : 32; }
+// k (the columns of every weight row) a whole number of the format's blocks;
+// Q6_K rows (210 bytes per 256) start on 16-byte boundaries only when k is a
+// multiple of 2048, and every Q6_K route reads them from such boundaries
+int k_unit(int qtype) { return qtype == kQ6_K ? 2048 : (kquant(qtype) ? 256 : 32); }
 bool k_fits(int qtype, int k) { return k > 0 && k % k_unit(qtype) == 0; }
 
 // a streaming GEMV kernel (integer-dot, whole-row, bulk, tensor-core or the K-quant one) takes the shape
@@ -211,7 +213,7 @@ int check(const Problem& p, size_t x_elem_bytes = 4) {
   const void* ptrs[5] = {p.W, p.Wu, p.X, p.R, p.Y};
   for (const void* q : ptrs)
     if (q && !aligned16(q)) return fail(APR_E_ALIGN, "pointer %p is not 16-byte aligned", q);
-  const size_t wbytes = (size_t)p.n * (size_t)(p.k / 32) * (size_t)block_bytes(p.qtype);
+  const size_t wbytes = (size_t)p.n * row_bytes_of(p.qtype, p.k);
   const size_t xbytes = (size_t)p.T * (size_t)p.k * x_elem_bytes;
   const size_t ybytes = ((size_t)(p.T - 1) * (size_t)ldy_of(p) + (size_t)p.n) * 4;  // first to last element
   if (overlap(p.Y, ybytes, p.X, xbytes)) return fail(APR_E_ALIAS, "Y overlaps X");
@@ -332,8 +334,8 @@ int run_ffn(const apr_ffn_args& a) {
   const void* ptrs[5] = {a.Wg, a.Wu, a.Wd, a.norm_weight, a.X};
   for (const void* q : ptrs)
     if (!aligned16(q)) return fail(APR_E_ALIGN, "pointer %p is not 16-byte aligned", q);
-  const size_t bb = (size_t)block_bytes(a.qtype);
-  const size_t wgu = (size_t)a.inter * (a.hidden / 32) * bb, wd = (size_t)a.hidden * (a.inter / 32) * bb;
+  const size_t wgu = (size_t)a.inter * row_bytes_of(a.qtype, a.hidden);
+  const size_t wd = (size_t)a.hidden * row_bytes_of(a.qtype, a.inter);
   const size_t xb = (size_t)a.T * a.hidden * 4;
   if (overlap(a.X, xb, a.Wg, wgu) || overlap(a.X, xb, a.Wu, wgu) || overlap(a.X, xb, a.Wd, wd) ||
       overlap(a.X, xb, a.norm_weight, (size_t)a.hidden * 4))
@@ -443,6 +445,9 @@ int run_layer(const apr_layer_args& a) {
   if (a.num_heads % a.num_kv_heads != 0)
     return fail(APR_E_INVAL, "num_heads (%d) must be a multiple of num_kv_heads (%d)", a.num_heads, a.num_kv_heads);
   const long long qd = (long long)a.num_heads * 256, kvd = (long long)a.num_kv_heads * 256;
+  if (qd > (1 << 20) || !k_fits(a.qtype, (int)qd))
+    return fail(APR_E_INVAL, "the out projection's k = num_heads x 256 = %lld must be a multiple of %d", qd,
+                k_unit(a.qtype));
   if (a.hidden > (1 << 20) || a.inter > (1 << 20) || a.T > (1 << 24) || a.chunk > (1 << 20) ||
       qd + 2 * kvd > (1 << 24) || (long long)a.pos0 + a.T > (1LL << 30) || kvd / 64 > 65535 ||
       (long long)a.hidden * (a.inter / 32) > (1LL << 31) || (qd + 2 * kvd) * (a.hidden / 32) > (1LL << 31) ||
@@ -455,10 +460,9 @@ int run_layer(const apr_layer_args& a) {
     if (!q) return fail(APR_E_INVAL, "null pointer");
     if (!aligned16(q)) return fail(APR_E_ALIGN, "pointer %p is not 16-byte aligned", q);
   }
-  const size_t bb = (size_t)block_bytes(a.qtype);
-  const size_t hrow = (size_t)(a.hidden / 32) * bb;  // bytes of a weight row over hidden columns
-  const size_t wqkv = (size_t)(qd + 2 * kvd) * hrow, wo = (size_t)a.hidden * (size_t)(qd / 32) * bb;
-  const size_t wgu = (size_t)a.inter * hrow, wd = (size_t)a.hidden * (size_t)(a.inter / 32) * bb;
+  const size_t hrow = row_bytes_of(a.qtype, a.hidden);  // bytes of a weight row over hidden columns
+  const size_t wqkv = (size_t)(qd + 2 * kvd) * hrow, wo = (size_t)a.hidden * row_bytes_of(a.qtype, (int)qd);
+  const size_t wgu = (size_t)a.inter * hrow, wd = (size_t)a.hidden * row_bytes_of(a.qtype, a.inter);
   const size_t xb = (size_t)a.T * a.hidden * 4, cb = ((size_t)a.pos0 + a.T) * (size_t)kvd * 4;
   const void* wts[7] = {a.Wqkv, a.Wo, a.Wg, a.Wu, a.Wd, a.attn_norm, a.ffn_norm};
   const size_t wsz[7] = {wqkv, wo, wgu, wgu, wd, (size_t)a.hidden * 4, (size_t)a.hidden * 4};
@@ -693,7 +697,7 @@ int apr_dequant(int qtype, const void* W, int n, int k, float* out, apr_stream_t
   if (n == 0) return APR_OK;
   if (!W || !out) return fail(APR_E_INVAL, "null pointer");
   if (qtype == APR_F16 && ((uintptr_t)W & 1) != 0) return fail(APR_E_ALIGN, "an F16 weight must be 2-byte aligned");
-  const size_t wbytes = (size_t)n * (size_t)(k / 32) * (size_t)block_bytes(qtype);
+  const size_t wbytes = (size_t)n * row_bytes_of(qtype, k);
   if (overlap(out, (size_t)n * k * 4, W, wbytes)) return fail(APR_E_ALIAS, "out overlaps W");
   DeviceState* st = nullptr;
   const int rc = device_state(&st);

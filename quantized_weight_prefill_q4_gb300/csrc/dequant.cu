@@ -1,5 +1,6 @@
-// Standalone dequant: out[n][k] = f32(d) * f32(q') (F16: f32(w); Q4_K: d sc q -
-// dmin m rounded once), bit exact against the oracle.
+// Standalone dequant: out[n][k] = f32(d) * f32(q') (F16: f32(w); Q4_K and Q5_K:
+// d sc q - dmin m rounded once; Q6_K: d sc (q - 32), exact), bit exact against
+// the oracle.
 //
 // The device dequant of aprender-serve 0.70.2 src/cuda/executor/gdn_prefill_ops.rs
 // (qwen35_dequant_f32: one 32-element block per warp, one element per lane),
@@ -24,6 +25,19 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
        idx += (size_t)gridDim.x * blockDim.x) {
     if constexpr (QT == kF16) {  // each element its own half: widening is exact
       out[idx] = __half2float(__ushort_as_half(reinterpret_cast<const uint16_t*>(W)[idx]));
+      continue;
+    }
+    if constexpr (QT == kQ6_K) {  // superblock of 256 in 210 bytes, read bytewise (2-byte aligned)
+      const size_t row = idx / (size_t)k;
+      const uint32_t col = (uint32_t)(idx - row * (size_t)k);
+      const uint8_t* sb = W + (row * (size_t)(k / 256) + col / 256) * 210;
+      const uint32_t e = col & 255u, h = e >> 7, c = (e >> 5) & 3u, l = e & 31u;
+      const uint32_t lo = (sb[64 * h + 32 * (c & 1u) + l] >> (4 * (c >> 1))) & 15u;
+      const uint32_t hi = (sb[128 + 32 * h + l] >> (2 * c)) & 3u;
+      const float d = __half2float(__ushort_as_half((uint16_t)(sb[208] | (sb[209] << 8))));
+      const int sc = (int)(int8_t)sb[192 + e / 16];
+      // d sc is exact (11 + 8 bits) and so is its product with q - 32
+      out[idx] = d * (float)sc * (float)((int)(lo | (hi << 4)) - 32);
       continue;
     }
     if constexpr (QT == kQ4_K || QT == kQ5_K) {  // superblock of 256 in 144 or 176 bytes
@@ -65,7 +79,9 @@ cudaError_t launch_dequant(int qtype, const void* W, int n, int k, float* out, c
   const size_t total = (size_t)n * (size_t)k;
   size_t blocks = (total + 255) / 256;
   if (blocks > 152 * 64) blocks = 152 * 64;
-  if (qtype == kQ5_K)
+  if (qtype == kQ6_K)
+    dequant_kernel<kQ6_K><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);
+  else if (qtype == kQ5_K)
     dequant_kernel<kQ5_K><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);
   else if (qtype == kQ4_K)
     dequant_kernel<kQ4_K><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);

@@ -110,16 +110,22 @@ struct Cfg {
   static constexpr int NWG = NM * DQ;                   // dequant / epilogue warpgroups
   static constexpr bool F16W = QT == kF16;
   static constexpr bool Q4W = QT == kQ4_0 || QT == kQ4_K || QT == kQ5_K;  // ring depths of the short-row formats
+  static constexpr bool Q6K = QT == kQ6_K;
   static constexpr int BB = QT == kQ4_0 || QT == kQ4_K ? 18 : (QT == kQ8_0 ? 34 : (QT == kQ5_K ? 22 : 64));
   // words a decode thread reads per stage: two blocks, or for Q4_K / Q5_K the
   // superblock's header and scales (4 words), Q5_K's fifth-bit bytes (8
-  // words) and the stage's 32 code bytes (8 words)
-  static constexpr int NWORDS = QT == kQ4_K ? 12 : (QT == kQ5_K ? 20 : 2 * BB / 4);
+  // words) and the stage's 32 code bytes (8 words); for Q6_K the aligned
+  // words over the stage's 64 low-nibble bytes, 32 high-bit bytes and 4
+  // scales (each one word more: the superblock may start 2 bytes into a
+  // word) and the word holding d
+  static constexpr int NWORDS = QT == kQ4_K ? 12 : (QT == kQ5_K ? 20 : (Q6K ? 29 : 2 * BB / 4));
   // k per raw slot: a chunk, or half of one for an F16 gate/up pair (four
   // slots of 32 KB keep each weight double-buffered)
   static constexpr int RAW_K = F16W && NM == 2 ? CHUNK / 2 : CHUNK;
   static constexpr int RAW_SUBS = RAW_K / BK;         // operand stages per raw slot
-  static constexpr int RAW_ROW = RAW_K / 32 * BB;     // 144 / 272 / 512 (or 256) bytes
+  // 144 / 272 / 512 (or 256) bytes; Q6_K: a 224-byte box from the 16-byte
+  // boundary at or below the 210-byte superblock
+  static constexpr int RAW_ROW = Q6K ? 224 : RAW_K / 32 * BB;
   static constexpr int RAW_BYTES = BM * RAW_ROW;      // one raw slot
   // F16 rows arrive as 64-column boxes of [128 rows][128 B], 128-byte
   // swizzled (conflict-free row reads); block formats as one unswizzled box
@@ -128,6 +134,7 @@ struct Cfg {
   static constexpr int NPIECE = BN / PIECE;
   // operand stages (A in TMEM and B in shared memory advance together)
   static constexpr int S = XS ? 2 : (NM == 2 ? 4 : (BN == 256 ? 4 : (Q4W ? 6 : (F16W ? 4 : 5))));
+  static_assert(!Q6K || RAW_K == 256, "a Q6_K raw slot is one superblock");
   // (with 256-token tiles the raw ring also receives the partner's half of a
   // split). With gate/up the chunks of the two weights alternate through the
   // ring, chunk j in slot j % S_RAW; S_RAW must be even so that a slot always
@@ -135,7 +142,7 @@ struct Cfg {
   // warpgroup. With an odd ring a warpgroup would wait on phase p + 2 of a slot
   // whose phase p + 1 belongs to the other warpgroup, and a parity wait cannot
   // tell phase p + 2 from phase p.
-  static constexpr int S_RAW = NM == 1 ? (Q4W ? (BN == 256 ? 4 : 3) : 2) : 4;
+  static constexpr int S_RAW = NM == 1 ? (Q4W ? (BN == 256 ? 4 : 3) : (Q6K ? 3 : 2)) : 4;
   static_assert(!XS || RAW_K == CHUNK, "the exact leg folds one raw slot per accumulation chunk");
   static_assert(!F16W || BN == 128, "F16 tiles take 128 tokens");
   static constexpr int NTHREADS = 128 + 128 * NWG;
@@ -368,6 +375,49 @@ __device__ __forceinline__ void q4k_row_stage(const uint32_t* w, uint32_t g, flo
   }
 }
 
+// Q6_K: stage g (64 k) of one row's superblock, from shared-memory words that
+// start at the word holding the superblock's first byte, sh bytes (0 or 2)
+// into it: w[0..16] over the low-nibble bytes 64 h .. 64 h + 63 (h = g / 2),
+// w[17..25] over the high-bit bytes 128 + 32 h .. 128 + 32 h + 31, w[26..27]
+// over the scale bytes 192 + 4 g .. 192 + 4 g + 3, w[28] the word holding d.
+// Element i of the stage takes nibble g % 2 of low byte i, bits 2 c of high
+// byte i % 32 (c = 2 (g % 2) + i / 32) and scale 4 g + i / 16; d sc (q - 32)
+// has at most 23 significant bits, so it is exact in fp32, then rounded once
+// to fp16 (xs = false) or scaled by sw = 2^e and split (xs = true).
+template <bool XSP>
+__device__ __forceinline__ void q6k_row_stage(const uint32_t* w, uint32_t g, uint32_t sh, float sw,
+                                              uint32_t (&a1)[32], uint32_t (&a2)[32]) {
+  const uint32_t s8 = 8 * sh;
+  auto at = [&](int m) { return __funnelshift_r(w[m], w[m + 1], s8); };
+  const float d = __half2float(__ushort_as_half((unsigned short)((w[28] >> s8) & 0xFFFFu)));
+  const uint32_t scw = at(26);
+  float A[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) A[j] = d * (float)((int)(scw << (24 - 8 * j)) >> 24);  // int8 scale j
+  const uint32_t nib = 4 * (g & 1u), hb = 4 * (g & 1u);
+  // q - 32 exactly: the float 2^23 + q less 2^23 + 32
+  auto centered = [](uint32_t q) { return __uint_as_float(q | 0x4B000000u) - 8388640.0f; };
+#pragma unroll
+  for (int v = 0; v < 16; ++v) {
+    const uint32_t x = at(v);                       // low bytes of elements 4 v .. 4 v + 3
+    const uint32_t y = at(17 + (v & 7));            // their high-bit bytes (element % 32)
+    const uint32_t hs = hb + 2 * (uint32_t)(v >> 3);  // 2 c
+    float q[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t qv = ((x >> (8 * b + nib)) & 15u) | (((y >> (8 * b + hs)) & 3u) << 4);
+      q[b] = A[v >> 2] * centered(qv);
+    }
+    if constexpr (XSP) {
+      split2(q[0] * sw, q[1] * sw, a1[2 * v], a2[2 * v]);
+      split2(q[2] * sw, q[3] * sw, a1[2 * v + 1], a2[2 * v + 1]);
+    } else {
+      a1[2 * v] = h2_as_u32(__floats2half2_rn(q[0], q[1]));
+      a1[2 * v + 1] = h2_as_u32(__floats2half2_rn(q[2], q[3]));
+    }
+  }
+}
+
 // ---------------------------------------------------------------- kernel
 template <int QT, int EPI, int BN, bool XS>
 __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
@@ -459,6 +509,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
       // x of box b of raw slot u (16-bit elements): the raw row bytes of block
       // formats, the k index itself for F16
       auto raw_x = [&](int u, int b) {
+        if constexpr (C::Q6K) return (((c0 + u) * 210) & ~15) / 2;  // 16-byte aligned; the decode skips the rest
         return C::F16W ? c0 * CHUNK + u * C::RAW_K + b * BK : (c0 + u) * (C::RAW_ROW / 2);
       };
       // an L2 prefetch changes no data, so it may run before the wait
@@ -638,6 +689,17 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
         uint32_t w[C::NWORDS], a[32], a2[32];
         if constexpr (C::F16W) {
           f16_row_stage(raw_slot + s * (C::RAW_BYTES / C::RAW_LOADS), r, w);
+        } else if constexpr (C::Q6K) {
+          // the superblock starts rem = 210 c mod 16 bytes into the box row
+          const uint32_t* sbw = raw_row + ((((c0 + c) * 2) & 15) >> 2);
+          const int h = s >> 1;
+#pragma unroll
+          for (int v = 0; v < 17; ++v) w[v] = sbw[16 * h + v];
+#pragma unroll
+          for (int v = 0; v < 9; ++v) w[17 + v] = sbw[32 + 8 * h + v];
+          w[26] = sbw[48 + s];
+          w[27] = sbw[49 + s];
+          w[28] = sbw[52];
         } else if constexpr (QT == kQ4_K || QT == kQ5_K) {
           constexpr int H = QT == kQ5_K ? 12 : 4;  // words before the code bytes
 #pragma unroll
@@ -648,8 +710,10 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
 #pragma unroll
           for (int v = 0; v < C::NWORDS; ++v) w[v] = raw_row[s * C::NWORDS + v];
         }
-        if constexpr (QT == kQ4_K || QT == kQ5_K)
-          q4k_row_stage<XS, QT == kQ5_K>(w, (uint32_t)s, sw, a, a2);  // overlaps the wait below
+        if constexpr (C::Q6K)
+          q6k_row_stage<XS>(w, (uint32_t)s, (uint32_t)((c0 + c) * 2) & 2u, sw, a, a2);  // overlaps the wait below
+        else if constexpr (QT == kQ4_K || QT == kQ5_K)
+          q4k_row_stage<XS, QT == kQ5_K>(w, (uint32_t)s, sw, a, a2);
         else if constexpr (XS)
           dequant_row_stage_xs<QT>(w, sw, a, a2);  // overlaps the wait below
         else if constexpr (C::F16W)
@@ -876,7 +940,7 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
   auto fn = encode_fn(msg, msg_len);
   if (!fn) return -1;
   CUtensorMap mW, mWu;
-  const uint64_t row_bytes = (uint64_t)(k / 32) * C::BB;
+  const uint64_t row_bytes = C::Q6K ? (uint64_t)(k / 256) * 210 : (uint64_t)(k / 32) * C::BB;
   const CUtensorMapSwizzle wswz = C::F16W ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
   if (!make_map_2d(fn, &mW, CU_TENSOR_MAP_DATA_TYPE_UINT16, W, row_bytes / 2, (uint64_t)n, row_bytes, C::RAW_BOX,
                    BM, wswz, msg, msg_len))
@@ -1016,20 +1080,21 @@ __global__ void row_exp_f16_kernel(const uint16_t* __restrict__ W, int n, int k,
   }
 }
 
-// Q4_K / Q5_K: the same exponent from a bound on the row's largest |w|, the
-// largest over its superblocks of |d| 63 qmax + |dmin| 63 (qmax 15 or 31: every
-// |d sc q - dmin m| is at most that). One warp per row.
-__global__ void row_exp_q4k_kernel(const uint8_t* __restrict__ W, int n, int nsb, int sbb, float qmax,
-                                   int* __restrict__ erow) {
+// K-quants: the same exponent from a bound on the row's largest |w|, the
+// largest over its superblocks of |d| cd + |dmin| cm: Q4_K and Q5_K |d| 63 qmax
+// + |dmin| 63 (qmax 15 or 31), Q6_K |d| 128 x 32 (d at byte 208, no dmin);
+// every weight's magnitude is at most that. One warp per row.
+__global__ void row_exp_kq_kernel(const uint8_t* __restrict__ W, int n, int nsb, int sbb, int doff, float cd,
+                                  float cm, int* __restrict__ erow) {
   const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (row >= n) return;
   const uint8_t* base = W + (size_t)row * nsb * sbb;
   float m = 0.f;
   for (int b = lane; b < nsb; b += 32) {
-    const uint32_t h = *reinterpret_cast<const uint32_t*>(base + (size_t)b * sbb);
-    const float d = fabsf(__half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu))));
-    const float dmin = fabsf(__half2float(__ushort_as_half((unsigned short)(h >> 16))));
-    m = fmaxf(m, d * (63.0f * qmax) + dmin * 63.0f);
+    const uint16_t* p = reinterpret_cast<const uint16_t*>(base + (size_t)b * sbb + doff);  // 2-byte aligned
+    const float d = fabsf(__half2float(__ushort_as_half(p[0])));
+    const float dmin = cm != 0.f ? fabsf(__half2float(__ushort_as_half(p[1]))) : 0.f;
+    m = fmaxf(m, d * cd + dmin * cm);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -1144,11 +1209,13 @@ int launch_gemm_xs(int qtype, const void* W, const void* Wu, int n, int k, const
     row_exp_f16_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint16_t*>(W), n, k, erow);
     if (Wu) row_exp_f16_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint16_t*>(Wu), n, k, erow + n);
   } else if (kquant(qtype)) {
-    const int sbb = qtype == kQ4_K ? 144 : 176;
-    const float qm = qtype == kQ4_K ? 15.f : 31.f;
-    row_exp_q4k_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(W), n, k / 256, sbb, qm, erow);
+    const int sbb = qtype == kQ4_K ? 144 : (qtype == kQ5_K ? 176 : 210), doff = qtype == kQ6_K ? 208 : 0;
+    const float cd = qtype == kQ4_K ? 63.f * 15.f : (qtype == kQ5_K ? 63.f * 31.f : 128.f * 32.f);
+    const float cm = qtype == kQ6_K ? 0.f : 63.f;
+    row_exp_kq_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(W), n, k / 256, sbb, doff, cd, cm, erow);
     if (Wu)
-      row_exp_q4k_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(Wu), n, k / 256, sbb, qm, erow + n);
+      row_exp_kq_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(Wu), n, k / 256, sbb, doff, cd, cm,
+                                                erow + n);
   } else {
     row_exp_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(W), n, k / 32, bb, qmax, erow);
     if (Wu) row_exp_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(Wu), n, k / 32, bb, qmax, erow + n);
@@ -1162,6 +1229,7 @@ int launch_gemm_xs(int qtype, const void* W, const void* Wu, int n, int k, const
   if (qtype == kF16) return launch_xs<kF16>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
   if (qtype == kQ4_K) return launch_xs<kQ4_K>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
   if (qtype == kQ5_K) return launch_xs<kQ5_K>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
+  if (qtype == kQ6_K) return launch_xs<kQ6_K>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
   return qtype == kQ4_0 ? launch_xs<kQ4_0>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len)
                         : launch_xs<kQ8_0>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
 }
@@ -1212,6 +1280,7 @@ int launch_gemm_tc(const GemmPlan& pl, int qtype, const void* W, const void* Wu,
   if (qtype == kF16) return launch_q<kF16>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
   if (qtype == kQ4_K) return launch_q<kQ4_K>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
   if (qtype == kQ5_K) return launch_q<kQ5_K>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
+  if (qtype == kQ6_K) return launch_q<kQ6_K>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
   return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows)
                         : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
 }

@@ -501,6 +501,143 @@ cudaError_t launch_q4k(const void* W, const void* Wu, int n, int k, const float*
   return launch_q4k_t<QT, 16, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
 }
 
+// Q6_K: a warp per row, lane L decoding elements 8 L .. 8 L + 7 of each
+// superblock: low nibbles from bytes 64 h + 32 (c % 2) + 8 (L % 4) .. (h = L /
+// 16, c = L / 4 % 4; nibble c / 2), high bit pairs from bytes 128 + 32 h +
+// 8 (L % 4) .. (bits 2 c), the int8 scale at byte 192 + L / 2 and d at 208.
+// Rows start on 16-byte boundaries, so superblock j starts 2 (j % 2) bytes
+// past a 4-byte one: an 8-byte field is read as three aligned words and
+// shifted. w = d sc (q - 32) is exact in fp32; products accumulate in fp32.
+template <int TMAX, bool SWI>
+__global__ void __launch_bounds__(kWarps * 32) gemv_q6k_kernel(const uint8_t* __restrict__ W,
+                                                               const uint8_t* __restrict__ Wu, int n, int k,
+                                                               const float* __restrict__ X, int T, float* Y, int ldy,
+                                                               const float* R) {
+  constexpr int NM = SWI ? 2 : 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nsb = k / 256;
+  const size_t row_bytes = (size_t)nsb * 210;
+  const uint32_t h = (uint32_t)lane >> 4, c = ((uint32_t)lane >> 2) & 3u, l0 = 8u * ((uint32_t)lane & 3u);
+  const uint32_t loff = 64 * h + 32 * (c & 1u) + l0, hoff = 128 + 32 * h + l0, soff = 192 + ((uint32_t)lane >> 1);
+  const uint32_t lsh = 4 * (c >> 1), hsh = 2 * c;
+  bool waited = false;
+  for (int row = blockIdx.x * kWarps + warp; row < n; row += gridDim.x * kWarps) {
+    float acc[NM][TMAX];
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) acc[m][t] = 0.f;
+    const uint8_t* base[NM];
+    base[0] = W + (size_t)row * row_bytes;
+    if (SWI) base[NM - 1] = Wu + (size_t)row * row_bytes;
+    for (int sb0 = 0; sb0 < nsb; sb0 += 2) {
+      uint32_t lw[2][NM][3], hw[2][NM][3], scb[2][NM];
+      unsigned short db[2][NM];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int m = 0; m < NM; ++m)
+          if (sb0 + u < nsb) {
+            const uint8_t* sb = base[m] + (size_t)(sb0 + u) * 210;
+            const uint32_t sh = 2u * ((uint32_t)(sb0 + u) & 1u);
+            const uint32_t* pl = reinterpret_cast<const uint32_t*>(sb + loff - sh);
+            const uint32_t* ph = reinterpret_cast<const uint32_t*>(sb + hoff - sh);
+#pragma unroll
+            for (int v = 0; v < 3; ++v) {
+              lw[u][m][v] = __ldg(pl + v);
+              hw[u][m][v] = __ldg(ph + v);
+            }
+            scb[u][m] = __ldg(sb + soff);
+            db[u][m] = __ldg(reinterpret_cast<const unsigned short*>(sb + 208));
+          }
+      if (!waited) {
+        grid_dependency_wait_inline();
+        waited = true;
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (sb0 + u >= nsb) break;
+        const uint32_t s8 = 16u * ((uint32_t)(sb0 + u) & 1u);
+        float w[NM][8];
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+          const uint32_t lo[2] = {__funnelshift_r(lw[u][m][0], lw[u][m][1], s8),
+                                  __funnelshift_r(lw[u][m][1], lw[u][m][2], s8)};
+          const uint32_t hi[2] = {__funnelshift_r(hw[u][m][0], hw[u][m][1], s8),
+                                  __funnelshift_r(hw[u][m][1], hw[u][m][2], s8)};
+          const float a = __half2float(__ushort_as_half(db[u][m])) * (float)(int)(int8_t)scb[u][m];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t qv = ((lo[e >> 2] >> (8 * (e & 3) + lsh)) & 15u) |
+                                (((hi[e >> 2] >> (8 * (e & 3) + hsh)) & 3u) << 4);
+            w[m][e] = a * (float)((int)qv - 32);
+          }
+        }
+        const int col = (sb0 + u) * 256 + 8 * lane;
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t) {
+          if (t < T) {
+            const float4* xr = reinterpret_cast<const float4*>(X + (size_t)t * k + col);
+            const float4 xa = __ldg(xr), xb = __ldg(xr + 1);
+            const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+            for (int m = 0; m < NM; ++m) {
+              float v = acc[m][t];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v = fmaf(w[m][e], xv[e], v);
+              acc[m][t] = v;
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) {
+        float v = acc[m][t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        acc[m][t] = v;
+      }
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+      if (lane == t && t < T) {
+        const size_t o = (size_t)t * ldy + row;
+        Y[o] = SWI ? silu_mul(acc[0][t], acc[NM - 1][t]) : acc[0][t] + (R ? R[o] : 0.f);
+      }
+    }
+  }
+  if (!waited) grid_dependency_wait_inline();  // a CTA without rows
+}
+
+template <int TMAX, bool SWI>
+cudaError_t launch_q6k_t(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
+                         const float* R, cudaStream_t s) {
+  long blocks = (n + kWarps - 1) / kWarps;
+  const long cap = (long)num_sms() * 2;
+  if (blocks > cap) blocks = cap;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemv_q6k_kernel<TMAX, SWI>, static_cast<const uint8_t*>(W),
+                            static_cast<const uint8_t*>(Wu), n, k, X, T, Y, ldy, R);
+}
+
+template <bool SWI>
+cudaError_t launch_q6k(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
+                       const float* R, cudaStream_t s) {
+  if (T <= 1) return launch_q6k_t<1, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 2) return launch_q6k_t<2, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 4) return launch_q6k_t<4, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 8) return launch_q6k_t<8, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  return launch_q6k_t<16, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+}
+
 }  // namespace
 
 cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
@@ -516,6 +653,8 @@ cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, 
   if (qtype == kQ5_K)
     return swi ? launch_q4k<kQ5_K, true>(W, Wu, n, k, X, T, Y, ldy, R, s)
                : launch_q4k<kQ5_K, false>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (qtype == kQ6_K)
+    return swi ? launch_q6k<true>(W, Wu, n, k, X, T, Y, ldy, R, s) : launch_q6k<false>(W, Wu, n, k, X, T, Y, ldy, R, s);
   if (qtype == kF16) {
     if (k % 256 == 0)
       return swi ? launch_f16<true>(W, Wu, n, k, X, T, Y, ldy, R, s) : launch_f16<false>(W, Wu, n, k, X, T, Y, ldy, R, s);

@@ -1,10 +1,12 @@
-"""GPU parity of Q4_K and Q5_K weights (256-element superblocks: fp16 d and
-dmin, 6-bit sub-block scales and mins, 4-bit codes, and for Q5_K a fifth code
-bit per element; the layouts read in the oracle) on every route, against the
-float64 oracle.
+"""GPU parity of the K-quant weights on every route, against the float64
+oracle: Q4_K and Q5_K (256-element superblocks: fp16 d and dmin, 6-bit
+sub-block scales and mins, 4-bit codes, and for Q5_K a fifth code bit per
+element) and Q6_K (6-bit codes, an int8 scale per 16 elements, fp16 d; rows
+take k % 2048 == 0); the layouts are those read in the oracle.
 
 Bars:
-* dequant: bit exact (d sc q - dmin m rounded once to f32 on both sides);
+* dequant: bit exact (d sc q - dmin m rounded once to f32 on both sides;
+  Q6_K's d sc (q - 32) is exact);
 * fp16 leg: against the oracle fed fp16-rounded X and weights, each element
   within 3e-5 of the sum of its terms' magnitudes, and the whole output within
   the fp16-leg bar against the float64 oracle (the kernel rounds the fp32 value
@@ -28,9 +30,14 @@ pytestmark = pytest.mark.gpu
 
 
 
-@pytest.fixture(params=[synth.Q4_K, synth.Q5_K], ids=["q4_k", "q5_k"])
+@pytest.fixture(params=[synth.Q4_K, synth.Q5_K, synth.Q6_K], ids=["q4_k", "q5_k", "q6_k"])
 def qk(request):
     return request.param
+
+
+def _k(qk, k):
+    """k as given, or for Q6_K raised to a multiple of 2048."""
+    return max(2048, -(-k // 2048) * 2048) if qk == synth.Q6_K else k
 
 CLASSES = ["subnormal", "small", "typical", "large", "mixed"]
 
@@ -88,6 +95,7 @@ def _call(q, qk, W, n, k, X, T, R=None, leg=0, path=0, Wu=None):
 @pytest.mark.parametrize("cls", CLASSES)
 @pytest.mark.parametrize("n,k", [(1, 256), (37, 768), (130, 4096)])
 def test_dequant_bit_exact_random_superblocks(q, qk, cls, n, k):
+    k = _k(qk, k)
     W = synth.random_blocks(qk, n, k, seed=n + k, scale_class=cls)
     out = torch.full((n, k), float("nan"), device="cuda")
     q.apr_dequant(qk, dev(W), n, k, out)
@@ -99,6 +107,18 @@ def test_dequant_bit_exact_random_superblocks(q, qk, cls, n, k):
 def test_dequant_hand_superblocks(q, qk):
     import test_oracle_pins as pins
 
+    if qk == synth.Q6_K:  # row 0: the int8 scales on their 16 elements; row 1: codes in element order
+        sc = [1, -1, 2, -128, 127, 0, 5, -7, 64, -64, 3, 33, -100, 99, 11, -2]
+        W = np.frombuffer(pins._q6_k_superblock(0x3C00, sc, [33] * 256) * 8 +
+                          pins._q6_k_superblock(0x3C00, [1] * 16, [e % 64 for e in range(256)]) * 8,
+                          np.uint8).reshape(2, 8 * 210).copy()
+        out = torch.empty((2, 2048), device="cuda")
+        q.apr_dequant(qk, dev(W), 2, 2048, out)
+        q.apr_stream_status()
+        got = out.cpu().numpy()
+        np.testing.assert_array_equal(got[0], np.tile(np.repeat(np.array(sc, np.float32), 16), 8))
+        np.testing.assert_array_equal(got[1], np.tile(np.array([e % 64 - 32 for e in range(256)], np.float32), 8))
+        return
     five = qk == synth.Q5_K
     build, qmax, sbb = (pins._q5_k_superblock, 32, 176) if five else (pins._q4_k_superblock, 16, 144)
     sc = [1, 2, 3, 4, 17, 33, 48, 63]
@@ -118,6 +138,7 @@ def test_dequant_hand_superblocks(q, qk):
 @pytest.mark.parametrize("n,k,T,res", [(300, 768, 200, True), (4096, 4096, 512, True), (128, 256, 9, False),
                                        (1000, 1024, 130, False), (256, 512, 100, True)])
 def test_gemm_synthetic(q, qk, n, k, T, res):
+    k = _k(qk, k)
     W, X, R = _synthetic(qk, n, k, T, seed=n + T, residual=res)
     y = _call(q, qk, W, n, k, X, T, R, leg=q.APR_LEG_F16, path=q.APR_PATH_GEMM)
     _check_f16(qk, W, n, k, X, R, y)
@@ -126,6 +147,7 @@ def test_gemm_synthetic(q, qk, n, k, T, res):
 @pytest.mark.parametrize("cls", ["small", "typical", "large", "mixed"])
 def test_gemm_random_superblocks(q, qk, cls):
     n, k, T = 300, 1024, 150
+    k = _k(qk, k)
     W = synth.random_blocks(qk, n, k, 60, cls, fp16_range=True)
     X = synth.activations(T, k, 61)
     R = synth.activations(T, n, 62)
@@ -135,6 +157,7 @@ def test_gemm_random_superblocks(q, qk, cls):
 
 def test_gate_up_swiglu(q, qk):
     n, k, T = 384, 1024, 200
+    k = _k(qk, k)
     Wg = synth.quantize(qk, synth.weight_f32(n, k, 5))
     Wu = synth.quantize(qk, synth.weight_f32(n, k, 6))
     X = synth.activations(T, k, 7)
@@ -150,6 +173,7 @@ def test_gate_up_swiglu(q, qk):
 
 def test_f16_input_entry_and_noalloc(q, qk):
     n, k, T = 300, 512, 64
+    k = _k(qk, k)
     W, X, R = _synthetic(qk, n, k, T, seed=9, residual=True)
     X16 = torch.empty((T, k), dtype=torch.float16, device="cuda")
     q.apr_convert_f32_to_f16(dev(X), T * k, X16)
@@ -169,6 +193,7 @@ def test_f16_input_entry_and_noalloc(q, qk):
 @pytest.mark.parametrize("cls", CLASSES)
 @pytest.mark.parametrize("n,k,T,res", [(130, 1024, 129, True), (200, 512, 40, False)])
 def test_exact_gemm(q, qk, cls, n, k, T, res):
+    k = _k(qk, k)
     W = synth.random_blocks(qk, n, k, 7 * n + T, cls)
     X = synth.activations(T, k, 8)
     R = synth.activations(T, n, 9) if res else None
@@ -178,6 +203,7 @@ def test_exact_gemm(q, qk, cls, n, k, T, res):
 
 def test_exact_gate_up(q, qk):
     n, k, T = 200, 512, 40
+    k = _k(qk, k)
     Wg = synth.random_blocks(qk, n, k, 15, "typical")
     Wu = synth.random_blocks(qk, n, k, 16, "typical")
     X = synth.activations(T, k, 17)
@@ -190,6 +216,7 @@ def test_exact_gate_up(q, qk):
 @pytest.mark.parametrize("n,k,T", [(300, 512, 1), (300, 512, 2), (300, 1024, 4), (300, 512, 8), (300, 512, 13),
                                    (77, 256, 1), (64, 12288, 3)])
 def test_gemv(q, qk, cls, n, k, T):
+    k = _k(qk, k)
     W = synth.random_blocks(qk, n, k, 3 * n + k + T, cls)
     X = synth.activations(T, k, 5)
     R = synth.activations(T, n, 6)
@@ -217,7 +244,7 @@ def test_auto_rule_and_gemv_gate_up(q, qk, T):
 # ------------------------------------------------------------------ composites
 @pytest.mark.parametrize("leg,T", [(0, 40), (1, 40), (0, 3), (1, 3)])
 def test_ffn_sublayer(q, qk, leg, T):
-    hidden, inter = 256, 512
+    hidden, inter = _k(qk, 256), _k(qk, 512)
     Ws = [synth.quantize(qk, synth.weight_f32(r, c, 30 + i))
           for i, (r, c) in enumerate(((inter, hidden), (inter, hidden), (hidden, inter)))]
     X = synth.activations(T, hidden, 33)
@@ -232,6 +259,7 @@ def test_ffn_sublayer(q, qk, leg, T):
 
 def test_normed_projection(q, qk):
     n, k, T = 300, 512, 50
+    k = _k(qk, k)
     W = synth.random_blocks(qk, n, k, 41, "typical")
     X = synth.activations(T, k, 42)
     w = (1.0 + 0.5 * synth.activations(1, k, 43)[0]).astype(np.float32)
@@ -246,5 +274,8 @@ def test_normed_projection(q, qk):
 def test_prefill_layer(q, qk, leg):
     import test_gpu_layer as lay
 
-    c = lay._case(qk, 512, 1024, 4, 2, 200, 37, seed=71)
+    if qk == synth.Q6_K:  # hidden, inter and 8 heads x 256 multiples of 2048
+        c = lay._case(qk, 2048, 2048, 8, 2, 100, 37, seed=71)
+    else:
+        c = lay._case(qk, 512, 1024, 4, 2, 200, 37, seed=71)
     lay._check(c, lay._run(q, c, leg=leg, chunk=128), leg)
