@@ -67,45 +67,67 @@ __device__ __forceinline__ int dp4a_ss(uint32_t a, int b, int c) {
   return d;
 }
 
-// One block's table entry, built by 8 consecutive lanes (u = lane % 8), each
-// from its 4 values of X (elements 4u .. 4u + 3 of the block): the block's
-// largest |x| and the digit sums by shuffles within the 8 lanes.
-template <int QT>
-__device__ __forceinline__ void block_digits8(float4 x, int u, uint32_t* out) {
-  float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+// The table entries of NB blocks, each built by 8 consecutive lanes (u =
+// lane % 8), each lane from its 4 values of X (elements 4u .. 4u + 3 of the
+// block): the block's largest |x| and the digit sums by shuffles within the 8
+// lanes. The blocks' shuffle chains are interleaved (they are independent);
+// out[i] == nullptr skips block i's stores (its shuffles still run: the 8-lane
+// groups of a warp take part in every shuffle).
+template <int QT, int NB>
+__device__ __forceinline__ void block_digits8(const float4 (&x)[NB], int u, uint32_t* const (&out)[NB]) {
+  float m[NB];
 #pragma unroll
-  for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  int e = 0;
-  if (m > 0.f) e = 21 - ((int)((__float_as_uint(m) >> 23) & 0xFFu) - 127);
-  e = e < -126 ? -126 : (e > 126 ? 126 : e);
-  const float sc = __int_as_float((127 + e) << 23);
-  const float xv[4] = {x.x, x.y, x.z, x.w};
-  uint32_t dig[3] = {0u, 0u, 0u};
-  int psum[3] = {0, 0, 0};
+  for (int i = 0; i < NB; ++i) m[i] = fmaxf(fmaxf(fabsf(x[i].x), fabsf(x[i].y)), fmaxf(fabsf(x[i].z), fabsf(x[i].w)));
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const int X = __float2int_rn(xv[b] * sc);
-    const int p0 = (X << 24) >> 24;
-    const int x1 = (X - p0) >> 8;
-    const int p1 = (x1 << 24) >> 24;
-    const int p2 = (x1 - p1) >> 8;
-    dig[0] |= (uint32_t)(p0 & 0xFF) << (8 * b);
-    dig[1] |= (uint32_t)(p1 & 0xFF) << (8 * b);
-    dig[2] |= (uint32_t)(p2 & 0xFF) << (8 * b);
-    psum[0] += p0;
-    psum[1] += p1;
-    psum[2] += p2;
+  for (int o = 1; o < 8; o <<= 1)
+#pragma unroll
+    for (int i = 0; i < NB; ++i) m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], o));
+  uint32_t dig[NB][3];
+  int psum[NB][3], e[NB];
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    int ei = 0;
+    if (m[i] > 0.f) ei = 21 - ((int)((__float_as_uint(m[i]) >> 23) & 0xFFu) - 127);
+    ei = ei < -126 ? -126 : (ei > 126 ? 126 : ei);
+    e[i] = ei;
+    const float sc = __int_as_float((127 + ei) << 23);
+    const float xv[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+#pragma unroll
+    for (int kd = 0; kd < 3; ++kd) {
+      dig[i][kd] = 0u;
+      psum[i][kd] = 0;
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int X = __float2int_rn(xv[b] * sc);
+      const int p0 = (X << 24) >> 24;
+      const int x1 = (X - p0) >> 8;
+      const int p1 = (x1 << 24) >> 24;
+      const int p2 = (x1 - p1) >> 8;
+      dig[i][0] |= (uint32_t)(p0 & 0xFF) << (8 * b);
+      dig[i][1] |= (uint32_t)(p1 & 0xFF) << (8 * b);
+      dig[i][2] |= (uint32_t)(p2 & 0xFF) << (8 * b);
+      psum[i][0] += p0;
+      psum[i][1] += p1;
+      psum[i][2] += p2;
+    }
   }
 #pragma unroll
-  for (int kd = 0; kd < 3; ++kd) {
-    out[8 * kd + u] = dig[kd];
+  for (int o = 1; o < 8; o <<= 1)
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) psum[kd] += __shfl_xor_sync(0xffffffffu, psum[kd], o);
-  }
-  if (u == 0) {
+    for (int i = 0; i < NB; ++i)
 #pragma unroll
-    for (int kd = 0; kd < 3; ++kd) out[24 + kd] = (uint32_t)(QT == kQ4_0 ? -8 * psum[kd] : 0);
-    out[27] = __float_as_uint(__int_as_float((127 - e) << 23));  // 2^-e
+      for (int kd = 0; kd < 3; ++kd) psum[i][kd] += __shfl_xor_sync(0xffffffffu, psum[i][kd], o);
+#pragma unroll
+  for (int i = 0; i < NB; ++i) {
+    if (!out[i]) continue;
+#pragma unroll
+    for (int kd = 0; kd < 3; ++kd) out[i][8 * kd + u] = dig[i][kd];
+    if (u == 0) {
+#pragma unroll
+      for (int kd = 0; kd < 3; ++kd) out[i][24 + kd] = (uint32_t)(QT == kQ4_0 ? -8 * psum[i][kd] : 0);
+      out[i][27] = __float_as_uint(__int_as_float((127 - e[i]) << 23));  // 2^-e
+    }
   }
 }
 
@@ -218,16 +240,15 @@ __global__ void __launch_bounds__(ITHREADS, 2)
   // loads of four passes are issued before any is used
   for (int base = (int)threadIdx.x / 8; base < nblk; base += 4 * (ICW * 32 / 8)) {
     float4 xv[4];
+    uint32_t* dst[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int b0 = base + u * (ICW * 32 / 8);
-      if (b0 < nblk) xv[u] = __ldg(reinterpret_cast<const float4*>(X) + (size_t)b0 * 8 + (threadIdx.x & 7));
+      xv[u] = b0 < nblk ? __ldg(reinterpret_cast<const float4*>(X) + (size_t)b0 * 8 + (threadIdx.x & 7))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      dst[u] = b0 < nblk ? xt + (size_t)b0 * XBW : nullptr;
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int b0 = base + u * (ICW * 32 / 8);
-      if (b0 < nblk) block_digits8<QT>(xv[u], threadIdx.x & 7, xt + (size_t)b0 * XBW);
-    }
+    block_digits8<QT, 4>(xv, threadIdx.x & 7, dst);
   }
   if (!SWI && R)
     for (int i = threadIdx.x; i < r1 - r0; i += ICW * 32) rres[i] = R[r0 + i];
