@@ -1,7 +1,11 @@
-// Single-token GEMV (T = 1) over Q4_0 / Q8_0 blocks with integer dot
-// products, exact to fp32 level (the single-token GEMVs gemv_q4_0_pf /
-// gemv_q8_0_pf of oxibonsai-kernels 0.1.4 src/gpu_backend/cuda_q_std_prefill.rs,
-// HBM-bound form).
+// Single-token GEMV (T = 1) over Q4_0 / Q8_0 blocks and Q4_K / Q5_K / Q6_K
+// superblocks with integer dot products, exact to fp32 level (the
+// single-token GEMVs gemv_q4_0_pf / gemv_q8_0_pf of oxibonsai-kernels 0.1.4
+// src/gpu_backend/cuda_q_std_prefill.rs, HBM-bound form). A K-quant lane
+// takes the 64 weights of one X block pair (Q4_K / Q5_K: one code group of a
+// superblock, two 32-weight sub-blocks; Q6_K: one 64-weight stage, four
+// 16-weight sub-blocks) and applies the sub-block scales, and for Q4_K / Q5_K
+// the mins against the block's sum of X, after the integer sums.
 //
 // X in fixed point per 32-block: for block b, e_b makes max_j |x_j| 2^e_b lie
 // in [2^21, 2^22), and X_j = rint(x_j 2^e_b) (a 23-bit integer, off by at most
@@ -45,6 +49,7 @@
 #include "apr_internal.h"
 #include "dev_common.cuh"
 #include "host_common.h"
+#include "q4k.cuh"
 
 namespace apr {
 namespace {
@@ -124,8 +129,16 @@ __device__ __forceinline__ void block_digits8(const float4 (&x)[NB], int u, uint
 #pragma unroll
     for (int kd = 0; kd < 3; ++kd) out[i][8 * kd + u] = dig[i][kd];
     if (u == 0) {
+      if constexpr (QT == kQ4_K || QT == kQ5_K) {
+        // the block's sum of X_j (an integer below 2^27, rounded to float)
+        // for the dmin m term; no start values
+        out[i][24] = __float_as_uint((float)(65536 * psum[i][2] + 256 * psum[i][1] + psum[i][0]));
+        out[i][25] = 0u;
+        out[i][26] = 0u;
+      } else {
 #pragma unroll
-      for (int kd = 0; kd < 3; ++kd) out[i][24 + kd] = (uint32_t)(QT == kQ4_0 ? -8 * psum[i][kd] : 0);
+        for (int kd = 0; kd < 3; ++kd) out[i][24 + kd] = (uint32_t)(QT == kQ4_0 ? -8 * psum[i][kd] : 0);
+      }
       out[i][27] = __float_as_uint(__int_as_float((127 - e[i]) << 23));  // 2^-e
     }
   }
@@ -160,8 +173,86 @@ __device__ __forceinline__ float block_dot(const uint32_t* p, const uint32_t (&t
   return v * (d * __uint_as_float(t[27]));
 }
 
+// Q4_K / Q5_K: the sum over a lane's 64 weights (group g of a superblock:
+// sub-block 2 g in the low nibbles of its 32 code bytes, 2 g + 1 in the high
+// ones; X blocks A and B). w[0] = d | dmin << 16, w[1..3] the packed scales,
+// (Q5_K) w[4..11] the fifth-bit bytes, then the group's 8 code words. For
+// each sub-block sum_j w_j x_j = 2^-e (d sc sum_j q_j X_j - dmin m sum_j X_j),
+// with the digit sums of q_j X_j exact in int32 (dp4a of the unsigned codes)
+// and the products and the difference rounded at fp32 level.
+template <int QT>
+__device__ __forceinline__ float kq_pair_dot(const uint32_t* w, uint32_t g, const uint32_t (&ta)[XBW],
+                                             const uint32_t (&tb)[XBW]) {
+  constexpr bool FIVE = QT == kQ5_K;
+  constexpr int CW = FIVE ? 12 : 4;  // first code word
+  const float d = __half2float(__ushort_as_half((unsigned short)(w[0] & 0xFFFFu)));
+  const float dmin = __half2float(__ushort_as_half((unsigned short)(w[0] >> 16)));
+  uint32_t scA, mA, scB, mB;
+  const uint32_t sw[3] = {w[1], w[2], w[3]};
+  q4k_scale_min_w(sw, 2 * g, scA, mA);
+  q4k_scale_min_w(sw, 2 * g + 1, scB, mB);
+  int a0 = 0, a1 = 0, a2 = 0, b0 = 0, b1 = 0, b2 = 0;
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    uint32_t lo = w[CW + v] & 0x0F0F0F0Fu, hi = (w[CW + v] >> 4) & 0x0F0F0F0Fu;
+    if constexpr (FIVE) {  // the fifth bits: bit 2 g (low) and 2 g + 1 (high) of each byte
+      lo |= ((w[4 + v] >> (2 * g)) & 0x01010101u) << 4;
+      hi |= ((w[4 + v] >> (2 * g + 1)) & 0x01010101u) << 4;
+    }
+    a0 = dp4a_us(lo, (int)ta[v], a0);
+    a1 = dp4a_us(lo, (int)ta[8 + v], a1);
+    a2 = dp4a_us(lo, (int)ta[16 + v], a2);
+    b0 = dp4a_us(hi, (int)tb[v], b0);
+    b1 = dp4a_us(hi, (int)tb[8 + v], b1);
+    b2 = dp4a_us(hi, (int)tb[16 + v], b2);
+  }
+  const float vA = fmaf((float)a2, 65536.f, fmaf((float)a1, 256.f, (float)a0));
+  const float vB = fmaf((float)b2, 65536.f, fmaf((float)b1, 256.f, (float)b0));
+  const float sA = fmaf(d * (float)scA, vA, -(dmin * (float)mA) * __uint_as_float(ta[24]));
+  const float sB = fmaf(d * (float)scB, vB, -(dmin * (float)mB) * __uint_as_float(tb[24]));
+  return fmaf(sA, __uint_as_float(ta[27]), sB * __uint_as_float(tb[27]));
+}
+
+// Q6_K: the sum over a lane's 64 weights (stage g of a superblock, X blocks A
+// and B), from shared-memory words that start at the word holding the
+// superblock's first byte, sh bytes (0 or 2) into it: w[0..16] over the low
+// nibble bytes 64 h .. (h = g / 2), w[17..25] over the high-bit bytes 128 +
+// 32 h .., w[26..27] over the scale bytes 192 + 4 g .., w[28] the word holding
+// d. The codes are centred to q - 32 as signed bytes, so each 16-weight
+// sub-block is d sc_j 2^-e sum (q - 32) X, its digit sums exact in int32.
+__device__ __forceinline__ float q6k_pair_dot(const uint32_t* w, uint32_t g, uint32_t sh, const uint32_t (&ta)[XBW],
+                                              const uint32_t (&tb)[XBW]) {
+  const uint32_t s8 = 8 * sh;
+  auto at = [&](int m) { return __funnelshift_r(w[m], w[m + 1], s8); };
+  const float d = __half2float(__ushort_as_half((unsigned short)((w[28] >> s8) & 0xFFFFu)));
+  const uint32_t scw = at(26);
+  const uint32_t nib = 4 * (g & 1u), hb = 4 * (g & 1u);
+  int acc[4][3];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = 0;
+#pragma unroll
+  for (int v = 0; v < 16; ++v) {
+    const uint32_t q = ((at(v) >> nib) & 0x0F0F0F0Fu) | (((at(17 + (v & 7)) >> (hb + 2 * (v >> 3))) & 0x03030303u) << 4);
+    // q - 32 in each byte: (q | 0x80) - 0x20 cannot borrow, and ^ 0x80 makes it signed
+    const uint32_t c = ((q | 0x80808080u) - 0x20202020u) ^ 0x80808080u;
+    const uint32_t (&t)[XBW] = v < 8 ? ta : tb;
+    const int j = v >> 2, u = v & 7;
+    acc[j][0] = dp4a_ss(c, (int)t[u], acc[j][0]);
+    acc[j][1] = dp4a_ss(c, (int)t[8 + u], acc[j][1]);
+    acc[j][2] = dp4a_ss(c, (int)t[16 + u], acc[j][2]);
+  }
+  float r = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float v = fmaf((float)acc[j][2], 65536.f, fmaf((float)acc[j][1], 256.f, (float)acc[j][0]));
+    const float sc = (float)((int)(scw << (24 - 8 * j)) >> 24);
+    r = fmaf(d * sc * __uint_as_float((j < 2 ? ta : tb)[27]), v, r);
+  }
+  return r;
+}
+
 int rows_per_stage(int qtype, int k, bool swiglu) {
-  const long row_bytes = (long)(k / 32) * block_bytes(qtype);
+  const long row_bytes = (long)row_bytes_of(qtype, k);
   return (int)(ISTAGE / ((swiglu ? 2 : 1) * row_bytes));
 }
 
@@ -170,8 +261,10 @@ __global__ void __launch_bounds__(ITHREADS, 2)
     gemv_i8_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ Wu, int n, int k,
                    const float* __restrict__ X, float* Y, const float* R, unsigned* status, int rs, int ns) {
   constexpr int NM = SWI ? 2 : 1;
-  constexpr int BB = QT == kQ4_0 ? 18 : 34;
-  constexpr int PW_WORDS = 2 * BB / 4;  // words of one block pair
+  constexpr bool KQ = QT == kQ4_K || QT == kQ5_K || QT == kQ6_K;
+  constexpr int BB = QT == kQ4_0 ? 18 : 34;                           // block formats
+  constexpr int SBB = QT == kQ4_K ? 144 : (QT == kQ5_K ? 176 : 210);  // K-quant superblocks
+  constexpr int PW_WORDS = 2 * BB / 4;                                // words of one block pair
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   const int nblk = k / 32, npk = nblk / 2;
@@ -185,7 +278,7 @@ __global__ void __launch_bounds__(ITHREADS, 2)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * INS_MAX);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const size_t row_bytes = (size_t)nblk * BB;
+  const size_t row_bytes = KQ ? (size_t)(k / 256) * SBB : (size_t)nblk * BB;
   const int r0 = (int)((long)n * blockIdx.x / gridDim.x);
   const int r1 = (int)((long)n * (blockIdx.x + 1) / gridDim.x);
   const int nst = (r1 - r0 + rs - 1) / rs;
@@ -267,8 +360,33 @@ __global__ void __launch_bounds__(ITHREADS, 2)
   // one row's partial of this lane (its block pair), weight m
   auto row_part = [&](int st, int m, int rr) -> float {
     if (!act) return 0.f;
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(smem + st * ISTAGE + (size_t)(m * rs + rr) * row_bytes) +
-                        P * PW_WORDS;
+    const uint32_t* rw = reinterpret_cast<const uint32_t*>(smem + st * ISTAGE + (size_t)(m * rs + rr) * row_bytes);
+    if constexpr (QT == kQ6_K) {
+      // superblock P / 4 from the word holding its first byte (2 (P / 4 mod
+      // 2) bytes into it: rows start on 16-byte boundaries); stage P mod 4
+      const uint32_t* w = rw + (((uint32_t)P >> 2) * 210u >> 2);
+      const int h = (P & 3) >> 1;
+      uint32_t wq[29];
+#pragma unroll
+      for (int v = 0; v < 17; ++v) wq[v] = w[16 * h + v];
+#pragma unroll
+      for (int v = 0; v < 9; ++v) wq[17 + v] = w[32 + 8 * h + v];
+      wq[26] = w[48 + (P & 3)];
+      wq[27] = w[49 + (P & 3)];
+      wq[28] = w[52];
+      return q6k_pair_dot(wq, (uint32_t)P & 3u, 2u * (((uint32_t)P >> 2) & 1u), ta, tb);
+    } else if constexpr (KQ) {
+      // superblock P / 4: header and scales, (Q5_K) fifth bits, then group P mod 4's codes
+      constexpr int CW = QT == kQ5_K ? 12 : 4;
+      const uint32_t* w = rw + ((uint32_t)P >> 2) * (SBB / 4);
+      uint32_t wq[CW + 8];
+#pragma unroll
+      for (int v = 0; v < CW; ++v) wq[v] = w[v];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) wq[CW + v] = w[CW + 8 * (P & 3) + v];
+      return kq_pair_dot<QT>(wq, (uint32_t)P & 3u, ta, tb);
+    }
+    const uint32_t* w = rw + P * PW_WORDS;
     uint32_t wr[PW_WORDS];
 #pragma unroll
     for (int i = 0; i < PW_WORDS; ++i) wr[i] = w[i];
@@ -477,7 +595,7 @@ cudaError_t launch_read_stream(const void* src, long long bytes, unsigned* statu
 bool gemv_i8_fits(int qtype, int n, int k, int T, bool swiglu) {
   // block formats, one token; k % 256 == 0 (whole rows 16-byte aligned in a stage); a row's
   // warps within the consumer warps; at most IMAXROWS rows a CTA
-  if (!block32_format(qtype) || T != 1 || k % 256 != 0 || (k / 64 + 31) / 32 > 8) return false;
+  if ((!block32_format(qtype) && !kquant(qtype)) || T != 1 || k % 256 != 0 || (k / 64 + 31) / 32 > 8) return false;
   if ((n + num_sms() - 1) / num_sms() > IMAXROWS) return false;
   return rows_per_stage(qtype, k, swiglu) >= 1 && i8_stages(k) >= 4;
 }
@@ -485,6 +603,15 @@ bool gemv_i8_fits(int qtype, int n, int k, int T, bool swiglu) {
 cudaError_t launch_gemv_i8(int qtype, const void* W, const void* Wu, int n, int k, const float* X, float* Y,
                            const float* R, unsigned* status, cudaStream_t s) {
   const bool swi = Wu != nullptr;
+  if (qtype == kQ4_K)
+    return swi ? launch_i8<kQ4_K, true>(W, Wu, n, k, X, Y, R, status, s)
+               : launch_i8<kQ4_K, false>(W, Wu, n, k, X, Y, R, status, s);
+  if (qtype == kQ5_K)
+    return swi ? launch_i8<kQ5_K, true>(W, Wu, n, k, X, Y, R, status, s)
+               : launch_i8<kQ5_K, false>(W, Wu, n, k, X, Y, R, status, s);
+  if (qtype == kQ6_K)
+    return swi ? launch_i8<kQ6_K, true>(W, Wu, n, k, X, Y, R, status, s)
+               : launch_i8<kQ6_K, false>(W, Wu, n, k, X, Y, R, status, s);
   if (qtype == kQ4_0)
     return swi ? launch_i8<kQ4_0, true>(W, Wu, n, k, X, Y, R, status, s)
                : launch_i8<kQ4_0, false>(W, Wu, n, k, X, Y, R, status, s);
