@@ -370,13 +370,18 @@ cudaError_t launch_f16(const void* W, const void* Wu, int n, int k, const float*
 // (sub-block 2 g + 1); Q5_K adds bit 2 g (or 2 g + 1) of the fifth-bit bytes
 // 8 (l mod 4) .. as 16. Each weight is d sc q - dmin m rounded once to fp32
 // (one fma of two exact products), then exact fp32 products with X. The loads
-// of two superblocks are issued before either is used.
+// of several superblocks are issued before any is used.
+// K-quant GEMVs: superblocks whose loads are issued together before any is
+// decoded, by the number of tokens (measured on 4096 and 12288 rows x 4096:
+// 8 at T <= 2, 4 above; 2 took 12-40 % longer at T = 2 and 8)
+constexpr int kq_unroll(int tmax) { return tmax <= 2 ? 8 : 4; }
 template <int QT, int TMAX, bool SWI>
 __global__ void __launch_bounds__(kWarps * 32) gemv_q4k_kernel(const uint8_t* __restrict__ W,
                                                                const uint8_t* __restrict__ Wu, int n, int k,
                                                                const float* __restrict__ X, int T, float* Y, int ldy,
                                                                const float* R) {
   constexpr int NM = SWI ? 2 : 1;
+  constexpr int U = kq_unroll(TMAX);
   constexpr bool FIVE = QT == kQ5_K;
   constexpr uint32_t SBB = FIVE ? 176 : 144;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -394,11 +399,11 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q4k_kernel(const uint8_t* __
     const uint8_t* base[NM];
     base[0] = W + (size_t)row * row_bytes;
     if (SWI) base[NM - 1] = Wu + (size_t)row * row_bytes;
-    for (int sb0 = 0; sb0 < nsb; sb0 += 2) {
-      uint4 h[2][NM];
-      uint2 c[2][NM], f[2][NM];
+    for (int sb0 = 0; sb0 < nsb; sb0 += U) {
+      uint4 h[U][NM];
+      uint2 c[U][NM], f[U][NM];
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
+      for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int m = 0; m < NM; ++m)
           if (sb0 + u < nsb) {
@@ -412,7 +417,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q4k_kernel(const uint8_t* __
         waited = true;
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < U; ++u) {
         if (sb0 + u >= nsb) break;
         float w[NM][8];
 #pragma unroll
@@ -514,6 +519,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q6k_kernel(const uint8_t* __
                                                                const float* __restrict__ X, int T, float* Y, int ldy,
                                                                const float* R) {
   constexpr int NM = SWI ? 2 : 1;
+  constexpr int U = kq_unroll(TMAX);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nsb = k / 256;
   const size_t row_bytes = (size_t)nsb * 210;
@@ -530,11 +536,11 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q6k_kernel(const uint8_t* __
     const uint8_t* base[NM];
     base[0] = W + (size_t)row * row_bytes;
     if (SWI) base[NM - 1] = Wu + (size_t)row * row_bytes;
-    for (int sb0 = 0; sb0 < nsb; sb0 += 2) {
-      uint32_t lw[2][NM][3], hw[2][NM][3], scb[2][NM];
-      unsigned short db[2][NM];
+    for (int sb0 = 0; sb0 < nsb; sb0 += U) {
+      uint32_t lw[U][NM][3], hw[U][NM][3], scb[U][NM];
+      unsigned short db[U][NM];
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
+      for (int u = 0; u < U; ++u)
 #pragma unroll
         for (int m = 0; m < NM; ++m)
           if (sb0 + u < nsb) {
@@ -555,7 +561,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q6k_kernel(const uint8_t* __
         waited = true;
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < U; ++u) {
         if (sb0 + u >= nsb) break;
         const uint32_t s8 = 16u * ((uint32_t)(sb0 + u) & 1u);
         float w[NM][8];
