@@ -227,6 +227,26 @@ def test_gemv(q, qk, cls, n, k, T):
     _check_exact(qk, W, n, k, X, R, Y.cpu().numpy())
 
 
+@pytest.mark.parametrize("n,k", [(300, 12288), (20000, 2048)])
+def test_one_token_gemv_large_shapes(q, qk, n, k):
+    """T = 1 with long rows (one Q6_K row a stage at k = 12288), a gate/up
+    pair, and more rows than the integer-dot kernel takes (the warp-per-row
+    kernel then runs)."""
+    k = _k(qk, k)
+    W = synth.random_blocks(qk, n, k, 11 + n, "typical")
+    X = synth.activations(1, k, 12)
+    R = synth.activations(1, n, 13)
+    buf, Y = guarded(1, n)
+    q.apr_qgemv(qk, dev(W), n, k, dev(X), 1, Y, dev(R))
+    q.apr_stream_status()
+    check_guards(buf, 1, n)
+    _check_exact(qk, W, n, k, X, R, Y.cpu().numpy())
+    if n <= 300:
+        Wu = synth.random_blocks(qk, n, k, 17 + n, "typical")
+        y = _call(q, qk, W, n, k, X, 1, leg=q.APR_LEG_EXACT_F32, path=q.APR_PATH_GEMV, Wu=Wu)
+        assert_exact_leg(y, oracle.gate_up_swiglu_f64(qk, W, Wu, n, k, X))
+
+
 @pytest.mark.parametrize("T", [1, 4, 7])
 def test_auto_rule_and_gemv_gate_up(q, qk, T):
     n, k = 4096, 4096
