@@ -393,8 +393,8 @@ cudaError_t launch_f16(const void* W, const void* Wu, int n, int k, const float*
   return launch_f16_t<16, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
 }
 
-// Q4_K and Q5_K weights: a warp per weight row, one 256-element superblock
-// (144 or 176 bytes) a step; lane l takes elements 8 l .. 8 l + 7 of it: group
+// Q4_K and Q5_K weights: a warp per weight row (two rows at T >= 2), one
+// 256-element superblock (144 or 176 bytes) a step; lane l takes elements 8 l .. 8 l + 7 of it: group
 // g = l / 8 (64 elements), low nibbles of code bytes 32 g + 8 (l mod 4) .. for
 // l mod 8 < 4 (sub-block 2 g), high nibbles of the same bytes otherwise
 // (sub-block 2 g + 1); Q5_K adds bit 2 g (or 2 g + 1) of the fifth-bit bytes
@@ -405,13 +405,44 @@ cudaError_t launch_f16(const void* W, const void* Wu, int n, int k, const float*
 // decoded, by the number of tokens (measured on 4096 and 12288 rows x 4096:
 // 8 at T <= 2, 4 above; 2 took 12-40 % longer at T = 2 and 8)
 __host__ __device__ constexpr int kq_unroll(int tmax) { return tmax <= 2 ? 8 : 4; }
+// rows a warp takes together at T >= 2: they share each load of X (4096 x
+// 4096, Q4_K: 21.9 -> 16.7 us at T = 4, 38.4 -> 25.5 us at T = 8)
+__host__ __device__ constexpr int kq_rows(int tmax) { return tmax >= 2 ? 2 : 1; }
+// Reduces a warp's lane partials of RB rows (NM weights each) over the warp
+// and writes rows row0 .. row0 + RB - 1 below n: token t's value by lane t.
+template <int TMAX, int NM, int RB, bool SWI>
+__device__ __forceinline__ void kq_rows_out(float (&acc)[RB * NM][TMAX], int row0, int n, int T, int lane, float* Y,
+                                            int ldy, const float* R) {
+#pragma unroll
+  for (int m = 0; m < RB * NM; ++m)
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+      float v = acc[m][t];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      acc[m][t] = v;
+    }
+#pragma unroll
+  for (int r = 0; r < RB; ++r) {
+    if (row0 + r >= n) break;
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+      if (lane == t && t < T) {
+        const size_t o = (size_t)t * ldy + row0 + r;
+        Y[o] = SWI ? silu_mul(acc[r * NM][t], acc[r * NM + NM - 1][t]) : acc[r * NM][t] + (R ? R[o] : 0.f);
+      }
+    }
+  }
+}
+
 template <int QT, int TMAX, bool SWI>
 __global__ void __launch_bounds__(kWarps * 32) gemv_q4k_kernel(const uint8_t* __restrict__ W,
                                                                const uint8_t* __restrict__ Wu, int n, int k,
                                                                const float* __restrict__ X, int T, float* Y, int ldy,
                                                                const float* R) {
   constexpr int NM = SWI ? 2 : 1;
-  constexpr int U = kq_unroll(TMAX);
+  constexpr int RB = kq_rows(TMAX), NS = RB * NM;  // rows together; weight rows read (row r, weight m: r NM + m)
+  constexpr int U = kq_unroll(TMAX) / RB;
   constexpr bool FIVE = QT == kQ5_K;
   constexpr uint32_t SBB = FIVE ? 176 : 144;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -420,22 +451,26 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q4k_kernel(const uint8_t* __
   const uint32_t g = (uint32_t)lane >> 3, part = (uint32_t)lane & 7u, hi = part >> 2, j = 2 * g + hi;
   const uint32_t qoff = (FIVE ? 48 : 16) + 32 * g + 8 * (part & 3u), hoff = 16 + 8 * (part & 3u);
   bool waited = false;
-  for (int row = blockIdx.x * kWarps + warp; row < n; row += gridDim.x * kWarps) {
-    float acc[NM][TMAX];
+  for (int row0 = (blockIdx.x * kWarps + warp) * RB; row0 < n; row0 += gridDim.x * kWarps * RB) {
+    float acc[NS][TMAX];
 #pragma unroll
-    for (int m = 0; m < NM; ++m)
+    for (int m = 0; m < NS; ++m)
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) acc[m][t] = 0.f;
-    const uint8_t* base[NM];
-    base[0] = W + (size_t)row * row_bytes;
-    if (SWI) base[NM - 1] = Wu + (size_t)row * row_bytes;
+    const uint8_t* base[NS];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      const size_t rr = (size_t)min(row0 + r, n - 1);  // a row past n repeats the last one, unstored
+      base[r * NM] = W + rr * row_bytes;
+      if (SWI) base[r * NM + 1] = Wu + rr * row_bytes;
+    }
     for (int sb0 = 0; sb0 < nsb; sb0 += U) {
-      uint4 h[U][NM];
-      uint2 c[U][NM], f[U][NM];
+      uint4 h[U][NS];
+      uint2 c[U][NS], f[U][NS];
 #pragma unroll
       for (int u = 0; u < U; ++u)
 #pragma unroll
-        for (int m = 0; m < NM; ++m)
+        for (int m = 0; m < NS; ++m)
           if (sb0 + u < nsb) {
             const uint8_t* sb = base[m] + (size_t)(sb0 + u) * SBB;
             h[u][m] = ldw_v4(sb);
@@ -449,9 +484,9 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q4k_kernel(const uint8_t* __
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         if (sb0 + u >= nsb) break;
-        float w[NM][8];
+        float w[NS][8];
 #pragma unroll
-        for (int m = 0; m < NM; ++m) {
+        for (int m = 0; m < NS; ++m) {
           const uint32_t sw[3] = {h[u][m].y, h[u][m].z, h[u][m].w};
           uint32_t sc, mn;
           q4k_scale_min_w(sw, j, sc, mn);
@@ -479,7 +514,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q4k_kernel(const uint8_t* __
             const float4 xa = __ldg(xr), xb = __ldg(xr + 1);
             const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
-            for (int m = 0; m < NM; ++m) {
+            for (int m = 0; m < NS; ++m) {
               float v = acc[m][t];
 #pragma unroll
               for (int e = 0; e < 8; ++e) v = fmaf(w[m][e], xv[e], v);
@@ -489,22 +524,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q4k_kernel(const uint8_t* __
         }
       }
     }
-#pragma unroll
-    for (int m = 0; m < NM; ++m)
-#pragma unroll
-      for (int t = 0; t < TMAX; ++t) {
-        float v = acc[m][t];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        acc[m][t] = v;
-      }
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t) {
-      if (lane == t && t < T) {
-        const size_t o = (size_t)t * ldy + row;
-        Y[o] = SWI ? silu_mul(acc[0][t], acc[NM - 1][t]) : acc[0][t] + (R ? R[o] : 0.f);
-      }
-    }
+    kq_rows_out<TMAX, NM, RB, SWI>(acc, row0, n, T, lane, Y, ldy, R);
   }
   if (!waited) grid_dependency_wait_inline();  // a CTA without rows
 }
@@ -512,7 +532,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q4k_kernel(const uint8_t* __
 template <int QT, int TMAX, bool SWI>
 cudaError_t launch_q4k_t(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
                          const float* R, cudaStream_t s) {
-  long blocks = (n + kWarps - 1) / kWarps;
+  const int rows = kWarps * kq_rows(TMAX);
+  long blocks = (n + rows - 1) / rows;
   const long cap = (long)num_sms() * 2;
   if (blocks > cap) blocks = cap;
   cudaLaunchConfig_t cfg = {};
@@ -536,10 +557,11 @@ cudaError_t launch_q4k(const void* W, const void* Wu, int n, int k, const float*
   return launch_q4k_t<QT, 16, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
 }
 
-// Q6_K: a warp per row, lane L decoding elements 8 L .. 8 L + 7 of each
-// superblock: low nibbles from bytes 64 h + 32 (c % 2) + 8 (L % 4) .. (h = L /
-// 16, c = L / 4 % 4; nibble c / 2), high bit pairs from bytes 128 + 32 h +
-// 8 (L % 4) .. (bits 2 c), the int8 scale at byte 192 + L / 2 and d at 208.
+// Q6_K: a warp per row (two rows at T >= 2), lane L decoding elements 8 L ..
+// 8 L + 7 of each superblock: low nibbles from bytes 64 h + 32 (c % 2) +
+// 8 (L % 4) .. (h = L / 16, c = L / 4 % 4; nibble c / 2), high bit pairs from
+// bytes 128 + 32 h + 8 (L % 4) .. (bits 2 c), the int8 scale at byte
+// 192 + L / 2 and d at 208.
 // Rows start on 16-byte boundaries, so superblock j starts 2 (j % 2) bytes
 // past a 4-byte one: an 8-byte field is read as three aligned words and
 // shifted. w = d sc (q - 32) is exact in fp32; products accumulate in fp32.
@@ -549,7 +571,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q6k_kernel(const uint8_t* __
                                                                const float* __restrict__ X, int T, float* Y, int ldy,
                                                                const float* R) {
   constexpr int NM = SWI ? 2 : 1;
-  constexpr int U = kq_unroll(TMAX);
+  constexpr int RB = kq_rows(TMAX), NS = RB * NM;  // rows together; weight rows read (row r, weight m: r NM + m)
+  constexpr int U = kq_unroll(TMAX) / RB;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nsb = k / 256;
   const size_t row_bytes = (size_t)nsb * 210;
@@ -557,22 +580,26 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q6k_kernel(const uint8_t* __
   const uint32_t loff = 64 * h + 32 * (c & 1u) + l0, hoff = 128 + 32 * h + l0, soff = 192 + ((uint32_t)lane >> 1);
   const uint32_t lsh = 4 * (c >> 1), hsh = 2 * c;
   bool waited = false;
-  for (int row = blockIdx.x * kWarps + warp; row < n; row += gridDim.x * kWarps) {
-    float acc[NM][TMAX];
+  for (int row0 = (blockIdx.x * kWarps + warp) * RB; row0 < n; row0 += gridDim.x * kWarps * RB) {
+    float acc[NS][TMAX];
 #pragma unroll
-    for (int m = 0; m < NM; ++m)
+    for (int m = 0; m < NS; ++m)
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) acc[m][t] = 0.f;
-    const uint8_t* base[NM];
-    base[0] = W + (size_t)row * row_bytes;
-    if (SWI) base[NM - 1] = Wu + (size_t)row * row_bytes;
+    const uint8_t* base[NS];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      const size_t rr = (size_t)min(row0 + r, n - 1);  // a row past n repeats the last one, unstored
+      base[r * NM] = W + rr * row_bytes;
+      if (SWI) base[r * NM + 1] = Wu + rr * row_bytes;
+    }
     for (int sb0 = 0; sb0 < nsb; sb0 += U) {
-      uint32_t lw[U][NM][3], hw[U][NM][3], scb[U][NM];
-      unsigned short db[U][NM];
+      uint32_t lw[U][NS][3], hw[U][NS][3], scb[U][NS];
+      unsigned short db[U][NS];
 #pragma unroll
       for (int u = 0; u < U; ++u)
 #pragma unroll
-        for (int m = 0; m < NM; ++m)
+        for (int m = 0; m < NS; ++m)
           if (sb0 + u < nsb) {
             const uint8_t* sb = base[m] + (size_t)(sb0 + u) * 210;
             const uint32_t sh = 2u * ((uint32_t)(sb0 + u) & 1u);
@@ -594,9 +621,9 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q6k_kernel(const uint8_t* __
       for (int u = 0; u < U; ++u) {
         if (sb0 + u >= nsb) break;
         const uint32_t s8 = 16u * ((uint32_t)(sb0 + u) & 1u);
-        float w[NM][8];
+        float w[NS][8];
 #pragma unroll
-        for (int m = 0; m < NM; ++m) {
+        for (int m = 0; m < NS; ++m) {
           const uint32_t lo[2] = {__funnelshift_r(lw[u][m][0], lw[u][m][1], s8),
                                   __funnelshift_r(lw[u][m][1], lw[u][m][2], s8)};
           const uint32_t hi[2] = {__funnelshift_r(hw[u][m][0], hw[u][m][1], s8),
@@ -617,7 +644,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q6k_kernel(const uint8_t* __
             const float4 xa = __ldg(xr), xb = __ldg(xr + 1);
             const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
-            for (int m = 0; m < NM; ++m) {
+            for (int m = 0; m < NS; ++m) {
               float v = acc[m][t];
 #pragma unroll
               for (int e = 0; e < 8; ++e) v = fmaf(w[m][e], xv[e], v);
@@ -627,22 +654,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q6k_kernel(const uint8_t* __
         }
       }
     }
-#pragma unroll
-    for (int m = 0; m < NM; ++m)
-#pragma unroll
-      for (int t = 0; t < TMAX; ++t) {
-        float v = acc[m][t];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        acc[m][t] = v;
-      }
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t) {
-      if (lane == t && t < T) {
-        const size_t o = (size_t)t * ldy + row;
-        Y[o] = SWI ? silu_mul(acc[0][t], acc[NM - 1][t]) : acc[0][t] + (R ? R[o] : 0.f);
-      }
-    }
+    kq_rows_out<TMAX, NM, RB, SWI>(acc, row0, n, T, lane, Y, ldy, R);
   }
   if (!waited) grid_dependency_wait_inline();  // a CTA without rows
 }
@@ -650,7 +662,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_q6k_kernel(const uint8_t* __
 template <int TMAX, bool SWI>
 cudaError_t launch_q6k_t(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
                          const float* R, cudaStream_t s) {
-  long blocks = (n + kWarps - 1) / kWarps;
+  const int rows = kWarps * kq_rows(TMAX);
+  long blocks = (n + rows - 1) / rows;
   const long cap = (long)num_sms() * 2;
   if (blocks > cap) blocks = cap;
   cudaLaunchConfig_t cfg = {};
