@@ -274,6 +274,42 @@ cudaError_t launch_q(const void* W, const void* Wu, int n, int k, const float* X
 // L1); exact fp32 products (a half widens exactly). The weights of the
 // warp's first chunks are requested before the dependency wait (they are
 // never the output of the preceding kernel); X, R and Y after it.
+// Streaming GEMVs (K-quants): superblocks whose loads are issued together before any is
+// decoded, by the number of tokens (measured on 4096 and 12288 rows x 4096:
+// 8 at T <= 2, 4 above; 2 took 12-40 % longer at T = 2 and 8)
+__host__ __device__ constexpr int kq_unroll(int tmax) { return tmax <= 2 ? 8 : 4; }
+// rows a warp takes together at T >= 2: they share each load of X (4096 x
+// 4096, Q4_K: 21.9 -> 16.7 us at T = 4, 38.4 -> 25.5 us at T = 8; F16: 22.2 ->
+// 17.9 us at T = 4)
+__host__ __device__ constexpr int kq_rows(int tmax) { return tmax >= 2 ? 2 : 1; }
+
+// Reduces a warp's lane partials of RB rows (NM weights each) over the warp
+// and writes rows row0 .. row0 + RB - 1 below n: token t's value by lane t.
+template <int TMAX, int NM, int RB, bool SWI>
+__device__ __forceinline__ void kq_rows_out(float (&acc)[RB * NM][TMAX], int row0, int n, int T, int lane, float* Y,
+                                            int ldy, const float* R) {
+#pragma unroll
+  for (int m = 0; m < RB * NM; ++m)
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+      float v = acc[m][t];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      acc[m][t] = v;
+    }
+#pragma unroll
+  for (int r = 0; r < RB; ++r) {
+    if (row0 + r >= n) break;
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+      if (lane == t && t < T) {
+        const size_t o = (size_t)t * ldy + row0 + r;
+        Y[o] = SWI ? silu_mul(acc[r * NM][t], acc[r * NM + NM - 1][t]) : acc[r * NM][t] + (R ? R[o] : 0.f);
+      }
+    }
+  }
+}
+
 constexpr int F16G = 8;  // chunks a lane loads at once
 
 template <int TMAX, bool SWI>
@@ -282,21 +318,27 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_f16_kernel(const uint16_t* _
                                                                const float* __restrict__ X, int T, float* Y, int ldy,
                                                                const float* R) {
   constexpr int NM = SWI ? 2 : 1;
+  constexpr int RB = kq_rows(TMAX), NS = RB * NM;  // rows together; weight rows read (row r, weight m: r NM + m)
+  constexpr int G = F16G / RB;                     // chunks a lane loads at once from each weight row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nchunk = k / 8;                 // 16-byte chunks a row
-  const int ngroup = nchunk / (32 * F16G);  // groups of F16G chunks a lane
-  const int rest = nchunk / 32 - ngroup * F16G;
+  const int nchunk = k / 8;              // 16-byte chunks a row
+  const int ngroup = nchunk / (32 * G);  // groups of G chunks a lane
+  const int rest = nchunk / 32 - ngroup * G;
   bool waited = false;
-  for (int row = blockIdx.x * kWarps + warp; row < n; row += gridDim.x * kWarps) {
-    float acc[NM][TMAX];
+  for (int row0 = (blockIdx.x * kWarps + warp) * RB; row0 < n; row0 += gridDim.x * kWarps * RB) {
+    float acc[NS][TMAX];
 #pragma unroll
-    for (int m = 0; m < NM; ++m)
+    for (int m = 0; m < NS; ++m)
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) acc[m][t] = 0.f;
-    const uint4* wr[NM];
-    wr[0] = reinterpret_cast<const uint4*>(W + (size_t)row * k);
-    if (SWI) wr[NM - 1] = reinterpret_cast<const uint4*>(Wu + (size_t)row * k);
-    auto chunk = [&](const uint4 (&w)[NM], int c) {
+    const uint4* wr[NS];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      const size_t rr = (size_t)min(row0 + r, n - 1);  // a row past n repeats the last one, unstored
+      wr[r * NM] = reinterpret_cast<const uint4*>(W + rr * k);
+      if (SWI) wr[r * NM + 1] = reinterpret_cast<const uint4*>(Wu + rr * k);
+    }
+    auto chunk = [&](const uint4 (&w)[NS], int c) {
       // chunk c: columns 8c .. 8c + 7
 #pragma unroll
       for (int t = 0; t < TMAX; ++t) {
@@ -304,7 +346,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_f16_kernel(const uint16_t* _
           const float4* xr = reinterpret_cast<const float4*>(X + (size_t)t * k + 8 * c);
           const float4 a = __ldg(xr), b = __ldg(xr + 1);
 #pragma unroll
-          for (int m = 0; m < NM; ++m) {
+          for (int m = 0; m < NS; ++m) {
             const float2 w0 = __half22float2(*reinterpret_cast<const __half2*>(&w[m].x));
             const float2 w1 = __half22float2(*reinterpret_cast<const __half2*>(&w[m].y));
             const float2 w2 = __half22float2(*reinterpret_cast<const __half2*>(&w[m].z));
@@ -324,44 +366,29 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_f16_kernel(const uint16_t* _
       }
     };
     for (int gi = 0; gi < ngroup; ++gi) {
-      uint4 w[F16G][NM];
+      uint4 w[G][NS];
 #pragma unroll
-      for (int i = 0; i < F16G; ++i)
+      for (int i = 0; i < G; ++i)
 #pragma unroll
-        for (int m = 0; m < NM; ++m) w[i][m] = ldw_v4(wr[m] + lane + 32 * (gi * F16G + i));
+        for (int m = 0; m < NS; ++m) w[i][m] = ldw_v4(wr[m] + lane + 32 * (gi * G + i));
       if (!waited) {
         grid_dependency_wait_inline();
         waited = true;
       }
 #pragma unroll
-      for (int i = 0; i < F16G; ++i) chunk(w[i], lane + 32 * (gi * F16G + i));
+      for (int i = 0; i < G; ++i) chunk(w[i], lane + 32 * (gi * G + i));
     }
     for (int i = 0; i < rest; ++i) {
-      uint4 w[NM];
+      uint4 w[NS];
 #pragma unroll
-      for (int m = 0; m < NM; ++m) w[m] = ldw_v4(wr[m] + lane + 32 * (ngroup * F16G + i));
+      for (int m = 0; m < NS; ++m) w[m] = ldw_v4(wr[m] + lane + 32 * (ngroup * G + i));
       if (!waited) {
         grid_dependency_wait_inline();
         waited = true;
       }
-      chunk(w, lane + 32 * (ngroup * F16G + i));
+      chunk(w, lane + 32 * (ngroup * G + i));
     }
-#pragma unroll
-    for (int m = 0; m < NM; ++m)
-#pragma unroll
-      for (int t = 0; t < TMAX; ++t) {
-        float v = acc[m][t];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        acc[m][t] = v;
-      }
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t) {
-      if (lane == t && t < T) {
-        const size_t o = (size_t)t * ldy + row;
-        Y[o] = SWI ? silu_mul(acc[0][t], acc[NM - 1][t]) : acc[0][t] + (R ? R[o] : 0.f);
-      }
-    }
+    kq_rows_out<TMAX, NM, RB, SWI>(acc, row0, n, T, lane, Y, ldy, R);
   }
   if (!waited) grid_dependency_wait_inline();  // a CTA without rows
 }
@@ -369,7 +396,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv_f16_kernel(const uint16_t* _
 template <int TMAX, bool SWI>
 cudaError_t launch_f16_t(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
                          const float* R, cudaStream_t s) {
-  long blocks = (n + kWarps - 1) / kWarps;
+  const int rows = kWarps * kq_rows(TMAX);
+  long blocks = (n + rows - 1) / rows;
   const long cap = (long)num_sms() * 2;
   if (blocks > cap) blocks = cap;
   cudaLaunchConfig_t cfg = {};
@@ -401,40 +429,6 @@ cudaError_t launch_f16(const void* W, const void* Wu, int n, int k, const float*
 // 8 (l mod 4) .. as 16. Each weight is d sc q - dmin m rounded once to fp32
 // (one fma of two exact products), then exact fp32 products with X. The loads
 // of several superblocks are issued before any is used.
-// K-quant GEMVs: superblocks whose loads are issued together before any is
-// decoded, by the number of tokens (measured on 4096 and 12288 rows x 4096:
-// 8 at T <= 2, 4 above; 2 took 12-40 % longer at T = 2 and 8)
-__host__ __device__ constexpr int kq_unroll(int tmax) { return tmax <= 2 ? 8 : 4; }
-// rows a warp takes together at T >= 2: they share each load of X (4096 x
-// 4096, Q4_K: 21.9 -> 16.7 us at T = 4, 38.4 -> 25.5 us at T = 8)
-__host__ __device__ constexpr int kq_rows(int tmax) { return tmax >= 2 ? 2 : 1; }
-// Reduces a warp's lane partials of RB rows (NM weights each) over the warp
-// and writes rows row0 .. row0 + RB - 1 below n: token t's value by lane t.
-template <int TMAX, int NM, int RB, bool SWI>
-__device__ __forceinline__ void kq_rows_out(float (&acc)[RB * NM][TMAX], int row0, int n, int T, int lane, float* Y,
-                                            int ldy, const float* R) {
-#pragma unroll
-  for (int m = 0; m < RB * NM; ++m)
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t) {
-      float v = acc[m][t];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      acc[m][t] = v;
-    }
-#pragma unroll
-  for (int r = 0; r < RB; ++r) {
-    if (row0 + r >= n) break;
-#pragma unroll
-    for (int t = 0; t < TMAX; ++t) {
-      if (lane == t && t < T) {
-        const size_t o = (size_t)t * ldy + row0 + r;
-        Y[o] = SWI ? silu_mul(acc[r * NM][t], acc[r * NM + NM - 1][t]) : acc[r * NM][t] + (R ? R[o] : 0.f);
-      }
-    }
-  }
-}
-
 template <int QT, int TMAX, bool SWI>
 __global__ void __launch_bounds__(kWarps * 32) gemv_q4k_kernel(const uint8_t* __restrict__ W,
                                                                const uint8_t* __restrict__ Wu, int n, int k,
