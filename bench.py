@@ -337,12 +337,13 @@ def run_ours(args):
 
     if args.only == "gemv":
         n, k, tg = args.gemv_rows, 4096, args.gemv_tokens
-        c = synth.make_case(QTYPE, n, k, tg, seed=0)
+        qg = args.kernel_qtype
+        c = synth.make_case(qg, n, k, tg, seed=0)
         Ws = [torch.from_numpy(c["W"]).to(dev) for _ in range(16)]
         X1 = torch.from_numpy(c["X"]).to(dev)
         Y1 = torch.empty((tg, n), device=dev)
         for i in range(args.warmup + args.steps):
-            q.apr_qgemv(QTYPE, Ws[i % 16], n, k, X1, tg, Y1, stream=stream)
+            q.apr_qgemv(qg, Ws[i % 16], n, k, X1, tg, Y1, stream=stream)
         q.apr_stream_status(stream)
         print(json.dumps({"only": "gemv", "launches": args.warmup + args.steps}), flush=True)
         return
@@ -853,7 +854,8 @@ def main(argv=None):
                          "gemv: only the T = 1 GEMV; attention: only the prefill attention (16 query heads, 4 KV "
                          "heads, --attn-tokens rows at position 0) (small, bounded runs for profilers)")
     ap.add_argument("--kernel-qtype", type=int, default=2, choices=[1, 2, 8, 12, 13, 14],
-                    help="weight type of the --only kernel run (GGUF id: 1 F16, 2 Q4_0, 8 Q8_0, 12 Q4_K, 13 Q5_K, 14 Q6_K)")
+                    help="weight type of the --only kernel and --only gemv runs (GGUF id: 1 F16, 2 Q4_0, 8 Q8_0, 12 Q4_K, "
+                         "13 Q5_K, 14 Q6_K)")
     ap.add_argument("--attn-tokens", type=int, default=2048, help="query rows of the --only attention run")
     ap.add_argument("--gemv-tokens", type=int, default=1, help="tokens of the --only gemv run (1..16)")
     ap.add_argument("--clocks-dir", default=None, help="where the raw nvidia-smi clock samples are written")
