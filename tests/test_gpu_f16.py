@@ -214,7 +214,7 @@ def test_exact_gate_up(q):
 # tensor-core GEMM; k = 288: the staged GEMV at every T
 @pytest.mark.parametrize("cls", ["subnormal", "typical", "large", "mixed"])
 @pytest.mark.parametrize("n,k,T", [(300, 512, 1), (300, 512, 2), (300, 1024, 4), (300, 512, 8), (300, 512, 13),
-                                   (77, 288, 1), (77, 288, 16)])
+                                   (77, 288, 1), (77, 288, 16), (77, 512, 3), (1, 256, 5)])
 def test_gemv(q, cls, n, k, T):
     W = synth.random_blocks(F16, n, k, 3 * n + k + T, cls)
     X = synth.activations(T, k, 5)
@@ -224,6 +224,18 @@ def test_gemv(q, cls, n, k, T):
     q.apr_stream_status()
     check_guards(buf, T, n)
     _check_exact(W, n, k, X, R, Y.cpu().numpy())
+
+
+@pytest.mark.parametrize("T", [2, 3, 6])
+def test_gemv_gate_up_odd_rows(q, T):
+    """Gate/up on the streaming GEMV with an odd row count: the last warp's
+    second row lies past n (its loads repeat row n - 1, nothing is stored for it)."""
+    n, k = 77, 512
+    Wg = synth.random_blocks(F16, n, k, 21 + T, "typical")
+    Wu = synth.random_blocks(F16, n, k, 22 + T, "typical")
+    X = synth.activations(T, k, 23)
+    y = _call(q, Wg, n, k, X, T, leg=q.APR_LEG_EXACT_F32, path=q.APR_PATH_GEMV, Wu=Wu)
+    assert_exact_leg(y, oracle.gate_up_swiglu_f64(F16, Wg, Wu, n, k, X))
 
 
 @pytest.mark.parametrize("T", [1, 3, 4, 7])

@@ -214,7 +214,8 @@ def test_exact_gate_up(q, qk):
 # T <= 8: the Q4_K GEMV; T = 13: the exact tensor-core GEMM
 @pytest.mark.parametrize("cls", ["subnormal", "typical", "large", "mixed"])
 @pytest.mark.parametrize("n,k,T", [(300, 512, 1), (300, 512, 2), (300, 1024, 4), (300, 512, 8), (300, 512, 13),
-                                   (77, 256, 1), (64, 12288, 3)])
+                                   (77, 256, 1), (64, 12288, 3),
+                                   (77, 512, 3), (1, 256, 5)])
 def test_gemv(q, qk, cls, n, k, T):
     k = _k(qk, k)
     W = synth.random_blocks(qk, n, k, 3 * n + k + T, cls)
@@ -245,6 +246,18 @@ def test_one_token_gemv_large_shapes(q, qk, n, k):
         Wu = synth.random_blocks(qk, n, k, 17 + n, "typical")
         y = _call(q, qk, W, n, k, X, 1, leg=q.APR_LEG_EXACT_F32, path=q.APR_PATH_GEMV, Wu=Wu)
         assert_exact_leg(y, oracle.gate_up_swiglu_f64(qk, W, Wu, n, k, X))
+
+
+@pytest.mark.parametrize("T", [2, 3, 6])
+def test_gemv_gate_up_odd_rows(q, qk, T):
+    """Gate/up on the GEMV path with an odd row count: the last warp's second
+    row lies past n (its loads repeat row n - 1, nothing is stored for it)."""
+    n, k = 77, _k(qk, 512)
+    Wg = synth.random_blocks(qk, n, k, 21 + T, "typical")
+    Wu = synth.random_blocks(qk, n, k, 22 + T, "typical")
+    X = synth.activations(T, k, 23)
+    y = _call(q, qk, Wg, n, k, X, T, leg=q.APR_LEG_EXACT_F32, path=q.APR_PATH_GEMV, Wu=Wu)
+    assert_exact_leg(y, oracle.gate_up_swiglu_f64(qk, Wg, Wu, n, k, X))
 
 
 @pytest.mark.parametrize("T", [1, 4, 7])
