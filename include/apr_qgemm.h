@@ -66,8 +66,9 @@
  * copy of X for the GEMM path (T*k*2 bytes), and, for the tensor-core GEMV
  * (T = 3 or 4, or T = 2 on weights of 2^25 or more elements), ticket counters
  * and partial sums (64 KiB plus 2 KiB per 128 weight rows and per SM, at
- * most), and, for apr_prefill_attention, the fp16 copies of the K and V
- * cache rows it reads. Calls on one stream share their stream's buffers,
+ * most), for the exact leg its split copies of X, exponents and, when k is
+ * split over CTAs, up to four partial outputs of T*n floats, and, for
+ * apr_prefill_attention, the fp16 copies of the K and V cache rows it reads. Calls on one stream share their stream's buffers,
  * which are ordered by the stream. A buffer grows on demand with cudaMalloc (also during a
  * stream capture: the calling thread's capture mode is relaxed for that
  * call) and is never freed while the process runs; a grown buffer replaces
@@ -191,13 +192,14 @@ int apr_qgemm_gate_up_swiglu(int qtype, const void* Wg, const void* Wu, int n, i
  * Small-T GEMV, 1 <= T <= APR_GEMV_MAX_T (T == 0 is a no-op), exact fp32
  * arithmetic, optional residual (gemv_q4_0_pf / gemv_q8_0_pf of
  * oxibonsai-kernels, used for the last-token lm_head in
- * try_cuda_prefill_q_std). For T <= 8 weight rows stream by bulk copies into
- * T fp32 accumulators (tensor cores for T = 3, 4 with Q4_0 / Q8_0; F16 and
- * K-quant weights always on the CUDA cores); for 9 <= T <= 16, and for smaller T
- * where no streaming kernel takes the shape (the X table of a long row does
- * not fit shared memory), the exact leg's tensor-core GEMM runs instead when
- * k % 256 == 0 (49-57 us at 4096 x 4096 and 12288 x 4096, against 50 to 700
- * us for the CUDA-core kernels at T = 12 and 16). T > APR_GEMV_MAX_T gives
+ * try_cuda_prefill_q_std). Weight rows stream by bulk copies into T fp32
+ * accumulators for T <= 4 with Q4_0 / Q8_0 (tensor cores for T = 3, 4) and
+ * T <= 8 with F16 and K-quant weights (CUDA cores); for larger T up to 16,
+ * and for smaller T where no streaming kernel takes the shape (the X table of
+ * a long row does not fit shared memory), the exact leg's tensor-core GEMM
+ * runs instead when k % 256 == 0 (22-24 us at 4096 x 4096 for T <= 16, with k
+ * split over CTAs when the grid is small; 53-57 us at 12288 x 4096; against
+ * 30-80 us for the CUDA-core kernels at T = 8). T > APR_GEMV_MAX_T gives
  * APR_E_INVAL. The weights are read early (see stream order above).
  */
 int apr_qgemv(int qtype, const void* W, int n, int k, const float* X, int T,
@@ -211,16 +213,18 @@ int apr_qgemv(int qtype, const void* W, int n, int k, const float* X, int T,
  * (per token) split into two fp16 pieces each, three products per term
  * (W1.X1 + W1.X2 + W2.X1), fp32 accumulation restarted every 256 k and the
  * partial sums added in fp32 (relative error about 1e-6 at k = 4096 and
- * 12288); gate/up takes two such products and an elementwise SwiGLU. Other
- * k run fp32 FFMA.
+ * 12288); when its 128 x 128 tiles leave most SMs idle, k is split over up to
+ * four CTAs whose partial outputs (scratch) a second kernel adds in a fixed
+ * order; gate/up takes two such products and an elementwise SwiGLU. Other k
+ * run fp32 FFMA.
  * ldy: strided output. Row t of Y starts at Y + t * ldy (and row t of
  * residual at residual + t * ldy), so Y can be a slice of a wider buffer, such
  * as the rows of a KV cache (aprender-serve writes attn_v straight into the
  * cache this way: forward_qwen35_cuda_prefill.rs). 0 means n (dense); else
  * n <= ldy <= 2^28 (APR_E_INVAL otherwise). Only the n floats of each row are
  * written. With residual == Y it accumulates into the strided rows. The
- * tensor-core path stores by TMA when n and ldy are multiples of 4, else
- * with plain stores. X stays dense [T][k].
+ * tensor-core path writes Y from registers (each warp 32 consecutive
+ * floats of a row). X stays dense [T][k].
  */
 typedef struct apr_qgemm_args {
   int qtype;

@@ -242,13 +242,16 @@ int run(const Problem& p) {
 
   int path = p.path;
   if (path == APR_PATH_AUTO) path = p.T <= APR_AUTO_GEMV_MAX_T ? APR_PATH_GEMV : APR_PATH_GEMM;
-  // From T = 9, and wherever no streaming GEMV kernel takes the shape (the
-  // staged fallback is several times slower), the exact leg's tensor-core
-  // GEMM beats the CUDA-core GEMVs (their FFMA work grows with T): the GEMV
-  // path takes it there. F16 weights stay on the GEMV kernels below T = 9.
+  // The exact leg's tensor-core GEMM beats the CUDA-core GEMVs (their FFMA
+  // work grows with T) from T = 5 for Q4_0 / Q8_0 (4096 x 4096 at T = 8: 21.6
+  // against 31.6 us; 12288 x 4096: 52.8 against 79.8 us) and from T = 9 for
+  // F16 and the K-quants (whose GEMVs take two rows a warp), and wherever no
+  // streaming GEMV kernel takes the shape (the staged fallback is several
+  // times slower): the GEMV path takes it there.
   int leg = p.leg;
+  const int gemv_last_t = block32_format(p.qtype) ? 4 : 8;
   if (path == APR_PATH_GEMV && p.k % 256 == 0 &&
-      (p.T > 8 || (p.qtype != APR_F16 && !gemv_streams(p.qtype, p.n, p.k, p.T, p.Wu != nullptr)))) {
+      (p.T > gemv_last_t || (p.qtype != APR_F16 && !gemv_streams(p.qtype, p.n, p.k, p.T, p.Wu != nullptr)))) {
     path = APR_PATH_GEMM;
     leg = APR_LEG_EXACT_F32;
   }

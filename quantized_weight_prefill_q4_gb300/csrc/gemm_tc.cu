@@ -459,13 +459,19 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
   const int nchunks_all = k / CHUNK;
   const int nsplit = gridDim.z, z = blockIdx.z;
   const int c0 = (int)((long)z * nchunks_all / nsplit), c1 = (int)((long)(z + 1) * nchunks_all / nsplit);
+  // k split: a cluster pair that exchanges halves (two splits), or, with bit
+  // 5 of `early`, independent splits each writing its own partial output (Y +
+  // z T ldy), added by a second kernel
+  const bool indep = (early & 32) != 0;
+  const bool clus = nsplit == 2 && !indep;
+  if (indep) Y += (size_t)z * (size_t)T * (size_t)ldy;
   const int nchunks = c1 - c0;
   const int nk = nchunks * SUBS;
   const int nunits = nk / C::RAW_SUBS;  // raw slots' worth of k
   // piece p (token columns t0 + 64 p ..) holds a token; with a split, CTA z
   // (its rank in the cluster) writes pieces 2 z and 2 z + 1
   auto live = [&](int p) { return t0 + p * PIECE < T; };
-  auto kept = [&](int p) { return nsplit == 1 || (p >> 1) == z; };
+  auto kept = [&](int p) { return !clus || (p >> 1) == z; };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::S; ++i) {
@@ -494,7 +500,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
   // access (the matching wait comes just before it); a thread arrives at the
   // closing barrier once it touches the partner's shared memory no more
   bool cl_started = false, cl_done = false;
-  if (nsplit == 2) cluster_arrive_relaxed();
+  if (clus) cluster_arrive_relaxed();
   if (warp == 1) tmem_alloc(tmem_holder, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -537,7 +543,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
           last_issued[slot] = j;
         }
       }
-      if (ok && nsplit == 2) {
+      if (ok && clus) {
         // every raw slot read for the last time: the partner may send into the ring
         const int total = nunits * C::NM;
         for (int v = total; v < total + C::S_RAW && ok; ++v)
@@ -743,10 +749,10 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
     grid_dependency_wait();
     const int row = m0 + (int)r;
     constexpr int PPW = C::NPIECE / C::NWG;
-    const int npw = nsplit == 2 ? 1 : PPW;
+    const int npw = clus ? 1 : PPW;
     // the pieces this warpgroup finalizes: all of the tile's pieces split
     // evenly, or with a split piece 2 z + wg
-    auto piece = [&](int pp) { return nsplit == 2 ? 2 * z + wg : wg * PPW + pp; };
+    auto piece = [&](int pp) { return clus ? 2 * z + wg : wg * PPW + pp; };
     // residual of piece p into registers (coalesced: the warp's lanes read 32
     // consecutive floats of one token's row)
     float rv[PIECE];
@@ -766,7 +772,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
       tc_fence_after();
     }
 
-    if (nsplit == 2) {
+    if (clus) {
       // the piece the partner keeps, pg, goes from registers straight into the
       // partner's raw ring at 32 KB x wg ([64 tokens][128 rows]); the
       // partner's copy of piece pk lands in this raw ring the same way
@@ -800,7 +806,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
       if (!live(p)) continue;  // the same for the whole warpgroup
       if (pp > 0 && EPI == kEpiResidual && ok) load_r(p);
       uint32_t v[64];
-      if (ok && nsplit == 2)  // the partner's half of this piece has landed
+      if (ok && clus)  // the partner's half of this piece has landed
         ok = __all_sync(0xffffffffu, mbar_wait_cluster(&xferFull[wg], 0, abort_flag, status));
       if (!ok) continue;
       if constexpr (XS) {
@@ -847,7 +853,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
           v[j] = __float_as_uint(gt / (1.0f + expf(-gt)) * __uint_as_float(u[j]));
         }
       }
-      if (nsplit == 2) {  // p0 + p1, in split order
+      if (clus) {  // p0 + p1, in split order
         const float* src = reinterpret_cast<const float*>(sRaw + wg * PIECE_BYTES) + r;
 #pragma unroll
         for (int j = 0; j < PIECE; ++j) {
@@ -881,7 +887,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
   }
 
   // split: neither CTA exits while the other may still access its shared memory
-  if (nsplit == 2) {
+  if (clus) {
     if (!cl_started) cluster_wait();
     if (!cl_done) cluster_arrive();
     cluster_wait();
@@ -993,7 +999,7 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
   cfg.stream = s;
   cudaLaunchAttribute attr[2] = {pdl_attr(), pdl_attr()};
   cfg.numAttrs = 1;
-  if (nsplit == 2) {  // the two k halves of a tile form a cluster
+  if (nsplit == 2 && !(early & 32)) {  // the two k halves of a tile form a cluster
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = 1;
     attr[1].val.clusterDim.y = 1;
@@ -1151,12 +1157,52 @@ __global__ void __launch_bounds__(256) x_split_kernel(const float* __restrict__ 
   }
 }
 
+// The exact leg's k splits added in split order (fp32), plus the residual:
+// Y[t][i] = sum_z P[z][t][i] (+ R[t][i]); P dense [ks][T][n]. R may be Y.
+__global__ void xs_reduce_kernel(const float* __restrict__ P, int ks, int T, int n, float* Y, int ldy, const float* R) {
+  const size_t total = (size_t)T * n;
+  for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (size_t)gridDim.x * blockDim.x) {
+    float v = P[idx];
+    for (int z = 1; z < ks; ++z) v += P[(size_t)z * total + idx];
+    const size_t t = idx / (size_t)n, i = idx - t * (size_t)n;
+    const size_t o = t * (size_t)ldy + i;
+    if (R) v += R[o];
+    Y[o] = v;
+  }
+}
+
+// Independent k splits of the exact leg (at most 4, at least one 256-k chunk
+// each) when its 128 x 128 tiles leave most SMs idle: as many as keep the
+// grid within one wave.
+int xs_ksplit(int n, int k, int T) {
+  const long ctas = (long)((n + BM - 1) / BM) * ((T + 127) / 128);
+  long ks = ctas > 0 ? (long)num_sms() / ctas : 1;
+  if (ks > 4) ks = 4;
+  if (ks > k / CHUNK) ks = k / CHUNK;
+  return ks < 1 ? 1 : (int)ks;
+}
+
 template <int QT>
 int launch_xs(const void* W, const void* Wu, int n, int k, const uint16_t* X1, const uint16_t* X2, const int* erow,
               const int* etok, int T, float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg,
-              size_t msg_len) {
+              size_t msg_len, int ks, float* part) {
   (void)Wu;
   const int xr = padded_x_rows(T);  // the split's scratch holds that many rows
+  if (ks > 1) {  // independent k splits into dense partials, then their sum (and R) into Y
+    if (launch_cfg<QT, kEpiPlain, 128, true>(W, Wu, n, k, X1, T, part, n, nullptr, status, s, msg, msg_len, ks,
+                                              kEarlyW | 32, xr, X2, erow, etok))
+      return -1;
+    const size_t total = (size_t)T * n;
+    size_t blocks = (total + 255) / 256;
+    if (blocks > (size_t)num_sms() * 8) blocks = (size_t)num_sms() * 8;
+    xs_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(part, ks, T, n, Y, ldy, R);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+      snprintf(msg, msg_len, "exact-leg split sum: %s", cudaGetErrorString(e));
+      return -1;
+    }
+    return 0;
+  }
   if (R)
     return launch_cfg<QT, kEpiResidual, 128, true>(W, Wu, n, k, X1, T, Y, ldy, R, status, s, msg, msg_len, 1, kEarlyW,
                                                     xr, X2, erow, etok);
@@ -1190,7 +1236,10 @@ cudaError_t launch_swiglu_rows(const float* G, const float* U, int T, int n, flo
 
 size_t gemm_xs_scratch_bytes(int n, int k, int T, bool swiglu) {
   const size_t xb = ((size_t)padded_x_rows(T) * k * 2 + 255) & ~(size_t)255;
-  return 2 * xb + (((size_t)T * 4 + 255) & ~(size_t)255) + (size_t)(swiglu ? 2 : 1) * n * 4;
+  const size_t base =
+      2 * xb + (((size_t)T * 4 + 255) & ~(size_t)255) + (((size_t)(swiglu ? 2 : 1) * n * 4 + 255) & ~(size_t)255);
+  const int ks = xs_ksplit(n, k, T);
+  return base + (ks > 1 ? (size_t)ks * T * n * 4 : 0);  // the splits' partial outputs
 }
 
 int launch_gemm_xs(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
@@ -1201,6 +1250,11 @@ int launch_gemm_xs(int qtype, const void* W, const void* Wu, int n, int k, const
   uint16_t* X2 = reinterpret_cast<uint16_t*>(base + xb);
   int* etok = reinterpret_cast<int*>(base + 2 * xb);
   int* erow = reinterpret_cast<int*>(base + 2 * xb + (((size_t)T * 4 + 255) & ~(size_t)255));
+  // the k splits' partial outputs, after the exponents (the layout of
+  // gemm_xs_scratch_bytes with swiglu = Wu != nullptr)
+  const int ks = xs_ksplit(n, k, T);
+  float* part = reinterpret_cast<float*>(base + 2 * xb + (((size_t)T * 4 + 255) & ~(size_t)255) +
+                                         (((size_t)(Wu ? 2 : 1) * n * 4 + 255) & ~(size_t)255));
   const int bb = block_bytes(qtype);
   const float qmax = qtype == kQ4_0 ? 8.f : 128.f;
   // plain stream order: the splits start once everything before is complete
@@ -1226,12 +1280,17 @@ int launch_gemm_xs(int qtype, const void* W, const void* Wu, int n, int k, const
     snprintf(msg, msg_len, "exact-leg splits: %s", cudaGetErrorString(e));
     return -1;
   }
-  if (qtype == kF16) return launch_xs<kF16>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
-  if (qtype == kQ4_K) return launch_xs<kQ4_K>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
-  if (qtype == kQ5_K) return launch_xs<kQ5_K>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
-  if (qtype == kQ6_K) return launch_xs<kQ6_K>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
-  return qtype == kQ4_0 ? launch_xs<kQ4_0>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len)
-                        : launch_xs<kQ8_0>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len);
+  if (qtype == kF16) return launch_xs<kF16>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len, ks,
+                                           part);
+  if (qtype == kQ4_K) return launch_xs<kQ4_K>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len, ks,
+                                           part);
+  if (qtype == kQ5_K) return launch_xs<kQ5_K>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len, ks,
+                                           part);
+  if (qtype == kQ6_K) return launch_xs<kQ6_K>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len, ks,
+                                           part);
+  return qtype == kQ4_0
+             ? launch_xs<kQ4_0>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len, ks, part)
+             : launch_xs<kQ8_0>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len, ks, part);
 }
 
 cudaError_t launch_x_to_f16(const float* X, uint16_t* X16, size_t count, cudaStream_t s) {
