@@ -368,11 +368,12 @@ int run_ffn(const apr_ffn_args& a) {
     if (tc) {
       char msg[256] = "";
       const GemmPlan pg = plan_gemm_tc(a.inter, a.hidden, rows, true);
-      if (launch_gemm_tc(pg, a.qtype, a.Wg, a.Wu, a.inter, a.hidden, static_cast<const uint16_t*>(h), rows, act,
-                         a.inter, nullptr, st->status, s, msg, sizeof msg, kEarlyWR, padded_x_rows(rows)) != 0)
+      // the SwiGLU output straight to fp16, the down GEMM's operand (the same
+      // rounding the conversion pass would apply to the fp32 value)
+      if (launch_gemm_tc(pg, a.qtype, a.Wg, a.Wu, a.inter, a.hidden, static_cast<const uint16_t*>(h), rows,
+                         reinterpret_cast<float*>(act16), a.inter, nullptr, st->status, s, msg, sizeof msg,
+                         kEarlyWR | kOutF16, padded_x_rows(rows)) != 0)
         return fail(APR_E_LAUNCH, "%s", msg);
-      rc = launched(launch_x_to_f16(act, act16, (size_t)rows * a.inter, s), "x_to_f16");
-      if (rc != APR_OK) return rc;
       const GemmPlan pd = plan_gemm_tc(a.hidden, a.inter, rows, false);
       if (launch_gemm_tc(pd, a.qtype, a.Wd, nullptr, a.hidden, a.inter, act16, rows, Xc, a.hidden, Xc, st->status, s,
                          msg, sizeof msg, kEarlyWR, padded_x_rows(rows)) != 0)

@@ -119,6 +119,10 @@ GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu);
 // conversion or norm kernel, which starts only once everything before it has
 // completed), kEarlyNone nothing.
 enum { kEarlyNone = 0, kEarlyWR = 1, kEarlyW = 2 };
+// A flag or-ed into `early` for a gate/up GEMM: the SwiGLU output is written
+// as fp16 (round to nearest even; Y is then a uint16 buffer, ldy counted in
+// its elements), the operand the next GEMM reads.
+constexpr int kOutF16 = 64;
 // x_rows: the rows of X16 the kernel may read (>= T; 0 means T). Rows past T
 // only feed output columns that are never stored; a buffer of at least
 // kMinXRows rows avoids the slow TMA loads from a tensor of fewer rows

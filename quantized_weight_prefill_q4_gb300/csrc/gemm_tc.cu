@@ -426,7 +426,8 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
                    const __grid_constant__ CUtensorMap tmR, int n, int k, int T, float* Y, int ldy, const float* R,
                    const int* erow, const int* etok, unsigned* status, int early) {
   // early: bits 0-3 what may be read before the dependency wait (kEarly*),
-  // bit 4 set when tmR describes the residual (L2 prefetches of it).
+  // bit 4 set when tmR describes the residual (L2 prefetches of it), bit 5
+  // independent k splits (below), bit 6 (kOutF16) an fp16 gate/up output.
   // Exact leg (XS): X and X2 are the two fp16 pieces of X * 2^etok[t];
   // erow[i] (erow[n + i] for the up weight) is the exponent e of the
   // row's scale 2^e (computed before the launch, see row_exp_kernel).
@@ -870,6 +871,18 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
           const int t = t0 + p * PIECE + j;
           const float stk = __int_as_float((127 - etok[t < T ? t : 0]) << 23);
           v[j] = __float_as_uint(__uint_as_float(v[j]) * sr * stk);
+        }
+      }
+      if constexpr (EPI == kEpiSwiGLU) {
+        if (row < n && (early & kOutF16)) {
+          // fp16 output, the next GEMM's operand (Y holds uint16, ldy in them)
+          uint16_t* Y16 = reinterpret_cast<uint16_t*>(Y);
+#pragma unroll
+          for (int j = 0; j < PIECE; ++j) {
+            const int t = t0 + p * PIECE + j;
+            if (t < T) Y16[(size_t)t * ldy + row] = __half_as_ushort(__float2half_rn(__uint_as_float(v[j])));
+          }
+          continue;
         }
       }
       if (row < n) {
