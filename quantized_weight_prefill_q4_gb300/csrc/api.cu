@@ -512,15 +512,20 @@ int run_layer(const apr_layer_args& a) {
     const void* Wp[3] = {Wq, Wk, Wv};
     float* Yp[3] = {qbuf, a.K_cache + (size_t)pos * kvd, a.V_cache + (size_t)pos * kvd};
     const int np[3] = {(int)qd, (int)kvd, (int)kvd};
-    for (int j = 0; j < 3; ++j) {
-      if (tc) {
-        char msg[256] = "";
-        const GemmPlan plan = plan_gemm_tc(np[j], a.hidden, rows, false);
-        if (launch_gemm_tc(plan, a.qtype, Wp[j], nullptr, np[j], a.hidden, static_cast<const uint16_t*>(h), rows,
-                           Yp[j], np[j], nullptr, st->status, s, msg, sizeof msg, j == 0 ? kEarlyWR : kEarlyW,
-                           padded_x_rows(rows)) != 0)
-          return fail(APR_E_LAUNCH, "%s", msg);
-      } else {
+    if (tc) {
+      // one GEMM over the fused weight (its q, k and v row ranges are
+      // multiples of 256 rows): q rows to the q buffer, k and v rows straight
+      // into the cache rows pos ..
+      char msg[256] = "";
+      const int nqkv = (int)(qd + 2 * kvd);
+      const GemmPlan plan = plan_gemm_tc(nqkv, a.hidden, rows, false);
+      const OutRegions reg{Yp[1], Yp[2], (int)qd, (int)(qd + kvd), (int)kvd, (int)kvd};
+      if (launch_gemm_tc(plan, a.qtype, a.Wqkv, nullptr, nqkv, a.hidden, static_cast<const uint16_t*>(h), rows,
+                         qbuf, (int)qd, nullptr, st->status, s, msg, sizeof msg, kEarlyWR, padded_x_rows(rows),
+                         &reg) != 0)
+        return fail(APR_E_LAUNCH, "%s", msg);
+    } else {
+      for (int j = 0; j < 3; ++j) {
         rc = run(Problem{a.qtype, a.leg, APR_PATH_AUTO, Wp[j], nullptr, np[j], a.hidden, rows,
                          static_cast<const float*>(h), nullptr, Yp[j], s});
         if (rc != APR_OK) return rc;

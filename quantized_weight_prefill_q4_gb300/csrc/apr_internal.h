@@ -119,6 +119,16 @@ GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu);
 // conversion or norm kernel, which starts only once everything before it has
 // completed), kEarlyNone nothing.
 enum { kEarlyNone = 0, kEarlyWR = 1, kEarlyW = 2 };
+// Output rows of a plain tensor-core GEMM sent to up to three places by row
+// range: rows [0, r1) to Y (ldy apart), rows [r1, r2) to y1 (row - r1, ld1
+// apart), rows [r2, n) to y2 (row - r2, ld2 apart); y1 == nullptr: all to Y.
+// r1 and r2 are multiples of 128 (a tile's rows go to one place).
+struct OutRegions {
+  float* y1;
+  float* y2;
+  int r1, r2, ld1, ld2;
+};
+
 // A flag or-ed into `early` for a gate/up GEMM: the SwiGLU output is written
 // as fp16 (round to nearest even; Y is then a uint16 buffer, ldy counted in
 // its elements), the operand the next GEMM reads.
@@ -131,7 +141,7 @@ constexpr int kMinXRows = 16;
 inline int padded_x_rows(int T) { return T < kMinXRows ? kMinXRows : T; }
 int launch_gemm_tc(const GemmPlan& plan, int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16,
                    int T, float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg,
-                   size_t msg_len, int early, int x_rows = 0);
+                   size_t msg_len, int early, int x_rows = 0, const OutRegions* regions = nullptr);
 
 // A kernel that waits (bounded, limit_ns) on an mbarrier nothing arrives on,
 // then records the timeout in the status word and returns (selftest.cu).

@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWu,
                    const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmX2,
                    const __grid_constant__ CUtensorMap tmR, int n, int k, int T, float* Y, int ldy, const float* R,
-                   const int* erow, const int* etok, unsigned* status, int early) {
+                   const int* erow, const int* etok, unsigned* status, int early, OutRegions reg) {
   // early: bits 0-3 what may be read before the dependency wait (kEarly*),
   // bit 4 set when tmR describes the residual (L2 prefetches of it), bit 5
   // independent k splits (below), bit 6 (kOutF16) an fp16 gate/up output.
@@ -886,13 +886,24 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
         }
       }
       if (row < n) {
+        // this row's place: Y, or (a plain GEMM) the region its row falls in
+        float* yb = Y;
+        int ld = ldy, rr = row;
+        if constexpr (EPI == kEpiPlain) {
+          if (reg.y1 && row >= reg.r1) {
+            const bool second = reg.y2 && row >= reg.r2;
+            yb = second ? reg.y2 : reg.y1;
+            ld = second ? reg.ld2 : reg.ld1;
+            rr = row - (second ? reg.r2 : reg.r1);
+          }
+        }
         // R row t was read before Y row t is written (Y may be R), by this thread
 #pragma unroll
         for (int j = 0; j < PIECE; ++j) {
           const int t = t0 + p * PIECE + j;
           float y = __uint_as_float(v[j]);
           if (EPI == kEpiResidual) y += rv[j];
-          if (t < T) Y[(size_t)t * ldy + row] = y;
+          if (t < T) yb[(size_t)t * ld + rr] = y;
         }
       }
     }
@@ -954,7 +965,8 @@ __global__ void __launch_bounds__(256, 4) x_to_f16_kernel(const float* __restric
 template <int QT, int EPI, int BN, bool XS = false>
 int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y, int ldy,
                const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int nsplit, int early,
-               int x_rows, const uint16_t* X16b = nullptr, const int* erow = nullptr, const int* etok = nullptr) {
+               int x_rows, const uint16_t* X16b = nullptr, const int* erow = nullptr, const int* etok = nullptr,
+               OutRegions reg = OutRegions{nullptr, nullptr, 0, 0, 0, 0}) {
   using C = Cfg<QT, EPI, BN, XS>;
   auto fn = encode_fn(msg, msg_len);
   if (!fn) return -1;
@@ -1021,7 +1033,8 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
   }
   cfg.attrs = attr;
   cudaError_t e =
-      cudaLaunchKernelEx(&cfg, kern, mW, mWu, mX, mX2, mR, n, k, T, Y, ldy, R, erow, etok, status, early | (r_pf << 4));
+      cudaLaunchKernelEx(&cfg, kern, mW, mWu, mX, mX2, mR, n, k, T, Y, ldy, R, erow, etok, status, early | (r_pf << 4),
+                         reg);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) {
     snprintf(msg, msg_len, "gemm_tc launch: %s", cudaGetErrorString(e));
@@ -1032,7 +1045,8 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
 
 template <int QT>
 int launch_q(const GemmPlan& pl, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y,
-             int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int w, int xr) {
+             int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int w, int xr,
+             const OutRegions& reg) {
   if (Wu) return launch_cfg<QT, kEpiSwiGLU, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w, xr);
   if constexpr (QT == kF16) {
     // an F16 raw slot is four times a Q4_0 one: 256-token tiles do not fit
@@ -1041,10 +1055,12 @@ int launch_q(const GemmPlan& pl, const void* W, const void* Wu, int n, int k, co
     if (R)
       return launch_cfg<QT, kEpiResidual, 256>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, pl.nsplit, w,
                                                xr);
-    return launch_cfg<QT, kEpiPlain, 256>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, pl.nsplit, w, xr);
+    return launch_cfg<QT, kEpiPlain, 256>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, pl.nsplit, w, xr,
+                                          nullptr, nullptr, nullptr, reg);
   }
   if (R) return launch_cfg<QT, kEpiResidual, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w, xr);
-  return launch_cfg<QT, kEpiPlain, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w, xr);
+  return launch_cfg<QT, kEpiPlain, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w, xr, nullptr,
+                                        nullptr, nullptr, reg);
 }
 
 // ---------------------------------------------------------------- exact-leg splits
@@ -1347,14 +1363,19 @@ GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu) {
 
 int launch_gemm_tc(const GemmPlan& pl, int qtype, const void* W, const void* Wu, int n, int k, const uint16_t* X16,
                    int T, float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg,
-                   size_t msg_len, int early, int x_rows) {
+                   size_t msg_len, int early, int x_rows, const OutRegions* regions) {
   const int w = early;
-  if (qtype == kF16) return launch_q<kF16>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
-  if (qtype == kQ4_K) return launch_q<kQ4_K>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
-  if (qtype == kQ5_K) return launch_q<kQ5_K>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
-  if (qtype == kQ6_K) return launch_q<kQ6_K>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
-  return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows)
-                        : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows);
+  const OutRegions reg = regions ? *regions : OutRegions{nullptr, nullptr, 0, 0, 0, 0};
+  if (qtype == kF16) return launch_q<kF16>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows,
+                                          reg);
+  if (qtype == kQ4_K) return launch_q<kQ4_K>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows,
+                                          reg);
+  if (qtype == kQ5_K) return launch_q<kQ5_K>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows,
+                                          reg);
+  if (qtype == kQ6_K) return launch_q<kQ6_K>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows,
+                                          reg);
+  return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows, reg)
+                        : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows, reg);
 }
 
 }  // namespace apr
