@@ -484,7 +484,9 @@ int run_layer(const apr_layer_args& a) {
   const int rmax = a.T < chunk ? a.T : chunk;
   // the chunk's normed rows (fp32 at most), q and the attention output
   const size_t h_bytes = align256(std::max((size_t)rmax * a.hidden * 4, (size_t)padded_x_rows(rmax) * a.hidden * 2));
-  const size_t q_bytes = align256((size_t)rmax * qd * 4);
+  // (the attention output is fp32, or fp16 over at least the 16 rows the
+  // tensor-core GEMM reads)
+  const size_t q_bytes = align256(std::max((size_t)rmax * qd * 4, (size_t)padded_x_rows(rmax) * qd * 2));
   void* scratch = nullptr;
   rc = stream_scratch(st->dev, s, kScratchLayer, h_bytes + 2 * q_bytes, &scratch);
   if (rc != APR_OK) return rc;
@@ -531,14 +533,23 @@ int run_layer(const apr_layer_args& a) {
         if (rc != APR_OK) return rc;
       }
     }
-    // 2. causal attention of the chunk's rows over the cache rows 0 .. pos + rows - 1
+    // 2. causal attention of the chunk's rows over the cache rows 0 .. pos + rows - 1;
+    // on the tensor-core route its output is written as fp16, the output
+    // projection's operand (the rounding the conversion pass would apply)
     char msg[256] = "";
     if (launch_prefill_attention(qbuf, a.K_cache, a.V_cache, abuf, rows, pos, a.num_heads, a.num_kv_heads, ascratch,
-                                 st->status, s, msg, sizeof msg) != 0)
+                                 st->status, s, msg, sizeof msg, tc) != 0)
       return fail(APR_E_LAUNCH, "%s", msg);
     // 3. output projection added into the chunk's rows of X
-    rc = run(Problem{a.qtype, a.leg, APR_PATH_AUTO, a.Wo, nullptr, a.hidden, (int)qd, rows, abuf, Xc, Xc, s});
-    if (rc != APR_OK) return rc;
+    if (tc) {
+      const GemmPlan plan = plan_gemm_tc(a.hidden, (int)qd, rows, false);
+      if (launch_gemm_tc(plan, a.qtype, a.Wo, nullptr, a.hidden, (int)qd, reinterpret_cast<const uint16_t*>(abuf),
+                         rows, Xc, a.hidden, Xc, st->status, s, msg, sizeof msg, kEarlyWR, padded_x_rows(rows)) != 0)
+        return fail(APR_E_LAUNCH, "%s", msg);
+    } else {
+      rc = run(Problem{a.qtype, a.leg, APR_PATH_AUTO, a.Wo, nullptr, a.hidden, (int)qd, rows, abuf, Xc, Xc, s});
+      if (rc != APR_OK) return rc;
+    }
     // 4. the FFN sublayer on the same rows
     apr_ffn_args f{a.qtype, a.leg, a.Wg, a.Wu, a.Wd, a.hidden, a.inter, rows, a.ffn_norm, a.eps, Xc, a.stream};
     rc = run_ffn(f);

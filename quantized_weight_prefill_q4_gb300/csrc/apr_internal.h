@@ -89,9 +89,11 @@ cudaError_t launch_rmsnorm_rows(const float* X, const float* w, float eps, int T
 // (prefill_attention_scratch_bytes, 256-byte aligned), then the attention.
 // Returns 0, or -1 with a message.
 size_t prefill_attention_scratch_bytes(int T, int pos0, int num_kv_heads);
+// o16: O is written as fp16 (round to nearest even of the fp32 value; O
+// then points to uint16 [T][num_heads * 256]), the next GEMM's operand.
 int launch_prefill_attention(const float* Q, const float* K, const float* V, float* O, int T, int pos0,
                              int num_heads, int num_kv_heads, void* scratch, unsigned* status, cudaStream_t s,
-                             char* msg, size_t msg_len);
+                             char* msg, size_t msg_len, bool o16 = false);
 
 // Exact-fp32 FFMA GEMM for any k % 32 == 0 (gemm_simt.cu).
 cudaError_t launch_gemm_simt(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,

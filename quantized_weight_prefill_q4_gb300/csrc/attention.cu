@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(256) kv_to_f16_kernel(const float* __restrict_
 __global__ void __launch_bounds__(A_THREADS, 1)
     prefill_attention_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                              const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO, int T,
-                             int pos0, int num_heads, int num_kv_heads, unsigned* status) {
+                             int pos0, int num_heads, int num_kv_heads, unsigned* status, int o16) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sK = smem + OFF_K;
@@ -457,24 +457,50 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     if (ok) {
       tc_fence_after();
       const float inv = 1.0f / l;
+      if (o16) {
+        // fp16 O: boxes of 64 dims (128 bytes a row), the same swizzle
 #pragma unroll 1
-      for (int cb = 0; cb < AD / 32; ++cb) {
-        uint32_t ov[32];
-        tmem_ld_32x32b_x32(lane_addr + COL_O + cb * 32, ov);
-        tmem_ld_wait_regs(ov);
-        uint8_t* row = smem + OFF_OST + cb * QBOX_BYTES + r * 128;
+        for (int cb = 0; cb < AD / 64; ++cb) {
+          uint32_t ov[64];
+          tmem_ld_32x32b_x32(lane_addr + COL_O + cb * 64, ov);
+          tmem_ld_32x32b_x32(lane_addr + COL_O + cb * 64 + 32, ov + 32);
+          tmem_ld_wait_regs(ov);
+          regs_after_wait(ov + 32);
+          uint8_t* row = smem + OFF_OST + cb * QBOX_BYTES + r * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<float4*>(row + ((c ^ (r & 7)) << 4)) =
-              make_float4(__uint_as_float(ov[4 * c]) * inv, __uint_as_float(ov[4 * c + 1]) * inv,
-                          __uint_as_float(ov[4 * c + 2]) * inv, __uint_as_float(ov[4 * c + 3]) * inv);
+          for (int c = 0; c < 8; ++c) {
+            uint32_t hv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const __half2 hp = __floats2half2_rn(__uint_as_float(ov[8 * c + 2 * u]) * inv,
+                                                   __uint_as_float(ov[8 * c + 2 * u + 1]) * inv);
+              hv[u] = *reinterpret_cast<const uint32_t*>(&hp);
+            }
+            *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int cb = 0; cb < AD / 32; ++cb) {
+          uint32_t ov[32];
+          tmem_ld_32x32b_x32(lane_addr + COL_O + cb * 32, ov);
+          tmem_ld_wait_regs(ov);
+          uint8_t* row = smem + OFF_OST + cb * QBOX_BYTES + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4*>(row + ((c ^ (r & 7)) << 4)) =
+                make_float4(__uint_as_float(ov[4 * c]) * inv, __uint_as_float(ov[4 * c + 1]) * inv,
+                            __uint_as_float(ov[4 * c + 2]) * inv, __uint_as_float(ov[4 * c + 3]) * inv);
+        }
       }
       fence_proxy_async_smem();   // the TMA store reads the boxes through the async proxy
     }
     named_sync(1, 32 * SOFT_WARPS);
     if (threadIdx.x == 0 && ok) {
-#pragma unroll
-      for (int cb = 0; cb < AD / 32; ++cb) tma_store_2d(&tmO, smem + OFF_OST + cb * QBOX_BYTES, h * AD + 32 * cb, t0);
+      const int dims = o16 ? 64 : 32;  // dims a box
+#pragma unroll 1
+      for (int cb = 0; cb < AD / dims; ++cb)
+        tma_store_2d(&tmO, smem + OFF_OST + cb * QBOX_BYTES, h * AD + dims * cb, t0);
       bulk_commit_group();
       bulk_wait_read_all();   // the boxes are read before the CTA's shared memory goes
     }
@@ -495,7 +521,7 @@ size_t prefill_attention_scratch_bytes(int T, int pos0, int num_kv_heads) {
 
 int launch_prefill_attention(const float* Q, const float* K, const float* V, float* O, int T, int pos0,
                              int num_heads, int num_kv_heads, void* scratch, unsigned* status, cudaStream_t s,
-                             char* msg, size_t msg_len) {
+                             char* msg, size_t msg_len, bool o16) {
   if (T <= 0) return 0;
   const size_t rows = (size_t)pos0 + (size_t)T, kv_dim = (size_t)num_kv_heads * AD;
   const size_t ldv = (rows + 15) & ~(size_t)15;
@@ -529,8 +555,10 @@ int launch_prefill_attention(const float* Q, const float* K, const float* V, flo
   CUtensorMap mQ, mO;
   if (!make_map_2d(fn, &mQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, Q, q_dim, (uint64_t)T, q_dim * 4, 32, AQ,
                    CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len) ||
-      !make_map_2d(fn, &mO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, O, q_dim, (uint64_t)T, q_dim * 4, 32, AQ,
-                   CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
+      !(o16 ? make_map_2d(fn, &mO, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, O, q_dim, (uint64_t)T, q_dim * 2, 64, AQ,
+                          CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len)
+            : make_map_2d(fn, &mO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, O, q_dim, (uint64_t)T, q_dim * 4, 32, AQ,
+                          CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len)))
     return -1;
 
   static int attr_set[64] = {0};
@@ -552,7 +580,8 @@ int launch_prefill_attention(const float* Q, const float* K, const float* V, flo
   cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, prefill_attention_kernel, mK, mV, mQ, mO, T, pos0, num_heads, num_kv_heads, status);
+  e = cudaLaunchKernelEx(&cfg, prefill_attention_kernel, mK, mV, mQ, mO, T, pos0, num_heads, num_kv_heads, status,
+                         o16 ? 1 : 0);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prefill attention");
   return 0;
