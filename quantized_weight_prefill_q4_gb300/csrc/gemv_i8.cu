@@ -58,7 +58,8 @@ constexpr int ICW = 8;                         // consumer warps
 constexpr int ITHREADS = 32 * (ICW + 1);
 constexpr int ISTAGE = 16384;                  // bytes of one stage
 constexpr int INS_MAX = 13;                    // stages at most (as many as shared memory holds)
-constexpr int IMAXROWS = 128;                  // rows a CTA may take
+// rows a CTA takes at most: the CTAs split the n rows evenly
+__host__ __device__ inline int i8_rcap(int n, int grid) { return (n + grid - 1) / grid; }
 constexpr int XBW = 28;                        // table words per block: 3 x 8 digit words, 3 starts, scale
 
 __device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
@@ -270,9 +271,10 @@ __global__ void __launch_bounds__(ITHREADS, 2)
   const int nblk = k / 32, npk = nblk / 2;
   const int PW = (npk + 31) / 32;  // warps per row
   uint32_t* xt = reinterpret_cast<uint32_t*>(smem + (size_t)ns * ISTAGE);  // X table, [nblk][XBW]
+  const int rcap = i8_rcap(n, gridDim.x);
   float* part = reinterpret_cast<float*>(xt + (size_t)nblk * XBW);     // [row slot][NM][PW]
-  float* rres = part + IMAXROWS * NM * 8;                              // residual of the CTA's rows
-  uint64_t* bars = reinterpret_cast<uint64_t*>(rres + IMAXROWS);
+  float* rres = part + (size_t)rcap * 2 * 8;                           // residual of the CTA's rows
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rres + ((rcap + 1) & ~1));
   uint64_t* full = bars;
   uint64_t* empty = bars + INS_MAX;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * INS_MAX);
@@ -461,23 +463,25 @@ __global__ void __launch_bounds__(ITHREADS, 2)
 }
 
 // shared memory besides the ring, and the stages that fit beside it
-size_t i8_fixed_smem(int k) {
-  return 128 + (size_t)(k / 32) * XBW * 4 + (size_t)IMAXROWS * (2 * 8 + 1) * 4 + 2 * INS_MAX * 8 + 16;
+int i8_grid(int n) { return n < num_sms() ? n : num_sms(); }
+size_t i8_fixed_smem(int k, int n) {
+  const size_t rcap = (size_t)i8_rcap(n, i8_grid(n));
+  return 128 + (size_t)(k / 32) * XBW * 4 + rcap * 2 * 8 * 4 + ((rcap + 1) & ~(size_t)1) * 4 + 2 * INS_MAX * 8 + 16;
 }
-int i8_stages(int k) {
+int i8_stages(int k, int n) {
   // two CTAs an SM (228 KB of shared memory, 1 KB reserved per CTA) when 5
   // stages fit beside the X table, else one with as many as fit
-  const long half = 232448L / 2 - 1024 - (long)i8_fixed_smem(k);
+  const long half = 232448L / 2 - 1024 - (long)i8_fixed_smem(k, n);
   if (half / ISTAGE >= 5) return 5;
-  const long ns = (232448L - (long)i8_fixed_smem(k)) / ISTAGE;
+  const long ns = (232448L - (long)i8_fixed_smem(k, n)) / ISTAGE;
   return (int)(ns < INS_MAX ? ns : INS_MAX);
 }
-size_t i8_smem(int k) { return i8_fixed_smem(k) + (size_t)i8_stages(k) * ISTAGE; }
+size_t i8_smem(int k, int n) { return i8_fixed_smem(k, n) + (size_t)i8_stages(k, n) * ISTAGE; }
 
 template <int QT, bool SWI>
 cudaError_t launch_i8(const void* W, const void* Wu, int n, int k, const float* X, float* Y, const float* R,
                       unsigned* status, cudaStream_t s) {
-  const size_t smem = i8_smem(k);
+  const size_t smem = i8_smem(k, n);
   auto kern = gemv_i8_kernel<QT, SWI>;
   static int attr_set[64] = {0};
   int dev = 0;
@@ -487,9 +491,8 @@ cudaError_t launch_i8(const void* W, const void* Wu, int n, int k, const float* 
     if (e != cudaSuccess) return e;
     attr_set[dev] = 1;
   }
-  const int nsm = num_sms();
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(n < nsm ? n : nsm));
+  cfg.gridDim = dim3((unsigned)i8_grid(n));
   cfg.blockDim = dim3(ITHREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -500,7 +503,7 @@ cudaError_t launch_i8(const void* W, const void* Wu, int n, int k, const float* 
   cfg.numAttrs = 1;
   cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, (const uint8_t*)W, (const uint8_t*)Wu, n, k, X, Y, R, status,
-                         rows_per_stage(QT, k, SWI), i8_stages(k));
+                         rows_per_stage(QT, k, SWI), i8_stages(k, n));
   if (e == cudaSuccess) e = cudaGetLastError();
   return e;
 }
@@ -593,11 +596,11 @@ cudaError_t launch_read_stream(const void* src, long long bytes, unsigned* statu
 }
 
 bool gemv_i8_fits(int qtype, int n, int k, int T, bool swiglu) {
-  // block formats, one token; k % 256 == 0 (whole rows 16-byte aligned in a stage); a row's
-  // warps within the consumer warps; at most IMAXROWS rows a CTA
+  // block formats and K-quants, one token; k % 256 == 0 (whole rows 16-byte
+  // aligned in a stage); a row's warps within the consumer warps; a ring of at
+  // least 4 stages beside the X table and the CTA's row sums
   if ((!block32_format(qtype) && !kquant(qtype)) || T != 1 || k % 256 != 0 || (k / 64 + 31) / 32 > 8) return false;
-  if ((n + num_sms() - 1) / num_sms() > IMAXROWS) return false;
-  return rows_per_stage(qtype, k, swiglu) >= 1 && i8_stages(k) >= 4;
+  return rows_per_stage(qtype, k, swiglu) >= 1 && i8_stages(k, n) >= 4;
 }
 
 cudaError_t launch_gemv_i8(int qtype, const void* W, const void* Wu, int n, int k, const float* X, float* Y,

@@ -79,6 +79,26 @@ def test_gemv_exact(q, qtype, T, n, k):
 
 
 @pytest.mark.parametrize("qtype", QTYPES)
+@pytest.mark.parametrize("swiglu", [False, True])
+def test_one_token_gemv_many_rows_a_cta(q, qtype, swiglu):
+    """40000 rows: each CTA of the one-token kernel takes 264 of them (its row
+    sums and residuals sized by that count)."""
+    n, k = 40000, 512
+    c = synth.make_case(qtype, n, k, 1, residual=not swiglu, gate_up=swiglu, seed=41)
+    buf, Y = guarded(1, n)
+    if swiglu:
+        q.apr_qgemm_ex(qtype, dev(c["W"]), n, k, dev(c["X"]), 1, Y, Wu=dev(c["Wu"]), leg=q.APR_LEG_EXACT_F32,
+                       path=q.APR_PATH_GEMV)
+        ref = oracle.gate_up_swiglu_f64(qtype, c["W"], c["Wu"], n, k, c["X"])
+    else:
+        q.apr_qgemv(qtype, dev(c["W"]), n, k, dev(c["X"]), 1, Y, dev(c["R"]))
+        ref = oracle.qgemm_f64(qtype, c["W"], n, k, c["X"], c["R"])
+    q.apr_stream_status()
+    check_guards(buf, 1, n)
+    assert_exact_leg(Y.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("qtype", QTYPES)
 @pytest.mark.parametrize("T", [1, 6, 16])
 def test_gemv_swiglu_exact(q, qtype, T):
     n, k = 200, 1024
