@@ -540,9 +540,15 @@ _HOST = {}
 
 
 def host_weight(qtype, n, k, seed):
-    """Seeded GGUF bytes of an n x k weight (the f32 draw shared by both formats)."""
+    """Seeded GGUF bytes of an n x k weight (the f32 draw shared by both formats).
+    Past 16384 rows the first 16384 rows repeat (timing only: such a weight
+    is far larger than L2, so the repeat gives no cache hits)."""
+    import numpy as np
     import synth
 
+    if n > 16384:
+        base = host_weight(qtype, 16384, k, seed)
+        return np.ascontiguousarray(np.tile(base, (-(-n // 16384), 1))[:n])
     key = ("w", qtype, n, k, seed)
     if key not in _HOST:
         fk = ("f", n, k, seed)
@@ -622,7 +628,8 @@ def every_workload(q, dev, stream, peak_tf, peak_gbs):
     * fused gate/up SwiGLU 12288 x 4096 then down 4096 x 12288 + residual, 512
       tokens, Q4_0 and Q8_0;
     * the small-T GEMV sweep: T in {1, 2, 4, 8, 16} over 4096 x 4096 and
-      12288 x 4096, Q4_0 and Q8_0 (GB/s against the HBM rate);
+      12288 x 4096, Q4_0 and Q8_0 (GB/s against the HBM rate), and a
+      151936 x 4096 output head at T = 1 (Q4_0, Q4_K);
     * the T rule: the GEMV (exact) against the forced tensor-core GEMM on the
       fp16 leg and on the exact leg at T = 4..16 (Q4_0, both weights), and the
       GEMMs at 24 and 32;
@@ -649,6 +656,10 @@ def every_workload(q, dev, stream, peak_tf, peak_gbs):
                 r = P(qtype=qt, n=n, k=k, T=T)
                 sweep[f"{name}_n{n}_k{k}_t{T}"] = {key: r[key] for key in ("us", "GB/s", "frac_hbm", "TFLOP/s")}
     out["gemv_sweep"] = sweep
+    # a vocabulary-sized output head at one token (the last-token projection)
+    out["gemv_head"] = {f"{name}_n151936_k4096_t1": {key: r[key] for key in ("us", "GB/s", "frac_hbm")}
+                        for qt, name in ((Q4, "q4_0"), (Q4K, "q4_k"))
+                        for r in [P(qtype=qt, n=151936, k=4096, T=1)]}
     rule = {}
     for n in (4096, 12288):
         for T in (4, 8, 12, 16, 24, 32):
