@@ -349,20 +349,20 @@ __device__ __forceinline__ void q4k_row_stage(const uint32_t* w, uint32_t g, flo
     A[h] = d * (float)sc;
     B[h] = -(dmin * (float)m);
   }
-  auto code = [](uint32_t c) { return __uint_as_float(c | 0x4B000000u) - 8388608.0f; };  // 0..15 exactly
 #pragma unroll
   for (int v = 0; v < 8; ++v) {
     const uint32_t x = w[(FIVE ? 12 : 4) + v];
     const uint32_t f = FIVE ? w[4 + v] : 0u;  // fifth bits of elements 4 v .. 4 v + 3 (and + 32)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
+      // the four codes of sub-block 2 g + h, one a byte (the fifth bit, bit
+      // 2 g + h of each fifth-bit byte, worth 16)
+      uint32_t qw = (x >> (4 * h)) & 0x0F0F0F0Fu;
+      if (FIVE) qw |= ((f >> (2 * g + h)) & 0x01010101u) << 4;
       float q[4];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        uint32_t qv = (x >> (8 * b + 4 * h)) & 15u;
-        if (FIVE) qv |= ((f >> (8 * b + 2 * g + h)) & 1u) << 4;
-        q[b] = fmaf(A[h], code(qv), B[h]);
-      }
+      for (int b = 0; b < 4; ++b)  // q exactly: the float 2^23 + q (byte b under exponent 0x4B) less 2^23
+        q[b] = fmaf(A[h], __uint_as_float(__byte_perm(qw, 0x4B000000u, 0x7440u + b)) - 8388608.0f, B[h]);
       const int j = 16 * h + 2 * v;
       if constexpr (XSP) {
         split2(q[0] * sw, q[1] * sw, a1[j], a2[j]);
@@ -395,19 +395,17 @@ __device__ __forceinline__ void q6k_row_stage(const uint32_t* w, uint32_t g, uin
 #pragma unroll
   for (int j = 0; j < 4; ++j) A[j] = d * (float)((int)(scw << (24 - 8 * j)) >> 24);  // int8 scale j
   const uint32_t nib = 4 * (g & 1u), hb = 4 * (g & 1u);
-  // q - 32 exactly: the float 2^23 + q less 2^23 + 32
-  auto centered = [](uint32_t q) { return __uint_as_float(q | 0x4B000000u) - 8388640.0f; };
 #pragma unroll
   for (int v = 0; v < 16; ++v) {
     const uint32_t x = at(v);                       // low bytes of elements 4 v .. 4 v + 3
     const uint32_t y = at(17 + (v & 7));            // their high-bit bytes (element % 32)
     const uint32_t hs = hb + 2 * (uint32_t)(v >> 3);  // 2 c
+    // the four 6-bit codes, one a byte
+    const uint32_t qw = ((x >> nib) & 0x0F0F0F0Fu) | (((y >> hs) & 0x03030303u) << 4);
     float q[4];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const uint32_t qv = ((x >> (8 * b + nib)) & 15u) | (((y >> (8 * b + hs)) & 3u) << 4);
-      q[b] = A[v >> 2] * centered(qv);
-    }
+    for (int b = 0; b < 4; ++b)  // q - 32 exactly: the float 2^23 + q (byte b under exponent 0x4B) less 2^23 + 32
+      q[b] = A[v >> 2] * (__uint_as_float(__byte_perm(qw, 0x4B000000u, 0x7440u + b)) - 8388640.0f);
     if constexpr (XSP) {
       split2(q[0] * sw, q[1] * sw, a1[2 * v], a2[2 * v]);
       split2(q[2] * sw, q[3] * sw, a1[2 * v + 1], a2[2 * v + 1]);
