@@ -279,7 +279,6 @@ __device__ __forceinline__ void split2(float x, float y, uint32_t& h1, uint32_t&
 template <int QT>
 __device__ __forceinline__ void dequant_row_stage_xs(const uint32_t* w, float sw, uint32_t (&a1)[32],
                                                      uint32_t (&a2)[32]) {
-  auto code = [](uint32_t c) { return __uint_as_float(c | 0x4B000000u); };
   if constexpr (QT == kF16) {
     // w holds the 64 halves themselves (f16_row_stage); v = w * 2^e is exact
 #pragma unroll
@@ -301,11 +300,13 @@ __device__ __forceinline__ void dequant_row_stage_xs(const uint32_t* w, float sw
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t x = p[blk * 4 + i];  // bytes m = 0..3: elements 4i + m (low), 16 + 4i + m (high)
+        // the nibbles four at a time; byte m under exponent 0x4B is 2^23 + n
+        const uint32_t xl = x & 0x0F0F0F0Fu, xh = (x >> 4) & 0x0F0F0F0Fu;
         float lo[4], hi[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-          lo[m] = (code((x >> (8 * m)) & 0xFu) - 8388616.0f) * d;
-          hi[m] = (code((x >> (8 * m + 4)) & 0xFu) - 8388616.0f) * d;
+          lo[m] = (__uint_as_float(__byte_perm(xl, 0x4B000000u, 0x7440u + m)) - 8388616.0f) * d;
+          hi[m] = (__uint_as_float(__byte_perm(xh, 0x4B000000u, 0x7440u + m)) - 8388616.0f) * d;
         }
         split2(lo[0], lo[1], a1[16 * blk + 2 * i], a2[16 * blk + 2 * i]);
         split2(lo[2], lo[3], a1[16 * blk + 2 * i + 1], a2[16 * blk + 2 * i + 1]);
@@ -322,7 +323,8 @@ __device__ __forceinline__ void dequant_row_stage_xs(const uint32_t* w, float sw
       const float d = c < 8 ? d0 : d1;
       float v[4];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) v[m] = (code((x >> (8 * m)) & 0xFFu) - 8388736.0f) * d;
+      for (int m = 0; m < 4; ++m)  // byte m under exponent 0x4B: 2^23 + 128 + q
+        v[m] = (__uint_as_float(__byte_perm(x, 0x4B000000u, 0x7440u + m)) - 8388736.0f) * d;
       split2(v[0], v[1], a1[2 * c], a2[2 * c]);
       split2(v[2], v[3], a1[2 * c + 1], a2[2 * c + 1]);
     }
