@@ -1,4 +1,4 @@
-"""CPU oracle (float64) for the Q4_0 / Q8_0 / F16 / Q4_K / Q5_K / Q6_K prefill projections.
+"""CPU oracle (float64) for the Q4_0 / Q8_0 / F16 / Q4_K / Q5_K / Q6_K / IQ4_XS prefill projections.
 
 TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and
 ``bench.py``'s CPU-baseline legs use it. It shares no code with the CUDA
@@ -12,6 +12,9 @@ from .qref import (  # noqa: F401
     Q4_K,
     Q5_K,
     Q6_K,
+    IQ4_XS,
+    IQ4_NL_VALUES,
+    iq4_xs_scales,
     q4_k_scales_mins,
     fp16_bits_to_f64,
     block_scales_and_codes,

@@ -1,4 +1,4 @@
-"""Plain CPU oracle for the Q4_0 / Q8_0 / F16 / Q4_K / Q5_K / Q6_K prefill projections (float64).
+"""Plain CPU oracle for the Q4_0 / Q8_0 / F16 / Q4_K / Q5_K / Q6_K / IQ4_XS prefill projections (float64).
 
 TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import or call
@@ -42,6 +42,21 @@ What is computed, and where the pages define it:
   (half ``h``, quarter ``c``, lane ``l`` < 32) takes nibble ``c / 2`` of low
   byte ``64 h + 32 (c % 2) + l`` and bits ``2 c .. 2 c + 1`` of high byte
   ``32 h + l`` as its six-bit code ``q``; ``w = d sc_{e/16} (q - 32)``.
+* IQ4_XS, dispatched by the same page (``Iq4XsDequantKernel``, kernel
+  ``iq4_xs_dequant_to_f32``, grid ``(n, k.div_ceil(256))``) without its
+  layout or its code table; read as the GGUF IQ4_XS superblock of 256
+  elements in 136 bytes: fp16 ``d`` (bytes 0-1), a little-endian 16-bit word
+  of high scale bits (2-3), 4 bytes of low scale nibbles (4-7), then 128 bytes
+  of 4-bit codes, 16 bytes a 32-element sub-block. Sub-block ``j`` has the
+  six-bit scale ``ls_j`` (low nibble: nibble ``j % 2`` of byte ``4 + j / 2``;
+  top two bits: bits ``2 j, 2 j + 1`` of the word) and byte ``8 + 16 j + l``
+  holds element ``32 j + l`` in its low nibble and ``32 j + 16 + l`` in its
+  high nibble (Q4_0's order). A code ``c`` does not stand for ``c - 8`` but
+  for entry ``c`` of the non-linear 16-value table ``IQ4_NL_VALUES`` (GGUF's
+  IQ4_NL code book); ``w = d (ls_j - 32) table[c]``. PARITY UNPINNED for the
+  table's values: nothing on the pages fixes them, so the pins check the
+  layout (with a linear table the superblock equals eight Q4_0 blocks) and
+  take the values as given.
 * Projection ``Y[T][n] = X[T][k] . W[n][k]^T`` (aprender-serve 0.70.2
   src/cuda/executor/gdn_prefill_ops.rs, doc of ``qwen35_project_rows``),
   optionally ``+ R[T][n]`` (the residual add that follows the down / output
@@ -98,10 +113,13 @@ Q8_0 = 8
 Q4_K = 12
 Q5_K = 13
 Q6_K = 14
+IQ4_XS = 23
 _QK = 32
 _QK_K = 256
 _BLOCK_BYTES = {F16: 64, Q4_0: 18, Q8_0: 34}
-_SUPER_BYTES = {Q4_K: 144, Q5_K: 176, Q6_K: 210}
+_SUPER_BYTES = {Q4_K: 144, Q5_K: 176, Q6_K: 210, IQ4_XS: 136}
+# the code book of IQ4_XS (and IQ4_NL): code c stands for entry c
+IQ4_NL_VALUES = (-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113)
 
 
 # --------------------------------------------------------------------------
@@ -189,6 +207,35 @@ def _dequant_q6_k(W: np.ndarray, n: int, k: int) -> np.ndarray:
     return w.reshape(n, k)
 
 
+def iq4_xs_scales(sb: np.ndarray) -> np.ndarray:
+    """The eight signed sub-block scales ``ls_j - 32`` of IQ4_XS superblocks
+    ``[..., 136]``: the low nibble of ``ls_j`` is nibble ``j % 2`` of byte
+    ``4 + j / 2``, its top two bits are bits ``2 j, 2 j + 1`` of the
+    little-endian word at bytes 2-3."""
+    hi = sb[..., 2].astype(np.int64) | (sb[..., 3].astype(np.int64) << 8)
+    ls = np.empty(sb.shape[:-1] + (8,), np.int64)
+    for j in range(8):
+        low = (sb[..., 4 + j // 2].astype(np.int64) >> (4 * (j % 2))) & 0x0F
+        ls[..., j] = low | (((hi >> (2 * j)) & 3) << 4)
+    return ls - 32
+
+
+def _dequant_iq4_xs(W: np.ndarray, n: int, k: int, table=IQ4_NL_VALUES) -> np.ndarray:
+    """IQ4_XS: ``w = d (ls_j - 32) table[c]`` for the code ``c`` of each
+    element, the codes of sub-block ``j`` in bytes ``8 + 16 j ..`` (low
+    nibbles the first 16 elements, high nibbles the next 16). ``table`` is a
+    parameter only so that a test can substitute a linear one."""
+    sb = _superblocks(IQ4_XS, W, n, k)
+    nsb = k // _QK_K
+    d = fp16_bits_to_f64(sb[..., 0].astype(np.uint16) | (sb[..., 1].astype(np.uint16) << 8))
+    s = iq4_xs_scales(sb).astype(np.float64)                           # [n][nsb][8]
+    qs = sb[..., 8:].astype(np.int64).reshape(n, nsb, 8, 16)
+    codes = np.concatenate([qs & 0x0F, qs >> 4], axis=-1)              # [n][nsb][8][32]
+    vals = np.asarray(table, dtype=np.float64)[codes]
+    w = d[..., None, None] * s[..., None] * vals
+    return w.reshape(n, k)
+
+
 def _row_bytes(qtype: int, k: int) -> int:
     """Bytes of one weight row of k elements."""
     if qtype in _SUPER_BYTES:
@@ -233,6 +280,8 @@ def dequant_f64(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
     for F16 the binary16 value of element ``(i, j)``."""
     if qtype == Q6_K:
         return _dequant_q6_k(W, n, k)
+    if qtype == IQ4_XS:
+        return _dequant_iq4_xs(W, n, k)
     if qtype in _SUPER_BYTES:
         return _dequant_k(qtype, W, n, k)
     if qtype == F16:
@@ -254,7 +303,8 @@ def dequant_f32(qtype: int, W: np.ndarray, n: int, k: int) -> np.ndarray:
     value, subnormals included, is a float32 value. Q4_K and Q5_K: the exact
     float64 value ``d sc q - dmin m`` rounded once to float32. Q6_K: ``d sc
     (q - 32)`` has at most 11 + 7 + 6 significant bits, so it is exact in
-    float32 too.
+    float32 too. IQ4_XS: ``d (ls - 32) table[c]`` has at most 11 + 5 + 7 bits
+    (|ls - 32| <= 32, every table entry below 128 in magnitude): exact.
     """
     return dequant_f64(qtype, W, n, k).astype(np.float32)
 

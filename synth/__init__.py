@@ -15,6 +15,7 @@ from .gen import (  # noqa: F401
     Q4_K,
     Q5_K,
     Q6_K,
+    IQ4_XS,
     BLOCK_ELEMS,
     block_bytes,
     quantize,
@@ -24,6 +25,7 @@ from .gen import (  # noqa: F401
     quantize_q4_k,
     quantize_q5_k,
     quantize_q6_k,
+    quantize_iq4_xs,
     row_bytes,
     weight_f32,
     activations,

@@ -1,4 +1,4 @@
-"""Seeded generators and the GGUF Q4_0 / Q8_0 / F16 weight encoders.
+"""Seeded generators and the GGUF weight encoders (Q4_0, Q8_0, F16, Q4_K, Q5_K, Q6_K, IQ4_XS).
 
 Recipe (the same for every workload):
 
@@ -41,9 +41,12 @@ Q8_0 = 8  # GGUF type id
 Q4_K = 12  # GGUF type id (256-element superblocks of 144 bytes)
 Q5_K = 13  # GGUF type id (256-element superblocks of 176 bytes)
 Q6_K = 14  # GGUF type id (256-element superblocks of 210 bytes)
+IQ4_XS = 23  # GGUF type id (256-element superblocks of 136 bytes)
 BLOCK_ELEMS = 32
-_BLOCK_BYTES = {F16: 64, Q4_0: 18, Q8_0: 34, Q4_K: 18, Q5_K: 22}
-_SUPER_BYTES = {Q4_K: 144, Q5_K: 176, Q6_K: 210}
+_BLOCK_BYTES = {F16: 64, Q4_0: 18, Q8_0: 34, Q4_K: 18, Q5_K: 22, IQ4_XS: 17}
+_SUPER_BYTES = {Q4_K: 144, Q5_K: 176, Q6_K: 210, IQ4_XS: 136}
+# IQ4_XS's code book, for the encoder's nearest-value search
+_IQ4_BOOK = np.array([-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113], np.float64)
 
 
 def block_bytes(qtype: int) -> int:
@@ -177,6 +180,44 @@ def quantize_q6_k(w: np.ndarray) -> np.ndarray:
     return out.reshape(n, -1)
 
 
+def quantize_iq4_xs(w: np.ndarray) -> np.ndarray:
+    """Encode an f32 ``[n][k]`` weight (k % 256 == 0) into IQ4_XS superblocks
+    ``[n][k/256*136]``: per 32-element sub-block the signed element m of
+    largest magnitude gives the sub-scale m / -127 (m maps to the book's
+    first entry, -127); d is the largest |sub-scale| over 31 (fp16), the
+    six-bit scales ls = round(sub-scale / d) + 32 clamped to 1..63, and each
+    element takes the book entry nearest to w / (d (ls - 32)). Byte
+    placement: d at bytes 0-1, the scales' top two bits at bits 2 j of the
+    little-endian word at bytes 2-3, their low nibbles at nibble j % 2 of
+    byte 4 + j / 2, the code of element 32 j + l (l < 16) in the low nibble
+    of byte 8 + 16 j + l and that of 32 j + 16 + l in its high nibble."""
+    w = np.ascontiguousarray(w, dtype=np.float32).astype(np.float64)
+    n, k = w.shape
+    nsb = k // 256
+    x = w.reshape(n, nsb, 8, 32)
+    idx = np.abs(x).argmax(axis=-1)
+    m = np.take_along_axis(x, idx[..., None], axis=-1)[..., 0]
+    sub = m / -127.0
+    d16 = (np.abs(sub).max(axis=-1) / 31.0).astype(np.float16)
+    df = d16.astype(np.float64)
+    s = np.where(df[..., None] > 0, np.clip(np.rint(sub / np.where(df > 0, df, 1.0)[..., None]), -31, 31), 0)
+    ls = (s + 32).astype(np.int64)
+    step = df[..., None] * s
+    ratio = np.where(step[..., None] != 0, x / np.where(step != 0, step, 1.0)[..., None], 1.0)
+    code = np.abs(ratio[..., None] - _IQ4_BOOK).argmin(axis=-1).astype(np.int64)  # [n][nsb][8][32]
+    out = np.zeros((n, nsb, 136), np.uint8)
+    out[..., 0:2] = d16.view(np.uint16)[..., None].view(np.uint8).reshape(n, nsb, 2)
+    hi = np.zeros((n, nsb), np.int64)
+    for j in range(8):
+        hi |= ((ls[..., j] >> 4) & 3) << (2 * j)
+        out[..., 4 + j // 2] |= ((ls[..., j] & 15) << (4 * (j % 2))).astype(np.uint8)
+    out[..., 2] = (hi & 0xFF).astype(np.uint8)
+    out[..., 3] = (hi >> 8).astype(np.uint8)
+    qs = code[..., 0:16] | (code[..., 16:32] << 4)                     # [n][nsb][8][16]
+    out[..., 8:] = qs.reshape(n, nsb, 128).astype(np.uint8)
+    return out.reshape(n, -1)
+
+
 def _quantize_k(w: np.ndarray, bits: int) -> np.ndarray:
     top = (1 << bits) - 1
     w = np.ascontiguousarray(w, dtype=np.float32).astype(np.float64)
@@ -226,6 +267,8 @@ def quantize(qtype: int, w: np.ndarray) -> np.ndarray:
         return quantize_q5_k(w)
     if qtype == Q6_K:
         return quantize_q6_k(w)
+    if qtype == IQ4_XS:
+        return quantize_iq4_xs(w)
     if qtype == Q4_0:
         return quantize_q4_0(w)
     if qtype == Q8_0:
@@ -269,14 +312,17 @@ def random_blocks(qtype: int, n: int, k: int, seed: int, scale_class: str = "mix
     """
     lo, hi = SCALE_CLASSES[scale_class]
     if qtype in _SUPER_BYTES:
-        # random bytes; d and dmin (Q6_K: d alone, at the end) of both signs
-        # drawn from the class
+        # random bytes; d and dmin (Q6_K: d alone, at the end; IQ4_XS: d
+        # alone, first) of both signs drawn from the class
         rng = np.random.default_rng(seed)
         raw = rng.integers(0, 256, size=(n, k // 256, _SUPER_BYTES[qtype]), dtype=np.uint8)
-        for off in ((208,) if qtype == Q6_K else (0, 2)):
+        offs = (208,) if qtype == Q6_K else ((0,) if qtype == IQ4_XS else (0, 2))
+        for off in offs:
             exp = rng.integers(lo, hi + 1, size=(n, k // 256)).astype(np.uint16)
-            if fp16_range:  # |w| within fp16's range: |d| < 2^5 (63 x 31 x 2^5 < 65504); Q6_K |d| < 16 (128 x 32 x 16)
-                exp = np.minimum(exp, 18 if qtype == Q6_K else 19)
+            # |w| within fp16's range: |d| < 2^5 (63 x 31 x 2^5 < 65504);
+            # Q6_K |d| < 16 (128 x 32 x 16), IQ4_XS |d| < 16 (127 x 32 x 16)
+            if fp16_range:
+                exp = np.minimum(exp, 18 if qtype in (Q6_K, IQ4_XS) else 19)
             man = rng.integers(0, 1024, size=(n, k // 256)).astype(np.uint16)
             man = np.where(exp == 0, np.maximum(man, 1), man)
             sign = rng.integers(0, 2, size=(n, k // 256)).astype(np.uint16)

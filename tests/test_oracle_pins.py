@@ -23,8 +23,8 @@ import oracle
 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-QTYPES = [synth.Q4_0, synth.Q8_0, synth.F16, synth.Q4_K, synth.Q5_K, synth.Q6_K]
-KQ = (synth.Q4_K, synth.Q5_K, synth.Q6_K)
+QTYPES = [synth.Q4_0, synth.Q8_0, synth.F16, synth.Q4_K, synth.Q5_K, synth.Q6_K, synth.IQ4_XS]
+KQ = (synth.Q4_K, synth.Q5_K, synth.Q6_K, synth.IQ4_XS)
 
 
 def _kk(qtype, k):
@@ -348,6 +348,95 @@ def test_fp16_decode_landmarks():
     assert oracle.fp16_bits_to_f64(np.uint16(0xC000)) == -2.0
     assert oracle.fp16_bits_to_f64(np.uint16(0x7C00)) == np.inf
 
+def _iq4_xs_superblock(d_bits, ls, codes):
+    """IQ4_XS bytes from d's fp16 bits, eight six-bit scales and 256 four-bit
+    codes, placed one at a time: scale j's low nibble at nibble j % 2 of byte
+    4 + j // 2, its top two bits at bits 2 j of the word at bytes 2-3; the code
+    of element 32 j + l at nibble l // 16 of byte 8 + 16 j + l % 16."""
+    b = bytearray(136)
+    b[0:2] = struct.pack("<H", d_bits)
+    word = 0
+    for j in range(8):
+        b[4 + j // 2] |= (ls[j] & 15) << (4 * (j % 2))
+        word |= (ls[j] >> 4) << (2 * j)
+    b[2:4] = struct.pack("<H", word)
+    for e in range(256):
+        j, l = e // 32, e % 32
+        b[8 + 16 * j + l % 16] |= codes[e] << (4 * (l // 16))
+    return bytes(b)
+
+
+def test_iq4_xs_with_a_linear_book_equals_q4_0_blocks():
+    # with the book replaced by c - 8, sub-block j is the Q4_0 block of scale
+    # d (ls_j - 32) over the same 16 code bytes (d a power of two, so that
+    # scale is an fp16 value)
+    rng = np.random.default_rng(31)
+    n, k = 3, 512
+    W4 = bytearray()
+    WX = bytearray()
+    for i in range(n):
+        for s_ in range(k // 256):
+            e = int(rng.integers(-8, 3))
+            ls = [int(v) for v in rng.integers(0, 64, size=8)]
+            codes = [int(v) for v in rng.integers(0, 16, size=256)]
+            sb = _iq4_xs_superblock(struct.unpack("<H", struct.pack("<e", 2.0 ** e))[0], ls, codes)
+            WX += sb
+            for j in range(8):
+                W4 += struct.pack("<e", 2.0 ** e * (ls[j] - 32)) + sb[8 + 16 * j:24 + 16 * j]
+    WX = np.frombuffer(bytes(WX), np.uint8).reshape(n, -1)
+    W4 = np.frombuffer(bytes(W4), np.uint8).reshape(n, -1)
+    lin = tuple(range(-8, 8))
+    np.testing.assert_array_equal(oracle.qref._dequant_iq4_xs(WX, n, k, table=lin),
+                                  oracle.dequant_f64(synth.Q4_0, W4, n, k))
+
+
+def test_iq4_xs_scales_land_on_their_sub_blocks():
+    # d = 1, every code 8 with the identity book (c stands for c): element e is
+    # 8 (ls_{e // 32} - 32); the default book gives entry 8 times ls - 32
+    ls = [0, 63, 32, 33, 17, 48, 31, 1]
+    raw = np.frombuffer(_iq4_xs_superblock(0x3C00, ls, [8] * 256), np.uint8).reshape(1, 136)
+    want = np.repeat(np.array(ls, np.float64) - 32, 32)
+    np.testing.assert_array_equal(oracle.qref._dequant_iq4_xs(raw, 1, 256, table=tuple(range(16)))[0], 8 * want)
+    np.testing.assert_array_equal(oracle.iq4_xs_scales(raw)[0], np.array(ls) - 32)
+    np.testing.assert_array_equal(oracle.dequant_f64(synth.IQ4_XS, raw, 1, 256)[0],
+                                  oracle.IQ4_NL_VALUES[8] * want)
+
+
+def test_iq4_xs_codes_in_element_order():
+    # d = 1, every scale 33 (ls - 32 = 1), the identity book: element e is its
+    # own code; then one element's code alone set
+    codes = [(e * 7 + e // 32) % 16 for e in range(256)]
+    raw = np.frombuffer(_iq4_xs_superblock(0x3C00, [33] * 8, codes), np.uint8).reshape(1, 136)
+    np.testing.assert_array_equal(oracle.qref._dequant_iq4_xs(raw, 1, 256, table=tuple(range(16)))[0],
+                                  np.array(codes, np.float64))
+    np.testing.assert_array_equal(oracle.dequant_f64(synth.IQ4_XS, raw, 1, 256)[0],
+                                  np.array([oracle.IQ4_NL_VALUES[c] for c in codes], np.float64))
+
+
+def test_iq4_xs_book_shape():
+    # the book's values are taken as given (nothing on the pages fixes them);
+    # what the format needs of it: 16 distinct increasing int8 values that
+    # reach -127, so that |w| <= 127 |d (ls - 32)| and fp32 holds w exactly
+    book = np.array(oracle.IQ4_NL_VALUES)
+    assert book.shape == (16,) and np.all(np.diff(book) > 0)
+    assert book.min() == -127 and book.max() < 128
+
+
+def test_iq4_xs_encoder_round_trip_and_sizes():
+    n, k = 16, 512
+    w = synth.weight_f32(n, k, seed=6)
+    W = synth.quantize(synth.IQ4_XS, w)
+    assert W.shape == (n, k // 256 * 136) == (n, synth.row_bytes(synth.IQ4_XS, k))
+    deq = oracle.dequant_f64(synth.IQ4_XS, W, n, k)
+    err = np.abs(deq - w.astype(np.float64)).reshape(n, k // 256, 8, 32)
+    amax = np.abs(w.reshape(n, k // 256, 8, 32)).max(-1)
+    # the book's widest gap (24 of 127) at a step of amax / 127, the 6-bit
+    # scale and fp16 d adding a few hundredths of the largest value
+    assert np.all(err.max(-1) <= amax * 12.5 / 127 + 0.04 * np.abs(w).max())
+    assert np.linalg.norm(deq - w) / np.linalg.norm(w) < 0.12
+    with pytest.raises(ValueError):
+        oracle.dequant_f64(synth.IQ4_XS, W[:, :136], n, 128)
+
 
 # ---------------------------------------------------------------- brute force
 def _parse_block_independent(qtype, blk: bytes):
@@ -366,9 +455,9 @@ def _random_blocks(rng, qtype, n, k):
     """Random raw bytes with finite scales (exponent field kept below 31); for
     F16 every element is such a half; for Q4_K d and dmin of every superblock."""
     if qtype in KQ:
-        sbb = {synth.Q4_K: 144, synth.Q5_K: 176, synth.Q6_K: 210}[qtype]
+        sbb = {synth.Q4_K: 144, synth.Q5_K: 176, synth.Q6_K: 210, synth.IQ4_XS: 136}[qtype]
         raw = rng.integers(0, 256, size=(n, k // 256, sbb), dtype=np.uint8)
-        for b in ((209,) if qtype == synth.Q6_K else (1, 3)):
+        for b in {synth.Q6_K: (209,), synth.IQ4_XS: (1,)}.get(qtype, (1, 3)):
             raw[..., b] = np.where((raw[..., b] & 0x7C) == 0x7C, raw[..., b] & 0xBF, raw[..., b])
         return raw.reshape(n, -1)
     bb = synth.block_bytes(qtype)
@@ -435,7 +524,30 @@ def _q6_k_row_independent(raw: bytes, k):
     return out
 
 
+_BOOK = [-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113]
+
+
+def _iq4_xs_row_independent(raw: bytes, k):
+    """Exact values of one IQ4_XS row, element by element with struct:
+    element 32 j + l takes nibble l // 16 of byte 8 + 16 j + l % 16 as its
+    code c, scale ls_j from nibble j % 2 of byte 4 + j // 2 and bits 2 j,
+    2 j + 1 of the word at bytes 2-3; w = d (ls_j - 32) book[c]."""
+    out = []
+    for sb in range(k // 256):
+        blk = raw[136 * sb:136 * (sb + 1)]
+        d = Fraction(struct.unpack("<e", blk[0:2])[0])
+        word = struct.unpack("<H", blk[2:4])[0]
+        for e in range(256):
+            j, l = e // 32, e % 32
+            ls = ((blk[4 + j // 2] >> (4 * (j % 2))) & 15) + 16 * ((word >> (2 * j)) & 3)
+            c = (blk[8 + 16 * j + l % 16] >> (4 * (l // 16))) & 15
+            out.append(d * (ls - 32) * _BOOK[c])
+    return out
+
+
 def _kq_row_independent(qtype, raw: bytes, k):
+    if qtype == synth.IQ4_XS:
+        return _iq4_xs_row_independent(raw, k)
     if qtype == synth.Q6_K:
         return _q6_k_row_independent(raw, k)
     return _q4_k_row_independent(raw, k, five=qtype == synth.Q5_K)
