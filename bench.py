@@ -590,8 +590,8 @@ def projection_rate(q, dev, stream, peak_tf, peak_gbs, *, qtype, n, k, T, residu
     2 T n k (x2 for gate/up), bytes = the quantized weight(s) + X + Y (+ R)."""
     import torch
 
-    # bytes per 256 weights (F16, Q4_0, Q8_0, Q4_K, Q5_K, Q6_K); every k here is a multiple of 256
-    b256 = {1: 512, 2: 144, 8: 272, 12: 144, 13: 176, 14: 210}[qtype]
+    # bytes per 256 weights (F16, Q4_0, Q8_0, Q4_K, Q5_K, Q6_K, IQ4_XS); every k here is a multiple of 256
+    b256 = {1: 512, 2: 144, 8: 272, 12: 144, 13: 176, 14: 210, 23: 136}[qtype]
     wbytes = n * (k // 256) * b256 * (2 if gate_up else 1)
     byts = wbytes + 4 * T * k + 4 * T * n * (2 if residual else 1)
     nsets = int(min(16, max(2, -(-2.5 * L2_BYTES // byts))))
@@ -638,10 +638,10 @@ def every_workload(q, dev, stream, peak_tf, peak_gbs):
       on the fp16 leg and the exact-fp32 leg;
     * F16 weights: 4096 x 4096 + R at 512 tokens on both legs, gate/up 12288 x
       4096 at 512 tokens, and the GEMV at T = 1 and 4;
-    * Q4_K, Q5_K and Q6_K weights: the same five workloads."""
+    * Q4_K, Q5_K, Q6_K and IQ4_XS weights: the same five workloads."""
     import torch
 
-    F16, Q4, Q8, Q4K, Q5K, Q6K = 1, 2, 8, 12, 13, 14
+    F16, Q4, Q8, Q4K, Q5K, Q6K, IQ4 = 1, 2, 8, 12, 13, 14, 23
     P = lambda **kw: projection_rate(q, dev, stream, peak_tf, peak_gbs, **kw)  # noqa: E731
     out = {}
     out["q8_0_n256_k512_t16"] = {"auto (T rule: the GEMM)": P(qtype=Q8, n=256, k=512, T=16),
@@ -679,7 +679,7 @@ def every_workload(q, dev, stream, peak_tf, peak_gbs):
                 "down_n4096_k12288_res": P(qtype=Q4, n=4096, k=12288, T=T, residual=True, leg=leg, seed=13),
             }
     out["layer_9b_q4_0"] = layer
-    for qt, name in ((F16, "f16"), (Q4K, "q4_k"), (Q5K, "q5_k"), (Q6K, "q6_k")):
+    for qt, name in ((F16, "f16"), (Q4K, "q4_k"), (Q5K, "q5_k"), (Q6K, "q6_k"), (IQ4, "iq4_xs")):
         out[name] = {
             "n4096_k4096_t512_res": P(qtype=qt, n=4096, k=4096, T=512, residual=True),
             "n4096_k4096_t512_res_exact": P(qtype=qt, n=4096, k=4096, T=512, residual=True, leg=1),
@@ -864,9 +864,9 @@ def main(argv=None):
                          "(--kernel-qtype weights); exact: only the exact-fp32 leg's GEMM call on the same problem; "
                          "gemv: only the T = 1 GEMV; attention: only the prefill attention (16 query heads, 4 KV "
                          "heads, --attn-tokens rows at position 0) (small, bounded runs for profilers)")
-    ap.add_argument("--kernel-qtype", type=int, default=2, choices=[1, 2, 8, 12, 13, 14],
+    ap.add_argument("--kernel-qtype", type=int, default=2, choices=[1, 2, 8, 12, 13, 14, 23],
                     help="weight type of the --only kernel and --only gemv runs (GGUF id: 1 F16, 2 Q4_0, 8 Q8_0, 12 Q4_K, "
-                         "13 Q5_K, 14 Q6_K)")
+                         "13 Q5_K, 14 Q6_K, 23 IQ4_XS)")
     ap.add_argument("--attn-tokens", type=int, default=2048, help="query rows of the --only attention run")
     ap.add_argument("--gemv-tokens", type=int, default=1, help="tokens of the --only gemv run (1..16)")
     ap.add_argument("--clocks-dir", default=None, help="where the raw nvidia-smi clock samples are written")

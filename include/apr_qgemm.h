@@ -1,6 +1,7 @@
 /*
  * apr_qgemm.h — C ABI of the GB300 (sm_103a) prefill projections over GGUF
- * Q4_0 / Q8_0 / Q4_K / Q5_K / Q6_K block-quantized weights and F16 weights.
+ * Q4_0 / Q8_0 / Q4_K / Q5_K / Q6_K / IQ4_XS block-quantized weights and F16
+ * weights.
  *
  * Every projection of a batched (chunked) prompt prefill is ONE product over
  * the chunk's T token rows, instead of T per-token GEMVs:
@@ -51,7 +52,22 @@
  *                    Element 128h + 32c + l (c < 4, l < 32) has nibble c / 2
  *                    of byte 64h + 32(c % 2) + l and bits 2c, 2c + 1 of byte
  *                    128 + 32h + l as its 6-bit code q; w = d * sc * (q - 32).
- * Row i of W is the k/32 consecutive blocks starting at byte i*(k/32)*bytes.
+ *   IQ4_XS (136 bytes per 256 weights, k % 512 == 0 so that every row starts
+ *                    on a 16-byte boundary): dispatched by the pages
+ *                    (Iq4XsDequantKernel, iq4_xs_dequant_to_f32) without its
+ *                    layout or code book; taken as the GGUF superblock: fp16
+ *                    d, a little-endian word of high scale bits, 4 bytes of
+ *                    low scale nibbles, then 128 code bytes, 16 per 32
+ *                    weights. Sub-block j (weights 32j ..) has the 6-bit
+ *                    scale ls_j (low nibble: nibble j % 2 of byte 4 + j / 2;
+ *                    top two bits: bits 2j, 2j + 1 of the word); byte
+ *                    8 + 16j + l holds the code c of weight 32j + l (low
+ *                    nibble) and of 32j + 16 + l (high nibble);
+ *                    w = d * (ls_j - 32) * book[c], book the IQ4_NL code
+ *                    book {-127, -104, -83, -65, -49, -35, -22, -10, 1, 13,
+ *                    25, 38, 53, 69, 89, 113}.
+ * Row i of W is the k/32 consecutive blocks starting at byte i*(k/32)*bytes
+ * (the superblock formats: k/256 superblocks).
  *
  * Memory and streams. Every pointer argument named W, Wu, X, residual, Y or
  * out is a DEVICE pointer on the current CUDA device, owned by the caller and
@@ -79,11 +95,11 @@
  * Errors. Arguments are checked on the host before anything is enqueued:
  *   APR_E_INVAL   null pointer with nonzero sizes, n < 0, T < 0, k <= 0,
  *                 k % 32 != 0 (k % 256 != 0 for Q4_K, Q5_K; k % 2048 != 0
- *                 for Q6_K), a size beyond the
+ *                 for Q6_K; k % 512 != 0 for IQ4_XS), a size beyond the
  *                 documented limits, or an
  *                 unknown leg / path
- *   APR_E_QTYPE   qtype is not APR_Q4_0, APR_Q8_0, APR_F16, APR_Q4_K, APR_Q5_K
- *                 or APR_Q6_K
+ *   APR_E_QTYPE   qtype is not APR_Q4_0, APR_Q8_0, APR_F16, APR_Q4_K, APR_Q5_K,
+ *                 APR_Q6_K or APR_IQ4_XS
  *   APR_E_ALIGN   a pointer is not 16-byte aligned
  *   APR_E_ALIAS   Y overlaps X, W or Wu, or overlaps residual without being
  *                 exactly the same buffer (Y == residual is allowed: it gives
@@ -119,7 +135,7 @@ extern "C" {
 typedef struct CUstream_st* apr_stream_t;
 
 /* GGUF tensor type ids. */
-enum { APR_F16 = 1, APR_Q4_0 = 2, APR_Q8_0 = 8, APR_Q4_K = 12, APR_Q5_K = 13, APR_Q6_K = 14 };
+enum { APR_F16 = 1, APR_Q4_0 = 2, APR_Q8_0 = 8, APR_Q4_K = 12, APR_Q5_K = 13, APR_Q6_K = 14, APR_IQ4_XS = 23 };
 
 /*
  * Arithmetic legs (aprender-serve gdn_prefill_ops.rs, module doc, group 1):
@@ -165,7 +181,8 @@ int apr_gemv_max_T(void);
 
 /*
  * Y = X . dequant(W)^T (+ residual), fp16 leg, T rule.
- *   qtype     APR_Q4_0, APR_Q8_0, APR_F16, APR_Q4_K, APR_Q5_K or APR_Q6_K
+ *   qtype     APR_Q4_0, APR_Q8_0, APR_F16, APR_Q4_K, APR_Q5_K, APR_Q6_K or
+ *             APR_IQ4_XS
  *   W         [n rows][k/32 blocks] GGUF blocks
  *   X         [T][k] f32;  Y [T][n] f32, overwritten
  *   residual  [T][n] f32 or NULL; may be Y itself (accumulate)
@@ -194,7 +211,7 @@ int apr_qgemm_gate_up_swiglu(int qtype, const void* Wg, const void* Wu, int n, i
  * oxibonsai-kernels, used for the last-token lm_head in
  * try_cuda_prefill_q_std). Weight rows stream by bulk copies into T fp32
  * accumulators for T <= 4 with Q4_0 / Q8_0 (tensor cores for T = 3, 4) and
- * T <= 8 with F16 and K-quant weights (CUDA cores); for larger T up to 16,
+ * T <= 8 with F16, K-quant and IQ4_XS weights (CUDA cores); for larger T up to 16,
  * and for smaller T where no streaming kernel takes the shape (the X table of
  * a long row does not fit shared memory), the exact leg's tensor-core GEMM
  * runs instead when k % 256 == 0 (22-24 us at 4096 x 4096 for T <= 16, with k
@@ -403,7 +420,8 @@ int apr_prefill_attention(const float* Q, const float* K_cache, const float* V_c
  *            k rows, then the v rows (the pages' fused qkv weight)
  *   Wo       [hidden][num_heads * 256];  Wg, Wu [inter][hidden];  Wd [hidden][inter]
  *   hidden, inter  multiples of the format's unit (32; 256 for Q4_K, Q5_K;
- *            2048 for Q6_K), and so must num_heads * 256 be (Wo's columns)
+ *            2048 for Q6_K; 512 for IQ4_XS), and so must num_heads * 256 be
+ *            (Wo's columns)
  *   num_heads, num_kv_heads, head_dim  as for apr_prefill_attention (256)
  *   T, pos0  rows of X and the position of the first; T == 0 is a no-op
  *   attn_norm, ffn_norm  [hidden] fp32;  eps >= 0 and finite
@@ -447,7 +465,8 @@ int apr_prefill_layer(const apr_layer_args* args);
  * Standalone dequant: out[n][k] f32 = f32(d) * f32(q'), bit exact (the product
  * of an fp16 scale and a code of at most 8 bits is exact in fp32); for F16
  * out = f32(w), also exact; for Q4_K and Q5_K the exact d * sc * q - dmin * m
- * rounded once to f32; for Q6_K d * sc * (q - 32), exact. The device dequant of aprender-serve
+ * rounded once to f32; for Q6_K d * sc * (q - 32) and for IQ4_XS
+ * d * (ls - 32) * book[c], both exact. The device dequant of aprender-serve
  * gdn_prefill_ops.rs qwen35_dequant_f32 (Q8_0, F16 and the other formats it
  * dispatches), here for every qtype above and meant for tests: the
  * projections never write decoded weights to memory. An F16 W needs only

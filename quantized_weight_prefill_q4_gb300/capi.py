@@ -21,6 +21,7 @@ APR_Q8_0 = 8
 APR_Q4_K = 12
 APR_Q5_K = 13
 APR_Q6_K = 14
+APR_IQ4_XS = 23
 APR_LEG_F16 = 0
 APR_LEG_EXACT_F32 = 1
 APR_PATH_AUTO = 0
@@ -40,7 +41,7 @@ APR_AUTO_GEMV_MAX_T = 4
 APR_NOALLOC_MAX_TK = 8 * 1024 * 1024
 APR_FFN_CHUNK_ROWS = 2048
 
-BLOCK_BYTES = {APR_F16: 64, APR_Q4_0: 18, APR_Q8_0: 34, APR_Q4_K: 18, APR_Q5_K: 22}  # bytes per 32 weights
+BLOCK_BYTES = {APR_F16: 64, APR_Q4_0: 18, APR_Q8_0: 34, APR_Q4_K: 18, APR_Q5_K: 22, APR_IQ4_XS: 17}  # per 32 weights
 SUPERBLOCK_BYTES = {APR_Q6_K: 210}  # bytes per 256 weights, for the formats without whole bytes per 32
 
 

@@ -179,12 +179,16 @@ struct Problem {
 int ldy_of(const Problem& p) { return p.ldy > 0 ? p.ldy : p.n; }
 
 bool known_qtype(int q) {
-  return q == APR_Q4_0 || q == APR_Q8_0 || q == APR_F16 || q == APR_Q4_K || q == APR_Q5_K || q == APR_Q6_K;
+  return q == APR_Q4_0 || q == APR_Q8_0 || q == APR_F16 || q == APR_Q4_K || q == APR_Q5_K || q == APR_Q6_K ||
+         q == APR_IQ4_XS;
 }
 // k (the columns of every weight row) a whole number of the format's blocks;
 // Q6_K rows (210 bytes per 256) start on 16-byte boundaries only when k is a
-// multiple of 2048, and every Q6_K route reads them from such boundaries
-int k_unit(int qtype) { return qtype == kQ6_K ? 2048 : (kquant(qtype) ? 256 : 32); }
+// multiple of 2048, IQ4_XS rows (136 bytes per 256) when k is a multiple of
+// 512, and every route reads them from such boundaries
+int k_unit(int qtype) {
+  return qtype == kQ6_K ? 2048 : (qtype == kIQ4_XS ? 512 : (kquant(qtype) ? 256 : 32));
+}
 bool k_fits(int qtype, int k) { return k > 0 && k % k_unit(qtype) == 0; }
 
 // a streaming GEMV kernel (integer-dot, whole-row, bulk, tensor-core or the K-quant one) takes the shape

@@ -14,14 +14,17 @@ constexpr int kQ8_0 = 8;
 constexpr int kQ4_K = 12;  // 256-element superblocks of 144 bytes (k % 256 == 0)
 constexpr int kQ5_K = 13;  // 256-element superblocks of 176 bytes (k % 256 == 0)
 constexpr int kQ6_K = 14;  // 256-element superblocks of 210 bytes (k % 2048 == 0: rows on 16-byte boundaries)
-inline bool kquant(int qtype) { return qtype == kQ4_K || qtype == kQ5_K || qtype == kQ6_K; }
+constexpr int kIQ4_XS = 23;  // 256-element superblocks of 136 bytes (k % 512 == 0: rows on 16-byte boundaries)
+// the 256-element superblock formats (the K-quants and IQ4_XS)
+inline bool kquant(int qtype) { return qtype == kQ4_K || qtype == kQ5_K || qtype == kQ6_K || qtype == kIQ4_XS; }
 
 // bytes of 32 consecutive elements of a weight row (one block; 64 for F16; an
-// eighth of a Q4_K or Q5_K superblock); 0 for Q6_K, whose eighth of a
+// eighth of a Q4_K, Q5_K or IQ4_XS superblock); 0 for Q6_K, whose eighth of a
 // superblock is not a whole number of bytes
 inline int block_bytes(int qtype) {
-  return qtype == kQ4_0 || qtype == kQ4_K ? 18
-                                          : (qtype == kQ8_0 ? 34 : (qtype == kQ5_K ? 22 : (qtype == kQ6_K ? 0 : 64)));
+  return qtype == kQ4_0 || qtype == kQ4_K
+             ? 18
+             : (qtype == kQ8_0 ? 34 : (qtype == kQ5_K ? 22 : (qtype == kQ6_K ? 0 : (qtype == kIQ4_XS ? 17 : 64))));
 }
 // bytes of one weight row of k elements (k a multiple of the format's unit)
 inline size_t row_bytes_of(int qtype, int k) {

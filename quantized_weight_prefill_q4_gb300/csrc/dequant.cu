@@ -1,6 +1,6 @@
 // Standalone dequant: out[n][k] = f32(d) * f32(q') (F16: f32(w); Q4_K and Q5_K:
-// d sc q - dmin m rounded once; Q6_K: d sc (q - 32), exact), bit exact against
-// the oracle.
+// d sc q - dmin m rounded once; Q6_K: d sc (q - 32), exact; IQ4_XS:
+// d (ls - 32) book[c], exact), bit exact against the oracle.
 //
 // The device dequant of aprender-serve 0.70.2 src/cuda/executor/gdn_prefill_ops.rs
 // (qwen35_dequant_f32: one 32-element block per warp, one element per lane),
@@ -10,6 +10,7 @@
 #include <cuda_fp16.h>
 
 #include "apr_internal.h"
+#include "iq4.cuh"
 #include "q4k.cuh"
 
 namespace apr {
@@ -38,6 +39,20 @@ __global__ void __launch_bounds__(256) dequant_kernel(const uint8_t* __restrict_
       const int sc = (int)(int8_t)sb[192 + e / 16];
       // d sc is exact (11 + 8 bits) and so is its product with q - 32
       out[idx] = d * (float)sc * (float)((int)(lo | (hi << 4)) - 32);
+      continue;
+    }
+    if constexpr (QT == kIQ4_XS) {  // superblock of 256 in 136 bytes, read bytewise
+      const size_t row = idx / (size_t)k;
+      const uint32_t col = (uint32_t)(idx - row * (size_t)k);
+      const uint8_t* sb = W + (row * (size_t)(k / 256) + col / 256) * 136;
+      const uint32_t e = col & 255u, j = e >> 5, l = e & 31u;
+      const uint32_t c = (sb[8 + 16 * j + (l & 15u)] >> (4 * (l >> 4))) & 15u;
+      // ls_j: nibble j % 2 of byte 4 + j / 2, and bits 2 (j % 4) of byte 2 + j / 4
+      const int ls = (int)(((sb[4 + j / 2] >> (4 * (j & 1u))) & 15u) | (((sb[2 + j / 4] >> (2 * (j & 3u))) & 3u) << 4));
+      const int v = (int)(iq4_bytes4(c) & 0xFFu) - 128;  // book[c]
+      const float d = __half2float(__ushort_as_half((uint16_t)(sb[0] | (sb[1] << 8))));
+      // d (ls - 32) is exact (11 + 5 bits) and so is its product with book[c]
+      out[idx] = d * (float)(ls - 32) * (float)v;
       continue;
     }
     if constexpr (QT == kQ4_K || QT == kQ5_K) {  // superblock of 256 in 144 or 176 bytes
@@ -79,7 +94,9 @@ cudaError_t launch_dequant(int qtype, const void* W, int n, int k, float* out, c
   const size_t total = (size_t)n * (size_t)k;
   size_t blocks = (total + 255) / 256;
   if (blocks > 152 * 64) blocks = 152 * 64;
-  if (qtype == kQ6_K)
+  if (qtype == kIQ4_XS)
+    dequant_kernel<kIQ4_XS><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);
+  else if (qtype == kQ6_K)
     dequant_kernel<kQ6_K><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);
   else if (qtype == kQ5_K)
     dequant_kernel<kQ5_K><<<(unsigned)blocks, 256, 0, s>>>((const uint8_t*)W, n, k, out);

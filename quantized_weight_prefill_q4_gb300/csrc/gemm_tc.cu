@@ -76,6 +76,7 @@
 #include "apr_internal.h"
 #include "dev_common.cuh"
 #include "host_common.h"
+#include "iq4.cuh"
 #include "q4k.cuh"
 
 namespace apr {
@@ -109,23 +110,29 @@ struct Cfg {
   static constexpr int DQ = NM == 1 ? 2 : 1;           // warpgroups per weight (alternate stages)
   static constexpr int NWG = NM * DQ;                   // dequant / epilogue warpgroups
   static constexpr bool F16W = QT == kF16;
-  static constexpr bool Q4W = QT == kQ4_0 || QT == kQ4_K || QT == kQ5_K;  // ring depths of the short-row formats
+  static constexpr bool IQ4 = QT == kIQ4_XS;
+  // ring depths of the short-row formats
+  static constexpr bool Q4W = QT == kQ4_0 || QT == kQ4_K || QT == kQ5_K || IQ4;
   static constexpr bool Q6K = QT == kQ6_K;
-  static constexpr int BB = QT == kQ4_0 || QT == kQ4_K ? 18 : (QT == kQ8_0 ? 34 : (QT == kQ5_K ? 22 : 64));
+  static constexpr int BB =
+      QT == kQ4_0 || QT == kQ4_K ? 18 : (QT == kQ8_0 ? 34 : (QT == kQ5_K ? 22 : (IQ4 ? 17 : 64)));
   // words a decode thread reads per stage: two blocks, or for Q4_K / Q5_K the
   // superblock's header and scales (4 words), Q5_K's fifth-bit bytes (8
   // words) and the stage's 32 code bytes (8 words); for Q6_K the aligned
   // words over the stage's 64 low-nibble bytes, 32 high-bit bytes and 4
   // scales (each one word more: the superblock may start 2 bytes into a
-  // word) and the word holding d
-  static constexpr int NWORDS = QT == kQ4_K ? 12 : (QT == kQ5_K ? 20 : (Q6K ? 29 : 2 * BB / 4));
+  // word) and the word holding d; for IQ4_XS the header's two words (d and
+  // the high scale bits, the low scale nibbles) and the stage's 32 code bytes
+  static constexpr int NWORDS = QT == kQ4_K ? 12 : (QT == kQ5_K ? 20 : (Q6K ? 29 : (IQ4 ? 10 : 2 * BB / 4)));
   // k per raw slot: a chunk, or half of one for an F16 gate/up pair (four
   // slots of 32 KB keep each weight double-buffered)
   static constexpr int RAW_K = F16W && NM == 2 ? CHUNK / 2 : CHUNK;
   static constexpr int RAW_SUBS = RAW_K / BK;         // operand stages per raw slot
   // 144 / 272 / 512 (or 256) bytes; Q6_K: a 224-byte box from the 16-byte
-  // boundary at or below the 210-byte superblock
-  static constexpr int RAW_ROW = Q6K ? 224 : RAW_K / 32 * BB;
+  // boundary at or below the 210-byte superblock; IQ4_XS: a 144-byte box from
+  // the 16-byte boundary at or below the 136-byte superblock (8 bytes below
+  // every other one)
+  static constexpr int RAW_ROW = Q6K ? 224 : (IQ4 ? 144 : RAW_K / 32 * BB);
   static constexpr int RAW_BYTES = BM * RAW_ROW;      // one raw slot
   // F16 rows arrive as 64-column boxes of [128 rows][128 B], 128-byte
   // swizzled (conflict-free row reads); block formats as one unswizzled box
@@ -135,6 +142,7 @@ struct Cfg {
   // operand stages (A in TMEM and B in shared memory advance together)
   static constexpr int S = XS ? 2 : (NM == 2 ? 4 : (BN == 256 ? 4 : (Q4W ? 6 : (F16W ? 4 : 5))));
   static_assert(!Q6K || RAW_K == 256, "a Q6_K raw slot is one superblock");
+  static_assert(!IQ4 || RAW_K == 256, "an IQ4_XS raw slot is one superblock");
   // (with 256-token tiles the raw ring also receives the partner's half of a
   // split). With gate/up the chunks of the two weights alternate through the
   // ring, chunk j in slot j % S_RAW; S_RAW must be even so that a slot always
@@ -418,6 +426,48 @@ __device__ __forceinline__ void q6k_row_stage(const uint32_t* w, uint32_t g, uin
   }
 }
 
+// IQ4_XS: stage g (64 k: sub-blocks 2 g and 2 g + 1) of one row's superblock,
+// words w[0] = d | high scale bits << 16, w[1] = the low scale nibbles, then
+// the stage's code bytes, w[2..5] for sub-block 2 g and w[6..9] for 2 g + 1.
+// Word v of a sub-block holds elements 4 v .. 4 v + 3 in its low nibbles and
+// 16 + 4 v .. in its high ones; the book lookup turns it into (A0, B0, A1, B1)
+// and (A2, B2, A3, B3) as bytes book + 128. d (ls - 32) book[c] has at most
+// 23 significant bits, so it is exact in fp32, then rounded once to fp16
+// (xs = false) or scaled by sw = 2^e and split (xs = true).
+template <bool XSP>
+__device__ __forceinline__ void iq4xs_row_stage(const uint32_t* w, uint32_t g, float sw, uint32_t (&a1)[32],
+                                                uint32_t (&a2)[32]) {
+  const float d = __half2float(__ushort_as_half((unsigned short)(w[0] & 0xFFFFu)));
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float D = d * (float)iq4_scale(w[0], w[1], 2 * g + h);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      uint32_t u[2];
+      iq4_word(w[2 + 4 * h + v], u[0], u[1]);
+      // element 4 v + m is byte 2 (m % 2) of u[m / 2], 16 + 4 v + m the byte after
+      float A[4], B[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {  // book[c] exactly: the float 2^23 + byte less 2^23 + 128
+        A[m] = (__uint_as_float(__byte_perm(u[m >> 1], 0x4B000000u, 0x7440u + 2 * (m & 1))) - 8388736.0f) * D;
+        B[m] = (__uint_as_float(__byte_perm(u[m >> 1], 0x4B000000u, 0x7441u + 2 * (m & 1))) - 8388736.0f) * D;
+      }
+      const int j = 16 * h + 2 * v;
+      if constexpr (XSP) {
+        split2(A[0] * sw, A[1] * sw, a1[j], a2[j]);
+        split2(A[2] * sw, A[3] * sw, a1[j + 1], a2[j + 1]);
+        split2(B[0] * sw, B[1] * sw, a1[j + 8], a2[j + 8]);
+        split2(B[2] * sw, B[3] * sw, a1[j + 9], a2[j + 9]);
+      } else {
+        a1[j] = h2_as_u32(__floats2half2_rn(A[0], A[1]));
+        a1[j + 1] = h2_as_u32(__floats2half2_rn(A[2], A[3]));
+        a1[j + 8] = h2_as_u32(__floats2half2_rn(B[0], B[1]));
+        a1[j + 9] = h2_as_u32(__floats2half2_rn(B[2], B[3]));
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- kernel
 template <int QT, int EPI, int BN, bool XS>
 __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
@@ -517,6 +567,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
       // formats, the k index itself for F16
       auto raw_x = [&](int u, int b) {
         if constexpr (C::Q6K) return (((c0 + u) * 210) & ~15) / 2;  // 16-byte aligned; the decode skips the rest
+        if constexpr (C::IQ4) return (((c0 + u) * 136) & ~15) / 2;
         return C::F16W ? c0 * CHUNK + u * C::RAW_K + b * BK : (c0 + u) * (C::RAW_ROW / 2);
       };
       // an L2 prefetch changes no data, so it may run before the wait
@@ -707,6 +758,13 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
           w[26] = sbw[48 + s];
           w[27] = sbw[49 + s];
           w[28] = sbw[52];
+        } else if constexpr (C::IQ4) {
+          // the superblock starts 8 bytes into the box row when its index is odd
+          const uint32_t* sbw = raw_row + 2 * ((c0 + c) & 1);
+          w[0] = sbw[0];
+          w[1] = sbw[1];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) w[2 + v] = sbw[2 + 8 * s + v];
         } else if constexpr (QT == kQ4_K || QT == kQ5_K) {
           constexpr int H = QT == kQ5_K ? 12 : 4;  // words before the code bytes
 #pragma unroll
@@ -719,6 +777,8 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
         }
         if constexpr (C::Q6K)
           q6k_row_stage<XS>(w, (uint32_t)s, (uint32_t)((c0 + c) * 2) & 2u, sw, a, a2);  // overlaps the wait below
+        else if constexpr (C::IQ4)
+          iq4xs_row_stage<XS>(w, (uint32_t)s, sw, a, a2);
         else if constexpr (QT == kQ4_K || QT == kQ5_K)
           q4k_row_stage<XS, QT == kQ5_K>(w, (uint32_t)s, sw, a, a2);
         else if constexpr (XS)
@@ -1117,8 +1177,9 @@ __global__ void row_exp_f16_kernel(const uint16_t* __restrict__ W, int n, int k,
 
 // K-quants: the same exponent from a bound on the row's largest |w|, the
 // largest over its superblocks of |d| cd + |dmin| cm: Q4_K and Q5_K |d| 63 qmax
-// + |dmin| 63 (qmax 15 or 31), Q6_K |d| 128 x 32 (d at byte 208, no dmin);
-// every weight's magnitude is at most that. One warp per row.
+// + |dmin| 63 (qmax 15 or 31), Q6_K |d| 128 x 32 (d at byte 208, no dmin),
+// IQ4_XS |d| 32 x 127 (no dmin); every weight's magnitude is at most that.
+// One warp per row.
 __global__ void row_exp_kq_kernel(const uint8_t* __restrict__ W, int n, int nsb, int sbb, int doff, float cd,
                                   float cm, int* __restrict__ erow) {
   const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -1292,9 +1353,13 @@ int launch_gemm_xs(int qtype, const void* W, const void* Wu, int n, int k, const
     row_exp_f16_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint16_t*>(W), n, k, erow);
     if (Wu) row_exp_f16_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint16_t*>(Wu), n, k, erow + n);
   } else if (kquant(qtype)) {
-    const int sbb = qtype == kQ4_K ? 144 : (qtype == kQ5_K ? 176 : 210), doff = qtype == kQ6_K ? 208 : 0;
-    const float cd = qtype == kQ4_K ? 63.f * 15.f : (qtype == kQ5_K ? 63.f * 31.f : 128.f * 32.f);
-    const float cm = qtype == kQ6_K ? 0.f : 63.f;
+    const int sbb = qtype == kQ4_K ? 144 : (qtype == kQ5_K ? 176 : (qtype == kQ6_K ? 210 : 136));
+    const int doff = qtype == kQ6_K ? 208 : 0;
+    const float cd = qtype == kQ4_K   ? 63.f * 15.f
+                     : qtype == kQ5_K ? 63.f * 31.f
+                     : qtype == kQ6_K ? 128.f * 32.f
+                                      : 32.f * 127.f;  // IQ4_XS: |ls - 32| <= 32, |book| <= 127
+    const float cm = qtype == kQ4_K || qtype == kQ5_K ? 63.f : 0.f;
     row_exp_kq_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(W), n, k / 256, sbb, doff, cd, cm, erow);
     if (Wu)
       row_exp_kq_kernel<<<rblocks, 256, 0, s>>>(static_cast<const uint8_t*>(Wu), n, k / 256, sbb, doff, cd, cm,
@@ -1317,6 +1382,8 @@ int launch_gemm_xs(int qtype, const void* W, const void* Wu, int n, int k, const
                                            part);
   if (qtype == kQ6_K) return launch_xs<kQ6_K>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len, ks,
                                            part);
+  if (qtype == kIQ4_XS)
+    return launch_xs<kIQ4_XS>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len, ks, part);
   return qtype == kQ4_0
              ? launch_xs<kQ4_0>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len, ks, part)
              : launch_xs<kQ8_0>(W, Wu, n, k, X1, X2, erow, etok, T, Y, ldy, R, status, s, msg, msg_len, ks, part);
@@ -1374,6 +1441,8 @@ int launch_gemm_tc(const GemmPlan& pl, int qtype, const void* W, const void* Wu,
                                           reg);
   if (qtype == kQ6_K) return launch_q<kQ6_K>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows,
                                           reg);
+  if (qtype == kIQ4_XS)
+    return launch_q<kIQ4_XS>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows, reg);
   return qtype == kQ4_0 ? launch_q<kQ4_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows, reg)
                         : launch_q<kQ8_0>(pl, W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, w, x_rows, reg);
 }

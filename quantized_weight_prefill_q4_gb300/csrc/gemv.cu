@@ -21,6 +21,7 @@
 
 #include "apr_internal.h"
 #include "host_common.h"
+#include "iq4.cuh"
 #include "q4k.cuh"
 
 namespace apr {
@@ -681,6 +682,121 @@ cudaError_t launch_q6k(const void* W, const void* Wu, int n, int k, const float*
   return launch_q6k_t<16, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
 }
 
+// IQ4_XS: a warp per row (two rows at T >= 2), lane L decoding elements
+// 8 L .. 8 L + 7 of each superblock: sub-block j = L / 4, its code bytes
+// 8 + 16 j + 8 (L % 2) .. (low nibbles for L % 4 < 2, high nibbles
+// otherwise), with the header's d and scale bits (bytes 0-7, one 8-byte
+// load). Rows start on 16-byte boundaries and superblocks on 8-byte ones.
+// w = d (ls - 32) book[c] is exact in fp32; products accumulate in fp32.
+template <int TMAX, bool SWI>
+__global__ void __launch_bounds__(kWarps * 32) gemv_iq4_kernel(const uint8_t* __restrict__ W,
+                                                               const uint8_t* __restrict__ Wu, int n, int k,
+                                                               const float* __restrict__ X, int T, float* Y, int ldy,
+                                                               const float* R) {
+  constexpr int NM = SWI ? 2 : 1;
+  constexpr int RB = kq_rows(TMAX), NS = RB * NM;  // rows together; weight rows read (row r, weight m: r NM + m)
+  constexpr int U = kq_unroll(TMAX) / RB;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nsb = k / 256;
+  const size_t row_bytes = (size_t)nsb * 136;
+  const uint32_t j = (uint32_t)lane >> 2, nsh = 4 * (((uint32_t)lane >> 1) & 1u);
+  const uint32_t coff = 8 + 16 * j + 8 * ((uint32_t)lane & 1u);
+  bool waited = false;
+  for (int row0 = (blockIdx.x * kWarps + warp) * RB; row0 < n; row0 += gridDim.x * kWarps * RB) {
+    float acc[NS][TMAX];
+#pragma unroll
+    for (int m = 0; m < NS; ++m)
+#pragma unroll
+      for (int t = 0; t < TMAX; ++t) acc[m][t] = 0.f;
+    const uint8_t* base[NS];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+      const size_t rr = (size_t)min(row0 + r, n - 1);  // a row past n repeats the last one, unstored
+      base[r * NM] = W + rr * row_bytes;
+      if (SWI) base[r * NM + 1] = Wu + rr * row_bytes;
+    }
+    for (int sb0 = 0; sb0 < nsb; sb0 += U) {
+      uint2 hd[U][NS], cw[U][NS];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int m = 0; m < NS; ++m)
+          if (sb0 + u < nsb) {
+            const uint8_t* sb = base[m] + (size_t)(sb0 + u) * 136;
+            hd[u][m] = ldw_v2(sb);
+            cw[u][m] = ldw_v2(sb + coff);
+          }
+      if (!waited) {
+        grid_dependency_wait_inline();
+        waited = true;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (sb0 + u >= nsb) break;
+        float w[NS][8];
+#pragma unroll
+        for (int m = 0; m < NS; ++m) {
+          const float a = __half2float(__ushort_as_half((unsigned short)(hd[u][m].x & 0xFFFFu))) *
+                          (float)iq4_scale(hd[u][m].x, hd[u][m].y, j);
+          // the lane's eight codes, one a byte, to book + 128
+          const uint32_t b0 = iq4_bytes4((cw[u][m].x >> nsh) & 0x0F0F0F0Fu);
+          const uint32_t b1 = iq4_bytes4((cw[u][m].y >> nsh) & 0x0F0F0F0Fu);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)  // book[c] exactly: the float 2^23 + byte less 2^23 + 128
+            w[m][e] = a * (__uint_as_float(__byte_perm(e < 4 ? b0 : b1, 0x4B000000u, 0x7440u + (e & 3))) -
+                           8388736.0f);
+        }
+        const int col = (sb0 + u) * 256 + 8 * lane;
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t) {
+          if (t < T) {
+            const float4* xr = reinterpret_cast<const float4*>(X + (size_t)t * k + col);
+            const float4 xa = __ldg(xr), xb = __ldg(xr + 1);
+            const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+            for (int m = 0; m < NS; ++m) {
+              float v = acc[m][t];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v = fmaf(w[m][e], xv[e], v);
+              acc[m][t] = v;
+            }
+          }
+        }
+      }
+    }
+    kq_rows_out<TMAX, NM, RB, SWI>(acc, row0, n, T, lane, Y, ldy, R);
+  }
+  if (!waited) grid_dependency_wait_inline();  // a CTA without rows
+}
+
+template <int TMAX, bool SWI>
+cudaError_t launch_iq4_t(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
+                         const float* R, cudaStream_t s) {
+  const int rows = kWarps * kq_rows(TMAX);
+  long blocks = (n + rows - 1) / rows;
+  const long cap = (long)num_sms() * 2;
+  if (blocks > cap) blocks = cap;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemv_iq4_kernel<TMAX, SWI>, static_cast<const uint8_t*>(W),
+                            static_cast<const uint8_t*>(Wu), n, k, X, T, Y, ldy, R);
+}
+
+template <bool SWI>
+cudaError_t launch_iq4(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
+                       const float* R, cudaStream_t s) {
+  if (T <= 1) return launch_iq4_t<1, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 2) return launch_iq4_t<2, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 4) return launch_iq4_t<4, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (T <= 8) return launch_iq4_t<8, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  return launch_iq4_t<16, SWI>(W, Wu, n, k, X, T, Y, ldy, R, s);
+}
+
 }  // namespace
 
 cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
@@ -698,6 +814,8 @@ cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, 
                : launch_q4k<kQ5_K, false>(W, Wu, n, k, X, T, Y, ldy, R, s);
   if (qtype == kQ6_K)
     return swi ? launch_q6k<true>(W, Wu, n, k, X, T, Y, ldy, R, s) : launch_q6k<false>(W, Wu, n, k, X, T, Y, ldy, R, s);
+  if (qtype == kIQ4_XS)
+    return swi ? launch_iq4<true>(W, Wu, n, k, X, T, Y, ldy, R, s) : launch_iq4<false>(W, Wu, n, k, X, T, Y, ldy, R, s);
   if (qtype == kF16) {
     if (k % 256 == 0)
       return swi ? launch_f16<true>(W, Wu, n, k, X, T, Y, ldy, R, s) : launch_f16<false>(W, Wu, n, k, X, T, Y, ldy, R, s);

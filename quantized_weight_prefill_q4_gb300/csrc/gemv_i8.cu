@@ -1,11 +1,13 @@
-// Single-token GEMV (T = 1) over Q4_0 / Q8_0 blocks and Q4_K / Q5_K / Q6_K
-// superblocks with integer dot products, exact to fp32 level (the
+// Single-token GEMV (T = 1) over Q4_0 / Q8_0 blocks and Q4_K / Q5_K / Q6_K /
+// IQ4_XS superblocks with integer dot products, exact to fp32 level (the
 // single-token GEMVs gemv_q4_0_pf / gemv_q8_0_pf of oxibonsai-kernels 0.1.4
-// src/gpu_backend/cuda_q_std_prefill.rs, HBM-bound form). A K-quant lane
+// src/gpu_backend/cuda_q_std_prefill.rs, HBM-bound form). A superblock lane
 // takes the 64 weights of one X block pair (Q4_K / Q5_K: one code group of a
 // superblock, two 32-weight sub-blocks; Q6_K: one 64-weight stage, four
-// 16-weight sub-blocks) and applies the sub-block scales, and for Q4_K / Q5_K
-// the mins against the block's sum of X, after the integer sums.
+// 16-weight sub-blocks; IQ4_XS: two 32-weight sub-blocks, their codes looked
+// up in the code book four at a time) and applies the sub-block scales, and
+// for Q4_K / Q5_K the mins against the block's sum of X, after the integer
+// sums.
 //
 // X in fixed point per 32-block: for block b, e_b makes max_j |x_j| 2^e_b lie
 // in [2^21, 2^22), and X_j = rint(x_j 2^e_b) (a 23-bit integer, off by at most
@@ -49,6 +51,7 @@
 #include "apr_internal.h"
 #include "dev_common.cuh"
 #include "host_common.h"
+#include "iq4.cuh"
 #include "q4k.cuh"
 
 namespace apr {
@@ -252,6 +255,59 @@ __device__ __forceinline__ float q6k_pair_dot(const uint32_t* w, uint32_t g, uin
   return r;
 }
 
+// IQ4_XS: the sum over a lane's 64 weights (stage g of a superblock:
+// sub-blocks 2 g and 2 g + 1, X blocks A and B). w[0] = d | high scale bits
+// << 16, w[1] the low scale nibbles, w[2..9] the stage's code words. The book
+// lookup gives each word's codes as (A0, B0, A1, B1) and (A2, B2, A3, B3)
+// (A_i: element 4 v + i, B_i: 16 + 4 v + i), signed bytes book[c], and the X
+// digit words of IQ4_XS lanes were put in that order when the table was
+// loaded (words 2 v and 2 v + 1 of each digit plane), so each sub-block is
+// d (ls - 32) 2^-e sum book[c] X with its digit sums exact in int32.
+__device__ __forceinline__ float iq4_pair_dot(const uint32_t* w, uint32_t g, const uint32_t (&ta)[XBW],
+                                              const uint32_t (&tb)[XBW]) {
+  const float d = __half2float(__ushort_as_half((unsigned short)(w[0] & 0xFFFFu)));
+  int acc[2][3];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t (&t)[XBW] = h ? tb : ta;
+    acc[h][0] = acc[h][1] = acc[h][2] = 0;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      uint32_t u0, u1;
+      iq4_word(w[2 + 4 * h + v], u0, u1);
+      u0 ^= 0x80808080u;  // book[c] + 128 to the signed byte book[c]
+      u1 ^= 0x80808080u;
+#pragma unroll
+      for (int kd = 0; kd < 3; ++kd) {
+        acc[h][kd] = dp4a_ss(u0, (int)t[8 * kd + 2 * v], acc[h][kd]);
+        acc[h][kd] = dp4a_ss(u1, (int)t[8 * kd + 2 * v + 1], acc[h][kd]);
+      }
+    }
+  }
+  const float vA = fmaf((float)acc[0][2], 65536.f, fmaf((float)acc[0][1], 256.f, (float)acc[0][0]));
+  const float vB = fmaf((float)acc[1][2], 65536.f, fmaf((float)acc[1][1], 256.f, (float)acc[1][0]));
+  const float sA = d * (float)iq4_scale(w[0], w[1], 2 * g) * __uint_as_float(ta[27]);
+  const float sB = d * (float)iq4_scale(w[0], w[1], 2 * g + 1) * __uint_as_float(tb[27]);
+  return fmaf(sA, vA, sB * vB);
+}
+
+// The X digit words of a block in the order of the IQ4_XS lookup's bytes:
+// word 2 v of a plane = (x_4v, x_16+4v, x_4v+1, x_17+4v), word 2 v + 1 =
+// (x_4v+2, x_18+4v, x_4v+3, x_19+4v)
+__device__ __forceinline__ void iq4_order_table(uint32_t (&t)[XBW]) {
+#pragma unroll
+  for (int kd = 0; kd < 3; ++kd) {
+    uint32_t o[8];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      o[2 * v] = __byte_perm(t[8 * kd + v], t[8 * kd + 4 + v], 0x5140);
+      o[2 * v + 1] = __byte_perm(t[8 * kd + v], t[8 * kd + 4 + v], 0x7362);
+    }
+#pragma unroll
+    for (int v = 0; v < 8; ++v) t[8 * kd + v] = o[v];
+  }
+}
+
 int rows_per_stage(int qtype, int k, bool swiglu) {
   const long row_bytes = (long)row_bytes_of(qtype, k);
   return (int)(ISTAGE / ((swiglu ? 2 : 1) * row_bytes));
@@ -262,9 +318,9 @@ __global__ void __launch_bounds__(ITHREADS, 2)
     gemv_i8_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ Wu, int n, int k,
                    const float* __restrict__ X, float* Y, const float* R, unsigned* status, int rs, int ns) {
   constexpr int NM = SWI ? 2 : 1;
-  constexpr bool KQ = QT == kQ4_K || QT == kQ5_K || QT == kQ6_K;
-  constexpr int BB = QT == kQ4_0 ? 18 : 34;                           // block formats
-  constexpr int SBB = QT == kQ4_K ? 144 : (QT == kQ5_K ? 176 : 210);  // K-quant superblocks
+  constexpr bool KQ = QT == kQ4_K || QT == kQ5_K || QT == kQ6_K || QT == kIQ4_XS;
+  constexpr int BB = QT == kQ4_0 ? 18 : 34;  // block formats
+  constexpr int SBB = QT == kQ4_K ? 144 : (QT == kQ5_K ? 176 : (QT == kQ6_K ? 210 : 136));  // superblocks
   constexpr int PW_WORDS = 2 * BB / 4;                                // words of one block pair
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
@@ -357,6 +413,10 @@ __global__ void __launch_bounds__(ITHREADS, 2)
       ta[4 * v] = a.x; ta[4 * v + 1] = a.y; ta[4 * v + 2] = a.z; ta[4 * v + 3] = a.w;
       tb[4 * v] = b.x; tb[4 * v + 1] = b.y; tb[4 * v + 2] = b.z; tb[4 * v + 3] = b.w;
     }
+    if constexpr (QT == kIQ4_XS) {
+      iq4_order_table(ta);
+      iq4_order_table(tb);
+    }
   }
 
   // one row's partial of this lane (its block pair), weight m
@@ -377,6 +437,16 @@ __global__ void __launch_bounds__(ITHREADS, 2)
       wq[27] = w[49 + (P & 3)];
       wq[28] = w[52];
       return q6k_pair_dot(wq, (uint32_t)P & 3u, 2u * (((uint32_t)P >> 2) & 1u), ta, tb);
+    } else if constexpr (QT == kIQ4_XS) {
+      // superblock P / 4 (34 words, rows on 16-byte boundaries): header words,
+      // then stage P mod 4's 8 code words
+      const uint32_t* w = rw + ((uint32_t)P >> 2) * 34u;
+      uint32_t wq[10];
+      wq[0] = w[0];
+      wq[1] = w[1];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) wq[2 + v] = w[2 + 8 * (P & 3) + v];
+      return iq4_pair_dot(wq, (uint32_t)P & 3u, ta, tb);
     } else if constexpr (KQ) {
       // superblock P / 4: header and scales, (Q5_K) fifth bits, then group P mod 4's codes
       constexpr int CW = QT == kQ5_K ? 12 : 4;
@@ -615,6 +685,9 @@ cudaError_t launch_gemv_i8(int qtype, const void* W, const void* Wu, int n, int 
   if (qtype == kQ6_K)
     return swi ? launch_i8<kQ6_K, true>(W, Wu, n, k, X, Y, R, status, s)
                : launch_i8<kQ6_K, false>(W, Wu, n, k, X, Y, R, status, s);
+  if (qtype == kIQ4_XS)
+    return swi ? launch_i8<kIQ4_XS, true>(W, Wu, n, k, X, Y, R, status, s)
+               : launch_i8<kIQ4_XS, false>(W, Wu, n, k, X, Y, R, status, s);
   if (qtype == kQ4_0)
     return swi ? launch_i8<kQ4_0, true>(W, Wu, n, k, X, Y, R, status, s)
                : launch_i8<kQ4_0, false>(W, Wu, n, k, X, Y, R, status, s);

@@ -191,8 +191,11 @@ def quantize_iq4_xs(w: np.ndarray) -> np.ndarray:
     little-endian word at bytes 2-3, their low nibbles at nibble j % 2 of
     byte 4 + j / 2, the code of element 32 j + l (l < 16) in the low nibble
     of byte 8 + 16 j + l and that of 32 j + 16 + l in its high nibble."""
-    w = np.ascontiguousarray(w, dtype=np.float32).astype(np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float32)
     n, k = w.shape
+    if n > 1024:  # row blocks bound the float64 temporaries
+        return np.concatenate([quantize_iq4_xs(w[i:i + 1024]) for i in range(0, n, 1024)])
+    w = w.astype(np.float64)
     nsb = k // 256
     x = w.reshape(n, nsb, 8, 32)
     idx = np.abs(x).argmax(axis=-1)
@@ -204,7 +207,8 @@ def quantize_iq4_xs(w: np.ndarray) -> np.ndarray:
     ls = (s + 32).astype(np.int64)
     step = df[..., None] * s
     ratio = np.where(step[..., None] != 0, x / np.where(step != 0, step, 1.0)[..., None], 1.0)
-    code = np.abs(ratio[..., None] - _IQ4_BOOK).argmin(axis=-1).astype(np.int64)  # [n][nsb][8][32]
+    # the nearest entry (the lower one on a tie) by the midpoints of the sorted book
+    code = np.searchsorted((_IQ4_BOOK[1:] + _IQ4_BOOK[:-1]) / 2, ratio, side="left").astype(np.int64)
     out = np.zeros((n, nsb, 136), np.uint8)
     out[..., 0:2] = d16.view(np.uint16)[..., None].view(np.uint8).reshape(n, nsb, 2)
     hi = np.zeros((n, nsb), np.int64)

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(q):
 
 def test_header_constants_match_binding(q):
     text = open(HEADER).read()
-    for name in ["APR_F16", "APR_Q4_0", "APR_Q8_0", "APR_Q4_K", "APR_Q5_K", "APR_Q6_K", "APR_LEG_F16", "APR_LEG_EXACT_F32", "APR_PATH_AUTO", "APR_PATH_GEMV",
+    for name in ["APR_F16", "APR_Q4_0", "APR_Q8_0", "APR_Q4_K", "APR_Q5_K", "APR_Q6_K", "APR_IQ4_XS", "APR_LEG_F16", "APR_LEG_EXACT_F32", "APR_PATH_AUTO", "APR_PATH_GEMV",
                  "APR_PATH_GEMM", "APR_OK", "APR_E_INVAL", "APR_E_QTYPE", "APR_E_ALIGN", "APR_E_ALIAS",
                  "APR_E_DEVICE", "APR_E_LAUNCH", "APR_E_TIMEOUT", "APR_E_NOMEM"]:
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
@@ -84,6 +84,9 @@ def call(q, *args):
     ((14, A, 64, 1024, 2 * A, 8, 3 * A, None, None), -1, "2048"),  # Q6_K rows on 16-byte boundaries
     # a Q6_K weight spans 210 bytes per 256 weights: 64 x 2048 -> 107520 bytes from A
     ((14, A, 64, 2048, 2 * A, 8, A + 107520 - 16, None, None), -4, "W"),
+    ((23, A, 64, 256, 2 * A, 8, 3 * A, None, None), -1, "512"),  # IQ4_XS rows on 16-byte boundaries
+    # an IQ4_XS weight spans 136 bytes per 256 weights: 64 x 512 -> 17408 bytes from A
+    ((23, A, 64, 512, 2 * A, 8, A + 17408 - 16, None, None), -4, "W"),
     # an F16 weight spans 2 bytes a weight: 64 x 64 -> 8192 bytes from A
     ((1, A, 64, 64, 2 * A, 8, A + 8192 - 16, None, None), -4, "W"),
     ((2, A, (1 << 24) + 1, 64, 2 * A, 8, 3 * A, None, None), -1, "limits"),

@@ -1,12 +1,14 @@
-"""GPU parity of the K-quant weights on every route, against the float64
-oracle: Q4_K and Q5_K (256-element superblocks: fp16 d and dmin, 6-bit
-sub-block scales and mins, 4-bit codes, and for Q5_K a fifth code bit per
-element) and Q6_K (6-bit codes, an int8 scale per 16 elements, fp16 d; rows
-take k % 2048 == 0); the layouts are those read in the oracle.
+"""GPU parity of the 256-element superblock weights on every route, against
+the float64 oracle: Q4_K and Q5_K (fp16 d and dmin, 6-bit sub-block scales
+and mins, 4-bit codes, and for Q5_K a fifth code bit per element), Q6_K
+(6-bit codes, an int8 scale per 16 elements, fp16 d; rows take k % 2048 ==
+0) and IQ4_XS (fp16 d, 6-bit scales per 32 elements, 4-bit codes standing for
+the entries of a 16-value code book; rows take k % 512 == 0); the layouts are
+those read in the oracle.
 
 Bars:
 * dequant: bit exact (d sc q - dmin m rounded once to f32 on both sides;
-  Q6_K's d sc (q - 32) is exact);
+  Q6_K's d sc (q - 32) and IQ4_XS's d (ls - 32) book[c] are exact);
 * fp16 leg: against the oracle fed fp16-rounded X and weights, each element
   within 3e-5 of the sum of its terms' magnitudes, and the whole output within
   the fp16-leg bar against the float64 oracle (the kernel rounds the fp32 value
@@ -30,14 +32,16 @@ pytestmark = pytest.mark.gpu
 
 
 
-@pytest.fixture(params=[synth.Q4_K, synth.Q5_K, synth.Q6_K], ids=["q4_k", "q5_k", "q6_k"])
+@pytest.fixture(params=[synth.Q4_K, synth.Q5_K, synth.Q6_K, synth.IQ4_XS], ids=["q4_k", "q5_k", "q6_k", "iq4_xs"])
 def qk(request):
     return request.param
 
 
 def _k(qk, k):
-    """k as given, or for Q6_K raised to a multiple of 2048."""
-    return max(2048, -(-k // 2048) * 2048) if qk == synth.Q6_K else k
+    """k as given, or raised to a multiple of the format's row unit (Q6_K
+    2048, IQ4_XS 512)."""
+    unit = {synth.Q6_K: 2048, synth.IQ4_XS: 512}.get(qk, 256)
+    return max(unit, -(-k // unit) * unit)
 
 CLASSES = ["subnormal", "small", "typical", "large", "mixed"]
 
@@ -118,6 +122,19 @@ def test_dequant_hand_superblocks(q, qk):
         got = out.cpu().numpy()
         np.testing.assert_array_equal(got[0], np.tile(np.repeat(np.array(sc, np.float32), 16), 8))
         np.testing.assert_array_equal(got[1], np.tile(np.array([e % 64 - 32 for e in range(256)], np.float32), 8))
+        return
+    if qk == synth.IQ4_XS:  # row 0: the scales on their sub-blocks (code 8: book 1); row 1: the book in order
+        ls = [0, 63, 32, 33, 17, 48, 31, 1]
+        W = np.frombuffer(pins._iq4_xs_superblock(0x3C00, ls, [8] * 256) * 2 +
+                          pins._iq4_xs_superblock(0x3C00, [33] * 8, [e % 16 for e in range(256)]) * 2,
+                          np.uint8).reshape(2, 2 * 136).copy()
+        out = torch.empty((2, 512), device="cuda")
+        q.apr_dequant(qk, dev(W), 2, 512, out)
+        q.apr_stream_status()
+        got = out.cpu().numpy()
+        book = np.array(oracle.IQ4_NL_VALUES, np.float32)
+        np.testing.assert_array_equal(got[0], np.tile(np.repeat(np.array(ls, np.float32) - 32, 32), 2))
+        np.testing.assert_array_equal(got[1], np.tile(book[np.arange(256) % 16], 2))
         return
     five = qk == synth.Q5_K
     build, qmax, sbb = (pins._q5_k_superblock, 32, 176) if five else (pins._q4_k_superblock, 16, 144)
