@@ -33,8 +33,9 @@ inline size_t row_bytes_of(int qtype, int k) {
 // formats of one scale and 32 codes per 32-element block (the block-GEMV kernels)
 inline bool block32_format(int qtype) { return qtype == kQ4_0 || qtype == kQ8_0; }
 
-// Epilogue of a projection.
-enum Epilogue { kEpiPlain = 0, kEpiResidual = 1, kEpiSwiGLU = 2 };
+// Epilogue of a projection. kEpiGluPair: gate/up SwiGLU computed by a
+// cluster pair of CTAs, one per weight (gemm_tc.cu).
+enum Epilogue { kEpiPlain = 0, kEpiResidual = 1, kEpiSwiGLU = 2, kEpiGluPair = 3 };
 
 // Standalone dequant (dequant.cu).
 cudaError_t launch_dequant(int qtype, const void* W, int n, int k, float* out, cudaStream_t s);
@@ -112,6 +113,7 @@ cudaError_t launch_x_to_f16(const float* X, uint16_t* X16, size_t count, cudaStr
 struct GemmPlan {
   int bn = 128;
   int nsplit = 1;
+  bool pair = false;  // gate/up: a cluster pair of CTAs per 256-token tile, one weight each
 };
 GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu);
 

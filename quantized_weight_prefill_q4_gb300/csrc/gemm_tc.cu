@@ -55,6 +55,12 @@
 // in split order, so the result does not depend on which CTA finishes first.
 // A cluster barrier at the end keeps both CTAs resident until neither touches
 // the other's shared memory.
+// Gate/up as a pair (kEpiGluPair, 256-token tiles): the same cluster of two,
+// but CTA z streams and decodes one weight over the whole of k (z = 0 the
+// gate, z = 1 the up weight) into its own accumulator, so that each decoded
+// weight serves 256 tokens (a single CTA holding both accumulators has TMEM
+// for 128 tokens only). The halves are exchanged as above and CTA z computes
+// silu(gate) * up for token columns [128 z, 128 z + 128).
 // Exact leg (XS): the pages' f32 leg (fp32 products, no reduced-precision
 // input) on the same skeleton; see the comment above Cfg.
 // Every mbarrier wait is bounded (2 s); a wait that gives up sets the device
@@ -506,10 +512,14 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
   const int lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * BM;
   const int t0 = blockIdx.y * BN;
-  // split-K: CTA z of gridDim.z takes raw chunks [c0, c1); ring indices are local
+  // split-K: CTA z of gridDim.z takes raw chunks [c0, c1); ring indices are
+  // local. A gate/up pair: CTA z takes all of k for weight z.
+  constexpr bool pair = EPI == kEpiGluPair;
   const int nchunks_all = k / CHUNK;
   const int nsplit = gridDim.z, z = blockIdx.z;
-  const int c0 = (int)((long)z * nchunks_all / nsplit), c1 = (int)((long)(z + 1) * nchunks_all / nsplit);
+  const int c0 = pair ? 0 : (int)((long)z * nchunks_all / nsplit);
+  const int c1 = pair ? nchunks_all : (int)((long)(z + 1) * nchunks_all / nsplit);
+  const CUtensorMap* wmap0 = pair && z ? &tmWu : &tmW;  // the weight of m = 0
   // k split: a cluster pair that exchanges halves (two splits), or, with bit
   // 5 of `early`, independent splits each writing its own partial output (Y +
   // z T ldy), added by a second kernel
@@ -561,7 +571,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------ raw weight producer
     if (lane == 0) {
-      tma_prefetch_desc(&tmW);
+      tma_prefetch_desc(wmap0);
       if (C::NM == 2) tma_prefetch_desc(&tmWu);
       // x of box b of raw slot u (16-bit elements): the raw row bytes of block
       // formats, the k index itself for F16
@@ -574,7 +584,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
       for (int u = 0; u < PF && u < nunits; ++u)
         for (int m = 0; m < C::NM; ++m)
           for (int b = 0; b < C::RAW_LOADS; ++b)
-            tma_prefetch_l2_2d(m ? (const void*)&tmWu : (const void*)&tmW, raw_x(u, b), m0);
+            tma_prefetch_l2_2d(m ? (const void*)&tmWu : (const void*)wmap0, raw_x(u, b), m0);
       if ((early & 15) == kEarlyNone) grid_dependency_wait();
       int last_issued[C::S_RAW];
       for (int i = 0; i < C::S_RAW; ++i) last_issued[i] = -1;
@@ -585,7 +595,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
           const int slot = j % C::S_RAW;
           ok = mbar_wait(&rawEmpty[slot], ((j / C::S_RAW) & 1) ^ 1, abort_flag, status);
           if (!ok) break;
-          const void* map = m ? (const void*)&tmWu : (const void*)&tmW;
+          const void* map = m ? (const void*)&tmWu : (const void*)wmap0;
           mbar_arrive_expect_tx(&rawFull[slot], C::RAW_BYTES);
           for (int b = 0; b < C::RAW_LOADS; ++b)
             tma_load_2d(sRaw + slot * C::RAW_BYTES + b * (C::RAW_BYTES / C::RAW_LOADS), map, raw_x(u, b), m0,
@@ -914,13 +924,18 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
           v[j] = __float_as_uint(gt / (1.0f + expf(-gt)) * __uint_as_float(u[j]));
         }
       }
-      if (clus) {  // p0 + p1, in split order
+      if (clus) {  // p0 + p1, in split order; a gate/up pair: silu(gate) * up
         const float* src = reinterpret_cast<const float*>(sRaw + wg * PIECE_BYTES) + r;
 #pragma unroll
         for (int j = 0; j < PIECE; ++j) {
           const float o = src[j * BM];
           const float mine = __uint_as_float(v[j]);
-          v[j] = __float_as_uint(z == 0 ? mine + o : o + mine);
+          if constexpr (pair) {
+            const float gt = z == 0 ? mine : o, up = z == 0 ? o : mine;
+            v[j] = __float_as_uint(gt / (1.0f + expf(-gt)) * up);
+          } else {
+            v[j] = __float_as_uint(z == 0 ? mine + o : o + mine);
+          }
         }
       }
       if constexpr (XS) {
@@ -933,7 +948,7 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
           v[j] = __float_as_uint(__uint_as_float(v[j]) * sr * stk);
         }
       }
-      if constexpr (EPI == kEpiSwiGLU) {
+      if constexpr (EPI == kEpiSwiGLU || pair) {
         if (row < n && (early & kOutF16)) {
           // fp16 output, the next GEMM's operand (Y holds uint16, ldy in them)
           uint16_t* Y16 = reinterpret_cast<uint16_t*>(Y);
@@ -1036,7 +1051,7 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
   if (!make_map_2d(fn, &mW, CU_TENSOR_MAP_DATA_TYPE_UINT16, W, row_bytes / 2, (uint64_t)n, row_bytes, C::RAW_BOX,
                    BM, wswz, msg, msg_len))
     return -1;
-  if (C::NM == 2) {
+  if (C::NM == 2 || EPI == kEpiGluPair) {
     if (!make_map_2d(fn, &mWu, CU_TENSOR_MAP_DATA_TYPE_UINT16, Wu, row_bytes / 2, (uint64_t)n, row_bytes, C::RAW_BOX,
                      BM, wswz, msg, msg_len))
       return -1;
@@ -1084,7 +1099,7 @@ int launch_cfg(const void* W, const void* Wu, int n, int k, const uint16_t* X16,
   cfg.stream = s;
   cudaLaunchAttribute attr[2] = {pdl_attr(), pdl_attr()};
   cfg.numAttrs = 1;
-  if (nsplit == 2 && !(early & 32)) {  // the two k halves of a tile form a cluster
+  if (nsplit == 2 && !(early & 32)) {  // the two k halves (or gate/up CTAs) of a tile form a cluster
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = 1;
     attr[1].val.clusterDim.y = 1;
@@ -1107,6 +1122,10 @@ template <int QT>
 int launch_q(const GemmPlan& pl, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y,
              int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int w, int xr,
              const OutRegions& reg) {
+  if constexpr (QT != kF16) {
+    if (Wu && pl.pair)
+      return launch_cfg<QT, kEpiGluPair, 256>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 2, w, xr);
+  }
   if (Wu) return launch_cfg<QT, kEpiSwiGLU, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w, xr);
   if constexpr (QT == kF16) {
     // an F16 raw slot is four times a Q4_0 one: 256-token tiles do not fit
@@ -1414,7 +1433,13 @@ cudaError_t launch_x_to_f16(const float* X, uint16_t* X16, size_t count, cudaStr
 
 GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu) {
   GemmPlan pl;
-  if (swiglu) return pl;  // 128-token tiles, two accumulators fill TMEM
+  if (swiglu) {
+    // a CTA pair per 256-token tile (one weight each) once a tile's second
+    // half holds tokens; else one CTA per 128-token tile with both weights
+    // (F16 weights always: their raw slots leave no room for 256-token tiles)
+    pl.pair = T > 128;
+    return pl;
+  }
   const int sms = num_sms();
   const long tiles256 = (long)((n + BM - 1) / BM) * ((T + 255) / 256);
   // 256-token tiles halve the MMA instructions per flop: taken when they
