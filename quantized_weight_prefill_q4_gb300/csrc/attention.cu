@@ -17,7 +17,14 @@
 // that TMA copies straight into the 128-byte-swizzled MMA layout.
 //
 // One CTA per (128 query rows, query head); the CTAs of the last query rows,
-// which see the most keys, are launched first. Keys go in tiles of 64. The
+// which see the most keys, are launched first. When that grid would leave
+// SMs idle, each query tile's key tiles are cut into parts of at most P
+// tiles (P the smallest that keeps the grid within one CTA per SM) and every
+// part gets its own CTA: a CTA of a cut tile writes its unnormalized O, its
+// reference max and its sum into the stream's scratch, and a second kernel
+// combines the parts of each row, O = sum_s 2^(m_s - m) O_s / sum_s 2^(m_s -
+// m) l_s (m the largest m_s of the parts the row sees keys in), in part
+// order. Keys go in tiles of 64. The
 // roles hand work to each other through mbarriers, so that the tensor cores
 // compute the scores of tile j + 1 while the softmax of tile j runs:
 //   warps 0-3   own the 128 query rows (one row per thread, TMEM lane = row):
@@ -161,10 +168,68 @@ __global__ void __launch_bounds__(256) kv_to_f16_kernel(const float* __restrict_
   }
 }
 
+// key tiles seen by the rows of query tile qt
+__host__ __device__ inline int attn_key_tiles(int qt, int T, int pos0) {
+  const int last = (qt + 1) * AQ < T ? (qt + 1) * AQ : T;
+  return (pos0 + last + AKEY - 1) / AKEY;
+}
+
+// The parts of the cut query tiles into O: a thread per 4 dims of a row,
+// 32 CTAs of 256 per (query tile, head) (every load of a thread issued at
+// once; the threads of a row read its parts' (m, l) through the same cache
+// lines). Rows past T are not written, and the query tiles of one part were
+// written by the attention kernel itself.
+__global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ part_o,
+                                                           const float2* __restrict__ part_ml, void* O, int T,
+                                                           int pos0, int num_heads, int P, int o16) {
+  constexpr int PER_TILE = AQ * (AD / 4) / 256;  // CTAs per (query tile, head)
+  const int nqt = (T + AQ - 1) / AQ;
+  const int th = (int)(blockIdx.x / PER_TILE), qt = th / num_heads, h = th % num_heads;
+  const int i = (int)(blockIdx.x % PER_TILE) * 256 + (int)threadIdx.x;
+  const int r = i / (AD / 4), d4 = i % (AD / 4), t = qt * AQ + r;
+  const int ns = (attn_key_tiles(qt, T, pos0) + P - 1) / P;
+  if (ns == 1 || t >= T) return;
+  int unit = 0;  // the first unit of this query tile (later tiles' parts come first)
+  for (int q2 = nqt - 1; q2 > qt; --q2) unit += (attn_key_tiles(q2, T, pos0) + P - 1) / P;
+  const size_t slot0 = (size_t)unit * num_heads + h, sstep = (size_t)num_heads;
+  float m = -INFINITY;
+  for (int s = 0; s < ns; ++s) {
+    const float2 ml = part_ml[(slot0 + s * sstep) * AQ + r];
+    if (ml.y > 0.f) m = fmaxf(m, ml.x);
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const size_t slot = slot0 + s * sstep;
+    const float2 ml = part_ml[slot * AQ + r];
+    if (!(ml.y > 0.f)) continue;  // the row sees no key of this part
+    const float w = exp2f(ml.x - m);
+    const float4 o = reinterpret_cast<const float4*>(part_o + (slot * AQ + r) * AD)[d4];
+    acc.x = fmaf(w, o.x, acc.x);
+    acc.y = fmaf(w, o.y, acc.y);
+    acc.z = fmaf(w, o.z, acc.z);
+    acc.w = fmaf(w, o.w, acc.w);
+    L = fmaf(w, ml.y, L);
+  }
+  const float inv = 1.0f / L;
+  const size_t at = (size_t)t * ((size_t)num_heads * AD) + (size_t)h * AD + 4 * d4;
+  if (o16) {
+    const __half2 a = __floats2half2_rn(acc.x * inv, acc.y * inv), b = __floats2half2_rn(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(O) + at) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(O) + at) =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  }
+}
+
 __global__ void __launch_bounds__(A_THREADS, 1)
     prefill_attention_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                             const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO, int T,
-                             int pos0, int num_heads, int num_kv_heads, unsigned* status, int o16) {
+                             const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmO,
+                             const __grid_constant__ CUtensorMap tmP, int T, int pos0, int num_heads,
+                             int num_kv_heads, unsigned* status, int o16, int P, float2* __restrict__ part_ml) {
+  // P > 0: key tiles in parts of at most P (see above); CTA b's unnormalized
+  // O goes to rows 128 b .. of tmP, its (m, l) per row to part_ml[128 b + r]
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sK = smem + OFF_K;
@@ -187,10 +252,25 @@ __global__ void __launch_bounds__(A_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqt = (T + AQ - 1) / AQ;
   const int h = blockIdx.x % num_heads;
-  const int t0 = (nqt - 1 - (int)(blockIdx.x / num_heads)) * AQ;
+  // the query tile, and with parts which part: units of num_heads CTAs, the
+  // last query tile's parts first
+  int qt = nqt - 1 - (int)(blockIdx.x / num_heads), part = 0, nparts = 1;
+  if (P > 0) {
+    int u = (int)(blockIdx.x / num_heads);
+    for (qt = nqt - 1; qt > 0; --qt) {
+      const int ns = (attn_key_tiles(qt, T, pos0) + P - 1) / P;
+      if (u < ns) break;
+      u -= ns;
+    }
+    nparts = (attn_key_tiles(qt, T, pos0) + P - 1) / P;
+    part = u;
+  }
+  const int t0 = qt * AQ;
   const int g = h / (num_heads / num_kv_heads);
-  const int nkeys = pos0 + min(t0 + AQ, T);      // keys this CTA's rows see
-  const int nkt = (nkeys + AKEY - 1) / AKEY;
+  const int nkt_all = attn_key_tiles(qt, T, pos0);   // key tiles this CTA's rows see
+  const int kt0 = part * nkt_all / nparts;          // this CTA's key tiles kt0 .. kt0 + nkt - 1
+  const int nkt = (part + 1) * nkt_all / nparts - kt0;
+  const bool partial = nparts > 1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 3; ++i) {
@@ -226,13 +306,13 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     mbar_arrive_expect_tx(&kFull[b], K_BYTES);
 #pragma unroll
     for (int p = 0; p < AD / 64; ++p)
-      tma_load_2d(sK + b * K_BYTES + p * K_PANEL, &tmK, g * AD + 64 * p, ti * AKEY, &kFull[b]);
+      tma_load_2d(sK + b * K_BYTES + p * K_PANEL, &tmK, g * AD + 64 * p, (kt0 + ti) * AKEY, &kFull[b]);
     last_k = ti;
   };
   auto send_v = [&](int ti) {
     const int b = ti % VBUF;
     mbar_arrive_expect_tx(&vFull[b], V_BYTES);
-    tma_load_2d(sV + b * V_BYTES, &tmV, ti * AKEY, g * AD, &vFull[b]);
+    tma_load_2d(sV + b * V_BYTES, &tmV, (kt0 + ti) * AKEY, g * AD, &vFull[b]);
     last_v = ti;
   };
 
@@ -384,7 +464,7 @@ __global__ void __launch_bounds__(A_THREADS, 1)
       tmem_ld_32x32b_x32(lane_addr + COL_S + AKEY * (j & 1) + 32, sv + 32);
       tmem_ld_wait_regs(sv);
       regs_after_wait(sv + 32);
-      const int kb = j * AKEY;
+      const int kb = (kt0 + j) * AKEY;
       float s[64];
       if (kb + AKEY - 1 <= plim) {   // every key of the tile visible to this row
 #pragma unroll
@@ -398,7 +478,10 @@ __global__ void __launch_bounds__(A_THREADS, 1)
       for (int c = 4; c < 64; ++c) mq[c & 3] = fmaxf(mq[c & 3], s[c]);
       const float m_new = fmaxf(m_run, fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])));
       if (j == 0) {
-        m_ref = m_new;   // key 0 is visible to every row: finite
+        // the first key of the CTA's range is visible to every row that sees
+        // any key of it (visibility is a prefix of the keys); a row that sees
+        // none keeps weights of 0 and a sum of 0, which the combination skips
+        m_ref = m_new == -INFINITY ? 0.f : m_new;
       } else if (__any_sync(0xffffffffu, m_new > m_ref + kRescaleAbove)) {
         // the whole warp moves its reference (tensor-memory access is per
         // warp), once O += P_{j-1} . V_{j-1} is done (S_j's completion already
@@ -456,8 +539,10 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(oLast, 0, abort_flag, status));
     if (ok) {
       tc_fence_after();
-      const float inv = 1.0f / l;
-      if (o16) {
+      // a part: O as accumulated, with the row's reference max and sum
+      const float inv = partial ? 1.0f : 1.0f / l;
+      if (partial) part_ml[(size_t)blockIdx.x * AQ + r] = make_float2(m_ref, l);
+      if (o16 && !partial) {
         // fp16 O: boxes of 64 dims (128 bytes a row), the same swizzle
 #pragma unroll 1
         for (int cb = 0; cb < AD / 64; ++cb) {
@@ -497,10 +582,14 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     }
     named_sync(1, 32 * SOFT_WARPS);
     if (threadIdx.x == 0 && ok) {
-      const int dims = o16 ? 64 : 32;  // dims a box
+      const int dims = o16 && !partial ? 64 : 32;  // dims a box
 #pragma unroll 1
-      for (int cb = 0; cb < AD / dims; ++cb)
-        tma_store_2d(&tmO, smem + OFF_OST + cb * QBOX_BYTES, h * AD + dims * cb, t0);
+      for (int cb = 0; cb < AD / dims; ++cb) {
+        if (partial)
+          tma_store_2d(&tmP, smem + OFF_OST + cb * QBOX_BYTES, dims * cb, (int)blockIdx.x * AQ);
+        else
+          tma_store_2d(&tmO, smem + OFF_OST + cb * QBOX_BYTES, h * AD + dims * cb, t0);
+      }
       bulk_commit_group();
       bulk_wait_read_all();   // the boxes are read before the CTA's shared memory goes
     }
@@ -513,10 +602,36 @@ __global__ void __launch_bounds__(A_THREADS, 1)
 
 }  // namespace
 
+// The key-tile part size P: 0 (no parts) when the plain grid already fills
+// the SMs or parts would shorten the longest CTA by fewer than 12 key tiles;
+// else the smallest P whose grid fits one CTA per SM. Measured on GB300
+// (16 / 4 heads): a CTA costs about 7 us besides about 1.1 us a key tile, and
+// the parts about 9 us more in all (the combining launch, the partial sums'
+// traffic, more CTAs' fixed costs): 512 rows at position 0 (the longest CTA
+// 8 tiles, parts of 3) took 21.4 us against 17.9 us whole, 512 rows at 1536
+// (32 tiles, parts of 15) 35.2 us against about 44.7.
+static int attn_parts(int T, int pos0, int num_heads) {
+  const int nqt = (T + AQ - 1) / AQ, sms = num_sms();
+  if ((long long)nqt * num_heads >= sms) return 0;
+  const int most = attn_key_tiles(nqt - 1, T, pos0);
+  for (int P = 1; P + 12 <= most; ++P) {
+    long long units = 0;
+    for (int qt = 0; qt < nqt; ++qt) units += (attn_key_tiles(qt, T, pos0) + P - 1) / P;
+    if (units * num_heads <= sms) return P;
+  }
+  return 0;
+}
+
+// scratch: K16, then VT16, then (parts) one CTA per SM at most of partial O
+// [128 rows][256] fp32 and (m, l) per row
+static size_t attn_part_offset(size_t rows, size_t kv_dim) {
+  const size_t ldv = (rows + 15) & ~(size_t)15;
+  return ((rows * kv_dim * 2 + 255) & ~(size_t)255) + ((kv_dim * ldv * 2 + 255) & ~(size_t)255);
+}
+
 size_t prefill_attention_scratch_bytes(int T, int pos0, int num_kv_heads) {
   const size_t rows = (size_t)pos0 + (size_t)T, kv_dim = (size_t)num_kv_heads * AD;
-  const size_t ldv = (rows + 15) & ~(size_t)15;
-  return ((rows * kv_dim * 2 + 255) & ~(size_t)255) + kv_dim * ldv * 2;
+  return attn_part_offset(rows, kv_dim) + (size_t)num_sms() * AQ * (AD * 4 + 8);
 }
 
 int launch_prefill_attention(const float* Q, const float* K, const float* V, float* O, int T, int pos0,
@@ -527,6 +642,9 @@ int launch_prefill_attention(const float* Q, const float* K, const float* V, flo
   const size_t ldv = (rows + 15) & ~(size_t)15;
   uint16_t* K16 = static_cast<uint16_t*>(scratch);
   uint16_t* VT16 = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(scratch) + ((rows * kv_dim * 2 + 255) & ~(size_t)255));
+  const int P = attn_parts(T, pos0, num_heads);
+  float* part_o = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + attn_part_offset(rows, kv_dim));
+  float2* part_ml = reinterpret_cast<float2*>(part_o + (size_t)num_sms() * AQ * AD);
   auto cuda_fail = [&](cudaError_t e, const char* what) {
     snprintf(msg, msg_len, "%s: %s", what, cudaGetErrorString(e));
     return -1;
@@ -561,6 +679,12 @@ int launch_prefill_attention(const float* Q, const float* K, const float* V, flo
                           CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len)))
     return -1;
 
+  // the parts' O: [one CTA per SM x 128 rows][256] fp32, the boxes of O's fp32 form
+  CUtensorMap mP = mO;
+  if (P > 0 && !make_map_2d(fn, &mP, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, part_o, AD, (uint64_t)num_sms() * AQ, AD * 4,
+                            32, AQ, CU_TENSOR_MAP_SWIZZLE_128B, msg, msg_len))
+    return -1;
+
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -569,7 +693,12 @@ int launch_prefill_attention(const float* Q, const float* K, const float* V, flo
     if (e != cudaSuccess) return cuda_fail(e, "prefill attention attributes");
     attr_set[dev] = 1;
   }
-  const long long grid = (long long)((T + AQ - 1) / AQ) * num_heads;
+  long long grid = (long long)((T + AQ - 1) / AQ) * num_heads;
+  if (P > 0) {
+    long long units = 0;
+    for (int qt = 0; qt < (T + AQ - 1) / AQ; ++qt) units += (attn_key_tiles(qt, T, pos0) + P - 1) / P;
+    grid = units * num_heads;  // at most one CTA per SM (attn_parts)
+  }
   // launched programmatically: its CTAs start (Q on its way) while the
   // conversion finishes; the K and V producers wait for it
   cudaLaunchConfig_t cfg = {};
@@ -580,10 +709,17 @@ int launch_prefill_attention(const float* Q, const float* K, const float* V, flo
   cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, prefill_attention_kernel, mK, mV, mQ, mO, T, pos0, num_heads, num_kv_heads, status,
-                         o16 ? 1 : 0);
+  e = cudaLaunchKernelEx(&cfg, prefill_attention_kernel, mK, mV, mQ, mO, mP, T, pos0, num_heads, num_kv_heads, status,
+                         o16 ? 1 : 0, P, part_ml);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prefill attention");
+  if (P > 0) {
+    // plain stream order: the parts are complete when it starts
+    const unsigned cblocks = (unsigned)((T + AQ - 1) / AQ * num_heads * (AQ * (AD / 4) / 256));
+    attn_combine_kernel<<<cblocks, 256, 0, s>>>(part_o, part_ml, O, T, pos0, num_heads, P, o16 ? 1 : 0);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "prefill attention parts");
+  }
   return 0;
 }
 

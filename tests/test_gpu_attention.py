@@ -12,8 +12,11 @@ the softmax weights rounded to fp16 for the value product, fp32 accumulation):
   most 2^-11 of itself, which moves a weighted mean of values by at most
   2 * 2^-11 * max|v|; the fp32 sums add far less.
 Bit for bit where the definition makes the result exact: the first position
-(one visible key, weight exactly 1) gives fp16(v_0); splitting a chunk into
-two calls changes no row.
+(one visible key, weight exactly 1) gives fp16(v_0), also when the call cuts
+the query tiles' key ranges into parts; splitting a chunk into two calls
+changes no row when neither call cuts key ranges (with parts, a row's sums
+are grouped by the call's shape: equal within the bars above, not bit for
+bit).
 """
 
 import numpy as np
@@ -69,12 +72,16 @@ def test_attention_matches_oracle(q, T, pos0, nh, nkv):
     assert_attention(run(q, c), c)
 
 
-def test_first_position_takes_its_own_value_exactly(q):
-    c = synth.attention_case(4, 0, 4, 2, seed=21)
+@pytest.mark.parametrize("T,nh,nkv", [(4, 4, 2), (1024, 2, 1)])
+def test_first_position_takes_its_own_value_exactly(q, T, nh, nkv):
+    # 1024 rows over 2 heads: 16 CTAs, the longest over 16 key tiles, so the
+    # key tiles are cut into parts of one and row 0 goes through the
+    # combination (its other part sees no key)
+    c = synth.attention_case(T, 0, nh, nkv, seed=21)
     y = run(q, c)
     v16 = c["V"].astype(np.float16).astype(np.float32)
-    for h in range(4):
-        g = h // 2
+    for h in range(nh):
+        g = h // (nh // nkv)
         assert np.array_equal(y[0, h * D:(h + 1) * D], v16[0, g * D:(g + 1) * D]), h
 
 
@@ -102,10 +109,12 @@ def test_cache_rows_past_the_chunk_are_never_read(q):
     assert np.array_equal(run(q, c2), y)
 
 
-def test_rescale_of_the_running_sum(q):
+@pytest.mark.parametrize("pos0", [200, 1000])
+def test_rescale_of_the_running_sum(q, pos0):
     # one key per 64-key tile whose score grows by 6 (8.7 in base 2) from tile
-    # to tile: the reference max moves at every tile
-    T, pos0, nh, nkv = 256, 200, 2, 1
+    # to tile: the reference max moves at every tile (at pos0 = 1000 the key
+    # tiles are cut into parts whose maxima differ by as much)
+    T, nh, nkv = 256, 2, 1
     c = synth.attention_case(T, pos0, nh, nkv, seed=24)
     u = np.zeros(D, np.float32)
     u[0] = 1.0
@@ -116,8 +125,9 @@ def test_rescale_of_the_running_sum(q):
 
 
 def test_splitting_a_chunk_changes_no_row(q):
-    # rows 0..99 at pos0, then rows 100..299 at pos0 + 100, over the same cache
-    c = synth.attention_case(300, 40, 4, 2, seed=25)
+    # rows 0..99 at pos0, then rows 100..299 at pos0 + 100, over the same
+    # cache; 64 query heads, so that no call cuts its key ranges into parts
+    c = synth.attention_case(300, 40, 64, 4, seed=25)
     whole = run(q, c)
     a = run(q, c, Q=c["Q"][:100], T=100)
     b = run(q, c, Q=c["Q"][100:], T=200, pos0=140)
@@ -135,6 +145,16 @@ def test_empty_chunk_writes_nothing(q):
     q.apr_prefill_attention(z, z, z, out, 0, 5, 2, 1, D)
     q.apr_stream_status()
     assert bool((out == 7.0).all())
+
+
+def test_key_parts_of_a_late_chunk(q):
+    # the last 256 rows of a 2048-token prompt (pos0 = 1792): 32 CTAs of up to
+    # 32 key tiles become parts of a few tiles each, then combined
+    c = synth.attention_case(256, 1792, 16, 4, seed=28)
+    y = run(q, c)
+    rows = np.array([0, 1, 63, 64, 127, 128, 200, 255])
+    assert_attention(y[rows], c, rows=rows)
+    assert np.array_equal(run(q, c), y)
 
 
 @pytest.mark.parametrize("T", [512, 2048])
