@@ -384,11 +384,15 @@ int apr_ffn_sublayer(const apr_ffn_args* args);
  *              num_heads <= 65536, num_kv_heads <= 16383
  *   head_dim   256 (the only size the fused form takes)
  * q, k and v enter the products rounded to fp16; the result is within fp16
- * input rounding of the exact attention (the tests bound it). All pointers
+ * input rounding of the exact attention (the tests bound it). When its
+ * (128 query rows, head) tiles leave SMs idle and the longest sees many key
+ * tiles, the call cuts each tile's keys into parts whose softmax sums a
+ * second kernel combines; a row's result then depends on the call's shape at
+ * rounding level (within the same bound). All pointers
  * 16-byte aligned, caller owned. Scratch per stream as for apr_qgemm: the
  * fp16 copies of the cache rows 0 .. pos0 + T - 1 that the call makes, K as
  * it is and V transposed (4 * (pos0 + T) * num_kv_heads * 256 bytes, plus
- * padding). Errors: APR_E_INVAL for negative sizes, num_heads not a multiple
+ * padding), and the parts' sums (132 KB per SM). Errors: APR_E_INVAL for negative sizes, num_heads not a multiple
  * of num_kv_heads, head_dim != 256, sizes past 2^30 positions, or a null
  * pointer with T > 0; APR_E_ALIGN; APR_E_ALIAS if out overlaps Q or a cache;
  * APR_E_NOMEM; APR_E_DEVICE; APR_E_LAUNCH. Asynchronous on the stream; apr_stream_status reports a
