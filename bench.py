@@ -229,11 +229,12 @@ def run_reference(args):
 
 
 def kernel_hash() -> str:
-    """sha256 (16 hex) of the GEMM kernel's sources, to tie ncu counters to a kernel version."""
+    """sha256 (16 hex) of the GEMM kernel's sources (the file and the headers
+    its device code includes), to tie ncu counters to a kernel version."""
     import hashlib
 
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "dev_common.cuh"):
+    for f in ("gemm_tc.cu", "dev_common.cuh", "apr_internal.h", "iq4.cuh", "q4k.cuh"):
         with open(os.path.join(ROOT, "quantized_weight_prefill_q4_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
