@@ -242,11 +242,14 @@ def kernel_hash() -> str:
 
 def gemm_label(n, T, sms):
     """The tile plan the library picks for this shape (the rule documented with
-    plan_gemm_tc: 256-token tiles when they keep most SMs busy, else split over
-    k in two when the tiles fit one wave twice, else 128-token tiles)."""
-    tiles256 = ((n + 127) // 128) * ((T + 255) // 256)
+    plan_gemm_tc: 256-token tiles when they keep most SMs busy (192-token ones
+    when those need no more waves), else split over k in two when the tiles
+    fit one wave twice, else 128-token tiles)."""
+    rt = (n + 127) // 128
+    tiles256, tiles192 = rt * ((T + 255) // 256), rt * ((T + 191) // 192)
     if 10 * tiles256 >= 6 * sms:
-        plan = "256-token tiles"
+        w256, w192 = -(-tiles256 // sms), -(-tiles192 // sms)
+        plan = "192-token tiles" if T > 128 and w192 <= w256 else "256-token tiles"
     elif 2 * tiles256 <= sms:
         plan = "256-token tiles split over k by 2-CTA clusters"
     else:

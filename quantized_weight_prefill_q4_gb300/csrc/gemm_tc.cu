@@ -174,7 +174,7 @@ struct Cfg {
   static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(NM == 1 || S_RAW % 2 == 0, "gate/up: each raw slot keeps one weight");
   static_assert(USED_COLS <= 512, "TMEM budget");
-  static_assert(NPIECE % NWG == 0, "epilogue pieces per warpgroup");
+  static_assert(BN % PIECE == 0 && NPIECE >= NWG, "epilogue pieces (of 64 tokens) per warpgroup");
   static_assert(BN != 256 || S_RAW * RAW_BYTES >= 2 * PIECE_BYTES, "split: the raw ring holds the partner's two pieces");
   static_assert(!XS || (BN == 128 && NM == 1), "the exact leg takes 128-token tiles of one weight");
 };
@@ -819,11 +819,11 @@ __global__ void __launch_bounds__(Cfg<QT, EPI, BN, XS>::NTHREADS, 1)
     // Y and R may still be in use by the preceding kernel
     grid_dependency_wait();
     const int row = m0 + (int)r;
-    constexpr int PPW = C::NPIECE / C::NWG;
-    const int npw = clus ? 1 : PPW;
+    // pieces wg, wg + NWG, ... (a 192-token tile: two for warpgroup 0, one for 1)
+    const int npw = clus ? 1 : (C::NPIECE - wg + C::NWG - 1) / C::NWG;
     // the pieces this warpgroup finalizes: all of the tile's pieces split
     // evenly, or with a split piece 2 z + wg
-    auto piece = [&](int pp) { return clus ? 2 * z + wg : wg * PPW + pp; };
+    auto piece = [&](int pp) { return clus ? 2 * z + wg : wg + pp * C::NWG; };
     // residual of piece p into registers (coalesced: the warp's lanes read 32
     // consecutive floats of one token's row)
     float rv[PIECE];
@@ -1136,6 +1136,10 @@ int launch_q(const GemmPlan& pl, const void* W, const void* Wu, int n, int k, co
                                                xr);
     return launch_cfg<QT, kEpiPlain, 256>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, pl.nsplit, w, xr,
                                           nullptr, nullptr, nullptr, reg);
+  } else if (pl.bn == 192) {
+    if (R) return launch_cfg<QT, kEpiResidual, 192>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w, xr);
+    return launch_cfg<QT, kEpiPlain, 192>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w, xr, nullptr,
+                                          nullptr, nullptr, reg);
   }
   if (R) return launch_cfg<QT, kEpiResidual, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w, xr);
   return launch_cfg<QT, kEpiPlain, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w, xr, nullptr,
@@ -1441,11 +1445,19 @@ GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu) {
     return pl;
   }
   const int sms = num_sms();
-  const long tiles256 = (long)((n + BM - 1) / BM) * ((T + 255) / 256);
+  const long rt = (n + BM - 1) / BM, tiles256 = rt * ((T + 255) / 256), tiles192 = rt * ((T + 191) / 192);
   // 256-token tiles halve the MMA instructions per flop: taken when they
-  // still keep most SMs busy, or, split over k in two, fit in one wave
+  // still keep most SMs busy, or, split over k in two, fit in one wave.
+  // 192-token tiles instead when they need no more waves: each does three
+  // quarters of the work and the SMs a 256-token grid leaves idle take the
+  // rest. Measured on GB300 (k = 4096, Q4_0 / Q4_K): 6144 rows at T = 512
+  // 24.5 / 31.2 us against 26.3 / 31.0 (96 tiles of 256 leave 56 SMs idle),
+  // 12288 rows at T = 512 45.4 / 57.7 us against 51.3 / 59.0; at T = 2048
+  // (7 waves of 192 against 6 of 256) 159.8 / 199.0 us against 154.9 / 178.6,
+  // so there they are not taken
   if (10 * tiles256 >= 6L * sms) {
-    pl.bn = 256;
+    const long w256 = (tiles256 + sms - 1) / sms, w192 = (tiles192 + sms - 1) / sms;
+    pl.bn = T > 128 && w192 <= w256 ? 192 : 256;
   } else if (2 * tiles256 <= sms && k / CHUNK >= 2) {
     pl.bn = 256;
     pl.nsplit = 2;

@@ -91,6 +91,14 @@ def test_layer_chunking_agrees(q):
     assert_f16_leg(b[0] - x0, a[0].astype(np.float64) - x0)
 
 
+def test_layer_qkv_on_192_token_tiles(q):
+    # 16 query heads over 4 KV heads (a 6144-row fused qkv weight) at 512
+    # rows: the qkv GEMM takes 192-token tiles and its epilogue sends the q,
+    # k and v rows to their places by row range
+    c = _case(synth.Q4_0, 512, 1024, 16, 4, 512, 0, seed=5)
+    _check(c, _run(q, c), 0)
+
+
 def test_layer_nine_b_shape(q):
     # hidden 4096, intermediate 12288, 16 query heads over 4 KV heads, 128 rows
     # after 64 cached positions

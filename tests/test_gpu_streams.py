@@ -73,3 +73,28 @@ def test_graph_captured_on_a_new_stream(q):
         assert_f16_leg(Yg.cpu().numpy(), ref_gemm)
         assert_exact_leg(Yv.cpu().numpy(), ref_gemv)
     q.apr_stream_status(s)
+
+
+@pytest.mark.parametrize("T", [1, 64])
+def test_weight_written_by_another_kernel_just_before_is_read_fresh(q, T):
+    # The library's kernels read their weights before the preceding kernel on
+    # the stream has finished only when that kernel is the library's own (it
+    # lets them launch early); a kernel of other code (here a torch XOR that
+    # turns weight A into weight B in place) always completes first, so the
+    # call sees B. T = 1 runs the one-token GEMV, T = 64 the tensor-core GEMM.
+    n, k = 1024, 2048
+    a = synth.make_case(synth.Q4_0, n, k, T, seed=31)
+    b = synth.make_case(synth.Q4_0, n, k, T, seed=32)
+    W = dev(a["W"])
+    flip = dev(np.bitwise_xor(a["W"], b["W"]))
+    X = dev(b["X"])
+    Y = torch.empty((T, n), device="cuda")
+    q.apr_qgemm(synth.Q4_0, W, n, k, X, T, Y)   # reads A
+    W.bitwise_xor_(flip)                         # A -> B on the same stream
+    q.apr_qgemm(synth.Q4_0, W, n, k, X, T, Y)   # must read B
+    q.apr_stream_status()
+    ref = oracle.qgemm_f64(synth.Q4_0, b["W"], n, k, b["X"])
+    if T == 1:
+        assert_exact_leg(Y.cpu().numpy(), ref)
+    else:
+        assert_f16_leg(Y.cpu().numpy(), ref)

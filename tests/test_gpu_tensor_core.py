@@ -239,3 +239,22 @@ def test_split_k_is_deterministic(q):
         outs.append(Y.cpu().numpy())
     np.testing.assert_array_equal(outs[0], outs[1])
     np.testing.assert_array_equal(outs[0], outs[2])
+
+
+# 192-token tiles: 6144 rows take them at T = 300, 400 and 512 (their waves
+# cost less than those of 256-token tiles, see plan_gemm_tc); ragged last
+# token tiles (300 = 192 + 108: two of its three
+# 64-token pieces hold tokens; 400 = 2 x 192 + 16: one), plain and residual
+# epilogues, a block format and a superblock format
+@pytest.mark.parametrize("qtype", [synth.Q4_0, synth.Q4_K])
+@pytest.mark.parametrize("T,res", [(300, True), (512, False), (400, True)])
+def test_192_token_tiles(q, qtype, T, res):
+    n, k = 6144, 512
+    c = synth.make_case(qtype, n, k, T, residual=res, seed=T + res)
+    buf, Y = guarded(T, n)
+    gemm(q, qtype, dev(c["W"]), n, k, dev(c["X"]), T, Y, R=dev(c["R"]) if res else None)
+    check_guards(buf, T, n)
+    y = Y.cpu().numpy()
+    assert_f16_leg(y, oracle.qgemm_f64(qtype, c["W"], n, k, c["X"], c["R"] if res else None))
+    rel, _, _ = errors(y, oracle.qgemm_f16_inputs_f64(qtype, c["W"], n, k, c["X"], c["R"] if res else None))
+    assert rel <= 2e-5, rel
