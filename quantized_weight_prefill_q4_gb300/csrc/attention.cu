@@ -183,6 +183,10 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
                                                            const float2* __restrict__ part_ml, void* O, int T,
                                                            int pos0, int num_heads, int P, int o16) {
   constexpr int PER_TILE = AQ * (AD / 4) / 256;  // CTAs per (query tile, head)
+  // launched programmatically behind the attention kernel: its parts are
+  // complete and visible after the wait
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
   const int nqt = (T + AQ - 1) / AQ;
   const int th = (int)(blockIdx.x / PER_TILE), qt = th / num_heads, h = th % num_heads;
   const int i = (int)(blockIdx.x % PER_TILE) * 256 + (int)threadIdx.x;
@@ -291,6 +295,10 @@ __global__ void __launch_bounds__(A_THREADS, 1)
     abort_flag[0] = 0;
     abort_flag[1] = 0;   // never set: the drain waits ignore the abort
     fence_mbar_init();
+    // the next kernel may launch (the parts' combination, or a GEMM that
+    // streams its weights on the SMs this grid leaves free); it reads this
+    // kernel's output only after its own dependency wait
+    grid_launch_dependents();
   }
   if (warp == 0) tmem_alloc(tmem_holder, A_TMEM_COLS);
   tc_fence_before();
@@ -714,10 +722,18 @@ int launch_prefill_attention(const float* Q, const float* K, const float* V, flo
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prefill attention");
   if (P > 0) {
-    // plain stream order: the parts are complete when it starts
-    const unsigned cblocks = (unsigned)((T + AQ - 1) / AQ * num_heads * (AQ * (AD / 4) / 256));
-    attn_combine_kernel<<<cblocks, 256, 0, s>>>(part_o, part_ml, O, T, pos0, num_heads, P, o16 ? 1 : 0);
-    e = cudaGetLastError();
+    // launched programmatically: its CTAs wait for the attention grid in
+    // griddepcontrol.wait
+    cudaLaunchConfig_t ccfg = {};
+    ccfg.gridDim = dim3((unsigned)((T + AQ - 1) / AQ * num_heads * (AQ * (AD / 4) / 256)));
+    ccfg.blockDim = dim3(256);
+    ccfg.stream = s;
+    cudaLaunchAttribute cattr[1] = {pdl_attr()};
+    ccfg.attrs = cattr;
+    ccfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&ccfg, attn_combine_kernel, (const float*)part_o, (const float2*)part_ml, (void*)O, T,
+                           pos0, num_heads, P, o16 ? 1 : 0);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "prefill attention parts");
   }
   return 0;
