@@ -619,9 +619,14 @@ def projection_rate(q, dev, stream, peak_tf, peak_gbs, *, qtype, n, k, T, residu
     flop = 2.0 * T * n * k * (2 if gate_up else 1)
     t_flop, t_byte = flop / (peak_tf * 1e12), byts / (peak_gbs * 1e9)
     del sets
-    return {"us": dt * 1e6, "TFLOP/s": flop / dt / 1e12, "GB/s": byts / dt / 1e9,
-            "frac_tensor": t_flop / dt, "frac_hbm": t_byte / dt,
-            "bound": "tensor" if t_flop >= t_byte else "hbm", "frac_roofline": max(t_flop, t_byte) / dt}
+    out = {"us": dt * 1e6, "TFLOP/s": flop / dt / 1e12, "GB/s": byts / dt / 1e9,
+           "frac_tensor": t_flop / dt, "frac_hbm": t_byte / dt,
+           "bound": "tensor" if t_flop >= t_byte else "hbm", "frac_roofline": max(t_flop, t_byte) / dt}
+    if leg == 1:
+        # the exact leg against a TF32 tensor path's peak: the measured bf16
+        # peak times the nominal dense ratio 1.1 / 2.25 PFLOP/s
+        out["frac_tf32_peak"] = flop / dt / (peak_tf * 1e12 * 1.1 / 2.25)
+    return out
 
 
 def every_workload(q, dev, stream, peak_tf, peak_gbs):
