@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(ITHREADS, 2)
   uint32_t* xt = reinterpret_cast<uint32_t*>(smem + (size_t)ns * ISTAGE);  // X table, [nblk][XBW]
   const int rcap = i8_rcap(n, gridDim.x);
   float* part = reinterpret_cast<float*>(xt + (size_t)nblk * XBW);     // [row slot][NM][PW]
-  float* rres = part + (size_t)rcap * 2 * 8;                           // residual of the CTA's rows
+  float* rres = part + (((size_t)rcap * NM * PW + 1) & ~(size_t)1);    // residual of the CTA's rows
   uint64_t* bars = reinterpret_cast<uint64_t*>(rres + ((rcap + 1) & ~1));
   uint64_t* full = bars;
   uint64_t* empty = bars + INS_MAX;
@@ -502,8 +502,8 @@ __global__ void __launch_bounds__(ITHREADS, 2)
           // the warp's share of the row, added with the others' after the
           // last stage
           if (lane == 0) {
-            part[((rb + rr - r0) * NM + m) * 8 + wi] = a;
-            if (two) part[((rb + rr + RG - r0) * NM + m) * 8 + wi] = b;
+            part[((rb + rr - r0) * NM + m) * PW + wi] = a;
+            if (two) part[((rb + rr + RG - r0) * NM + m) * PW + wi] = b;
           }
         }
       }
@@ -519,7 +519,7 @@ __global__ void __launch_bounds__(ITHREADS, 2)
 #pragma unroll
       for (int m = 0; m < NM; ++m) {
         float v = 0.f;
-        for (int w2 = 0; w2 < PW; ++w2) v += part[(slot * NM + m) * 8 + w2];
+        for (int w2 = 0; w2 < PW; ++w2) v += part[(slot * NM + m) * PW + w2];
         acc[m] = v;
       }
       float y;
@@ -533,19 +533,37 @@ __global__ void __launch_bounds__(ITHREADS, 2)
 }
 
 // shared memory besides the ring, and the stages that fit beside it
-int i8_grid(int n) { return n < num_sms() ? n : num_sms(); }
-size_t i8_fixed_smem(int k, int n) {
-  const size_t rcap = (size_t)i8_rcap(n, i8_grid(n));
-  return 128 + (size_t)(k / 32) * XBW * 4 + rcap * 2 * 8 * 4 + ((rcap + 1) & ~(size_t)1) * 4 + 2 * INS_MAX * 8 + 16;
+// shared memory besides the ring (the X table, the row partials [rows][2
+// weights at most][warps a row], the residuals, the barriers) for a grid of
+// `grid` CTAs, and the stages that fit beside it
+size_t i8_fixed_smem(int k, int n, int grid) {
+  const size_t rcap = (size_t)i8_rcap(n, grid), pw = (size_t)((k / 64 + 31) / 32);
+  return 128 + (size_t)(k / 32) * XBW * 4 + ((rcap * 2 * pw + 1) & ~(size_t)1) * 4 + ((rcap + 1) & ~(size_t)1) * 4 +
+         2 * INS_MAX * 8 + 16;
 }
-int i8_stages(int k, int n) {
+int i8_stages_for(int k, int n, int grid) {
   // two CTAs an SM (228 KB of shared memory, 1 KB reserved per CTA) when 5
   // stages fit beside the X table, else one with as many as fit
-  const long half = 232448L / 2 - 1024 - (long)i8_fixed_smem(k, n);
+  const long half = 232448L / 2 - 1024 - (long)i8_fixed_smem(k, n, grid);
   if (half / ISTAGE >= 5) return 5;
-  const long ns = (232448L - (long)i8_fixed_smem(k, n)) / ISTAGE;
+  const long ns = (232448L - (long)i8_fixed_smem(k, n, grid)) / ISTAGE;
   return (int)(ns < INS_MAX ? ns : INS_MAX);
 }
+// One CTA an SM (half of one when it fits, so that the next launch's CTAs
+// start beside it), or, for weights of 128 rows a CTA and more in that form,
+// two half-SM CTAs an SM: twice the consumer warps to hide the latency of
+// the dot products' dependent chains, which bound such weights (measured on
+// GB300 with a 49152 x 4096 Q4_0 weight: 2 warps a scheduler issuing 45 % of
+// cycles, stalled mostly on fixed-latency dependencies, while the same
+// launch shape only streaming the bytes reaches the HBM rate).
+int i8_grid(int k, int n) {
+  const int sms = num_sms();
+  if (n < sms) return n;
+  if ((long)n >= 2L * sms * 128 && i8_stages_for(k, n, 2 * sms) == 5) return 2 * sms;
+  return sms;
+}
+int i8_stages(int k, int n) { return i8_stages_for(k, n, i8_grid(k, n)); }
+size_t i8_fixed_smem(int k, int n) { return i8_fixed_smem(k, n, i8_grid(k, n)); }
 size_t i8_smem(int k, int n) { return i8_fixed_smem(k, n) + (size_t)i8_stages(k, n) * ISTAGE; }
 
 template <int QT, bool SWI>
@@ -562,7 +580,7 @@ cudaError_t launch_i8(const void* W, const void* Wu, int n, int k, const float* 
     attr_set[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)i8_grid(n));
+  cfg.gridDim = dim3((unsigned)i8_grid(k, n));
   cfg.blockDim = dim3(ITHREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
