@@ -536,7 +536,7 @@ __global__ void __launch_bounds__(ITHREADS, 2)
 // shared memory besides the ring (the X table, the row partials [rows][2
 // weights at most][warps a row], the residuals, the barriers) for a grid of
 // `grid` CTAs, and the stages that fit beside it
-size_t i8_fixed_smem(int k, int n, int grid) {
+size_t i8_fixed_smem_grid(int k, int n, int grid) {
   const size_t rcap = (size_t)i8_rcap(n, grid), pw = (size_t)((k / 64 + 31) / 32);
   return 128 + (size_t)(k / 32) * XBW * 4 + ((rcap * 2 * pw + 1) & ~(size_t)1) * 4 + ((rcap + 1) & ~(size_t)1) * 4 +
          2 * INS_MAX * 8 + 16;
@@ -544,32 +544,39 @@ size_t i8_fixed_smem(int k, int n, int grid) {
 int i8_stages_for(int k, int n, int grid) {
   // two CTAs an SM (228 KB of shared memory, 1 KB reserved per CTA) when 5
   // stages fit beside the X table, else one with as many as fit
-  const long half = 232448L / 2 - 1024 - (long)i8_fixed_smem(k, n, grid);
+  const long half = 232448L / 2 - 1024 - (long)i8_fixed_smem_grid(k, n, grid);
   if (half / ISTAGE >= 5) return 5;
-  const long ns = (232448L - (long)i8_fixed_smem(k, n, grid)) / ISTAGE;
+  const long ns = (232448L - (long)i8_fixed_smem_grid(k, n, grid)) / ISTAGE;
   return (int)(ns < INS_MAX ? ns : INS_MAX);
 }
 // One CTA an SM (half of one when it fits, so that the next launch's CTAs
-// start beside it), or, for weights of 128 rows a CTA and more in that form,
-// two half-SM CTAs an SM: twice the consumer warps to hide the latency of
-// the dot products' dependent chains, which bound such weights (measured on
-// GB300 with a 49152 x 4096 Q4_0 weight: 2 warps a scheduler issuing 45 % of
-// cycles, stalled mostly on fixed-latency dependencies, while the same
-// launch shape only streaming the bytes reaches the HBM rate).
-int i8_grid(int k, int n) {
+// start beside it), or, for weights of 16 MiB and more when the half-SM form
+// fits them, two half-SM CTAs an SM: twice the consumer warps to hide the
+// latency of the dot products' dependent chains, which bound larger weights
+// (measured on GB300 with a 49152 x 4096 Q4_0 weight: 2 warps a scheduler
+// issuing 45 % of cycles, stalled mostly on fixed-latency dependencies, while
+// the same launch shape only streaming the bytes reaches the HBM rate). Two
+// CTAs an SM measured faster from about 16 MiB (Q4_0 8192 x 4096: 8.0 -> 7.6
+// us, Q8_0 4096 x 4096: 7.8 -> 7.2, 12288 x 4096: 17.3 -> 13.5) and slower
+// below, where the next launch's start beside this one counts for more
+// (Q4_0 / Q4_K 4096 x 4096: 5.4 -> 5.5, 6.3 -> 6.5 us).
+int i8_grid(int qtype, int k, int n) {
   const int sms = num_sms();
   if (n < sms) return n;
-  if ((long)n >= 2L * sms * 128 && i8_stages_for(k, n, 2 * sms) == 5) return 2 * sms;
+  if ((double)n * (double)row_bytes_of(qtype, k) >= 16.0 * 1048576.0 && i8_stages_for(k, n, 2 * sms) == 5)
+    return 2 * sms;
   return sms;
 }
-int i8_stages(int k, int n) { return i8_stages_for(k, n, i8_grid(k, n)); }
-size_t i8_fixed_smem(int k, int n) { return i8_fixed_smem(k, n, i8_grid(k, n)); }
-size_t i8_smem(int k, int n) { return i8_fixed_smem(k, n) + (size_t)i8_stages(k, n) * ISTAGE; }
+int i8_stages(int qtype, int k, int n) { return i8_stages_for(k, n, i8_grid(qtype, k, n)); }
+size_t i8_fixed_smem(int qtype, int k, int n) { return i8_fixed_smem_grid(k, n, i8_grid(qtype, k, n)); }
+size_t i8_smem(int qtype, int k, int n) {
+  return i8_fixed_smem(qtype, k, n) + (size_t)i8_stages(qtype, k, n) * ISTAGE;
+}
 
 template <int QT, bool SWI>
 cudaError_t launch_i8(const void* W, const void* Wu, int n, int k, const float* X, float* Y, const float* R,
                       unsigned* status, cudaStream_t s) {
-  const size_t smem = i8_smem(k, n);
+  const size_t smem = i8_smem(QT, k, n);
   auto kern = gemv_i8_kernel<QT, SWI>;
   static int attr_set[64] = {0};
   int dev = 0;
@@ -580,7 +587,7 @@ cudaError_t launch_i8(const void* W, const void* Wu, int n, int k, const float* 
     attr_set[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)i8_grid(k, n));
+  cfg.gridDim = dim3((unsigned)i8_grid(QT, k, n));
   cfg.blockDim = dim3(ITHREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -591,7 +598,7 @@ cudaError_t launch_i8(const void* W, const void* Wu, int n, int k, const float* 
   cfg.numAttrs = 1;
   cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, (const uint8_t*)W, (const uint8_t*)Wu, n, k, X, Y, R, status,
-                         rows_per_stage(QT, k, SWI), i8_stages(k, n));
+                         rows_per_stage(QT, k, SWI), i8_stages(QT, k, n));
   if (e == cudaSuccess) e = cudaGetLastError();
   return e;
 }
@@ -688,7 +695,7 @@ bool gemv_i8_fits(int qtype, int n, int k, int T, bool swiglu) {
   // aligned in a stage); a row's warps within the consumer warps; a ring of at
   // least 4 stages beside the X table and the CTA's row sums
   if ((!block32_format(qtype) && !kquant(qtype)) || T != 1 || k % 256 != 0 || (k / 64 + 31) / 32 > 8) return false;
-  return rows_per_stage(qtype, k, swiglu) >= 1 && i8_stages(k, n) >= 4;
+  return rows_per_stage(qtype, k, swiglu) >= 1 && i8_stages(qtype, k, n) >= 4;
 }
 
 cudaError_t launch_gemv_i8(int qtype, const void* W, const void* Wu, int n, int k, const float* X, float* Y,

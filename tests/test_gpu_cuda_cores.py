@@ -80,13 +80,11 @@ def test_gemv_exact(q, qtype, T, n, k):
 
 @pytest.mark.parametrize("qtype", QTYPES)
 @pytest.mark.parametrize("swiglu", [False, True])
-@pytest.mark.parametrize("n", [20000, 40000])
-def test_one_token_gemv_many_rows_a_cta(q, qtype, swiglu, n):
+@pytest.mark.parametrize("n,k", [(20000, 512), (40000, 1024)])
+def test_one_token_gemv_many_rows_a_cta(q, qtype, swiglu, n, k):
     """Many rows a CTA of the one-token kernel (its row sums and residuals
-    sized by that count): 20000 rows on one CTA an SM (132 rows each), 40000
-    on two CTAs an SM (132 rows each), the form of weights of 128 rows a CTA
-    and more."""
-    k = 512
+    sized by that count): 20000 x 512 (under 16 MiB of weight) on one CTA an
+    SM, 132 rows each; 40000 x 1024 (over) on two CTAs an SM, 132 rows each."""
     c = synth.make_case(qtype, n, k, 1, residual=not swiglu, gate_up=swiglu, seed=41)
     buf, Y = guarded(1, n)
     if swiglu:

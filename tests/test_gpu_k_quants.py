@@ -245,11 +245,11 @@ def test_gemv(q, qk, cls, n, k, T):
     _check_exact(qk, W, n, k, X, R, Y.cpu().numpy())
 
 
-@pytest.mark.parametrize("n,k", [(300, 12288), (20000, 2048), (40000, 512)])
+@pytest.mark.parametrize("n,k", [(300, 12288), (20000, 2048), (40000, 1024)])
 def test_one_token_gemv_large_shapes(q, qk, n, k):
     """T = 1 with long rows (one Q6_K row a stage at k = 12288), a gate/up
-    pair, many rows a CTA (20000 on one CTA an SM) and 40000 rows (two CTAs
-    an SM for IQ4_XS, Q4_K, Q5_K; Q6_K rows of 2048 keep one)."""
+    pair, and many rows a CTA on two CTAs an SM (20000 x 2048 and 40000 x
+    1024: over 16 MiB of weight in every format)."""
     k = _k(qk, k)
     W = synth.random_blocks(qk, n, k, 11 + n, "typical")
     X = synth.activations(1, k, 12)
