@@ -260,8 +260,10 @@ int run(const Problem& p) {
     leg = APR_LEG_EXACT_F32;
   }
   if (path == APR_PATH_GEMV) {
-    // the tensor-core GEMV multiplies integer codes: block formats only
-    if (!block32_format(p.qtype) || !gemv_tc_takes(p.n, p.k, p.T, p.Wu != nullptr))
+    // the tensor-core GEMV multiplies integer codes: block formats only; the
+    // integer-dot GEMV takes one and two tokens before it
+    if (!block32_format(p.qtype) || !gemv_tc_takes(p.n, p.k, p.T, p.Wu != nullptr) ||
+        gemv_i8_fits(p.qtype, p.n, p.k, p.T, p.Wu != nullptr))
       return launched(launch_gemv(p.qtype, p.W, p.Wu, p.n, p.k, p.X, p.T, p.Y, ldy_of(p), p.R, st->status, p.s),
                       "gemv");
     // tensor-core GEMV: the stream's scratch holds its split X, scales and

@@ -51,11 +51,12 @@ size_t gemv_rows_smem(int qtype, int k, int T);
 bool gemv_rows_fits(int qtype, int n, int k, int T, bool swiglu);
 cudaError_t launch_gemv_rows(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
                              float* Y, const float* R, unsigned* status, cudaStream_t s);
-// T = 1 with integer dot products (gemv_i8.cu): X per 32-block in fixed point
-// as three signed byte digits, dp4a against the codes, fp32 per block.
+// T = 1, 2 with integer dot products (gemv_i8.cu): X per 32-block in fixed
+// point as three signed byte digits, dp4a against the codes, fp32 per block;
+// Y and R rows ldy apart.
 bool gemv_i8_fits(int qtype, int n, int k, int T, bool swiglu);
-cudaError_t launch_gemv_i8(int qtype, const void* W, const void* Wu, int n, int k, const float* X, float* Y,
-                           const float* R, unsigned* status, cudaStream_t s);
+cudaError_t launch_gemv_i8(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y,
+                           int ldy, const float* R, unsigned* status, cudaStream_t s);
 // The T = 1 GEMV's data movement alone (gemv_i8.cu): `bytes` (a multiple of
 // 16, src 16-byte aligned) streamed into shared memory and dropped.
 cudaError_t launch_read_stream(const void* src, long long bytes, unsigned* status, cudaStream_t s);

@@ -802,8 +802,9 @@ cudaError_t launch_iq4(const void* W, const void* Wu, int n, int k, const float*
 cudaError_t launch_gemv(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T,
                         float* Y, int ldy, const float* R, unsigned* status, cudaStream_t s) {
   const bool swi = Wu != nullptr;
-  // one token: one row of Y, so the row kernels need no stride
-  if (gemv_i8_fits(qtype, n, k, T, swi)) return launch_gemv_i8(qtype, W, Wu, n, k, X, Y, R, status, s);
+  // one and two tokens: the integer-dot kernel; the whole-row kernel (one
+  // token) needs no stride
+  if (gemv_i8_fits(qtype, n, k, T, swi)) return launch_gemv_i8(qtype, W, Wu, n, k, X, T, Y, ldy, R, status, s);
   if (gemv_rows_fits(qtype, n, k, T, swi)) return launch_gemv_rows(qtype, W, Wu, n, k, X, T, Y, R, status, s);
   if (gemv_bulk_fits(qtype, k, T, swi)) return launch_gemv_bulk(qtype, W, Wu, n, k, X, T, Y, ldy, R, status, s);
   if (qtype == kQ4_K)

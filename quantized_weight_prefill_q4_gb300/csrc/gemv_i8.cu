@@ -313,10 +313,13 @@ int rows_per_stage(int qtype, int k, bool swiglu) {
   return (int)(ISTAGE / ((swiglu ? 2 : 1) * row_bytes));
 }
 
-template <int QT, bool SWI>
-__global__ void __launch_bounds__(ITHREADS, 2)
+// NT tokens (1 or 2): with two, one CTA an SM (the two tokens' digit tables
+// stay in registers), X rows k apart, Y and R rows ldy apart.
+template <int QT, bool SWI, int NT>
+__global__ void __launch_bounds__(ITHREADS, NT == 1 ? 2 : 1)
     gemv_i8_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ Wu, int n, int k,
-                   const float* __restrict__ X, float* Y, const float* R, unsigned* status, int rs, int ns) {
+                   const float* __restrict__ X, float* Y, const float* R, unsigned* status, int rs, int ns,
+                   int ldy) {
   constexpr int NM = SWI ? 2 : 1;
   constexpr bool KQ = QT == kQ4_K || QT == kQ5_K || QT == kQ6_K || QT == kIQ4_XS;
   constexpr int BB = QT == kQ4_0 ? 18 : 34;  // block formats
@@ -326,11 +329,11 @@ __global__ void __launch_bounds__(ITHREADS, 2)
   uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   const int nblk = k / 32, npk = nblk / 2;
   const int PW = (npk + 31) / 32;  // warps per row
-  uint32_t* xt = reinterpret_cast<uint32_t*>(smem + (size_t)ns * ISTAGE);  // X table, [nblk][XBW]
+  uint32_t* xt = reinterpret_cast<uint32_t*>(smem + (size_t)ns * ISTAGE);  // X tables, [NT][nblk][XBW]
   const int rcap = i8_rcap(n, gridDim.x);
-  float* part = reinterpret_cast<float*>(xt + (size_t)nblk * XBW);     // [row slot][NM][PW]
-  float* rres = part + (((size_t)rcap * NM * PW + 1) & ~(size_t)1);    // residual of the CTA's rows
-  uint64_t* bars = reinterpret_cast<uint64_t*>(rres + ((rcap + 1) & ~1));
+  float* part = reinterpret_cast<float*>(xt + (size_t)NT * nblk * XBW);  // [row slot][NM][NT][PW]
+  float* rres = part + (((size_t)rcap * NM * NT * PW + 1) & ~(size_t)1);  // [NT][row slot] residuals
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rres + ((NT * rcap + 1) & ~1));
   uint64_t* full = bars;
   uint64_t* empty = bars + INS_MAX;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * INS_MAX);
@@ -389,39 +392,50 @@ __global__ void __launch_bounds__(ITHREADS, 2)
   // 8 lanes a block, 32 blocks a pass of the consumers (nblk is a multiple of
   // 8, so a warp's 4 blocks of a pass are all present or all absent); the X
   // loads of four passes are issued before any is used
-  for (int base = (int)threadIdx.x / 8; base < nblk; base += 4 * (ICW * 32 / 8)) {
-    float4 xv[4];
-    uint32_t* dst[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int b0 = base + u * (ICW * 32 / 8);
-      xv[u] = b0 < nblk ? __ldg(reinterpret_cast<const float4*>(X) + (size_t)b0 * 8 + (threadIdx.x & 7))
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-      dst[u] = b0 < nblk ? xt + (size_t)b0 * XBW : nullptr;
+  for (int tk = 0; tk < NT; ++tk) {
+    const float4* x4 = reinterpret_cast<const float4*>(X + (size_t)tk * k);
+    uint32_t* xtt = xt + (size_t)tk * nblk * XBW;
+    for (int base = (int)threadIdx.x / 8; base < nblk; base += 4 * (ICW * 32 / 8)) {
+      float4 xv[4];
+      uint32_t* dst[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int b0 = base + u * (ICW * 32 / 8);
+        xv[u] = b0 < nblk ? __ldg(x4 + (size_t)b0 * 8 + (threadIdx.x & 7)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        dst[u] = b0 < nblk ? xtt + (size_t)b0 * XBW : nullptr;
+      }
+      block_digits8<QT, 4>(xv, threadIdx.x & 7, dst);
     }
-    block_digits8<QT, 4>(xv, threadIdx.x & 7, dst);
   }
   if (!SWI && R)
-    for (int i = threadIdx.x; i < r1 - r0; i += ICW * 32) rres[i] = R[r0 + i];
-  named_sync(1, ICW * 32);
-  uint32_t ta[XBW], tb[XBW];
-  if (act) {
-    const uint4* src = reinterpret_cast<const uint4*>(xt + (size_t)2 * P * XBW);
 #pragma unroll
-    for (int v = 0; v < XBW / 4; ++v) {
-      const uint4 a = src[v], b = src[XBW / 4 + v];
-      ta[4 * v] = a.x; ta[4 * v + 1] = a.y; ta[4 * v + 2] = a.z; ta[4 * v + 3] = a.w;
-      tb[4 * v] = b.x; tb[4 * v + 1] = b.y; tb[4 * v + 2] = b.z; tb[4 * v + 3] = b.w;
-    }
-    if constexpr (QT == kIQ4_XS) {
-      iq4_order_table(ta);
-      iq4_order_table(tb);
+    for (int tk = 0; tk < NT; ++tk)
+      for (int i = threadIdx.x; i < r1 - r0; i += ICW * 32) rres[tk * rcap + i] = R[(size_t)tk * ldy + r0 + i];
+  named_sync(1, ICW * 32);
+  uint32_t ta[NT][XBW], tb[NT][XBW];
+  if (act) {
+#pragma unroll
+    for (int tk = 0; tk < NT; ++tk) {
+      const uint4* src = reinterpret_cast<const uint4*>(xt + ((size_t)tk * nblk + 2 * P) * XBW);
+#pragma unroll
+      for (int v = 0; v < XBW / 4; ++v) {
+        const uint4 a = src[v], b = src[XBW / 4 + v];
+        ta[tk][4 * v] = a.x; ta[tk][4 * v + 1] = a.y; ta[tk][4 * v + 2] = a.z; ta[tk][4 * v + 3] = a.w;
+        tb[tk][4 * v] = b.x; tb[tk][4 * v + 1] = b.y; tb[tk][4 * v + 2] = b.z; tb[tk][4 * v + 3] = b.w;
+      }
+      if constexpr (QT == kIQ4_XS) {
+        iq4_order_table(ta[tk]);
+        iq4_order_table(tb[tk]);
+      }
     }
   }
 
-  // one row's partial of this lane (its block pair), weight m
-  auto row_part = [&](int st, int m, int rr) -> float {
-    if (!act) return 0.f;
+  // one row's partials of this lane (its block pair), weight m, one a token
+  auto row_part = [&](int st, int m, int rr, float (&res)[NT]) {
+#pragma unroll
+    for (int tk = 0; tk < NT; ++tk) res[tk] = 0.f;
+    if (!act) return;
     const uint32_t* rw = reinterpret_cast<const uint32_t*>(smem + st * ISTAGE + (size_t)(m * rs + rr) * row_bytes);
     if constexpr (QT == kQ6_K) {
       // superblock P / 4 from the word holding its first byte (2 (P / 4 mod
@@ -436,7 +450,10 @@ __global__ void __launch_bounds__(ITHREADS, 2)
       wq[26] = w[48 + (P & 3)];
       wq[27] = w[49 + (P & 3)];
       wq[28] = w[52];
-      return q6k_pair_dot(wq, (uint32_t)P & 3u, 2u * (((uint32_t)P >> 2) & 1u), ta, tb);
+#pragma unroll
+      for (int tk = 0; tk < NT; ++tk)
+        res[tk] = q6k_pair_dot(wq, (uint32_t)P & 3u, 2u * (((uint32_t)P >> 2) & 1u), ta[tk], tb[tk]);
+      return;
     } else if constexpr (QT == kIQ4_XS) {
       // superblock P / 4 (34 words, rows on 16-byte boundaries): header words,
       // then stage P mod 4's 8 code words
@@ -446,7 +463,9 @@ __global__ void __launch_bounds__(ITHREADS, 2)
       wq[1] = w[1];
 #pragma unroll
       for (int v = 0; v < 8; ++v) wq[2 + v] = w[2 + 8 * (P & 3) + v];
-      return iq4_pair_dot(wq, (uint32_t)P & 3u, ta, tb);
+#pragma unroll
+      for (int tk = 0; tk < NT; ++tk) res[tk] = iq4_pair_dot(wq, (uint32_t)P & 3u, ta[tk], tb[tk]);
+      return;
     } else if constexpr (KQ) {
       // superblock P / 4: header and scales, (Q5_K) fifth bits, then group P mod 4's codes
       constexpr int CW = QT == kQ5_K ? 12 : 4;
@@ -456,7 +475,9 @@ __global__ void __launch_bounds__(ITHREADS, 2)
       for (int v = 0; v < CW; ++v) wq[v] = w[v];
 #pragma unroll
       for (int v = 0; v < 8; ++v) wq[CW + v] = w[CW + 8 * (P & 3) + v];
-      return kq_pair_dot<QT>(wq, (uint32_t)P & 3u, ta, tb);
+#pragma unroll
+      for (int tk = 0; tk < NT; ++tk) res[tk] = kq_pair_dot<QT>(wq, (uint32_t)P & 3u, ta[tk], tb[tk]);
+      return;
     }
     const uint32_t* w = rw + P * PW_WORDS;
     uint32_t wr[PW_WORDS];
@@ -469,14 +490,16 @@ __global__ void __launch_bounds__(ITHREADS, 2)
       for (int i = 0; i < 4; ++i) pa[i] = __byte_perm(wr[i], wr[i + 1], 0x5432);
       const float dA = __half2float(__ushort_as_half((unsigned short)(wr[0] & 0xFFFFu)));
       const float dB = __half2float(__ushort_as_half((unsigned short)(wr[4] >> 16)));
-      return block_dot<QT>(pa, ta, dA) + block_dot<QT>(wr + 5, tb, dB);
+#pragma unroll
+      for (int tk = 0; tk < NT; ++tk) res[tk] = block_dot<QT>(pa, ta[tk], dA) + block_dot<QT>(wr + 5, tb[tk], dB);
     } else {
       // block A: d in bytes 0-1, codes 2..33; block B: d in 34-35, codes 36..67
 #pragma unroll
       for (int i = 0; i < 8; ++i) pa[i] = __byte_perm(wr[i], wr[i + 1], 0x5432);
       const float dA = __half2float(__ushort_as_half((unsigned short)(wr[0] & 0xFFFFu)));
       const float dB = __half2float(__ushort_as_half((unsigned short)(wr[8] >> 16)));
-      return block_dot<QT>(pa, ta, dA) + block_dot<QT>(wr + 9, tb, dB);
+#pragma unroll
+      for (int tk = 0; tk < NT; ++tk) res[tk] = block_dot<QT>(pa, ta[tk], dA) + block_dot<QT>(wr + 9, tb[tk], dB);
     }
   };
 
@@ -492,19 +515,29 @@ __global__ void __launch_bounds__(ITHREADS, 2)
         const bool two = rr + RG < rows;
 #pragma unroll
         for (int m = 0; m < NM; ++m) {
-          float a = row_part(st, m, rr);
-          float b = two ? row_part(st, m, rr + RG) : 0.f;
+          float a[NT], b[NT];
+          row_part(st, m, rr, a);
+          if (two) {
+            row_part(st, m, rr + RG, b);
+          } else {
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            a += __shfl_xor_sync(0xffffffffu, a, o);
-            b += __shfl_xor_sync(0xffffffffu, b, o);
+            for (int tk = 0; tk < NT; ++tk) b[tk] = 0.f;
           }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int tk = 0; tk < NT; ++tk) {
+              a[tk] += __shfl_xor_sync(0xffffffffu, a[tk], o);
+              b[tk] += __shfl_xor_sync(0xffffffffu, b[tk], o);
+            }
           // the warp's share of the row, added with the others' after the
           // last stage
-          if (lane == 0) {
-            part[((rb + rr - r0) * NM + m) * PW + wi] = a;
-            if (two) part[((rb + rr + RG - r0) * NM + m) * PW + wi] = b;
-          }
+          if (lane == 0)
+#pragma unroll
+            for (int tk = 0; tk < NT; ++tk) {
+              part[(((rb + rr - r0) * NM + m) * NT + tk) * PW + wi] = a[tk];
+              if (two) part[(((rb + rr + RG - r0) * NM + m) * NT + tk) * PW + wi] = b[tk];
+            }
         }
       }
     }
@@ -514,70 +547,75 @@ __global__ void __launch_bounds__(ITHREADS, 2)
   // every row's warp shares are in shared memory: add them in warp order
   named_sync(1, ICW * 32);
   if (ok)
-    for (int slot = threadIdx.x; slot < r1 - r0; slot += ICW * 32) {
-      float acc[NM];
+    for (int slot = threadIdx.x; slot < r1 - r0; slot += ICW * 32)
 #pragma unroll
-      for (int m = 0; m < NM; ++m) {
-        float v = 0.f;
-        for (int w2 = 0; w2 < PW; ++w2) v += part[(slot * NM + m) * PW + w2];
-        acc[m] = v;
+      for (int tk = 0; tk < NT; ++tk) {
+        float acc[NM];
+#pragma unroll
+        for (int m = 0; m < NM; ++m) {
+          float v = 0.f;
+          for (int w2 = 0; w2 < PW; ++w2) v += part[((slot * NM + m) * NT + tk) * PW + w2];
+          acc[m] = v;
+        }
+        float y;
+        if (SWI) {
+          y = acc[0] / (1.0f + expf(-acc[0])) * acc[NM - 1];
+        } else {
+          y = acc[0] + (R ? rres[tk * rcap + slot] : 0.f);
+        }
+        Y[(size_t)tk * ldy + r0 + slot] = y;
       }
-      float y;
-      if (SWI) {
-        y = acc[0] / (1.0f + expf(-acc[0])) * acc[NM - 1];
-      } else {
-        y = acc[0] + (R ? rres[slot] : 0.f);
-      }
-      Y[r0 + slot] = y;
-    }
 }
 
-// shared memory besides the ring, and the stages that fit beside it
-// shared memory besides the ring (the X table, the row partials [rows][2
-// weights at most][warps a row], the residuals, the barriers) for a grid of
-// `grid` CTAs, and the stages that fit beside it
-size_t i8_fixed_smem_grid(int k, int n, int grid) {
+// shared memory besides the ring (the nt tokens' X tables, the row partials
+// [rows][2 weights at most][nt][warps a row], the residuals, the barriers)
+// for a grid of `grid` CTAs, and the stages that fit beside it
+size_t i8_fixed_smem_grid(int k, int n, int grid, int nt) {
   const size_t rcap = (size_t)i8_rcap(n, grid), pw = (size_t)((k / 64 + 31) / 32);
-  return 128 + (size_t)(k / 32) * XBW * 4 + ((rcap * 2 * pw + 1) & ~(size_t)1) * 4 + ((rcap + 1) & ~(size_t)1) * 4 +
-         2 * INS_MAX * 8 + 16;
+  return 128 + (size_t)nt * (k / 32) * XBW * 4 + ((rcap * 2 * nt * pw + 1) & ~(size_t)1) * 4 +
+         ((nt * rcap + 1) & ~(size_t)1) * 4 + 2 * INS_MAX * 8 + 16;
 }
-int i8_stages_for(int k, int n, int grid) {
-  // two CTAs an SM (228 KB of shared memory, 1 KB reserved per CTA) when 5
-  // stages fit beside the X table, else one with as many as fit
-  const long half = 232448L / 2 - 1024 - (long)i8_fixed_smem_grid(k, n, grid);
-  if (half / ISTAGE >= 5) return 5;
-  const long ns = (232448L - (long)i8_fixed_smem_grid(k, n, grid)) / ISTAGE;
+int i8_stages_for(int k, int n, int grid, int nt) {
+  // one token: two CTAs an SM (228 KB of shared memory, 1 KB reserved per
+  // CTA) when 5 stages fit beside the X table, else one with as many as fit;
+  // two tokens: one CTA an SM
+  if (nt == 1) {
+    const long half = 232448L / 2 - 1024 - (long)i8_fixed_smem_grid(k, n, grid, 1);
+    if (half / ISTAGE >= 5) return 5;
+  }
+  const long ns = (232448L - (long)i8_fixed_smem_grid(k, n, grid, nt)) / ISTAGE;
   return (int)(ns < INS_MAX ? ns : INS_MAX);
 }
-// One CTA an SM (half of one when it fits, so that the next launch's CTAs
-// start beside it), or, for weights of 16 MiB and more when the half-SM form
-// fits them, two half-SM CTAs an SM: twice the consumer warps to hide the
-// latency of the dot products' dependent chains, which bound larger weights
-// (measured on GB300 with a 49152 x 4096 Q4_0 weight: 2 warps a scheduler
-// issuing 45 % of cycles, stalled mostly on fixed-latency dependencies, while
-// the same launch shape only streaming the bytes reaches the HBM rate). Two
-// CTAs an SM measured faster from about 16 MiB (Q4_0 8192 x 4096: 8.0 -> 7.6
-// us, Q8_0 4096 x 4096: 7.8 -> 7.2, 12288 x 4096: 17.3 -> 13.5) and slower
-// below, where the next launch's start beside this one counts for more
-// (Q4_0 / Q4_K 4096 x 4096: 5.4 -> 5.5, 6.3 -> 6.5 us).
-int i8_grid(int qtype, int k, int n) {
+// One token: one CTA an SM (half of one when it fits, so that the next
+// launch's CTAs start beside it), or, for weights of 16 MiB and more when the
+// half-SM form fits them, two half-SM CTAs an SM: twice the consumer warps to
+// hide the latency of the dot products' dependent chains, which bound larger
+// weights (measured on GB300 with a 49152 x 4096 Q4_0 weight: 2 warps a
+// scheduler issuing 45 % of cycles, stalled mostly on fixed-latency
+// dependencies, while the same launch shape only streaming the bytes reaches
+// the HBM rate). Two CTAs an SM measured faster from about 16 MiB (Q4_0
+// 8192 x 4096: 8.0 -> 7.6 us, Q8_0 4096 x 4096: 7.8 -> 7.2, 12288 x 4096:
+// 17.3 -> 13.5) and slower below, where the next launch's start beside this
+// one counts for more (Q4_0 / Q4_K 4096 x 4096: 5.4 -> 5.5, 6.3 -> 6.5 us).
+// Two tokens: one CTA an SM.
+int i8_grid(int qtype, int k, int n, int nt) {
   const int sms = num_sms();
   if (n < sms) return n;
-  if ((double)n * (double)row_bytes_of(qtype, k) >= 16.0 * 1048576.0 && i8_stages_for(k, n, 2 * sms) == 5)
+  if (nt == 1 && (double)n * (double)row_bytes_of(qtype, k) >= 16.0 * 1048576.0 &&
+      i8_stages_for(k, n, 2 * sms, 1) == 5)
     return 2 * sms;
   return sms;
 }
-int i8_stages(int qtype, int k, int n) { return i8_stages_for(k, n, i8_grid(qtype, k, n)); }
-size_t i8_fixed_smem(int qtype, int k, int n) { return i8_fixed_smem_grid(k, n, i8_grid(qtype, k, n)); }
-size_t i8_smem(int qtype, int k, int n) {
-  return i8_fixed_smem(qtype, k, n) + (size_t)i8_stages(qtype, k, n) * ISTAGE;
+int i8_stages(int qtype, int k, int n, int nt) { return i8_stages_for(k, n, i8_grid(qtype, k, n, nt), nt); }
+size_t i8_smem(int qtype, int k, int n, int nt) {
+  return i8_fixed_smem_grid(k, n, i8_grid(qtype, k, n, nt), nt) + (size_t)i8_stages(qtype, k, n, nt) * ISTAGE;
 }
 
-template <int QT, bool SWI>
-cudaError_t launch_i8(const void* W, const void* Wu, int n, int k, const float* X, float* Y, const float* R,
+template <int QT, bool SWI, int NT>
+cudaError_t launch_i8(const void* W, const void* Wu, int n, int k, const float* X, float* Y, int ldy, const float* R,
                       unsigned* status, cudaStream_t s) {
-  const size_t smem = i8_smem(QT, k, n);
-  auto kern = gemv_i8_kernel<QT, SWI>;
+  const size_t smem = i8_smem(QT, k, n, NT);
+  auto kern = gemv_i8_kernel<QT, SWI, NT>;
   static int attr_set[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -587,7 +625,7 @@ cudaError_t launch_i8(const void* W, const void* Wu, int n, int k, const float* 
     attr_set[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)i8_grid(QT, k, n));
+  cfg.gridDim = dim3((unsigned)i8_grid(QT, k, n, NT));
   cfg.blockDim = dim3(ITHREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -598,9 +636,16 @@ cudaError_t launch_i8(const void* W, const void* Wu, int n, int k, const float* 
   cfg.numAttrs = 1;
   cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, (const uint8_t*)W, (const uint8_t*)Wu, n, k, X, Y, R, status,
-                         rows_per_stage(QT, k, SWI), i8_stages(QT, k, n));
+                         rows_per_stage(QT, k, SWI), i8_stages(QT, k, n, NT), ldy);
   if (e == cudaSuccess) e = cudaGetLastError();
   return e;
+}
+
+template <int QT, bool SWI>
+cudaError_t launch_i8_t(const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y, int ldy,
+                        const float* R, unsigned* status, cudaStream_t s) {
+  return T == 2 ? launch_i8<QT, SWI, 2>(W, Wu, n, k, X, Y, ldy, R, status, s)
+                : launch_i8<QT, SWI, 1>(W, Wu, n, k, X, Y, ldy, R, status, s);
 }
 
 // The GEMV's data movement alone: each CTA streams its contiguous share of
@@ -691,33 +736,39 @@ cudaError_t launch_read_stream(const void* src, long long bytes, unsigned* statu
 }
 
 bool gemv_i8_fits(int qtype, int n, int k, int T, bool swiglu) {
-  // block formats and K-quants, one token; k % 256 == 0 (whole rows 16-byte
-  // aligned in a stage); a row's warps within the consumer warps; a ring of at
-  // least 4 stages beside the X table and the CTA's row sums
-  if ((!block32_format(qtype) && !kquant(qtype)) || T != 1 || k % 256 != 0 || (k / 64 + 31) / 32 > 8) return false;
-  return rows_per_stage(qtype, k, swiglu) >= 1 && i8_stages(qtype, k, n) >= 4;
+  // block formats and K-quants, one or two tokens; k % 256 == 0 (whole rows
+  // 16-byte aligned in a stage); a row's warps within the consumer warps; a
+  // ring of at least 4 stages beside the X tables and the CTA's row sums
+  if ((!block32_format(qtype) && !kquant(qtype)) || T < 1 || T > 2 || k % 256 != 0 || (k / 64 + 31) / 32 > 8)
+    return false;
+  // two tokens of Q8_0 below 2^25 weight elements: the bulk CUDA-core kernel
+  // measured faster (4096 x 4096: 9.4 against 10.5 us; at 12288 x 4096 this
+  // kernel takes 21.4 against 22.4 us on the tensor cores, and Q4_0 8.5 / 15.9
+  // against 10.2 / 20.8 us)
+  if (T == 2 && qtype == kQ8_0 && (long)n * k < (1L << 25)) return false;
+  return rows_per_stage(qtype, k, swiglu) >= 1 && i8_stages(qtype, k, n, T) >= 4;
 }
 
-cudaError_t launch_gemv_i8(int qtype, const void* W, const void* Wu, int n, int k, const float* X, float* Y,
-                           const float* R, unsigned* status, cudaStream_t s) {
+cudaError_t launch_gemv_i8(int qtype, const void* W, const void* Wu, int n, int k, const float* X, int T, float* Y,
+                           int ldy, const float* R, unsigned* status, cudaStream_t s) {
   const bool swi = Wu != nullptr;
   if (qtype == kQ4_K)
-    return swi ? launch_i8<kQ4_K, true>(W, Wu, n, k, X, Y, R, status, s)
-               : launch_i8<kQ4_K, false>(W, Wu, n, k, X, Y, R, status, s);
+    return swi ? launch_i8_t<kQ4_K, true>(W, Wu, n, k, X, T, Y, ldy, R, status, s)
+               : launch_i8_t<kQ4_K, false>(W, Wu, n, k, X, T, Y, ldy, R, status, s);
   if (qtype == kQ5_K)
-    return swi ? launch_i8<kQ5_K, true>(W, Wu, n, k, X, Y, R, status, s)
-               : launch_i8<kQ5_K, false>(W, Wu, n, k, X, Y, R, status, s);
+    return swi ? launch_i8_t<kQ5_K, true>(W, Wu, n, k, X, T, Y, ldy, R, status, s)
+               : launch_i8_t<kQ5_K, false>(W, Wu, n, k, X, T, Y, ldy, R, status, s);
   if (qtype == kQ6_K)
-    return swi ? launch_i8<kQ6_K, true>(W, Wu, n, k, X, Y, R, status, s)
-               : launch_i8<kQ6_K, false>(W, Wu, n, k, X, Y, R, status, s);
+    return swi ? launch_i8_t<kQ6_K, true>(W, Wu, n, k, X, T, Y, ldy, R, status, s)
+               : launch_i8_t<kQ6_K, false>(W, Wu, n, k, X, T, Y, ldy, R, status, s);
   if (qtype == kIQ4_XS)
-    return swi ? launch_i8<kIQ4_XS, true>(W, Wu, n, k, X, Y, R, status, s)
-               : launch_i8<kIQ4_XS, false>(W, Wu, n, k, X, Y, R, status, s);
+    return swi ? launch_i8_t<kIQ4_XS, true>(W, Wu, n, k, X, T, Y, ldy, R, status, s)
+               : launch_i8_t<kIQ4_XS, false>(W, Wu, n, k, X, T, Y, ldy, R, status, s);
   if (qtype == kQ4_0)
-    return swi ? launch_i8<kQ4_0, true>(W, Wu, n, k, X, Y, R, status, s)
-               : launch_i8<kQ4_0, false>(W, Wu, n, k, X, Y, R, status, s);
-  return swi ? launch_i8<kQ8_0, true>(W, Wu, n, k, X, Y, R, status, s)
-             : launch_i8<kQ8_0, false>(W, Wu, n, k, X, Y, R, status, s);
+    return swi ? launch_i8_t<kQ4_0, true>(W, Wu, n, k, X, T, Y, ldy, R, status, s)
+               : launch_i8_t<kQ4_0, false>(W, Wu, n, k, X, T, Y, ldy, R, status, s);
+  return swi ? launch_i8_t<kQ8_0, true>(W, Wu, n, k, X, T, Y, ldy, R, status, s)
+             : launch_i8_t<kQ8_0, false>(W, Wu, n, k, X, T, Y, ldy, R, status, s);
 }
 
 }  // namespace apr

@@ -159,9 +159,10 @@ def test_exact_gate_up(q, qtype, cls):
 
 
 # ------------------------------------------------------------------ GEMV routes
-# T = 1 at k % 256 == 0: whole-row kernel; T = 2 (small weight), 5, 8: bulk
-# kernel; T = 3, 4: tensor cores; T = 13: staged fallback; k = 288: the
-# staged fallback at every T
+# T = 1, 2 at k % 256 == 0: the integer-dot kernel (Q8_0 at T = 2 on this
+# small weight: the bulk kernel); T = 5, 8: bulk kernel;
+# T = 3, 4: tensor cores; T = 13: staged fallback; k = 288: the staged
+# fallback at every T
 @pytest.mark.parametrize("qtype", QTYPES)
 @pytest.mark.parametrize("cls", CLASSES)
 @pytest.mark.parametrize("n,k,T", [(300, 512, 1), (300, 512, 2), (300, 1024, 3), (300, 1024, 4), (300, 512, 5),
@@ -175,7 +176,8 @@ def test_gemv_routes(q, qtype, cls, n, k, T):
     _check_exact(qtype, W, n, k, X, R, Y.cpu().numpy())
 
 
-# T = 2 on a weight of 2^25 elements runs on the tensor cores
+# T = 2 on a weight of 2^25 elements: the integer-dot kernel's two-token
+# form (one CTA an SM), 54 rows a CTA
 @pytest.mark.parametrize("qtype", QTYPES)
 @pytest.mark.parametrize("cls", ["subnormal", "mixed"])
 def test_gemv_tensor_core_two_tokens(q, qtype, cls):

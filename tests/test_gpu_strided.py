@@ -107,10 +107,10 @@ def test_gemm_strided_accumulate(q, ldy):
 
 
 # ------------------------------------------------------------------ GEMV (exact fp32)
-# T = 1 at k % 256 == 0: whole-row kernel; T = 5 and 13: chunked bulk kernel
-# (up to 8) and the staged kernel (k = 288, or T > 8)
+# T = 1, 2 at k % 256 == 0: the integer-dot kernel; T = 5 and 13: chunked
+# bulk kernel (up to 8) and the staged kernel (k = 288, or T > 8)
 @pytest.mark.parametrize("qtype", QTYPES)
-@pytest.mark.parametrize("n,k,T,ldy", [(300, 512, 1, 301), (300, 512, 5, 303), (77, 288, 5, 80),
+@pytest.mark.parametrize("n,k,T,ldy", [(300, 512, 1, 301), (300, 512, 2, 307), (300, 512, 5, 303), (77, 288, 5, 80),
                                        (10, 2304, 13, 17)])
 def test_gemv_strided(q, qtype, n, k, T, ldy):
     c = synth.make_case(qtype, n, k, T, residual=True, seed=T + ldy)
@@ -118,7 +118,7 @@ def test_gemv_strided(q, qtype, n, k, T, ldy):
     assert_exact_leg(y, ref)
 
 
-@pytest.mark.parametrize("T", [1, 3])
+@pytest.mark.parametrize("T", [1, 2, 3])
 def test_gemv_swiglu_strided(q, T):
     n, k = 300, 1024
     c = synth.make_case(synth.Q8_0, n, k, T, gate_up=True, seed=T)
@@ -126,8 +126,9 @@ def test_gemv_swiglu_strided(q, T):
     assert_exact_leg(y, ref)
 
 
-def test_gemv_strided_accumulate(q):
-    n, k, T = 300, 512, 4
+@pytest.mark.parametrize("T", [2, 4])
+def test_gemv_strided_accumulate(q, T):
+    n, k = 300, 512
     c = synth.make_case(synth.Q4_0, n, k, T, residual=True, seed=5)
     y, ref = run(q, synth.Q4_0, c, n, k, T, 333, leg=q.APR_LEG_F16, path=q.APR_PATH_GEMV, residual=True,
                  accumulate=True)
