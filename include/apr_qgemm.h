@@ -80,7 +80,7 @@
  *
  * Scratch. The library owns device scratch per (device, stream): the fp16
  * copy of X for the GEMM path (T*k*2 bytes), and, for the tensor-core GEMV
- * (T = 3 or 4, or T = 2 on weights of 2^25 or more elements), ticket counters
+ * (T = 3 or 4, or T = 2 where the integer-dot GEMV does not run), ticket counters
  * and partial sums (64 KiB plus 2 KiB per 128 weight rows and per SM, at
  * most), for the exact leg its split copies of X, exponents and, when k is
  * split over CTAs, up to four partial outputs of T*n floats, and, for
@@ -210,8 +210,10 @@ int apr_qgemm_gate_up_swiglu(int qtype, const void* Wg, const void* Wu, int n, i
  * arithmetic, optional residual (gemv_q4_0_pf / gemv_q8_0_pf of
  * oxibonsai-kernels, used for the last-token lm_head in
  * try_cuda_prefill_q_std). Weight rows stream by bulk copies into T fp32
- * accumulators for T <= 4 with Q4_0 / Q8_0 (tensor cores for T = 3, 4) and
- * T <= 8 with F16, K-quant and IQ4_XS weights (CUDA cores); for larger T up to 16,
+ * accumulators for T <= 4 with Q4_0 / Q8_0 (integer dot products of X in
+ * fixed point against the codes for T = 1, 2, also for the K-quants and
+ * IQ4_XS; tensor cores for T = 3, 4) and T <= 8 with F16, K-quant and IQ4_XS
+ * weights (CUDA cores); for larger T up to 16,
  * and for smaller T where no streaming kernel takes the shape (the X table of
  * a long row does not fit shared memory), the exact leg's tensor-core GEMM
  * runs instead when k % 256 == 0 (22-24 us at 4096 x 4096 for T <= 16, with k
