@@ -130,9 +130,10 @@ struct Cfg {
   // word) and the word holding d; for IQ4_XS the header's two words (d and
   // the high scale bits, the low scale nibbles) and the stage's 32 code bytes
   static constexpr int NWORDS = QT == kQ4_K ? 12 : (QT == kQ5_K ? 20 : (Q6K ? 29 : (IQ4 ? 10 : 2 * BB / 4)));
-  // k per raw slot: a chunk, or half of one for an F16 gate/up pair (four
-  // slots of 32 KB keep each weight double-buffered)
-  static constexpr int RAW_K = F16W && NM == 2 ? CHUNK / 2 : CHUNK;
+  // k per raw slot: a chunk, or half of one for F16 gate/up (four slots of
+  // 32 KB keep each weight double-buffered; a CTA pair's two 32 KB slots
+  // beside its 256-token B ring)
+  static constexpr int RAW_K = F16W && (NM == 2 || BN == 256) ? CHUNK / 2 : CHUNK;
   static constexpr int RAW_SUBS = RAW_K / BK;         // operand stages per raw slot
   // 144 / 272 / 512 (or 256) bytes; Q6_K: a 224-byte box from the 16-byte
   // boundary at or below the 210-byte superblock; IQ4_XS: a 144-byte box from
@@ -158,7 +159,7 @@ struct Cfg {
   // tell phase p + 2 from phase p.
   static constexpr int S_RAW = NM == 1 ? (Q4W ? (BN == 256 ? 4 : 3) : (Q6K ? 3 : 2)) : 4;
   static_assert(!XS || RAW_K == CHUNK, "the exact leg folds one raw slot per accumulation chunk");
-  static_assert(!F16W || BN == 128, "F16 tiles take 128 tokens");
+  static_assert(!F16W || BN == 128 || EPI == kEpiGluPair, "F16 tiles take 128 tokens, except a gate/up pair's");
   static constexpr int NTHREADS = 128 + 128 * NWG;
   static constexpr int ACC_COLS = (XS ? 3 : NM) * BN;
   static constexpr int A_COL0 = ACC_COLS;                       // first A column
@@ -1122,10 +1123,8 @@ template <int QT>
 int launch_q(const GemmPlan& pl, const void* W, const void* Wu, int n, int k, const uint16_t* X16, int T, float* Y,
              int ldy, const float* R, unsigned* status, cudaStream_t s, char* msg, size_t msg_len, int w, int xr,
              const OutRegions& reg) {
-  if constexpr (QT != kF16) {
-    if (Wu && pl.pair)
-      return launch_cfg<QT, kEpiGluPair, 256>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 2, w, xr);
-  }
+  if (Wu && pl.pair)
+    return launch_cfg<QT, kEpiGluPair, 256>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 2, w, xr);
   if (Wu) return launch_cfg<QT, kEpiSwiGLU, 128>(W, Wu, n, k, X16, T, Y, ldy, R, status, s, msg, msg_len, 1, w, xr);
   if constexpr (QT == kF16) {
     // an F16 raw slot is four times a Q4_0 one: 256-token tiles do not fit
@@ -1440,7 +1439,6 @@ GemmPlan plan_gemm_tc(int n, int k, int T, bool swiglu) {
   if (swiglu) {
     // a CTA pair per 256-token tile (one weight each) once a tile's second
     // half holds tokens; else one CTA per 128-token tile with both weights
-    // (F16 weights always: their raw slots leave no room for 256-token tiles)
     pl.pair = T > 128;
     return pl;
   }
